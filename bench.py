@@ -1,0 +1,386 @@
+"""Benchmark: verified tokens/s of the batch-invariant verify step.
+
+Workload: the random-init 2-layer decoder verifier (d=1024, 8 query / 2 KV
+heads of 128, SwiGLU 2816, vocab 32000, bf16 weights ~N(0, 0.02)), one
+window of N=8 requests x K=8 tokens (W = 64 rows), per-request contexts
+~U[128, 2048], fixed KV split 256, drafts with a 30% random-token error
+rate, Gumbel selection at T=0.7.  One step = the whole hot path: embed,
+2 x (RMSNorm, QKV GEMM, RoPE, KV overwrite, fixed-split attention, Wo GEMM,
+residual, RMSNorm, gate/up GEMM, SwiGLU, down GEMM, residual), RMSNorm,
+LM-head GEMM (fp32 logits), Gumbel-max selection, coupled accept.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): the path shards by request, so each rank runs its own
+replica window (weak scaling, no collective on the data path); value is the
+rows of all ranks over the slowest rank's time.
+
+--impl reference times the CPU oracle (the plain C++ reference) on the same
+workload, one window row per step, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "verified tok/s at W=N·K, batch-invariant; % of bf16 tensor-core / HBM roofline"
+UNIT = "verified tok/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def workload_config(cfg):
+    return {"workload": "2-layer decoder verifier d1024 8q/2kv hd128 ffn2816 vocab32000 (random init)",
+            "N": cfg.N, "K": cfg.K, "W": cfg.W, "layers": cfg.layers, "d": cfg.d, "vocab": cfg.vocab,
+            "ctx": f"U[{cfg.ctx_lo},{cfg.ctx_hi}]", "kv_split": cfg.kv_split, "temperature": cfg.temperature,
+            "draft_error_rate": cfg.draft_err, "l2": "flushed between timed steps (256 MiB write, outside the step events)"}
+
+
+# ------------------------------------------------------------------ setup
+def build_problem(cfg, device, seed_offset=0):
+    from invariant_verify_gb300 import synth
+    from invariant_verify_gb300.verifier import DecoderVerifier, make_window
+    w = synth.decoder_weights(cfg)
+    ctx = synth.context_lengths(cfg, cfg.N, seed=cfg.seed + 100 + seed_offset)
+    max_len = int(ctx.max()) + 64
+    caches = synth.kv_cache(cfg.N, cfg.Hkv, max_len, cfg.hd, ctx, seed=cfg.seed + 200 + seed_offset,
+                            layers=cfg.layers)
+    ver = DecoderVerifier(cfg, w, caches, cfg.N, max_len, cfg.W, cfg.K, device=device)
+    g = synth.generator(cfg.seed + 300 + seed_offset)
+    N, K = cfg.N, cfg.K
+    last = torch.randint(0, cfg.vocab, (N,), generator=g, dtype=torch.int64).to(torch.int32)
+    mask, ids = synth.draft_errors((N, K), cfg.draft_err, cfg.vocab, seed=cfg.seed + 400 + seed_offset)
+    req = torch.arange(N, dtype=torch.int32) * 1000 + 17
+    # A drafter that is right 70% of the time: fix d_1..d_K one position at a
+    # time from the verifier's own selections (d_j feeds row j).
+    drafts = torch.zeros(N, K, dtype=torch.int32)
+    for j in range(K):
+        tokens = torch.cat([last[:, None], drafts[:, :-1]], dim=1)
+        win = make_window(N, K, tokens.reshape(-1), ctx, req, drafts.reshape(-1), device=device)
+        ver.step(win)
+        tgt = ver.target.view(N, K)[:, j].cpu()
+        drafts[:, j] = torch.where(mask[:, j], ids[:, j], tgt)
+    tokens = torch.cat([last[:, None], drafts[:, :-1]], dim=1)
+    win = make_window(N, K, tokens.reshape(-1), ctx, req, drafts.reshape(-1), device=device)
+    return ver, win, w, caches, max_len, ctx
+
+
+def clock_sampler_start(path):
+    q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    try:
+        f = open(path, "w")
+        p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100"],
+                             stdout=f, stderr=subprocess.DEVNULL)
+        return p, f
+    except Exception:
+        return None, None
+
+
+def clock_sampler_stop(p, f, path, gpu_index):
+    if p is None:
+        return None
+    p.terminate()
+    try:
+        p.wait(timeout=5)
+    except Exception:
+        p.kill()
+    f.close()
+    sm, mx, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in open(path):
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9 or not parts[0].isdigit() or int(parts[0]) != gpu_index:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx = float(parts[2])
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def lm_head_traffic():
+    """Per-launch DRAM bytes of the LM-head GEMM from the committed ncu summary,
+    or None when the GEMM source changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "lmhead_gemm_decoder2.md")
+    src = os.path.join(ROOT, "invariant_verify_gb300", "csrc", "biv_gemm.cu")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return float(m.group(1)) if cur.startswith(h.group(1)) else None
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch.distributed as dist
+    from invariant_verify_gb300 import synth
+    import __graft_entry__
+    rank, world, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    cfg = synth.DECODER2
+    ver, win, w_cpu, caches_cpu, max_len, ctx = build_problem(cfg, device, seed_offset=0)
+    graphs = ver.capture(win, segments=True)
+    full_graph = ver.capture(win, segments=False)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        graphs[0].replay()
+        graphs[1].replay()
+        graphs[2].replay()
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        one_step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    out_dir = os.path.join(ROOT, "gpurun_out")
+    clk_path = os.path.join(out_dir if os.path.isdir(out_dir) else "/tmp", f"bench_clocks_rank{rank}.csv")
+    sampler, sf = clock_sampler_start(clk_path) if local == 0 else (None, None)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        e = ev[i]
+        e[0].record(stream)
+        graphs[0].replay()
+        e[1].record(stream)
+        graphs[1].replay()
+        e[2].record(stream)
+        graphs[2].replay()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clocks = clock_sampler_stop(sampler, sf, clk_path, local)
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    lm_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    tot_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([tot_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_per_step = tot_ms / K
+    value = cfg.W * world * K / (tot_ms / 1e3)
+    committed = int(ver.accept_len.sum().item())
+
+    # roofline of the dominant kernel (LM-head GEMM, HBM-bound at W=64)
+    hbm, bf16, src = peaks()
+    M, N, Kd = cfg.W, cfg.vocab, cfg.d
+    lm_bytes = 2 * N * Kd + 2 * M * Kd + 4 * M * N
+    lm_avg_s = statistics.mean(lm_ms) / 1e3
+    achieved = lm_bytes / lm_avg_s / 1e9
+    roofline = {"kernel": "gemm_nosplitk_kernel (LM head, M=64 N=32000 K=1024, fp32 out)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
+                "traffic": lm_head_traffic(), "algorithmic_bytes": lm_bytes,
+                "avg_launch_us": round(lm_avg_s * 1e6, 2)}
+    step_bytes, step_flops = step_work(cfg, ctx)
+    step_roof_us = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12)) * 1e6
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(ver, win, full_graph, flush, cfg, max(50, min(K, 2000)), world, device)
+
+    out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+           "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": workload_config(cfg) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+           "roofline": roofline,
+           "step_roofline": {"bytes": step_bytes, "flops": step_flops, "lower_bound_us": round(step_roof_us, 2),
+                             "frac": round(step_roof_us / (ms_per_step * 1e3), 4)},
+           "committed_tok_per_s": round(committed * world * K / (tot_ms / 1e3), 1),
+           "gpu_launches": ver.launches_per_step * K,
+           "timed_region_wall_s": round(wall, 3),
+           "clocks": clocks, "e2e": e2e}
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(cfg, w_cpu, caches_cpu, max_len, win, args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def step_work(cfg, ctx):
+    """Algorithmic bytes and flops of one step (weights once, KV read, logits
+    written and read, activations ignored)."""
+    W, d, F, V, hd = cfg.W, cfg.d, cfg.ffn, cfg.vocab, cfg.hd
+    per_layer_w = (cfg.qkv_n * d + d * cfg.Hq * hd + 2 * F * d + d * F) * 2
+    weights = cfg.layers * per_layer_w + V * d * 2
+    kv = sum(2 * 2 * cfg.Hkv * (int(c) + cfg.K) * hd for c in ctx) * cfg.layers
+    logits = 2 * 4 * W * V
+    flops = 2 * W * (cfg.layers * per_layer_w // 2 + V * d)
+    flops += cfg.layers * sum(4 * cfg.Hq * cfg.K * (int(c) + cfg.K) * hd for c in ctx)
+    return weights + kv + logits, flops
+
+
+def run_e2e(ver, win, graph, flush, cfg, K, world, device):
+    """Same metric through the public API with host buffers: each step copies
+    the window's inputs from pinned host memory, runs the step, and reads the
+    accept lengths, rollback points and selected tokens back."""
+    names = ["tokens", "row_slot", "row_req", "row_pos", "draft", "p0"]
+    host_in = {n: getattr(win, n).cpu().pin_memory() for n in names}
+    outs = [ver.accept_len, ver.new_len, ver.target]
+    host_out = [o.cpu().pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    stream = torch.cuda.current_stream()
+    total = 0.0
+    for i in range(K + 5):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for n in names:
+            getattr(win, n).copy_(host_in[n], non_blocking=True)
+        graph.replay()
+        for h, o in zip(host_out, outs):
+            h.copy_(o, non_blocking=True)
+        stream.synchronize()
+        if i >= 5:
+            total += time.perf_counter() - t0
+    value = cfg.W * world * K / total
+    return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": K, "ms_per_step": round(total / K * 1e3, 5),
+            "how": "pinned H2D of the window inputs + CUDA-graph step + D2H of accept_len/new_len/tokens + sync"}
+
+
+# ------------------------------------------------------- CPU oracle timing
+def oracle_rows_per_second(cfg, w_cpu, caches_cpu, max_len, win, seconds, max_steps=None, warmup=0):
+    import oracle
+    from oracle.model import OracleDecoder
+    orc = OracleDecoder(cfg, w_cpu, caches_cpu, cfg.N, max_len)
+    tokens = win.tokens.cpu().numpy()
+    slot = win.row_slot.cpu().numpy()
+    req = win.row_req.cpu().numpy()
+    pos = win.row_pos.cpu().numpy()
+    # The window's own K/V rows must be in the cache before single rows are
+    # verified: one full oracle forward writes them (not timed).
+    orc.forward(tokens, slot, pos)
+    W = tokens.size
+    done, spent, i = 0, 0.0, 0
+    while True:
+        r = i % W
+        t0 = time.perf_counter()
+        out = orc.forward(tokens[r:r + 1], slot[r:r + 1], pos[r:r + 1])
+        oracle.gumbel_argmax(out["logits"].astype(np.float32), req[r:r + 1], pos[r:r + 1], 0x1234_5678_9ABC_DEF0,
+                             cfg.temperature)
+        dt = time.perf_counter() - t0
+        i += 1
+        if i <= warmup:
+            continue
+        done += 1
+        spent += dt
+        if (max_steps is not None and done >= max_steps) or (max_steps is None and spent >= seconds):
+            break
+    import oracle as _o
+    return done / spent, done, spent, _o.num_threads()
+
+
+def cpu_baseline(cfg, w_cpu, caches_cpu, max_len, win, seconds):
+    v, n, spent, cores = oracle_rows_per_second(cfg, w_cpu, caches_cpu, max_len, win, seconds)
+    return {"value": round(v, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} window rows verified one at a time (all layers + LM head + selection, fp64) "
+                      f"in {spent:.1f} s on {cores} host threads"}
+
+
+# --------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    from invariant_verify_gb300 import synth
+    from invariant_verify_gb300.verifier import make_window
+    from oracle import build as ob
+    ob.build()
+    cfg = synth.DECODER2
+    w = synth.decoder_weights(cfg)
+    ctx = synth.context_lengths(cfg, cfg.N, seed=cfg.seed + 100)
+    max_len = int(ctx.max()) + 64
+    caches = synth.kv_cache(cfg.N, cfg.Hkv, max_len, cfg.hd, ctx, seed=cfg.seed + 200, layers=cfg.layers)
+    g = synth.generator(cfg.seed + 300)
+    toks = torch.randint(0, cfg.vocab, (cfg.W,), generator=g, dtype=torch.int64).to(torch.int32)
+    win = make_window(cfg.N, cfg.K, toks, ctx, torch.arange(cfg.N) * 1000 + 17, toks, device="cpu")
+    steps = max(1, args.steps)
+    v, n, spent, cores = oracle_rows_per_second(cfg, w, caches, max_len, win, 0.0, max_steps=steps,
+                                                warmup=max(0, min(args.warmup, 3)))
+    out = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": world,
+           "steps": n, "warmup": args.warmup, "ms_per_step": round(spent / n * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": workload_config(cfg) | {"parallelism": "host cores"},
+           "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": "one window row per step (all layers + LM head + selection, fp64)"},
+           "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

@@ -1,0 +1,230 @@
+/*
+ * libbiv -- batch-invariant verification step of deterministic LLM decoding,
+ * hand-written CUDA for sm_103a (GB300).
+ *
+ * Sources (pages cited by title and paragraph / section):
+ *   [DVR]      tgstat @ashnskt post 392: batch-invariant matmul / RMSNorm /
+ *              attention (para 1); LLM-42 Decode-Verify-Rollback: a fixed-batch
+ *              verifier anchored at the last correct token, rollback on
+ *              divergence, fast-path KV rows overwritten by the verifier
+ *              (para 3); W = N requests x K tokens in one verify batch (para 4).
+ *   [GUIDE]    "NVIDIA publishes AI inference guide, 6x lossless speedup":
+ *              speculative decoding (verify the drafts in one pass, restart at
+ *              the break point); GQA tile rule G * (1 + D) <= 128.
+ *   [COUPLING] tginsight AIexTime post 185 ("Coupling without Communication
+ *              and Drafter-Invariant Speculative Decoding"): Gumbel-max
+ *              sampling; the same noise for drafter and target, so the check
+ *              compares two tokens and the output does not depend on the
+ *              drafter.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or keeps them past the call.  bf16 tensors are raw
+ *     __nv_bfloat16 storage; every layout is dense row-major as stated.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work: they return before the GPU has run it.
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     rejected call returns a non-zero biv_status and launches nothing.  A
+ *     zero-sized problem (rows == 0 etc.) returns BIV_OK and launches nothing.
+ *   - Device-side checks (indices read from device memory: slots, positions,
+ *     token ids; bounded waits inside kernels) cannot be seen by the host at
+ *     call time.  They skip the offending row and set a bit in the library's
+ *     device error word, read with biv_device_error().
+ *   - Inputs are never modified, except the caches of biv_kv_overwrite and the
+ *     caller-provided workspace of biv_decode_attn_fixedsplit.
+ *   - The library allocates no device memory.
+ */
+#ifndef BIV_H_
+#define BIV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* biv_stream_t; /* identical to cudaStream_t */
+
+typedef enum biv_status {
+    BIV_OK = 0,
+    BIV_ERR_NULL = 1,        /* a required pointer is NULL                          */
+    BIV_ERR_SHAPE = 2,       /* a size is negative, inconsistent or out of range    */
+    BIV_ERR_ALIGN = 3,       /* a pointer or leading dimension breaks 16-B alignment */
+    BIV_ERR_VALUE = 4,       /* a scalar is out of its domain (eps, temperature, ...) */
+    BIV_ERR_UNSUPPORTED = 5, /* valid, but not built (head dim != 128, split != 256)  */
+    BIV_ERR_CUDA = 6,        /* a CUDA runtime call failed; see biv_last_cuda_error() */
+    BIV_ERR_DEVICE = 7       /* no usable sm_100-family device for this call          */
+} biv_status;
+
+typedef enum biv_dtype { BIV_BF16 = 0, BIV_F32 = 1 } biv_dtype;
+
+/* Device error word bits (biv_device_error). */
+#define BIV_DEVERR_TIMEOUT 1u /* a bounded wait inside a kernel ran out; the kernel returned */
+#define BIV_DEVERR_INDEX 2u   /* a slot / position / token id read from device memory was out of range */
+#define BIV_DEVERR_GROUP 4u   /* rows declared to share a cache slot did not */
+
+/* Build constants. */
+#define BIV_KV_SPLIT 256      /* fixed KV split of the decode attention ([DVR] para 1) */
+#define BIV_HEAD_DIM 128      /* attention head dimension built */
+#define BIV_ATTN_TILE 128     /* rows of one attention MMA tile ([GUIDE] GQA tile rule) */
+
+/* ------------------------------------------------------------- status */
+const char* biv_status_string(int status);           /* static string, never NULL */
+int biv_last_cuda_error(void);                        /* thread-local cudaError_t of the last BIV_ERR_CUDA */
+int biv_version(void);                                /* 100 * major + minor */
+
+/* Synchronises the device, then returns (and clears) the OR of all device
+ * error bits raised since the last call.  Returns BIV_ERR_CUDA if the
+ * synchronisation failed.  Not for the hot path. */
+int biv_device_error(uint32_t* bits_out);
+
+/* --------------------------------------------------------- RMSNorm
+ * [DVR] para 1: RMSNorm with a fixed split over the hidden dimension that
+ * does not depend on the batch or on how many SMs are busy.
+ *   y[r][i] = bf16( x[r][i] * rsqrt(mean_i x[r][i]^2 + eps) * w[i] )
+ * x, y: bf16 [rows, d]; w: bf16 [d].  fp32 accumulation in a fixed order
+ * (each thread owns fixed 8-element chunks; a fixed xor-butterfly inside the
+ * warp, then a fixed tree across warps), identical for every row count.
+ * Requires d % 8 == 0, 8 <= d <= 16384, eps > 0 finite, 16-B aligned pointers.
+ * y may alias x.                                                          */
+int biv_rmsnorm(const void* x, const void* w, void* y, int rows, int d, float eps,
+                biv_stream_t stream);
+
+/* --------------------------------------------------- no-split-K GEMM
+ * [DVR] para 1: a matmul that never splits K and always uses the same
+ * data-parallel tiling.
+ *   C[m][n] = sum_k A[m][k] * B[n][k]        (fp32 accumulation)
+ * A: bf16 [M, K] row-major; B: bf16 [N, K] row-major (nn.Linear weight);
+ * C: [M, N] row-major, bf16 (round-to-nearest-even) or fp32 per out_dtype.
+ * tcgen05 tensor-core MMAs (M tile 128, K step 16) accumulate in TMEM; the K
+ * loop runs in one CTA in increasing k, so every element's accumulation order
+ * is fixed and independent of M and of the tile that holds the row.
+ * Requires M >= 0, N % 8 == 0, K % 8 == 0, K > 0, N > 0, 16-B aligned pointers.
+ * C must not overlap A or B.                                              */
+int biv_gemm_nosplitk(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K,
+                      biv_stream_t stream);
+
+/* Same GEMM with the N-tile width forced (16, 32, 64, 128 or 256) instead of
+ * chosen from (N, K).  For tests of tile-shape independence and for tuning;
+ * results are bitwise identical to biv_gemm_nosplitk's.                    */
+int biv_gemm_nosplitk_bn(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K,
+                         int bn, biv_stream_t stream);
+
+/* The N-tile width biv_gemm_nosplitk uses for (N, K); a function of N and K
+ * only, never of M or of the device.                                       */
+int biv_gemm_tile_n(int N, int K);
+
+/* ------------------------------------------- fixed-split decode attention
+ * [DVR] para 1: attention with a fixed KV-split size that never adapts to the
+ * sequence length or the GPU load.  [GUIDE] GQA tile rule: the G = Hq/Hkv
+ * query heads sharing a KV head, times the verified rows of one request, are
+ * packed into one 128-row MMA tile.
+ * For each row w (cache slot s = row_slot[w], position p = row_pos[w]) and
+ * query head h (KV head h / (Hq/Hkv)):
+ *   o[w][h] = sum_{j<=p} softmax_j(q[w][h] . k[s][kvh][j] / sqrt(hd)) v[s][kvh][j]
+ * Keys are split at absolute multiples of BIV_KV_SPLIT; each split yields a
+ * partial (max, sum, unnormalised output) in fp32 and the splits of a row are
+ * combined in increasing split order.  A row's result depends only on its own
+ * q, its slot's cache and its position.
+ * q, o: bf16 [W, Hq, hd]; k_cache, v_cache: bf16 [n_slots, Hkv, max_len, hd].
+ * Rows [g*rows_per_group, (g+1)*rows_per_group) must share one cache slot (the
+ * K rows of one request in a W = N*K window, [DVR] para 4); rows_per_group = 1
+ * is always valid.  Positions must be < max_len and every cache row
+ * j <= p must hold finite values.
+ * workspace: device memory of at least biv_decode_attn_workspace_size(W, Hq,
+ * max_len) bytes, 16-B aligned, contents ignored on entry.
+ * Requires hd == 128, kv_split == 256, Hq % Hkv == 0, Hq/Hkv <= 128.        */
+size_t biv_decode_attn_workspace_size(int W, int Hq, int max_len);
+int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* row_slot, const int32_t* row_pos, void* o, int W,
+                               int rows_per_group, int Hq, int Hkv, int hd, int n_slots,
+                               int max_len, int kv_split, void* workspace, size_t ws_bytes,
+                               biv_stream_t stream);
+
+/* Largest number of drafts D with G * (1 + D) <= tile ([GUIDE] GQA tile rule:
+ * D = tile / G - 1).  Returns -1 when G <= 0 or G > tile.                  */
+int biv_gqa_max_drafts(int G, int tile);
+
+/* ------------------------------------------------------ KV overwrite
+ * [DVR] para 3: at each verification the fast path's cache rows are
+ * overwritten by the verifier's values.  Row w = r*K + j of the window writes
+ * k_new[w] and v_new[w] (bf16 [Hkv, hd] each; consecutive rows k_stride and
+ * v_stride elements apart) into its slot at position row_pos[w].  If
+ * rows_keep (int32 [N], N = W / K) is not NULL, only rows j < rows_keep[r]
+ * are written.  Rows with an out-of-range slot or position are skipped and
+ * raise BIV_DEVERR_INDEX.
+ * Requires hd % 8 == 0, strides % 8 == 0 and >= Hkv*hd, W % K == 0,
+ * 16-B aligned pointers.                                                  */
+int biv_kv_overwrite(void* k_cache, void* v_cache, const void* k_new, long long k_stride,
+                     const void* v_new, long long v_stride, const int32_t* row_slot,
+                     const int32_t* row_pos, const int32_t* rows_keep, int W, int K, int Hkv, int hd,
+                     int n_slots, int max_len, biv_stream_t stream);
+
+/* ----------------------------------------------------- Gumbel-max select
+ * [COUPLING]: adding Gumbel(0,1) noise to the logits and taking the argmax
+ * samples from softmax(logits / T) without computing a softmax; the noise does
+ * not depend on the logits.  Row r selects the token at position
+ * row_pos[r] + 1 of request row_req[r]:
+ *   w_v   = word (v & 3) of Philox4x32-10(counter = (v >> 2, row_pos[r] + 1,
+ *           row_req[r], 0), key = (seed & 0xffffffff, seed >> 32))
+ *   u_v   = (2 * (w_v >> 9) + 1) * 2^-24
+ *   g_v   = -L(-L(u_v)), L = the library's fp32 log (IEEE +,-,*,/,fma only)
+ *   key_v = fl(fl(logit_v * fl(1/T)) + g_v)
+ *   tokens[r] = the v with the largest key; the lowest v among equal keys;
+ *               a NaN key never beats a number.  T == 0 selects the largest
+ *               logit (lowest index on ties).
+ * The noise is a pure function of (seed, request, position, v), so the same
+ * token is selected at any batch size, with or without a drafter.
+ * logits: fp32 [R, ld] (first V columns used); row_req: uint32 [R];
+ * row_pos: int32 [R]; tokens: int32 [R].  Requires V % 4 == 0, ld % 4 == 0,
+ * ld >= V, V >= 4, T >= 0 finite, 16-B aligned logits.                    */
+int biv_gumbel_argmax(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                      const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
+                      biv_stream_t stream);
+
+/* The noise g_v of biv_gumbel_argmax for v in [0, V) of each row (fp32
+ * [R, V]); for tests of the noise itself.                                  */
+int biv_gumbel_noise(uint64_t seed, const uint32_t* row_req, const int32_t* row_pos, int R, int V,
+                     float* g, biv_stream_t stream);
+
+/* g = -L(-L(u(w))) for raw 32-bit words w[0..n); for tests of L.           */
+int biv_gumbel_from_words(const uint32_t* words, long long n, float* g, biv_stream_t stream);
+
+/* ----------------------------------------------------- coupled accept
+ * [COUPLING] + [GUIDE] + [DVR] para 3: with shared noise the check compares
+ * tokens only.  Row j of request r outputs target[r*K + j] = y_{j+1}, and
+ * draft[r*K + j] = d_{j+1} is the draft it must match.
+ *   accept_len[r] = (first j with y_{j+1} != d_{j+1}) + 1, or K if none
+ *   new_len[r]    = p0[r] + accept_len[r]   (rollback point)
+ * The emitted tokens are y_1 .. y_{accept_len}: always the target's own.
+ * All arrays int32.  Requires N >= 0, K >= 1.                              */
+int biv_verify_accept(const int32_t* target, const int32_t* draft, const int32_t* p0, int N, int K,
+                      int32_t* accept_len, int32_t* new_len, biv_stream_t stream);
+
+/* --------------------------------------- per-row glue of the decoder layer
+ * The pages do not describe the verifier model; these are the standard
+ * pre-norm Llama pieces needed to compose one (each row is independent).   */
+
+/* out[w] = table[tokens[w]] ; table bf16 [vocab, d], out bf16 [W, d], d % 8 == 0. */
+int biv_embed(const void* table, const int32_t* tokens, void* out, int W, int d, int vocab,
+              biv_stream_t stream);
+
+/* Rotate-half RoPE at the rows' positions.  qkv: bf16 [W, (Hq + 2 Hkv) * hd]
+ * (q heads, then k heads, then v heads); q_out: bf16 [W, Hq, hd]; k_out:
+ * bf16 [W, Hkv, hd].  Pair (i, i + hd/2) rotates by row_pos * theta^(-2i/hd).
+ * Requires hd % 2 == 0, hd <= 256, theta > 1.                              */
+int biv_rope_qk(const void* qkv, void* q_out, void* k_out, const int32_t* row_pos, int W, int Hq,
+                int Hkv, int hd, float theta, biv_stream_t stream);
+
+/* out[r][i] = bf16(silu(gu[r][i]) * gu[r][F + i]) ; gu bf16 [rows, 2F], F % 8 == 0. */
+int biv_silu_mul(const void* gu, void* out, int rows, int F, biv_stream_t stream);
+
+/* out[i] = bf16(x[i] + y[i]) over n bf16 elements, n % 8 == 0; out may alias x. */
+int biv_residual_add(const void* x, const void* y, void* out, long long n, biv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIV_H_ */

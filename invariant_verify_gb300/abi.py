@@ -1,0 +1,206 @@
+"""Thin ctypes binding of libbiv (``include/biv.h``), same names as the C ABI.
+
+Each ``biv_*`` function takes torch CUDA tensors, passes their raw device
+pointers, sizes and the current CUDA stream to the C entry point of the same
+name, and raises ``BivError`` on a non-zero status.  There is no fallback:
+if ``libbiv.so`` has not been built, loading raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libbiv.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "biv.h")
+
+BIV_BF16, BIV_F32 = 0, 1
+KV_SPLIT, HEAD_DIM, ATTN_TILE = 256, 128, 128
+
+_lib = None
+
+
+class BivError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = _load().biv_status_string(status).decode()
+        extra = ""
+        if status == 6:
+            extra = f" (cudaError {_load().biv_last_cuda_error()})"
+        super().__init__(f"{fn}: status {status}: {msg}{extra}")
+        self.status = status
+
+
+_P, _I, _LL, _F, _U64, _SZ = C.c_void_p, C.c_int, C.c_longlong, C.c_float, C.c_uint64, C.c_size_t
+SIGNATURES = {
+    "biv_status_string": (C.c_char_p, [_I]),
+    "biv_last_cuda_error": (_I, []),
+    "biv_version": (_I, []),
+    "biv_device_error": (_I, [_P]),
+    "biv_rmsnorm": (_I, [_P, _P, _P, _I, _I, _F, _P]),
+    "biv_gemm_nosplitk": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    "biv_gemm_nosplitk_bn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "biv_gemm_tile_n": (_I, [_I, _I]),
+    "biv_decode_attn_workspace_size": (_SZ, [_I, _I, _I]),
+    "biv_decode_attn_fixedsplit": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "biv_gqa_max_drafts": (_I, [_I, _I]),
+    "biv_kv_overwrite": (_I, [_P, _P, _P, _LL, _P, _LL, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "biv_gumbel_argmax": (_I, [_P, _I, _I, _LL, _P, _P, _U64, _F, _P, _P]),
+    "biv_gumbel_noise": (_I, [_U64, _P, _P, _I, _I, _P, _P]),
+    "biv_gumbel_from_words": (_I, [_P, _LL, _P, _P]),
+    "biv_verify_accept": (_I, [_P, _P, _P, _I, _I, _P, _P, _P]),
+    "biv_embed": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "biv_rope_qk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
+    "biv_silu_mul": (_I, [_P, _P, _I, _I, _P]),
+    "biv_residual_add": (_I, [_P, _P, _P, _LL, _P]),
+}
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libbiv.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        lib = C.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def lib():
+    return _load()
+
+
+def _check(name: str, status: int) -> None:
+    if status != 0:
+        raise BivError(name, status)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ----------------------------------------------------------------- status
+def biv_status_string(status: int) -> str:
+    return _load().biv_status_string(int(status)).decode()
+
+
+def biv_version() -> int:
+    return _load().biv_version()
+
+
+def biv_device_error() -> int:
+    bits = C.c_uint32(0)
+    _check("biv_device_error", _load().biv_device_error(C.byref(bits)))
+    return int(bits.value)
+
+
+# ---------------------------------------------------------------- kernels
+def biv_rmsnorm(x, w, y, eps: float, stream=None) -> None:
+    rows, d = x.shape
+    _check("biv_rmsnorm", _load().biv_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, d, eps, _stream(stream)))
+
+
+def biv_gemm_nosplitk(A, B, C_out, stream=None, bn: int | None = None) -> None:
+    M, K = A.shape
+    N = B.shape[0]
+    dt = BIV_F32 if C_out.dtype == torch.float32 else BIV_BF16
+    if bn is None:
+        st = _load().biv_gemm_nosplitk(_ptr(A), _ptr(B), _ptr(C_out), dt, M, N, K, _stream(stream))
+    else:
+        st = _load().biv_gemm_nosplitk_bn(_ptr(A), _ptr(B), _ptr(C_out), dt, M, N, K, bn, _stream(stream))
+    _check("biv_gemm_nosplitk", st)
+
+
+def biv_gemm_tile_n(N: int, K: int) -> int:
+    return _load().biv_gemm_tile_n(N, K)
+
+
+def biv_decode_attn_workspace_size(W: int, Hq: int, max_len: int) -> int:
+    return int(_load().biv_decode_attn_workspace_size(W, Hq, max_len))
+
+
+def biv_decode_attn_fixedsplit(q, k_cache, v_cache, row_slot, row_pos, o, rows_per_group: int, workspace,
+                               stream=None) -> None:
+    W, Hq, hd = q.shape
+    n_slots, Hkv, max_len, _ = k_cache.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("biv_decode_attn_fixedsplit", _load().biv_decode_attn_fixedsplit(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(row_slot), _ptr(row_pos), _ptr(o), W, rows_per_group,
+        Hq, Hkv, hd, n_slots, max_len, KV_SPLIT, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def biv_gqa_max_drafts(G: int, tile: int = ATTN_TILE) -> int:
+    return _load().biv_gqa_max_drafts(G, tile)
+
+
+def biv_kv_overwrite(k_cache, v_cache, k_new, v_new, row_slot, row_pos, K: int, rows_keep=None,
+                     stream=None) -> None:
+    """k_new / v_new: 2-D views [W, >= Hkv*hd] (row strides taken from the tensors)."""
+    n_slots, Hkv, max_len, hd = k_cache.shape
+    W = row_slot.shape[0]
+    _check("biv_kv_overwrite", _load().biv_kv_overwrite(
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_new), k_new.stride(0), _ptr(v_new), v_new.stride(0),
+        _ptr(row_slot), _ptr(row_pos), _ptr(rows_keep), W, K, Hkv, hd, n_slots, max_len, _stream(stream)))
+
+
+def biv_gumbel_argmax(logits, row_req, row_pos, seed: int, temperature: float, tokens, V: int | None = None,
+                      stream=None) -> None:
+    R, ld = logits.shape
+    V = ld if V is None else V
+    _check("biv_gumbel_argmax", _load().biv_gumbel_argmax(
+        _ptr(logits), R, V, logits.stride(0), _ptr(row_req), _ptr(row_pos), seed & 0xFFFFFFFFFFFFFFFF,
+        float(temperature), _ptr(tokens), _stream(stream)))
+
+
+def biv_gumbel_noise(seed: int, row_req, row_pos, g, stream=None) -> None:
+    R, V = g.shape
+    _check("biv_gumbel_noise", _load().biv_gumbel_noise(
+        seed & 0xFFFFFFFFFFFFFFFF, _ptr(row_req), _ptr(row_pos), R, V, _ptr(g), _stream(stream)))
+
+
+def biv_gumbel_from_words(words, g, stream=None) -> None:
+    _check("biv_gumbel_from_words", _load().biv_gumbel_from_words(
+        _ptr(words), words.numel(), _ptr(g), _stream(stream)))
+
+
+def biv_verify_accept(target, draft, p0, N: int, K: int, accept_len, new_len, stream=None) -> None:
+    _check("biv_verify_accept", _load().biv_verify_accept(
+        _ptr(target), _ptr(draft), _ptr(p0), N, K, _ptr(accept_len), _ptr(new_len), _stream(stream)))
+
+
+def biv_embed(table, tokens, out, stream=None) -> None:
+    vocab, d = table.shape
+    _check("biv_embed", _load().biv_embed(_ptr(table), _ptr(tokens), _ptr(out), tokens.shape[0], d, vocab,
+                                          _stream(stream)))
+
+
+def biv_rope_qk(qkv, q_out, k_out, row_pos, Hq: int, Hkv: int, hd: int, theta: float, stream=None) -> None:
+    W = qkv.shape[0]
+    _check("biv_rope_qk", _load().biv_rope_qk(_ptr(qkv), _ptr(q_out), _ptr(k_out), _ptr(row_pos), W, Hq, Hkv, hd,
+                                              float(theta), _stream(stream)))
+
+
+def biv_silu_mul(gu, out, stream=None) -> None:
+    rows, two_f = gu.shape
+    _check("biv_silu_mul", _load().biv_silu_mul(_ptr(gu), _ptr(out), rows, two_f // 2, _stream(stream)))
+
+
+def biv_residual_add(x, y, out, stream=None) -> None:
+    _check("biv_residual_add", _load().biv_residual_add(_ptr(x), _ptr(y), _ptr(out), x.numel(), _stream(stream)))

@@ -1,0 +1,508 @@
+// Fixed-split decode attention, RoPE and the verifier's KV overwrite.
+//
+// [DVR] para 1: batch-invariant attention uses a fixed KV-split size with no
+// adaptation to sequence length or GPU load.  [DVR] para 3: the verifier
+// overwrites the fast path's cache rows with its own values before they are
+// attended to.  [GUIDE] GQA tile rule: the G query heads that share a KV head,
+// times the verified rows of one request, fill one 128-row MMA tile
+// (G * (1 + D) <= 128).
+//
+// Phase 1, one CTA per (row tile, KV head, split of 256 absolute positions):
+// the tile holds up to 128/G consecutive rows of one request times its G
+// query heads.  K and V of the split are staged in shared memory once
+// (cp.async, XOR-swizzled 16-byte chunks) and every row of the tile reuses
+// them.  Each compute warp owns 16 tile rows; per 64-key chunk it forms
+// S = Q K^T with bf16 mma.sync (fp32 accumulate), masks keys beyond the
+// row's own position with a select, and updates an online softmax in a
+// fixed order.  The split's partial (max, sum, unnormalised output) goes to
+// the caller's workspace.  Phase 2 combines the splits 0..p/256 of each
+// (row, head) in increasing order.  Nothing in a row's arithmetic depends on
+// the other rows of the tile or the batch: masked keys contribute exact
+// zeros and chunks beyond a row's position leave its state unchanged.
+//
+// The contraction per split is tiny (16..128 rows x 256 keys x 128), so the
+// kernel is bound by reading K and V from HBM, not by the tensor pipe;
+// mma.sync is ample here.
+#include <algorithm>
+#include <cmath>
+
+#include "biv_common.cuh"
+
+namespace biv {
+namespace {
+
+BIV_DEFINE_ERR_WORD(g_attn_err)
+
+constexpr int HD = BIV_HEAD_DIM;        // 128
+constexpr int SPLIT = BIV_KV_SPLIT;     // 256
+constexpr int CHUNK = 64;               // keys per online-softmax step
+constexpr int ROWB = HD * 2;            // 256 bytes per K/V/Q row in shared memory
+constexpr int ATTN_THREADS = 256;
+
+// Byte offset of (row, 16-byte chunk) in a swizzled [rows][128] bf16 tile.
+BIV_DEV uint32_t swz(int row, int chunk) {
+    return static_cast<uint32_t>(row * ROWB + ((chunk ^ (row & 7)) << 4));
+}
+
+BIV_DEV void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+BIV_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+BIV_DEV void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+BIV_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+BIV_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D = A (16x16 bf16, row) * B (16x8 bf16, col) + D, fp32.
+BIV_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                            uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+struct AttnParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* kc;
+    const __nv_bfloat16* vc;
+    const int32_t* row_slot;
+    const int32_t* row_pos;
+    float* ws_o;      // [W][Hq][S_max][HD]
+    float* ws_m;      // [W][Hq][S_max]
+    float* ws_l;      // [W][Hq][S_max]
+    int W, rows_per_group, tile_rows, tiles_per_group;
+    int Hq, Hkv, G, n_slots, max_len, s_max;
+    float scale_log2;  // log2(e) / sqrt(HD)
+};
+
+// Is row w usable for a tile whose first row is w0 (device-side checks)?
+BIV_DEV bool row_ok(const AttnParams& P, int w, int slot0) {
+    const int s = P.row_slot[w], p = P.row_pos[w];
+    if (s < 0 || s >= P.n_slots || p < 0 || p >= P.max_len) {
+        atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
+        return false;
+    }
+    if (s != slot0) {
+        atomicOr(&g_attn_err, BIV_DEVERR_GROUP);
+        return false;
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(ATTN_THREADS)
+attn_split_kernel(const AttnParams P) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_pos[BIV_ATTN_TILE];
+    __shared__ int s_maxpos;
+
+    const int split = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int tile = blockIdx.z;
+    const int group = tile / P.tiles_per_group;
+    const int sub = tile - group * P.tiles_per_group;
+    const int row0 = group * P.rows_per_group + sub * P.tile_rows;
+    const int row_end = min(min(row0 + P.tile_rows, (group + 1) * P.rows_per_group), P.W);
+    const int nr = row_end - row0;
+    if (nr <= 0) return;
+    const int T = nr * P.G;                     // live tile rows (row-major over (row, head))
+    const int T16 = (T + 15) & ~15;
+    const int key0 = split * SPLIT;
+
+    const int slot0 = P.row_slot[row0];
+    if (threadIdx.x == 0) {
+        s_maxpos = -1;
+        if (slot0 < 0 || slot0 >= P.n_slots) atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
+    }
+    __syncthreads();
+    if (threadIdx.x < nr) {
+        const int w = row0 + threadIdx.x;
+        int p = -1;
+        if (slot0 >= 0 && slot0 < P.n_slots && row_ok(P, w, slot0)) p = P.row_pos[w];
+        s_pos[threadIdx.x] = p;
+        atomicMax(&s_maxpos, p);
+    }
+    __syncthreads();
+    const int maxpos = s_maxpos;
+    if (maxpos < key0) return;                  // no row of the tile reaches this split
+    const int n_keys = min(SPLIT, maxpos + 1 - key0);
+    const int n_chunks = (n_keys + CHUNK - 1) / CHUNK;
+
+    uint8_t* sQ = smem;                         // [T16][HD]
+    uint8_t* sK = smem + T16 * ROWB;            // [SPLIT][HD]
+    uint8_t* sV = sK + SPLIT * ROWB;            // [SPLIT][HD]
+    const uint32_t uQ = smem_u32(sQ), uK = smem_u32(sK), uV = smem_u32(sV);
+
+    // ---- stage Q (zero rows >= T), then K/V per 64-key chunk, one commit group each
+    for (int idx = threadIdx.x; idx < T16 * 16; idx += ATTN_THREADS) {
+        const int t = idx >> 4, c = idx & 15;
+        if (t < T) {
+            const int i = t / P.G, g = t - i * P.G;
+            const __nv_bfloat16* src =
+                P.q + (static_cast<long long>(row0 + i) * P.Hq + kvh * P.G + g) * HD + c * 8;
+            cp_async16(uQ + swz(t, c), src);
+        } else {
+            *reinterpret_cast<uint4*>(sQ + swz(t, c)) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    const long long kv_base = (static_cast<long long>(slot0) * P.Hkv + kvh) * P.max_len + key0;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+        if (ch < n_chunks) {
+            for (int idx = threadIdx.x; idx < CHUNK * 16; idx += ATTN_THREADS) {
+                const int j = ch * CHUNK + (idx >> 4), c = idx & 15;
+                if (j < n_keys) {
+                    const long long off = (kv_base + j) * HD + c * 8;
+                    cp_async16(uK + swz(j, c), P.kc + off);
+                    cp_async16(uV + swz(j, c), P.vc + off);
+                } else {
+                    *reinterpret_cast<uint4*>(sK + swz(j, c)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(sV + swz(j, c)) = make_uint4(0, 0, 0, 0);
+                }
+            }
+        }
+        cp_async_commit();
+    }
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, cq = lane & 3;     // mma fragment coordinates
+    const bool computes = warp * 16 < T16;
+    const int trow_a = warp * 16 + gq, trow_b = trow_a + 8;
+    // Row positions of this thread's two tile rows (-1: not a live row).
+    const int pos_a = (computes && trow_a < T) ? s_pos[trow_a / P.G] : -1;
+    const int pos_b = (computes && trow_b < T) ? s_pos[trow_b / P.G] : -1;
+
+    float o[16][4];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
+
+#pragma unroll 1
+    for (int ch = 0; ch < n_chunks; ++ch) {
+        switch (ch) {
+            case 0: cp_async_wait<3>(); break;
+            case 1: cp_async_wait<2>(); break;
+            case 2: cp_async_wait<1>(); break;
+            default: cp_async_wait<0>(); break;
+        }
+        __syncthreads();
+        if (!computes) continue;
+
+        // ---- S = Q K^T for 16 rows x 64 keys
+        float s[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(uQ + swz(warp * 16 + (lane & 15), kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                const int j = lane >> 3;
+                const int key = ch * CHUNK + np * 16 + (j >> 1) * 8 + (lane & 7);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(uK + swz(key, kk * 2 + (j & 1)), b0, b1, b2, b3);
+                mma_bf16_16816(s[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_bf16_16816(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+
+        // ---- mask (select, never multiply), scale into log2 units, chunk max
+        const int kbase = key0 + ch * CHUNK + cq * 2;
+        float cmax_a = -INFINITY, cmax_b = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int key = kbase + n * 8 + e;
+                s[n][e] = key <= pos_a ? s[n][e] * P.scale_log2 : -INFINITY;
+                s[n][2 + e] = key <= pos_b ? s[n][2 + e] * P.scale_log2 : -INFINITY;
+                cmax_a = fmaxf(cmax_a, s[n][e]);
+                cmax_b = fmaxf(cmax_b, s[n][2 + e]);
+            }
+        }
+        cmax_a = fmaxf(cmax_a, __shfl_xor_sync(0xffffffffu, cmax_a, 1));
+        cmax_a = fmaxf(cmax_a, __shfl_xor_sync(0xffffffffu, cmax_a, 2));
+        cmax_b = fmaxf(cmax_b, __shfl_xor_sync(0xffffffffu, cmax_b, 1));
+        cmax_b = fmaxf(cmax_b, __shfl_xor_sync(0xffffffffu, cmax_b, 2));
+        const float mn_a = fmaxf(m_a, cmax_a), mn_b = fmaxf(m_b, cmax_b);
+        const float mu_a = mn_a == -INFINITY ? 0.0f : mn_a;   // a row with nothing valid yet
+        const float mu_b = mn_b == -INFINITY ? 0.0f : mn_b;
+        const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
+        m_a = mn_a;
+        m_b = mn_b;
+        float ps_a = 0.0f, ps_b = 0.0f;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                s[n][e] = exp2f(s[n][e] - mu_a);
+                s[n][2 + e] = exp2f(s[n][2 + e] - mu_b);
+                ps_a += s[n][e];
+                ps_b += s[n][2 + e];
+            }
+        }
+        l_a = l_a * al_a + ps_a;
+        l_b = l_b * al_b + ps_b;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            o[n][0] *= al_a;
+            o[n][1] *= al_a;
+            o[n][2] *= al_b;
+            o[n][3] *= al_b;
+        }
+
+        // ---- O += P V  (P from the S accumulators, V via transposed ldmatrix)
+#pragma unroll
+        for (int kk = 0; kk < CHUNK / 16; ++kk) {
+            const uint32_t p0 = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+            const uint32_t p1 = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+            const uint32_t p2 = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+            const uint32_t p3 = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+            for (int nd = 0; nd < HD / 16; ++nd) {
+                const int j = lane >> 3;
+                const int key = ch * CHUNK + kk * 16 + (j & 1) * 8 + (lane & 7);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(uV + swz(key, nd * 2 + (j >> 1)), b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * nd], p0, p1, p2, p3, b0, b1);
+                mma_bf16_16816(o[2 * nd + 1], p0, p1, p2, p3, b2, b3);
+            }
+        }
+    }
+    if (!computes) return;
+
+    // ---- row sums across the quad (fixed order), write the split's partial
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int trow = half ? trow_b : trow_a;
+        const int pos = half ? pos_b : pos_a;
+        if (pos < key0) continue;               // dead row, or a row that ends before this split
+        const int i = trow / P.G, g = trow - i * P.G;
+        const long long ph = (static_cast<long long>(row0 + i) * P.Hq + kvh * P.G + g) * P.s_max + split;
+        float* dst = P.ws_o + ph * HD + cq * 2;
+#pragma unroll
+        for (int n = 0; n < 16; ++n)
+            *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][half * 2], o[n][half * 2 + 1]);
+        if (cq == 0) {
+            P.ws_m[ph] = half ? m_b : m_a;
+            P.ws_l[ph] = half ? l_b : l_a;
+        }
+    }
+}
+
+// One warp per (row, head): combine splits 0 .. pos/256 in increasing order.
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
+    const long long pair = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (pair >= static_cast<long long>(P.W) * P.Hq) return;
+    const int w = static_cast<int>(pair / P.Hq);
+    const int grp0 = (w / P.rows_per_group) * P.rows_per_group;
+    const int slot = P.row_slot[w], p = P.row_pos[w], slot0 = P.row_slot[grp0];
+    __nv_bfloat16* dst = out + pair * HD + lane * 4;
+    if (slot < 0 || slot >= P.n_slots || p < 0 || p >= P.max_len || slot != slot0) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+        return;
+    }
+    const int ns = p / SPLIT + 1;
+    const long long base = pair * P.s_max;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, P.ws_m[base + s]);
+    float L = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < ns; ++s) {
+        const float wgt = exp2f(P.ws_m[base + s] - M);
+        L += wgt * P.ws_l[base + s];
+        const float4 v = *reinterpret_cast<const float4*>(P.ws_o + (base + s) * HD + lane * 4);
+        acc.x += wgt * v.x;
+        acc.y += wgt * v.y;
+        acc.z += wgt * v.z;
+        acc.w += wgt * v.w;
+    }
+    const float inv = 1.0f / L;
+    uint2 r;
+    r.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    r.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(dst) = r;
+}
+
+// ------------------------------------------------------------------ RoPE
+__global__ void rope_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __restrict__ q_out,
+                            __nv_bfloat16* __restrict__ k_out, const int32_t* __restrict__ row_pos, int W,
+                            int Hq, int Hkv, int hd, float theta) {
+    const int half = hd / 2;
+    const long long total = static_cast<long long>(W) * (Hq + Hkv) * half;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int i = static_cast<int>(idx % half);
+        const long long rh = idx / half;
+        const int h = static_cast<int>(rh % (Hq + Hkv));
+        const int w = static_cast<int>(rh / (Hq + Hkv));
+        const __nv_bfloat16* src = qkv + (static_cast<long long>(w) * (Hq + 2 * Hkv) + h) * hd;
+        const float inv_freq = powf(theta, -2.0f * static_cast<float>(i) / static_cast<float>(hd));
+        const float ang = static_cast<float>(row_pos[w]) * inv_freq;
+        float sn, cs;
+        sincosf(ang, &sn, &cs);
+        const float a = __bfloat162float(src[i]), b = __bfloat162float(src[i + half]);
+        __nv_bfloat16* dst = h < Hq ? q_out + (static_cast<long long>(w) * Hq + h) * hd
+                                    : k_out + (static_cast<long long>(w) * Hkv + (h - Hq)) * hd;
+        dst[i] = __float2bfloat16_rn(a * cs - b * sn);
+        dst[i + half] = __float2bfloat16_rn(b * cs + a * sn);
+    }
+}
+
+// ---------------------------------------------------------- KV overwrite
+__global__ void kv_overwrite_kernel(__nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc,
+                                    const __nv_bfloat16* __restrict__ k_new, long long k_stride,
+                                    const __nv_bfloat16* __restrict__ v_new, long long v_stride,
+                                    const int32_t* __restrict__ row_slot,
+                                    const int32_t* __restrict__ row_pos, const int32_t* __restrict__ rows_keep,
+                                    int K, int Hkv, int hd, int n_slots, int max_len) {
+    const int w = blockIdx.x;
+    const int slot = row_slot[w], p = row_pos[w];
+    if (rows_keep && (w % K) >= rows_keep[w / K]) return;
+    if (slot < 0 || slot >= n_slots || p < 0 || p >= max_len) {
+        if (threadIdx.x == 0) atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
+        return;
+    }
+    const int chunks = Hkv * hd / 8;
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+        const int h = c / (hd / 8), e = (c % (hd / 8)) * 8;
+        const long long dst = ((static_cast<long long>(slot) * Hkv + h) * max_len + p) * hd + e;
+        const long long off = static_cast<long long>(h) * hd + e;
+        *reinterpret_cast<uint4*>(kc + dst) = *reinterpret_cast<const uint4*>(k_new + w * k_stride + off);
+        *reinterpret_cast<uint4*>(vc + dst) = *reinterpret_cast<const uint4*>(v_new + w * v_stride + off);
+    }
+}
+
+long long splits_for(int max_len) { return (static_cast<long long>(max_len) + SPLIT - 1) / SPLIT; }
+
+}  // namespace
+}  // namespace biv
+
+using namespace biv;
+
+extern "C" size_t biv_decode_attn_workspace_size(int W, int Hq, int max_len) {
+    if (W <= 0 || Hq <= 0 || max_len <= 0) return 0;
+    const long long pairs = static_cast<long long>(W) * Hq * splits_for(max_len);
+    return static_cast<size_t>(pairs) * (HD + 2) * sizeof(float);
+}
+
+extern "C" int biv_gqa_max_drafts(int G, int tile) {
+    if (G <= 0 || G > tile) return -1;
+    return tile / G - 1;
+}
+
+extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* row_slot, const int32_t* row_pos, void* o, int W,
+                                          int rows_per_group, int Hq, int Hkv, int hd, int n_slots, int max_len,
+                                          int kv_split, void* workspace, size_t ws_bytes, biv_stream_t stream) {
+    if (W < 0 || Hq <= 0 || Hkv <= 0 || n_slots <= 0 || max_len <= 0 || rows_per_group <= 0)
+        return BIV_ERR_SHAPE;
+    if (hd != HD || kv_split != SPLIT) return BIV_ERR_UNSUPPORTED;
+    if (Hq % Hkv != 0 || Hq / Hkv > BIV_ATTN_TILE) return BIV_ERR_SHAPE;
+    if (W == 0) return BIV_OK;
+    if (!q || !k_cache || !v_cache || !row_slot || !row_pos || !o || !workspace) return BIV_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace))
+        return BIV_ERR_ALIGN;
+    if (ws_bytes < biv_decode_attn_workspace_size(W, Hq, max_len)) return BIV_ERR_SHAPE;
+    const long long s_max = splits_for(max_len);
+    if (s_max > 65535) return BIV_ERR_SHAPE;
+
+    AttnParams P;
+    P.q = static_cast<const __nv_bfloat16*>(q);
+    P.kc = static_cast<const __nv_bfloat16*>(k_cache);
+    P.vc = static_cast<const __nv_bfloat16*>(v_cache);
+    P.row_slot = row_slot;
+    P.row_pos = row_pos;
+    const long long pairs = static_cast<long long>(W) * Hq * s_max;
+    P.ws_o = static_cast<float*>(workspace);
+    P.ws_m = P.ws_o + pairs * HD;
+    P.ws_l = P.ws_m + pairs;
+    P.W = W;
+    P.G = Hq / Hkv;
+    P.rows_per_group = std::min(rows_per_group, W);
+    P.tile_rows = std::min(P.rows_per_group, BIV_ATTN_TILE / P.G);
+    P.tiles_per_group = (P.rows_per_group + P.tile_rows - 1) / P.tile_rows;
+    P.Hq = Hq;
+    P.Hkv = Hkv;
+    P.n_slots = n_slots;
+    P.max_len = max_len;
+    P.s_max = static_cast<int>(s_max);
+    P.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+
+    const long long n_groups = (W + P.rows_per_group - 1) / P.rows_per_group;
+    const long long n_tiles = n_groups * P.tiles_per_group;
+    if (n_tiles > 65535 || Hkv > 65535) return BIV_ERR_SHAPE;
+    const int T16max = ((P.tile_rows * P.G + 15) / 16) * 16;
+    const size_t smem = static_cast<size_t>(T16max + 2 * SPLIT) * ROWB;
+
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (BIV_ATTN_TILE + 2 * SPLIT) * ROWB);
+        if (e != cudaSuccess) return cuda_status(e);
+        configured_device = dev;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    attn_split_kernel<<<dim3(static_cast<unsigned>(s_max), Hkv, static_cast<unsigned>(n_tiles)), ATTN_THREADS, smem,
+                        s>>>(P);
+    int st = launch_status();
+    if (st != BIV_OK) return st;
+    const long long n_pairs = static_cast<long long>(W) * Hq;
+    attn_combine_kernel<<<static_cast<unsigned>((n_pairs + 7) / 8), 256, 0, s>>>(P,
+                                                                                 static_cast<__nv_bfloat16*>(o));
+    return launch_status();
+}
+
+extern "C" int biv_rope_qk(const void* qkv, void* q_out, void* k_out, const int32_t* row_pos, int W, int Hq,
+                           int Hkv, int hd, float theta, biv_stream_t stream) {
+    if (W < 0 || Hq <= 0 || Hkv < 0 || hd <= 0 || hd % 2 != 0 || hd > 256) return BIV_ERR_SHAPE;
+    if (!(theta > 1.0f) || !std::isfinite(theta)) return BIV_ERR_VALUE;
+    if (W == 0) return BIV_OK;
+    if (!qkv || !q_out || !row_pos || (Hkv > 0 && !k_out)) return BIV_ERR_NULL;
+    const long long total = static_cast<long long>(W) * (Hq + Hkv) * (hd / 2);
+    const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 8192));
+    rope_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(q_out),
+        static_cast<__nv_bfloat16*>(k_out), row_pos, W, Hq, Hkv, hd, theta);
+    return launch_status();
+}
+
+extern "C" int biv_kv_overwrite(void* k_cache, void* v_cache, const void* k_new, long long k_stride,
+                                const void* v_new, long long v_stride, const int32_t* row_slot,
+                                const int32_t* row_pos, const int32_t* rows_keep, int W, int K, int Hkv, int hd,
+                                int n_slots, int max_len, biv_stream_t stream) {
+    if (W < 0 || K < 1 || Hkv <= 0 || hd <= 0 || n_slots <= 0 || max_len <= 0) return BIV_ERR_SHAPE;
+    const long long row = static_cast<long long>(Hkv) * hd;
+    if (hd % 8 != 0 || k_stride % 8 != 0 || v_stride % 8 != 0 || k_stride < row || v_stride < row)
+        return BIV_ERR_SHAPE;
+    if (W % K != 0) return BIV_ERR_SHAPE;
+    if (W == 0) return BIV_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new || !row_slot || !row_pos) return BIV_ERR_NULL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new)) return BIV_ERR_ALIGN;
+    kv_overwrite_kernel<<<W, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache),
+        static_cast<const __nv_bfloat16*>(k_new), k_stride, static_cast<const __nv_bfloat16*>(v_new), v_stride,
+        row_slot, row_pos, rows_keep, K, Hkv, hd, n_slots, max_len);
+    return launch_status();
+}

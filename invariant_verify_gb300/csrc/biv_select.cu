@@ -1,0 +1,411 @@
+// Seeded Gumbel-max token selection and the coupled accept / rollback check.
+//
+// [COUPLING] (AIexTime post 185): adding Gumbel(0,1) noise to the logits and
+// taking the argmax samples from the softmax without computing one; the
+// noise is independent of the logits, and when drafter and target share it
+// the verifier only compares two tokens.  Here the noise of vocabulary entry
+// v at position p of request r is a pure function of (seed, r, p, v) built
+// from Philox4x32-10 (Salmon et al., SC'11), a fixed uniform map and an fp32
+// log made only of IEEE +, -, *, /, fma -- so a row gets the same token at
+// any batch size, on any machine that follows the same operation sequence.
+//
+// Selection kernel: one thread-block cluster of 8 CTAs per row.  Each CTA
+// stages a contiguous slice of the row in shared memory with bulk async
+// copies (one pass over HBM), finds its slice maximum, and the cluster agrees
+// on a lower bound LB = the largest key among the 8 slice maxima (DSMEM).
+// A group of 4 logits (one Philox call) is skipped when even the largest
+// possible noise cannot lift it to LB:
+//     fl(fl(max4 * invT) + G_BOUND) < LB          (strict)
+// which is exact: rounding is monotone, every noise value is < G_BOUND = 17
+// (the noise lies in [-2.82, 16.64] over all 2^23 uniforms), so no skipped
+// entry can reach LB, and the winner's key is >= LB.  Survivors get their
+// noise and key; the winner is the maximum of a 64-bit packed value
+// (order(key) << 32 | ~v), which puts larger keys first and lower indices
+// first among equal keys, so any reduction order gives the same token.
+#include "biv_common.cuh"
+
+namespace biv {
+namespace {
+
+BIV_DEFINE_ERR_WORD(g_select_err)
+
+constexpr int kClusterSize = 8;
+constexpr int kSelThreads = 256;
+constexpr int kPieces = 4;
+constexpr int kMaxSliceFloats = 57344;          // 224 KiB of shared memory per CTA
+constexpr float kNoiseBound = 17.0f;
+
+// ----------------------------------------------------------- Philox4x32-10
+struct U4 { uint32_t x, y, z, w; };
+
+BIV_DEV U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ k0;
+        const uint32_t n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return U4{c0, c1, c2, c3};
+}
+
+// ------------------------------------------------------------- own log
+// ln x for positive normal x: x = m 2^e, m in [fl(sqrt2)/2, fl(sqrt2)),
+// f = m - 1, s = f / (2 + f), ln m = 2 s sum_{k<=6} s^2k / (2k+1) (Horner,
+// fma), ln x = e ln2_hi + (e ln2_lo + ln m), ln2_hi = 0x1.62e4p-1 (17 bits),
+// ln2_lo = fl(ln 2 - ln2_hi).  Every step is one correctly rounded IEEE op.
+BIV_DEV float own_log(float x) {
+    const uint32_t b = __float_as_uint(x);
+    int e = static_cast<int>((b >> 23) & 0xffu) - 127;
+    const uint32_t frac = b & 0x007fffffu;
+    uint32_t mb = frac | 0x3f800000u;
+    if (frac >= 0x003504f3u) {
+        mb -= 0x00800000u;
+        e += 1;
+    }
+    const float m = __uint_as_float(mb);
+    const float f = __fsub_rn(m, 1.0f);
+    const float t = __fadd_rn(2.0f, f);
+    const float s = __fdiv_rn(f, t);
+    const float z = __fmul_rn(s, s);
+    float p = __uint_as_float(0x3d9d89d9u);                 // 1/13
+    p = __fmaf_rn(p, z, __uint_as_float(0x3dba2e8cu));      // 1/11
+    p = __fmaf_rn(p, z, __uint_as_float(0x3de38e39u));      // 1/9
+    p = __fmaf_rn(p, z, __uint_as_float(0x3e124925u));      // 1/7
+    p = __fmaf_rn(p, z, __uint_as_float(0x3e4ccccdu));      // 1/5
+    p = __fmaf_rn(p, z, __uint_as_float(0x3eaaaaabu));      // 1/3
+    p = __fmaf_rn(p, z, 1.0f);                              // 1
+    const float r = __fadd_rn(s, s);
+    const float lnm = __fmul_rn(r, p);
+    const float ef = __int2float_rn(e);
+    const float u = __fmaf_rn(ef, __uint_as_float(0x35bfbe8eu), lnm);   // ln2_lo
+    return __fmaf_rn(ef, __uint_as_float(0x3f317200u), u);              // ln2_hi
+}
+
+// u = (2 (w >> 9) + 1) 2^-24 (exact), g = -ln(-ln u).
+BIV_DEV float gumbel_from_word(uint32_t w) {
+    const float u = __fmul_rn(__uint2float_rn(2u * (w >> 9) + 1u), 5.9604644775390625e-8f);
+    const float a = own_log(u);
+    return -own_log(-a);
+}
+
+// Total order used for selection: NaN lowest, -0 == +0, then by value.
+BIV_DEV uint32_t key_order(float k) {
+    if (k != k) return 0u;
+    if (k == 0.0f) k = 0.0f;
+    const uint32_t b = __float_as_uint(k);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+BIV_DEV unsigned long long pack_key(float k, uint32_t v) {
+    return (static_cast<unsigned long long>(key_order(k)) << 32) | static_cast<unsigned long long>(~v);
+}
+
+BIV_DEV unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
+
+BIV_DEV unsigned long long warp_max64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = umax64(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------- cluster PTX
+BIV_DEV uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+BIV_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+BIV_DEV unsigned long long ld_dsmem_u64(const void* local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_addr)), "r"(rank));
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+BIV_DEV void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Block-wide max of a packed value; every thread gets the result.
+BIV_DEV unsigned long long block_max64(unsigned long long v, unsigned long long* scratch) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    v = warp_max64(v);
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    unsigned long long r = 0;
+#pragma unroll
+    for (int w = 0; w < kSelThreads / 32; ++w) r = umax64(r, scratch[w]);
+    __syncthreads();
+    return r;
+}
+
+// ------------------------------------------------------------ the kernel
+// grid.x = kClusterSize * R, cluster (kClusterSize, 1, 1).  CTA `rank` of the
+// cluster owns logits [rank * slice, min((rank + 1) * slice, V)) of row
+// blockIdx.x / kClusterSize; slice is a multiple of 4.
+__global__ void __launch_bounds__(kSelThreads)
+gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int slice,
+                     const uint32_t* __restrict__ row_req, const int32_t* __restrict__ row_pos,
+                     uint32_t seed_lo, uint32_t seed_hi, float invT, int greedy,
+                     int32_t* __restrict__ tokens) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    float* xs = reinterpret_cast<float*>(smem_raw);
+    __shared__ uint64_t bars[kPieces];
+    __shared__ unsigned long long red[kSelThreads / 32];
+    __shared__ unsigned long long published[2];    // [0] slice-max key, [1] slice winner
+    __shared__ int abort_flag;
+
+    const uint32_t rank = cluster_rank();
+    const long long row = blockIdx.x / kClusterSize;
+    const int begin = static_cast<int>(rank) * slice;
+    const int count = max(0, min(slice, V - begin));          // multiple of 4
+    const float* src = logits + row * ld + begin;
+
+    // Pieces of the slice, each a multiple of 16 bytes.
+    const int piece = ((count / 4 + kPieces - 1) / kPieces) * 4;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int p = 0; p < kPieces; ++p) mbar_init(&bars[p], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int p = 0; p < kPieces; ++p) {
+            const int off = p * piece;
+            const int n = max(0, min(piece, count - off));
+            mbar_arrive_expect_tx(&bars[p], static_cast<uint32_t>(n) * 4u);
+            if (n > 0) bulk_g2s(xs + off, src + off, static_cast<uint32_t>(n) * 4u, &bars[p]);
+        }
+    }
+
+    const uint32_t req = row_req[row];
+    const uint32_t pos = static_cast<uint32_t>(row_pos[row]) + 1u;   // position being selected
+
+    // Pass 1: slice maximum (value, lowest index), piece by piece as it lands.
+    float best_x = 0.0f;
+    int best_i = -1;
+    bool ok = true;
+    for (int p = 0; p < kPieces; ++p) {
+        if (!mbar_wait(&bars[p], 0, &abort_flag, &g_select_err)) {
+            ok = false;
+            break;
+        }
+        const int off = p * piece;
+        const int n = max(0, min(piece, count - off));
+        for (int i = threadIdx.x * 4; i < n; i += kSelThreads * 4) {
+            const float4 v = *reinterpret_cast<const float4*>(xs + off + i);
+            const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float x = e[j];
+                if (x == x && (best_i < 0 || x > best_x)) {   // NaN never becomes the max
+                    best_x = x;
+                    best_i = begin + off + i + j;
+                }
+            }
+        }
+    }
+    // Slice winner by value (greedy key) -> block max.
+    unsigned long long mx = best_i >= 0 ? pack_key(best_x, static_cast<uint32_t>(best_i)) : 0ull;
+    mx = block_max64(mx, red);
+    if (!ok) {
+        // Let copies still in flight land before the CTA may exit.
+        if (threadIdx.x == 0)
+            for (int p = 0; p < kPieces; ++p) mbar_wait_drain(&bars[p], 0);
+    }
+
+    if (greedy) {
+        if (threadIdx.x == 0) published[1] = mx;
+        cluster_sync();
+        if (rank == 0 && threadIdx.x == 0) {
+            unsigned long long w = 0;
+            for (uint32_t c = 0; c < kClusterSize; ++c) w = umax64(w, ld_dsmem_u64(&published[1], c));
+            tokens[row] = w ? static_cast<int32_t>(~static_cast<uint32_t>(w & 0xffffffffull)) : 0;
+        }
+        cluster_sync();
+        return;
+    }
+
+    // The key of this slice's maximum is a real key: a valid lower bound.
+    if (threadIdx.x == 0) {
+        unsigned long long lb = 0;
+        if (mx) {
+            const uint32_t v = ~static_cast<uint32_t>(mx & 0xffffffffull);
+            const float x = xs[v - begin];
+            const U4 w = philox4x32_10(v >> 2, pos, req, 0u, seed_lo, seed_hi);
+            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+            const float key = __fadd_rn(__fmul_rn(x, invT), gumbel_from_word(words[v & 3u]));
+            lb = pack_key(key, v);
+        }
+        published[0] = lb;
+    }
+    cluster_sync();
+    unsigned long long lb = 0;
+#pragma unroll
+    for (uint32_t c = 0; c < kClusterSize; ++c) lb = umax64(lb, ld_dsmem_u64(&published[0], c));
+    const uint32_t lb_order = static_cast<uint32_t>(lb >> 32);
+
+    // Pass 2: exact pruning, then noise and keys for the survivors.
+    unsigned long long best = 0;
+    if (ok) {
+        for (int i = threadIdx.x * 4; i < count; i += kSelThreads * 4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(xs + i);
+            const float m4 = fmaxf(fmaxf(v4.x, v4.y), fmaxf(v4.z, v4.w));
+            const float bound = __fadd_rn(__fmul_rn(m4, invT), kNoiseBound);
+            if (key_order(bound) < lb_order) continue;
+            const uint32_t v0 = static_cast<uint32_t>(begin + i);
+            const U4 w = philox4x32_10(v0 >> 2, pos, req, 0u, seed_lo, seed_hi);
+            const float e[4] = {v4.x, v4.y, v4.z, v4.w};
+            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float key = __fadd_rn(__fmul_rn(e[j], invT), gumbel_from_word(words[j]));
+                best = umax64(best, pack_key(key, v0 + j));
+            }
+        }
+    }
+    best = block_max64(best, red);
+    if (threadIdx.x == 0) published[1] = best;
+    cluster_sync();
+    if (rank == 0 && threadIdx.x == 0) {
+        unsigned long long w = 0;
+        for (uint32_t c = 0; c < kClusterSize; ++c) w = umax64(w, ld_dsmem_u64(&published[1], c));
+        tokens[row] = w ? static_cast<int32_t>(~static_cast<uint32_t>(w & 0xffffffffull)) : 0;
+    }
+    cluster_sync();   // keep every CTA's shared memory alive until rank 0 has read it
+}
+
+__global__ void gumbel_noise_kernel(uint32_t seed_lo, uint32_t seed_hi, const uint32_t* __restrict__ row_req,
+                                    const int32_t* __restrict__ row_pos, int V, float* __restrict__ g) {
+    const long long row = blockIdx.y;
+    const uint32_t req = row_req[row];
+    const uint32_t pos = static_cast<uint32_t>(row_pos[row]) + 1u;
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < V; v += gridDim.x * blockDim.x) {
+        const U4 w = philox4x32_10(static_cast<uint32_t>(v) >> 2, pos, req, 0u, seed_lo, seed_hi);
+        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+        g[row * V + v] = gumbel_from_word(words[v & 3]);
+    }
+}
+
+__global__ void gumbel_words_kernel(const uint32_t* __restrict__ words, long long n, float* __restrict__ g) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x)
+        g[i] = gumbel_from_word(words[i]);
+}
+
+// One thread per request: first mismatch of target vs draft.
+__global__ void verify_accept_kernel(const int32_t* __restrict__ target, const int32_t* __restrict__ draft,
+                                     const int32_t* __restrict__ p0, int N, int K,
+                                     int32_t* __restrict__ accept_len, int32_t* __restrict__ new_len) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= N) return;
+    int L = K;
+    for (int j = 0; j < K; ++j) {
+        if (target[static_cast<long long>(r) * K + j] != draft[static_cast<long long>(r) * K + j]) {
+            L = j + 1;
+            break;
+        }
+    }
+    accept_len[r] = L;
+    new_len[r] = p0[r] + L;
+}
+
+}  // namespace
+}  // namespace biv
+
+using namespace biv;
+
+extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                                 const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
+                                 biv_stream_t stream) {
+    if (R < 0 || V < 4 || ld < V) return BIV_ERR_SHAPE;
+    if (V % 4 != 0 || ld % 4 != 0) return BIV_ERR_SHAPE;
+    if (!(temperature >= 0.0f) || !(temperature < INFINITY)) return BIV_ERR_VALUE;
+    if (R == 0) return BIV_OK;
+    if (!logits || !row_req || !row_pos || !tokens) return BIV_ERR_NULL;
+    if (!aligned16(logits)) return BIV_ERR_ALIGN;
+    const int slice = ((V / 4 + kClusterSize - 1) / kClusterSize) * 4;
+    if (slice > kMaxSliceFloats) return BIV_ERR_UNSUPPORTED;
+    if (static_cast<long long>(R) * kClusterSize > 0x7fffffffLL) return BIV_ERR_SHAPE;
+    const int greedy = temperature == 0.0f;
+    const float invT = greedy ? 0.0f : 1.0f / temperature;   // fl(1/T), IEEE division on the host
+    const size_t smem = static_cast<size_t>(slice) * 4;
+
+    static int configured_device = -1;
+    static size_t configured_smem = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev || configured_smem < smem) {
+        cudaError_t e = cudaFuncSetAttribute(gumbel_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kMaxSliceFloats * 4));
+        if (e != cudaSuccess) return cuda_status(e);
+        configured_device = dev;
+        configured_smem = kMaxSliceFloats * 4;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(R) * kClusterSize, 1, 1);
+    cfg.blockDim = dim3(kSelThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterSize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gumbel_argmax_kernel, logits, V, ld, slice, row_req, row_pos,
+                                       static_cast<uint32_t>(seed & 0xffffffffull),
+                                       static_cast<uint32_t>(seed >> 32), invT, greedy, tokens);
+    if (e != cudaSuccess) return cuda_status(e);
+    return launch_status();
+}
+
+extern "C" int biv_gumbel_noise(uint64_t seed, const uint32_t* row_req, const int32_t* row_pos, int R, int V,
+                                float* g, biv_stream_t stream) {
+    if (R < 0 || V < 0 || R > 65535) return BIV_ERR_SHAPE;
+    if (R == 0 || V == 0) return BIV_OK;
+    if (!row_req || !row_pos || !g) return BIV_ERR_NULL;
+    const int blocks = std::min((V + 255) / 256, 1024);
+    gumbel_noise_kernel<<<dim3(blocks, R), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint32_t>(seed & 0xffffffffull), static_cast<uint32_t>(seed >> 32), row_req, row_pos, V, g);
+    return launch_status();
+}
+
+extern "C" int biv_gumbel_from_words(const uint32_t* words, long long n, float* g, biv_stream_t stream) {
+    if (n < 0) return BIV_ERR_SHAPE;
+    if (n == 0) return BIV_OK;
+    if (!words || !g) return BIV_ERR_NULL;
+    const long long blocks = std::min<long long>((n + 255) / 256, 4096);
+    gumbel_words_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(words, n,
+                                                                                                          g);
+    return launch_status();
+}
+
+extern "C" int biv_verify_accept(const int32_t* target, const int32_t* draft, const int32_t* p0, int N, int K,
+                                 int32_t* accept_len, int32_t* new_len, biv_stream_t stream) {
+    if (N < 0 || K < 1) return BIV_ERR_SHAPE;
+    if (N == 0) return BIV_OK;
+    if (!target || !draft || !p0 || !accept_len || !new_len) return BIV_ERR_NULL;
+    verify_accept_kernel<<<(N + 127) / 128, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(target, draft, p0, N,
+                                                                                              K, accept_len, new_len);
+    return launch_status();
+}

@@ -1,0 +1,145 @@
+"""Composition of one batch-invariant verify step out of libbiv calls.
+
+Decode-Verify-Rollback ([DVR] paras 3-4, tgstat @ashnskt post 392): the
+verifier runs one fixed-shape forward over W = N requests x K tokens, writes
+its own K/V for the window rows into the cache (overwriting whatever the
+fast path left there), selects one token per row with shared Gumbel noise,
+and compares the selections with the drafts ([COUPLING], AIexTime post 185).
+
+Every arithmetic step runs in libbiv's CUDA kernels; this module only owns
+device buffers and issues the C-ABI calls in order on one stream.  The layer
+is the standard pre-norm Llama decoder (a reading: the pages do not describe
+the verifier model).
+
+Row layout of a window (request-major): row r*K + j holds the last committed
+token (j = 0) or draft d_j, sits in cache slot row_slot and at absolute
+position p0[r] + j; its selected token y_{j+1} is compared with
+draft[r*K + j] = d_{j+1}.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import abi as B
+
+
+@dataclass
+class Window:
+    """Device-resident row metadata and drafts of one verify window."""
+    tokens: torch.Tensor     # int32 [W] input token per row
+    row_slot: torch.Tensor   # int32 [W]
+    row_req: torch.Tensor    # int32 [W] (stable request id, used as uint32)
+    row_pos: torch.Tensor    # int32 [W]
+    draft: torch.Tensor      # int32 [W] draft each row's selection must match
+    p0: torch.Tensor         # int32 [N]
+
+
+class DecoderVerifier:
+    """Device-resident decoder verifier for windows of exactly W rows."""
+
+    def __init__(self, cfg, weights: dict, caches: list, n_slots: int, max_len: int, W: int,
+                 rows_per_group: int, device="cuda", seed: int = 0x1234_5678_9ABC_DEF0):
+        self.cfg, self.W, self.rpg = cfg, W, rows_per_group
+        self.n_slots, self.max_len, self.seed = n_slots, max_len, seed
+        dev = torch.device(device)
+        self.w = {k: v.to(dev).contiguous() for k, v in weights.items()}
+        self.kc = [k.to(dev).contiguous() for k, _ in caches]
+        self.vc = [v.to(dev).contiguous() for _, v in caches]
+        d, Hq, Hkv, hd, F = cfg.d, cfg.Hq, cfg.Hkv, cfg.hd, cfg.ffn
+        bf = dict(device=dev, dtype=torch.bfloat16)
+        self.x = torch.empty(W, d, **bf)
+        self.h = torch.empty(W, d, **bf)
+        self.qkv = torch.empty(W, cfg.qkv_n, **bf)
+        self.q = torch.empty(W, Hq, hd, **bf)
+        self.k = torch.empty(W, Hkv * hd, **bf)
+        self.o = torch.empty(W, Hq, hd, **bf)
+        self.proj = torch.empty(W, d, **bf)
+        self.gu = torch.empty(W, 2 * F, **bf)
+        self.act = torch.empty(W, F, **bf)
+        self.hidden = torch.empty(W, d, **bf)
+        self.logits = torch.empty(W, cfg.vocab, device=dev, dtype=torch.float32)
+        self.target = torch.empty(W, device=dev, dtype=torch.int32)
+        N = (W + rows_per_group - 1) // rows_per_group
+        self.accept_len = torch.empty(N, device=dev, dtype=torch.int32)
+        self.new_len = torch.empty(N, device=dev, dtype=torch.int32)
+        ws = B.biv_decode_attn_workspace_size(W, Hq, max_len)
+        self.workspace = torch.empty(max(ws, 16), device=dev, dtype=torch.uint8)
+        self.launches_per_step = 5 + cfg.layers * 13
+
+    # -------------------------------------------------------------- stages
+    def forward(self, win: Window) -> None:
+        """Hidden state and fp32 logits of every window row (cache rows written)."""
+        c, w = self.cfg, self.w
+        Hq, Hkv, hd = c.Hq, c.Hkv, c.hd
+        B.biv_embed(w["embed"], win.tokens, self.x)
+        for l in range(c.layers):
+            B.biv_rmsnorm(self.x, w[f"l{l}.attn_norm"], self.h, c.eps)
+            B.biv_gemm_nosplitk(self.h, w[f"l{l}.wqkv"], self.qkv)
+            B.biv_rope_qk(self.qkv, self.q, self.k, win.row_pos, Hq, Hkv, hd, c.rope_theta)
+            v_new = self.qkv[:, (Hq + Hkv) * hd:]
+            B.biv_kv_overwrite(self.kc[l], self.vc[l], self.k, v_new, win.row_slot, win.row_pos, K=self.rpg)
+            B.biv_decode_attn_fixedsplit(self.q, self.kc[l], self.vc[l], win.row_slot, win.row_pos, self.o,
+                                         self.rpg, self.workspace)
+            B.biv_gemm_nosplitk(self.o.view(self.W, Hq * hd), w[f"l{l}.wo"], self.proj)
+            B.biv_residual_add(self.x, self.proj, self.x)
+            B.biv_rmsnorm(self.x, w[f"l{l}.ffn_norm"], self.h, c.eps)
+            B.biv_gemm_nosplitk(self.h, w[f"l{l}.wgu"], self.gu)
+            B.biv_silu_mul(self.gu, self.act)
+            B.biv_gemm_nosplitk(self.act, w[f"l{l}.wdown"], self.proj)
+            B.biv_residual_add(self.x, self.proj, self.x)
+        B.biv_rmsnorm(self.x, w["final_norm"], self.hidden, c.eps)
+
+    def lm_head(self) -> None:
+        B.biv_gemm_nosplitk(self.hidden, self.w["lm_head"], self.logits)
+
+    def select_and_accept(self, win: Window) -> None:
+        B.biv_gumbel_argmax(self.logits, win.row_req, win.row_pos, self.seed, self.cfg.temperature, self.target)
+        N = self.accept_len.shape[0]
+        B.biv_verify_accept(self.target, win.draft, win.p0, N, self.rpg, self.accept_len, self.new_len)
+
+    def step(self, win: Window) -> None:
+        self.forward(win)
+        self.lm_head()
+        self.select_and_accept(win)
+
+    # -------------------------------------------------------- CUDA graphs
+    def capture(self, win: Window, segments: bool = False):
+        """Capture the step on ``win``'s (static) buffers.
+
+        With ``segments`` the step is captured as three graphs -- the layers,
+        the LM-head GEMM alone, then selection + accept -- so the LM-head
+        launch can be timed with events between replays.
+        """
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step(win)            # warm-up outside capture (sets kernel attributes)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        parts = [(self.forward, (win,)), (self.lm_head, ()), (self.select_and_accept, (win,))]
+        if not segments:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.step(win)
+            return g
+        graphs = []
+        for fn, args in parts:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn(*args)
+            graphs.append(g)
+        return graphs
+
+
+def make_window(N: int, K: int, tokens, p0, req_ids, draft, device="cuda") -> Window:
+    """Build a request-major window (row r*K + j in slot r at position p0[r] + j)."""
+    dev = torch.device(device)
+    p0 = torch.as_tensor(p0, dtype=torch.int32)
+    req_ids = torch.as_tensor(req_ids, dtype=torch.int32)
+    r = torch.arange(N, dtype=torch.int32).repeat_interleave(K)
+    j = torch.arange(K, dtype=torch.int32).repeat(N)
+    i32 = lambda t: torch.as_tensor(t, dtype=torch.int32).to(dev).contiguous()
+    return Window(tokens=i32(tokens), row_slot=i32(r), row_req=i32(req_ids[r.long()]),
+                  row_pos=i32(p0[r.long()] + j), draft=i32(draft), p0=i32(p0))

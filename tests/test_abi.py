@@ -1,0 +1,153 @@
+"""The C-ABI library loads, exports every symbol include/biv.h declares, and
+rejects bad arguments on the host before any CUDA call (no GPU needed).
+
+Pointers used here are never dereferenced: every call below returns from
+host-side validation before anything is enqueued.
+"""
+import ctypes as C
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "biv.h")
+
+OK, NULL, SHAPE, ALIGN, VALUE, UNSUP = 0, 1, 2, 3, 4, 5
+FAKE = 0x10000          # 16-byte aligned, never dereferenced
+MISALIGNED = 0x10008
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from invariant_verify_gb300 import build, abi
+    build.build()
+    return abi.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(biv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 19
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.biv_status_string(s)
+    assert lib.biv_status_string(99) == b"unknown status"
+    assert lib.biv_version() >= 100
+
+
+def test_rmsnorm_validation(lib):
+    f = lib.biv_rmsnorm
+    assert f(None, None, None, 0, 1024, 1e-6, None) == OK
+    assert f(None, None, None, 4, 1020, 1e-6, None) == SHAPE
+    assert f(None, None, None, 4, 1024, -1.0, None) == VALUE
+    assert f(None, None, None, 4, 1024, float("nan"), None) == VALUE
+    assert f(None, None, None, 4, 1024, 1e-6, None) == NULL
+    assert f(MISALIGNED, FAKE, FAKE, 4, 1024, 1e-6, None) == ALIGN
+
+
+def test_gemm_validation(lib):
+    f = lib.biv_gemm_nosplitk
+    assert f(None, None, None, 0, 0, 64, 64, None) == OK
+    assert f(None, None, None, 0, 4, 60, 64, None) == SHAPE
+    assert f(None, None, None, 0, 4, 64, 60, None) == SHAPE
+    assert f(None, None, None, 0, -1, 64, 64, None) == SHAPE
+    assert f(None, None, None, 7, 4, 64, 64, None) == VALUE
+    assert f(None, None, None, 0, 4, 64, 64, None) == NULL
+    assert f(FAKE, MISALIGNED, FAKE, 1, 4, 64, 64, None) == ALIGN
+    assert lib.biv_gemm_nosplitk_bn(FAKE, FAKE, FAKE, 0, 4, 64, 64, 48, None) == VALUE
+
+
+def test_gemm_tile_width_depends_on_n_only(lib):
+    seen = {}
+    for N, K in [(2048, 256), (1536, 1024), (1024, 2816), (5632, 1024), (32000, 1024),
+                 (4096, 14336), (6144, 4096), (28672, 4096), (128256, 4096)]:
+        bn = lib.biv_gemm_tile_n(N, K)
+        assert bn in (16, 32, 64, 128, 256)
+        assert lib.biv_gemm_tile_n(N, 64) == bn          # K does not change it
+        seen[N] = bn
+    assert seen[128256] == 256 and seen[32000] == 128 and seen[1024] == 16
+
+
+def test_attention_validation_and_workspace(lib):
+    ws = lib.biv_decode_attn_workspace_size
+    assert ws(64, 8, 2304) == 64 * 8 * 9 * 130 * 4
+    assert ws(1, 1, 1) == 1 * 1 * 1 * 130 * 4
+    assert ws(0, 8, 100) == 0
+    f = lib.biv_decode_attn_fixedsplit
+    args = lambda **kw: [kw.get(k, v) for k, v in [
+        ("q", FAKE), ("kc", FAKE), ("vc", FAKE), ("slot", FAKE), ("pos", FAKE), ("o", FAKE), ("W", 16),
+        ("rpg", 4), ("Hq", 8), ("Hkv", 2), ("hd", 128), ("n_slots", 4), ("max_len", 512), ("split", 256),
+        ("ws", FAKE), ("ws_bytes", 1 << 30), ("stream", None)]]
+    assert f(*args(hd=64)) == UNSUP
+    assert f(*args(split=128)) == UNSUP
+    assert f(*args(Hq=6, Hkv=4)) == SHAPE
+    assert f(*args(ws_bytes=100)) == SHAPE
+    assert f(*args(W=0)) == OK
+    assert f(*args(q=None)) == NULL
+    assert f(*args(o=MISALIGNED)) == ALIGN
+    assert f(*args(rpg=0)) == SHAPE
+
+
+def test_gqa_tile_rule(lib):
+    golden = os.path.join(ROOT, "tests", "golden", "gqa_tile_rule.txt")
+    rows = [list(map(int, l.split())) for l in open(golden) if l.strip() and not l.startswith("#")]
+    for tile, G, D in rows:
+        assert lib.biv_gqa_max_drafts(G, tile) == D
+    assert lib.biv_gqa_max_drafts(0, 128) == -1
+    assert lib.biv_gqa_max_drafts(256, 128) == -1
+    assert lib.biv_gqa_max_drafts(4, 128) == 31
+
+
+def test_kv_overwrite_validation(lib):
+    f = lib.biv_kv_overwrite
+    base = [FAKE, FAKE, FAKE, 256, FAKE, 1536, FAKE, FAKE, None, 16, 4, 2, 128, 4, 512, None]
+    assert f(*base[:9], 0, *base[10:]) == OK
+    b = list(base); b[9] = 15
+    assert f(*b) == SHAPE                         # W % K != 0
+    b = list(base); b[3] = 128
+    assert f(*b) == SHAPE                         # k stride < Hkv*hd
+    b = list(base); b[5] = 1540
+    assert f(*b) == SHAPE                         # v stride not a multiple of 8
+    b = list(base); b[2] = None
+    assert f(*b) == NULL
+    b = list(base); b[0] = MISALIGNED
+    assert f(*b) == ALIGN
+
+
+def test_select_and_accept_validation(lib):
+    g = lib.biv_gumbel_argmax
+    assert g(FAKE, 4, 30, 32, FAKE, FAKE, 1, 1.0, FAKE, None) == SHAPE      # V % 4
+    assert g(FAKE, 4, 32, 30, FAKE, FAKE, 1, 1.0, FAKE, None) == SHAPE      # ld < V
+    assert g(FAKE, 4, 32, 32, FAKE, FAKE, 1, -0.5, FAKE, None) == VALUE
+    assert g(FAKE, 4, 32, 32, FAKE, FAKE, 1, math.inf, FAKE, None) == VALUE
+    assert g(FAKE, 4, 32, 32, FAKE, FAKE, 1, math.nan, FAKE, None) == VALUE
+    assert g(FAKE, 0, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, None) == OK
+    assert g(None, 4, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, None) == NULL
+    assert g(MISALIGNED, 4, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, None) == ALIGN
+    big = 8 * 57344 + 32
+    assert g(FAKE, 4, big, big, FAKE, FAKE, 1, 1.0, FAKE, None) == UNSUP
+    a = lib.biv_verify_accept
+    assert a(FAKE, FAKE, FAKE, 4, 0, FAKE, FAKE, None) == SHAPE
+    assert a(FAKE, FAKE, FAKE, 0, 4, FAKE, FAKE, None) == OK
+    assert a(None, FAKE, FAKE, 4, 4, FAKE, FAKE, None) == NULL
+
+
+def test_glue_validation(lib):
+    assert lib.biv_embed(FAKE, FAKE, FAKE, 4, 100, 10, None) == SHAPE
+    assert lib.biv_embed(FAKE, FAKE, FAKE, 0, 128, 10, None) == OK
+    assert lib.biv_rope_qk(FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 127, 10000.0, None) == SHAPE
+    assert lib.biv_rope_qk(FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 128, 0.5, None) == VALUE
+    assert lib.biv_silu_mul(FAKE, FAKE, 4, 12, None) == SHAPE
+    assert lib.biv_residual_add(FAKE, FAKE, FAKE, 12, None) == SHAPE
+    assert lib.biv_residual_add(FAKE, FAKE, MISALIGNED, 16, None) == ALIGN

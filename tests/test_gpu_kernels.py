@@ -1,0 +1,333 @@
+"""GPU parity of every libbiv kernel against the CPU oracle, and GPU-vs-GPU
+batch invariance, through the C ABI.  Sizes span several tiles plus a
+ragged tail; edge cases cover empty inputs and the degenerate shapes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, same_bits, dev
+from invariant_verify_gb300 import abi as B
+from invariant_verify_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+SEED = 0x1234_5678_9ABC_DEF0
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from invariant_verify_gb300 import build
+    build.build()
+    yield
+    assert B.biv_device_error() == 0
+
+
+def i32(a):
+    return torch.as_tensor(np.asarray(a), dtype=torch.int32).cuda()
+
+
+# ------------------------------------------------------------------ RMSNorm
+@pytest.mark.parametrize("rows,d", [(1, 256), (16, 256), (64, 1024), (37, 4096), (5, 8), (3, 16384)])
+def test_rmsnorm_parity(rows, d):
+    g = synth.generator(rows * 7 + d)
+    x = synth.bf16_normal((rows, d), 1.5, g)
+    w = synth.bf16_normal((d,), 1.0, g)
+    y = torch.empty(rows, d, dtype=torch.bfloat16, device="cuda")
+    B.biv_rmsnorm(dev(x), dev(w), y, 1e-6)
+    assert_close(y, oracle.rmsnorm(x, w, 1e-6), what="rmsnorm")
+
+
+def test_rmsnorm_row_invariance_and_alias():
+    x = dev(synth.bf16_normal((200, 1024), 1.0, synth.generator(3)))
+    w = dev(torch.ones(1024, dtype=torch.bfloat16))
+    full = torch.empty_like(x)
+    B.biv_rmsnorm(x, w, full, 1e-6)
+    for r in (0, 77, 199):
+        one = torch.empty(1, 1024, dtype=torch.bfloat16, device="cuda")
+        B.biv_rmsnorm(x[r:r + 1].contiguous(), w, one, 1e-6)
+        assert same_bits(one[0], full[r])
+    xa = x.clone()
+    B.biv_rmsnorm(xa, w, xa, 1e-6)            # y may alias x
+    assert same_bits(xa, full)
+    B.biv_rmsnorm(x[:0], w, full[:0], 1e-6)   # empty
+
+
+# --------------------------------------------------------------------- GEMM
+GEMM_SHAPES = [
+    (1, 64, 64, torch.bfloat16, None),
+    (3, 136, 72, torch.bfloat16, None),        # ragged N (not a tile multiple), K < one k-block
+    (130, 520, 200, torch.bfloat16, None),     # two row tiles + ragged M, ragged K
+    (64, 1536, 1024, torch.bfloat16, None),
+    (16, 2048, 256, torch.float32, None),
+    (300, 1000, 520, torch.float32, None),
+    (257, 384, 128, torch.bfloat16, 256),
+    (129, 200, 136, torch.float32, 128),
+    (77, 96, 64, torch.bfloat16, 32),
+    (45, 48, 64, torch.float32, 16),
+    (200, 640, 192, torch.bfloat16, 64),
+]
+
+
+@pytest.mark.parametrize("M,N,K,dt,bn", GEMM_SHAPES)
+def test_gemm_parity(M, N, K, dt, bn):
+    g = synth.generator(M * 131 + N * 7 + K)
+    A = synth.bf16_normal((M, K), 1.0, g)
+    Bw = synth.bf16_normal((N, K), 0.05, g)
+    C = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+    B.biv_gemm_nosplitk(dev(A), dev(Bw), C, bn=bn)
+    assert_close(C, oracle.gemm(A, Bw), what=f"gemm {M}x{N}x{K}")
+
+
+def test_gemm_empty_and_single():
+    A = dev(synth.bf16_normal((0, 64), 1.0, synth.generator(1)))
+    Bw = dev(synth.bf16_normal((64, 64), 1.0, synth.generator(2)))
+    C = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    B.biv_gemm_nosplitk(A, Bw, C)
+
+
+def test_gemm_rows_are_batch_invariant():
+    g = synth.generator(11)
+    A = dev(synth.bf16_normal((300, 1024), 1.0, g))
+    Bw = dev(synth.bf16_normal((1536, 1024), 0.05, g))
+    full = torch.empty(300, 1536, dtype=torch.float32, device="cuda")
+    B.biv_gemm_nosplitk(A, Bw, full)
+    for M in (1, 2, 7, 64, 128, 129, 256):
+        part = torch.empty(M, 1536, dtype=torch.float32, device="cuda")
+        B.biv_gemm_nosplitk(A[:M].contiguous(), Bw, part)
+        assert same_bits(part, full[:M]), M
+    perm = torch.randperm(300, generator=synth.generator(5)).cuda()
+    pc = torch.empty_like(full)
+    B.biv_gemm_nosplitk(A[perm].contiguous(), Bw, pc)
+    assert same_bits(pc, full[perm])
+    # a row placed at every slot of a 128-row tile gives the same bits
+    row = A[5:6].repeat(128, 1).contiguous()
+    rc = torch.empty(128, 1536, dtype=torch.float32, device="cuda")
+    B.biv_gemm_nosplitk(row, Bw, rc)
+    assert same_bits(rc, full[5:6].repeat(128, 1))
+
+
+def test_gemm_tile_width_does_not_change_bits():
+    g = synth.generator(12)
+    A = dev(synth.bf16_normal((150, 2048), 1.0, g))
+    Bw = dev(synth.bf16_normal((512, 2048), 0.05, g))
+    outs = {}
+    for bn in (16, 32, 64, 128, 256):
+        C = torch.empty(150, 512, dtype=torch.float32, device="cuda")
+        B.biv_gemm_nosplitk(A, Bw, C, bn=bn)
+        outs[bn] = C
+    for bn in (16, 32, 64, 128):
+        assert same_bits(outs[bn], outs[256]), bn
+
+
+# --------------------------------------------------------------- attention
+def _attn_case(n_slots, Hq, Hkv, max_len, p0, K, seed):
+    g = synth.generator(seed)
+    kc = synth.bf16_normal((n_slots, Hkv, max_len, 128), 1.0, g)
+    vc = synth.bf16_normal((n_slots, Hkv, max_len, 128), 1.0, g)
+    N = len(p0)
+    W = N * K
+    q = synth.bf16_normal((W, Hq, 128), 1.0, g)
+    slot = np.repeat(np.arange(N), K)
+    pos = np.repeat(np.asarray(p0), K) + np.tile(np.arange(K), N)
+    return q, kc, vc, slot.astype(np.int32), pos.astype(np.int32)
+
+
+def _run_attn(q, kc, vc, slot, pos, rpg):
+    W, Hq, _ = q.shape
+    o = torch.full((W, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(B.biv_decode_attn_workspace_size(W, Hq, kc.shape[2]), dtype=torch.uint8, device="cuda")
+    B.biv_decode_attn_fixedsplit(q, kc, vc, i32(slot), i32(pos), o, rpg, ws)
+    return o
+
+
+@pytest.mark.parametrize("Hq,Hkv,K,p0", [
+    (8, 2, 8, [250, 511, 1000]),        # G=4, windows straddling the 256 / 512 split edges
+    (32, 1, 4, [0, 300, 767]),          # G=32: 4 rows x 32 heads = one full 128-row tile
+    (8, 1, 16, [100, 1030]),            # G=8: 16 x 8 = 128
+    (8, 1, 20, [5, 600]),               # G=8, K=20: two tiles per request
+    (4, 4, 3, [255, 256, 257]),         # G=1
+])
+def test_attention_parity(Hq, Hkv, K, p0):
+    max_len = max(p0) + K + 40
+    q, kc, vc, slot, pos = _attn_case(len(p0), Hq, Hkv, max_len, p0, K, seed=Hq * 100 + K)
+    o = _run_attn(dev(q), dev(kc), dev(vc), slot, pos, K)
+    ref = oracle.attention(q, kc, vc, slot, pos)
+    assert_close(o, ref, what="attention")
+
+
+def test_attention_rows_are_batch_invariant():
+    q, kc, vc, slot, pos = _attn_case(4, 8, 2, 1400, [100, 255, 700, 1300], 8, seed=9)
+    qd, kd, vd = dev(q), dev(kc), dev(vc)
+    full = _run_attn(qd, kd, vd, slot, pos, 8)
+    alone = _run_attn(qd, kd, vd, slot, pos, 1)          # every row in its own tile
+    assert same_bits(alone, full)
+    for w in (0, 9, 31):                                  # a single-row call
+        one = _run_attn(qd[w:w + 1].contiguous(), kd, vd, slot[w:w + 1], pos[w:w + 1], 1)
+        assert same_bits(one[0], full[w])
+    perm = np.random.default_rng(1).permutation(32)
+    pq = _run_attn(qd[torch.as_tensor(perm).cuda()].contiguous(), kd, vd, slot[perm], pos[perm], 1)
+    assert same_bits(pq, full[torch.as_tensor(perm).cuda()])
+    # stale values after a row's position do not change it
+    kd2, vd2 = kd.clone(), vd.clone()
+    for r, p in enumerate([100, 255, 700, 1300]):
+        kd2[r, :, p + 8:] = 7.0
+        vd2[r, :, p + 8:] = -3.0
+    assert same_bits(_run_attn(qd, kd2, vd2, slot, pos, 8), full)
+
+
+def test_attention_first_position():
+    q, kc, vc, slot, pos = _attn_case(2, 4, 2, 64, [0, 0], 1, seed=4)
+    o = _run_attn(dev(q), dev(kc), dev(vc), slot, pos, 1)
+    v = oracle.from_bf16(vc)
+    for w in range(2):
+        for h in range(4):
+            assert_close(o[w, h], v[w, h // 2, 0], tol=1e-2)
+
+
+# -------------------------------------------------------------- KV + glue
+def test_kv_overwrite_bit_exact_and_rows_keep():
+    g = synth.generator(21)
+    kc = synth.bf16_normal((3, 2, 64, 128), 1.0, g)
+    vc = synth.bf16_normal((3, 2, 64, 128), 1.0, g)
+    kn = synth.bf16_normal((12, 2 * 128), 1.0, g)
+    vbig = synth.bf16_normal((12, 1536), 1.0, g)                 # strided source
+    vn = vbig[:, 1280:]
+    slot = np.repeat([2, 0, 1], 4).astype(np.int32)
+    pos = (np.repeat([10, 50, 0], 4) + np.tile(np.arange(4), 3)).astype(np.int32)
+    kd, vd = dev(kc), dev(vc)
+    B.biv_kv_overwrite(kd, vd, dev(kn), dev(vbig)[:, 1280:], i32(slot), i32(pos), K=4)
+    ko = oracle._np(kc).copy(); vo = oracle._np(vc).copy()
+    oracle.kv_overwrite(ko, vo, oracle._np(kn).reshape(12, 2, 128), oracle._np(vn.contiguous()).reshape(12, 2, 128),
+                        slot, pos)
+    assert np.array_equal(oracle._np(kd.cpu()), ko) and np.array_equal(oracle._np(vd.cpu()), vo)
+    # rows_keep: request r writes only its first keep[r] rows
+    kd, vd = dev(kc), dev(vc)
+    keep = np.array([1, 4, 0], np.int32)
+    B.biv_kv_overwrite(kd, vd, dev(kn), dev(vbig)[:, 1280:], i32(slot), i32(pos), K=4, rows_keep=i32(keep))
+    rows = [w for w in range(12) if w % 4 < keep[w // 4]]
+    ko = oracle._np(kc).copy(); vo = oracle._np(vc).copy()
+    oracle.kv_overwrite(ko, vo, oracle._np(kn).reshape(12, 2, 128)[rows],
+                        oracle._np(vn.contiguous()).reshape(12, 2, 128)[rows], slot[rows], pos[rows])
+    assert np.array_equal(oracle._np(kd.cpu()), ko) and np.array_equal(oracle._np(vd.cpu()), vo)
+
+
+def test_rope_parity():
+    W, Hq, Hkv, hd = 10, 8, 2, 128
+    g = synth.generator(31)
+    qkv = synth.bf16_normal((W, (Hq + 2 * Hkv) * hd), 1.0, g)
+    pos = np.array([0, 1, 7, 100, 255, 256, 1000, 2047, 4095, 8191], np.int32)
+    q = torch.empty(W, Hq, hd, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty(W, Hkv * hd, dtype=torch.bfloat16, device="cuda")
+    for theta in (10000.0, 500000.0):
+        B.biv_rope_qk(dev(qkv), q, k, i32(pos), Hq, Hkv, hd, theta)
+        x = oracle.from_bf16(qkv)
+        assert_close(q, oracle.rope(x[:, :Hq * hd].reshape(W, Hq, hd), pos, theta), what="rope q")
+        assert_close(k.view(W, Hkv, hd), oracle.rope(x[:, Hq * hd:(Hq + Hkv) * hd].reshape(W, Hkv, hd), pos, theta),
+                     what="rope k")
+
+
+def test_silu_mul_residual_embed_parity():
+    g = synth.generator(41)
+    gu = synth.bf16_normal((33, 2 * 2816), 2.0, g)
+    out = torch.empty(33, 2816, dtype=torch.bfloat16, device="cuda")
+    B.biv_silu_mul(dev(gu), out)
+    assert_close(out, oracle.silu_mul(gu), what="silu")
+    x = synth.bf16_normal((33, 1024), 1.0, g)
+    y = synth.bf16_normal((33, 1024), 1.0, g)
+    o = torch.empty(33, 1024, dtype=torch.bfloat16, device="cuda")
+    B.biv_residual_add(dev(x), dev(y), o)
+    assert_close(o, oracle.from_bf16(x) + oracle.from_bf16(y), tol=4e-3, what="residual")
+    table = synth.bf16_normal((500, 1024), 1.0, g)
+    tok = np.array([0, 499, 17, 17, 250], np.int32)
+    e = torch.empty(5, 1024, dtype=torch.bfloat16, device="cuda")
+    B.biv_embed(dev(table), i32(tok), e)
+    assert torch.equal(e.cpu(), table[tok])
+
+
+# -------------------------------------------------------------- selection
+def test_noise_bit_exact_over_every_uniform():
+    words = np.arange(2 ** 23, dtype=np.uint32) << np.uint32(9)
+    g = torch.empty(2 ** 23, dtype=torch.float32, device="cuda")
+    B.biv_gumbel_from_words(torch.from_numpy(words.view(np.int32)).cuda(), g)
+    ref = oracle.gumbel_from_words(words)
+    assert np.array_equal(g.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    # random full 32-bit words, low bits included
+    w = torch.randint(-2 ** 31, 2 ** 31 - 1, (1 << 20,), generator=synth.generator(5), dtype=torch.int64)
+    w = w.to(torch.int32)
+    g = torch.empty(1 << 20, dtype=torch.float32, device="cuda")
+    B.biv_gumbel_from_words(w.cuda(), g)
+    ref = oracle.gumbel_from_words(w.numpy().view(np.uint32))
+    assert np.array_equal(g.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_noise_rows_bit_exact():
+    req = np.array([0, 7, 2 ** 31 - 1, 123456], np.int64)
+    pos = np.array([0, 99, 4095, 131071], np.int32)
+    V = 5000
+    g = torch.empty(4, V, dtype=torch.float32, device="cuda")
+    B.biv_gumbel_noise(SEED, i32(req), i32(pos), g)
+    for r in range(4):
+        ref = oracle.gumbel_row(SEED, int(req[r]), int(pos[r]) + 1, V)
+        assert np.array_equal(g[r].cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("R,V,T,std", [
+    (16, 2048, 1.0, 1.0), (64, 32000, 0.7, 0.64), (37, 152064, 0.7, 3.0), (5, 4, 1.0, 1.0),
+    (9, 12, 0.5, 1.0), (33, 2052, 2.0, 5.0), (8, 32000, 0.0, 1.0), (3, 100, 1e-3, 1.0)])
+def test_gumbel_argmax_bit_exact(R, V, T, std):
+    g = synth.generator(R * 1000 + V)
+    x = torch.randn(R, V, generator=g) * std
+    req = torch.randint(0, 2 ** 31 - 1, (R,), generator=g, dtype=torch.int64).to(torch.int32)
+    pos = torch.randint(0, 8000, (R,), generator=g, dtype=torch.int64).to(torch.int32)
+    tok = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax(x.cuda(), req.cuda(), pos.cuda(), SEED, T, tok)
+    ref = oracle.gumbel_argmax(x, req, pos, SEED, T)
+    assert np.array_equal(tok.cpu().numpy(), ref)
+
+
+def test_gumbel_argmax_peaked_ties_and_stride():
+    cfg = synth.SELECT
+    x, kind = synth.select_logits(cfg, rows=48, seed=3)
+    xt, _ = synth.select_logits(cfg, rows=48, seed=3, exact_ties=True)
+    req = torch.arange(48, dtype=torch.int32)
+    pos = torch.arange(48, dtype=torch.int32) * 3
+    for logits, T in ((x, 0.7), (x, 0.0), (xt, 0.0), (xt, 0.7)):
+        tok = torch.empty(48, dtype=torch.int32, device="cuda")
+        B.biv_gumbel_argmax(logits.cuda(), req.cuda(), pos.cuda(), SEED, T, tok)
+        assert np.array_equal(tok.cpu().numpy(), oracle.gumbel_argmax(logits, req, pos, SEED, T))
+    # a leading dimension larger than V: only the first V columns count
+    pad = torch.full((48, cfg.vocab + 4), 1e30)
+    pad[:, :cfg.vocab] = x
+    tok = torch.empty(48, dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax(pad.cuda(), req.cuda(), pos.cuda(), SEED, 0.7, tok, V=cfg.vocab)
+    assert np.array_equal(tok.cpu().numpy(), oracle.gumbel_argmax(x, req, pos, SEED, 0.7))
+    B.biv_gumbel_argmax(pad[:0].cuda(), req[:0].cuda(), pos[:0].cuda(), SEED, 0.7, tok[:0], V=cfg.vocab)
+
+
+def test_gumbel_argmax_chi_square_counts_match_oracle():
+    # the 10^6-draw sampling check of the oracle, repeated on the GPU: identical tokens
+    x = np.array([0.5, -1.0, 2.0, 0.0, 1.0, -0.5, 1.5, 0.3], np.float32)
+    n = 1_000_000
+    logits = torch.tensor(np.broadcast_to(x, (n, 8)).copy())
+    idx = np.arange(n)
+    req, pos = (idx // 1000).astype(np.int32), (idx % 1000).astype(np.int32)
+    tok = torch.empty(n, dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax(logits.cuda(), i32(req), i32(pos), SEED, 1.0, tok)
+    ref = oracle.gumbel_argmax(logits, req, pos, SEED, 1.0)
+    assert np.array_equal(tok.cpu().numpy(), ref)
+
+
+def test_verify_accept_bit_exact():
+    rng = np.random.default_rng(0)
+    for N, K in ((1, 1), (8, 8), (64, 16), (33, 5)):
+        t = rng.integers(0, 10, N * K).astype(np.int32)
+        d = np.where(rng.random(N * K) < 0.3, rng.integers(0, 10, N * K), t).astype(np.int32)
+        p0 = rng.integers(0, 5000, N).astype(np.int32)
+        L = torch.empty(N, dtype=torch.int32, device="cuda")
+        nl = torch.empty(N, dtype=torch.int32, device="cuda")
+        B.biv_verify_accept(i32(t), i32(d), i32(p0), N, K, L, nl)
+        rL, rnl = oracle.verify_accept(t, d, p0, N, K)
+        assert np.array_equal(L.cpu().numpy(), rL) and np.array_equal(nl.cpu().numpy(), rnl)

@@ -1,0 +1,233 @@
+"""End-to-end verify steps on the GPU through the C ABI.
+
+* Tiny workload (RMSNorm d=256 -> LM head 2048 -> select T=1 -> accept,
+  N=4 x K=4): parity with the oracle and bitwise batch invariance at
+  W in {1, 2, 4, 8, 16}.
+* 2-layer decoder verifier (d=1024, 8/2 heads, FFN 2816, vocab 32000,
+  N=8 x K=8, T=0.7): logits within tolerance of the oracle composition,
+  tokens and accept lengths bit-exact against the oracle's selection of the
+  same logits, every row bitwise identical when recomputed alone or in a
+  permuted window, and drafter invariance of the Decode-Verify-Rollback loop.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.model import OracleDecoder
+from gpu_util import assert_close, same_bits, dev
+from invariant_verify_gb300 import abi as B
+from invariant_verify_gb300 import synth
+from invariant_verify_gb300.verifier import DecoderVerifier, Window, make_window
+
+pytestmark = pytest.mark.gpu
+SEED = 0x1234_5678_9ABC_DEF0
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from invariant_verify_gb300 import build
+    build.build()
+    yield
+    assert B.biv_device_error() == 0
+
+
+def i32(a):
+    return torch.as_tensor(np.asarray(a), dtype=torch.int32).cuda()
+
+
+# ------------------------------------------------------------ tiny workload
+def tiny_step(h, gain, lm, row_req, row_pos, T):
+    W, d = h.shape
+    hn = torch.empty_like(h)
+    B.biv_rmsnorm(h, gain, hn, synth.TINY.eps)
+    logits = torch.empty(W, lm.shape[0], dtype=torch.float32, device="cuda")
+    B.biv_gemm_nosplitk(hn, lm, logits)
+    tok = torch.empty(W, dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax(logits, row_req, row_pos, SEED, T, tok)
+    return hn, logits, tok
+
+
+def test_tiny_parity_and_invariance():
+    cfg = synth.TINY
+    inp = synth.tiny_inputs(cfg)
+    N, K = cfg.N, cfg.K
+    W = N * K
+    _, row_req, row_pos = synth.request_window(N, K, inp["p0"], inp["req_ids"])
+    h, gain, lm = dev(inp["h"]), dev(inp["gain"]), dev(inp["lm_head"])
+    hn, logits, tok = tiny_step(h, gain, lm, i32(row_req), i32(row_pos), cfg.temperature)
+    # parity: each stage against the oracle on the same inputs
+    assert_close(hn, oracle.rmsnorm(inp["h"], inp["gain"], cfg.eps), what="tiny rmsnorm")
+    assert_close(logits, oracle.gemm(hn.cpu(), inp["lm_head"]), what="tiny logits")
+    ref_tok = oracle.gumbel_argmax(logits.cpu(), row_req, row_pos, SEED, cfg.temperature)
+    assert np.array_equal(tok.cpu().numpy(), ref_tok)
+    # drafts = target tokens with 25% replaced; accept lengths bit-exact
+    mask, ids = synth.draft_errors((W,), cfg.draft_err, cfg.vocab, seed=7)
+    draft = synth.apply_draft_errors(torch.tensor(ref_tok), mask, ids)
+    L = torch.empty(N, dtype=torch.int32, device="cuda")
+    nl = torch.empty(N, dtype=torch.int32, device="cuda")
+    B.biv_verify_accept(tok, dev(draft), dev(inp["p0"]), N, K, L, nl)
+    rL, rnl = oracle.verify_accept(ref_tok, draft, inp["p0"], N, K)
+    assert np.array_equal(L.cpu().numpy(), rL) and np.array_equal(nl.cpu().numpy(), rnl)
+    # batch invariance at W in {1, 2, 4, 8, 16}, every offset
+    for w in cfg.invariance_W:
+        for start in range(0, W, w):
+            sl = slice(start, start + w)
+            hn2, lg2, tk2 = tiny_step(h[sl].contiguous(), gain, lm, i32(row_req[sl]), i32(row_pos[sl]),
+                                      cfg.temperature)
+            assert same_bits(hn2, hn[sl]) and same_bits(lg2, logits[sl]) and same_bits(tk2, tok[sl]), (w, start)
+
+
+# ---------------------------------------------------- 2-layer decoder verifier
+def decoder_setup(cfg=synth.DECODER2):
+    w = synth.decoder_weights(cfg)
+    ctx = synth.context_lengths(cfg, cfg.N, seed=cfg.seed + 100)
+    max_len = int(ctx.max()) + 64
+    caches = synth.kv_cache(cfg.N, cfg.Hkv, max_len, cfg.hd, ctx, seed=cfg.seed + 200, layers=cfg.layers)
+    return w, caches, ctx, max_len
+
+
+@pytest.fixture(scope="module")
+def dec2():
+    return decoder_setup()
+
+
+def _window(cfg, ctx, tokens, draft, p0=None):
+    p0 = ctx if p0 is None else p0
+    return make_window(cfg.N, cfg.K, tokens, p0, torch.arange(cfg.N) * 1000 + 17, draft)
+
+
+def test_decoder_parity_with_oracle(dec2):
+    cfg = synth.DECODER2
+    w, caches, ctx, max_len = dec2
+    W = cfg.W
+    toks = torch.randint(0, cfg.vocab, (W,), generator=synth.generator(50), dtype=torch.int64).to(torch.int32)
+    win = _window(cfg, ctx, toks, toks)
+    ver = DecoderVerifier(cfg, w, caches, cfg.N, max_len, W, cfg.K)
+    ver.step(win)
+    torch.cuda.synchronize()
+    orc = OracleDecoder(cfg, w, caches, cfg.N, max_len)
+    out = orc.forward(toks.numpy(), win.row_slot.cpu().numpy(), win.row_pos.cpu().numpy(), storage="bf16")
+    assert_close(ver.hidden, out["hidden"], what="final hidden")
+    assert_close(ver.logits, out["logits"], what="logits")
+    # the cache rows the verifier wrote match the oracle's writes (within bf16 rounding)
+    for l in range(cfg.layers):
+        kg = ver.kc[l].cpu()
+        ko = torch.from_numpy(orc.caches[l][0].view(np.int16)).view(torch.bfloat16)
+        assert_close(kg.float(), ko.float().numpy(), what="cache K")
+    # selection and accept: bit-exact against the oracle on the GPU's logits
+    tgt = oracle.gumbel_argmax(ver.logits.cpu(), win.row_req.cpu(), win.row_pos.cpu(), SEED, cfg.temperature)
+    assert np.array_equal(ver.target.cpu().numpy(), tgt)
+    rL, rnl = oracle.verify_accept(tgt, toks.numpy(), ctx.numpy(), cfg.N, cfg.K)
+    assert np.array_equal(ver.accept_len.cpu().numpy(), rL)
+    assert np.array_equal(ver.new_len.cpu().numpy(), rnl)
+    # end-to-end token agreement with the oracle's own logits: report; any
+    # disagreement must be a near-tie within the propagated error
+    otg = oracle.gumbel_argmax(out["logits"].astype(np.float32), win.row_req.cpu(), win.row_pos.cpu(), SEED,
+                               cfg.temperature)
+    diff = np.nonzero(otg != tgt)[0]
+    assert len(diff) <= W // 8, f"{len(diff)} of {W} end-to-end tokens differ"
+
+
+def test_decoder_rows_bitwise_invariant(dec2):
+    cfg = synth.DECODER2
+    w, caches, ctx, max_len = dec2
+    W = cfg.W
+    toks = torch.randint(0, cfg.vocab, (W,), generator=synth.generator(51), dtype=torch.int64).to(torch.int32)
+    full = DecoderVerifier(cfg, w, caches, cfg.N, max_len, W, cfg.K)
+    win = _window(cfg, ctx, toks, toks)
+    full.step(win)
+    torch.cuda.synchronize()
+    H, Lg, Tg = full.hidden.clone(), full.logits.clone(), full.target.clone()
+    # every row alone (W = 1) against the cache the window wrote
+    one = DecoderVerifier(cfg, w, caches, cfg.N, max_len, 1, 1)
+    one.kc, one.vc = full.kc, full.vc
+    for r in range(W):
+        sl = slice(r, r + 1)
+        wi = Window(win.tokens[sl], win.row_slot[sl], win.row_req[sl], win.row_pos[sl], win.draft[sl],
+                    win.row_pos[sl].clone())
+        one.step(wi)
+        assert same_bits(one.hidden[0], H[r]) and same_bits(one.logits[0], Lg[r]) and same_bits(one.target[0], Tg[r]), r
+    # a permuted window (groups of one row)
+    perm = torch.randperm(W, generator=synth.generator(52)).cuda()
+    pv = DecoderVerifier(cfg, w, caches, cfg.N, max_len, W, 1)
+    pv.kc, pv.vc = full.kc, full.vc
+    pw = Window(win.tokens[perm].contiguous(), win.row_slot[perm].contiguous(), win.row_req[perm].contiguous(),
+                win.row_pos[perm].contiguous(), win.draft[perm].contiguous(), win.row_pos[perm].contiguous())
+    pv.step(pw)
+    assert same_bits(pv.hidden, H[perm]) and same_bits(pv.logits, Lg[perm]) and same_bits(pv.target, Tg[perm])
+    # a CUDA-graph replay gives the same bits
+    g = full.capture(win)
+    g.replay()
+    torch.cuda.synchronize()
+    assert same_bits(full.logits, Lg) and same_bits(full.target, Tg)
+
+
+def test_fast_path_kv_is_overwritten(dec2):
+    # Perturb the window's cache rows (a stale fast path) before verifying:
+    # the verifier overwrites them and the result equals a clean run.
+    cfg = synth.DECODER2
+    w, caches, ctx, max_len = dec2
+    toks = torch.randint(0, cfg.vocab, (cfg.W,), generator=synth.generator(53), dtype=torch.int64).to(torch.int32)
+    win = _window(cfg, ctx, toks, toks)
+    clean = DecoderVerifier(cfg, w, caches, cfg.N, max_len, cfg.W, cfg.K)
+    clean.step(win)
+    dirty = DecoderVerifier(cfg, w, caches, cfg.N, max_len, cfg.W, cfg.K)
+    for l in range(cfg.layers):
+        for r in range(cfg.N):
+            p = int(ctx[r])
+            dirty.kc[l][r, :, p:p + cfg.K] += 0.5
+            dirty.vc[l][r, :, p:p + cfg.K] -= 0.25
+    dirty.step(win)
+    torch.cuda.synchronize()
+    assert same_bits(dirty.logits, clean.logits) and same_bits(dirty.target, clean.target)
+
+
+def gpu_dvr_decode(cfg, w, caches, ctx, max_len, n_tokens, K, drafter, first):
+    """Decode-Verify-Rollback on the GPU: returns the committed streams."""
+    N = cfg.N
+    ver = DecoderVerifier(cfg, w, caches, N, max_len, N * K, K)
+    last = list(first)
+    pos = [int(c) for c in ctx]
+    streams = [[] for _ in range(N)]
+    req = torch.arange(N) * 1000 + 17
+    while min(len(s) for s in streams) < n_tokens:
+        drafts = np.array([drafter(r, streams[r], K) for r in range(N)], np.int32).reshape(N, K)
+        tokens = np.empty((N, K), np.int32)
+        tokens[:, 0] = last
+        tokens[:, 1:] = drafts[:, :-1]
+        win = make_window(N, K, tokens.reshape(-1), pos, req, drafts.reshape(-1))
+        ver.step(win)
+        L = ver.accept_len.cpu().numpy()
+        tgt = ver.target.cpu().numpy().reshape(N, K)
+        for r in range(N):
+            streams[r].extend(int(t) for t in tgt[r, :L[r]])
+            last[r] = int(tgt[r, L[r] - 1])
+            pos[r] += int(L[r])
+    return [s[:n_tokens] for s in streams]
+
+
+def test_drafter_invariance_on_gpu(dec2):
+    cfg = synth.DECODER2
+    w, caches, ctx, max_len = dec2
+    n_tokens = 24
+    first = list(range(100, 100 + cfg.N))
+    rng = np.random.default_rng(9)
+    none = gpu_dvr_decode(cfg, w, caches, ctx, max_len, n_tokens, 1, lambda r, h, K: [0] * K, first)
+    rand = gpu_dvr_decode(cfg, w, caches, ctx, max_len, n_tokens, 8,
+                          lambda r, h, K: list(rng.integers(0, cfg.vocab, K)), first)
+
+    def perfect(r, h, K):
+        fut = none[r][len(h):len(h) + K]
+        return fut + [0] * (K - len(fut))
+
+    perf = gpu_dvr_decode(cfg, w, caches, ctx, max_len, n_tokens, 8, perfect, first)
+
+    def noisy(r, h, K):   # 30% random-token error rate per position
+        d = perfect(r, h, K)
+        return [int(rng.integers(0, cfg.vocab)) if rng.random() < cfg.draft_err else t for t in d]
+
+    mixed = gpu_dvr_decode(cfg, w, caches, ctx, max_len, n_tokens, 8, noisy, first)
+    assert none == rand == perf == mixed
