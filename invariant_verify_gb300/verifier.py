@@ -69,27 +69,53 @@ class DecoderVerifier:
         self.launches_per_step = 5 + cfg.layers * 13
 
     # -------------------------------------------------------------- stages
-    def forward(self, win: Window) -> None:
-        """Hidden state and fp32 logits of every window row (cache rows written)."""
+    def forward(self, win: Window, trace: dict | None = None) -> None:
+        """Hidden state of every window row (cache rows written).
+
+        ``trace``, if given, receives a copy of every intermediate (for
+        stage-by-stage parity tests); it adds device copies, so it is not for
+        the timed path.
+        """
         c, w = self.cfg, self.w
         Hq, Hkv, hd = c.Hq, c.Hkv, c.hd
+
+        def snap(name, t):
+            if trace is not None:
+                trace[name] = t.clone()
+
         B.biv_embed(w["embed"], win.tokens, self.x)
+        snap("x_in", self.x)
         for l in range(c.layers):
             B.biv_rmsnorm(self.x, w[f"l{l}.attn_norm"], self.h, c.eps)
+            snap(f"l{l}.h_attn", self.h)
             B.biv_gemm_nosplitk(self.h, w[f"l{l}.wqkv"], self.qkv)
+            snap(f"l{l}.qkv", self.qkv)
             B.biv_rope_qk(self.qkv, self.q, self.k, win.row_pos, Hq, Hkv, hd, c.rope_theta)
+            snap(f"l{l}.q", self.q)
+            snap(f"l{l}.k", self.k)
             v_new = self.qkv[:, (Hq + Hkv) * hd:]
             B.biv_kv_overwrite(self.kc[l], self.vc[l], self.k, v_new, win.row_slot, win.row_pos, K=self.rpg)
+            if trace is not None:
+                trace[f"l{l}.kc"], trace[f"l{l}.vc"] = self.kc[l].clone(), self.vc[l].clone()
             B.biv_decode_attn_fixedsplit(self.q, self.kc[l], self.vc[l], win.row_slot, win.row_pos, self.o,
                                          self.rpg, self.workspace)
+            snap(f"l{l}.o", self.o)
             B.biv_gemm_nosplitk(self.o.view(self.W, Hq * hd), w[f"l{l}.wo"], self.proj)
+            snap(f"l{l}.attn_proj", self.proj)
             B.biv_residual_add(self.x, self.proj, self.x)
+            snap(f"l{l}.x_mid", self.x)
             B.biv_rmsnorm(self.x, w[f"l{l}.ffn_norm"], self.h, c.eps)
+            snap(f"l{l}.h_ffn", self.h)
             B.biv_gemm_nosplitk(self.h, w[f"l{l}.wgu"], self.gu)
+            snap(f"l{l}.gu", self.gu)
             B.biv_silu_mul(self.gu, self.act)
+            snap(f"l{l}.act", self.act)
             B.biv_gemm_nosplitk(self.act, w[f"l{l}.wdown"], self.proj)
+            snap(f"l{l}.down", self.proj)
             B.biv_residual_add(self.x, self.proj, self.x)
+            snap(f"l{l}.x_out", self.x)
         B.biv_rmsnorm(self.x, w["final_norm"], self.hidden, c.eps)
+        snap("hidden", self.hidden)
 
     def lm_head(self) -> None:
         B.biv_gemm_nosplitk(self.hidden, self.w["lm_head"], self.logits)

@@ -99,7 +99,73 @@ def _window(cfg, ctx, tokens, draft, p0=None):
     return make_window(cfg.N, cfg.K, tokens, p0, torch.arange(cfg.N) * 1000 + 17, draft)
 
 
-def test_decoder_parity_with_oracle(dec2):
+def _cpu(t):
+    return t.detach().cpu()
+
+
+def test_decoder_stagewise_parity(dec2):
+    """Every kernel of the composed step against the oracle, each fed the
+    GPU's own inputs for that stage (so the tolerance is the per-kernel one)."""
+    cfg = synth.DECODER2
+    w, caches, ctx, max_len = dec2
+    W, Hq, Hkv, hd = cfg.W, cfg.Hq, cfg.Hkv, cfg.hd
+    toks = torch.randint(0, cfg.vocab, (W,), generator=synth.generator(50), dtype=torch.int64).to(torch.int32)
+    win = _window(cfg, ctx, toks, toks)
+    ver = DecoderVerifier(cfg, w, caches, cfg.N, max_len, W, cfg.K)
+    tr = {}
+    ver.forward(win, trace=tr)
+    ver.lm_head()
+    ver.select_and_accept(win)
+    torch.cuda.synchronize()
+    slot, pos = win.row_slot.cpu().numpy(), win.row_pos.cpu().numpy()
+    ones = np.ones(cfg.d)
+    assert torch.equal(_cpu(tr["x_in"]), w["embed"][toks.long()])
+    x = tr["x_in"]
+    for l in range(cfg.layers):
+        assert_close(tr[f"l{l}.h_attn"], oracle.rmsnorm(_cpu(x), ones, cfg.eps), what=f"l{l} rmsnorm")
+        assert_close(tr[f"l{l}.qkv"], oracle.gemm(_cpu(tr[f"l{l}.h_attn"]), w[f"l{l}.wqkv"]), what=f"l{l} qkv")
+        qkv = oracle.from_bf16(_cpu(tr[f"l{l}.qkv"]))
+        assert_close(tr[f"l{l}.q"], oracle.rope(qkv[:, :Hq * hd].reshape(W, Hq, hd), pos, cfg.rope_theta),
+                     what=f"l{l} rope q")
+        assert_close(tr[f"l{l}.k"].view(W, Hkv, hd),
+                     oracle.rope(qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(W, Hkv, hd), pos, cfg.rope_theta),
+                     what=f"l{l} rope k")
+        # KV overwrite: exactly the window rows now hold the verifier's k and v
+        kc = oracle._np(caches[l][0]).copy(); vc = oracle._np(caches[l][1]).copy()
+        vnew = oracle._np(_cpu(tr[f"l{l}.qkv"])[:, (Hq + Hkv) * hd:].contiguous()).reshape(W, Hkv, hd)
+        oracle.kv_overwrite(kc, vc, oracle._np(_cpu(tr[f"l{l}.k"])).reshape(W, Hkv, hd), vnew, slot, pos)
+        assert np.array_equal(oracle._np(_cpu(tr[f"l{l}.kc"])), kc)
+        assert np.array_equal(oracle._np(_cpu(tr[f"l{l}.vc"])), vc)
+        assert_close(tr[f"l{l}.o"], oracle.attention(_cpu(tr[f"l{l}.q"]), kc, vc, slot, pos), what=f"l{l} attn")
+        assert_close(tr[f"l{l}.attn_proj"], oracle.gemm(_cpu(tr[f"l{l}.o"]).view(W, Hq * hd), w[f"l{l}.wo"]),
+                     what=f"l{l} wo")
+        assert_close(tr[f"l{l}.x_mid"], oracle.from_bf16(_cpu(x)) + oracle.from_bf16(_cpu(tr[f"l{l}.attn_proj"])),
+                     what=f"l{l} residual")
+        assert_close(tr[f"l{l}.h_ffn"], oracle.rmsnorm(_cpu(tr[f"l{l}.x_mid"]), ones, cfg.eps), what=f"l{l} norm2")
+        assert_close(tr[f"l{l}.gu"], oracle.gemm(_cpu(tr[f"l{l}.h_ffn"]), w[f"l{l}.wgu"]), what=f"l{l} gate/up")
+        assert_close(tr[f"l{l}.act"], oracle.silu_mul(_cpu(tr[f"l{l}.gu"])), what=f"l{l} swiglu")
+        assert_close(tr[f"l{l}.down"], oracle.gemm(_cpu(tr[f"l{l}.act"]), w[f"l{l}.wdown"]), what=f"l{l} down")
+        assert_close(tr[f"l{l}.x_out"], oracle.from_bf16(_cpu(tr[f"l{l}.x_mid"])) +
+                     oracle.from_bf16(_cpu(tr[f"l{l}.down"])), what=f"l{l} residual 2")
+        x = tr[f"l{l}.x_out"]
+    assert_close(tr["hidden"], oracle.rmsnorm(_cpu(x), ones, cfg.eps), what="final norm")
+    assert_close(ver.logits, oracle.gemm(_cpu(tr["hidden"]), w["lm_head"]), what="lm head")
+    # selection and accept: bit-exact against the oracle on the GPU's logits
+    tgt = oracle.gumbel_argmax(_cpu(ver.logits), _cpu(win.row_req), pos, SEED, cfg.temperature)
+    assert np.array_equal(ver.target.cpu().numpy(), tgt)
+    rL, rnl = oracle.verify_accept(tgt, toks.numpy(), ctx.numpy(), cfg.N, cfg.K)
+    assert np.array_equal(ver.accept_len.cpu().numpy(), rL)
+    assert np.array_equal(ver.new_len.cpu().numpy(), rnl)
+
+
+# End-to-end, GPU and oracle drift apart through 24 chained bf16 storage
+# points (each a rounding of up to 2^-9 relative, taken on slightly different
+# fp32 / fp64 values) and are re-amplified by the final RMSNorm; this bound
+# is for that drift, not the per-kernel tolerance.
+E2E_LOGIT_TOL = 0.1
+
+
+def test_decoder_end_to_end_against_oracle(dec2):
     cfg = synth.DECODER2
     w, caches, ctx, max_len = dec2
     W = cfg.W
@@ -110,24 +176,13 @@ def test_decoder_parity_with_oracle(dec2):
     torch.cuda.synchronize()
     orc = OracleDecoder(cfg, w, caches, cfg.N, max_len)
     out = orc.forward(toks.numpy(), win.row_slot.cpu().numpy(), win.row_pos.cpu().numpy(), storage="bf16")
-    assert_close(ver.hidden, out["hidden"], what="final hidden")
-    assert_close(ver.logits, out["logits"], what="logits")
-    # the cache rows the verifier wrote match the oracle's writes (within bf16 rounding)
-    for l in range(cfg.layers):
-        kg = ver.kc[l].cpu()
-        ko = torch.from_numpy(orc.caches[l][0].view(np.int16)).view(torch.bfloat16)
-        assert_close(kg.float(), ko.float().numpy(), what="cache K")
-    # selection and accept: bit-exact against the oracle on the GPU's logits
-    tgt = oracle.gumbel_argmax(ver.logits.cpu(), win.row_req.cpu(), win.row_pos.cpu(), SEED, cfg.temperature)
-    assert np.array_equal(ver.target.cpu().numpy(), tgt)
-    rL, rnl = oracle.verify_accept(tgt, toks.numpy(), ctx.numpy(), cfg.N, cfg.K)
-    assert np.array_equal(ver.accept_len.cpu().numpy(), rL)
-    assert np.array_equal(ver.new_len.cpu().numpy(), rnl)
-    # end-to-end token agreement with the oracle's own logits: report; any
-    # disagreement must be a near-tie within the propagated error
+    err = assert_close(ver.logits, out["logits"], tol=E2E_LOGIT_TOL, what="end-to-end logits")
+    print(f"end-to-end logits max rel err {err:.4f}")
+    tgt = ver.target.cpu().numpy()
     otg = oracle.gumbel_argmax(out["logits"].astype(np.float32), win.row_req.cpu(), win.row_pos.cpu(), SEED,
                                cfg.temperature)
     diff = np.nonzero(otg != tgt)[0]
+    print(f"end-to-end token agreement {W - len(diff)}/{W}")
     assert len(diff) <= W // 8, f"{len(diff)} of {W} end-to-end tokens differ"
 
 
