@@ -32,7 +32,10 @@
  *     device error word, read with biv_device_error().
  *   - Inputs are never modified, except the caches of biv_kv_overwrite and the
  *     caller-provided workspace of biv_decode_attn_fixedsplit.
- *   - The library allocates no device memory.
+ *   - No call allocates device memory.  The one exception in kind is the fixed
+ *     scratch array behind biv_decode_attn_fixedsplit_noalloc, which is part
+ *     of the loaded module (BIV_NOALLOC_SCRATCH_BYTES per GPU, held until the
+ *     process exits).
  */
 #ifndef BIV_H_
 #define BIV_H_
@@ -54,7 +57,8 @@ typedef enum biv_status {
     BIV_ERR_VALUE = 4,       /* a scalar is out of its domain (eps, temperature, ...) */
     BIV_ERR_UNSUPPORTED = 5, /* valid, but not built (head dim != 128, split != 256)  */
     BIV_ERR_CUDA = 6,        /* a CUDA runtime call failed; see biv_last_cuda_error() */
-    BIV_ERR_DEVICE = 7       /* no usable sm_100-family device for this call          */
+    BIV_ERR_DEVICE = 7,      /* no usable sm_100-family device for this call          */
+    BIV_ERR_SCRATCH = 8      /* the problem needs more than the fixed no-alloc scratch */
 } biv_status;
 
 typedef enum biv_dtype { BIV_BF16 = 0, BIV_F32 = 1 } biv_dtype;
@@ -145,6 +149,33 @@ int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, const void* v
 /* Largest number of drafts D with G * (1 + D) <= tile ([GUIDE] GQA tile rule:
  * D = tile / G - 1).  Returns -1 when G <= 0 or G > tile.                  */
 int biv_gqa_max_drafts(int G, int tile);
+
+/* Bytes of the scratch array that biv_decode_attn_fixedsplit_noalloc uses. */
+#define BIV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* The same attention as biv_decode_attn_fixedsplit, for callers that cannot
+ * allocate device memory: code that runs where cudaMalloc is unavailable or
+ * forbidden (inside a memory-pool-managed runtime that owns every device
+ * allocation, a plugin with no allocator handle, or a step that must not
+ * touch the allocator mid-run).  The pages have no counterpart; this is a
+ * convenience of the library.
+ * Instead of a caller workspace it uses one file-scope device array of
+ * BIV_NOALLOC_SCRATCH_BYTES (16 MiB) that every GPU loading the library holds
+ * until the process exits.  Problems whose workspace
+ * (biv_decode_attn_workspace_size) exceeds that return BIV_ERR_SCRATCH and
+ * launch nothing.  The first call on each device looks up the array's device
+ * address (with that device current), so make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last
+ * call's contents (nothing in it has to start at zero: every partial is
+ * written before it is read); calls whose kernels overlap on the GPU -- on
+ * different streams, or from different threads -- race on it.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.  Other arguments and
+ * results are exactly those of biv_decode_attn_fixedsplit.              */
+int biv_decode_attn_fixedsplit_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* row_slot, const int32_t* row_pos, void* o,
+                                       int W, int rows_per_group, int Hq, int Hkv, int hd,
+                                       int n_slots, int max_len, int kv_split,
+                                       biv_stream_t stream);
 
 /* ------------------------------------------------------ KV overwrite
  * [DVR] para 3: at each verification the fast path's cache rows are

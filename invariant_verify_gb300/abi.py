@@ -18,6 +18,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "biv.h")
 
 BIV_BF16, BIV_F32 = 0, 1
 KV_SPLIT, HEAD_DIM, ATTN_TILE = 256, 128, 128
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
 
@@ -44,6 +45,7 @@ SIGNATURES = {
     "biv_gemm_tile_n": (_I, [_I, _I]),
     "biv_decode_attn_workspace_size": (_SZ, [_I, _I, _I]),
     "biv_decode_attn_fixedsplit": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "biv_decode_attn_fixedsplit_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "biv_gqa_max_drafts": (_I, [_I, _I]),
     "biv_kv_overwrite": (_I, [_P, _P, _P, _LL, _P, _LL, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "biv_gumbel_argmax": (_I, [_P, _I, _I, _LL, _P, _P, _U64, _F, _P, _P]),
@@ -144,6 +146,17 @@ def biv_decode_attn_fixedsplit(q, k_cache, v_cache, row_slot, row_pos, o, rows_p
     _check("biv_decode_attn_fixedsplit", _load().biv_decode_attn_fixedsplit(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(row_slot), _ptr(row_pos), _ptr(o), W, rows_per_group,
         Hq, Hkv, hd, n_slots, max_len, KV_SPLIT, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def biv_decode_attn_fixedsplit_noalloc(q, k_cache, v_cache, row_slot, row_pos, o, rows_per_group: int,
+                                       stream=None) -> None:
+    """Attention without a workspace argument: the library's fixed 16 MiB
+    scratch array holds the partials (for callers that cannot allocate)."""
+    W, Hq, hd = q.shape
+    n_slots, Hkv, max_len, _ = k_cache.shape
+    _check("biv_decode_attn_fixedsplit_noalloc", _load().biv_decode_attn_fixedsplit_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(row_slot), _ptr(row_pos), _ptr(o), W, rows_per_group,
+        Hq, Hkv, hd, n_slots, max_len, KV_SPLIT, _stream(stream)))
 
 
 def biv_gqa_max_drafts(G: int, tile: int = ATTN_TILE) -> int:

@@ -53,6 +53,7 @@ extern "C" const char* biv_status_string(int status) {
         case BIV_ERR_UNSUPPORTED: return "valid arguments, but this configuration is not built";
         case BIV_ERR_CUDA: return "a CUDA runtime call failed (see biv_last_cuda_error)";
         case BIV_ERR_DEVICE: return "no usable device for this call";
+        case BIV_ERR_SCRATCH: return "the problem needs more scratch than the no-alloc entry point holds";
         default: return "unknown status";
     }
 }

@@ -25,6 +25,7 @@
 // mma.sync is ample here.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "biv_common.cuh"
 
@@ -505,4 +506,67 @@ extern "C" int biv_kv_overwrite(void* k_cache, void* v_cache, const void* k_new,
         static_cast<const __nv_bfloat16*>(k_new), k_stride, static_cast<const __nv_bfloat16*>(v_new), v_stride,
         row_slot, row_pos, rows_keep, K, Hkv, hd, n_slots, max_len);
     return launch_status();
+}
+
+// ------------------------------------------------ no-alloc attention variant
+// For callers that may not allocate device memory (an allocator owned by a
+// host runtime, a plugin with no allocator handle): the attention partials
+// live in this fixed array instead of a caller workspace.  It is device
+// memory of the loaded module, BIV_NOALLOC_SCRATCH_BYTES per GPU, kept until
+// the process exits.  In host code `g_attn_scratch` is only a stand-in for the
+// symbol; its device address comes from cudaGetSymbolAddress, looked up once
+// per device with that device current.
+namespace biv {
+namespace {
+
+static __device__ __align__(256) unsigned char g_attn_scratch[BIV_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, or nullptr with
+// *status set.
+void* attn_scratch(int* status) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *status = cuda_status(e);
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        *status = BIV_ERR_DEVICE;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> g(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attn_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            *status = cuda_status(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+            return nullptr;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *status = BIV_OK;
+    return g_scratch_addr[dev];
+}
+
+}  // namespace
+}  // namespace biv
+
+extern "C" int biv_decode_attn_fixedsplit_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                                  const int32_t* row_slot, const int32_t* row_pos, void* o, int W,
+                                                  int rows_per_group, int Hq, int Hkv, int hd, int n_slots,
+                                                  int max_len, int kv_split, biv_stream_t stream) {
+    if (W < 0 || Hq <= 0 || Hkv <= 0 || n_slots <= 0 || max_len <= 0 || rows_per_group <= 0)
+        return BIV_ERR_SHAPE;
+    if (hd != HD || kv_split != SPLIT) return BIV_ERR_UNSUPPORTED;
+    if (W == 0) return BIV_OK;
+    if (biv_decode_attn_workspace_size(W, Hq, max_len) > BIV_NOALLOC_SCRATCH_BYTES) return BIV_ERR_SCRATCH;
+    int st = BIV_OK;
+    void* scratch = attn_scratch(&st);
+    if (!scratch) return st;
+    return biv_decode_attn_fixedsplit(q, k_cache, v_cache, row_slot, row_pos, o, W, rows_per_group, Hq, Hkv, hd,
+                                      n_slots, max_len, kv_split, scratch, BIV_NOALLOC_SCRATCH_BYTES, stream);
 }
