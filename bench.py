@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--gemm-sweep", action="store_true",
+                   help="instead of the step bench: no-split-K GEMM vs cuBLAS on the Llama-3-8B shapes")
     return p.parse_args()
 
 
@@ -309,6 +311,66 @@ def run_e2e(ver, win, graph, flush, cfg, K, world, device):
             "how": "pinned H2D of the window inputs + CUDA-graph step + D2H of accept_len/new_len/tokens + sync"}
 
 
+# ------------------------------------------------------------ GEMM sweep
+def run_gemm_sweep(args):
+    """TFLOP/s and HBM GB/s of the no-split-K GEMM against cuBLAS's default
+    (torch.matmul, free to split K) on the Llama-3-8B-shaped weights, and how
+    many output rows cuBLAS changes bitwise when the same rows are computed
+    at another M (the cost and the need for invariance)."""
+    from invariant_verify_gb300 import abi as B
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    hbm, bf16, _ = peaks()
+    shapes = {"qkv": (6144, 4096), "wo": (4096, 4096), "gate_up": (28672, 4096), "down": (4096, 14336),
+              "lm_head": (128256, 4096)}
+    Ms = [1, 8, 32, 64, 128, 256, 512, 1024]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    rows = []
+    for name, (N, K) in shapes.items():
+        g = torch.Generator(device="cuda").manual_seed(N + K)
+        Bw = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        A = torch.randn(max(Ms), K, device="cuda", generator=g).to(torch.bfloat16)
+        ref_ours = torch.empty(max(Ms), N, device="cuda", dtype=torch.bfloat16)
+        B.biv_gemm_nosplitk(A, Bw, ref_ours)
+        ref_cublas = A @ Bw.t()
+        for M in Ms:
+            a = A[:M].contiguous()
+            c = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+            times = {}
+            for impl in ("ours", "cublas"):
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * 20)]
+                for i in range(23):
+                    flush.zero_()
+                    if i >= 3:
+                        ev[2 * (i - 3)].record()
+                    if impl == "ours":
+                        B.biv_gemm_nosplitk(a, Bw, c)
+                    else:
+                        torch.matmul(a, Bw.t(), out=c)
+                    if i >= 3:
+                        ev[2 * (i - 3) + 1].record()
+                torch.cuda.synchronize()
+                times[impl] = statistics.median(ev[2 * j].elapsed_time(ev[2 * j + 1]) for j in range(20)) / 1e3
+            ours_rows = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+            B.biv_gemm_nosplitk(a, Bw, ours_rows)
+            diff_ours = int((ours_rows.view(torch.int16) != ref_ours[:M].view(torch.int16)).any(dim=1).sum())
+            diff_cublas = int((torch.matmul(a, Bw.t()).view(torch.int16) !=
+                               ref_cublas[:M].view(torch.int16)).any(dim=1).sum())
+            flops = 2.0 * M * N * K
+            byts = 2.0 * N * K + 2.0 * M * K + 2.0 * M * N
+            rows.append({"gemm": name, "M": M, "N": N, "K": K,
+                         "ours_us": round(times["ours"] * 1e6, 2), "cublas_us": round(times["cublas"] * 1e6, 2),
+                         "ours_tflops": round(flops / times["ours"] / 1e12, 1),
+                         "cublas_tflops": round(flops / times["cublas"] / 1e12, 1),
+                         "ours_gbs": round(byts / times["ours"] / 1e9, 1),
+                         "ours_frac_hbm": round(byts / times["ours"] / 1e9 / hbm, 3),
+                         "ours_frac_tensor": round(flops / times["ours"] / 1e12 / bf16, 3),
+                         "rows_differing_vs_M1024": {"ours": diff_ours, "cublas": diff_cublas}})
+            print(json.dumps(rows[-1]), flush=True)
+    return rows
+
+
 # ------------------------------------------------------- CPU oracle timing
 def oracle_rows_per_second(cfg, w_cpu, caches_cpu, max_len, win, seconds, max_steps=None, warmup=0):
     import oracle
@@ -380,7 +442,9 @@ def run_reference(args):
 
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    if a.gemm_sweep:
+        run_gemm_sweep(a)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)

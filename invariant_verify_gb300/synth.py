@@ -140,6 +140,45 @@ def bf16_normal(shape, std: float, gen: torch.Generator) -> torch.Tensor:
     return (torch.randn(*shape, generator=gen, dtype=torch.float32) * std).to(torch.bfloat16)
 
 
+def bf16_normal_device(shape, std: float, seed: int, device="cuda") -> torch.Tensor:
+    """N(0, std^2) bf16 samples drawn on the device with a seeded generator
+    (for multi-GB inputs; the stream differs from the CPU generator's)."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    return (torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+def decoder_weights_device(cfg: DecoderConfig, seed: int | None = None, device="cuda") -> dict:
+    """Like decoder_weights, drawn on the device (same layout, other stream)."""
+    s0 = cfg.seed if seed is None else seed
+    w = {"embed": bf16_normal_device((cfg.vocab, cfg.d), cfg.w_std, s0 * 1000 + 1, device)}
+    for l in range(cfg.layers):
+        b = s0 * 1000 + 10 * (l + 1)
+        w[f"l{l}.attn_norm"] = torch.ones(cfg.d, dtype=torch.bfloat16, device=device)
+        w[f"l{l}.wqkv"] = bf16_normal_device((cfg.qkv_n, cfg.d), cfg.w_std, b + 1, device)
+        w[f"l{l}.wo"] = bf16_normal_device((cfg.d, cfg.Hq * cfg.hd), cfg.w_std, b + 2, device)
+        w[f"l{l}.ffn_norm"] = torch.ones(cfg.d, dtype=torch.bfloat16, device=device)
+        w[f"l{l}.wgu"] = bf16_normal_device((2 * cfg.ffn, cfg.d), cfg.w_std, b + 3, device)
+        w[f"l{l}.wdown"] = bf16_normal_device((cfg.d, cfg.ffn), cfg.w_std, b + 4, device)
+    w["final_norm"] = torch.ones(cfg.d, dtype=torch.bfloat16, device=device)
+    w["lm_head"] = bf16_normal_device((cfg.vocab, cfg.d), cfg.w_std, s0 * 1000 + 2, device)
+    return w
+
+
+def kv_cache_device(n_slots: int, Hkv: int, max_len: int, hd: int, ctx: torch.Tensor, seed: int,
+                    layers: int = 1, device="cuda") -> list:
+    """Like kv_cache, drawn on the device: N(0,1) below ctx[slot], zero above."""
+    out = []
+    pos = torch.arange(max_len, device=device)
+    keep = (pos[None, :] < ctx.to(device)[:, None])[:, None, :, None]
+    for l in range(layers):
+        pair = []
+        for kv in range(2):
+            c = bf16_normal_device((n_slots, Hkv, max_len, hd), 1.0, seed * 100 + 2 * l + kv, device)
+            pair.append(torch.where(keep, c, torch.zeros((), dtype=c.dtype, device=device)).contiguous())
+        out.append(tuple(pair))
+    return out
+
+
 def decoder_weights(cfg: DecoderConfig, seed: int | None = None) -> dict:
     """Random-init decoder verifier weights, nn.Linear layout [out, in].
 
