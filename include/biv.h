@@ -101,23 +101,28 @@ int biv_rmsnorm(const void* x, const void* w, void* y, int rows, int d, float ep
  *   C[m][n] = sum_k A[m][k] * B[n][k]        (fp32 accumulation)
  * A: bf16 [M, K] row-major; B: bf16 [N, K] row-major (nn.Linear weight);
  * C: [M, N] row-major, bf16 (round-to-nearest-even) or fp32 per out_dtype.
- * tcgen05 tensor-core MMAs (M tile 128, K step 16) accumulate in TMEM; the K
- * loop runs in one CTA in increasing k, so every element's accumulation order
- * is fixed and independent of M and of the tile that holds the row.
+ * tcgen05 tensor-core MMAs (M tile 128, K step 16) accumulate in TMEM; each
+ * output tile's K loop runs in one CTA in increasing k, so every element's
+ * accumulation order is fixed and independent of M, of the tile width and of
+ * the row's position inside the tile (outputs are bitwise identical for any
+ * M; tests check this).  Launched with programmatic dependent launch.
  * Requires M >= 0, N % 8 == 0, K % 8 == 0, K > 0, N > 0, 16-B aligned pointers.
  * C must not overlap A or B.                                              */
 int biv_gemm_nosplitk(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K,
                       biv_stream_t stream);
 
-/* Same GEMM with the N-tile width forced (16, 32, 64, 128 or 256) instead of
- * chosen from (N, K).  For tests of tile-shape independence and for tuning;
- * results are bitwise identical to biv_gemm_nosplitk's.                    */
+/* Same GEMM with the N-tile width forced (a multiple of 16 in [16, 256])
+ * instead of chosen by biv_gemm_tile_n.  For tests of tile-width
+ * independence and for tuning; results are bitwise identical to
+ * biv_gemm_nosplitk's.                                                    */
 int biv_gemm_nosplitk_bn(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K,
                          int bn, biv_stream_t stream);
 
-/* The N-tile width biv_gemm_nosplitk uses for (N, K); a function of N and K
- * only, never of M or of the device.                                       */
-int biv_gemm_tile_n(int N, int K);
+/* The N-tile width biv_gemm_nosplitk uses: with one row tile (M <= 128) the
+ * widest tile that keeps the N tiles within one wave of 152 CTAs; otherwise
+ * the width in [64, 256] that best fills whole waves (mildly preferring wide
+ * tiles).  Only the work split depends on it, never an element's arithmetic. */
+int biv_gemm_tile_n(int M, int N, int K);
 
 /* ------------------------------------------- fixed-split decode attention
  * [DVR] para 1: attention with a fixed KV-split size that never adapts to the
@@ -236,6 +241,17 @@ int biv_verify_accept(const int32_t* target, const int32_t* draft, const int32_t
 /* --------------------------------------- per-row glue of the decoder layer
  * The pages do not describe the verifier model; these are the standard
  * pre-norm Llama pieces needed to compose one (each row is independent).   */
+
+/* Fused residual add + RMSNorm: x_out = bf16(x + r), y = RMSNorm(x_out) * w,
+ * bit-identical to biv_residual_add followed by biv_rmsnorm.  x_out may alias
+ * x.  Same requirements as biv_rmsnorm.                                    */
+int biv_add_rmsnorm(const void* x, const void* r, const void* w, void* x_out, void* y, int rows, int d,
+                    float eps, biv_stream_t stream);
+
+/* Fused embedding gather + RMSNorm: x_out = table[tokens], y = RMSNorm(x_out) * w,
+ * bit-identical to biv_embed followed by biv_rmsnorm.                      */
+int biv_embed_rmsnorm(const void* table, const int32_t* tokens, const void* w, void* x_out, void* y,
+                      int W, int d, int vocab, float eps, biv_stream_t stream);
 
 /* out[w] = table[tokens[w]] ; table bf16 [vocab, d], out bf16 [W, d], d % 8 == 0. */
 int biv_embed(const void* table, const int32_t* tokens, void* out, int W, int d, int vocab,

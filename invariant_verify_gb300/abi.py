@@ -42,7 +42,7 @@ SIGNATURES = {
     "biv_rmsnorm": (_I, [_P, _P, _P, _I, _I, _F, _P]),
     "biv_gemm_nosplitk": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "biv_gemm_nosplitk_bn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
-    "biv_gemm_tile_n": (_I, [_I, _I]),
+    "biv_gemm_tile_n": (_I, [_I, _I, _I]),
     "biv_decode_attn_workspace_size": (_SZ, [_I, _I, _I]),
     "biv_decode_attn_fixedsplit": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "biv_decode_attn_fixedsplit_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
@@ -53,6 +53,8 @@ SIGNATURES = {
     "biv_gumbel_from_words": (_I, [_P, _LL, _P, _P]),
     "biv_verify_accept": (_I, [_P, _P, _P, _I, _I, _P, _P, _P]),
     "biv_embed": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "biv_add_rmsnorm": (_I, [_P, _P, _P, _P, _P, _I, _I, _F, _P]),
+    "biv_embed_rmsnorm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P]),
     "biv_rope_qk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
     "biv_silu_mul": (_I, [_P, _P, _I, _I, _P]),
     "biv_residual_add": (_I, [_P, _P, _P, _LL, _P]),
@@ -130,8 +132,8 @@ def biv_gemm_nosplitk(A, B, C_out, stream=None, bn: int | None = None) -> None:
     _check("biv_gemm_nosplitk", st)
 
 
-def biv_gemm_tile_n(N: int, K: int) -> int:
-    return _load().biv_gemm_tile_n(N, K)
+def biv_gemm_tile_n(M: int, N: int, K: int) -> int:
+    return _load().biv_gemm_tile_n(M, N, K)
 
 
 def biv_decode_attn_workspace_size(W: int, Hq: int, max_len: int) -> int:
@@ -196,6 +198,18 @@ def biv_gumbel_from_words(words, g, stream=None) -> None:
 def biv_verify_accept(target, draft, p0, N: int, K: int, accept_len, new_len, stream=None) -> None:
     _check("biv_verify_accept", _load().biv_verify_accept(
         _ptr(target), _ptr(draft), _ptr(p0), N, K, _ptr(accept_len), _ptr(new_len), _stream(stream)))
+
+
+def biv_add_rmsnorm(x, r, w, x_out, y, eps: float, stream=None) -> None:
+    rows, d = x.shape
+    _check("biv_add_rmsnorm", _load().biv_add_rmsnorm(_ptr(x), _ptr(r), _ptr(w), _ptr(x_out), _ptr(y), rows, d,
+                                                      eps, _stream(stream)))
+
+
+def biv_embed_rmsnorm(table, tokens, w, x_out, y, eps: float, stream=None) -> None:
+    vocab, d = table.shape
+    _check("biv_embed_rmsnorm", _load().biv_embed_rmsnorm(_ptr(table), _ptr(tokens), _ptr(w), _ptr(x_out), _ptr(y),
+                                                          tokens.shape[0], d, vocab, eps, _stream(stream)))
 
 
 def biv_embed(table, tokens, out, stream=None) -> None:

@@ -109,6 +109,8 @@ attn_split_kernel(const AttnParams P) {
     __shared__ int s_pos[BIV_ATTN_TILE];
     __shared__ int s_maxpos;
 
+    pdl_wait();
+    pdl_trigger();
     const int split = blockIdx.x;
     const int kvh = blockIdx.y;
     const int tile = blockIdx.z;
@@ -308,9 +310,14 @@ attn_split_kernel(const AttnParams P) {
     }
 }
 
-// One warp per (row, head): combine splits 0 .. pos/256 in increasing order.
+// One warp per (row, head): combine splits 0 .. pos/256 of the row.  Lane s
+// holds split s (32 at a time); the maximum and the weight sum are reduced
+// with a fixed xor butterfly, the outputs are summed in increasing split
+// order.  All loads of a group of splits are independent, so they overlap.
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const long long pair = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (pair >= static_cast<long long>(P.W) * P.Hq) return;
@@ -324,18 +331,34 @@ attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
     }
     const int ns = p / SPLIT + 1;
     const long long base = pair * P.s_max;
+    // Row maximum over all splits.
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, P.ws_m[base + s]);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+        float m = (s0 + lane < ns) ? P.ws_m[base + s0 + lane] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        M = fmaxf(M, m);
+    }
     float L = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < ns; ++s) {
-        const float wgt = exp2f(P.ws_m[base + s] - M);
-        L += wgt * P.ws_l[base + s];
-        const float4 v = *reinterpret_cast<const float4*>(P.ws_o + (base + s) * HD + lane * 4);
-        acc.x += wgt * v.x;
-        acc.y += wgt * v.y;
-        acc.z += wgt * v.z;
-        acc.w += wgt * v.w;
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+        const int s = s0 + lane;
+        const float wgt = (s < ns) ? exp2f(P.ws_m[base + s] - M) : 0.0f;
+        float lw = (s < ns) ? wgt * P.ws_l[base + s] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+        L += lw;
+        const int cnt = min(32, ns - s0);
+        const float4* src = reinterpret_cast<const float4*>(P.ws_o + (base + s0) * HD) + lane;
+#pragma unroll 4
+        for (int j = 0; j < cnt; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wgt, j);
+            const float4 v = src[static_cast<long long>(j) * (HD / 4)];
+            acc.x += wj * v.x;
+            acc.y += wj * v.y;
+            acc.z += wj * v.z;
+            acc.w += wj * v.w;
+        }
     }
     const float inv = 1.0f / L;
     uint2 r;
@@ -348,6 +371,8 @@ attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
 __global__ void rope_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __restrict__ q_out,
                             __nv_bfloat16* __restrict__ k_out, const int32_t* __restrict__ row_pos, int W,
                             int Hq, int Hkv, int hd, float theta) {
+    pdl_wait();
+    pdl_trigger();
     const int half = hd / 2;
     const long long total = static_cast<long long>(W) * (Hq + Hkv) * half;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
@@ -376,6 +401,8 @@ __global__ void kv_overwrite_kernel(__nv_bfloat16* __restrict__ kc, __nv_bfloat1
                                     const int32_t* __restrict__ row_slot,
                                     const int32_t* __restrict__ row_pos, const int32_t* __restrict__ rows_keep,
                                     int K, int Hkv, int hd, int n_slots, int max_len) {
+    pdl_wait();
+    pdl_trigger();
     const int w = blockIdx.x;
     const int slot = row_slot[w], p = row_pos[w];
     if (rows_keep && (w % K) >= rows_keep[w / K]) return;
@@ -465,14 +492,12 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
         configured_device = dev;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    attn_split_kernel<<<dim3(static_cast<unsigned>(s_max), Hkv, static_cast<unsigned>(n_tiles)), ATTN_THREADS, smem,
-                        s>>>(P);
-    int st = launch_status();
+    int st = launch_pdl(attn_split_kernel, dim3(static_cast<unsigned>(s_max), Hkv, static_cast<unsigned>(n_tiles)),
+                        dim3(ATTN_THREADS), smem, s, P);
     if (st != BIV_OK) return st;
     const long long n_pairs = static_cast<long long>(W) * Hq;
-    attn_combine_kernel<<<static_cast<unsigned>((n_pairs + 7) / 8), 256, 0, s>>>(P,
-                                                                                 static_cast<__nv_bfloat16*>(o));
-    return launch_status();
+    return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>((n_pairs + 7) / 8)), dim3(256), 0, s, P,
+                      static_cast<__nv_bfloat16*>(o));
 }
 
 extern "C" int biv_rope_qk(const void* qkv, void* q_out, void* k_out, const int32_t* row_pos, int W, int Hq,
@@ -483,10 +508,9 @@ extern "C" int biv_rope_qk(const void* qkv, void* q_out, void* k_out, const int3
     if (!qkv || !q_out || !row_pos || (Hkv > 0 && !k_out)) return BIV_ERR_NULL;
     const long long total = static_cast<long long>(W) * (Hq + Hkv) * (hd / 2);
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 8192));
-    rope_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(q_out),
-        static_cast<__nv_bfloat16*>(k_out), row_pos, W, Hq, Hkv, hd, theta);
-    return launch_status();
+    return launch_pdl(rope_kernel, dim3(blocks), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(q_out),
+                      static_cast<__nv_bfloat16*>(k_out), row_pos, W, Hq, Hkv, hd, theta);
 }
 
 extern "C" int biv_kv_overwrite(void* k_cache, void* v_cache, const void* k_new, long long k_stride,
@@ -501,11 +525,10 @@ extern "C" int biv_kv_overwrite(void* k_cache, void* v_cache, const void* k_new,
     if (W == 0) return BIV_OK;
     if (!k_cache || !v_cache || !k_new || !v_new || !row_slot || !row_pos) return BIV_ERR_NULL;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new)) return BIV_ERR_ALIGN;
-    kv_overwrite_kernel<<<W, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache),
-        static_cast<const __nv_bfloat16*>(k_new), k_stride, static_cast<const __nv_bfloat16*>(v_new), v_stride,
-        row_slot, row_pos, rows_keep, K, Hkv, hd, n_slots, max_len);
-    return launch_status();
+    return launch_pdl(kv_overwrite_kernel, dim3(W), dim3(128), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache),
+                      static_cast<const __nv_bfloat16*>(k_new), k_stride, static_cast<const __nv_bfloat16*>(v_new),
+                      v_stride, row_slot, row_pos, rows_keep, K, Hkv, hd, n_slots, max_len);
 }
 
 // ------------------------------------------------ no-alloc attention variant

@@ -25,6 +25,26 @@ inline int launch_status() { return cuda_status(cudaGetLastError()); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int num_sms();                                      // of the current device, cached
 
+// Launch with programmatic dependent launch: the kernel may start while the
+// previous kernel on the stream is finishing; it must execute pdl_wait()
+// before its first global-memory access.  Captured launches keep the
+// programmatic edge inside CUDA graphs.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...));
+}
+
 // Each translation unit owns one device error word and registers a reader.
 typedef cudaError_t (*err_reader_fn)(uint32_t* bits, bool clear);
 void register_err_reader(err_reader_fn fn);
@@ -55,6 +75,13 @@ BIV_DEV uint64_t globaltimer() {
     return t;
 }
 
+// Programmatic dependent launch: wait until the preceding kernel of the
+// stream has completed and its writes are visible (a no-op when the kernel
+// was launched without a programmatic dependency), and let the next kernel
+// begin launching.
+BIV_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+BIV_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 BIV_DEV uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -62,6 +89,10 @@ BIV_DEV uint32_t smem_u32(const void* p) {
 BIV_DEV void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tensor-core operand reads).
+BIV_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 BIV_DEV void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

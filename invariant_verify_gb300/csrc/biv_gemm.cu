@@ -4,20 +4,27 @@
 // Batch invariance ([DVR] para 1: batch-invariant matmul never splits K and
 // always uses the same data-parallel tiling): every output tile is owned by
 // one CTA, whose single MMA thread walks K from 0 upwards in steps of 16
-// (tcgen05.mma kind::f16, M = 128) into one TMEM accumulator.  The tile width
-// is chosen from (N, K) only, and the sequence of MMAs that produces C[m][n]
-// is the same for every M and for every row position inside the tile.
+// (tcgen05.mma kind::f16, M = 128) into one TMEM accumulator.  The sequence of
+// MMAs that produces C[m][n] -- which k-chunks, in which order, into one
+// accumulator -- is the same for every M, every tile width and every row
+// position inside the tile; the tensor core computes each output element of an
+// MMA independently of the instruction's N (checked bitwise on the GPU for
+// N = 16..256), so the tile width is free to follow the problem size.
 //
 // Kernel layout (192 threads, one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per stage,
-//               128-byte swizzle, mbarrier transaction counts.
+//   warp 0      TMA producer: A tile [a_rows x 64] and B tile [BN x 64] per
+//               stage, 128-byte swizzle, mbarrier transaction counts.  For
+//               M <= 128 only the real rows of A are copied (a_rows =
+//               M rounded up to 8); the rest of each A stage is zeroed once.
 //   warp 1      TMEM allocator + single-thread MMA issuer; commits free smem
 //               stages and publish finished accumulators.
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 16 columns, convert, store.
 // Two accumulators in TMEM let the epilogue of tile i overlap the MMAs of
-// tile i + 1.  Every wait is bounded (2 s); on time-out the kernel raises
-// BIV_DEVERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and
-// returns.
+// tile i + 1.  Up to 24 stages keep a whole small weight slice in flight.
+// Launched with programmatic dependent launch: barrier set-up, TMEM
+// allocation and the zero fill overlap the previous kernel.  Every wait is
+// bounded (2 s); on time-out the kernel raises BIV_DEVERR_TIMEOUT, drains its
+// in-flight copies and MMAs, frees TMEM and returns.
 #include <algorithm>
 
 #include "biv_common.cuh"
@@ -27,36 +34,38 @@ namespace {
 
 BIV_DEFINE_ERR_WORD(g_gemm_err)
 
-constexpr int kSmemBudget = 196608;   // bytes of pipeline stages per CTA
+constexpr int kBM = 128;
+constexpr int kBK = 64;                       // 64 bf16 = one 128-byte swizzle row
+constexpr int kABytes = kBM * kBK * 2;        // full A stage (16 KiB)
+constexpr int kRingBudget = 200 * 1024;       // bytes of pipeline stages per CTA
+constexpr int kMaxStages = 24;
+constexpr int kBarBytes = 512;
+constexpr int kWave = 152;                    // CTAs of one wave on a 152-SM part
 
-template <int BN>
-struct GemmShape {
-    static constexpr int BM = 128;
-    static constexpr int BK = 64;                 // 64 bf16 = one 128-byte swizzle row
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (kSmemBudget / STAGE) > 8 ? 8 : (kSmemBudget / STAGE);
-    static constexpr int TMEM_COLS = (2 * BN) < 32 ? 32 : 2 * BN;   // two accumulators
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES;
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0, 16..256");
-    static_assert(STAGE % 1024 == 0, "stages must stay 1024-byte aligned");
-    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+struct GemmArgs {
+    int M, N, K;
+    int BN;          // tile width (multiple of 16, 16..256)
+    int stages;      // ring depth
+    int a_rows;      // rows of A copied per stage (multiple of 8, <= 128)
+    uint32_t idesc;  // tcgen05 instruction descriptor for M=128, N=BN
+    uint32_t tmem_cols;
 };
 
-template <int BN, bool OUT_F32>
+inline int stage_bytes(int BN) { return kABytes + BN * kBK * 2; }
+
+template <bool OUT_F32>
 __global__ void __launch_bounds__(192, 1)
 gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     void* __restrict__ C, int M, int N, int K) {
-    using S = GemmShape<BN>;
+                     void* __restrict__ C, const GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
+    const int STAGE = kABytes + g.BN * kBK * 2;
+    const int S = g.stages;
     uint8_t* tiles = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::STAGES * S::STAGE);
-    uint64_t* empty = full + S::STAGES;
-    uint64_t* tfull = empty + S::STAGES;      // [2]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* tfull = empty + kMaxStages;     // [2]
     uint64_t* tempty = tfull + 2;             // [2]
     uint64_t* drain = tempty + 2;             // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -64,13 +73,15 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m_tiles = (M + S::BM - 1) / S::BM;
+    const int M = g.M, N = g.N, BN = g.BN;
+    const int m_tiles = (M + kBM - 1) / kBM;
     const int n_tiles = (N + BN - 1) / BN;
     const int n_work = m_tiles * n_tiles;
-    const int KB = (K + S::BK - 1) / S::BK;
+    const int KB = (g.K + kBK - 1) / kBK;
+    const uint32_t tx_bytes = static_cast<uint32_t>(g.a_rows * kBK * 2 + BN * kBK * 2);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S::STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -87,13 +98,25 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         prefetch_tensormap(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, S::TMEM_COLS);
+        tmem_alloc(tmem_slot, g.tmem_cols);
         tmem_relinquish();
+    }
+    // Rows of A that TMA does not write stay zero for the whole kernel.
+    if (g.a_rows < kBM) {
+        const int zero_off = g.a_rows * kBK * 2;
+        const int chunks = (kABytes - zero_off) / 16;
+        for (int s = 0; s < S; ++s) {
+            uint4* z = reinterpret_cast<uint4*>(tiles + s * STAGE + zero_off);
+            for (int i = threadIdx.x; i < chunks; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();       // inputs of the previous kernel are complete and visible from here on
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -112,12 +135,12 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = tiles + stage * S::STAGE;
-                    mbar_arrive_expect_tx(&full[stage], S::STAGE);
-                    tma_load_2d(sa, &tmA, &full[stage], kb * S::BK, m_blk * S::BM, pol_a);
-                    tma_load_2d(sa + S::A_BYTES, &tmB, &full[stage], kb * S::BK, n_blk * BN, pol_b);
+                    uint8_t* sa = tiles + stage * STAGE;
+                    mbar_arrive_expect_tx(&full[stage], tx_bytes);
+                    tma_load_2d(sa, &tmA, &full[stage], kb * kBK, m_blk * kBM, pol_a);
+                    tma_load_2d(sa + kABytes, &tmB, &full[stage], kb * kBK, n_blk * BN, pol_b);
                     ++issued;
-                    if (++stage == S::STAGES) {
+                    if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -125,15 +148,14 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             }
             if (!ok) {
                 // Let the copies that may still be in flight land before the CTA exits.
-                long long first = issued > S::STAGES ? issued - S::STAGES : 0;
+                long long first = issued > S ? issued - S : 0;
                 for (long long i = first; i < issued; ++i)
-                    mbar_wait_drain(&full[i % S::STAGES], static_cast<uint32_t>((i / S::STAGES) & 1));
+                    mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1));
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // --------------------------------------------------- MMA issuer
-            constexpr uint32_t IDESC = idesc_bf16_f32(S::BM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -153,18 +175,17 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(tiles + stage * S::STAGE);
+                    const uint32_t a_addr = smem_u32(tiles + stage * STAGE);
                     const uint64_t a_desc = sw128_kmajor_desc(a_addr);
-                    const uint64_t b_desc = sw128_kmajor_desc(a_addr + S::A_BYTES);
+                    const uint64_t b_desc = sw128_kmajor_desc(a_addr + kABytes);
 #pragma unroll
-                    for (int k = 0; k < S::BK / 16; ++k) {
+                    for (int k = 0; k < kBK / 16; ++k) {
                         // +32 bytes along K inside the swizzle row = +2 in 16-byte units.
-                        umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, IDESC,
-                                  (kb > 0 || k > 0) ? 1u : 0u);
+                        umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, g.idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     any = true;
                     umma_commit(&empty[stage]);
-                    if (++stage == S::STAGES) {
+                    if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -190,7 +211,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             const int m_blk = t - n_blk * m_tiles;
             if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err)) break;
             tc_fence_after();
-            const int row = m_blk * S::BM + q * 32 + lane;
+            const int row = m_blk * kBM + q * 32 + lane;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -234,7 +255,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, S::TMEM_COLS);
+    if (warp == 1) tmem_dealloc(tmem_base, g.tmem_cols);
 }
 
 // --------------------------------------------------------------- host side
@@ -270,39 +291,42 @@ bool encode_kmajor(CUtensorMap* map, const void* base, int cols, int rows, int b
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool F32>
-int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream) {
-    using S = GemmShape<BN>;
+uint32_t tmem_cols_for(int BN) {
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(2 * BN)) c <<= 1;
+    return c;
+}
+
+template <bool F32>
+int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream) {
+    GemmArgs g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.BN = BN;
+    g.stages = std::min(kMaxStages, kRingBudget / stage_bytes(BN));
+    g.a_rows = M >= kBM ? kBM : ((M + 7) / 8) * 8;
+    g.idesc = idesc_bf16_f32(kBM, BN);
+    g.tmem_cols = tmem_cols_for(BN);
     CUtensorMap ta, tb;
-    if (!encode_kmajor(&ta, A, K, M, S::BM) || !encode_kmajor(&tb, B, K, N, BN)) {
+    if (!encode_kmajor(&ta, A, K, M, g.a_rows) || !encode_kmajor(&tb, B, K, N, BN)) {
         set_cuda_error(cudaErrorInvalidValue);
         return BIV_ERR_CUDA;
     }
-    auto kern = gemm_nosplitk_kernel<BN, F32>;
+    const int smem = 1024 + g.stages * stage_bytes(BN) + kBarBytes;
+    auto kern = gemm_nosplitk_kernel<F32>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             1024 + kRingBudget + kBarBytes);
         if (e != cudaSuccess) return cuda_status(e);
         configured_device = dev;
     }
-    const long long work = static_cast<long long>((M + S::BM - 1) / S::BM) * ((N + BN - 1) / BN);
+    const long long work = static_cast<long long>((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<long long>(work, num_sms()));
-    kern<<<grid, 192, S::SMEM, stream>>>(ta, tb, C, M, N, K);
-    return launch_status();
-}
-
-template <bool F32>
-int dispatch_bn(int bn, const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t s) {
-    switch (bn) {
-        case 16: return launch_gemm<16, F32>(A, B, C, M, N, K, s);
-        case 32: return launch_gemm<32, F32>(A, B, C, M, N, K, s);
-        case 64: return launch_gemm<64, F32>(A, B, C, M, N, K, s);
-        case 128: return launch_gemm<128, F32>(A, B, C, M, N, K, s);
-        case 256: return launch_gemm<256, F32>(A, B, C, M, N, K, s);
-        default: return BIV_ERR_VALUE;
-    }
+    return launch_pdl(kern, dim3(grid), dim3(192), static_cast<size_t>(smem), stream, ta, tb, C, g);
 }
 
 int check_gemm(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K) {
@@ -315,36 +339,51 @@ int check_gemm(const void* A, const void* B, void* C, int out_dtype, int M, int 
     return BIV_OK;
 }
 
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
 }  // namespace
 }  // namespace biv
 
 using namespace biv;
 
-extern "C" int biv_gemm_tile_n(int N, int K) {
+extern "C" int biv_gemm_tile_n(int M, int N, int K) {
     (void)K;
-    // Widest tile that still gives one full wave of a 152-SM part at one row
-    // tile; narrower tiles only when N is small.  A build constant, not the
-    // device's SM count, so the choice is the same on every GPU.
-    const int wave = 152;
-    const int cands[4] = {256, 128, 64, 32};
-    for (int bn : cands)
-        if ((N + bn - 1) / bn >= wave) return bn;
-    return 16;
+    const long long m_tiles = std::max<long long>(1, ceil_div(M, kBM));
+    if (m_tiles == 1) {
+        // Weight streaming: one wave of tiles, each as wide as that allows.
+        const int bn = static_cast<int>(std::min<long long>(256, std::max<long long>(16, ceil_div(ceil_div(N, kWave), 16) * 16)));
+        if (ceil_div(N, bn) <= kWave) return bn;
+    }
+    // Several waves: the width in [64, 256] that best fills the waves, with a
+    // mild preference for wide tiles (less activation traffic per weight byte).
+    int best = 256;
+    double best_score = -1.0;
+    for (int bn = 256; bn >= 64; bn -= 16) {
+        const long long tiles = m_tiles * ceil_div(N, bn);
+        const long long waves = ceil_div(tiles, kWave);
+        const double fill = static_cast<double>(tiles) / static_cast<double>(waves * kWave);
+        const double score = fill * bn / (bn + 32.0);
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = bn;
+        }
+    }
+    return best;
 }
 
 extern "C" int biv_gemm_nosplitk_bn(const void* A, const void* B, void* C, int out_dtype, int M, int N,
                                     int K, int bn, biv_stream_t stream) {
     int st = check_gemm(A, B, C, out_dtype, M, N, K);
     if (st != BIV_OK || M == 0) return st;
-    if (bn != 16 && bn != 32 && bn != 64 && bn != 128 && bn != 256) return BIV_ERR_VALUE;
+    if (bn < 16 || bn > 256 || bn % 16 != 0) return BIV_ERR_VALUE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return out_dtype == BIV_F32 ? dispatch_bn<true>(bn, A, B, C, M, N, K, s)
-                                : dispatch_bn<false>(bn, A, B, C, M, N, K, s);
+    return out_dtype == BIV_F32 ? launch_gemm<true>(A, B, C, M, N, K, bn, s)
+                                : launch_gemm<false>(A, B, C, M, N, K, bn, s);
 }
 
 extern "C" int biv_gemm_nosplitk(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K,
                                  biv_stream_t stream) {
     int st = check_gemm(A, B, C, out_dtype, M, N, K);
     if (st != BIV_OK || M == 0) return st;
-    return biv_gemm_nosplitk_bn(A, B, C, out_dtype, M, N, K, biv_gemm_tile_n(N, K), stream);
+    return biv_gemm_nosplitk_bn(A, B, C, out_dtype, M, N, K, biv_gemm_tile_n(M, N, K), stream);
 }

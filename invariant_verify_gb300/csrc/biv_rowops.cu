@@ -25,12 +25,31 @@ int rms_threads(int d) {
     return (t + 31) / 32 * 32;
 }
 
-__global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
-                               __nv_bfloat16* __restrict__ y, int d, float eps) {
+// MODE 0: y = rmsnorm(x).  MODE 1: x_out = bf16(x + r), y = rmsnorm(x_out).
+// MODE 2: x_out = table[tokens[row]], y = rmsnorm(x_out).  The norm always
+// reads the bf16 row it stores, with the same chunking and reduction tree, so
+// the fused modes give the same bits as the separate kernels.
+template <int MODE>
+__global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ r,
+                               const int32_t* __restrict__ tokens, int vocab, const __nv_bfloat16* __restrict__ w,
+                               __nv_bfloat16* __restrict__ x_out, __nv_bfloat16* __restrict__ y, int d, float eps) {
     __shared__ float warp_part[32];
+    pdl_wait();
+    pdl_trigger();
     const long long row = blockIdx.x;
     const int chunks = d / 8;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + row * d);
+    const uint4* xr;
+    if constexpr (MODE == 2) {
+        int tok = tokens[row];
+        if (tok < 0 || tok >= vocab) {
+            if (threadIdx.x == 0) atomicOr(&g_rowops_err, BIV_DEVERR_INDEX);
+            tok = -1;
+        }
+        xr = reinterpret_cast<const uint4*>(x + static_cast<long long>(tok < 0 ? 0 : tok) * d);
+        if (tok < 0) xr = nullptr;
+    } else {
+        xr = reinterpret_cast<const uint4*>(x + row * d);
+    }
     uint4 v[kMaxChunksPerThread];
     float ss = 0.0f;
 #pragma unroll
@@ -38,7 +57,20 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_b
         const int c = threadIdx.x + k * blockDim.x;
         v[k] = make_uint4(0, 0, 0, 0);
         if (c < chunks) {
-            v[k] = xr[c];
+            if constexpr (MODE == 1) {
+                const uint4 a = xr[c];
+                const uint4 b = reinterpret_cast<const uint4*>(r + row * d)[c];
+                const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    o[e] = pack_bf16x2(__fadd_rn(bf16lo(aa[e]), bf16lo(bb[e])), __fadd_rn(bf16hi(aa[e]), bf16hi(bb[e])));
+                v[k] = make_uint4(o[0], o[1], o[2], o[3]);
+            } else if constexpr (MODE == 2) {
+                if (xr) v[k] = xr[c];
+            } else {
+                v[k] = xr[c];
+            }
             const uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -69,6 +101,7 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_b
     for (int k = 0; k < kMaxChunksPerThread; ++k) {
         const int c = threadIdx.x + k * blockDim.x;
         if (c < chunks) {
+            if constexpr (MODE != 0) reinterpret_cast<uint4*>(x_out + row * d)[c] = v[k];
             const uint4 g = wr[c];
             const uint32_t u[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
             const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
@@ -84,6 +117,8 @@ __global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_b
 
 __global__ void embed_kernel(const __nv_bfloat16* __restrict__ table, const int32_t* __restrict__ tokens,
                              __nv_bfloat16* __restrict__ out, int d, int vocab) {
+    pdl_wait();
+    pdl_trigger();
     const long long w = blockIdx.x;
     const int tok = tokens[w];
     uint4* dst = reinterpret_cast<uint4*>(out + w * d);
@@ -97,6 +132,8 @@ BIV_DEV float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
 
 __global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, __nv_bfloat16* __restrict__ out, int rows,
                                 int F) {
+    pdl_wait();
+    pdl_trigger();
     const long long per_row = F / 8;
     const long long total = static_cast<long long>(rows) * per_row;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -116,6 +153,8 @@ __global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, __nv_bfloa
 
 __global__ void residual_add_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ y,
                                     __nv_bfloat16* __restrict__ out, long long n8) {
+    pdl_wait();
+    pdl_trigger();
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         const uint4 a = reinterpret_cast<const uint4*>(x)[i];
@@ -146,10 +185,36 @@ extern "C" int biv_rmsnorm(const void* x, const void* w, void* y, int rows, int 
     if (rows == 0) return BIV_OK;
     if (!x || !w || !y) return BIV_ERR_NULL;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return BIV_ERR_ALIGN;
-    rmsnorm_kernel<<<rows, rms_threads(d), 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y), d,
-        eps);
-    return launch_status();
+    return launch_pdl(rmsnorm_kernel<0>, dim3(rows), dim3(rms_threads(d)), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(nullptr),
+                      static_cast<const int32_t*>(nullptr), 0, static_cast<const __nv_bfloat16*>(w),
+                      static_cast<__nv_bfloat16*>(nullptr), static_cast<__nv_bfloat16*>(y), d, eps);
+}
+
+extern "C" int biv_add_rmsnorm(const void* x, const void* r, const void* w, void* x_out, void* y, int rows, int d,
+                               float eps, biv_stream_t stream) {
+    if (rows < 0 || d < 8 || d % 8 != 0 || d > 8 * 1024 * kMaxChunksPerThread) return BIV_ERR_SHAPE;
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return BIV_ERR_VALUE;
+    if (rows == 0) return BIV_OK;
+    if (!x || !r || !w || !x_out || !y) return BIV_ERR_NULL;
+    if (!aligned16(x) || !aligned16(r) || !aligned16(w) || !aligned16(x_out) || !aligned16(y)) return BIV_ERR_ALIGN;
+    return launch_pdl(rmsnorm_kernel<1>, dim3(rows), dim3(rms_threads(d)), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(r),
+                      static_cast<const int32_t*>(nullptr), 0, static_cast<const __nv_bfloat16*>(w),
+                      static_cast<__nv_bfloat16*>(x_out), static_cast<__nv_bfloat16*>(y), d, eps);
+}
+
+extern "C" int biv_embed_rmsnorm(const void* table, const int32_t* tokens, const void* w, void* x_out, void* y,
+                                 int W, int d, int vocab, float eps, biv_stream_t stream) {
+    if (W < 0 || d < 8 || d % 8 != 0 || d > 8 * 1024 * kMaxChunksPerThread || vocab <= 0) return BIV_ERR_SHAPE;
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return BIV_ERR_VALUE;
+    if (W == 0) return BIV_OK;
+    if (!table || !tokens || !w || !x_out || !y) return BIV_ERR_NULL;
+    if (!aligned16(table) || !aligned16(w) || !aligned16(x_out) || !aligned16(y)) return BIV_ERR_ALIGN;
+    return launch_pdl(rmsnorm_kernel<2>, dim3(W), dim3(rms_threads(d)), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<const __nv_bfloat16*>(table), static_cast<const __nv_bfloat16*>(nullptr), tokens,
+                      vocab, static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(x_out),
+                      static_cast<__nv_bfloat16*>(y), d, eps);
 }
 
 extern "C" int biv_embed(const void* table, const int32_t* tokens, void* out, int W, int d, int vocab,
@@ -158,9 +223,8 @@ extern "C" int biv_embed(const void* table, const int32_t* tokens, void* out, in
     if (W == 0) return BIV_OK;
     if (!table || !tokens || !out) return BIV_ERR_NULL;
     if (!aligned16(table) || !aligned16(out)) return BIV_ERR_ALIGN;
-    embed_kernel<<<W, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(table), tokens, static_cast<__nv_bfloat16*>(out), d, vocab);
-    return launch_status();
+    return launch_pdl(embed_kernel, dim3(W), dim3(128), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<const __nv_bfloat16*>(table), tokens, static_cast<__nv_bfloat16*>(out), d, vocab);
 }
 
 extern "C" int biv_silu_mul(const void* gu, void* out, int rows, int F, biv_stream_t stream) {
@@ -169,9 +233,8 @@ extern "C" int biv_silu_mul(const void* gu, void* out, int rows, int F, biv_stre
     if (!gu || !out) return BIV_ERR_NULL;
     if (!aligned16(gu) || !aligned16(out)) return BIV_ERR_ALIGN;
     const long long work = static_cast<long long>(rows) * (F / 8);
-    silu_mul_kernel<<<grid_for(work, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(gu), static_cast<__nv_bfloat16*>(out), rows, F);
-    return launch_status();
+    return launch_pdl(silu_mul_kernel, dim3(grid_for(work, 256)), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<const __nv_bfloat16*>(gu), static_cast<__nv_bfloat16*>(out), rows, F);
 }
 
 extern "C" int biv_residual_add(const void* x, const void* y, void* out, long long n, biv_stream_t stream) {
@@ -179,8 +242,7 @@ extern "C" int biv_residual_add(const void* x, const void* y, void* out, long lo
     if (n == 0) return BIV_OK;
     if (!x || !y || !out) return BIV_ERR_NULL;
     if (!aligned16(x) || !aligned16(y) || !aligned16(out)) return BIV_ERR_ALIGN;
-    residual_add_kernel<<<grid_for(n / 8, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(out),
-        n / 8);
-    return launch_status();
+    return launch_pdl(residual_add_kernel, dim3(grid_for(n / 8, 256)), dim3(256), 0,
+                      reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(x),
+                      static_cast<const __nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(out), n / 8);
 }

@@ -173,6 +173,8 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
     __shared__ unsigned long long published[2];    // [0] slice-max key, [1] slice winner
     __shared__ int abort_flag;
 
+    pdl_wait();
+    pdl_trigger();
     const uint32_t rank = cluster_rank();
     const long long row = blockIdx.x / kClusterSize;
     const int begin = static_cast<int>(rank) * slice;
@@ -295,6 +297,8 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
 
 __global__ void gumbel_noise_kernel(uint32_t seed_lo, uint32_t seed_hi, const uint32_t* __restrict__ row_req,
                                     const int32_t* __restrict__ row_pos, int V, float* __restrict__ g) {
+    pdl_wait();
+    pdl_trigger();
     const long long row = blockIdx.y;
     const uint32_t req = row_req[row];
     const uint32_t pos = static_cast<uint32_t>(row_pos[row]) + 1u;
@@ -306,6 +310,8 @@ __global__ void gumbel_noise_kernel(uint32_t seed_lo, uint32_t seed_hi, const ui
 }
 
 __global__ void gumbel_words_kernel(const uint32_t* __restrict__ words, long long n, float* __restrict__ g) {
+    pdl_wait();
+    pdl_trigger();
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<long long>(gridDim.x) * blockDim.x)
         g[i] = gumbel_from_word(words[i]);
@@ -315,6 +321,8 @@ __global__ void gumbel_words_kernel(const uint32_t* __restrict__ words, long lon
 __global__ void verify_accept_kernel(const int32_t* __restrict__ target, const int32_t* __restrict__ draft,
                                      const int32_t* __restrict__ p0, int N, int K,
                                      int32_t* __restrict__ accept_len, int32_t* __restrict__ new_len) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= N) return;
     int L = K;
@@ -365,13 +373,15 @@ extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld
     cfg.blockDim = dim3(kSelThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kClusterSize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, gumbel_argmax_kernel, logits, V, ld, slice, row_req, row_pos,
                                        static_cast<uint32_t>(seed & 0xffffffffull),
                                        static_cast<uint32_t>(seed >> 32), invT, greedy, tokens);
@@ -385,9 +395,9 @@ extern "C" int biv_gumbel_noise(uint64_t seed, const uint32_t* row_req, const in
     if (R == 0 || V == 0) return BIV_OK;
     if (!row_req || !row_pos || !g) return BIV_ERR_NULL;
     const int blocks = std::min((V + 255) / 256, 1024);
-    gumbel_noise_kernel<<<dim3(blocks, R), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint32_t>(seed & 0xffffffffull), static_cast<uint32_t>(seed >> 32), row_req, row_pos, V, g);
-    return launch_status();
+    return launch_pdl(gumbel_noise_kernel, dim3(blocks, R), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<uint32_t>(seed & 0xffffffffull), static_cast<uint32_t>(seed >> 32), row_req,
+                      row_pos, V, g);
 }
 
 extern "C" int biv_gumbel_from_words(const uint32_t* words, long long n, float* g, biv_stream_t stream) {
@@ -395,9 +405,8 @@ extern "C" int biv_gumbel_from_words(const uint32_t* words, long long n, float* 
     if (n == 0) return BIV_OK;
     if (!words || !g) return BIV_ERR_NULL;
     const long long blocks = std::min<long long>((n + 255) / 256, 4096);
-    gumbel_words_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(words, n,
-                                                                                                          g);
-    return launch_status();
+    return launch_pdl(gumbel_words_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                      reinterpret_cast<cudaStream_t>(stream), words, n, g);
 }
 
 extern "C" int biv_verify_accept(const int32_t* target, const int32_t* draft, const int32_t* p0, int N, int K,
@@ -405,7 +414,6 @@ extern "C" int biv_verify_accept(const int32_t* target, const int32_t* draft, co
     if (N < 0 || K < 1) return BIV_ERR_SHAPE;
     if (N == 0) return BIV_OK;
     if (!target || !draft || !p0 || !accept_len || !new_len) return BIV_ERR_NULL;
-    verify_accept_kernel<<<(N + 127) / 128, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(target, draft, p0, N,
-                                                                                              K, accept_len, new_len);
-    return launch_status();
+    return launch_pdl(verify_accept_kernel, dim3((N + 127) / 128), dim3(128), 0, reinterpret_cast<cudaStream_t>(stream),
+                      target, draft, p0, N, K, accept_len, new_len);
 }

@@ -66,7 +66,8 @@ class DecoderVerifier:
         self.new_len = torch.empty(N, device=dev, dtype=torch.int32)
         ws = B.biv_decode_attn_workspace_size(W, Hq, max_len)
         self.workspace = torch.empty(max(ws, 16), device=dev, dtype=torch.uint8)
-        self.launches_per_step = 5 + cfg.layers * 13
+        # embed+norm, per layer 11 kernels (attention is two), LM head, select, accept
+        self.launches_per_step = 4 + cfg.layers * 11
 
     # -------------------------------------------------------------- stages
     def forward(self, win: Window, trace: dict | None = None) -> None:
@@ -83,10 +84,9 @@ class DecoderVerifier:
             if trace is not None:
                 trace[name] = t.clone()
 
-        B.biv_embed(w["embed"], win.tokens, self.x)
+        B.biv_embed_rmsnorm(w["embed"], win.tokens, w["l0.attn_norm"], self.x, self.h, c.eps)
         snap("x_in", self.x)
         for l in range(c.layers):
-            B.biv_rmsnorm(self.x, w[f"l{l}.attn_norm"], self.h, c.eps)
             snap(f"l{l}.h_attn", self.h)
             B.biv_gemm_nosplitk(self.h, w[f"l{l}.wqkv"], self.qkv)
             snap(f"l{l}.qkv", self.qkv)
@@ -102,9 +102,8 @@ class DecoderVerifier:
             snap(f"l{l}.o", self.o)
             B.biv_gemm_nosplitk(self.o.view(self.W, Hq * hd), w[f"l{l}.wo"], self.proj)
             snap(f"l{l}.attn_proj", self.proj)
-            B.biv_residual_add(self.x, self.proj, self.x)
+            B.biv_add_rmsnorm(self.x, self.proj, w[f"l{l}.ffn_norm"], self.x, self.h, c.eps)
             snap(f"l{l}.x_mid", self.x)
-            B.biv_rmsnorm(self.x, w[f"l{l}.ffn_norm"], self.h, c.eps)
             snap(f"l{l}.h_ffn", self.h)
             B.biv_gemm_nosplitk(self.h, w[f"l{l}.wgu"], self.gu)
             snap(f"l{l}.gu", self.gu)
@@ -112,9 +111,10 @@ class DecoderVerifier:
             snap(f"l{l}.act", self.act)
             B.biv_gemm_nosplitk(self.act, w[f"l{l}.wdown"], self.proj)
             snap(f"l{l}.down", self.proj)
-            B.biv_residual_add(self.x, self.proj, self.x)
+            last = l + 1 == c.layers
+            gain = w["final_norm"] if last else w[f"l{l + 1}.attn_norm"]
+            B.biv_add_rmsnorm(self.x, self.proj, gain, self.x, self.hidden if last else self.h, c.eps)
             snap(f"l{l}.x_out", self.x)
-        B.biv_rmsnorm(self.x, w["final_norm"], self.hidden, c.eps)
         snap("hidden", self.hidden)
 
     def lm_head(self) -> None:

@@ -54,6 +54,14 @@ def test_rmsnorm_validation(lib):
     assert f(None, None, None, 4, 1024, float("nan"), None) == VALUE
     assert f(None, None, None, 4, 1024, 1e-6, None) == NULL
     assert f(MISALIGNED, FAKE, FAKE, 4, 1024, 1e-6, None) == ALIGN
+    a = lib.biv_add_rmsnorm
+    assert a(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1020, 1e-6, None) == SHAPE
+    assert a(FAKE, None, FAKE, FAKE, FAKE, 4, 1024, 1e-6, None) == NULL
+    assert a(FAKE, FAKE, FAKE, MISALIGNED, FAKE, 4, 1024, 1e-6, None) == ALIGN
+    assert a(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1024, 1e-6, None) == OK
+    e = lib.biv_embed_rmsnorm
+    assert e(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1024, 0, 1e-6, None) == SHAPE
+    assert e(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1024, 10, 0.0, None) == VALUE
 
 
 def test_gemm_validation(lib):
@@ -65,18 +73,25 @@ def test_gemm_validation(lib):
     assert f(None, None, None, 7, 4, 64, 64, None) == VALUE
     assert f(None, None, None, 0, 4, 64, 64, None) == NULL
     assert f(FAKE, MISALIGNED, FAKE, 1, 4, 64, 64, None) == ALIGN
-    assert lib.biv_gemm_nosplitk_bn(FAKE, FAKE, FAKE, 0, 4, 64, 64, 48, None) == VALUE
+    assert lib.biv_gemm_nosplitk_bn(FAKE, FAKE, FAKE, 0, 4, 64, 64, 40, None) == VALUE
+    assert lib.biv_gemm_nosplitk_bn(FAKE, FAKE, FAKE, 0, 4, 64, 64, 272, None) == VALUE
 
 
-def test_gemm_tile_width_depends_on_n_only(lib):
-    seen = {}
-    for N, K in [(2048, 256), (1536, 1024), (1024, 2816), (5632, 1024), (32000, 1024),
-                 (4096, 14336), (6144, 4096), (28672, 4096), (128256, 4096)]:
-        bn = lib.biv_gemm_tile_n(N, K)
-        assert bn in (16, 32, 64, 128, 256)
-        assert lib.biv_gemm_tile_n(N, 64) == bn          # K does not change it
-        seen[N] = bn
-    assert seen[128256] == 256 and seen[32000] == 128 and seen[1024] == 16
+def test_gemm_tile_width_rule(lib):
+    for M in (1, 8, 64, 128):                       # one row tile: one wave of N tiles
+        assert lib.biv_gemm_tile_n(M, 1024, 1024) == 16
+        assert lib.biv_gemm_tile_n(M, 1536, 1024) == 16
+        assert lib.biv_gemm_tile_n(M, 5632, 1024) == 48
+        assert lib.biv_gemm_tile_n(M, 32000, 1024) == 224    # 143 tiles
+        assert lib.biv_gemm_tile_n(M, 128256, 4096) == 224   # 573 tiles, 4 nearly full waves
+    for M, N in ((1024, 4096), (256, 6144), (1024, 128256), (300, 1000)):
+        bn = lib.biv_gemm_tile_n(M, N, 4096)
+        assert 64 <= bn <= 256 and bn % 16 == 0
+    assert lib.biv_gemm_tile_n(1024, 4096, 4096) == 224      # 8 x 19 = 152 tiles
+    for M in (1, 1000):
+        for N in (8, 24, 4096, 152064):
+            bn = lib.biv_gemm_tile_n(M, N, 64)
+            assert 16 <= bn <= 256 and bn % 16 == 0
 
 
 def test_attention_validation_and_workspace(lib):

@@ -55,6 +55,32 @@ def test_rmsnorm_row_invariance_and_alias():
     B.biv_rmsnorm(x[:0], w, full[:0], 1e-6)   # empty
 
 
+def test_fused_norms_equal_separate_kernels():
+    g = synth.generator(17)
+    for rows, d in ((64, 1024), (3, 4096), (16, 256)):
+        x = dev(synth.bf16_normal((rows, d), 1.0, g))
+        r = dev(synth.bf16_normal((rows, d), 0.3, g))
+        w = dev(synth.bf16_normal((d,), 1.0, g))
+        s_sum = torch.empty_like(x)
+        s_norm = torch.empty_like(x)
+        B.biv_residual_add(x, r, s_sum)
+        B.biv_rmsnorm(s_sum, w, s_norm, 1e-6)
+        f_sum = x.clone()
+        f_norm = torch.empty_like(x)
+        B.biv_add_rmsnorm(f_sum, r, w, f_sum, f_norm, 1e-6)      # x_out aliases x
+        assert same_bits(f_sum, s_sum) and same_bits(f_norm, s_norm)
+        table = dev(synth.bf16_normal((97, d), 1.0, g))
+        tok = i32(np.arange(rows) * 7 % 97)
+        e = torch.empty(rows, d, dtype=torch.bfloat16, device="cuda")
+        en = torch.empty_like(e)
+        B.biv_embed(table, tok, e)
+        B.biv_rmsnorm(e, w, en, 1e-6)
+        fe = torch.empty_like(e)
+        fen = torch.empty_like(e)
+        B.biv_embed_rmsnorm(table, tok, w, fe, fen, 1e-6)
+        assert same_bits(fe, e) and same_bits(fen, en)
+
+
 # --------------------------------------------------------------------- GEMM
 GEMM_SHAPES = [
     (1, 64, 64, torch.bfloat16, None),
