@@ -197,6 +197,16 @@ int biv_kv_overwrite(void* k_cache, void* v_cache, const void* k_new, long long 
                      const int32_t* row_pos, const int32_t* rows_keep, int W, int K, int Hkv, int hd,
                      int n_slots, int max_len, biv_stream_t stream);
 
+/* RoPE and KV overwrite in one pass: q heads of qkv (bf16 [W, (Hq + 2 Hkv) hd])
+ * are rotated into q_out (bf16 [W, Hq, hd]); k heads are rotated and written,
+ * with the v heads, into the caches at (row_slot[w], row_pos[w]).  Bitwise the
+ * same as biv_rope_qk followed by biv_kv_overwrite (same rows_keep rule).
+ * Requires hd % 8 == 0, hd <= 256, theta > 1, W % K == 0, aligned pointers. */
+int biv_rope_kv_write(const void* qkv, void* q_out, void* k_cache, void* v_cache,
+                      const int32_t* row_slot, const int32_t* row_pos, const int32_t* rows_keep, int W,
+                      int K, int Hq, int Hkv, int hd, int n_slots, int max_len, float theta,
+                      biv_stream_t stream);
+
 /* ----------------------------------------------------- Gumbel-max select
  * [COUPLING]: adding Gumbel(0,1) noise to the logits and taking the argmax
  * samples from softmax(logits / T) without computing a softmax; the noise does
@@ -226,6 +236,11 @@ int biv_gumbel_noise(uint64_t seed, const uint32_t* row_req, const int32_t* row_
 
 /* g = -L(-L(u(w))) for raw 32-bit words w[0..n); for tests of L.           */
 int biv_gumbel_from_words(const uint32_t* words, long long n, float* g, biv_stream_t stream);
+
+/* The 256 per-bucket noise bounds biv_gumbel_argmax prunes with (host memory,
+ * float[256]): every noise value whose word has top byte b is <= bounds[b].
+ * For tests of the pruning bound.                                         */
+int biv_gumbel_bucket_bounds(float* bounds_out);
 
 /* ----------------------------------------------------- coupled accept
  * [COUPLING] + [GUIDE] + [DVR] para 3: with shared noise the check compares
@@ -265,7 +280,21 @@ int biv_rope_qk(const void* qkv, void* q_out, void* k_out, const int32_t* row_po
                 int Hkv, int hd, float theta, biv_stream_t stream);
 
 /* out[r][i] = bf16(silu(gu[r][i]) * gu[r][F + i]) ; gu bf16 [rows, 2F], F % 8 == 0. */
+
 int biv_silu_mul(const void* gu, void* out, int rows, int F, biv_stream_t stream);
+
+/* Gate/up GEMM with SwiGLU in the epilogue: act[m][i] = bf16(silu(bf16(g)) *
+ * bf16(u)) with g = A[m]·Wg[i], u = A[m]·Wu[i]; bitwise the same as
+ * biv_gemm_nosplitk (bf16 out) on the stacked weight followed by
+ * biv_silu_mul.  B_packed is the [2F, K] weight rearranged by
+ * biv_swiglu_pack_weights; act bf16 [M, F].  F % 16 == 0, K % 8 == 0.      */
+int biv_gemm_swiglu(const void* A, const void* B_packed, void* act, int M, int F, int K,
+                    biv_stream_t stream);
+
+/* Rearrange a stacked gate/up weight ([2F, K], the F gate rows first) into the
+ * layout biv_gemm_swiglu reads: blocks of 32 rows, 16 gate rows then the same
+ * 16 up rows.  w_packed must not overlap w_gu.                             */
+int biv_swiglu_pack_weights(const void* w_gu, void* w_packed, int F, int K, biv_stream_t stream);
 
 /* out[i] = bf16(x[i] + y[i]) over n bf16 elements, n % 8 == 0; out may alias x. */
 int biv_residual_add(const void* x, const void* y, void* out, long long n, biv_stream_t stream);

@@ -52,11 +52,15 @@ SIGNATURES = {
     "biv_gumbel_noise": (_I, [_U64, _P, _P, _I, _I, _P, _P]),
     "biv_gumbel_from_words": (_I, [_P, _LL, _P, _P]),
     "biv_verify_accept": (_I, [_P, _P, _P, _I, _I, _P, _P, _P]),
+    "biv_gumbel_bucket_bounds": (_I, [_P]),
     "biv_embed": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "biv_add_rmsnorm": (_I, [_P, _P, _P, _P, _P, _I, _I, _F, _P]),
     "biv_embed_rmsnorm": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P]),
     "biv_rope_qk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _P]),
     "biv_silu_mul": (_I, [_P, _P, _I, _I, _P]),
+    "biv_gemm_swiglu": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "biv_swiglu_pack_weights": (_I, [_P, _P, _I, _I, _P]),
+    "biv_rope_kv_write": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "biv_residual_add": (_I, [_P, _P, _P, _LL, _P]),
 }
 
@@ -195,6 +199,13 @@ def biv_gumbel_from_words(words, g, stream=None) -> None:
         _ptr(words), words.numel(), _ptr(g), _stream(stream)))
 
 
+def biv_gumbel_bucket_bounds():
+    import numpy as np
+    out = np.empty(256, np.float32)
+    _check("biv_gumbel_bucket_bounds", _load().biv_gumbel_bucket_bounds(out.ctypes.data_as(C.c_void_p)))
+    return out
+
+
 def biv_verify_accept(target, draft, p0, N: int, K: int, accept_len, new_len, stream=None) -> None:
     _check("biv_verify_accept", _load().biv_verify_accept(
         _ptr(target), _ptr(draft), _ptr(p0), N, K, _ptr(accept_len), _ptr(new_len), _stream(stream)))
@@ -227,6 +238,28 @@ def biv_rope_qk(qkv, q_out, k_out, row_pos, Hq: int, Hkv: int, hd: int, theta: f
 def biv_silu_mul(gu, out, stream=None) -> None:
     rows, two_f = gu.shape
     _check("biv_silu_mul", _load().biv_silu_mul(_ptr(gu), _ptr(out), rows, two_f // 2, _stream(stream)))
+
+
+def biv_gemm_swiglu(A, B_packed, act, stream=None) -> None:
+    M, K = A.shape
+    F = act.shape[1]
+    _check("biv_gemm_swiglu", _load().biv_gemm_swiglu(_ptr(A), _ptr(B_packed), _ptr(act), M, F, K,
+                                                      _stream(stream)))
+
+
+def biv_swiglu_pack_weights(w_gu, w_packed, stream=None) -> None:
+    two_f, K = w_gu.shape
+    _check("biv_swiglu_pack_weights", _load().biv_swiglu_pack_weights(_ptr(w_gu), _ptr(w_packed), two_f // 2, K,
+                                                                      _stream(stream)))
+
+
+def biv_rope_kv_write(qkv, q_out, k_cache, v_cache, row_slot, row_pos, Hq: int, theta: float, K: int,
+                      rows_keep=None, stream=None) -> None:
+    n_slots, Hkv, max_len, hd = k_cache.shape
+    W = qkv.shape[0]
+    _check("biv_rope_kv_write", _load().biv_rope_kv_write(
+        _ptr(qkv), _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(row_slot), _ptr(row_pos), _ptr(rows_keep),
+        W, K, Hq, Hkv, hd, n_slots, max_len, float(theta), _stream(stream)))
 
 
 def biv_residual_add(x, y, out, stream=None) -> None:

@@ -368,6 +368,19 @@ attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
 }
 
 // ------------------------------------------------------------------ RoPE
+// Rotate the pair (a, b) = (x[i], x[i + hd/2]) of one head by pos * theta^(-2i/hd);
+// one definition for the RoPE kernel and the fused RoPE + KV-write kernel.
+BIV_DEV void rope_rotate(float a, float b, int pos, int i, int hd, float theta, __nv_bfloat16* o1,
+                         __nv_bfloat16* o2) {
+    const float inv_freq = powf(theta, -2.0f * static_cast<float>(i) / static_cast<float>(hd));
+    const float ang = static_cast<float>(pos) * inv_freq;
+    float sn, cs;
+    sincosf(ang, &sn, &cs);
+    // explicit roundings: no fma contraction, the same bits in every caller
+    *o1 = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)));
+    *o2 = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, cs), __fmul_rn(a, sn)));
+}
+
 __global__ void rope_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __restrict__ q_out,
                             __nv_bfloat16* __restrict__ k_out, const int32_t* __restrict__ row_pos, int W,
                             int Hq, int Hkv, int hd, float theta) {
@@ -382,15 +395,50 @@ __global__ void rope_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16
         const int h = static_cast<int>(rh % (Hq + Hkv));
         const int w = static_cast<int>(rh / (Hq + Hkv));
         const __nv_bfloat16* src = qkv + (static_cast<long long>(w) * (Hq + 2 * Hkv) + h) * hd;
-        const float inv_freq = powf(theta, -2.0f * static_cast<float>(i) / static_cast<float>(hd));
-        const float ang = static_cast<float>(row_pos[w]) * inv_freq;
-        float sn, cs;
-        sincosf(ang, &sn, &cs);
-        const float a = __bfloat162float(src[i]), b = __bfloat162float(src[i + half]);
         __nv_bfloat16* dst = h < Hq ? q_out + (static_cast<long long>(w) * Hq + h) * hd
                                     : k_out + (static_cast<long long>(w) * Hkv + (h - Hq)) * hd;
-        dst[i] = __float2bfloat16_rn(a * cs - b * sn);
-        dst[i + half] = __float2bfloat16_rn(b * cs + a * sn);
+        rope_rotate(__bfloat162float(src[i]), __bfloat162float(src[i + half]), row_pos[w], i, hd, theta, dst + i,
+                    dst + i + half);
+    }
+}
+
+// RoPE on q and k of one row, with the rotated k and the v of the row written
+// straight into the caches at (row_slot, row_pos) -- the verifier's KV
+// overwrite in the same pass.  One CTA per row.
+__global__ void rope_kv_write_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __restrict__ q_out,
+                                     __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc,
+                                     const int32_t* __restrict__ row_slot, const int32_t* __restrict__ row_pos,
+                                     const int32_t* __restrict__ rows_keep, int K, int Hq, int Hkv, int hd,
+                                     int n_slots, int max_len, float theta) {
+    pdl_wait();
+    pdl_trigger();
+    const int w = blockIdx.x;
+    const int half = hd / 2;
+    const int pos = row_pos[w], slot = row_slot[w];
+    const __nv_bfloat16* src = qkv + static_cast<long long>(w) * (Hq + 2 * Hkv) * hd;
+    const bool keep = !rows_keep || (w % K) < rows_keep[w / K];
+    const bool cache_ok = slot >= 0 && slot < n_slots && pos >= 0 && pos < max_len;
+    if (keep && !cache_ok && threadIdx.x == 0) atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
+    const bool write_kv = keep && cache_ok;
+    for (int idx = threadIdx.x; idx < (Hq + Hkv) * half; idx += blockDim.x) {
+        const int h = idx / half, i = idx - h * half;
+        const __nv_bfloat16* x = src + static_cast<long long>(h) * hd;
+        __nv_bfloat16* dst;
+        if (h < Hq) {
+            dst = q_out + (static_cast<long long>(w) * Hq + h) * hd;
+        } else {
+            if (!write_kv) continue;
+            dst = kc + ((static_cast<long long>(slot) * Hkv + (h - Hq)) * max_len + pos) * hd;
+        }
+        rope_rotate(__bfloat162float(x[i]), __bfloat162float(x[i + half]), pos, i, hd, theta, dst + i, dst + i + half);
+    }
+    if (write_kv) {
+        const int chunks = Hkv * hd / 8;
+        for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+            const int h = c / (hd / 8), e = (c % (hd / 8)) * 8;
+            *reinterpret_cast<uint4*>(vc + ((static_cast<long long>(slot) * Hkv + h) * max_len + pos) * hd + e) =
+                *reinterpret_cast<const uint4*>(src + static_cast<long long>(Hq + Hkv + h) * hd + e);
+        }
     }
 }
 
@@ -511,6 +559,24 @@ extern "C" int biv_rope_qk(const void* qkv, void* q_out, void* k_out, const int3
     return launch_pdl(rope_kernel, dim3(blocks), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
                       static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(q_out),
                       static_cast<__nv_bfloat16*>(k_out), row_pos, W, Hq, Hkv, hd, theta);
+}
+
+extern "C" int biv_rope_kv_write(const void* qkv, void* q_out, void* k_cache, void* v_cache,
+                                 const int32_t* row_slot, const int32_t* row_pos, const int32_t* rows_keep, int W,
+                                 int K, int Hq, int Hkv, int hd, int n_slots, int max_len, float theta,
+                                 biv_stream_t stream) {
+    if (W < 0 || K < 1 || Hq <= 0 || Hkv <= 0 || hd <= 0 || hd % 8 != 0 || hd > 256 || n_slots <= 0 ||
+        max_len <= 0)
+        return BIV_ERR_SHAPE;
+    if (W % K != 0) return BIV_ERR_SHAPE;
+    if (!(theta > 1.0f) || !std::isfinite(theta)) return BIV_ERR_VALUE;
+    if (W == 0) return BIV_OK;
+    if (!qkv || !q_out || !k_cache || !v_cache || !row_slot || !row_pos) return BIV_ERR_NULL;
+    if (!aligned16(qkv) || !aligned16(q_out) || !aligned16(k_cache) || !aligned16(v_cache)) return BIV_ERR_ALIGN;
+    return launch_pdl(rope_kv_write_kernel, dim3(W), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<const __nv_bfloat16*>(qkv), static_cast<__nv_bfloat16*>(q_out),
+                      static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), row_slot, row_pos,
+                      rows_keep, K, Hq, Hkv, hd, n_slots, max_len, theta);
 }
 
 extern "C" int biv_kv_overwrite(void* k_cache, void* v_cache, const void* k_new, long long k_stride,

@@ -120,16 +120,39 @@ BIV_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of a phase: never suspends the thread.
+BIV_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete, for at most
-// kWaitLimitNs.  On time-out: raise BIV_DEVERR_TIMEOUT in *err, set the CTA's
-// abort flag (shared memory) and return false.  Also returns false as soon as
-// another thread of the CTA has aborted.
-BIV_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+// about kWaitLimitNs.  The first kFastPolls polls touch nothing but the
+// barrier (reading the global timer is slow); only a wait that outlasts them
+// starts the clock.  On time-out: raise BIV_DEVERR_TIMEOUT in *err, set the
+// CTA's abort flag (shared memory) and return false.  Also returns false as
+// soon as another thread of the CTA has aborted.
+constexpr int kFastPolls = 4096;
+
+// spin = true polls with test_wait (no suspension: the single producer / MMA
+// threads of a pipeline react at once); spin = false uses try_wait, which may
+// park the thread until the phase completes (for warps that wait long).
+BIV_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned int* err,
+                       bool spin = false) {
+#pragma unroll 1
+    for (int i = 0; i < kFastPolls; ++i)
+        if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 256; ++i)
+            if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -156,6 +179,16 @@ BIV_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, 
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(cache_policy)
+        : "memory");
+}
+
+// 3-D tiled TMA load (coordinates innermost first), completion on `bar`.
+BIV_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                         uint64_t cache_policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(cache_policy)
         : "memory");
 }
 
@@ -258,5 +291,14 @@ BIV_DEV uint32_t pack_bf16x2(float lo, float hi) {
 
 BIV_DEV float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 BIV_DEV float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// SiLU(g) = g / (1 + e^-g), one definition for every kernel that applies it
+// (the SwiGLU kernel and the gate/up GEMM epilogue give the same bits).
+BIV_DEV float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+
+// bf16(silu(g) * u) of two bf16 values packed as (lo, hi) pairs.
+BIV_DEV uint32_t swiglu_pack(uint32_t g2, uint32_t u2) {
+    return pack_bf16x2(__fmul_rn(silu(bf16lo(g2)), bf16lo(u2)), __fmul_rn(silu(bf16hi(g2)), bf16hi(u2)));
+}
 
 }  // namespace biv

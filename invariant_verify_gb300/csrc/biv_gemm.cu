@@ -12,17 +12,22 @@
 // N = 16..256), so the tile width is free to follow the problem size.
 //
 // Kernel layout (192 threads, one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer: A tile [a_rows x 64] and B tile [BN x 64] per
-//               stage, 128-byte swizzle, mbarrier transaction counts.  For
-//               M <= 128 only the real rows of A are copied (a_rows =
-//               M rounded up to 8); the rest of each A stage is zeroed once.
+//   warp 0      TMA producer: per stage one box of A [a_rows x KS*64] and one of
+//               B [BN x KS*64] (3-D tensor maps: KS k-blocks of 64 per box; the
+//               TMA unit spends a fixed ~275 ns per box whatever its size, so
+//               weight-streaming tiles take as many k-blocks per box as two
+//               stages allow), 128-byte swizzle, mbarrier transaction counts.  For M <= 128 only the real rows of A are
+//               copied (a_rows = M rounded up to 8) and packed back to back;
+//               the MMA still reads 128 rows per k-block, and the rows past
+//               a_rows hold unrelated data -- harmless, because each row of the
+//               product depends only on its own row of A and rows >= M are
+//               never stored.
 //   warp 1      TMEM allocator + single-thread MMA issuer; commits free smem
 //               stages and publish finished accumulators.
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 16 columns, convert, store.
 // Two accumulators in TMEM let the epilogue of tile i overlap the MMAs of
-// tile i + 1.  Up to 24 stages keep a whole small weight slice in flight.
-// Launched with programmatic dependent launch: barrier set-up, TMEM
-// allocation and the zero fill overlap the previous kernel.  Every wait is
+// tile i + 1.  Launched with programmatic dependent launch: barrier set-up
+// and TMEM allocation overlap the previous kernel.  Every wait is
 // bounded (2 s); on time-out the kernel raises BIV_DEVERR_TIMEOUT, drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 #include <algorithm>
@@ -36,8 +41,9 @@ BIV_DEFINE_ERR_WORD(g_gemm_err)
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;                       // 64 bf16 = one 128-byte swizzle row
-constexpr int kABytes = kBM * kBK * 2;        // full A stage (16 KiB)
-constexpr int kRingBudget = 200 * 1024;       // bytes of pipeline stages per CTA
+constexpr int kRowBytes = kBK * 2;            // one 64-wide k-block row: 128 B
+constexpr int kRingBudget = 208 * 1024;       // bytes of pipeline stages per CTA
+constexpr int kTailSlack = kBM * kRowBytes;   // the MMA may read 128 A rows past the last stage
 constexpr int kMaxStages = 24;
 constexpr int kBarBytes = 512;
 constexpr int kWave = 152;                    // CTAs of one wave on a 152-SM part
@@ -45,25 +51,31 @@ constexpr int kWave = 152;                    // CTAs of one wave on a 152-SM pa
 struct GemmArgs {
     int M, N, K;
     int BN;          // tile width (multiple of 16, 16..256)
+    int KS;          // 64-wide k-blocks per stage (one TMA box each for A and B)
+    int KB;          // k-blocks in K
+    int three_d;     // 3-D tensor maps (K % 64 == 0), else 2-D with KS = 1
     int stages;      // ring depth
-    int a_rows;      // rows of A copied per stage (multiple of 8, <= 128)
+    int a_rows;      // rows of A copied per k-block (multiple of 8, <= 128)
     uint32_t idesc;  // tcgen05 instruction descriptor for M=128, N=BN
     uint32_t tmem_cols;
 };
 
-inline int stage_bytes(int BN) { return kABytes + BN * kBK * 2; }
+inline int stage_bytes(int KS, int a_rows, int BN) { return KS * (a_rows + BN) * kRowBytes; }
 
-template <bool OUT_F32>
+// EPI: 0 = bf16 C, 1 = fp32 C, 2 = SwiGLU of gate/up-interleaved B (bf16
+// activation [M, N/2]; see biv_gemm_swiglu).
+template <int EPI>
 __global__ void __launch_bounds__(192, 1)
 gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      void* __restrict__ C, const GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    const int STAGE = kABytes + g.BN * kBK * 2;
+    const int A_BYTES = g.KS * g.a_rows * kRowBytes;     // A region of a stage
+    const int STAGE = A_BYTES + g.KS * g.BN * kRowBytes;
     const int S = g.stages;
     uint8_t* tiles = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE + (g.a_rows < kBM ? kTailSlack : 0));
     uint64_t* empty = full + kMaxStages;
     uint64_t* tfull = empty + kMaxStages;     // [2]
     uint64_t* tempty = tfull + 2;             // [2]
@@ -77,8 +89,10 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const int m_tiles = (M + kBM - 1) / kBM;
     const int n_tiles = (N + BN - 1) / BN;
     const int n_work = m_tiles * n_tiles;
-    const int KB = (g.K + kBK - 1) / kBK;
-    const uint32_t tx_bytes = static_cast<uint32_t>(g.a_rows * kBK * 2 + BN * kBK * 2);
+    const int KB = g.KB;
+    const int KS = g.KS;
+    const int n_stage_blocks = (KB + KS - 1) / KS;        // stages per tile
+    const uint32_t tx_bytes = static_cast<uint32_t>(STAGE);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -101,16 +115,6 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         tmem_alloc(tmem_slot, g.tmem_cols);
         tmem_relinquish();
     }
-    // Rows of A that TMA does not write stay zero for the whole kernel.
-    if (g.a_rows < kBM) {
-        const int zero_off = g.a_rows * kBK * 2;
-        const int chunks = (kABytes - zero_off) / 16;
-        for (int s = 0; s < S; ++s) {
-            uint4* z = reinterpret_cast<uint4*>(tiles + s * STAGE + zero_off);
-            for (int i = threadIdx.x; i < chunks; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -130,15 +134,20 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             for (int t = blockIdx.x; t < n_work && ok; t += gridDim.x) {
                 const int n_blk = t / m_tiles;
                 const int m_blk = t - n_blk * m_tiles;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_gemm_err)) {
+                for (int sb = 0; sb < n_stage_blocks; ++sb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_gemm_err, true)) {
                         ok = false;
                         break;
                     }
                     uint8_t* sa = tiles + stage * STAGE;
                     mbar_arrive_expect_tx(&full[stage], tx_bytes);
-                    tma_load_2d(sa, &tmA, &full[stage], kb * kBK, m_blk * kBM, pol_a);
-                    tma_load_2d(sa + kABytes, &tmB, &full[stage], kb * kBK, n_blk * BN, pol_b);
+                    if (g.three_d) {
+                        tma_load_3d(sa, &tmA, &full[stage], 0, m_blk * kBM, sb * KS, pol_a);
+                        tma_load_3d(sa + A_BYTES, &tmB, &full[stage], 0, n_blk * BN, sb * KS, pol_b);
+                    } else {
+                        tma_load_2d(sa, &tmA, &full[stage], sb * kBK, m_blk * kBM, pol_a);
+                        tma_load_2d(sa + A_BYTES, &tmB, &full[stage], sb * kBK, n_blk * BN, pol_b);
+                    }
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -163,25 +172,30 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             bool ok = true;
             bool any = false;
             for (int t = blockIdx.x; t < n_work && ok; t += gridDim.x) {
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, &g_gemm_err)) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, &g_gemm_err, true)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, &g_gemm_err)) {
+                for (int sb = 0; sb < n_stage_blocks; ++sb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, &g_gemm_err, true)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(tiles + stage * STAGE);
-                    const uint64_t a_desc = sw128_kmajor_desc(a_addr);
-                    const uint64_t b_desc = sw128_kmajor_desc(a_addr + kABytes);
+                    const uint32_t b_addr = a_addr + static_cast<uint32_t>(A_BYTES);
+                    for (int j = 0; j < KS; ++j) {
+                        const int kb = sb * KS + j;
+                        if (kb >= KB) break;
+                        const uint64_t a_desc = sw128_kmajor_desc(a_addr + static_cast<uint32_t>(j * g.a_rows * kRowBytes));
+                        const uint64_t b_desc = sw128_kmajor_desc(b_addr + static_cast<uint32_t>(j * BN * kRowBytes));
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // +32 bytes along K inside the swizzle row = +2 in 16-byte units.
-                        umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, g.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            // +32 bytes along K inside the swizzle row = +2 in 16-byte units.
+                            umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, g.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     any = true;
                     umma_commit(&empty[stage]);
@@ -214,6 +228,30 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             const int row = m_blk * kBM + q * 32 + lane;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            if constexpr (EPI == 2) {
+                // Columns [32j, 32j + 16) of the tile are gate rows, [32j + 16, 32j + 32)
+                // the matching up rows: act = bf16(silu(bf16(g)) * bf16(u)).
+                const int F = N / 2;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t gr[16], ur[16];
+                    tmem_ld16(taddr + static_cast<uint32_t>(c), gr);
+                    tmem_ld16(taddr + static_cast<uint32_t>(c + 16), ur);
+                    tmem_ld_wait();
+                    const int col = n_blk * BN + c;
+                    if (row < M && col < N) {
+                        uint32_t o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            o[e] = swiglu_pack(pack_bf16x2(__uint_as_float(gr[2 * e]), __uint_as_float(gr[2 * e + 1])),
+                                               pack_bf16x2(__uint_as_float(ur[2 * e]), __uint_as_float(ur[2 * e + 1])));
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(C) +
+                                                              static_cast<long long>(row) * F + col / 2);
+                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+            } else {
 #pragma unroll 1
             for (int c = 0; c < BN; c += 16) {
                 uint32_t r[16];
@@ -225,7 +263,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                         const int col = n_blk * BN + c + h * 8;
                         if (col < N) {
                             const uint32_t* v = r + h * 8;
-                            if constexpr (OUT_F32) {
+                            if constexpr (EPI == 1) {
                                 float4* dst = reinterpret_cast<float4*>(
                                     static_cast<float*>(C) + static_cast<long long>(row) * N + col);
                                 dst[0] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]),
@@ -244,6 +282,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                         }
                     }
                 }
+            }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -277,17 +316,31 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Row-major bf16 [rows, cols] viewed by TMA as boxes of [box_rows x 64], 128-B swizzle.
-bool encode_kmajor(CUtensorMap* map, const void* base, int cols, int rows, int box_rows) {
+// Row-major bf16 [rows, cols] viewed by TMA with 128-B swizzle.  2-D: boxes of
+// [box_rows x 64].  3-D (cols % 64 == 0): the view [cols/64][rows][64] (k-block,
+// row, column; strides 128 B and cols*2 B), boxes of [ks][box_rows][64], so
+// one box brings ks consecutive k-blocks, each a [box_rows x 64] swizzled tile.
+bool encode_kmajor(CUtensorMap* map, const void* base, int cols, int rows, int box_rows, int ks, bool three_d) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (!three_d) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+        cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+        cuuint32_t estr[2] = {1, 1};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
+        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(ks)};
+        cuuint32_t estr[3] = {1, 1, 1};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS;
 }
 
@@ -297,24 +350,40 @@ uint32_t tmem_cols_for(int BN) {
     return c;
 }
 
-template <bool F32>
+template <int EPI>
 int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream) {
     GemmArgs g;
     g.M = M;
     g.N = N;
     g.K = K;
     g.BN = BN;
-    g.stages = std::min(kMaxStages, kRingBudget / stage_bytes(BN));
     g.a_rows = M >= kBM ? kBM : ((M + 7) / 8) * 8;
+    g.KB = (K + kBK - 1) / kBK;
+    g.three_d = (K % kBK == 0) ? 1 : 0;
+    // The TMA unit spends a fixed ~275 ns per box whatever its size, so a box
+    // should be as large as possible.  With one row tile (M <= 128, weight
+    // streaming) each stage takes as many k-blocks as let two stages fit the
+    // ring; the MMA may then read past the packed A rows of the last stage, so
+    // the ring keeps a tail.  Otherwise (full 128-row tiles, compute-bound) one
+    // k-block per stage and as many stages as fit.
+    int ks = 1;
+    const int tail = g.a_rows < kBM ? kTailSlack : 0;
+    if (g.three_d && g.a_rows < kBM) {
+        const int per_kb = (g.a_rows + BN) * kRowBytes;
+        ks = std::max(1, (kRingBudget - tail) / (2 * per_kb));
+        ks = std::min(ks, std::min(g.KB, 256));
+    }
+    g.KS = ks;
+    g.stages = std::min(kMaxStages, std::max(1, (kRingBudget - tail) / stage_bytes(ks, g.a_rows, BN)));
     g.idesc = idesc_bf16_f32(kBM, BN);
     g.tmem_cols = tmem_cols_for(BN);
     CUtensorMap ta, tb;
-    if (!encode_kmajor(&ta, A, K, M, g.a_rows) || !encode_kmajor(&tb, B, K, N, BN)) {
+    if (!encode_kmajor(&ta, A, K, M, g.a_rows, ks, g.three_d) || !encode_kmajor(&tb, B, K, N, BN, ks, g.three_d)) {
         set_cuda_error(cudaErrorInvalidValue);
         return BIV_ERR_CUDA;
     }
-    const int smem = 1024 + g.stages * stage_bytes(BN) + kBarBytes;
-    auto kern = gemm_nosplitk_kernel<F32>;
+    const int smem = 1024 + g.stages * stage_bytes(ks, g.a_rows, BN) + tail + kBarBytes;
+    auto kern = gemm_nosplitk_kernel<EPI>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -340,6 +409,20 @@ int check_gemm(const void* A, const void* B, void* C, int out_dtype, int M, int 
 }
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Packed row p: block j = p / 32; rows 32j..32j+15 are gate rows 16j..16j+15,
+// rows 32j+16..32j+31 the up rows 16j..16j+15 (source: F gate rows, then F up rows).
+__global__ void swiglu_pack_kernel(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst, int F,
+                                   int K) {
+    pdl_wait();
+    pdl_trigger();
+    const long long p = blockIdx.x;
+    const int j = static_cast<int>(p / 32), r = static_cast<int>(p % 32);
+    const long long s = r < 16 ? 16LL * j + r : static_cast<long long>(F) + 16LL * j + (r - 16);
+    const uint4* in = reinterpret_cast<const uint4*>(src + s * K);
+    uint4* out = reinterpret_cast<uint4*>(dst + p * K);
+    for (int c = threadIdx.x; c < K / 8; c += blockDim.x) out[c] = in[c];
+}
 
 }  // namespace
 }  // namespace biv
@@ -377,8 +460,8 @@ extern "C" int biv_gemm_nosplitk_bn(const void* A, const void* B, void* C, int o
     if (st != BIV_OK || M == 0) return st;
     if (bn < 16 || bn > 256 || bn % 16 != 0) return BIV_ERR_VALUE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return out_dtype == BIV_F32 ? launch_gemm<true>(A, B, C, M, N, K, bn, s)
-                                : launch_gemm<false>(A, B, C, M, N, K, bn, s);
+    return out_dtype == BIV_F32 ? launch_gemm<1>(A, B, C, M, N, K, bn, s)
+                                : launch_gemm<0>(A, B, C, M, N, K, bn, s);
 }
 
 extern "C" int biv_gemm_nosplitk(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K,
@@ -386,4 +469,23 @@ extern "C" int biv_gemm_nosplitk(const void* A, const void* B, void* C, int out_
     int st = check_gemm(A, B, C, out_dtype, M, N, K);
     if (st != BIV_OK || M == 0) return st;
     return biv_gemm_nosplitk_bn(A, B, C, out_dtype, M, N, K, biv_gemm_tile_n(M, N, K), stream);
+}
+
+extern "C" int biv_swiglu_pack_weights(const void* w_gu, void* w_packed, int F, int K, biv_stream_t stream) {
+    if (F <= 0 || K <= 0 || F % 16 != 0 || K % 8 != 0) return BIV_ERR_SHAPE;
+    if (!w_gu || !w_packed) return BIV_ERR_NULL;
+    if (!aligned16(w_gu) || !aligned16(w_packed)) return BIV_ERR_ALIGN;
+    if (w_gu == w_packed) return BIV_ERR_VALUE;
+    return launch_pdl(swiglu_pack_kernel, dim3(2 * F), dim3(128), 0, reinterpret_cast<cudaStream_t>(stream),
+                      static_cast<const __nv_bfloat16*>(w_gu), static_cast<__nv_bfloat16*>(w_packed), F, K);
+}
+
+extern "C" int biv_gemm_swiglu(const void* A, const void* B_packed, void* act, int M, int F, int K,
+                               biv_stream_t stream) {
+    if (F <= 0 || F % 16 != 0) return BIV_ERR_SHAPE;
+    const int N = 2 * F;
+    int st = check_gemm(A, B_packed, act, BIV_BF16, M, N, K);
+    if (st != BIV_OK || M == 0) return st;
+    const int bn = static_cast<int>(std::min<long long>(256, ceil_div(biv_gemm_tile_n(M, N, K), 32) * 32));
+    return launch_gemm<2>(A, B_packed, act, M, N, K, bn, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -128,8 +128,6 @@ __global__ void embed_kernel(const __nv_bfloat16* __restrict__ table, const int3
     for (int c = threadIdx.x; c < d / 8; c += blockDim.x) dst[c] = ok ? src[c] : make_uint4(0, 0, 0, 0);
 }
 
-BIV_DEV float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
-
 __global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, __nv_bfloat16* __restrict__ out, int rows,
                                 int F) {
     pdl_wait();
@@ -145,8 +143,7 @@ __global__ void silu_mul_kernel(const __nv_bfloat16* __restrict__ gu, __nv_bfloa
         uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            o[e] = pack_bf16x2(__fmul_rn(silu(bf16lo(gg[e])), bf16lo(uu[e])),
-                               __fmul_rn(silu(bf16hi(gg[e])), bf16hi(uu[e])));
+            o[e] = swiglu_pack(gg[e], uu[e]);
         reinterpret_cast<uint4*>(out + r * F)[c] = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }

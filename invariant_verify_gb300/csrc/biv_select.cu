@@ -11,17 +11,32 @@
 //
 // Selection kernel: one thread-block cluster of 8 CTAs per row.  Each CTA
 // stages a contiguous slice of the row in shared memory with bulk async
-// copies (one pass over HBM), finds its slice maximum, and the cluster agrees
-// on a lower bound LB = the largest key among the 8 slice maxima (DSMEM).
-// A group of 4 logits (one Philox call) is skipped when even the largest
-// possible noise cannot lift it to LB:
-//     fl(fl(max4 * invT) + G_BOUND) < LB          (strict)
-// which is exact: rounding is monotone, every noise value is < G_BOUND = 17
-// (the noise lies in [-2.82, 16.64] over all 2^23 uniforms), so no skipped
-// entry can reach LB, and the winner's key is >= LB.  Survivors get their
-// noise and key; the winner is the maximum of a 64-bit packed value
-// (order(key) << 32 | ~v), which puts larger keys first and lower indices
-// first among equal keys, so any reduction order gives the same token.
+// copies (one pass over HBM) and finds the winner of its slice; rank 0 takes
+// the largest of the 8 slice winners.  Within a slice, candidates are pruned
+// exactly in two levels, each against a key that some entry of the slice
+// really has (so the slice winner's key is >= the bound):
+//   0. LB = the exact key of the slice's largest logit;
+//   1. a group of 4 logits (one Philox call) is dropped when even the largest
+//      noise cannot lift it to LB: fl(fl(max4 * invT) + 17) < LB -- every
+//      noise value is < 17 (the noise lies in [-2.82, 16.64]);
+//   2. for the rest, the Philox words are drawn and each entry gets the bound
+//      fl(fl(x * invT) + T[w >> 24]), where T[b] bounds the noise of uniform
+//      bucket b from above (the noise is a non-decreasing function of the
+//      23-bit uniform index, checked over all 2^23 values, so the noise at the
+//      bucket's top plus a margin far above the log's error bounds the whole
+//      bucket; a GPU test checks every one of the 2^23 noise values against
+//      it); the best-bounded entry is evaluated exactly and the larger of its
+//      key and LB becomes LB2; only entries whose bound reaches LB2 get their
+//      two logs.
+// No bound crosses CTAs, so the cluster meets only once, at start-up (every
+// CTA's barriers exist before any remote arrive); at the end each CTA stores
+// its winner into rank 0's shared memory and arrives on rank 0's barrier.
+// Rounding is monotone, so no dropped entry can reach the bound.  The winner
+// is the maximum of a 64-bit packed value (order(key) << 32 | ~v), which puts
+// larger keys first and lower indices first among equal keys, so any
+// reduction order gives the same token.
+#include <cmath>
+
 #include "biv_common.cuh"
 
 namespace biv {
@@ -32,8 +47,33 @@ BIV_DEFINE_ERR_WORD(g_select_err)
 constexpr int kClusterSize = 8;
 constexpr int kSelThreads = 256;
 constexpr int kPieces = 4;
-constexpr int kMaxSliceFloats = 57344;          // 224 KiB of shared memory per CTA
+constexpr int kMaxSliceFloats = 45872;          // 5 bytes per logit (value + group bound) <= 224 KiB
 constexpr float kNoiseBound = 17.0f;
+
+// Upper bounds of the noise per uniform bucket (top 8 bits of the 23-bit
+// uniform index), passed to the kernel by value.
+struct NoiseBounds {
+    float v[256];
+};
+
+// Bucket b holds indices k in [b * 2^15, (b + 1) * 2^15); its largest uniform
+// is u = (2 k_max + 1) 2^-24.  Bound = -ln(-ln u) in double + 1e-3, rounded up
+// to float: the fp32 noise routine is within a few ulp of the exact value.
+const NoiseBounds& noise_bounds() {
+    static NoiseBounds nb = [] {
+        NoiseBounds t;
+        for (int b = 0; b < 256; ++b) {
+            const double k = static_cast<double>((b << 15) | 0x7fff);
+            const double u = (2.0 * k + 1.0) * 5.9604644775390625e-8;
+            const double g = -std::log(-std::log(u)) + 1e-3;
+            float f = static_cast<float>(g);
+            if (static_cast<double>(f) < g) f = std::nextafter(f, INFINITY);
+            t.v[b] = f;
+        }
+        return t;
+    }();
+    return nb;
+}
 
 // ----------------------------------------------------------- Philox4x32-10
 struct U4 { uint32_t x, y, z, w; };
@@ -128,14 +168,6 @@ BIV_DEV void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-BIV_DEV unsigned long long ld_dsmem_u64(const void* local_addr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_addr)), "r"(rank));
-    unsigned long long v;
-    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
-    return v;
-}
-
 BIV_DEV void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -157,38 +189,72 @@ BIV_DEV unsigned long long block_max64(unsigned long long v, unsigned long long*
     return r;
 }
 
+// Remote (cluster) store of a 64-bit value and a release-arrive on a remote
+// mbarrier: CTA `rank`'s copy of the shared variable at `local_addr`.
+BIV_DEV uint32_t dsmem_addr(const void* local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_addr)), "r"(rank));
+    return remote;
+}
+
+BIV_DEV void push_to_rank(unsigned long long* slot, uint64_t* bar, uint32_t rank, unsigned long long v) {
+    const uint32_t rs = dsmem_addr(slot, rank), rb = dsmem_addr(bar, rank);
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(rs), "l"(v) : "memory");
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rb) : "memory");
+}
+
+BIV_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // ------------------------------------------------------------ the kernel
 // grid.x = kClusterSize * R, cluster (kClusterSize, 1, 1).  CTA `rank` of the
 // cluster owns logits [rank * slice, min((rank + 1) * slice, V)) of row
-// blockIdx.x / kClusterSize; slice is a multiple of 4.
+// blockIdx.x / kClusterSize; slice is a multiple of 4.  Each CTA prunes
+// against lower bounds of its own slice (any real key is a valid bound for
+// the whole row) and pushes its slice winner into rank 0, which reduces.
 __global__ void __launch_bounds__(kSelThreads)
 gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int slice,
                      const uint32_t* __restrict__ row_req, const int32_t* __restrict__ row_pos,
                      uint32_t seed_lo, uint32_t seed_hi, float invT, int greedy,
-                     int32_t* __restrict__ tokens) {
+                     int32_t* __restrict__ tokens, const __grid_constant__ NoiseBounds nb) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     float* xs = reinterpret_cast<float*>(smem_raw);
+    uint32_t* gub = reinterpret_cast<uint32_t*>(smem_raw + static_cast<size_t>(slice) * 4);  // per group
     __shared__ uint64_t bars[kPieces];
+    __shared__ uint64_t inbox_bar;                             // rank 0: one arrival per CTA
+    __shared__ unsigned long long inbox[kClusterSize];         // rank 0: slice winners
     __shared__ unsigned long long red[kSelThreads / 32];
-    __shared__ unsigned long long published[2];    // [0] slice-max key, [1] slice winner
+    __shared__ unsigned long long bcast;
+    __shared__ float gtab[256];                                // noise bound of each uniform bucket
     __shared__ int abort_flag;
 
+    static_assert(kSelThreads == 256, "one bucket per thread");
+    const uint32_t rank = cluster_rank();
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int p = 0; p < kPieces; ++p) mbar_init(&bars[p], 1);
+        mbar_init(&inbox_bar, kClusterSize);
+        fence_mbar_init();
+    }
+    gtab[threadIdx.x] = nb.v[threadIdx.x];
+    cluster_sync();           // every CTA's barriers exist before any remote arrive
     pdl_wait();
     pdl_trigger();
-    const uint32_t rank = cluster_rank();
+
     const long long row = blockIdx.x / kClusterSize;
     const int begin = static_cast<int>(rank) * slice;
     const int count = max(0, min(slice, V - begin));          // multiple of 4
     const float* src = logits + row * ld + begin;
-
-    // Pieces of the slice, each a multiple of 16 bytes.
     const int piece = ((count / 4 + kPieces - 1) / kPieces) * 4;
-    if (threadIdx.x == 0) {
-        abort_flag = 0;
-        for (int p = 0; p < kPieces; ++p) mbar_init(&bars[p], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
     if (threadIdx.x == 0) {
         for (int p = 0; p < kPieces; ++p) {
             const int off = p * piece;
@@ -197,7 +263,6 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
             if (n > 0) bulk_g2s(xs + off, src + off, static_cast<uint32_t>(n) * 4u, &bars[p]);
         }
     }
-
     const uint32_t req = row_req[row];
     const uint32_t pos = static_cast<uint32_t>(row_pos[row]) + 1u;   // position being selected
 
@@ -225,74 +290,103 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
             }
         }
     }
-    // Slice winner by value (greedy key) -> block max.
     unsigned long long mx = best_i >= 0 ? pack_key(best_x, static_cast<uint32_t>(best_i)) : 0ull;
     mx = block_max64(mx, red);
-    if (!ok) {
-        // Let copies still in flight land before the CTA may exit.
-        if (threadIdx.x == 0)
-            for (int p = 0; p < kPieces; ++p) mbar_wait_drain(&bars[p], 0);
-    }
+    if (!ok && threadIdx.x == 0)
+        for (int p = 0; p < kPieces; ++p) mbar_wait_drain(&bars[p], 0);   // copies in flight land first
 
-    if (greedy) {
-        if (threadIdx.x == 0) published[1] = mx;
-        cluster_sync();
-        if (rank == 0 && threadIdx.x == 0) {
-            unsigned long long w = 0;
-            for (uint32_t c = 0; c < kClusterSize; ++c) w = umax64(w, ld_dsmem_u64(&published[1], c));
-            tokens[row] = w ? static_cast<int32_t>(~static_cast<uint32_t>(w & 0xffffffffull)) : 0;
+    unsigned long long best = mx;
+    if (!greedy && ok) {
+        // LB: the exact key of this slice's largest logit.
+        if (threadIdx.x == 0) {
+            unsigned long long lb = 0;
+            if (mx) {
+                const uint32_t v = ~static_cast<uint32_t>(mx & 0xffffffffull);
+                const U4 w = philox4x32_10(v >> 2, pos, req, 0u, seed_lo, seed_hi);
+                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+                lb = pack_key(__fadd_rn(__fmul_rn(xs[v - begin], invT), gumbel_from_word(words[v & 3u])), v);
+            }
+            bcast = lb;
         }
-        cluster_sync();
-        return;
-    }
+        __syncthreads();
+        const unsigned long long lb = bcast;
+        const uint32_t lb_order = static_cast<uint32_t>(lb >> 32);
 
-    // The key of this slice's maximum is a real key: a valid lower bound.
-    if (threadIdx.x == 0) {
-        unsigned long long lb = 0;
-        if (mx) {
-            const uint32_t v = ~static_cast<uint32_t>(mx & 0xffffffffull);
-            const float x = xs[v - begin];
-            const U4 w = philox4x32_10(v >> 2, pos, req, 0u, seed_lo, seed_hi);
-            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-            const float key = __fadd_rn(__fmul_rn(x, invT), gumbel_from_word(words[v & 3u]));
-            lb = pack_key(key, v);
-        }
-        published[0] = lb;
-    }
-    cluster_sync();
-    unsigned long long lb = 0;
-#pragma unroll
-    for (uint32_t c = 0; c < kClusterSize; ++c) lb = umax64(lb, ld_dsmem_u64(&published[0], c));
-    const uint32_t lb_order = static_cast<uint32_t>(lb >> 32);
-
-    // Pass 2: exact pruning, then noise and keys for the survivors.
-    unsigned long long best = 0;
-    if (ok) {
-        for (int i = threadIdx.x * 4; i < count; i += kSelThreads * 4) {
-            const float4 v4 = *reinterpret_cast<const float4*>(xs + i);
+        // Pass A: level-1 pruning, then Philox words and level-2 bounds.
+        const int n_groups = count / 4;
+        unsigned long long cb = 0;          // best level-2 bound of this thread (order, ~index)
+        for (int gi = threadIdx.x; gi < n_groups; gi += kSelThreads) {
+            const float4 v4 = *reinterpret_cast<const float4*>(xs + 4 * gi);
             const float m4 = fmaxf(fmaxf(v4.x, v4.y), fmaxf(v4.z, v4.w));
-            const float bound = __fadd_rn(__fmul_rn(m4, invT), kNoiseBound);
-            if (key_order(bound) < lb_order) continue;
-            const uint32_t v0 = static_cast<uint32_t>(begin + i);
+            uint32_t g_ord = 0;
+            if (key_order(__fadd_rn(__fmul_rn(m4, invT), kNoiseBound)) >= lb_order) {
+                const uint32_t v0 = static_cast<uint32_t>(begin + 4 * gi);
+                const U4 w = philox4x32_10(v0 >> 2, pos, req, 0u, seed_lo, seed_hi);
+                const float e[4] = {v4.x, v4.y, v4.z, v4.w};
+                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t o = key_order(__fadd_rn(__fmul_rn(e[j], invT), gtab[words[j] >> 24]));
+                    g_ord = max(g_ord, o);
+                    cb = umax64(cb, (static_cast<unsigned long long>(o) << 32) |
+                                        static_cast<unsigned long long>(~(v0 + j)));
+                }
+            }
+            gub[gi] = g_ord;
+        }
+        cb = block_max64(cb, red);
+        // LB2: the exact key of the best-bounded entry (a real key), or LB.
+        if (threadIdx.x == 0) {
+            unsigned long long cand = lb;
+            if (cb) {
+                const uint32_t v = ~static_cast<uint32_t>(cb & 0xffffffffull);
+                const U4 w = philox4x32_10(v >> 2, pos, req, 0u, seed_lo, seed_hi);
+                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+                cand = umax64(cand, pack_key(__fadd_rn(__fmul_rn(xs[v - begin], invT),
+                                                       gumbel_from_word(words[v & 3u])), v));
+            }
+            bcast = cand;
+        }
+        __syncthreads();
+        const unsigned long long lb2 = bcast;
+        const uint32_t lb2_order = static_cast<uint32_t>(lb2 >> 32);
+
+        // Pass B: exact keys only where the level-2 bound reaches LB2.
+        best = lb2;
+        for (int gi = threadIdx.x; gi < n_groups; gi += kSelThreads) {
+            if (gub[gi] < lb2_order) continue;
+            const float4 v4 = *reinterpret_cast<const float4*>(xs + 4 * gi);
+            const uint32_t v0 = static_cast<uint32_t>(begin + 4 * gi);
             const U4 w = philox4x32_10(v0 >> 2, pos, req, 0u, seed_lo, seed_hi);
             const float e[4] = {v4.x, v4.y, v4.z, v4.w};
             const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float key = __fadd_rn(__fmul_rn(e[j], invT), gumbel_from_word(words[j]));
-                best = umax64(best, pack_key(key, v0 + j));
+                const float a = __fmul_rn(e[j], invT);
+                if (key_order(__fadd_rn(a, gtab[words[j] >> 24])) < lb2_order) continue;
+                best = umax64(best, pack_key(__fadd_rn(a, gumbel_from_word(words[j])), v0 + j));
             }
         }
+        best = block_max64(best, red);
     }
-    best = block_max64(best, red);
-    if (threadIdx.x == 0) published[1] = best;
-    cluster_sync();
+
+    // The slice winner goes to rank 0; rank 0 waits for all, reduces and stores.
+    if (threadIdx.x == 0) push_to_rank(&inbox[rank], &inbox_bar, 0, best);
     if (rank == 0 && threadIdx.x == 0) {
+        const uint64_t t0 = globaltimer();
+        bool got = true;
+        while (!mbar_try_wait_cluster(&inbox_bar, 0)) {
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                atomicOr(&g_select_err, BIV_DEVERR_TIMEOUT);
+                got = false;
+                break;
+            }
+        }
         unsigned long long w = 0;
-        for (uint32_t c = 0; c < kClusterSize; ++c) w = umax64(w, ld_dsmem_u64(&published[1], c));
+        if (got)
+            for (int c = 0; c < kClusterSize; ++c) w = umax64(w, inbox[c]);
         tokens[row] = w ? static_cast<int32_t>(~static_cast<uint32_t>(w & 0xffffffffull)) : 0;
     }
-    cluster_sync();   // keep every CTA's shared memory alive until rank 0 has read it
 }
 
 __global__ void gumbel_noise_kernel(uint32_t seed_lo, uint32_t seed_hi, const uint32_t* __restrict__ row_req,
@@ -355,7 +449,7 @@ extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld
     if (static_cast<long long>(R) * kClusterSize > 0x7fffffffLL) return BIV_ERR_SHAPE;
     const int greedy = temperature == 0.0f;
     const float invT = greedy ? 0.0f : 1.0f / temperature;   // fl(1/T), IEEE division on the host
-    const size_t smem = static_cast<size_t>(slice) * 4;
+    const size_t smem = static_cast<size_t>(slice) * 5;
 
     static int configured_device = -1;
     static size_t configured_smem = 0;
@@ -363,10 +457,10 @@ extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld
     cudaGetDevice(&dev);
     if (configured_device != dev || configured_smem < smem) {
         cudaError_t e = cudaFuncSetAttribute(gumbel_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kMaxSliceFloats * 4));
+                                             static_cast<int>(kMaxSliceFloats * 5));
         if (e != cudaSuccess) return cuda_status(e);
         configured_device = dev;
-        configured_smem = kMaxSliceFloats * 4;
+        configured_smem = kMaxSliceFloats * 5;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(R) * kClusterSize, 1, 1);
@@ -384,7 +478,7 @@ extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld
     cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, gumbel_argmax_kernel, logits, V, ld, slice, row_req, row_pos,
                                        static_cast<uint32_t>(seed & 0xffffffffull),
-                                       static_cast<uint32_t>(seed >> 32), invT, greedy, tokens);
+                                       static_cast<uint32_t>(seed >> 32), invT, greedy, tokens, noise_bounds());
     if (e != cudaSuccess) return cuda_status(e);
     return launch_status();
 }
@@ -416,4 +510,11 @@ extern "C" int biv_verify_accept(const int32_t* target, const int32_t* draft, co
     if (!target || !draft || !p0 || !accept_len || !new_len) return BIV_ERR_NULL;
     return launch_pdl(verify_accept_kernel, dim3((N + 127) / 128), dim3(128), 0, reinterpret_cast<cudaStream_t>(stream),
                       target, draft, p0, N, K, accept_len, new_len);
+}
+
+extern "C" int biv_gumbel_bucket_bounds(float* bounds_out) {
+    if (!bounds_out) return BIV_ERR_NULL;
+    const NoiseBounds& nb = noise_bounds();
+    for (int b = 0; b < 256; ++b) bounds_out[b] = nb.v[b];
+    return BIV_OK;
 }

@@ -45,6 +45,12 @@ class DecoderVerifier:
         self.n_slots, self.max_len, self.seed = n_slots, max_len, seed
         dev = torch.device(device)
         self.w = {k: v.to(dev).contiguous() for k, v in weights.items()}
+        # gate/up weights rearranged once for the SwiGLU-epilogue GEMM
+        for l in range(cfg.layers):
+            wgu = self.w[f"l{l}.wgu"]
+            packed = torch.empty_like(wgu)
+            B.biv_swiglu_pack_weights(wgu, packed)
+            self.w[f"l{l}.wgu_packed"] = packed
         self.kc = [k.to(dev).contiguous() for k, _ in caches]
         self.vc = [v.to(dev).contiguous() for _, v in caches]
         d, Hq, Hkv, hd, F = cfg.d, cfg.Hq, cfg.Hkv, cfg.hd, cfg.ffn
@@ -53,10 +59,8 @@ class DecoderVerifier:
         self.h = torch.empty(W, d, **bf)
         self.qkv = torch.empty(W, cfg.qkv_n, **bf)
         self.q = torch.empty(W, Hq, hd, **bf)
-        self.k = torch.empty(W, Hkv * hd, **bf)
         self.o = torch.empty(W, Hq, hd, **bf)
         self.proj = torch.empty(W, d, **bf)
-        self.gu = torch.empty(W, 2 * F, **bf)
         self.act = torch.empty(W, F, **bf)
         self.hidden = torch.empty(W, d, **bf)
         self.logits = torch.empty(W, cfg.vocab, device=dev, dtype=torch.float32)
@@ -66,8 +70,8 @@ class DecoderVerifier:
         self.new_len = torch.empty(N, device=dev, dtype=torch.int32)
         ws = B.biv_decode_attn_workspace_size(W, Hq, max_len)
         self.workspace = torch.empty(max(ws, 16), device=dev, dtype=torch.uint8)
-        # embed+norm, per layer 11 kernels (attention is two), LM head, select, accept
-        self.launches_per_step = 4 + cfg.layers * 11
+        # embed+norm, per layer 9 kernels (attention is two), LM head, select, accept
+        self.launches_per_step = 4 + cfg.layers * 9
 
     # -------------------------------------------------------------- stages
     def forward(self, win: Window, trace: dict | None = None) -> None:
@@ -90,11 +94,10 @@ class DecoderVerifier:
             snap(f"l{l}.h_attn", self.h)
             B.biv_gemm_nosplitk(self.h, w[f"l{l}.wqkv"], self.qkv)
             snap(f"l{l}.qkv", self.qkv)
-            B.biv_rope_qk(self.qkv, self.q, self.k, win.row_pos, Hq, Hkv, hd, c.rope_theta)
+            # RoPE on q and k; k and v go straight into the cache rows of the window
+            B.biv_rope_kv_write(self.qkv, self.q, self.kc[l], self.vc[l], win.row_slot, win.row_pos, Hq,
+                                c.rope_theta, K=self.rpg)
             snap(f"l{l}.q", self.q)
-            snap(f"l{l}.k", self.k)
-            v_new = self.qkv[:, (Hq + Hkv) * hd:]
-            B.biv_kv_overwrite(self.kc[l], self.vc[l], self.k, v_new, win.row_slot, win.row_pos, K=self.rpg)
             if trace is not None:
                 trace[f"l{l}.kc"], trace[f"l{l}.vc"] = self.kc[l].clone(), self.vc[l].clone()
             B.biv_decode_attn_fixedsplit(self.q, self.kc[l], self.vc[l], win.row_slot, win.row_pos, self.o,
@@ -105,9 +108,7 @@ class DecoderVerifier:
             B.biv_add_rmsnorm(self.x, self.proj, w[f"l{l}.ffn_norm"], self.x, self.h, c.eps)
             snap(f"l{l}.x_mid", self.x)
             snap(f"l{l}.h_ffn", self.h)
-            B.biv_gemm_nosplitk(self.h, w[f"l{l}.wgu"], self.gu)
-            snap(f"l{l}.gu", self.gu)
-            B.biv_silu_mul(self.gu, self.act)
+            B.biv_gemm_swiglu(self.h, w[f"l{l}.wgu_packed"], self.act)
             snap(f"l{l}.act", self.act)
             B.biv_gemm_nosplitk(self.act, w[f"l{l}.wdown"], self.proj)
             snap(f"l{l}.down", self.proj)

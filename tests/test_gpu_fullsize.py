@@ -141,8 +141,14 @@ def test_llama_layer_sampled_parity(llama):
     got = cpu["l0.o"][rows, heads].float()
     assert_close(got, ref, what="attention")
     gemm_check(cpu["l0.o"].view(M, Hq * hd), "l0.wo", cpu["l0.attn_proj"], 2, "wo")
-    gemm_check(cpu["l0.h_ffn"], "l0.wgu", cpu["l0.gu"], 3, "gate/up")
-    assert_close(cpu["l0.act"][:8], oracle.silu_mul(cpu["l0.gu"][:8]), what="swiglu")
+    # gate/up + SwiGLU on sampled (row, i): act = silu(bf16(g)) * bf16(u)
+    F = cfg.ffn
+    m, i = _sample_pairs(M, F, 256, 3)
+    wgu = w["l0.wgu"].cpu()
+    g = oracle.round_bf16(oracle.gemm_sampled(cpu["l0.h_ffn"], wgu, m, i))
+    u = oracle.round_bf16(oracle.gemm_sampled(cpu["l0.h_ffn"], wgu, m, F + i))
+    ref = oracle.silu_mul(np.stack([g, u], axis=1))[:, 0]
+    assert_close(torch.from_numpy(cpu["l0.act"].float().numpy()[m, i]), ref, what="gate/up + swiglu")
     gemm_check(cpu["l0.act"], "l0.wdown", cpu["l0.down"], 4, "down")
     gemm_check(cpu["hidden"], "lm_head", ver.logits.cpu(), 5, "lm head")
     tgt = oracle.gumbel_argmax(ver.logits.cpu(), win.row_req.cpu(), pos, SEED, cfg.temperature)

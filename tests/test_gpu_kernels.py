@@ -148,6 +148,22 @@ def test_gemm_tile_width_does_not_change_bits():
         assert same_bits(outs[bn], outs[256]), bn
 
 
+@pytest.mark.parametrize("M,F,K", [(64, 2816, 1024), (1, 48, 64), (130, 1024, 200), (300, 112, 136)])
+def test_gemm_swiglu_equals_gemm_then_silu(M, F, K):
+    g = synth.generator(M + F + K)
+    A = dev(synth.bf16_normal((M, K), 1.0, g))
+    wgu = dev(synth.bf16_normal((2 * F, K), 0.05, g))
+    gu = torch.empty(M, 2 * F, dtype=torch.bfloat16, device="cuda")
+    ref = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+    B.biv_gemm_nosplitk(A, wgu, gu)
+    B.biv_silu_mul(gu, ref)
+    packed = torch.empty_like(wgu)
+    B.biv_swiglu_pack_weights(wgu, packed)
+    act = torch.full((M, F), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.biv_gemm_swiglu(A, packed, act)
+    assert same_bits(act, ref)
+
+
 # --------------------------------------------------------------- attention
 def _attn_case(n_slots, Hq, Hkv, max_len, p0, K, seed):
     g = synth.generator(seed)
@@ -240,6 +256,26 @@ def test_kv_overwrite_bit_exact_and_rows_keep():
     assert np.array_equal(oracle._np(kd.cpu()), ko) and np.array_equal(oracle._np(vd.cpu()), vo)
 
 
+def test_rope_kv_write_equals_rope_then_overwrite():
+    W, K, Hq, Hkv, hd = 12, 4, 8, 2, 128
+    g = synth.generator(61)
+    qkv = dev(synth.bf16_normal((W, (Hq + 2 * Hkv) * hd), 1.0, g))
+    kc = dev(synth.bf16_normal((3, Hkv, 80, hd), 1.0, g))
+    vc = dev(synth.bf16_normal((3, Hkv, 80, hd), 1.0, g))
+    slot = i32(np.repeat([2, 0, 1], K))
+    pos = i32(np.repeat([10, 50, 0], K) + np.tile(np.arange(K), 3))
+    for keep in (None, i32([1, 4, 0])):
+        q1 = torch.empty(W, Hq, hd, dtype=torch.bfloat16, device="cuda")
+        k1 = torch.empty(W, Hkv * hd, dtype=torch.bfloat16, device="cuda")
+        kc1, vc1 = kc.clone(), vc.clone()
+        B.biv_rope_qk(qkv, q1, k1, pos, Hq, Hkv, hd, 10000.0)
+        B.biv_kv_overwrite(kc1, vc1, k1, qkv[:, (Hq + Hkv) * hd:], slot, pos, K=K, rows_keep=keep)
+        q2 = torch.empty_like(q1)
+        kc2, vc2 = kc.clone(), vc.clone()
+        B.biv_rope_kv_write(qkv, q2, kc2, vc2, slot, pos, Hq, 10000.0, K=K, rows_keep=keep)
+        assert same_bits(q2, q1) and same_bits(kc2, kc1) and same_bits(vc2, vc1)
+
+
 def test_rope_parity():
     W, Hq, Hkv, hd = 10, 8, 2, 128
     g = synth.generator(31)
@@ -287,6 +323,20 @@ def test_noise_bit_exact_over_every_uniform():
     B.biv_gumbel_from_words(w.cuda(), g)
     ref = oracle.gumbel_from_words(w.numpy().view(np.uint32))
     assert np.array_equal(g.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_noise_bucket_bounds_hold_for_every_word():
+    # The selection kernel's pruning bound: noise(word) <= bounds[word >> 24]
+    # for all 2^23 uniforms (the low 9 bits do not change the uniform).
+    words = np.arange(2 ** 23, dtype=np.uint32) << np.uint32(9)
+    g = torch.empty(2 ** 23, dtype=torch.float32, device="cuda")
+    B.biv_gumbel_from_words(torch.from_numpy(words.view(np.int32)).cuda(), g)
+    bounds = B.biv_gumbel_bucket_bounds()
+    gb = g.cpu().numpy()
+    assert np.all(gb <= bounds[words >> 24])
+    # and the bound is tight enough to prune: within 2e-3 of each bucket's top
+    top = gb.reshape(256, -1).max(axis=1)
+    assert np.all(bounds - top < 2e-3)
 
 
 def test_noise_rows_bit_exact():

@@ -127,14 +127,14 @@ def test_decoder_stagewise_parity(dec2):
         qkv = oracle.from_bf16(_cpu(tr[f"l{l}.qkv"]))
         assert_close(tr[f"l{l}.q"], oracle.rope(qkv[:, :Hq * hd].reshape(W, Hq, hd), pos, cfg.rope_theta),
                      what=f"l{l} rope q")
-        assert_close(tr[f"l{l}.k"].view(W, Hkv, hd),
-                     oracle.rope(qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(W, Hkv, hd), pos, cfg.rope_theta),
-                     what=f"l{l} rope k")
-        # KV overwrite: exactly the window rows now hold the verifier's k and v
+        # KV overwrite: the window rows hold the rotated k and the raw v, every other row is untouched
+        k_ref = oracle.rope(qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(W, Hkv, hd), pos, cfg.rope_theta)
+        kc_gpu = _cpu(tr[f"l{l}.kc"])
+        assert_close(kc_gpu[slot, :, pos].float(), k_ref, what=f"l{l} rope k in cache")
         kc = oracle._np(caches[l][0]).copy(); vc = oracle._np(caches[l][1]).copy()
         vnew = oracle._np(_cpu(tr[f"l{l}.qkv"])[:, (Hq + Hkv) * hd:].contiguous()).reshape(W, Hkv, hd)
-        oracle.kv_overwrite(kc, vc, oracle._np(_cpu(tr[f"l{l}.k"])).reshape(W, Hkv, hd), vnew, slot, pos)
-        assert np.array_equal(oracle._np(_cpu(tr[f"l{l}.kc"])), kc)
+        oracle.kv_overwrite(kc, vc, oracle._np(kc_gpu[slot, :, pos].contiguous()), vnew, slot, pos)
+        assert np.array_equal(oracle._np(kc_gpu), kc)
         assert np.array_equal(oracle._np(_cpu(tr[f"l{l}.vc"])), vc)
         assert_close(tr[f"l{l}.o"], oracle.attention(_cpu(tr[f"l{l}.q"]), kc, vc, slot, pos), what=f"l{l} attn")
         assert_close(tr[f"l{l}.attn_proj"], oracle.gemm(_cpu(tr[f"l{l}.o"]).view(W, Hq * hd), w[f"l{l}.wo"]),
@@ -142,8 +142,8 @@ def test_decoder_stagewise_parity(dec2):
         assert_close(tr[f"l{l}.x_mid"], oracle.from_bf16(_cpu(x)) + oracle.from_bf16(_cpu(tr[f"l{l}.attn_proj"])),
                      what=f"l{l} residual")
         assert_close(tr[f"l{l}.h_ffn"], oracle.rmsnorm(_cpu(tr[f"l{l}.x_mid"]), ones, cfg.eps), what=f"l{l} norm2")
-        assert_close(tr[f"l{l}.gu"], oracle.gemm(_cpu(tr[f"l{l}.h_ffn"]), w[f"l{l}.wgu"]), what=f"l{l} gate/up")
-        assert_close(tr[f"l{l}.act"], oracle.silu_mul(_cpu(tr[f"l{l}.gu"])), what=f"l{l} swiglu")
+        gu = oracle.round_bf16(oracle.gemm(_cpu(tr[f"l{l}.h_ffn"]), w[f"l{l}.wgu"]))
+        assert_close(tr[f"l{l}.act"], oracle.silu_mul(gu), what=f"l{l} gate/up + swiglu")
         assert_close(tr[f"l{l}.down"], oracle.gemm(_cpu(tr[f"l{l}.act"]), w[f"l{l}.wdown"]), what=f"l{l} down")
         assert_close(tr[f"l{l}.x_out"], oracle.from_bf16(_cpu(tr[f"l{l}.x_mid"])) +
                      oracle.from_bf16(_cpu(tr[f"l{l}.down"])), what=f"l{l} residual 2")
