@@ -53,6 +53,8 @@ def lib():
             "orc_gumbel_row": (None, [u64, u32, u32, i32, P]),
             "orc_gumbel_argmax": (None, [P, i32, i32, i64, P, P, u64, f32, P]),
             "orc_verify_accept": (None, [P, P, P, i32, i32, P, P]),
+            "orc_gumbel_topk": (None, [P, i32, i32, i64, P, P, u64, f32, i32, P]),
+            "orc_ngram_draft": (None, [P, i32, i64, P, i32, i32, i32, P, P]),
             "orc_gqa_max_drafts": (i32, [i32, i32]),
         }
         for name, (res, args) in sig.items():
@@ -254,6 +256,31 @@ def gumbel_argmax(logits, row_req, row_pos, seed: int, temperature: float) -> np
     out = np.empty(R, np.int32)
     lib().orc_gumbel_argmax(_p(x), R, V, V, _p(rq), _p(rp), int(seed), float(temperature), _p(out))
     return out
+
+
+def gumbel_topk(logits, row_req, row_pos, seed: int, temperature: float, k: int) -> np.ndarray:
+    """The k largest Gumbel keys of each row, in order (int32 [R, k])."""
+    x = _np(logits, np.float32)
+    R, V = x.shape
+    assert 1 <= k <= V
+    rq = np.ascontiguousarray(_np(row_req).astype(np.int64) & 0xFFFFFFFF, np.uint32)
+    rp = np.ascontiguousarray(_np(row_pos), np.int32)
+    out = np.empty((R, k), np.int32)
+    lib().orc_gumbel_topk(_p(x), R, V, V, _p(rq), _p(rp), int(seed), float(temperature), int(k), _p(out))
+    return out
+
+
+def ngram_draft(hist, lengths, n_max: int, n_min: int, K: int):
+    """n-gram lookup drafts (int32 [N, K]) and the copy source per request
+    (longest n-gram suffix match, most recent occurrence, LZ-style copy)."""
+    h = np.ascontiguousarray(_np(hist), np.int32)
+    N, ld = h.shape
+    ln = np.ascontiguousarray(_np(lengths), np.int32)
+    assert ln.shape == (N,) and (ln >= 0).all() and (ln <= ld).all() and 1 <= n_min <= n_max
+    d = np.empty((N, K), np.int32)
+    src = np.empty(N, np.int32)
+    lib().orc_ngram_draft(_p(h), N, ld, _p(ln), int(n_max), int(n_min), int(K), _p(d), _p(src))
+    return d, src
 
 
 def verify_accept(target, draft, p0, N: int, K: int):

@@ -31,6 +31,7 @@
 // v & 3; uniform u = (2*(w >> 9) + 1) * 2^-24; the log is the routine below;
 // key = fl(fl(x * fl(1/T)) + g); ties go to the lowest index; T = 0 is greedy.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -412,6 +413,78 @@ void orc_gumbel_argmax(const float* logits, int R, int V, long long ld, const ui
             if (best_v < 0 || key_beats(key, v, best, best_v)) { best = key; best_v = v; }
         }
         tokens[r] = best_v;
+    }
+}
+
+// ----------------------------------------------------------- Gumbel top-k
+// [COUPLING]: the Gumbel-max trick gives top-k sampling directly: the k
+// entries with the largest keys, in decreasing key order, are a sample of k
+// distinct tokens without replacement from softmax(x / T) (Kool, van Hoof &
+// Welling, "Stochastic Beams and Where to Find Them", ICML 2019).  Same keys,
+// same order (ties -> lower index, NaN keys last) as orc_gumbel_argmax, so
+// column 0 is the Gumbel-max token.
+void orc_gumbel_topk(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                     const int* row_pos, uint64_t seed, float temperature, int k, int* out) {
+    float invT = temperature > 0.0f ? 1.0f / temperature : 0.0f;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < R; ++r) {
+        const float* x = logits + (long long)r * ld;
+        uint32_t pos = (uint32_t)(row_pos[r] + 1);
+        std::vector<float> key(V);
+        std::vector<int> idx(V);
+        for (int v = 0; v < V; ++v) {
+            if (temperature > 0.0f) {
+                float a = x[v] * invT;
+                key[v] = a + orc_gumbel(seed, row_req[r], pos, (uint32_t)v);
+            } else {
+                key[v] = x[v];
+            }
+            idx[v] = v;
+        }
+        std::partial_sort(idx.begin(), idx.begin() + k, idx.end(),
+                          [&](int a, int b) { return key_beats(key[a], a, key[b], b); });
+        for (int j = 0; j < k; ++j) out[(long long)r * k + j] = idx[j];
+    }
+}
+
+// ------------------------------------------------------- n-gram drafter
+// Training-free n-gram lookup drafter (NVIDIA inference guide page, the
+// drafting methods it lists: repeated fragments of the earlier text are found
+// and copied).  Reading: for request r with committed history h[0..L) take
+// the longest n in [n_min, n_max] whose last-n-token suffix also occurs
+// earlier with at least one token after it; of those occurrences take the
+// most recent (largest start p <= L - n - 1); the drafts copy the K tokens
+// that followed it, s = p + n: d_j = e[s + j] where e is the history with the
+// drafts appended (a copy that runs past the end continues from its own
+// output, as an LZ77 copy does, so a periodic text is continued exactly).  No
+// match for any n: all K drafts are h[L - 1] (0 for an empty history).
+// draft_src[r] = s, or -1.
+void orc_ngram_draft(const int* hist, int N, long long ld, const int* len, int n_max, int n_min, int K,
+                     int* drafts, int* draft_src) {
+    for (int r = 0; r < N; ++r) {
+        const int* h = hist + (long long)r * ld;
+        const int L = len[r];
+        int src = -1;
+        for (int n = n_max; n >= n_min && src < 0; --n) {
+            if (L < n + 1) continue;
+            for (int p = L - n - 1; p >= 0; --p) {
+                bool match = true;
+                for (int i = 0; i < n; ++i) {
+                    if (h[p + i] != h[L - n + i]) { match = false; break; }
+                }
+                if (match) { src = p + n; break; }
+            }
+        }
+        draft_src[r] = src;
+        int* d = drafts + (long long)r * K;
+        for (int j = 0; j < K; ++j) {
+            if (src < 0) {
+                d[j] = L > 0 ? h[L - 1] : 0;
+            } else {
+                const int t = src + j;
+                d[j] = t < L ? h[t] : d[t - L];
+            }
+        }
     }
 }
 
