@@ -79,20 +79,23 @@ def workload_config(cfg):
 
 
 # ------------------------------------------------------------------ setup
-def build_problem(cfg, device, seed_offset=0):
-    from invariant_verify_gb300 import synth
+def build_problem(cfg, device, rank=0):
+    """The rank's own window: requests rank*N .. rank*N + N - 1 of the job,
+    with their own contexts, caches and drafts (weak scaling)."""
+    from invariant_verify_gb300 import replicas, synth
     from invariant_verify_gb300.verifier import DecoderVerifier, make_window
     w = synth.decoder_weights(cfg)
-    ctx = synth.context_lengths(cfg, cfg.N, seed=cfg.seed + 100 + seed_offset)
+    ctx = synth.context_lengths(cfg, cfg.N, seed=cfg.seed + 100 + rank)
     max_len = int(ctx.max()) + 64
-    caches = synth.kv_cache(cfg.N, cfg.Hkv, max_len, cfg.hd, ctx, seed=cfg.seed + 200 + seed_offset,
+    caches = synth.kv_cache(cfg.N, cfg.Hkv, max_len, cfg.hd, ctx, seed=cfg.seed + 200 + rank,
                             layers=cfg.layers)
-    ver = DecoderVerifier(cfg, w, caches, cfg.N, max_len, cfg.W, cfg.K, device=device)
-    g = synth.generator(cfg.seed + 300 + seed_offset)
+    ver = DecoderVerifier(cfg, w, caches, cfg.N, max_len, cfg.W, cfg.K, device=device, fused_select=True,
+                          keep_logits=False)
+    g = synth.generator(cfg.seed + 300 + rank)
     N, K = cfg.N, cfg.K
     last = torch.randint(0, cfg.vocab, (N,), generator=g, dtype=torch.int64).to(torch.int32)
-    mask, ids = synth.draft_errors((N, K), cfg.draft_err, cfg.vocab, seed=cfg.seed + 400 + seed_offset)
-    req = torch.arange(N, dtype=torch.int32) * 1000 + 17
+    mask, ids = synth.draft_errors((N, K), cfg.draft_err, cfg.vocab, seed=cfg.seed + 400 + rank)
+    req = replicas.request_ids(replicas.rank_requests(N, rank))
     # A drafter that is right 70% of the time: fix d_1..d_K one position at a
     # time from the verifier's own selections (d_j feeds row j).
     drafts = torch.zeros(N, K, dtype=torch.int32)
@@ -149,10 +152,10 @@ def clock_sampler_stop(p, f, path, gpu_index):
 
 
 def lm_head_traffic():
-    """Per-launch DRAM bytes of the LM-head GEMM from the committed ncu summary,
-    or None when the GEMM source changed since that capture."""
-    path = os.path.join(ROOT, "profiles", "lmhead_gemm_decoder2.md")
-    src = os.path.join(ROOT, "invariant_verify_gb300", "csrc", "biv_gemm.cu")
+    """Per-launch DRAM bytes of the fused LM-head/selection kernel from the
+    committed ncu summary, or None when the kernel source changed since that
+    capture."""
+    path = os.path.join(ROOT, "profiles", "lmhead_select_fused_decoder2.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -160,14 +163,51 @@ def lm_head_traffic():
     h = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     if not m or not h:
         return None
-    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return float(m.group(1)) if cur.startswith(h.group(1)) else None
+    return float(m.group(1)) if kernel_source_sha256().startswith(h.group(1)) else None
+
+
+def kernel_source_sha256():
+    """Hash of the sources the fused LM-head/selection kernel is built from."""
+    csrc = os.path.join(ROOT, "invariant_verify_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("biv_gemm.cu", "biv_gumbel.cuh", "biv_common.cuh"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()
+
+
+def marked_graphs(ver, win, n):
+    """``n`` graphs of the whole step, each with its own pair of timing events
+    recorded as graph nodes immediately before and after the LM-head launch;
+    None where this PyTorch cannot record events inside a graph."""
+    try:
+        pool = []
+        for _ in range(n):
+            ea = torch.cuda.Event(enable_timing=True, external=True)
+            eb = torch.cuda.Event(enable_timing=True, external=True)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                ver.forward(win)
+                ea.record()
+                ver.lm_head(win)
+                eb.record()
+                ver.select_and_accept(win)
+            pool.append((g, ea, eb))
+        g, ea, eb = pool[0]
+        g.replay()
+        eb.synchronize()
+        ea.elapsed_time(eb)
+        return pool
+    except (TypeError, RuntimeError) as exc:
+        print(f"bench: no event nodes in graphs ({exc}); timing the LM head between graph segments",
+              file=sys.stderr)
+        torch.cuda.synchronize()
+        return None
 
 
 # --------------------------------------------------------------- our arm
 def run_ours(args):
     import torch.distributed as dist
-    from invariant_verify_gb300 import synth
+    from invariant_verify_gb300 import replicas, synth
     import __graft_entry__
     rank, world, local = dist_info()
     if world > 1:
@@ -179,24 +219,40 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     cfg = synth.DECODER2
-    ver, win, w_cpu, caches_cpu, max_len, ctx = build_problem(cfg, device, seed_offset=0)
-    graphs = ver.capture(win, segments=True)
+    ver, win, w_cpu, caches_cpu, max_len, ctx = build_problem(cfg, device, rank=rank)
     full_graph = ver.capture(win, segments=False)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
+    K = args.steps
+    # Each timed step replays one graph of the whole step.  The LM-head launch
+    # is bracketed by event-record nodes inside that graph (a pool of graphs,
+    # each with its own event pair, read back once its replay has finished);
+    # where event nodes are unavailable the step is replayed as three graphs
+    # with events between them.
+    pool = marked_graphs(ver, win, min(K, 16))
+    lm_timing = "event-record nodes around the LM-head launch inside the step graph"
+    if pool is None:
+        segs = ver.capture(win, segments=True)
+        lm_timing = "events between graph segments (layers | LM head | select+accept)"
 
-    def one_step():
-        graphs[0].replay()
-        graphs[1].replay()
-        graphs[2].replay()
+    def one_step(i):
+        if pool is None:
+            segs[0].replay()
+            seg_ev[i][0].record(stream)
+            segs[1].replay()
+            seg_ev[i][1].record(stream)
+            segs[2].replay()
+        else:
+            pool[i % len(pool)][0].replay()
 
-    for _ in range(max(3, args.warmup)):
+    seg_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)] if pool is None else None
+    for i in range(max(3, args.warmup)):
         flush.zero_()
-        one_step()
+        one_step(i % K)
     torch.cuda.synchronize()
 
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    lm_ms = []
     out_dir = os.path.join(ROOT, "gpurun_out")
     clk_path = os.path.join(out_dir if os.path.isdir(out_dir) else "/tmp", f"bench_clocks_rank{rank}.csv")
     sampler, sf = clock_sampler_start(clk_path) if local == 0 else (None, None)
@@ -205,27 +261,28 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(K):
+        if pool is not None and i >= len(pool):
+            _, ea, eb = pool[i % len(pool)]
+            eb.synchronize()                 # that graph's previous replay is done
+            lm_ms.append(ea.elapsed_time(eb))
         flush.zero_()
         e = ev[i]
         e[0].record(stream)
-        graphs[0].replay()
+        one_step(i)
         e[1].record(stream)
-        graphs[1].replay()
-        e[2].record(stream)
-        graphs[2].replay()
-        e[3].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - t0
     clocks = clock_sampler_stop(sampler, sf, clk_path, local)
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    lm_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    tot_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([tot_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    if pool is not None:
+        for i in range(max(0, K - len(pool)), K):
+            _, ea, eb = pool[i % len(pool)]
+            lm_ms.append(ea.elapsed_time(eb))
+    else:
+        lm_ms = [a.elapsed_time(b) for a, b in seg_ev]
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    tot_ms = replicas.slowest(float(sum(step_ms)), device=device)
     ms_per_step = tot_ms / K
     value = cfg.W * world * K / (tot_ms / 1e3)
     committed = int(ver.accept_len.sum().item())
@@ -233,14 +290,18 @@ def run_ours(args):
     # roofline of the dominant kernel (LM-head GEMM, HBM-bound at W=64)
     hbm, bf16, src = peaks()
     M, N, Kd = cfg.W, cfg.vocab, cfg.d
-    lm_bytes = 2 * N * Kd + 2 * M * Kd + 4 * M * N
+    # weights + activations in, request ids / positions in, tokens out (the
+    # logits stay in TMEM; the per-tile winners are not counted)
+    lm_bytes = 2 * N * Kd + 2 * M * Kd + 12 * M
     lm_avg_s = statistics.mean(lm_ms) / 1e3
     achieved = lm_bytes / lm_avg_s / 1e9
-    roofline = {"kernel": "gemm_nosplitk_kernel (LM head, M=64 N=32000 K=1024, fp32 out)", "bound": "hbm",
+    roofline = {"kernel": "gemm_nosplitk_kernel<3> + tile_winners_kernel (LM head M=64 N=32000 K=1024 with "
+                          "the Gumbel-max selection in its epilogue, then the per-row winner)",
+                "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
                 "traffic": lm_head_traffic(), "algorithmic_bytes": lm_bytes,
-                "avg_launch_us": round(lm_avg_s * 1e6, 2)}
+                "avg_launch_us": round(lm_avg_s * 1e6, 2), "launch_timing": lm_timing}
     step_bytes, step_flops = step_work(cfg, ctx)
     step_roof_us = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12)) * 1e6
 
@@ -269,13 +330,13 @@ def run_ours(args):
 
 
 def step_work(cfg, ctx):
-    """Algorithmic bytes and flops of one step (weights once, KV read, logits
-    written and read, activations ignored)."""
+    """Algorithmic bytes and flops of one step (weights once, KV read,
+    activations ignored; the logits never reach HBM)."""
     W, d, F, V, hd = cfg.W, cfg.d, cfg.ffn, cfg.vocab, cfg.hd
     per_layer_w = (cfg.qkv_n * d + d * cfg.Hq * hd + 2 * F * d + d * F) * 2
     weights = cfg.layers * per_layer_w + V * d * 2
     kv = sum(2 * 2 * cfg.Hkv * (int(c) + cfg.K) * hd for c in ctx) * cfg.layers
-    logits = 2 * 4 * W * V
+    logits = 0
     flops = 2 * W * (cfg.layers * per_layer_w // 2 + V * d)
     flops += cfg.layers * sum(4 * cfg.Hq * cfg.K * (int(c) + cfg.K) * hd for c in ctx)
     return weights + kv + logits, flops
@@ -415,7 +476,7 @@ def run_reference(args):
     rank, world, _ = dist_info()
     if rank != 0:
         return
-    from invariant_verify_gb300 import synth
+    from invariant_verify_gb300 import replicas, synth
     from invariant_verify_gb300.verifier import make_window
     from oracle import build as ob
     ob.build()
@@ -426,7 +487,7 @@ def run_reference(args):
     caches = synth.kv_cache(cfg.N, cfg.Hkv, max_len, cfg.hd, ctx, seed=cfg.seed + 200, layers=cfg.layers)
     g = synth.generator(cfg.seed + 300)
     toks = torch.randint(0, cfg.vocab, (cfg.W,), generator=g, dtype=torch.int64).to(torch.int32)
-    win = make_window(cfg.N, cfg.K, toks, ctx, torch.arange(cfg.N) * 1000 + 17, toks, device="cpu")
+    win = make_window(cfg.N, cfg.K, toks, ctx, replicas.request_ids(range(cfg.N)), toks, device="cpu")
     steps = max(1, args.steps)
     v, n, spent, cores = oracle_rows_per_second(cfg, w, caches, max_len, win, 0.0, max_steps=steps,
                                                 warmup=max(0, min(args.warmup, 3)))

@@ -242,6 +242,58 @@ int biv_gumbel_from_words(const uint32_t* words, long long n, float* g, biv_stre
  * For tests of the pruning bound.                                         */
 int biv_gumbel_bucket_bounds(float* bounds_out);
 
+/* LM head with the selection fused into its epilogue ([COUPLING]: the noise
+ * does not depend on the logits, so it can be applied where the logits are
+ * made).  tokens[r] is bit-identical to biv_gemm_nosplitk(A, B, C, BIV_F32,
+ * M, N, K) followed by biv_gumbel_argmax(C, M, N, N, row_req, row_pos, seed,
+ * temperature, tokens): the keys are formed from the same fp32 accumulators.
+ * Each CTA selects the winner of every row of its output tile from TMEM and
+ * writes it (a 64-bit packed key) to the workspace; a second kernel takes the
+ * largest per row.  The fp32 logits are stored only if `logits` is non-NULL.
+ *   A: bf16 [M, K] row-major; B: bf16 [N, K] row-major (nn.Linear weight);
+ *   logits: fp32 [M, N] or NULL; row_req, row_pos, tokens: [M] as in
+ *   biv_gumbel_argmax; workspace: device memory of at least
+ *   biv_lm_head_gumbel_workspace_size(M, N, K) bytes, 16-B aligned, owned by
+ *   the caller and overwritten.
+ * Requires N % 8 == 0, K % 8 == 0, T >= 0 finite, 16-B aligned A, B, logits.
+ * Errors: BIV_ERR_SHAPE (also for a workspace that is too small),
+ * BIV_ERR_VALUE, BIV_ERR_NULL, BIV_ERR_ALIGN; nothing is launched then.   */
+size_t biv_lm_head_gumbel_workspace_size(int M, int N, int K);
+int biv_lm_head_gumbel(const void* A, const void* B, float* logits, int M, int N, int K,
+                       const uint32_t* row_req, const int32_t* row_pos, uint64_t seed, float temperature,
+                       int32_t* tokens, void* workspace, size_t ws_bytes, biv_stream_t stream);
+
+/* Gumbel top-k ([COUPLING]: the trick gives top-k sampling as it stands;
+ * Kool, van Hoof & Welling, "Stochastic Beams and Where to Find Them"):
+ * out[r * k + j] = the entry with the (j+1)-th largest key of row r, keys and
+ * order exactly as biv_gumbel_argmax (so column 0 is its token); the k
+ * entries are k draws without replacement from softmax(logits / T).
+ * logits: fp32 [R, ld]; row_req, row_pos: [R]; out: int32 [R, k].
+ * Requires 1 <= k <= min(64, V), V % 4 == 0, ld % 4 == 0, ld >= V,
+ * T >= 0 finite, 16-B aligned logits; otherwise BIV_ERR_SHAPE /
+ * BIV_ERR_VALUE / BIV_ERR_NULL / BIV_ERR_ALIGN and nothing is launched.   */
+int biv_gumbel_topk(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                    const int32_t* row_pos, uint64_t seed, float temperature, int k, int32_t* out,
+                    biv_stream_t stream);
+
+/* ----------------------------------------------------- n-gram drafter
+ * Training-free n-gram lookup drafter ([GUIDE]: a drafting method that finds
+ * and copies repeated fragments of the earlier text).  For request r with
+ * committed history hist[r * ld + 0 .. len[r]): the longest n in
+ * [n_min, n_max] whose last-n-token suffix occurs earlier with at least one
+ * token after it, at its most recent such occurrence p; the drafts copy the
+ * tokens from s = p + n on, continuing from the drafts themselves once the
+ * copy reaches the end of the history (LZ77-style), so periodic text is
+ * continued exactly.  No match: all K drafts are the last token (0 for an
+ * empty history).  draft_src[r] = s, or -1.
+ * hist: int32 [N, ld]; len: int32 [N] (each in [0, ld], else the device error
+ * word gets BIV_DEVERR_INDEX and the length is clamped); drafts: int32
+ * [N, K]; draft_src: int32 [N].  Requires 1 <= n_min <= n_max <= 64,
+ * 1 <= K <= 1024, ld >= 1.  The drafts never change what a coupled verify
+ * step commits, only how many tokens it can accept.                      */
+int biv_ngram_draft(const int32_t* hist, int N, long long ld, const int32_t* len, int n_max, int n_min,
+                    int K, int32_t* drafts, int32_t* draft_src, biv_stream_t stream);
+
 /* ----------------------------------------------------- coupled accept
  * [COUPLING] + [GUIDE] + [DVR] para 3: with shared noise the check compares
  * tokens only.  Row j of request r outputs target[r*K + j] = y_{j+1}, and

@@ -50,6 +50,10 @@ SIGNATURES = {
     "biv_kv_overwrite": (_I, [_P, _P, _P, _LL, _P, _LL, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "biv_gumbel_argmax": (_I, [_P, _I, _I, _LL, _P, _P, _U64, _F, _P, _P]),
     "biv_gumbel_noise": (_I, [_U64, _P, _P, _I, _I, _P, _P]),
+    "biv_gumbel_topk": (_I, [_P, _I, _I, _LL, _P, _P, _U64, _F, _I, _P, _P]),
+    "biv_ngram_draft": (_I, [_P, _I, _LL, _P, _I, _I, _I, _P, _P, _P]),
+    "biv_lm_head_gumbel_workspace_size": (_SZ, [_I, _I, _I]),
+    "biv_lm_head_gumbel": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _U64, _F, _P, _P, _SZ, _P]),
     "biv_gumbel_from_words": (_I, [_P, _LL, _P, _P]),
     "biv_verify_accept": (_I, [_P, _P, _P, _I, _I, _P, _P, _P]),
     "biv_gumbel_bucket_bounds": (_I, [_P]),
@@ -186,6 +190,38 @@ def biv_gumbel_argmax(logits, row_req, row_pos, seed: int, temperature: float, t
     _check("biv_gumbel_argmax", _load().biv_gumbel_argmax(
         _ptr(logits), R, V, logits.stride(0), _ptr(row_req), _ptr(row_pos), seed & 0xFFFFFFFFFFFFFFFF,
         float(temperature), _ptr(tokens), _stream(stream)))
+
+
+def biv_gumbel_topk(logits, row_req, row_pos, seed: int, temperature: float, out, V: int | None = None,
+                    stream=None) -> None:
+    R, ld = logits.shape
+    V = ld if V is None else V
+    k = out.shape[1]
+    _check("biv_gumbel_topk", _load().biv_gumbel_topk(
+        _ptr(logits), R, V, logits.stride(0), _ptr(row_req), _ptr(row_pos), seed & 0xFFFFFFFFFFFFFFFF,
+        float(temperature), k, _ptr(out), _stream(stream)))
+
+
+def biv_ngram_draft(hist, lengths, n_max: int, n_min: int, drafts, draft_src, stream=None) -> None:
+    N, ld = hist.shape
+    K = drafts.shape[1]
+    _check("biv_ngram_draft", _load().biv_ngram_draft(
+        _ptr(hist), N, hist.stride(0), _ptr(lengths), n_max, n_min, K, _ptr(drafts), _ptr(draft_src),
+        _stream(stream)))
+
+
+def biv_lm_head_gumbel_workspace_size(M: int, N: int, K: int) -> int:
+    return int(_load().biv_lm_head_gumbel_workspace_size(M, N, K))
+
+
+def biv_lm_head_gumbel(A, B, row_req, row_pos, seed: int, temperature: float, tokens, workspace, logits=None,
+                       stream=None) -> None:
+    M, K = A.shape
+    N = B.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("biv_lm_head_gumbel", _load().biv_lm_head_gumbel(
+        _ptr(A), _ptr(B), _ptr(logits) if logits is not None else None, M, N, K, _ptr(row_req), _ptr(row_pos),
+        seed & 0xFFFFFFFFFFFFFFFF, float(temperature), _ptr(tokens), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def biv_gumbel_noise(seed: int, row_req, row_pos, g, stream=None) -> None:

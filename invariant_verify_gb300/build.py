@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbiv.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["biv_api.cu", "biv_gemm.cu", "biv_select.cu", "biv_attn.cu", "biv_rowops.cu"]
+SOURCES = ["biv_api.cu", "biv_gemm.cu", "biv_select.cu", "biv_attn.cu", "biv_rowops.cu", "biv_draft.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -31,8 +31,10 @@
 // bounded (2 s); on time-out the kernel raises BIV_DEVERR_TIMEOUT, drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 #include <algorithm>
+#include <cmath>
 
 #include "biv_common.cuh"
+#include "biv_gumbel.cuh"
 
 namespace biv {
 namespace {
@@ -47,6 +49,7 @@ constexpr int kTailSlack = kBM * kRowBytes;   // the MMA may read 128 A rows pas
 constexpr int kMaxStages = 24;
 constexpr int kBarBytes = 512;
 constexpr int kWave = 152;                    // CTAs of one wave on a 152-SM part
+constexpr int kMaxSmem = 227 * 1024;          // opt-in shared memory per block
 
 struct GemmArgs {
     int M, N, K;
@@ -62,12 +65,227 @@ struct GemmArgs {
 
 inline int stage_bytes(int KS, int a_rows, int BN) { return KS * (a_rows + BN) * kRowBytes; }
 
+// Selection fused into the LM-head epilogue (EPI 3): every tile-row's Gumbel
+// winner, packed as (order(key) << 32 | ~v), goes to cand[row * n_tiles + n_blk].
+struct SelectArgs {
+    const uint32_t* row_req;
+    const int32_t* row_pos;
+    unsigned long long* cand;
+    uint32_t seed_lo, seed_hi;
+    float invT;
+    int greedy;
+};
+
+BIV_DEV uint32_t pick_word(const U4& w, uint32_t j) {
+    return j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
+}
+
+BIV_DEV void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Barrier over the 128 epilogue threads that also ANDs a flag across them, so
+// that a failed wait makes all of them leave the tile loop together.
+BIV_DEV bool epilogue_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
+}
+
+// Noise buckets (EPI 3): bucket b of a Philox word w is its top 12 bits,
+// b = w >> 20 (2^11 consecutive uniform indices).  The noise is a
+// non-decreasing function of the uniform index, so the noise at a bucket's
+// top word bounds every noise in the bucket.  T[b] is that bound for the top
+// 256 buckets (noise above 2.7, where the winners are decided) and the bound
+// of the enclosing 8-bit bucket (top byte b >> 4) below them.
+constexpr int kBucketBits = 12;
+constexpr int kBuckets = 1 << kBucketBits;
+constexpr int kNoiseTableBytes = kBuckets * 4 + 256 * 4;
+constexpr int kExactBuckets = 256;
+constexpr int kChunk = 32;                    // TMEM columns per load
+constexpr int kMaxChunks = 256 / kChunk;
+
+BIV_DEV void fill_noise_table(float* ntab, float* t8) {
+    const int e = static_cast<int>(threadIdx.x) - 64;            // 0..127
+    for (int b = e; b < 256; b += 128) t8[b] = gumbel_from_word((static_cast<uint32_t>(b) << 24) | 0x00ffffffu);
+    for (int b = e; b < kExactBuckets; b += 128) {
+        const uint32_t bb = static_cast<uint32_t>(kBuckets - kExactBuckets + b);
+        ntab[bb] = gumbel_from_word((bb << (32 - kBucketBits)) | ((1u << (32 - kBucketBits)) - 1u));
+    }
+    epilogue_bar();
+    for (int b = e; b < kBuckets - kExactBuckets; b += 128) ntab[b] = t8[b >> (kBucketBits - 8)];
+}
+
+// Buckets of one output tile, computed by the 128 epilogue threads while the
+// tile's MMAs run (the noise does not depend on the logits): for row r and
+// group gq (entries v0 = n0 + 4 gq .. v0 + 3) bk[r * BN/4 + gq] holds the four
+// 16-bit buckets, entry j in bits [16 j, 16 j + 16).
+BIV_DEV void tile_buckets(unsigned long long* bk, int rows, int BN, int n0, int N, int row0,
+                          const SelectArgs& sel) {
+    const int G4 = BN / 4;
+    const int total = rows * G4;
+    int r = 0, gq = static_cast<int>(threadIdx.x) - 64;
+    while (gq >= G4) { gq -= G4; ++r; }
+    for (int idx = static_cast<int>(threadIdx.x) - 64; idx < total; idx += 128) {
+        const uint32_t v0 = static_cast<uint32_t>(n0 + 4 * gq);
+        unsigned long long packed = 0;
+        if (v0 < static_cast<uint32_t>(N)) {
+            const uint32_t req = sel.row_req[row0 + r];
+            const uint32_t pos = static_cast<uint32_t>(sel.row_pos[row0 + r]) + 1u;
+            const U4 w = philox4x32_10(v0 >> 2, pos, req, 0u, sel.seed_lo, sel.seed_hi);
+            constexpr int sh = 32 - kBucketBits;
+            packed = static_cast<unsigned long long>((w.x >> sh) | ((w.y >> sh) << 16)) |
+                     (static_cast<unsigned long long>((w.z >> sh) | ((w.w >> sh) << 16)) << 32);
+        }
+        bk[idx] = packed;
+        gq += 128;
+        while (gq >= G4) { gq -= G4; ++r; }
+    }
+}
+
+// Bounds fl(fl(x * invT) + T[bucket]) of 32 entries of a row.
+BIV_DEV void chunk_bounds(const uint32_t (&r)[32], const unsigned long long* bk32, const float* ntab, float invT,
+                          float (&bound)[32]) {
+    const uint4 q0 = *reinterpret_cast<const uint4*>(bk32);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(bk32 + 2);
+    const uint4 q2 = *reinterpret_cast<const uint4*>(bk32 + 4);
+    const uint4 q3 = *reinterpret_cast<const uint4*>(bk32 + 6);
+    const uint32_t bw[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
+                             q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        const uint32_t b = (bw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+        bound[e] = __fadd_rn(__fmul_rn(__uint_as_float(r[e]), invT), ntab[b]);
+    }
+}
+
+// Winner of one tile-row of logits held in TMEM (columns [n0, n0 + BN) of
+// row `row`, valid below N; BN a multiple of 32), exactly as the selection
+// kernel defines it: key = fl(fl(x * invT) + g), largest key, lowest index
+// among equal keys, a NaN never beats a number.  Every entry has the bound
+// fl(fl(x * invT) + T[bucket]) >= its key (fp32 rounding is monotone).  Pass 1
+// finds the entry with the largest bound (its exact key is the lower bound
+// LB) and each 32-column chunk's largest bound; pass 2 revisits only chunks
+// whose largest bound reaches LB and evaluates the exact key only of their
+// entries whose bound does (the winner is among them).  T = 0 takes the
+// largest logit.  TMEM loads are warp-wide: a chunk is reloaded when any
+// lane of the warp needs it.  `bkrow` is this row's buckets, `cm` its chunk
+// maxima (shared memory).
+BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N, bool live, uint32_t req,
+                                           uint32_t pos, const SelectArgs& sel, const float* ntab,
+                                           const unsigned long long* bkrow, float* cm, float* logits_row) {
+    float bx = -INFINITY;       // largest logit (T = 0) or largest bound (T > 0)
+    float bxv = 0.0f;           // the logit of that entry
+    int bi = -1;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += kChunk) {
+        uint32_t r[32];
+        tmem_ld32_sync(taddr + static_cast<uint32_t>(c), r);
+        if (!live) continue;
+        const int lim = N - (n0 + c);          // entries of this chunk below N
+        if (sel.greedy) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float x = __uint_as_float(r[e]);
+                if (e < lim && (x > bx || (bi < 0 && x == x))) {
+                    bx = x;
+                    bi = n0 + c + e;
+                }
+            }
+        } else {
+            float bound[32];
+            chunk_bounds(r, bkrow + c / 4, ntab, sel.invT, bound);
+            float m = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                if (e < lim) {
+                    m = fmaxf(m, bound[e]);
+                    if (bound[e] > bx || (bi < 0 && bound[e] == bound[e])) {
+                        bx = bound[e];
+                        bxv = __uint_as_float(r[e]);
+                        bi = n0 + c + e;
+                    }
+                }
+            }
+            cm[c / kChunk] = m;
+        }
+        if (logits_row) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int col = n0 + c + h * 8;
+                if (col < N) {
+                    const uint32_t* v = r + h * 8;
+                    float4* dst = reinterpret_cast<float4*>(logits_row + col);
+                    dst[0] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                                         __uint_as_float(v[3]));
+                    dst[1] = make_float4(__uint_as_float(v[4]), __uint_as_float(v[5]), __uint_as_float(v[6]),
+                                         __uint_as_float(v[7]));
+                }
+            }
+        }
+    }
+    unsigned long long best = 0;
+    float thr = 0.0f;
+    const bool act = live && n0 < N && bi >= 0 && !sel.greedy;
+    if (live && n0 < N) {
+        if (bi < 0) {
+            best = static_cast<unsigned long long>(~static_cast<uint32_t>(n0));   // all NaN: key order 0
+        } else if (sel.greedy) {
+            best = pack_key(bx, static_cast<uint32_t>(bi));
+        } else {
+            // LB: the exact key of the entry with the largest bound.
+            const uint32_t v = static_cast<uint32_t>(bi);
+            const U4 w = philox4x32_10(v >> 2, pos, req, 0u, sel.seed_lo, sel.seed_hi);
+            thr = __fadd_rn(__fmul_rn(bxv, sel.invT), gumbel_from_word(pick_word(w, v & 3u)));
+            best = pack_key(thr, v);
+        }
+    }
+    if (sel.greedy) return best;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += kChunk) {
+        const bool need = act && cm[c / kChunk] >= thr;
+        if (!__any_sync(0xffffffffu, need)) continue;
+        uint32_t r[32];
+        tmem_ld32_sync(taddr + static_cast<uint32_t>(c), r);
+        if (!need) continue;
+        float bound[32];
+        chunk_bounds(r, bkrow + c / 4, ntab, sel.invT, bound);
+        const int lim = N - (n0 + c);
+        uint32_t hit = 0;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            if (e < lim && bound[e] >= thr && n0 + c + e != bi) hit |= 1u << e;
+        while (hit) {
+            const int e = __ffs(hit) - 1;
+            hit &= hit - 1;
+            const uint32_t v = static_cast<uint32_t>(n0 + c + e);
+            float xv = 0.0f;              // r[e] without a dynamic register index
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xv = (j == e) ? __uint_as_float(r[j]) : xv;
+            const U4 w = philox4x32_10(v >> 2, pos, req, 0u, sel.seed_lo, sel.seed_hi);
+            const float key = __fadd_rn(__fmul_rn(xv, sel.invT), gumbel_from_word(pick_word(w, v & 3u)));
+            const unsigned long long pk = pack_key(key, v);
+            if (pk > best) {
+                best = pk;
+                thr = key;
+            }
+        }
+    }
+    return best;
+}
+
 // EPI: 0 = bf16 C, 1 = fp32 C, 2 = SwiGLU of gate/up-interleaved B (bf16
-// activation [M, N/2]; see biv_gemm_swiglu).
+// activation [M, N/2]; see biv_gemm_swiglu), 3 = Gumbel-max selection of each
+// tile-row (optional fp32 C; see biv_lm_head_gumbel).
 template <int EPI>
 __global__ void __launch_bounds__(192, 1)
 gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     void* __restrict__ C, const GemmArgs g) {
+                     void* __restrict__ C, const GemmArgs g, const SelectArgs sel) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -82,6 +300,10 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     uint64_t* drain = tempty + 2;             // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* ntab = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + kBarBytes);   // EPI 3 only
+    float* t8 = ntab + kBuckets;                                                             // EPI 3 only
+    float* cmax = t8 + 256;                                                                  // EPI 3: [128][8]
+    unsigned long long* bk = reinterpret_cast<unsigned long long*>(cmax + kBM * kMaxChunks);  // EPI 3 only
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -218,17 +440,43 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     } else {
         // ------------------------------------------------------- epilogue
         const int q = warp & 3;                   // TMEM lane quarter of this warp
+        if constexpr (EPI == 3) {
+            // Largest noise of each bucket, while the first tile's data arrives.
+            if (!sel.greedy) fill_noise_table(ntab, t8);
+        }
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < n_work; t += gridDim.x) {
             const int n_blk = t / m_tiles;
             const int m_blk = t - n_blk * m_tiles;
-            if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err)) break;
+            bool ok;
+            if constexpr (EPI == 3) {
+                // This tile's noise buckets while its MMAs run; the vote is also
+                // the barrier that makes them (and the table) visible.
+                if (!sel.greedy)
+                    tile_buckets(bk, min(kBM, M - m_blk * kBM), BN, n_blk * BN, N, m_blk * kBM, sel);
+                ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err);
+                ok = epilogue_all(ok);
+            } else {
+                ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err);
+            }
+            if (!ok) break;
             tc_fence_after();
             const int row = m_blk * kBM + q * 32 + lane;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            if constexpr (EPI == 2) {
+            if constexpr (EPI == 3) {
+                const bool live = row < M;
+                const uint32_t req = live ? sel.row_req[row] : 0u;
+                const uint32_t pos = live ? static_cast<uint32_t>(sel.row_pos[row]) + 1u : 0u;
+                float* lrow = (C != nullptr && live) ? static_cast<float*>(C) + static_cast<long long>(row) * N
+                                                     : nullptr;
+                const unsigned long long best =
+                    tile_row_winner(taddr, BN, n_blk * BN, N, live, req, pos, sel, ntab, bk + (q * 32 + lane) * (BN / 4),
+                                    cmax + (q * 32 + lane) * kMaxChunks, lrow);
+                if (live) sel.cand[static_cast<long long>(row) * n_tiles + n_blk] = best;
+                epilogue_bar();       // every row is done with the buckets before the next tile's
+            } else if constexpr (EPI == 2) {
                 // Columns [32j, 32j + 16) of the tile are gate rows, [32j + 16, 32j + 32)
                 // the matching up rows: act = bf16(silu(bf16(g)) * bf16(u)).
                 const int F = N / 2;
@@ -351,7 +599,8 @@ uint32_t tmem_cols_for(int BN) {
 }
 
 template <int EPI>
-int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream) {
+int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream,
+                const SelectArgs& sel = SelectArgs{}) {
     GemmArgs g;
     g.M = M;
     g.N = N;
@@ -368,13 +617,17 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
     // k-block per stage and as many stages as fit.
     int ks = 1;
     const int tail = g.a_rows < kBM ? kTailSlack : 0;
+    // EPI 3 keeps the noise table, chunk maxima and one tile of noise buckets
+    // beside the ring, and takes all of the opt-in shared memory.
+    const int extra = EPI == 3 ? kNoiseTableBytes + kBM * kMaxChunks * 4 + g.a_rows * BN * 2 : 0;
+    const int ring = EPI == 3 ? kMaxSmem - 1024 - kBarBytes - extra : kRingBudget;
     if (g.three_d && g.a_rows < kBM) {
         const int per_kb = (g.a_rows + BN) * kRowBytes;
-        ks = std::max(1, (kRingBudget - tail) / (2 * per_kb));
+        ks = std::max(1, (ring - tail) / (2 * per_kb));
         ks = std::min(ks, std::min(g.KB, 256));
     }
     g.KS = ks;
-    g.stages = std::min(kMaxStages, std::max(1, (kRingBudget - tail) / stage_bytes(ks, g.a_rows, BN)));
+    g.stages = std::min(kMaxStages, std::max(1, (ring - tail) / stage_bytes(ks, g.a_rows, BN)));
     g.idesc = idesc_bf16_f32(kBM, BN);
     g.tmem_cols = tmem_cols_for(BN);
     CUtensorMap ta, tb;
@@ -382,20 +635,20 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
         set_cuda_error(cudaErrorInvalidValue);
         return BIV_ERR_CUDA;
     }
-    const int smem = 1024 + g.stages * stage_bytes(ks, g.a_rows, BN) + tail + kBarBytes;
+    const int smem = 1024 + g.stages * stage_bytes(ks, g.a_rows, BN) + tail + kBarBytes + extra;
     auto kern = gemm_nosplitk_kernel<EPI>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             1024 + kRingBudget + kBarBytes);
+                                             EPI == 3 ? kMaxSmem : 1024 + kRingBudget + kBarBytes);
         if (e != cudaSuccess) return cuda_status(e);
         configured_device = dev;
     }
     const long long work = static_cast<long long>((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<long long>(work, num_sms()));
-    return launch_pdl(kern, dim3(grid), dim3(192), static_cast<size_t>(smem), stream, ta, tb, C, g);
+    return launch_pdl(kern, dim3(grid), dim3(192), static_cast<size_t>(smem), stream, ta, tb, C, g, sel);
 }
 
 int check_gemm(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K) {
@@ -422,6 +675,21 @@ __global__ void swiglu_pack_kernel(const __nv_bfloat16* __restrict__ src, __nv_b
     const uint4* in = reinterpret_cast<const uint4*>(src + s * K);
     uint4* out = reinterpret_cast<uint4*>(dst + p * K);
     for (int c = threadIdx.x; c < K / 8; c += blockDim.x) out[c] = in[c];
+}
+
+// tokens[row] = the index of the largest of the row's tile winners (0 for a
+// row with no number); one warp per row.
+__global__ void tile_winners_kernel(const unsigned long long* __restrict__ cand, int M, int n_tiles,
+                                    int32_t* __restrict__ tokens) {
+    pdl_wait();
+    pdl_trigger();
+    const int row = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
+    const int lane = threadIdx.x & 31;
+    if (row >= M) return;
+    unsigned long long b = 0;
+    for (int t = lane; t < n_tiles; t += 32) b = umax64(b, cand[static_cast<long long>(row) * n_tiles + t]);
+    b = warp_max64(b);
+    if (lane == 0) tokens[row] = b ? static_cast<int32_t>(~static_cast<uint32_t>(b & 0xffffffffull)) : 0;
 }
 
 }  // namespace
@@ -488,4 +756,45 @@ extern "C" int biv_gemm_swiglu(const void* A, const void* B_packed, void* act, i
     if (st != BIV_OK || M == 0) return st;
     const int bn = static_cast<int>(std::min<long long>(256, ceil_div(biv_gemm_tile_n(M, N, K), 32) * 32));
     return launch_gemm<2>(A, B_packed, act, M, N, K, bn, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Tile width of the fused LM head: the GEMM's rounded up to a multiple of 32
+// (whole TMEM loads), at most 128 for full 128-row tiles (the buckets of one
+// tile stay within 32 KiB of shared memory).
+static int lm_head_tile_n(int M, int N, int K) {
+    const int bn = static_cast<int>(std::min<long long>(256, ceil_div(biv_gemm_tile_n(M, N, K), 32) * 32));
+    return M >= 128 ? std::min(bn, 128) : bn;
+}
+
+extern "C" size_t biv_lm_head_gumbel_workspace_size(int M, int N, int K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    const long long n_tiles = ceil_div(N, lm_head_tile_n(M, N, K));
+    return static_cast<size_t>(M) * static_cast<size_t>(n_tiles) * sizeof(unsigned long long);
+}
+
+extern "C" int biv_lm_head_gumbel(const void* A, const void* B, float* logits, int M, int N, int K,
+                                  const uint32_t* row_req, const int32_t* row_pos, uint64_t seed, float temperature,
+                                  int32_t* tokens, void* workspace, size_t ws_bytes, biv_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || N % 8 != 0 || K % 8 != 0) return BIV_ERR_SHAPE;
+    if (!(temperature >= 0.0f) || !(temperature < INFINITY)) return BIV_ERR_VALUE;
+    if (M == 0) return BIV_OK;
+    if (!A || !B || !row_req || !row_pos || !tokens || !workspace) return BIV_ERR_NULL;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(workspace) || (logits && !aligned16(logits)))
+        return BIV_ERR_ALIGN;
+    if (ws_bytes < biv_lm_head_gumbel_workspace_size(M, N, K)) return BIV_ERR_SHAPE;
+    const int bn = lm_head_tile_n(M, N, K);
+    const int n_tiles = static_cast<int>(ceil_div(N, bn));
+    SelectArgs sel;
+    sel.row_req = row_req;
+    sel.row_pos = row_pos;
+    sel.cand = static_cast<unsigned long long*>(workspace);
+    sel.seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
+    sel.seed_hi = static_cast<uint32_t>(seed >> 32);
+    sel.greedy = temperature == 0.0f;
+    sel.invT = sel.greedy ? 0.0f : 1.0f / temperature;    // fl(1/T), IEEE division on the host
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int st = launch_gemm<3>(A, B, logits, M, N, K, bn, s, sel);
+    if (st != BIV_OK) return st;
+    return launch_pdl(tile_winners_kernel, dim3((M + 7) / 8), dim3(256), 0, s,
+                      static_cast<const unsigned long long*>(workspace), M, n_tiles, tokens);
 }

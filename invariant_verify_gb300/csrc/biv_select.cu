@@ -38,6 +38,7 @@
 #include <cmath>
 
 #include "biv_common.cuh"
+#include "biv_gumbel.cuh"
 
 namespace biv {
 namespace {
@@ -73,88 +74,6 @@ const NoiseBounds& noise_bounds() {
         return t;
     }();
     return nb;
-}
-
-// ----------------------------------------------------------- Philox4x32-10
-struct U4 { uint32_t x, y, z, w; };
-
-BIV_DEV U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0, uint32_t k1) {
-#pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        if (round > 0) {
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
-        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
-        const uint32_t n0 = hi1 ^ c1 ^ k0;
-        const uint32_t n2 = hi0 ^ c3 ^ k1;
-        c0 = n0;
-        c1 = lo1;
-        c2 = n2;
-        c3 = lo0;
-    }
-    return U4{c0, c1, c2, c3};
-}
-
-// ------------------------------------------------------------- own log
-// ln x for positive normal x: x = m 2^e, m in [fl(sqrt2)/2, fl(sqrt2)),
-// f = m - 1, s = f / (2 + f), ln m = 2 s sum_{k<=6} s^2k / (2k+1) (Horner,
-// fma), ln x = e ln2_hi + (e ln2_lo + ln m), ln2_hi = 0x1.62e4p-1 (17 bits),
-// ln2_lo = fl(ln 2 - ln2_hi).  Every step is one correctly rounded IEEE op.
-BIV_DEV float own_log(float x) {
-    const uint32_t b = __float_as_uint(x);
-    int e = static_cast<int>((b >> 23) & 0xffu) - 127;
-    const uint32_t frac = b & 0x007fffffu;
-    uint32_t mb = frac | 0x3f800000u;
-    if (frac >= 0x003504f3u) {
-        mb -= 0x00800000u;
-        e += 1;
-    }
-    const float m = __uint_as_float(mb);
-    const float f = __fsub_rn(m, 1.0f);
-    const float t = __fadd_rn(2.0f, f);
-    const float s = __fdiv_rn(f, t);
-    const float z = __fmul_rn(s, s);
-    float p = __uint_as_float(0x3d9d89d9u);                 // 1/13
-    p = __fmaf_rn(p, z, __uint_as_float(0x3dba2e8cu));      // 1/11
-    p = __fmaf_rn(p, z, __uint_as_float(0x3de38e39u));      // 1/9
-    p = __fmaf_rn(p, z, __uint_as_float(0x3e124925u));      // 1/7
-    p = __fmaf_rn(p, z, __uint_as_float(0x3e4ccccdu));      // 1/5
-    p = __fmaf_rn(p, z, __uint_as_float(0x3eaaaaabu));      // 1/3
-    p = __fmaf_rn(p, z, 1.0f);                              // 1
-    const float r = __fadd_rn(s, s);
-    const float lnm = __fmul_rn(r, p);
-    const float ef = __int2float_rn(e);
-    const float u = __fmaf_rn(ef, __uint_as_float(0x35bfbe8eu), lnm);   // ln2_lo
-    return __fmaf_rn(ef, __uint_as_float(0x3f317200u), u);              // ln2_hi
-}
-
-// u = (2 (w >> 9) + 1) 2^-24 (exact), g = -ln(-ln u).
-BIV_DEV float gumbel_from_word(uint32_t w) {
-    const float u = __fmul_rn(__uint2float_rn(2u * (w >> 9) + 1u), 5.9604644775390625e-8f);
-    const float a = own_log(u);
-    return -own_log(-a);
-}
-
-// Total order used for selection: NaN lowest, -0 == +0, then by value.
-BIV_DEV uint32_t key_order(float k) {
-    if (k != k) return 0u;
-    if (k == 0.0f) k = 0.0f;
-    const uint32_t b = __float_as_uint(k);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-BIV_DEV unsigned long long pack_key(float k, uint32_t v) {
-    return (static_cast<unsigned long long>(key_order(k)) << 32) | static_cast<unsigned long long>(~v);
-}
-
-BIV_DEV unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
-
-BIV_DEV unsigned long long warp_max64(unsigned long long v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = umax64(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
 }
 
 // ------------------------------------------------------------- cluster PTX
@@ -389,6 +308,89 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
     }
 }
 
+// ---------------------------------------------------------- Gumbel top-k
+// [COUPLING]: the Gumbel-max trick gives top-k sampling as it stands -- the k
+// largest keys, in decreasing order, are k draws without replacement from
+// softmax(x / T) (Kool, van Hoof & Welling, "Stochastic Beams and Where to Find
+// Them").  Same keys and order as gumbel_argmax_kernel, so column 0 is its
+// token.  One CTA per row: every thread keeps its own k best packed keys
+// (sorted, in shared memory); an entry is evaluated exactly only if its bound
+// beats the thread's k-th best once the list is full (group bound with the
+// largest noise, then the bucket bound of its word); the CTA then takes the
+// k largest heads one by one.
+constexpr int kTopkThreads = 256;
+constexpr int kMaxTopk = 64;
+
+__global__ void __launch_bounds__(kTopkThreads)
+gumbel_topk_kernel(const float* __restrict__ logits, int V, long long ld, const uint32_t* __restrict__ row_req,
+                   const int32_t* __restrict__ row_pos, uint32_t seed_lo, uint32_t seed_hi, float invT, int greedy,
+                   int k, int32_t* __restrict__ out) {
+    extern __shared__ __align__(16) unsigned long long lists[];   // [k][kTopkThreads]
+    __shared__ float tab[256];                                   // largest noise of each top-byte bucket
+    __shared__ unsigned long long red[kTopkThreads / 32];
+    const int t = threadIdx.x;
+    tab[t] = gumbel_from_word((static_cast<uint32_t>(t) << 24) | 0x00ffffffu);
+    for (int i = 0; i < k; ++i) lists[i * kTopkThreads + t] = 0ull;
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    const long long row = blockIdx.x;
+    const float* x = logits + row * ld;
+    const uint32_t req = row_req[row];
+    const uint32_t pos = static_cast<uint32_t>(row_pos[row]) + 1u;
+    const float gmax = tab[255];
+    int count = 0;
+    unsigned long long kth = 0;          // the thread's k-th best once its list is full
+    auto insert = [&](unsigned long long pk) {
+        int i = count < k ? count : k - 1;
+        while (i > 0 && lists[(i - 1) * kTopkThreads + t] < pk) {
+            lists[i * kTopkThreads + t] = lists[(i - 1) * kTopkThreads + t];
+            --i;
+        }
+        lists[i * kTopkThreads + t] = pk;
+        if (count < k) ++count;
+        if (count == k) kth = lists[(k - 1) * kTopkThreads + t];
+    };
+    for (int gi = t; gi < V / 4; gi += kTopkThreads) {
+        const float4 v4 = *reinterpret_cast<const float4*>(x + 4 * gi);
+        const float e[4] = {v4.x, v4.y, v4.z, v4.w};
+        const uint32_t v0 = static_cast<uint32_t>(4 * gi);
+        if (greedy) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const unsigned long long pk = pack_key(e[j], v0 + j);
+                if (pk > kth) insert(pk);
+            }
+            continue;
+        }
+        const float m4 = fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3]));
+        const unsigned long long gb =
+            (static_cast<unsigned long long>(key_order(__fadd_rn(__fmul_rn(m4, invT), gmax))) << 32) |
+            static_cast<unsigned long long>(~v0);
+        if (count == k && gb <= kth) continue;
+        const U4 w = philox4x32_10(v0 >> 2, pos, req, 0u, seed_lo, seed_hi);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = __fmul_rn(e[j], invT);
+            const unsigned long long eb =
+                (static_cast<unsigned long long>(key_order(__fadd_rn(a, tab[ws[j] >> 24]))) << 32) |
+                static_cast<unsigned long long>(~(v0 + j));
+            if (count == k && eb <= kth) continue;
+            const unsigned long long pk = pack_key(__fadd_rn(a, gumbel_from_word(ws[j])), v0 + j);
+            if (pk > kth) insert(pk);
+        }
+    }
+    // Merge: k rounds of the largest head.
+    int head = 0;
+    for (int i = 0; i < k; ++i) {
+        const unsigned long long mine = head < count ? lists[head * kTopkThreads + t] : 0ull;
+        const unsigned long long best = block_max64(mine, red);
+        if (best != 0 && mine == best) ++head;
+        if (t == 0) out[row * k + i] = best ? static_cast<int32_t>(~static_cast<uint32_t>(best & 0xffffffffull)) : -1;
+    }
+}
+
 __global__ void gumbel_noise_kernel(uint32_t seed_lo, uint32_t seed_hi, const uint32_t* __restrict__ row_req,
                                     const int32_t* __restrict__ row_pos, int V, float* __restrict__ g) {
     pdl_wait();
@@ -481,6 +483,33 @@ extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld
                                        static_cast<uint32_t>(seed >> 32), invT, greedy, tokens, noise_bounds());
     if (e != cudaSuccess) return cuda_status(e);
     return launch_status();
+}
+
+extern "C" int biv_gumbel_topk(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                               const int32_t* row_pos, uint64_t seed, float temperature, int k, int32_t* out,
+                               biv_stream_t stream) {
+    if (R < 0 || V < 4 || ld < V || V % 4 != 0 || ld % 4 != 0) return BIV_ERR_SHAPE;
+    if (k < 1 || k > kMaxTopk || k > V) return BIV_ERR_SHAPE;
+    if (!(temperature >= 0.0f) || !(temperature < INFINITY)) return BIV_ERR_VALUE;
+    if (R == 0) return BIV_OK;
+    if (!logits || !row_req || !row_pos || !out) return BIV_ERR_NULL;
+    if (!aligned16(logits)) return BIV_ERR_ALIGN;
+    const int greedy = temperature == 0.0f;
+    const float invT = greedy ? 0.0f : 1.0f / temperature;   // fl(1/T), IEEE division on the host
+    const size_t smem = static_cast<size_t>(k) * kTopkThreads * sizeof(unsigned long long);
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(gumbel_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kMaxTopk * kTopkThreads * sizeof(unsigned long long)));
+        if (e != cudaSuccess) return cuda_status(e);
+        configured_device = dev;
+    }
+    return launch_pdl(gumbel_topk_kernel, dim3(static_cast<unsigned>(R)), dim3(kTopkThreads), smem,
+                      reinterpret_cast<cudaStream_t>(stream), logits, V, ld, row_req, row_pos,
+                      static_cast<uint32_t>(seed & 0xffffffffull), static_cast<uint32_t>(seed >> 32), invT, greedy, k,
+                      out);
 }
 
 extern "C" int biv_gumbel_noise(uint64_t seed, const uint32_t* row_req, const int32_t* row_pos, int R, int V,

@@ -37,11 +37,19 @@ class Window:
 
 
 class DecoderVerifier:
-    """Device-resident decoder verifier for windows of exactly W rows."""
+    """Device-resident decoder verifier for windows of exactly W rows.
+
+    ``fused_select``: the LM-head GEMM selects each row's token in its
+    epilogue (biv_lm_head_gumbel), bit-identical to the LM head followed by
+    biv_gumbel_argmax; ``keep_logits`` then decides whether the fp32 logits
+    are also stored (they always are without fusion)."""
 
     def __init__(self, cfg, weights: dict, caches: list, n_slots: int, max_len: int, W: int,
-                 rows_per_group: int, device="cuda", seed: int = 0x1234_5678_9ABC_DEF0):
+                 rows_per_group: int, device="cuda", seed: int = 0x1234_5678_9ABC_DEF0,
+                 fused_select: bool = True, keep_logits: bool = True):
         self.cfg, self.W, self.rpg = cfg, W, rows_per_group
+        self.fused_select = fused_select
+        self.keep_logits = keep_logits or not fused_select
         self.n_slots, self.max_len, self.seed = n_slots, max_len, seed
         dev = torch.device(device)
         self.w = {k: v.to(dev).contiguous() for k, v in weights.items()}
@@ -63,14 +71,18 @@ class DecoderVerifier:
         self.proj = torch.empty(W, d, **bf)
         self.act = torch.empty(W, F, **bf)
         self.hidden = torch.empty(W, d, **bf)
-        self.logits = torch.empty(W, cfg.vocab, device=dev, dtype=torch.float32)
+        self.logits = torch.empty(W, cfg.vocab, device=dev, dtype=torch.float32) if self.keep_logits else None
+        if fused_select:
+            n = B.biv_lm_head_gumbel_workspace_size(W, cfg.vocab, d)
+            self.select_ws = torch.empty(max(n, 16), device=dev, dtype=torch.uint8)
         self.target = torch.empty(W, device=dev, dtype=torch.int32)
         N = (W + rows_per_group - 1) // rows_per_group
         self.accept_len = torch.empty(N, device=dev, dtype=torch.int32)
         self.new_len = torch.empty(N, device=dev, dtype=torch.int32)
         ws = B.biv_decode_attn_workspace_size(W, Hq, max_len)
         self.workspace = torch.empty(max(ws, 16), device=dev, dtype=torch.uint8)
-        # embed+norm, per layer 9 kernels (attention is two), LM head, select, accept
+        # embed+norm, per layer 9 kernels (attention is two), LM head, select
+        # (or fused LM head + per-row winner), accept
         self.launches_per_step = 4 + cfg.layers * 9
 
     # -------------------------------------------------------------- stages
@@ -118,18 +130,37 @@ class DecoderVerifier:
             snap(f"l{l}.x_out", self.x)
         snap("hidden", self.hidden)
 
-    def lm_head(self) -> None:
-        B.biv_gemm_nosplitk(self.hidden, self.w["lm_head"], self.logits)
+    def lm_head(self, win: Window) -> None:
+        """fp32 logits (unfused), or logits (if kept) and the selected tokens."""
+        if self.fused_select:
+            B.biv_lm_head_gumbel(self.hidden, self.w["lm_head"], win.row_req, win.row_pos, self.seed,
+                                 self.cfg.temperature, self.target, self.select_ws, logits=self.logits)
+        else:
+            B.biv_gemm_nosplitk(self.hidden, self.w["lm_head"], self.logits)
 
     def select_and_accept(self, win: Window) -> None:
-        B.biv_gumbel_argmax(self.logits, win.row_req, win.row_pos, self.seed, self.cfg.temperature, self.target)
+        if not self.fused_select:
+            B.biv_gumbel_argmax(self.logits, win.row_req, win.row_pos, self.seed, self.cfg.temperature,
+                                self.target)
         N = self.accept_len.shape[0]
         B.biv_verify_accept(self.target, win.draft, win.p0, N, self.rpg, self.accept_len, self.new_len)
 
     def step(self, win: Window) -> None:
         self.forward(win)
-        self.lm_head()
+        self.lm_head(win)
         self.select_and_accept(win)
+
+    def prefill(self, win: Window) -> None:
+        """Deterministic prefill ([DVR] para 3: the verifier's fixed-shape
+        forward also produces the first token and the initial KV): the prompt
+        is one window of one request, rows at positions 0..P-1, so every row's
+        K/V lands in the cache and row P-1 selects the first new token
+        (``target[P-1]``).  No accept step: there are no drafts."""
+        self.forward(win)
+        self.lm_head(win)
+        if not self.fused_select:
+            B.biv_gumbel_argmax(self.logits, win.row_req, win.row_pos, self.seed, self.cfg.temperature,
+                                self.target)
 
     # -------------------------------------------------------- CUDA graphs
     def capture(self, win: Window, segments: bool = False):
@@ -145,7 +176,7 @@ class DecoderVerifier:
             self.step(win)            # warm-up outside capture (sets kernel attributes)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
-        parts = [(self.forward, (win,)), (self.lm_head, ()), (self.select_and_accept, (win,))]
+        parts = [(self.forward, (win,)), (self.lm_head, (win,)), (self.select_and_accept, (win,))]
         if not segments:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
@@ -158,6 +189,17 @@ class DecoderVerifier:
                 fn(*args)
             graphs.append(g)
         return graphs
+
+
+def prefill_window(prompt, slot: int, req_id: int, device="cuda") -> Window:
+    """The window of a prefill: one request, one row per prompt token at
+    positions 0..P-1 of cache slot ``slot``."""
+    prompt = torch.as_tensor(prompt, dtype=torch.int32)
+    P = prompt.numel()
+    win = make_window(1, P, prompt, torch.zeros(1, dtype=torch.int32), torch.tensor([req_id], dtype=torch.int32),
+                      torch.zeros(P, dtype=torch.int32), device=device)
+    win.row_slot.fill_(slot)
+    return win
 
 
 def make_window(N: int, K: int, tokens, p0, req_ids, draft, device="cuda") -> Window:

@@ -176,6 +176,46 @@ def test_fused_entry_validation(lib):
     assert r(*b) == OK
 
 
+def test_lm_head_gumbel_validation(lib):
+    f = lib.biv_lm_head_gumbel
+    ws = lib.biv_lm_head_gumbel_workspace_size(64, 32000, 1024)
+    assert ws == 64 * -(-32000 // lib.biv_gemm_tile_n(64, 32000, 1024)) * 8
+    assert lib.biv_lm_head_gumbel_workspace_size(0, 32000, 1024) == 0
+    base = [FAKE, FAKE, FAKE, 64, 32000, 1024, FAKE, FAKE, 1, 0.7, FAKE, FAKE, ws, None]
+    b = list(base); b[4] = 32004
+    assert f(*b) == SHAPE                       # N % 8
+    b = list(base); b[9] = -1.0
+    assert f(*b) == VALUE
+    b = list(base); b[9] = math.nan
+    assert f(*b) == VALUE
+    b = list(base); b[12] = ws - 8
+    assert f(*b) == SHAPE                       # workspace too small
+    b = list(base); b[11] = None
+    assert f(*b) == NULL
+    b = list(base); b[2] = MISALIGNED
+    assert f(*b) == ALIGN                       # logits, when given, aligned
+    b = list(base); b[3] = 0
+    assert f(*b) == OK
+
+
+def test_topk_and_ngram_validation(lib):
+    t = lib.biv_gumbel_topk
+    assert t(FAKE, 4, 32, 32, FAKE, FAKE, 1, 0.7, 0, FAKE, None) == SHAPE          # k < 1
+    assert t(FAKE, 4, 32, 32, FAKE, FAKE, 1, 0.7, 65, FAKE, None) == SHAPE         # k > 64
+    assert t(FAKE, 4, 8, 8, FAKE, FAKE, 1, 0.7, 9, FAKE, None) == SHAPE            # k > V
+    assert t(FAKE, 4, 30, 32, FAKE, FAKE, 1, 0.7, 4, FAKE, None) == SHAPE          # V % 4
+    assert t(FAKE, 4, 32, 32, FAKE, FAKE, 1, -1.0, 4, FAKE, None) == VALUE
+    assert t(FAKE, 0, 32, 32, FAKE, FAKE, 1, 0.7, 4, FAKE, None) == OK
+    assert t(MISALIGNED, 4, 32, 32, FAKE, FAKE, 1, 0.7, 4, FAKE, None) == ALIGN
+    n = lib.biv_ngram_draft
+    assert n(FAKE, 4, 100, FAKE, 3, 1, 0, FAKE, FAKE, None) == SHAPE               # K < 1
+    assert n(FAKE, 4, 100, FAKE, 3, 1, 1025, FAKE, FAKE, None) == SHAPE
+    assert n(FAKE, 4, 100, FAKE, 1, 2, 4, FAKE, FAKE, None) == VALUE               # n_max < n_min
+    assert n(FAKE, 4, 100, FAKE, 65, 1, 4, FAKE, FAKE, None) == VALUE
+    assert n(FAKE, 0, 100, FAKE, 3, 1, 4, FAKE, FAKE, None) == OK
+    assert n(None, 4, 100, FAKE, 3, 1, 4, FAKE, FAKE, None) == NULL
+
+
 def test_glue_validation(lib):
     assert lib.biv_embed(FAKE, FAKE, FAKE, 4, 100, 10, None) == SHAPE
     assert lib.biv_embed(FAKE, FAKE, FAKE, 0, 128, 10, None) == OK

@@ -112,7 +112,7 @@ def test_llama_layer_sampled_parity(llama):
     win = make_window(M, 1, toks, ctx, req, toks)
     tr = {}
     ver.forward(win, trace=tr)
-    ver.lm_head()
+    ver.lm_head(win)
     ver.select_and_accept(win)
     torch.cuda.synchronize()
     cpu = {k: v.cpu() for k, v in tr.items() if not k.endswith("kc") and not k.endswith("vc")}

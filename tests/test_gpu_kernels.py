@@ -407,3 +407,79 @@ def test_verify_accept_bit_exact():
         B.biv_verify_accept(i32(t), i32(d), i32(p0), N, K, L, nl)
         rL, rnl = oracle.verify_accept(t, d, p0, N, K)
         assert np.array_equal(L.cpu().numpy(), rL) and np.array_equal(nl.cpu().numpy(), rnl)
+
+
+# ------------------------------------------- LM head + selection, fused
+def _fused_vs_unfused(A, Bw, T, seed=SEED, write_logits=True):
+    M, K = A.shape
+    N = Bw.shape[0]
+    g = synth.generator(M * 31 + N)
+    req = torch.randint(0, 2 ** 31 - 1, (M,), generator=g, dtype=torch.int64).to(torch.int32).cuda()
+    pos = torch.randint(0, 100000, (M,), generator=g, dtype=torch.int64).to(torch.int32).cuda()
+    ref_logits = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    B.biv_gemm_nosplitk(A, Bw, ref_logits)
+    ref_tok = torch.full((M,), -5, dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax(ref_logits, req, pos, seed, T, ref_tok)
+    ws = torch.empty(max(16, B.biv_lm_head_gumbel_workspace_size(M, N, K)), dtype=torch.uint8, device="cuda")
+    tok = torch.full((M,), -9, dtype=torch.int32, device="cuda")
+    logits = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda") if write_logits else None
+    B.biv_lm_head_gumbel(A, Bw, req, pos, seed, T, tok, ws, logits=logits)
+    torch.cuda.synchronize()
+    assert torch.equal(tok, ref_tok)
+    if write_logits:
+        assert same_bits(logits, ref_logits)
+    return tok.cpu().numpy(), ref_logits.cpu(), req.cpu(), pos.cpu()
+
+
+@pytest.mark.parametrize("M,N,K,T,std", [
+    (64, 32000, 1024, 0.7, 0.02), (1, 2048, 256, 1.0, 1.0 / 16), (7, 4104, 192, 0.5, 0.1),
+    (130, 5000, 512, 0.7, 0.05), (64, 32000, 1024, 0.0, 0.02), (300, 2056, 136, 2.0, 0.2),
+    (16, 152064, 256, 0.7, 0.2)])
+def test_lm_head_gumbel_fused_bit_exact(M, N, K, T, std):
+    g = synth.generator(M + N + K)
+    A = synth.bf16_normal((M, K), 1.0, g).cuda()
+    Bw = synth.bf16_normal((N, K), std, g).cuda()
+    tok, logits, req, pos = _fused_vs_unfused(A, Bw, T, write_logits=(N * M <= 40_000_000))
+    ref = oracle.gumbel_argmax(logits, req, pos, SEED, T)
+    assert np.array_equal(tok, ref)
+
+
+def test_lm_head_gumbel_fused_peaked_ties_and_nan():
+    M, N, K = 48, 8192, 256
+    g = synth.generator(4242)
+    A = synth.bf16_normal((M, K), 1.0, g)
+    Bw = synth.bf16_normal((N, K), 0.05, g)
+    # peaked rows: B row 777 aligned with A row 0, row 5000 with A row 1
+    Bw[777] = A[0] * 0.5
+    Bw[5000] = A[1] * 0.5
+    # exact ties: two identical B rows give identical logits in every row
+    Bw[123] = Bw[4000]
+    Bw[6001] = Bw[6000]
+    # a NaN column (never wins) and an all-NaN row (selects 0)
+    Bw[2500, 3] = float("nan")
+    A[7] = float("nan")
+    A, Bw = A.cuda(), Bw.cuda()
+    for T in (0.0, 0.7, 1e-3):
+        tok, logits, req, pos = _fused_vs_unfused(A, Bw, T)
+        assert np.array_equal(tok, oracle.gumbel_argmax(logits, req, pos, SEED, T))
+        assert tok[7] == 0
+        assert np.all(tok != 2500)
+        if T == 0.0:
+            assert tok[0] == 777 and tok[1] == 5000
+
+
+def test_lm_head_gumbel_rows_invariant_across_M():
+    N, K = 32000, 1024
+    g = synth.generator(99)
+    A = synth.bf16_normal((256, K), 1.0, g).cuda()
+    Bw = synth.bf16_normal((N, K), 0.02, g).cuda()
+    req = torch.arange(256, dtype=torch.int32, device="cuda") * 3 + 1
+    pos = torch.arange(256, dtype=torch.int32, device="cuda") + 500
+    outs = {}
+    for M in (1, 8, 64, 129, 256):
+        ws = torch.empty(B.biv_lm_head_gumbel_workspace_size(M, N, K), dtype=torch.uint8, device="cuda")
+        tok = torch.empty(M, dtype=torch.int32, device="cuda")
+        B.biv_lm_head_gumbel(A[:M], Bw, req[:M], pos[:M], SEED, 0.7, tok, ws)
+        outs[M] = tok.cpu()
+    for M, t in outs.items():
+        assert torch.equal(t, outs[256][:M]), M

@@ -114,7 +114,7 @@ def test_decoder_stagewise_parity(dec2):
     ver = DecoderVerifier(cfg, w, caches, cfg.N, max_len, W, cfg.K)
     tr = {}
     ver.forward(win, trace=tr)
-    ver.lm_head()
+    ver.lm_head(win)
     ver.select_and_accept(win)
     torch.cuda.synchronize()
     slot, pos = win.row_slot.cpu().numpy(), win.row_pos.cpu().numpy()
