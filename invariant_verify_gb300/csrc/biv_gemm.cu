@@ -123,14 +123,15 @@ BIV_DEV void fill_noise_table(float* ntab, float* t8) {
 
 // Buckets of one output tile, computed by the 128 epilogue threads while the
 // tile's MMAs run (the noise does not depend on the logits): for row r and
-// group gq (entries v0 = n0 + 4 gq .. v0 + 3) bk[r * BN/4 + gq] holds the four
-// 16-bit buckets, entry j in bits [16 j, 16 j + 16).
-BIV_DEV void tile_buckets(unsigned long long* bk, int rows, int BN, int n0, int N, int row0,
+// group gq (entries v0 = n0 + 4 gq .. v0 + 3) bk[gq * RC + r] holds the four
+// 16-bit buckets, entry j in bits [16 j, 16 j + 16) (group-major, so the 32
+// rows of a warp read 32 consecutive words).
+BIV_DEV void tile_buckets(unsigned long long* bk, int RC, int rows, int BN, int n0, int N, int row0,
                           const SelectArgs& sel) {
     const int G4 = BN / 4;
     const int total = rows * G4;
-    int r = 0, gq = static_cast<int>(threadIdx.x) - 64;
-    while (gq >= G4) { gq -= G4; ++r; }
+    int gq = 0, r = static_cast<int>(threadIdx.x) - 64;
+    while (r >= rows) { r -= rows; ++gq; }
     for (int idx = static_cast<int>(threadIdx.x) - 64; idx < total; idx += 128) {
         const uint32_t v0 = static_cast<uint32_t>(n0 + 4 * gq);
         unsigned long long packed = 0;
@@ -142,26 +143,42 @@ BIV_DEV void tile_buckets(unsigned long long* bk, int rows, int BN, int n0, int 
             packed = static_cast<unsigned long long>((w.x >> sh) | ((w.y >> sh) << 16)) |
                      (static_cast<unsigned long long>((w.z >> sh) | ((w.w >> sh) << 16)) << 32);
         }
-        bk[idx] = packed;
-        gq += 128;
-        while (gq >= G4) { gq -= G4; ++r; }
+        bk[gq * RC + r] = packed;
+        r += 128;
+        while (r >= rows) { r -= rows; ++gq; }
     }
 }
 
-// Bounds fl(fl(x * invT) + T[bucket]) of 32 entries of a row.
-BIV_DEV void chunk_bounds(const uint32_t (&r)[32], const unsigned long long* bk32, const float* ntab, float invT,
-                          float (&bound)[32]) {
-    const uint4 q0 = *reinterpret_cast<const uint4*>(bk32);
-    const uint4 q1 = *reinterpret_cast<const uint4*>(bk32 + 2);
-    const uint4 q2 = *reinterpret_cast<const uint4*>(bk32 + 4);
-    const uint4 q3 = *reinterpret_cast<const uint4*>(bk32 + 6);
-    const uint32_t bw[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
-                             q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+// Bounds fl(fl(x * invT) + T[bucket]) of the 32 entries of a chunk of a row
+// (`bkc` = the row's bucket word of the chunk's first group, RC words apart).
+BIV_DEV void chunk_bounds(const uint32_t (&r)[32], const unsigned long long* bkc, int RC, const float* ntab,
+                          float invT, float (&bound)[32]) {
+    unsigned long long bw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bw[i] = bkc[i * RC];
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-        const uint32_t b = (bw[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+        const uint32_t b = static_cast<uint32_t>(bw[e >> 2] >> (16 * (e & 3))) & 0xffffu;
         bound[e] = __fadd_rn(__fmul_rn(__uint_as_float(r[e]), invT), ntab[b]);
     }
+}
+
+// Largest of 32 values (NaN only if all are NaN) and the lowest index holding
+// it (-1 if none): a tree, then a mask of the equal entries.
+BIV_DEV float chunk_max(const float (&v)[32], int lim, int& idx) {
+    float t[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) t[e] = e < lim ? v[e] : __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+    const float m = t[0];
+    uint32_t mask = 0;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) mask |= (e < lim && v[e] == m) ? (1u << e) : 0u;
+    idx = mask ? __ffs(mask) - 1 : -1;
+    return m;
 }
 
 // Winner of one tile-row of logits held in TMEM (columns [n0, n0 + BN) of
@@ -178,9 +195,10 @@ BIV_DEV void chunk_bounds(const uint32_t (&r)[32], const unsigned long long* bk3
 // maxima (shared memory).
 BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N, bool live, uint32_t req,
                                            uint32_t pos, const SelectArgs& sel, const float* ntab,
-                                           const unsigned long long* bkrow, float* cm, float* logits_row) {
+                                           const unsigned long long* bkrow, int RC, float* cm, float* logits_row) {
     float bx = -INFINITY;       // largest logit (T = 0) or largest bound (T > 0)
     float bxv = 0.0f;           // the logit of that entry
+    float bm2 = -INFINITY;      // the largest other bound of that entry's chunk
     int bi = -1;
 #pragma unroll 1
     for (int c = 0; c < BN; c += kChunk) {
@@ -188,31 +206,31 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
         tmem_ld32_sync(taddr + static_cast<uint32_t>(c), r);
         if (!live) continue;
         const int lim = N - (n0 + c);          // entries of this chunk below N
+        float val[32];
         if (sel.greedy) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float x = __uint_as_float(r[e]);
-                if (e < lim && (x > bx || (bi < 0 && x == x))) {
-                    bx = x;
-                    bi = n0 + c + e;
-                }
-            }
+            for (int e = 0; e < 32; ++e) val[e] = __uint_as_float(r[e]);
         } else {
-            float bound[32];
-            chunk_bounds(r, bkrow + c / 4, ntab, sel.invT, bound);
-            float m = -INFINITY;
+            chunk_bounds(r, bkrow + (c / 4) * RC, RC, ntab, sel.invT, val);
+        }
+        int e = -1;
+        const float m = chunk_max(val, lim, e);
+        if (!sel.greedy) cm[c / kChunk] = m;
+        if (e >= 0 && (m > bx || bi < 0)) {
+            bx = m;
+            bi = n0 + c + e;
+            float xv = 0.0f;          // r[e] without a dynamic register index
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                if (e < lim) {
-                    m = fmaxf(m, bound[e]);
-                    if (bound[e] > bx || (bi < 0 && bound[e] == bound[e])) {
-                        bx = bound[e];
-                        bxv = __uint_as_float(r[e]);
-                        bi = n0 + c + e;
-                    }
-                }
+            for (int j = 0; j < 32; ++j) xv = (j == e) ? __uint_as_float(r[j]) : xv;
+            bxv = xv;
+            if (!sel.greedy) {
+                // the chunk's largest bound apart from that entry (pass 2 revisits
+                // the chunk only if it reaches LB)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) val[j] = (j == e) ? __int_as_float(0x7fc00000) : val[j];
+                int e2;
+                bm2 = chunk_max(val, lim, e2);
             }
-            cm[c / kChunk] = m;
         }
         if (logits_row) {
 #pragma unroll
@@ -248,13 +266,14 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
     if (sel.greedy) return best;
 #pragma unroll 1
     for (int c = 0; c < BN; c += kChunk) {
-        const bool need = act && cm[c / kChunk] >= thr;
+        const bool own = bi >= n0 + c && bi < n0 + c + kChunk;
+        const bool need = act && (own ? bm2 : cm[c / kChunk]) >= thr;
         if (!__any_sync(0xffffffffu, need)) continue;
         uint32_t r[32];
         tmem_ld32_sync(taddr + static_cast<uint32_t>(c), r);
         if (!need) continue;
         float bound[32];
-        chunk_bounds(r, bkrow + c / 4, ntab, sel.invT, bound);
+        chunk_bounds(r, bkrow + (c / 4) * RC, RC, ntab, sel.invT, bound);
         const int lim = N - (n0 + c);
         uint32_t hit = 0;
 #pragma unroll
@@ -449,17 +468,16 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         for (int t = blockIdx.x; t < n_work; t += gridDim.x) {
             const int n_blk = t / m_tiles;
             const int m_blk = t - n_blk * m_tiles;
-            bool ok;
             if constexpr (EPI == 3) {
-                // This tile's noise buckets while its MMAs run; the vote is also
-                // the barrier that makes them (and the table) visible.
+                // This tile's noise buckets while its MMAs run; the vote below is
+                // also the barrier that makes them (and the table) visible.
                 if (!sel.greedy)
-                    tile_buckets(bk, min(kBM, M - m_blk * kBM), BN, n_blk * BN, N, m_blk * kBM, sel);
-                ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err);
-                ok = epilogue_all(ok);
-            } else {
-                ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err);
+                    tile_buckets(bk, g.a_rows, min(kBM, M - m_blk * kBM), BN, n_blk * BN, N, m_blk * kBM, sel);
             }
+            // One thread polls the accumulator barrier; the vote hands its
+            // outcome to the other 127 (no polling traffic beside the copies).
+            bool ok = threadIdx.x == 64 ? mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err) : true;
+            ok = epilogue_all(ok);
             if (!ok) break;
             tc_fence_after();
             const int row = m_blk * kBM + q * 32 + lane;
@@ -472,7 +490,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 float* lrow = (C != nullptr && live) ? static_cast<float*>(C) + static_cast<long long>(row) * N
                                                      : nullptr;
                 const unsigned long long best =
-                    tile_row_winner(taddr, BN, n_blk * BN, N, live, req, pos, sel, ntab, bk + (q * 32 + lane) * (BN / 4),
+                    tile_row_winner(taddr, BN, n_blk * BN, N, live, req, pos, sel, ntab, bk + (q * 32 + lane), g.a_rows,
                                     cmax + (q * 32 + lane) * kMaxChunks, lrow);
                 if (live) sel.cand[static_cast<long long>(row) * n_tiles + n_blk] = best;
                 epilogue_bar();       // every row is done with the buckets before the next tile's
