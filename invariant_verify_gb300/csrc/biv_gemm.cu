@@ -58,12 +58,26 @@ struct GemmArgs {
     int KB;          // k-blocks in K
     int three_d;     // 3-D tensor maps (K % 64 == 0), else 2-D with KS = 1
     int stages;      // ring depth
+    int first1;      // the first stage of every tile is one k-block (3-D maps tmA1/tmB1), so the
+                     // MMAs start as soon as it lands; the others hold KS k-blocks
+    int m64;         // one row tile of at most 64 rows: M = 64 MMAs
     int a_rows;      // rows of A copied per k-block (multiple of 8, <= 128)
     uint32_t idesc;  // tcgen05 instruction descriptor for M=128, N=BN
     uint32_t tmem_cols;
 };
 
 inline int stage_bytes(int KS, int a_rows, int BN) { return KS * (a_rows + BN) * kRowBytes; }
+
+// k-blocks [kb0, kb0 + nkb) of stage sb of a tile.
+BIV_DEV void stage_range(const GemmArgs& g, int sb, int& kb0, int& nkb) {
+    if (g.first1) {
+        kb0 = sb == 0 ? 0 : 1 + (sb - 1) * g.KS;
+        nkb = sb == 0 ? 1 : min(g.KS, g.KB - kb0);
+    } else {
+        kb0 = sb * g.KS;
+        nkb = min(g.KS, g.KB - kb0);
+    }
+}
 
 // Selection fused into the LM-head epilogue (EPI 3): every tile-row's Gumbel
 // winner, packed as (order(key) << 32 | ~v), goes to cand[row * n_tiles + n_blk].
@@ -304,6 +318,7 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
 template <int EPI>
 __global__ void __launch_bounds__(192, 1)
 gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                      void* __restrict__ C, const GemmArgs g, const SelectArgs sel) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -332,8 +347,9 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const int n_work = m_tiles * n_tiles;
     const int KB = g.KB;
     const int KS = g.KS;
-    const int n_stage_blocks = (KB + KS - 1) / KS;        // stages per tile
+    const int n_stage_blocks = g.first1 ? 1 + (KB - 1 + KS - 1) / KS : (KB + KS - 1) / KS;   // stages per tile
     const uint32_t tx_bytes = static_cast<uint32_t>(STAGE);
+    const uint32_t tx_bytes1 = static_cast<uint32_t>((g.a_rows + g.BN) * kRowBytes);     // a one-k-block stage
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -351,6 +367,10 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (g.first1) {
+            prefetch_tensormap(&tmA1);
+            prefetch_tensormap(&tmB1);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, g.tmem_cols);
@@ -381,11 +401,18 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                         break;
                     }
                     uint8_t* sa = tiles + stage * STAGE;
-                    mbar_arrive_expect_tx(&full[stage], tx_bytes);
-                    if (g.three_d) {
-                        tma_load_3d(sa, &tmA, &full[stage], 0, m_blk * kBM, sb * KS, pol_a);
-                        tma_load_3d(sa + A_BYTES, &tmB, &full[stage], 0, n_blk * BN, sb * KS, pol_b);
+                    int kb0, nkb;
+                    stage_range(g, sb, kb0, nkb);
+                    if (g.first1 && sb == 0) {
+                        mbar_arrive_expect_tx(&full[stage], tx_bytes1);
+                        tma_load_3d(sa, &tmA1, &full[stage], 0, m_blk * kBM, 0, pol_a);
+                        tma_load_3d(sa + A_BYTES, &tmB1, &full[stage], 0, n_blk * BN, 0, pol_b);
+                    } else if (g.three_d) {
+                        mbar_arrive_expect_tx(&full[stage], tx_bytes);
+                        tma_load_3d(sa, &tmA, &full[stage], 0, m_blk * kBM, kb0, pol_a);
+                        tma_load_3d(sa + A_BYTES, &tmB, &full[stage], 0, n_blk * BN, kb0, pol_b);
                     } else {
+                        mbar_arrive_expect_tx(&full[stage], tx_bytes);
                         tma_load_2d(sa, &tmA, &full[stage], sb * kBK, m_blk * kBM, pol_a);
                         tma_load_2d(sa + A_BYTES, &tmB, &full[stage], sb * kBK, n_blk * BN, pol_b);
                     }
@@ -427,9 +454,10 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(tiles + stage * STAGE);
                     const uint32_t b_addr = a_addr + static_cast<uint32_t>(A_BYTES);
-                    for (int j = 0; j < KS; ++j) {
-                        const int kb = sb * KS + j;
-                        if (kb >= KB) break;
+                    int kb0, nkb;
+                    stage_range(g, sb, kb0, nkb);
+                    for (int j = 0; j < nkb; ++j) {
+                        const int kb = kb0 + j;
                         const uint64_t a_desc = sw128_kmajor_desc(a_addr + static_cast<uint32_t>(j * g.a_rows * kRowBytes));
                         const uint64_t b_desc = sw128_kmajor_desc(b_addr + static_cast<uint32_t>(j * BN * kRowBytes));
 #pragma unroll
@@ -480,17 +508,20 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             ok = epilogue_all(ok);
             if (!ok) break;
             tc_fence_after();
-            const int row = m_blk * kBM + q * 32 + lane;
+            // M = 128 MMAs put tile row r in TMEM lane r; M = 64 MMAs put row r in
+            // lane 32 (r / 16) + r % 16, so each warp owns 16 rows in lanes 0..15.
+            const int rloc = g.m64 ? q * 16 + lane : q * 32 + lane;
+            const int row = m_blk * kBM + rloc;
+            const bool live = row < M && (!g.m64 || lane < 16);
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             if constexpr (EPI == 3) {
-                const bool live = row < M;
                 const uint32_t req = live ? sel.row_req[row] : 0u;
                 const uint32_t pos = live ? static_cast<uint32_t>(sel.row_pos[row]) + 1u : 0u;
                 float* lrow = (C != nullptr && live) ? static_cast<float*>(C) + static_cast<long long>(row) * N
                                                      : nullptr;
                 const unsigned long long best =
-                    tile_row_winner(taddr, BN, n_blk * BN, N, live, req, pos, sel, ntab, bk + (q * 32 + lane), g.a_rows,
+                    tile_row_winner(taddr, BN, n_blk * BN, N, live, req, pos, sel, ntab, bk + rloc, g.a_rows,
                                     cmax + (q * 32 + lane) * kMaxChunks, lrow);
                 if (live) sel.cand[static_cast<long long>(row) * n_tiles + n_blk] = best;
                 epilogue_bar();       // every row is done with the buckets before the next tile's
@@ -505,7 +536,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     tmem_ld16(taddr + static_cast<uint32_t>(c + 16), ur);
                     tmem_ld_wait();
                     const int col = n_blk * BN + c;
-                    if (row < M && col < N) {
+                    if (live && col < N) {
                         uint32_t o[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
@@ -523,7 +554,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 uint32_t r[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(c), r);
                 tmem_ld_wait();
-                if (row < M) {
+                if (live) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int col = n_blk * BN + c + h * 8;
@@ -645,11 +676,22 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
         ks = std::min(ks, std::min(g.KB, 256));
     }
     g.KS = ks;
+    // A one-k-block first stage pays off where the MMA chain, not the copy,
+    // sets the pace (narrow tiles with many k-blocks per stage).
+    g.first1 = (g.three_d && ks >= 4 && g.KB > 1) ? 1 : 0;
+    g.m64 = g.a_rows <= 64 ? 1 : 0;
     g.stages = std::min(kMaxStages, std::max(1, (ring - tail) / stage_bytes(ks, g.a_rows, BN)));
-    g.idesc = idesc_bf16_f32(kBM, BN);
+    g.idesc = idesc_bf16_f32(g.m64 ? 64 : kBM, BN);
     g.tmem_cols = tmem_cols_for(BN);
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ta1, tb1;
     if (!encode_kmajor(&ta, A, K, M, g.a_rows, ks, g.three_d) || !encode_kmajor(&tb, B, K, N, BN, ks, g.three_d)) {
+        set_cuda_error(cudaErrorInvalidValue);
+        return BIV_ERR_CUDA;
+    }
+    ta1 = ta;
+    tb1 = tb;
+    if (g.first1 &&
+        (!encode_kmajor(&ta1, A, K, M, g.a_rows, 1, true) || !encode_kmajor(&tb1, B, K, N, BN, 1, true))) {
         set_cuda_error(cudaErrorInvalidValue);
         return BIV_ERR_CUDA;
     }
@@ -666,7 +708,7 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
     }
     const long long work = static_cast<long long>((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<long long>(work, num_sms()));
-    return launch_pdl(kern, dim3(grid), dim3(192), static_cast<size_t>(smem), stream, ta, tb, C, g, sel);
+    return launch_pdl(kern, dim3(grid), dim3(192), static_cast<size_t>(smem), stream, ta, tb, ta1, tb1, C, g, sel);
 }
 
 int check_gemm(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K) {
