@@ -51,6 +51,8 @@ SIGNATURES = {
     "biv_gumbel_argmax": (_I, [_P, _I, _I, _LL, _P, _P, _U64, _F, _P, _P]),
     "biv_gumbel_noise": (_I, [_U64, _P, _P, _I, _I, _P, _P]),
     "biv_gumbel_topk": (_I, [_P, _I, _I, _LL, _P, _P, _U64, _F, _I, _P, _P]),
+    "biv_gemm_qkv_rope": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "biv_rope_pack_qkv_weights": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "biv_ngram_draft": (_I, [_P, _I, _LL, _P, _I, _I, _I, _P, _P, _P]),
     "biv_lm_head_gumbel_workspace_size": (_SZ, [_I, _I, _I]),
     "biv_lm_head_gumbel": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _U64, _F, _P, _P, _SZ, _P]),
@@ -190,6 +192,21 @@ def biv_gumbel_argmax(logits, row_req, row_pos, seed: int, temperature: float, t
     _check("biv_gumbel_argmax", _load().biv_gumbel_argmax(
         _ptr(logits), R, V, logits.stride(0), _ptr(row_req), _ptr(row_pos), seed & 0xFFFFFFFFFFFFFFFF,
         float(temperature), _ptr(tokens), _stream(stream)))
+
+
+def biv_rope_pack_qkv_weights(w_qkv, w_packed, Hq: int, Hkv: int, hd: int, stream=None) -> None:
+    _check("biv_rope_pack_qkv_weights", _load().biv_rope_pack_qkv_weights(
+        _ptr(w_qkv), _ptr(w_packed), Hq, Hkv, hd, w_qkv.shape[1], _stream(stream)))
+
+
+def biv_gemm_qkv_rope(A, B_packed, q_out, k_cache, v_cache, row_slot, row_pos, theta: float, K: int,
+                      rows_keep=None, qkv_out=None, stream=None) -> None:
+    W, d = A.shape
+    _, Hq, hd = q_out.shape
+    n_slots, Hkv, max_len, _ = k_cache.shape
+    _check("biv_gemm_qkv_rope", _load().biv_gemm_qkv_rope(
+        _ptr(A), _ptr(B_packed), _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(qkv_out), _ptr(row_slot),
+        _ptr(row_pos), _ptr(rows_keep), W, K, d, Hq, Hkv, hd, n_slots, max_len, float(theta), _stream(stream)))
 
 
 def biv_gumbel_topk(logits, row_req, row_pos, seed: int, temperature: float, out, V: int | None = None,

@@ -368,19 +368,6 @@ attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
 }
 
 // ------------------------------------------------------------------ RoPE
-// Rotate the pair (a, b) = (x[i], x[i + hd/2]) of one head by pos * theta^(-2i/hd);
-// one definition for the RoPE kernel and the fused RoPE + KV-write kernel.
-BIV_DEV void rope_rotate(float a, float b, int pos, int i, int hd, float theta, __nv_bfloat16* o1,
-                         __nv_bfloat16* o2) {
-    const float inv_freq = powf(theta, -2.0f * static_cast<float>(i) / static_cast<float>(hd));
-    const float ang = static_cast<float>(pos) * inv_freq;
-    float sn, cs;
-    sincosf(ang, &sn, &cs);
-    // explicit roundings: no fma contraction, the same bits in every caller
-    *o1 = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)));
-    *o2 = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, cs), __fmul_rn(a, sn)));
-}
-
 __global__ void rope_kernel(const __nv_bfloat16* __restrict__ qkv, __nv_bfloat16* __restrict__ q_out,
                             __nv_bfloat16* __restrict__ k_out, const int32_t* __restrict__ row_pos, int W,
                             int Hq, int Hkv, int hd, float theta) {

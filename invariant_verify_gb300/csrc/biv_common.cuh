@@ -318,4 +318,23 @@ BIV_DEV uint32_t swiglu_pack(uint32_t g2, uint32_t u2) {
     return pack_bf16x2(__fmul_rn(silu(bf16lo(g2)), bf16lo(u2)), __fmul_rn(silu(bf16hi(g2)), bf16hi(u2)));
 }
 
+// Rotate-half RoPE of the pair (a, b) = (x[i], x[i + hd/2]) of one head by the
+// angle pos * theta^(-2i/hd); one definition for every kernel that rotates
+// (the RoPE kernels and the QKV GEMM's RoPE epilogue), so all give the same
+// bits.  Explicit roundings: no fma contraction.
+BIV_DEV void rope_pair(float a, float b, int pos, int i, int hd, float theta, __nv_bfloat16& o1,
+                       __nv_bfloat16& o2) {
+    const float inv_freq = powf(theta, -2.0f * static_cast<float>(i) / static_cast<float>(hd));
+    const float ang = static_cast<float>(pos) * inv_freq;
+    float sn, cs;
+    sincosf(ang, &sn, &cs);
+    o1 = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)));
+    o2 = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, cs), __fmul_rn(a, sn)));
+}
+
+BIV_DEV void rope_rotate(float a, float b, int pos, int i, int hd, float theta, __nv_bfloat16* o1,
+                         __nv_bfloat16* o2) {
+    rope_pair(a, b, pos, i, hd, theta, *o1, *o2);
+}
+
 }  // namespace biv

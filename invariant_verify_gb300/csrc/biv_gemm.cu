@@ -119,6 +119,22 @@ BIV_DEV bool epilogue_all(bool v) {
 // of the enclosing 8-bit bucket (top byte b >> 4) below them.
 constexpr int kBucketBits = 12;
 constexpr int kBuckets = 1 << kBucketBits;
+// RoPE + KV-write epilogue (EPI 4) of the QKV projection: the weight rows are
+// rearranged (biv_rope_pack_qkv_weights) so that every 16 output columns of a
+// q or k head hold 8 rotation pairs -- dims i0..i0+7 then i0+hd/2..i0+hd/2+7,
+// i0 = 8 (col % hd / 16) -- and one thread rotates them from its own registers.
+struct RopeArgs {
+    __nv_bfloat16* q_out;      // [M, Hq, hd]
+    __nv_bfloat16* kc;         // [n_slots, Hkv, max_len, hd]
+    __nv_bfloat16* vc;
+    __nv_bfloat16* qkv_out;    // the unrotated projection in the original column order, or null
+    const int32_t* row_slot;
+    const int32_t* row_pos;
+    const int32_t* rows_keep;  // [M / K] or null
+    int Hq, Hkv, hd, n_slots, max_len, K;
+    float theta;
+};
+
 constexpr int kNoiseTableBytes = kBuckets * 4 + 256 * 4;
 constexpr int kExactBuckets = 256;
 constexpr int kChunk = 32;                    // TMEM columns per load
@@ -314,12 +330,13 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
 
 // EPI: 0 = bf16 C, 1 = fp32 C, 2 = SwiGLU of gate/up-interleaved B (bf16
 // activation [M, N/2]; see biv_gemm_swiglu), 3 = Gumbel-max selection of each
-// tile-row (optional fp32 C; see biv_lm_head_gumbel).
+// tile-row (optional fp32 C; see biv_lm_head_gumbel), 4 = RoPE of q and k, k
+// and v into the KV cache (see biv_gemm_qkv_rope).
 template <int EPI>
 __global__ void __launch_bounds__(192, 1)
 gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
-                     void* __restrict__ C, const GemmArgs g, const SelectArgs sel) {
+                     void* __restrict__ C, const GemmArgs g, const SelectArgs sel, const RopeArgs rp) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -525,6 +542,78 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                                     cmax + (q * 32 + lane) * kMaxChunks, lrow);
                 if (live) sel.cand[static_cast<long long>(row) * n_tiles + n_blk] = best;
                 epilogue_bar();       // every row is done with the buckets before the next tile's
+            } else if constexpr (EPI == 4) {
+                int slot = 0, pos = 0;
+                bool write_kv = false;
+                if (live) {
+                    pos = rp.row_pos[row];
+                    slot = rp.row_slot[row];
+                    const bool keep = !rp.rows_keep || (row % rp.K) < rp.rows_keep[row / rp.K];
+                    const bool cache_ok = slot >= 0 && slot < rp.n_slots && pos >= 0 && pos < rp.max_len;
+                    if (keep && !cache_ok) atomicOr(&g_gemm_err, BIV_DEVERR_INDEX);
+                    write_kv = keep && cache_ok;
+                }
+                const int hd = rp.hd, half = hd / 2;
+                const int qn = rp.Hq * hd, kn = rp.Hkv * hd;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + static_cast<uint32_t>(c), r);
+                    tmem_ld_wait();
+                    const int col = n_blk * BN + c;
+                    if (!live || col >= N) continue;
+                    uint32_t v2[8];                   // bf16 pairs, as the plain GEMM stores them
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        v2[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                    __nv_bfloat16* qkv_row =
+                        rp.qkv_out ? rp.qkv_out + static_cast<long long>(row) * (qn + 2 * kn) : nullptr;
+                    if (col < qn + kn) {
+                        const bool isq = col < qn;
+                        const int cc = isq ? col : col - qn;
+                        const int h = cc / hd, i0 = (cc % hd) / 16 * 8;
+                        uint32_t o1[4], o2[4];
+#pragma unroll
+                        for (int j = 0; j < 8; j += 2) {
+                            __nv_bfloat16 a0, a1, b0, b1;
+                            // pair j: column j (first half of the pairs) and column 8 + j
+                            rope_pair(bf16lo(v2[j / 2]), bf16lo(v2[4 + j / 2]), pos, i0 + j, hd, rp.theta, a0, b0);
+                            rope_pair(bf16hi(v2[j / 2]), bf16hi(v2[4 + j / 2]), pos, i0 + j + 1, hd, rp.theta, a1, b1);
+                            o1[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(a0)) |
+                                        (static_cast<uint32_t>(__bfloat16_as_ushort(a1)) << 16);
+                            o2[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) |
+                                        (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
+                        }
+                        __nv_bfloat16* dst = nullptr;
+                        if (isq)
+                            dst = rp.q_out + (static_cast<long long>(row) * rp.Hq + h) * hd;
+                        else if (write_kv)
+                            dst = rp.kc + ((static_cast<long long>(slot) * rp.Hkv + h) * rp.max_len + pos) * hd;
+                        if (dst) {
+                            *reinterpret_cast<uint4*>(dst + i0) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                            *reinterpret_cast<uint4*>(dst + half + i0) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                        }
+                        if (qkv_row) {
+                            __nv_bfloat16* b = qkv_row + (isq ? 0 : qn) + h * hd;
+                            *reinterpret_cast<uint4*>(b + i0) = make_uint4(v2[0], v2[1], v2[2], v2[3]);
+                            *reinterpret_cast<uint4*>(b + half + i0) = make_uint4(v2[4], v2[5], v2[6], v2[7]);
+                        }
+                    } else {
+                        const int cc = col - qn - kn;
+                        const int h = cc / hd, d0 = cc % hd;
+                        if (write_kv) {
+                            uint4* dst = reinterpret_cast<uint4*>(
+                                rp.vc + ((static_cast<long long>(slot) * rp.Hkv + h) * rp.max_len + pos) * hd + d0);
+                            dst[0] = make_uint4(v2[0], v2[1], v2[2], v2[3]);
+                            dst[1] = make_uint4(v2[4], v2[5], v2[6], v2[7]);
+                        }
+                        if (qkv_row) {
+                            uint4* b = reinterpret_cast<uint4*>(qkv_row + qn + kn + cc);
+                            b[0] = make_uint4(v2[0], v2[1], v2[2], v2[3]);
+                            b[1] = make_uint4(v2[4], v2[5], v2[6], v2[7]);
+                        }
+                    }
+                }
             } else if constexpr (EPI == 2) {
                 // Columns [32j, 32j + 16) of the tile are gate rows, [32j + 16, 32j + 32)
                 // the matching up rows: act = bf16(silu(bf16(g)) * bf16(u)).
@@ -649,7 +738,7 @@ uint32_t tmem_cols_for(int BN) {
 
 template <int EPI>
 int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream,
-                const SelectArgs& sel = SelectArgs{}) {
+                const SelectArgs& sel = SelectArgs{}, const RopeArgs& rp = RopeArgs{}) {
     GemmArgs g;
     g.M = M;
     g.N = N;
@@ -708,7 +797,8 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
     }
     const long long work = static_cast<long long>((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<long long>(work, num_sms()));
-    return launch_pdl(kern, dim3(grid), dim3(192), static_cast<size_t>(smem), stream, ta, tb, ta1, tb1, C, g, sel);
+    return launch_pdl(kern, dim3(grid), dim3(192), static_cast<size_t>(smem), stream, ta, tb, ta1, tb1, C, g, sel,
+                      rp);
 }
 
 int check_gemm(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K) {
@@ -732,6 +822,25 @@ __global__ void swiglu_pack_kernel(const __nv_bfloat16* __restrict__ src, __nv_b
     const long long p = blockIdx.x;
     const int j = static_cast<int>(p / 32), r = static_cast<int>(p % 32);
     const long long s = r < 16 ? 16LL * j + r : static_cast<long long>(F) + 16LL * j + (r - 16);
+    const uint4* in = reinterpret_cast<const uint4*>(src + s * K);
+    uint4* out = reinterpret_cast<uint4*>(dst + p * K);
+    for (int c = threadIdx.x; c < K / 8; c += blockDim.x) out[c] = in[c];
+}
+
+// Packed row p of the QKV weight: in the q and k heads, rows 16 g .. 16 g + 7 of
+// a head are its dims 8 g .. 8 g + 7 and rows 16 g + 8 .. 16 g + 15 its dims
+// hd/2 + 8 g .. hd/2 + 8 g + 7 (the RoPE partners); the v heads are unchanged.
+__global__ void rope_pack_kernel(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst, int Hq,
+                                 int Hkv, int hd, int K) {
+    pdl_wait();
+    const long long p = blockIdx.x;
+    long long s = p;
+    if (p < static_cast<long long>(Hq + Hkv) * hd) {
+        const int h = static_cast<int>(p / hd), j = static_cast<int>(p % hd);
+        const int gq = j / 16, e = j % 16;
+        const int dim = e < 8 ? 8 * gq + e : hd / 2 + 8 * gq + (e - 8);
+        s = static_cast<long long>(h) * hd + dim;
+    }
     const uint4* in = reinterpret_cast<const uint4*>(src + s * K);
     uint4* out = reinterpret_cast<uint4*>(dst + p * K);
     for (int c = threadIdx.x; c < K / 8; c += blockDim.x) out[c] = in[c];
@@ -857,4 +966,53 @@ extern "C" int biv_lm_head_gumbel(const void* A, const void* B, float* logits, i
     if (st != BIV_OK) return st;
     return launch_pdl(tile_winners_kernel, dim3((M + 7) / 8), dim3(256), 0, s,
                       static_cast<const unsigned long long*>(workspace), M, n_tiles, tokens);
+}
+
+extern "C" int biv_rope_pack_qkv_weights(const void* w_qkv, void* w_packed, int Hq, int Hkv, int hd, int K,
+                                         biv_stream_t stream) {
+    if (Hq <= 0 || Hkv <= 0 || hd <= 0 || hd % 16 != 0 || hd > 256 || K <= 0 || K % 8 != 0) return BIV_ERR_SHAPE;
+    if (!w_qkv || !w_packed) return BIV_ERR_NULL;
+    if (!aligned16(w_qkv) || !aligned16(w_packed)) return BIV_ERR_ALIGN;
+    if (w_qkv == w_packed) return BIV_ERR_VALUE;
+    // no early trigger: a GEMM launched right after reads these weights
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((Hq + 2 * Hkv) * hd));
+    cfg.blockDim = dim3(128);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    return cuda_status(cudaLaunchKernelEx(&cfg, rope_pack_kernel, static_cast<const __nv_bfloat16*>(w_qkv),
+                                          static_cast<__nv_bfloat16*>(w_packed), Hq, Hkv, hd, K));
+}
+
+extern "C" int biv_gemm_qkv_rope(const void* A, const void* B_packed, void* q_out, void* k_cache, void* v_cache,
+                                 void* qkv_out, const int32_t* row_slot, const int32_t* row_pos,
+                                 const int32_t* rows_keep, int W, int K, int d, int Hq, int Hkv, int hd, int n_slots,
+                                 int max_len, float theta, biv_stream_t stream) {
+    if (W < 0 || K < 1 || d <= 0 || d % 8 != 0 || Hq <= 0 || Hkv <= 0 || hd <= 0 || hd % 16 != 0 || hd > 256 ||
+        n_slots <= 0 || max_len <= 0 || Hq % Hkv != 0)
+        return BIV_ERR_SHAPE;
+    if (W % K != 0) return BIV_ERR_SHAPE;
+    if (!(theta > 1.0f) || !std::isfinite(theta)) return BIV_ERR_VALUE;
+    if (W == 0) return BIV_OK;
+    if (!A || !B_packed || !q_out || !k_cache || !v_cache || !row_slot || !row_pos) return BIV_ERR_NULL;
+    if (!aligned16(A) || !aligned16(B_packed) || !aligned16(q_out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (qkv_out && !aligned16(qkv_out)))
+        return BIV_ERR_ALIGN;
+    const int N = (Hq + 2 * Hkv) * hd;
+    RopeArgs rp;
+    rp.q_out = static_cast<__nv_bfloat16*>(q_out);
+    rp.kc = static_cast<__nv_bfloat16*>(k_cache);
+    rp.vc = static_cast<__nv_bfloat16*>(v_cache);
+    rp.qkv_out = static_cast<__nv_bfloat16*>(qkv_out);
+    rp.row_slot = row_slot;
+    rp.row_pos = row_pos;
+    rp.rows_keep = rows_keep;
+    rp.Hq = Hq;
+    rp.Hkv = Hkv;
+    rp.hd = hd;
+    rp.n_slots = n_slots;
+    rp.max_len = max_len;
+    rp.K = K;
+    rp.theta = theta;
+    return launch_gemm<4>(A, B_packed, nullptr, W, N, d, biv_gemm_tile_n(W, N, d), reinterpret_cast<cudaStream_t>(stream),
+                          SelectArgs{}, rp);
 }

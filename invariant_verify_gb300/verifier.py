@@ -59,6 +59,11 @@ class DecoderVerifier:
             packed = torch.empty_like(wgu)
             B.biv_swiglu_pack_weights(wgu, packed)
             self.w[f"l{l}.wgu_packed"] = packed
+            # QKV rows rearranged once for the RoPE/KV-write epilogue
+            wqkv = self.w[f"l{l}.wqkv"]
+            rpk = torch.empty_like(wqkv)
+            B.biv_rope_pack_qkv_weights(wqkv, rpk, cfg.Hq, cfg.Hkv, cfg.hd)
+            self.w[f"l{l}.wqkv_rope"] = rpk
         self.kc = [k.to(dev).contiguous() for k, _ in caches]
         self.vc = [v.to(dev).contiguous() for _, v in caches]
         d, Hq, Hkv, hd, F = cfg.d, cfg.Hq, cfg.Hkv, cfg.hd, cfg.ffn
@@ -81,9 +86,9 @@ class DecoderVerifier:
         self.new_len = torch.empty(N, device=dev, dtype=torch.int32)
         ws = B.biv_decode_attn_workspace_size(W, Hq, max_len)
         self.workspace = torch.empty(max(ws, 16), device=dev, dtype=torch.uint8)
-        # embed+norm, per layer 9 kernels (attention is two), LM head, select
-        # (or fused LM head + per-row winner), accept
-        self.launches_per_step = 4 + cfg.layers * 9
+        # embed+norm; per layer QKV+RoPE, attention (two), Wo, add+norm,
+        # gate/up+SwiGLU, down, add+norm; LM head + per-row winner; accept
+        self.launches_per_step = 4 + cfg.layers * 8
 
     # -------------------------------------------------------------- stages
     def forward(self, win: Window, trace: dict | None = None) -> None:
@@ -104,11 +109,13 @@ class DecoderVerifier:
         snap("x_in", self.x)
         for l in range(c.layers):
             snap(f"l{l}.h_attn", self.h)
-            B.biv_gemm_nosplitk(self.h, w[f"l{l}.wqkv"], self.qkv)
+            # QKV projection; its epilogue rotates q and k and writes k and v
+            # straight into the cache rows of the window (the unrotated
+            # projection is stored only when tracing)
+            B.biv_gemm_qkv_rope(self.h, w[f"l{l}.wqkv_rope"], self.q, self.kc[l], self.vc[l], win.row_slot,
+                                win.row_pos, c.rope_theta, K=self.rpg,
+                                qkv_out=self.qkv if trace is not None else None)
             snap(f"l{l}.qkv", self.qkv)
-            # RoPE on q and k; k and v go straight into the cache rows of the window
-            B.biv_rope_kv_write(self.qkv, self.q, self.kc[l], self.vc[l], win.row_slot, win.row_pos, Hq,
-                                c.rope_theta, K=self.rpg)
             snap(f"l{l}.q", self.q)
             if trace is not None:
                 trace[f"l{l}.kc"], trace[f"l{l}.vc"] = self.kc[l].clone(), self.vc[l].clone()

@@ -216,6 +216,26 @@ def test_topk_and_ngram_validation(lib):
     assert n(None, 4, 100, FAKE, 3, 1, 4, FAKE, FAKE, None) == NULL
 
 
+def test_qkv_rope_validation(lib):
+    f = lib.biv_gemm_qkv_rope
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, 64, 8, 1024, 8, 2, 128, 8, 4096, 10000.0, None]
+    b = list(base); b[14] = 120
+    assert f(*b) == SHAPE                       # hd % 16
+    b = list(base); b[9] = 60
+    assert f(*b) == SHAPE                       # W % K
+    b = list(base); b[17] = 1.0
+    assert f(*b) == VALUE
+    b = list(base); b[5] = MISALIGNED
+    assert f(*b) == ALIGN                       # qkv_out, when given
+    b = list(base); b[2] = None
+    assert f(*b) == NULL
+    b = list(base); b[9] = 0
+    assert f(*b) == OK
+    p = lib.biv_rope_pack_qkv_weights
+    assert p(FAKE, FAKE, 8, 2, 128, 1024, None) == VALUE          # in place
+    assert p(FAKE, FAKE + 4096, 8, 2, 72, 1024, None) == SHAPE
+
+
 def test_glue_validation(lib):
     assert lib.biv_embed(FAKE, FAKE, FAKE, 4, 100, 10, None) == SHAPE
     assert lib.biv_embed(FAKE, FAKE, FAKE, 0, 128, 10, None) == OK

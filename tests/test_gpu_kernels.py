@@ -276,6 +276,42 @@ def test_rope_kv_write_equals_rope_then_overwrite():
         assert same_bits(q2, q1) and same_bits(kc2, kc1) and same_bits(vc2, vc1)
 
 
+@pytest.mark.parametrize("W,K,d,Hq,Hkv,hd", [(12, 4, 256, 8, 2, 128), (64, 8, 1024, 8, 2, 128),
+                                             (130, 1, 512, 4, 4, 64), (256, 256, 4096, 32, 8, 128)])
+def test_qkv_rope_gemm_equals_gemm_then_rope_kv_write(W, K, d, Hq, Hkv, hd):
+    g = synth.generator(W + d)
+    n_slots, max_len = W // K + 1, 400
+    A = dev(synth.bf16_normal((W, d), 1.0, g))
+    wqkv = dev(synth.bf16_normal(((Hq + 2 * Hkv) * hd, d), 0.02, g))
+    kc = dev(synth.bf16_normal((n_slots, Hkv, max_len, hd), 1.0, g))
+    vc = dev(synth.bf16_normal((n_slots, Hkv, max_len, hd), 1.0, g))
+    groups = W // K
+    slot = i32(np.repeat(np.arange(groups)[::-1], K))
+    base = np.random.default_rng(W).integers(0, max_len - K, groups)
+    pos = i32(np.repeat(base, K) + np.tile(np.arange(K), groups))
+    packed = torch.empty_like(wqkv)
+    B.biv_rope_pack_qkv_weights(wqkv, packed, Hq, Hkv, hd)
+    keeps = [None] + ([i32(np.random.default_rng(1).integers(0, K + 1, groups))] if K > 1 else [])
+    for keep in keeps:
+        for theta in (10000.0, 500000.0):
+            qkv = torch.empty(W, (Hq + 2 * Hkv) * hd, dtype=torch.bfloat16, device="cuda")
+            B.biv_gemm_nosplitk(A, wqkv, qkv)
+            q1 = torch.empty(W, Hq, hd, dtype=torch.bfloat16, device="cuda")
+            kc1, vc1 = kc.clone(), vc.clone()
+            B.biv_rope_kv_write(qkv, q1, kc1, vc1, slot, pos, Hq, theta, K=K, rows_keep=keep)
+            q2 = torch.empty_like(q1)
+            kc2, vc2 = kc.clone(), vc.clone()
+            qkv2 = torch.empty_like(qkv)
+            B.biv_gemm_qkv_rope(A, packed, q2, kc2, vc2, slot, pos, theta, K=K, rows_keep=keep, qkv_out=qkv2)
+            assert same_bits(qkv2, qkv)
+            assert same_bits(q2, q1) and same_bits(kc2, kc1) and same_bits(vc2, vc1)
+            # without the projection copy
+            q3 = torch.empty_like(q1)
+            kc3, vc3 = kc.clone(), vc.clone()
+            B.biv_gemm_qkv_rope(A, packed, q3, kc3, vc3, slot, pos, theta, K=K, rows_keep=keep)
+            assert same_bits(q3, q1) and same_bits(kc3, kc1) and same_bits(vc3, vc1)
+
+
 def test_rope_parity():
     W, Hq, Hkv, hd = 10, 8, 2, 128
     g = synth.generator(31)
