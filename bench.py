@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--gemm-sweep", action="store_true",
                    help="instead of the step bench: no-split-K GEMM vs cuBLAS on the Llama-3-8B shapes")
+    p.add_argument("--kernel-sweep", action="store_true",
+                   help="instead of the step bench: HBM GB/s of RMSNorm, attention and Gumbel-max at full sizes")
     return p.parse_args()
 
 
@@ -372,6 +374,79 @@ def run_e2e(ver, win, graph, flush, cfg, K, world, device):
             "how": "pinned H2D of the window inputs + CUDA-graph step + D2H of accept_len/new_len/tokens + sync"}
 
 
+# ---------------------------------------------------------- kernel sweep
+def _time_us(fn, reps=20, warm=3):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+    for i in range(reps):
+        ev[2 * i].record()
+        fn()
+        ev[2 * i + 1].record()
+    torch.cuda.synchronize()
+    return statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(reps)) * 1e3
+
+
+def run_kernel_sweep(args):
+    """Achieved HBM bandwidth of the bandwidth-bound kernels at sizes far above
+    L2 (inputs > 129 MB, so no flush is needed between launches): RMSNorm over
+    [32768, 4096] bf16, the selection workload (fp32 [4096, 152064], T = 0.7),
+    and the fixed-split attention of the verifier sweep's largest window
+    (64 requests x 16 rows, Llama-3-8B heads, lognormal contexts)."""
+    from invariant_verify_gb300 import abi as B
+    from invariant_verify_gb300 import synth
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    hbm, _, src = peaks()
+    out = []
+
+    def line(kernel, workload, nbytes, us):
+        gbs = nbytes / us / 1e3
+        out.append({"kernel": kernel, "workload": workload, "algorithmic_bytes": int(nbytes), "us": round(us, 2),
+                    "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4), "peak_source": src})
+        print(json.dumps(out[-1]), flush=True)
+
+    rows, d = 32768, 4096
+    x = synth.bf16_normal_device((rows, d), 1.0, 7)
+    w = torch.ones(d, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    line("rmsnorm_kernel", "rmsnorm bf16 [32768, 4096]", 4 * rows * d + 2 * d,
+         _time_us(lambda: B.biv_rmsnorm(x, w, y, 1e-6)))
+    del x, y
+
+    cfg = synth.SELECT
+    logits = synth.select_logits_device(cfg)
+    R = cfg.R
+    req = (torch.arange(R, dtype=torch.int32, device="cuda") // cfg.K) * 7 + 3
+    pos = (torch.arange(R, dtype=torch.int32, device="cuda") % cfg.K) + 1000
+    tok = torch.empty(R, dtype=torch.int32, device="cuda")
+    line("gumbel_argmax_kernel", "select fp32 [4096, 152064], T=0.7, 90% peaked rows",
+         4 * R * cfg.vocab + 12 * R, _time_us(lambda: B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.7, tok)))
+    line("gumbel_argmax_kernel", "select fp32 [4096, 152064], T=0 (greedy)",
+         4 * R * cfg.vocab + 12 * R, _time_us(lambda: B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.0, tok)))
+    del logits
+
+    sw = synth.SWEEP
+    N, K = 64, 16
+    W = N * K
+    ctx = synth.context_lengths(sw, N, seed=123)
+    max_len = int(ctx.max()) + K + 8
+    kc, vc = synth.kv_cache_device(N, sw.Hkv, max_len, sw.hd, ctx, seed=124, layers=1)[0]
+    q = synth.bf16_normal_device((W, sw.Hq, sw.hd), 1.0, 125)
+    o = torch.empty_like(q)
+    slot = torch.arange(N, dtype=torch.int32, device="cuda").repeat_interleave(K)
+    rpos = (ctx.cuda().repeat_interleave(K) + torch.arange(K, device="cuda").repeat(N)).to(torch.int32)
+    ws = torch.empty(B.biv_decode_attn_workspace_size(W, sw.Hq, max_len), dtype=torch.uint8, device="cuda")
+    kv_bytes = sum(2 * 2 * sw.Hkv * (int(c) + K) * sw.hd for c in ctx)
+    line("attn_split_kernel + attn_combine_kernel",
+         f"attention W={W} (64 x 16), Hq 32 / Hkv 8, lognormal ctx mean {float(ctx.float().mean()):.0f}",
+         kv_bytes + 2 * 2 * W * sw.Hq * sw.hd,
+         _time_us(lambda: B.biv_decode_attn_fixedsplit(q, kc, vc, slot, rpos, o, K, ws)))
+    return out
+
+
 # ------------------------------------------------------------ GEMM sweep
 def run_gemm_sweep(args):
     """TFLOP/s and HBM GB/s of the no-split-K GEMM against cuBLAS's default
@@ -505,6 +580,8 @@ if __name__ == "__main__":
     a = parse()
     if a.gemm_sweep:
         run_gemm_sweep(a)
+    elif a.kernel_sweep:
+        run_kernel_sweep(a)
     elif a.impl == "reference":
         run_reference(a)
     else:

@@ -179,93 +179,107 @@ BIV_DEV void tile_buckets(unsigned long long* bk, int RC, int rows, int BN, int 
     }
 }
 
-// Bounds fl(fl(x * invT) + T[bucket]) of the 32 entries of a chunk of a row
-// (`bkc` = the row's bucket word of the chunk's first group, RC words apart).
-BIV_DEV void chunk_bounds(const uint32_t (&r)[32], const unsigned long long* bkc, int RC, const float* ntab,
-                          float invT, float (&bound)[32]) {
-    unsigned long long bw[8];
+// Bounds fl(fl(x * invT) + T[bucket]) of SEGW consecutive entries of a row
+// (`bkc` = the row's bucket word of their first group, RC words apart).
+template <int SEGW>
+BIV_DEV void seg_bounds(const uint32_t (&r)[SEGW], const unsigned long long* bkc, int RC, const float* ntab,
+                        float invT, float (&bound)[SEGW]) {
+    unsigned long long bw[SEGW / 4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) bw[i] = bkc[i * RC];
+    for (int i = 0; i < SEGW / 4; ++i) bw[i] = bkc[i * RC];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < SEGW; ++e) {
         const uint32_t b = static_cast<uint32_t>(bw[e >> 2] >> (16 * (e & 3))) & 0xffffu;
         bound[e] = __fadd_rn(__fmul_rn(__uint_as_float(r[e]), invT), ntab[b]);
     }
 }
 
-// Largest of 32 values (NaN only if all are NaN) and the lowest index holding
-// it (-1 if none): a tree, then a mask of the equal entries.
-BIV_DEV float chunk_max(const float (&v)[32], int lim, int& idx) {
-    float t[32];
+// Largest of SEGW values (NaN only if all are NaN) and the lowest index
+// holding it (-1 if none): a tree, then a mask of the equal entries.
+template <int SEGW>
+BIV_DEV float seg_max(const float (&v)[SEGW], int lim, int& idx) {
+    float t[SEGW];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) t[e] = e < lim ? v[e] : __int_as_float(0x7fc00000);
+    for (int e = 0; e < SEGW; ++e) t[e] = e < lim ? v[e] : __int_as_float(0x7fc00000);
 #pragma unroll
-    for (int w = 16; w > 0; w >>= 1)
+    for (int w = SEGW / 2; w > 0; w >>= 1)
 #pragma unroll
         for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
     const float m = t[0];
     uint32_t mask = 0;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) mask |= (e < lim && v[e] == m) ? (1u << e) : 0u;
+    for (int e = 0; e < SEGW; ++e) mask |= (e < lim && v[e] == m) ? (1u << e) : 0u;
     idx = mask ? __ffs(mask) - 1 : -1;
     return m;
 }
 
-// Winner of one tile-row of logits held in TMEM (columns [n0, n0 + BN) of
-// row `row`, valid below N; BN a multiple of 32), exactly as the selection
-// kernel defines it: key = fl(fl(x * invT) + g), largest key, lowest index
-// among equal keys, a NaN never beats a number.  Every entry has the bound
+template <int SEGW>
+BIV_DEV void seg_load(uint32_t taddr, uint32_t (&r)[SEGW]);
+template <>
+BIV_DEV void seg_load<32>(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32_sync(taddr, r); }
+template <>
+BIV_DEV void seg_load<16>(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16x2_sync(taddr, r); }
+
+// Winner of one tile-row of logits held in TMEM (columns [n0, n0 + BN) of a
+// row, valid below N; BN a multiple of 32), exactly as the selection kernel
+// defines it: key = fl(fl(x * invT) + g), largest key, lowest index among
+// equal keys, a NaN never beats a number.  The row is walked in 32-column
+// chunks; with SEGW = 32 one thread owns the row (M = 128 accumulators), with
+// SEGW = 16 two threads share it (M = 64 accumulators: threads l and l + 16
+// take columns [c, c + 16) and [c + 16, c + 32) of every chunk) and their
+// winners are merged at the end.  Every entry has the bound
 // fl(fl(x * invT) + T[bucket]) >= its key (fp32 rounding is monotone).  Pass 1
-// finds the entry with the largest bound (its exact key is the lower bound
-// LB) and each 32-column chunk's largest bound; pass 2 revisits only chunks
-// whose largest bound reaches LB and evaluates the exact key only of their
-// entries whose bound does (the winner is among them).  T = 0 takes the
-// largest logit.  TMEM loads are warp-wide: a chunk is reloaded when any
-// lane of the warp needs it.  `bkrow` is this row's buckets, `cm` its chunk
-// maxima (shared memory).
+// finds a thread's entry with the largest bound (its exact key is the lower
+// bound LB) and each chunk's largest bound; pass 2 revisits only chunks whose
+// largest bound reaches LB (for LB's own chunk, the largest other bound) and
+// evaluates the exact key only of entries whose bound does.  T = 0 takes the
+// largest logit.  TMEM loads are warp-wide: a chunk is reloaded when any lane
+// of the warp needs it.  `bkrow` is the row's buckets, `cm` the thread's
+// chunk maxima (shared memory).
+template <int SEGW>
 BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N, bool live, uint32_t req,
                                            uint32_t pos, const SelectArgs& sel, const float* ntab,
                                            const unsigned long long* bkrow, int RC, float* cm, float* logits_row) {
+    const int hoff = SEGW == 16 ? static_cast<int>(threadIdx.x & 16) : 0;
     float bx = -INFINITY;       // largest logit (T = 0) or largest bound (T > 0)
     float bxv = 0.0f;           // the logit of that entry
     float bm2 = -INFINITY;      // the largest other bound of that entry's chunk
     int bi = -1;
 #pragma unroll 1
     for (int c = 0; c < BN; c += kChunk) {
-        uint32_t r[32];
-        tmem_ld32_sync(taddr + static_cast<uint32_t>(c), r);
+        uint32_t r[SEGW];
+        seg_load<SEGW>(taddr + static_cast<uint32_t>(c), r);
         if (!live) continue;
-        const int lim = N - (n0 + c);          // entries of this chunk below N
-        float val[32];
+        const int col0 = n0 + c + hoff;
+        const int lim = N - col0;               // entries of this segment below N
+        float val[SEGW];
         if (sel.greedy) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) val[e] = __uint_as_float(r[e]);
+            for (int e = 0; e < SEGW; ++e) val[e] = __uint_as_float(r[e]);
         } else {
-            chunk_bounds(r, bkrow + (c / 4) * RC, RC, ntab, sel.invT, val);
+            seg_bounds<SEGW>(r, bkrow + ((c + hoff) / 4) * RC, RC, ntab, sel.invT, val);
         }
         int e = -1;
-        const float m = chunk_max(val, lim, e);
+        const float m = seg_max<SEGW>(val, lim, e);
         if (!sel.greedy) cm[c / kChunk] = m;
         if (e >= 0 && (m > bx || bi < 0)) {
             bx = m;
-            bi = n0 + c + e;
+            bi = col0 + e;
             float xv = 0.0f;          // r[e] without a dynamic register index
 #pragma unroll
-            for (int j = 0; j < 32; ++j) xv = (j == e) ? __uint_as_float(r[j]) : xv;
+            for (int j = 0; j < SEGW; ++j) xv = (j == e) ? __uint_as_float(r[j]) : xv;
             bxv = xv;
             if (!sel.greedy) {
-                // the chunk's largest bound apart from that entry (pass 2 revisits
-                // the chunk only if it reaches LB)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) val[j] = (j == e) ? __int_as_float(0x7fc00000) : val[j];
+                for (int j = 0; j < SEGW; ++j) val[j] = (j == e) ? __int_as_float(0x7fc00000) : val[j];
                 int e2;
-                bm2 = chunk_max(val, lim, e2);
+                bm2 = seg_max<SEGW>(val, lim, e2);
             }
         }
         if (logits_row) {
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int col = n0 + c + h * 8;
+            for (int h = 0; h < SEGW / 8; ++h) {
+                const int col = col0 + h * 8;
                 if (col < N) {
                     const uint32_t* v = r + h * 8;
                     float4* dst = reinterpret_cast<float4*>(logits_row + col);
@@ -279,10 +293,10 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
     }
     unsigned long long best = 0;
     float thr = 0.0f;
-    const bool act = live && n0 < N && bi >= 0 && !sel.greedy;
-    if (live && n0 < N) {
+    const bool act = live && n0 + hoff < N && bi >= 0 && !sel.greedy;
+    if (live && n0 + hoff < N) {
         if (bi < 0) {
-            best = static_cast<unsigned long long>(~static_cast<uint32_t>(n0));   // all NaN: key order 0
+            best = static_cast<unsigned long long>(~static_cast<uint32_t>(n0 + hoff));   // all NaN: key order 0
         } else if (sel.greedy) {
             best = pack_key(bx, static_cast<uint32_t>(bi));
         } else {
@@ -293,37 +307,43 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
             best = pack_key(thr, v);
         }
     }
-    if (sel.greedy) return best;
+    if (!sel.greedy) {
 #pragma unroll 1
-    for (int c = 0; c < BN; c += kChunk) {
-        const bool own = bi >= n0 + c && bi < n0 + c + kChunk;
-        const bool need = act && (own ? bm2 : cm[c / kChunk]) >= thr;
-        if (!__any_sync(0xffffffffu, need)) continue;
-        uint32_t r[32];
-        tmem_ld32_sync(taddr + static_cast<uint32_t>(c), r);
-        if (!need) continue;
-        float bound[32];
-        chunk_bounds(r, bkrow + (c / 4) * RC, RC, ntab, sel.invT, bound);
-        const int lim = N - (n0 + c);
-        uint32_t hit = 0;
+        for (int c = 0; c < BN; c += kChunk) {
+            const int col0 = n0 + c + hoff;
+            const bool own = bi >= col0 && bi < col0 + SEGW;
+            const bool need = act && (own ? bm2 : cm[c / kChunk]) >= thr;
+            if (!__any_sync(0xffffffffu, need)) continue;
+            uint32_t r[SEGW];
+            seg_load<SEGW>(taddr + static_cast<uint32_t>(c), r);
+            if (!need) continue;
+            float bound[SEGW];
+            seg_bounds<SEGW>(r, bkrow + ((c + hoff) / 4) * RC, RC, ntab, sel.invT, bound);
+            const int lim = N - col0;
+            uint32_t hit = 0;
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-            if (e < lim && bound[e] >= thr && n0 + c + e != bi) hit |= 1u << e;
-        while (hit) {
-            const int e = __ffs(hit) - 1;
-            hit &= hit - 1;
-            const uint32_t v = static_cast<uint32_t>(n0 + c + e);
-            float xv = 0.0f;              // r[e] without a dynamic register index
+            for (int e = 0; e < SEGW; ++e)
+                if (e < lim && bound[e] >= thr && col0 + e != bi) hit |= 1u << e;
+            while (hit) {
+                const int e = __ffs(hit) - 1;
+                hit &= hit - 1;
+                const uint32_t v = static_cast<uint32_t>(col0 + e);
+                float xv = 0.0f;          // r[e] without a dynamic register index
 #pragma unroll
-            for (int j = 0; j < 32; ++j) xv = (j == e) ? __uint_as_float(r[j]) : xv;
-            const U4 w = philox4x32_10(v >> 2, pos, req, 0u, sel.seed_lo, sel.seed_hi);
-            const float key = __fadd_rn(__fmul_rn(xv, sel.invT), gumbel_from_word(pick_word(w, v & 3u)));
-            const unsigned long long pk = pack_key(key, v);
-            if (pk > best) {
-                best = pk;
-                thr = key;
+                for (int j = 0; j < SEGW; ++j) xv = (j == e) ? __uint_as_float(r[j]) : xv;
+                const U4 w = philox4x32_10(v >> 2, pos, req, 0u, sel.seed_lo, sel.seed_hi);
+                const float key = __fadd_rn(__fmul_rn(xv, sel.invT), gumbel_from_word(pick_word(w, v & 3u)));
+                const unsigned long long pk = pack_key(key, v);
+                if (pk > best) {
+                    best = pk;
+                    thr = key;
+                }
             }
         }
+    }
+    if (SEGW == 16) {             // the two threads of the row: the larger packed key
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, 16);
+        best = umax64(best, other);
     }
     return best;
 }
@@ -533,14 +553,21 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             if constexpr (EPI == 3) {
-                const uint32_t req = live ? sel.row_req[row] : 0u;
-                const uint32_t pos = live ? static_cast<uint32_t>(sel.row_pos[row]) + 1u : 0u;
-                float* lrow = (C != nullptr && live) ? static_cast<float*>(C) + static_cast<long long>(row) * N
-                                                     : nullptr;
+                // with M = 64 accumulators the two half-warps share each row
+                const int srloc = g.m64 ? q * 16 + (lane & 15) : rloc;
+                const int srow = m_blk * kBM + srloc;
+                const bool slive = srow < M;
+                const uint32_t req = slive ? sel.row_req[srow] : 0u;
+                const uint32_t pos = slive ? static_cast<uint32_t>(sel.row_pos[srow]) + 1u : 0u;
+                float* lrow = (C != nullptr && slive) ? static_cast<float*>(C) + static_cast<long long>(srow) * N
+                                                      : nullptr;
+                float* cmt = cmax + (q * 32 + lane) * kMaxChunks;
                 const unsigned long long best =
-                    tile_row_winner(taddr, BN, n_blk * BN, N, live, req, pos, sel, ntab, bk + rloc, g.a_rows,
-                                    cmax + (q * 32 + lane) * kMaxChunks, lrow);
-                if (live) sel.cand[static_cast<long long>(row) * n_tiles + n_blk] = best;
+                    g.m64 ? tile_row_winner<16>(taddr, BN, n_blk * BN, N, slive, req, pos, sel, ntab, bk + srloc,
+                                                g.a_rows, cmt, lrow)
+                          : tile_row_winner<32>(taddr, BN, n_blk * BN, N, slive, req, pos, sel, ntab, bk + srloc,
+                                                g.a_rows, cmt, lrow);
+                if (live) sel.cand[static_cast<long long>(srow) * n_tiles + n_blk] = best;
                 epilogue_bar();       // every row is done with the buckets before the next tile's
             } else if constexpr (EPI == 4) {
                 int slot = 0, pos = 0;
@@ -684,24 +711,6 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
 }
 
 // --------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
 // Row-major bf16 [rows, cols] viewed by TMA with 128-B swizzle.  2-D: boxes of
 // [box_rows x 64].  3-D (cols % 64 == 0): the view [cols/64][rows][64] (k-block,
 // row, column; strides 128 B and cols*2 B), boxes of [ks][box_rows][64], so

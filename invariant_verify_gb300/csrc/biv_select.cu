@@ -28,9 +28,15 @@
 //      it); the best-bounded entry is evaluated exactly and the larger of its
 //      key and LB becomes LB2; only entries whose bound reaches LB2 get their
 //      two logs.
-// No bound crosses CTAs, so the cluster meets only once, at start-up (every
-// CTA's barriers exist before any remote arrive); at the end each CTA stores
-// its winner into rank 0's shared memory and arrives on rank 0's barrier.
+// Each CTA also raises its peers' copies of a shared bound (a remote atomic
+// max in DSMEM) to every real key it evaluates for LB and LB2, and prunes
+// against the larger of its own and the shared one -- on a peaked row the
+// slice holding the peak prunes every other slice.  The cluster meets at
+// start-up (every CTA's barriers exist before any remote operation), and every
+// CTA arrives on a cluster barrier after its last remote bound and waits on
+// it before leaving, so no CTA exits while a peer may still write to it.  At
+// the end each CTA stores its winner into rank 0's shared memory and arrives
+// on rank 0's barrier.
 // Rounding is monotone, so no dropped entry can reach the bound.  The winner
 // is the maximum of a 64-bit packed value (order(key) << 32 | ~v), which puts
 // larger keys first and lower indices first among equal keys, so any
@@ -83,6 +89,9 @@ BIV_DEV uint32_t cluster_rank() {
     return r;
 }
 
+BIV_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+BIV_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 BIV_DEV void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -122,6 +131,13 @@ BIV_DEV void push_to_rank(unsigned long long* slot, uint64_t* bar, uint32_t rank
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rb) : "memory");
 }
 
+// Raise every cluster CTA's copy of `slot` to at least v (relaxed remote max).
+BIV_DEV void share_bound(unsigned long long* slot, unsigned long long v) {
+#pragma unroll 1
+    for (uint32_t r = 0; r < kClusterSize; ++r)
+        asm volatile("red.shared::cluster.max.u64 [%0], %1;" ::"r"(dsmem_addr(slot, r)), "l"(v) : "memory");
+}
+
 BIV_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -153,6 +169,7 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
     __shared__ unsigned long long inbox[kClusterSize];         // rank 0: slice winners
     __shared__ unsigned long long red[kSelThreads / 32];
     __shared__ unsigned long long bcast;
+    __shared__ unsigned long long lb_all;                      // largest real key any CTA of the row has found
     __shared__ float gtab[256];                                // noise bound of each uniform bucket
     __shared__ int abort_flag;
 
@@ -160,6 +177,7 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
     const uint32_t rank = cluster_rank();
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        lb_all = 0;
         for (int p = 0; p < kPieces; ++p) mbar_init(&bars[p], 1);
         mbar_init(&inbox_bar, kClusterSize);
         fence_mbar_init();
@@ -226,10 +244,14 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
                 lb = pack_key(__fadd_rn(__fmul_rn(xs[v - begin], invT), gumbel_from_word(words[v & 3u])), v);
             }
             bcast = lb;
+            share_bound(&lb_all, lb);
         }
         __syncthreads();
         const unsigned long long lb = bcast;
         const uint32_t lb_order = static_cast<uint32_t>(lb >> 32);
+        // Any real key of the row bounds its winner, so the bound used below is
+        // the larger of this slice's and whatever the other slices have sent.
+        const volatile unsigned long long* lbv = &lb_all;
 
         // Pass A: level-1 pruning, then Philox words and level-2 bounds.
         const int n_groups = count / 4;
@@ -238,7 +260,8 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
             const float4 v4 = *reinterpret_cast<const float4*>(xs + 4 * gi);
             const float m4 = fmaxf(fmaxf(v4.x, v4.y), fmaxf(v4.z, v4.w));
             uint32_t g_ord = 0;
-            if (key_order(__fadd_rn(__fmul_rn(m4, invT), kNoiseBound)) >= lb_order) {
+            const uint32_t lbo = max(lb_order, static_cast<uint32_t>(*lbv >> 32));
+            if (key_order(__fadd_rn(__fmul_rn(m4, invT), kNoiseBound)) >= lbo) {
                 const uint32_t v0 = static_cast<uint32_t>(begin + 4 * gi);
                 const U4 w = philox4x32_10(v0 >> 2, pos, req, 0u, seed_lo, seed_hi);
                 const float e[4] = {v4.x, v4.y, v4.z, v4.w};
@@ -265,15 +288,18 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
                                                        gumbel_from_word(words[v & 3u])), v));
             }
             bcast = cand;
+            share_bound(&lb_all, cand);
         }
         __syncthreads();
+        cluster_arrive();         // this CTA sends no more bounds
         const unsigned long long lb2 = bcast;
         const uint32_t lb2_order = static_cast<uint32_t>(lb2 >> 32);
 
         // Pass B: exact keys only where the level-2 bound reaches LB2.
         best = lb2;
         for (int gi = threadIdx.x; gi < n_groups; gi += kSelThreads) {
-            if (gub[gi] < lb2_order) continue;
+            const uint32_t lbo = max(lb2_order, static_cast<uint32_t>(*lbv >> 32));
+            if (gub[gi] < lbo) continue;
             const float4 v4 = *reinterpret_cast<const float4*>(xs + 4 * gi);
             const uint32_t v0 = static_cast<uint32_t>(begin + 4 * gi);
             const U4 w = philox4x32_10(v0 >> 2, pos, req, 0u, seed_lo, seed_hi);
@@ -282,11 +308,13 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float a = __fmul_rn(e[j], invT);
-                if (key_order(__fadd_rn(a, gtab[words[j] >> 24])) < lb2_order) continue;
+                if (key_order(__fadd_rn(a, gtab[words[j] >> 24])) < lbo) continue;
                 best = umax64(best, pack_key(__fadd_rn(a, gumbel_from_word(words[j])), v0 + j));
             }
         }
         best = block_max64(best, red);
+    } else {
+        cluster_arrive();
     }
 
     // The slice winner goes to rank 0; rank 0 waits for all, reduces and stores.
@@ -306,6 +334,7 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
             for (int c = 0; c < kClusterSize; ++c) w = umax64(w, inbox[c]);
         tokens[row] = w ? static_cast<int32_t>(~static_cast<uint32_t>(w & 0xffffffffull)) : 0;
     }
+    cluster_wait();               // no CTA leaves while a peer may still send it a bound
 }
 
 // ---------------------------------------------------------- Gumbel top-k

@@ -288,6 +288,24 @@ def select_logits(cfg: SelectConfig = SELECT, rows: int | None = None, seed: int
     return x, kind
 
 
+def select_logits_device(cfg: SelectConfig = SELECT, seed: int | None = None, device="cuda") -> torch.Tensor:
+    """select_logits' recipe drawn on the device (the full 2.49 GB workload)."""
+    R, V = cfg.R, cfg.vocab
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg.seed if seed is None else seed)
+    x = torch.randn(R, V, generator=g, device=device, dtype=torch.float32) * cfg.base_std
+    kind = (torch.rand(R, generator=g, device=device) >= cfg.peaked_frac)
+    i1 = torch.randint(0, V, (R,), generator=g, device=device)
+    i2 = torch.randint(0, V, (R,), generator=g, device=device)
+    i2 = torch.where(i2 == i1, (i1 + 1) % V, i2)
+    delta = torch.rand(R, generator=g, device=device, dtype=torch.float32) * cfg.tie_gap
+    rmax = x.max(dim=1).values
+    ar = torch.arange(R, device=device)
+    x[ar, i1] = torch.where(kind, rmax, rmax + cfg.peak)
+    x[ar[kind], i2[kind]] = (rmax - delta)[kind]
+    return x
+
+
 def tiny_inputs(cfg: TinyConfig = TINY, seed: int | None = None) -> dict:
     g = generator(cfg.seed if seed is None else seed)
     W = cfg.N * cfg.K
