@@ -39,10 +39,22 @@ constexpr int SPLIT = BIV_KV_SPLIT;     // 256
 constexpr int CHUNK = 64;               // keys per online-softmax step
 constexpr int ROWB = HD * 2;            // 256 bytes per K/V/Q row in shared memory
 constexpr int ATTN_THREADS = 256;
+constexpr int kPartialBytes = (4 * 16 * HD + 2 * 4 * 16) * 4;   // chunk partials of one 16-row block
 
 // Byte offset of (row, 16-byte chunk) in a swizzled [rows][128] bf16 tile.
 BIV_DEV uint32_t swz(int row, int chunk) {
     return static_cast<uint32_t>(row * ROWB + ((chunk ^ (row & 7)) << 4));
+}
+
+// K or V of one split as TMA writes it: per 64-key chunk a [2 halves][64 keys]
+// [128 B] image with 128-byte swizzle (16-byte piece j of a 128-byte row r is
+// stored at piece j ^ (r % 8)).  Byte offset of (key, 16-byte piece c of the
+// 256-byte row).
+constexpr int kKvChunkBytes = CHUNK * ROWB;   // 16 KiB
+BIV_DEV uint32_t swz_kv(int key, int c) {
+    const int r = key & (CHUNK - 1);
+    return static_cast<uint32_t>((key >> 6) * kKvChunkBytes + (c >> 3) * (kKvChunkBytes / 2) + r * 128 +
+                                 (((c & 7) ^ (r & 7)) << 4));
 }
 
 BIV_DEV void cp_async16(uint32_t dst, const void* src) {
@@ -104,10 +116,15 @@ BIV_DEV bool row_ok(const AttnParams& P, int w, int slot0) {
 }
 
 __global__ void __launch_bounds__(ATTN_THREADS)
-attn_split_kernel(const AttnParams P) {
-    extern __shared__ __align__(128) uint8_t smem[];
+attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const AttnParams P) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
     __shared__ int s_pos[BIV_ATTN_TILE];
     __shared__ int s_maxpos;
+    __shared__ __align__(8) uint64_t kv_bar[SPLIT / CHUNK];    // one per 64-key chunk (K and V)
+    __shared__ int abort_flag;
 
     pdl_wait();
     pdl_trigger();
@@ -143,12 +160,24 @@ attn_split_kernel(const AttnParams P) {
     const int n_keys = min(SPLIT, maxpos + 1 - key0);
     const int n_chunks = (n_keys + CHUNK - 1) / CHUNK;
 
-    uint8_t* sQ = smem;                         // [T16][HD]
-    uint8_t* sK = smem + T16 * ROWB;            // [SPLIT][HD]
-    uint8_t* sV = sK + SPLIT * ROWB;            // [SPLIT][HD]
+    uint8_t* sQ = smem;                         // [T16][HD], 256-B rows, swz()
+    uint8_t* sK = smem + ((T16 * ROWB + 1023) & ~1023);   // [4 chunks] TMA images, swz_kv()
+    uint8_t* sV = sK + SPLIT * ROWB;
     const uint32_t uQ = smem_u32(sQ), uK = smem_u32(sK), uV = smem_u32(sV);
 
-    // ---- stage Q (zero rows >= T), then K/V per 64-key chunk, one commit group each
+    // ---- K/V of the split: one TMA box per 64-key chunk and matrix, each chunk
+    // completing on its own barrier; then Q (zero rows >= T) with cp.async.
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int c = 0; c < SPLIT / CHUNK; ++c) mbar_init(&kv_bar[c], 1);
+        fence_mbar_init();
+        const int kv_row = (slot0 * P.Hkv + kvh) * P.max_len + key0;
+        for (int c = 0; c < n_chunks; ++c) {
+            mbar_arrive_expect_tx(&kv_bar[c], 2u * kKvChunkBytes);
+            tma_load_3d(sK + c * kKvChunkBytes, &tmK, &kv_bar[c], 0, kv_row + c * CHUNK, 0, policy_evict_first());
+            tma_load_3d(sV + c * kKvChunkBytes, &tmV, &kv_bar[c], 0, kv_row + c * CHUNK, 0, policy_evict_first());
+        }
+    }
     for (int idx = threadIdx.x; idx < T16 * 16; idx += ATTN_THREADS) {
         const int t = idx >> 4, c = idx & 15;
         if (t < T) {
@@ -160,154 +189,171 @@ attn_split_kernel(const AttnParams P) {
             *reinterpret_cast<uint4*>(sQ + swz(t, c)) = make_uint4(0, 0, 0, 0);
         }
     }
-    const long long kv_base = (static_cast<long long>(slot0) * P.Hkv + kvh) * P.max_len + key0;
+    cp_async_commit();
+
+    // ---- per block of 16 tile rows, warp w takes 64-key chunk w / 2 and head
+    // dims [64 (w % 2), 64 (w % 2) + 64): S = Q K^T over the chunk, its softmax,
+    // O = P V for its dims.  The four chunk partials are merged in increasing
+    // chunk order.  Every row's arithmetic is the same whatever else is in
+    // the tile.
+    cp_async_wait<0>();
+    __syncthreads();                            // Q (and the barrier init) visible to all
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, cq = lane & 3;     // mma fragment coordinates
+    const int ch = warp >> 1, hh = warp & 1;
+    bool have = false;                          // this warp's chunk landed
+    if (ch < n_chunks) {
+        have = mbar_wait(&kv_bar[ch], 0, &abort_flag, &g_attn_err);
+        // Keys past the last one any row of the tile reads may hold anything
+        // (they are read in whole 64-key boxes): zero this warp's half of V there,
+        // so a masked score (p = 0) never meets a NaN.  K needs nothing: its
+        // scores are replaced by -inf with a select.
+        const int nk = n_keys - ch * CHUNK;
+        if (have && nk < CHUNK) {
+            for (int idx = lane; idx < (CHUNK - nk) * 8; idx += 32) {
+                const int key = ch * CHUNK + nk + (idx >> 3), c = hh * 8 + (idx & 7);
+                *reinterpret_cast<uint4*>(sV + swz_kv(key, c)) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        __syncwarp();
+    }
+    float* sPO = reinterpret_cast<float*>(sV + SPLIT * ROWB);    // [4 chunks][16 rows][HD]
+    float* sPM = sPO + 4 * 16 * HD;                              // [4][16] chunk maxima (log2 units)
+    float* sPL = sPM + 4 * 16;                                   // [4][16] chunk weight sums
+
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
-        if (ch < n_chunks) {
-            for (int idx = threadIdx.x; idx < CHUNK * 16; idx += ATTN_THREADS) {
-                const int j = ch * CHUNK + (idx >> 4), c = idx & 15;
-                if (j < n_keys) {
-                    const long long off = (kv_base + j) * HD + c * 8;
-                    cp_async16(uK + swz(j, c), P.kc + off);
-                    cp_async16(uV + swz(j, c), P.vc + off);
-                } else {
-                    *reinterpret_cast<uint4*>(sK + swz(j, c)) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(sV + swz(j, c)) = make_uint4(0, 0, 0, 0);
+    for (int rb = 0; rb < T16 / 16; ++rb) {
+        const int trow_a = rb * 16 + gq, trow_b = trow_a + 8;
+        const int pos_a = trow_a < T ? s_pos[trow_a / P.G] : -1;
+        const int pos_b = trow_b < T ? s_pos[trow_b / P.G] : -1;
+        float o[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+        float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
+        if (have) {
+            // ---- S = Q K^T for 16 rows x 64 keys
+            float sc[8][4];
+#pragma unroll
+            for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(uQ + swz(rb * 16 + (lane & 15), kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    const int j = lane >> 3;
+                    const int key = ch * CHUNK + np * 16 + (j >> 1) * 8 + (lane & 7);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(uK + swz_kv(key, kk * 2 + (j & 1)), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[2 * np], a0, a1, a2, a3, b0, b1);
+                    mma_bf16_16816(sc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+            // ---- mask (select, never multiply), scale into log2 units, chunk max
+            const int kbase = key0 + ch * CHUNK + cq * 2;
+            float cmax_a = -INFINITY, cmax_b = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = kbase + n * 8 + e;
+                    sc[n][e] = key <= pos_a ? sc[n][e] * P.scale_log2 : -INFINITY;
+                    sc[n][2 + e] = key <= pos_b ? sc[n][2 + e] * P.scale_log2 : -INFINITY;
+                    cmax_a = fmaxf(cmax_a, sc[n][e]);
+                    cmax_b = fmaxf(cmax_b, sc[n][2 + e]);
+                }
+            }
+            cmax_a = fmaxf(cmax_a, __shfl_xor_sync(0xffffffffu, cmax_a, 1));
+            cmax_a = fmaxf(cmax_a, __shfl_xor_sync(0xffffffffu, cmax_a, 2));
+            cmax_b = fmaxf(cmax_b, __shfl_xor_sync(0xffffffffu, cmax_b, 1));
+            cmax_b = fmaxf(cmax_b, __shfl_xor_sync(0xffffffffu, cmax_b, 2));
+            const float mu_a = cmax_a == -INFINITY ? 0.0f : cmax_a;   // a row with no key in the chunk
+            const float mu_b = cmax_b == -INFINITY ? 0.0f : cmax_b;
+            m_a = cmax_a;
+            m_b = cmax_b;
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    sc[n][e] = exp2f(sc[n][e] - mu_a);
+                    sc[n][2 + e] = exp2f(sc[n][2 + e] - mu_b);
+                    l_a += sc[n][e];
+                    l_b += sc[n][2 + e];
+                }
+            }
+            // ---- O = P V for this warp's 64 dims (P from the S accumulators)
+#pragma unroll
+            for (int kk = 0; kk < CHUNK / 16; ++kk) {
+                const uint32_t p0 = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
+                const uint32_t p1 = pack_bf16x2(sc[2 * kk][2], sc[2 * kk][3]);
+                const uint32_t p2 = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+                const uint32_t p3 = pack_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+                for (int nd = 0; nd < 4; ++nd) {
+                    const int j = lane >> 3;
+                    const int key = ch * CHUNK + kk * 16 + (j & 1) * 8 + (lane & 7);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(uV + swz_kv(key, (hh * 4 + nd) * 2 + (j >> 1)), b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * nd], p0, p1, p2, p3, b0, b1);
+                    mma_bf16_16816(o[2 * nd + 1], p0, p1, p2, p3, b2, b3);
+                }
+            }
+            // row sums across the quad (fixed order)
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+        }
+        // ---- the chunk partial into shared memory
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            const int d = hh * 64 + n * 8 + cq * 2;
+            *reinterpret_cast<float2*>(sPO + (ch * 16 + gq) * HD + d) = make_float2(o[n][0], o[n][1]);
+            *reinterpret_cast<float2*>(sPO + (ch * 16 + gq + 8) * HD + d) = make_float2(o[n][2], o[n][3]);
+        }
+        if (hh == 0 && cq == 0) {
+            sPM[ch * 16 + gq] = m_a;
+            sPM[ch * 16 + gq + 8] = m_b;
+            sPL[ch * 16 + gq] = l_a;
+            sPL[ch * 16 + gq + 8] = l_b;
+        }
+        __syncthreads();
+        // ---- merge the four chunks (increasing order), write the split's partial
+        {
+            const int r = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
+            const int trow = rb * 16 + r;
+            const int pos = trow < T ? s_pos[trow / P.G] : -1;
+            if (pos >= key0) {
+                float M = sPM[r];
+#pragma unroll
+                for (int c = 1; c < 4; ++c) M = fmaxf(M, sPM[c * 16 + r]);
+                float L = 0.0f;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float mc = sPM[c * 16 + r];
+                    const float wc = mc == -INFINITY ? 0.0f : exp2f(mc - M);
+                    L += wc * sPL[c * 16 + r];
+                    const float4 u0 = *reinterpret_cast<const float4*>(sPO + (c * 16 + r) * HD + d0);
+                    const float4 u1 = *reinterpret_cast<const float4*>(sPO + (c * 16 + r) * HD + d0 + 4);
+                    acc[0] += wc * u0.x; acc[1] += wc * u0.y; acc[2] += wc * u0.z; acc[3] += wc * u0.w;
+                    acc[4] += wc * u1.x; acc[5] += wc * u1.y; acc[6] += wc * u1.z; acc[7] += wc * u1.w;
+                }
+                const int i = trow / P.G, g = trow - i * P.G;
+                const long long ph = (static_cast<long long>(row0 + i) * P.Hq + kvh * P.G + g) * P.s_max + split;
+                float* dst = P.ws_o + ph * HD + d0;
+                *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                if (d0 == 0) {
+                    P.ws_m[ph] = M;
+                    P.ws_l[ph] = L;
                 }
             }
         }
-        cp_async_commit();
+        __syncthreads();      // the partial buffers are reused by the next row block
     }
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 2, cq = lane & 3;     // mma fragment coordinates
-    const bool computes = warp * 16 < T16;
-    const int trow_a = warp * 16 + gq, trow_b = trow_a + 8;
-    // Row positions of this thread's two tile rows (-1: not a live row).
-    const int pos_a = (computes && trow_a < T) ? s_pos[trow_a / P.G] : -1;
-    const int pos_b = (computes && trow_b < T) ? s_pos[trow_b / P.G] : -1;
-
-    float o[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
-
-#pragma unroll 1
-    for (int ch = 0; ch < n_chunks; ++ch) {
-        switch (ch) {
-            case 0: cp_async_wait<3>(); break;
-            case 1: cp_async_wait<2>(); break;
-            case 2: cp_async_wait<1>(); break;
-            default: cp_async_wait<0>(); break;
-        }
-        __syncthreads();
-        if (!computes) continue;
-
-        // ---- S = Q K^T for 16 rows x 64 keys
-        float s[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(uQ + swz(warp * 16 + (lane & 15), kk * 2 + (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                const int j = lane >> 3;
-                const int key = ch * CHUNK + np * 16 + (j >> 1) * 8 + (lane & 7);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(uK + swz(key, kk * 2 + (j & 1)), b0, b1, b2, b3);
-                mma_bf16_16816(s[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
-            }
-        }
-
-        // ---- mask (select, never multiply), scale into log2 units, chunk max
-        const int kbase = key0 + ch * CHUNK + cq * 2;
-        float cmax_a = -INFINITY, cmax_b = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int key = kbase + n * 8 + e;
-                s[n][e] = key <= pos_a ? s[n][e] * P.scale_log2 : -INFINITY;
-                s[n][2 + e] = key <= pos_b ? s[n][2 + e] * P.scale_log2 : -INFINITY;
-                cmax_a = fmaxf(cmax_a, s[n][e]);
-                cmax_b = fmaxf(cmax_b, s[n][2 + e]);
-            }
-        }
-        cmax_a = fmaxf(cmax_a, __shfl_xor_sync(0xffffffffu, cmax_a, 1));
-        cmax_a = fmaxf(cmax_a, __shfl_xor_sync(0xffffffffu, cmax_a, 2));
-        cmax_b = fmaxf(cmax_b, __shfl_xor_sync(0xffffffffu, cmax_b, 1));
-        cmax_b = fmaxf(cmax_b, __shfl_xor_sync(0xffffffffu, cmax_b, 2));
-        const float mn_a = fmaxf(m_a, cmax_a), mn_b = fmaxf(m_b, cmax_b);
-        const float mu_a = mn_a == -INFINITY ? 0.0f : mn_a;   // a row with nothing valid yet
-        const float mu_b = mn_b == -INFINITY ? 0.0f : mn_b;
-        const float al_a = exp2f(m_a - mu_a), al_b = exp2f(m_b - mu_b);
-        m_a = mn_a;
-        m_b = mn_b;
-        float ps_a = 0.0f, ps_b = 0.0f;
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                s[n][e] = exp2f(s[n][e] - mu_a);
-                s[n][2 + e] = exp2f(s[n][2 + e] - mu_b);
-                ps_a += s[n][e];
-                ps_b += s[n][2 + e];
-            }
-        }
-        l_a = l_a * al_a + ps_a;
-        l_b = l_b * al_b + ps_b;
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            o[n][0] *= al_a;
-            o[n][1] *= al_a;
-            o[n][2] *= al_b;
-            o[n][3] *= al_b;
-        }
-
-        // ---- O += P V  (P from the S accumulators, V via transposed ldmatrix)
-#pragma unroll
-        for (int kk = 0; kk < CHUNK / 16; ++kk) {
-            const uint32_t p0 = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-            const uint32_t p1 = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-            const uint32_t p2 = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-            const uint32_t p3 = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-            for (int nd = 0; nd < HD / 16; ++nd) {
-                const int j = lane >> 3;
-                const int key = ch * CHUNK + kk * 16 + (j & 1) * 8 + (lane & 7);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(uV + swz(key, nd * 2 + (j >> 1)), b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * nd], p0, p1, p2, p3, b0, b1);
-                mma_bf16_16816(o[2 * nd + 1], p0, p1, p2, p3, b2, b3);
-            }
-        }
-    }
-    if (!computes) return;
-
-    // ---- row sums across the quad (fixed order), write the split's partial
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int trow = half ? trow_b : trow_a;
-        const int pos = half ? pos_b : pos_a;
-        if (pos < key0) continue;               // dead row, or a row that ends before this split
-        const int i = trow / P.G, g = trow - i * P.G;
-        const long long ph = (static_cast<long long>(row0 + i) * P.Hq + kvh * P.G + g) * P.s_max + split;
-        float* dst = P.ws_o + ph * HD + cq * 2;
-#pragma unroll
-        for (int n = 0; n < 16; ++n)
-            *reinterpret_cast<float2*>(dst + n * 8) = make_float2(o[n][half * 2], o[n][half * 2 + 1]);
-        if (cq == 0) {
-            P.ws_m[ph] = half ? m_b : m_a;
-            P.ws_l[ph] = half ? l_b : l_a;
-        }
-    }
+    if (threadIdx.x == 0 && abort_flag)
+        for (int c = 0; c < n_chunks; ++c) mbar_wait_drain(&kv_bar[c], 0);   // copies land before exit
 }
 
 // One warp per (row, head): combine splits 0 .. pos/256 of the row.  Lane s
@@ -515,20 +561,44 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
     const long long n_tiles = n_groups * P.tiles_per_group;
     if (n_tiles > 65535 || Hkv > 65535) return BIV_ERR_SHAPE;
     const int T16max = ((P.tile_rows * P.G + 15) / 16) * 16;
-    const size_t smem = static_cast<size_t>(T16max + 2 * SPLIT) * ROWB;
+    const size_t smem = 1024 + ((static_cast<size_t>(T16max) * ROWB + 1023) & ~static_cast<size_t>(1023)) +
+                        2 * SPLIT * ROWB + kPartialBytes;
+    // K and V caches as TMA sees them: [2 halves of a row][n_slots*Hkv*max_len rows][64 elements]
+    CUtensorMap tk, tv;
+    {
+        EncodeTiledFn enc = encode_fn();
+        if (!enc) {
+            set_cuda_error(cudaErrorNotSupported);
+            return BIV_ERR_CUDA;
+        }
+        cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(n_slots) * Hkv * max_len, 2};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(ROWB), 128};
+        cuuint32_t box[3] = {64, CHUNK, 2};
+        cuuint32_t es[3] = {1, 1, 1};
+        const void* bases[2] = {k_cache, v_cache};
+        CUtensorMap* maps[2] = {&tk, &tv};
+        for (int i = 0; i < 2; ++i) {
+            if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(bases[i]), dims, strides, box,
+                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+                set_cuda_error(cudaErrorInvalidValue);
+                return BIV_ERR_CUDA;
+            }
+        }
+    }
 
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
         cudaError_t e = cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (BIV_ATTN_TILE + 2 * SPLIT) * ROWB);
+                                             1024 + BIV_ATTN_TILE * ROWB + 2 * SPLIT * ROWB + kPartialBytes);
         if (e != cudaSuccess) return cuda_status(e);
         configured_device = dev;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int st = launch_pdl(attn_split_kernel, dim3(static_cast<unsigned>(s_max), Hkv, static_cast<unsigned>(n_tiles)),
-                        dim3(ATTN_THREADS), smem, s, P);
+                        dim3(ATTN_THREADS), smem, s, tk, tv, P);
     if (st != BIV_OK) return st;
     const long long n_pairs = static_cast<long long>(W) * Hq;
     return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>((n_pairs + 7) / 8)), dim3(256), 0, s, P,
