@@ -422,9 +422,9 @@ def run_kernel_sweep(args):
     req = (torch.arange(R, dtype=torch.int32, device="cuda") // cfg.K) * 7 + 3
     pos = (torch.arange(R, dtype=torch.int32, device="cuda") % cfg.K) + 1000
     tok = torch.empty(R, dtype=torch.int32, device="cuda")
-    line("gumbel_argmax_kernel", "select fp32 [4096, 152064], T=0.7, 90% peaked rows",
+    line("gumbel_stream_kernel", "select fp32 [4096, 152064], T=0.7, 90% peaked rows",
          4 * R * cfg.vocab + 12 * R, _time_us(lambda: B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.7, tok)))
-    line("gumbel_argmax_kernel", "select fp32 [4096, 152064], T=0 (greedy)",
+    line("gumbel_stream_kernel", "select fp32 [4096, 152064], T=0 (greedy)",
          4 * R * cfg.vocab + 12 * R, _time_us(lambda: B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.0, tok)))
     del logits
 

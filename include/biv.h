@@ -247,7 +247,11 @@ int biv_rope_pack_qkv_weights(const void* w_qkv, void* w_packed, int Hq, int Hkv
  * token is selected at any batch size, with or without a drafter.
  * logits: fp32 [R, ld] (first V columns used); row_req: uint32 [R];
  * row_pos: int32 [R]; tokens: int32 [R].  Requires V % 4 == 0, ld % 4 == 0,
- * ld >= V, V >= 4, T >= 0 finite, 16-B aligned logits.                    */
+ * ld >= V, 4 <= V <= 2^22 (BIV_ERR_UNSUPPORTED above), T >= 0 finite, 16-B
+ * aligned logits.  Two or more rows per SM are streamed one row per CTA
+ * (rows dealt out by a counter of the library's; up to 64 such calls may
+ * run at the same time); fewer rows are shared by eight-CTA clusters; both
+ * give the same tokens.                                                   */
 int biv_gumbel_argmax(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
                       const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
                       biv_stream_t stream);

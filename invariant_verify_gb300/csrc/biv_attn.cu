@@ -96,7 +96,7 @@ struct AttnParams {
     float* ws_o;      // [W][Hq][S_max][HD]
     float* ws_m;      // [W][Hq][S_max]
     float* ws_l;      // [W][Hq][S_max]
-    int W, rows_per_group, tile_rows, tiles_per_group;
+    int W, rows_per_group, tile_rows, tiles_per_group, n_tiles;
     int Hq, Hkv, G, n_slots, max_len, s_max;
     float scale_log2;  // log2(e) / sqrt(HD)
 };
@@ -115,6 +115,100 @@ BIV_DEV bool row_ok(const AttnParams& P, int w, int slot0) {
     return true;
 }
 
+// First row and row count of tile t (row-major groups of rows_per_group rows,
+// each cut into tiles of tile_rows).
+BIV_DEV void tile_rows_of(const AttnParams& P, int t, int& row0, int& nr) {
+    const int group = t / P.tiles_per_group;
+    const int sub = t - group * P.tiles_per_group;
+    row0 = group * P.rows_per_group + sub * P.tile_rows;
+    const int row_end = min(min(row0 + P.tile_rows, (group + 1) * P.rows_per_group), P.W);
+    nr = row_end - row0;
+}
+
+// Largest position of a usable row of tile t (-1 if none).  A tile whose
+// first row's slot is out of range raises BIV_DEVERR_INDEX here (it is never
+// processed); the other row errors are raised where the tile is processed.
+BIV_DEV int tile_maxpos(const AttnParams& P, int t) {
+    int row0, nr;
+    tile_rows_of(P, t, row0, nr);
+    if (nr <= 0) return -1;
+    const int slot0 = P.row_slot[row0];
+    if (slot0 < 0 || slot0 >= P.n_slots) {
+        atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
+        return -1;
+    }
+    int m = -1;
+    for (int w = row0; w < row0 + nr; ++w) {
+        const int s = P.row_slot[w], p = P.row_pos[w];
+        if (s == slot0 && p >= 0 && p < P.max_len) m = max(m, p);
+    }
+    return m;
+}
+
+constexpr int kMaxTilesSmem = 2048;
+
+// Per-tile tables in shared memory, built by all threads of the CTA: the
+// largest usable position of each tile (-1: none), its first row's cache
+// slot, and the exclusive prefix sums of its live work items
+// (Hkv * (tmax / SPLIT + 1) each); s_pref[kMaxTilesSmem] is the live total.
+// Returns whether the tables cover every tile (else callers fall back to all
+// (split, KV head, tile) triples with the dead ones skipped).
+BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, int* s_slot0, int* s_wsum) {
+    const int n_tiles = P.n_tiles;
+    // Largest usable position of each tile, one thread per row (independent
+    // loads); tiles past the table are scanned where they are processed.
+    for (int t = threadIdx.x; t < min(n_tiles, kMaxTilesSmem); t += ATTN_THREADS) s_tmax[t] = -1;
+    __syncthreads();
+    for (int w = threadIdx.x; w < P.W; w += ATTN_THREADS) {
+        const int group = w / P.rows_per_group;
+        const int sub = (w - group * P.rows_per_group) / P.tile_rows;
+        const int t = group * P.tiles_per_group + sub;
+        if (t >= kMaxTilesSmem) break;                       // rows only grow the tile index
+        const int row0 = group * P.rows_per_group + sub * P.tile_rows;
+        const int slot0 = P.row_slot[row0];
+        if (w == row0) s_slot0[t] = slot0;
+        if (slot0 < 0 || slot0 >= P.n_slots) {
+            if (w == row0 && blockIdx.x == 0) atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
+            continue;
+        }
+        const int s = P.row_slot[w], p = P.row_pos[w];
+        if (s == slot0 && p >= 0 && p < P.max_len) atomicMax(&s_tmax[t], p);
+    }
+    __syncthreads();
+    // Live work items: tile t has Hkv * (s_tmax[t] / SPLIT + 1) of them (none
+    // if no row is usable); s_pref holds their exclusive prefix sums, so the
+    // CTAs can deal out exactly the live items, consecutive ones to
+    // consecutive CTAs.  Tables too large for shared memory fall back to all
+    // (split, KV head, tile) triples with the dead ones skipped.
+    const bool live_mode = n_tiles <= kMaxTilesSmem;
+    if (live_mode) {
+        // thread i scans tiles [i * per, (i + 1) * per); warp and block prefix
+        const int per = (n_tiles + ATTN_THREADS - 1) / ATTN_THREADS;
+        const int t0 = min(static_cast<int>(threadIdx.x) * per, n_tiles);
+        const int t1 = min(t0 + per, n_tiles);
+        int sum = 0;
+        for (int t = t0; t < t1; ++t) sum += s_tmax[t] >= 0 ? P.Hkv * (s_tmax[t] / SPLIT + 1) : 0;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int inc = sum;                                       // inclusive scan over the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        if (lane == 31) s_wsum[warp] = inc;
+        __syncthreads();
+        int base = inc - sum;
+        for (int w = 0; w < warp; ++w) base += s_wsum[w];
+        for (int t = t0; t < t1; ++t) {
+            s_pref[t] = base;
+            base += s_tmax[t] >= 0 ? P.Hkv * (s_tmax[t] / SPLIT + 1) : 0;
+        }
+        if (threadIdx.x == ATTN_THREADS - 1) s_pref[kMaxTilesSmem] = base;   // the live total
+        __syncthreads();
+    }
+    return live_mode;
+}
+
 __global__ void __launch_bounds__(ATTN_THREADS)
 attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const AttnParams P) {
@@ -122,41 +216,55 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     __shared__ int s_pos[BIV_ATTN_TILE];
-    __shared__ int s_maxpos;
     __shared__ __align__(8) uint64_t kv_bar[SPLIT / CHUNK];    // one per 64-key chunk (K and V)
     __shared__ int abort_flag;
+    __shared__ int s_tmax[kMaxTilesSmem];                      // largest row position per tile
+    __shared__ int s_pref[kMaxTilesSmem + 1];                  // live items before each tile; [kMax] = total
+    __shared__ int s_slot0[kMaxTilesSmem];                     // cache slot of each tile's first row
+    __shared__ int s_wsum[ATTN_THREADS / 32];
 
     pdl_wait();
     pdl_trigger();
-    const int split = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int tile = blockIdx.z;
-    const int group = tile / P.tiles_per_group;
-    const int sub = tile - group * P.tiles_per_group;
-    const int row0 = group * P.rows_per_group + sub * P.tile_rows;
-    const int row_end = min(min(row0 + P.tile_rows, (group + 1) * P.rows_per_group), P.W);
-    const int nr = row_end - row0;
-    if (nr <= 0) return;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int c = 0; c < SPLIT / CHUNK; ++c) mbar_init(&kv_bar[c], 1);
+        fence_mbar_init();
+    }
+    const int n_tiles = P.n_tiles;
+    const bool live_mode = build_tile_tables(P, s_tmax, s_pref, s_slot0, s_wsum);
+    uint32_t kv_parity = 0;                     // bit c: phase parity of chunk barrier c
+    const long long n_work =
+        live_mode ? s_pref[kMaxTilesSmem] : static_cast<long long>(P.s_max) * P.Hkv * n_tiles;
+#pragma unroll 1
+    for (long long item = blockIdx.x; item < n_work; item += gridDim.x) {
+    int tile, kvh, split;
+    if (live_mode) {
+        // the tile whose prefix range holds the item: the last t with s_pref[t] <= item
+        int lo = 0, hi = n_tiles - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_pref[mid] <= item) lo = mid; else hi = mid - 1;
+        }
+        tile = lo;
+        const int r = static_cast<int>(item - s_pref[lo]);
+        kvh = r % P.Hkv;
+        split = r / P.Hkv;
+    } else {
+        tile = static_cast<int>(item % n_tiles);
+        const long long rest = item / n_tiles;
+        kvh = static_cast<int>(rest % P.Hkv);
+        split = static_cast<int>(rest / P.Hkv);
+    }
+    const int key0 = split * SPLIT;
+    const int maxpos = tile < kMaxTilesSmem ? s_tmax[tile] : tile_maxpos(P, tile);
+    if (maxpos < key0) continue;                // no row of the tile reaches this split
+    int row0, nr;
+    tile_rows_of(P, tile, row0, nr);
     const int T = nr * P.G;                     // live tile rows (row-major over (row, head))
     const int T16 = (T + 15) & ~15;
-    const int key0 = split * SPLIT;
 
-    const int slot0 = P.row_slot[row0];
-    if (threadIdx.x == 0) {
-        s_maxpos = -1;
-        if (slot0 < 0 || slot0 >= P.n_slots) atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
-    }
-    __syncthreads();
-    if (threadIdx.x < nr) {
-        const int w = row0 + threadIdx.x;
-        int p = -1;
-        if (slot0 >= 0 && slot0 < P.n_slots && row_ok(P, w, slot0)) p = P.row_pos[w];
-        s_pos[threadIdx.x] = p;
-        atomicMax(&s_maxpos, p);
-    }
-    __syncthreads();
-    const int maxpos = s_maxpos;
-    if (maxpos < key0) return;                  // no row of the tile reaches this split
+    // a processed tile's first row has a usable slot (else the tile has no items)
+    const int slot0 = live_mode ? s_slot0[tile] : P.row_slot[row0];
     const int n_keys = min(SPLIT, maxpos + 1 - key0);
     const int n_chunks = (n_keys + CHUNK - 1) / CHUNK;
 
@@ -165,18 +273,23 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     uint8_t* sV = sK + SPLIT * ROWB;
     const uint32_t uQ = smem_u32(sQ), uK = smem_u32(sK), uV = smem_u32(sV);
 
-    // ---- K/V of the split: one TMA box per 64-key chunk and matrix, each chunk
-    // completing on its own barrier; then Q (zero rows >= T) with cp.async.
+    // ---- K/V of the split first: one TMA box per 64-key chunk and matrix,
+    // each chunk completing on its own barrier; then the rows' positions and
+    // Q (zero rows >= T) with cp.async.
     if (threadIdx.x == 0) {
-        abort_flag = 0;
-        for (int c = 0; c < SPLIT / CHUNK; ++c) mbar_init(&kv_bar[c], 1);
-        fence_mbar_init();
+        fence_proxy_async_smem();               // earlier generic writes to this memory come first
         const int kv_row = (slot0 * P.Hkv + kvh) * P.max_len + key0;
         for (int c = 0; c < n_chunks; ++c) {
             mbar_arrive_expect_tx(&kv_bar[c], 2u * kKvChunkBytes);
             tma_load_3d(sK + c * kKvChunkBytes, &tmK, &kv_bar[c], 0, kv_row + c * CHUNK, 0, policy_evict_first());
             tma_load_3d(sV + c * kKvChunkBytes, &tmV, &kv_bar[c], 0, kv_row + c * CHUNK, 0, policy_evict_first());
         }
+    }
+    if (threadIdx.x < nr) {
+        const int w = row0 + threadIdx.x;
+        int p = -1;
+        if (row_ok(P, w, slot0)) p = P.row_pos[w];
+        s_pos[threadIdx.x] = p;
     }
     for (int idx = threadIdx.x; idx < T16 * 16; idx += ATTN_THREADS) {
         const int t = idx >> 4, c = idx & 15;
@@ -203,7 +316,7 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const int ch = warp >> 1, hh = warp & 1;
     bool have = false;                          // this warp's chunk landed
     if (ch < n_chunks) {
-        have = mbar_wait(&kv_bar[ch], 0, &abort_flag, &g_attn_err);
+        have = mbar_wait(&kv_bar[ch], (kv_parity >> ch) & 1u, &abort_flag, &g_attn_err);
         // Keys past the last one any row of the tile reads may hold anything
         // (they are read in whole 64-key boxes): zero this warp's half of V there,
         // so a masked score (p = 0) never meets a NaN.  K needs nothing: its
@@ -353,7 +466,10 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         __syncthreads();      // the partial buffers are reused by the next row block
     }
     if (threadIdx.x == 0 && abort_flag)
-        for (int c = 0; c < n_chunks; ++c) mbar_wait_drain(&kv_bar[c], 0);   // copies land before exit
+        for (int c = 0; c < n_chunks; ++c) mbar_wait_drain(&kv_bar[c], (kv_parity >> c) & 1u);   // land first
+    kv_parity ^= (1u << n_chunks) - 1u;
+    if (abort_flag) break;
+    }
 }
 
 // One warp per (row, head): combine splits 0 .. pos/256 of the row.  Lane s
@@ -559,7 +675,8 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
 
     const long long n_groups = (W + P.rows_per_group - 1) / P.rows_per_group;
     const long long n_tiles = n_groups * P.tiles_per_group;
-    if (n_tiles > 65535 || Hkv > 65535) return BIV_ERR_SHAPE;
+    if (n_tiles > 0x7fffffffLL / 64 || Hkv > 65535) return BIV_ERR_SHAPE;
+    P.n_tiles = static_cast<int>(n_tiles);
     const int T16max = ((P.tile_rows * P.G + 15) / 16) * 16;
     const size_t smem = 1024 + ((static_cast<size_t>(T16max) * ROWB + 1023) & ~static_cast<size_t>(1023)) +
                         2 * SPLIT * ROWB + kPartialBytes;
@@ -597,8 +714,9 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
         configured_device = dev;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int st = launch_pdl(attn_split_kernel, dim3(static_cast<unsigned>(s_max), Hkv, static_cast<unsigned>(n_tiles)),
-                        dim3(ATTN_THREADS), smem, s, tk, tv, P);
+    const long long n_items = static_cast<long long>(s_max) * Hkv * n_tiles;
+    const int grid = static_cast<int>(std::min<long long>(n_items, num_sms()));
+    int st = launch_pdl(attn_split_kernel, dim3(static_cast<unsigned>(grid)), dim3(ATTN_THREADS), smem, s, tk, tv, P);
     if (st != BIV_OK) return st;
     const long long n_pairs = static_cast<long long>(W) * Hq;
     return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>((n_pairs + 7) / 8)), dim3(256), 0, s, P,

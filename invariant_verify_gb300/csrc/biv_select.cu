@@ -41,6 +41,8 @@
 // is the maximum of a 64-bit packed value (order(key) << 32 | ~v), which puts
 // larger keys first and lower indices first among equal keys, so any
 // reduction order gives the same token.
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "biv_common.cuh"
@@ -80,6 +82,11 @@ const NoiseBounds& noise_bounds() {
         return t;
     }();
     return nb;
+}
+
+// Inverse of key_order for orders of numbers (order 0, NaN, maps to NaN).
+BIV_DEV float order_to_float(uint32_t o) {
+    return o == 0u ? __int_as_float(0x7fc00000) : __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
 }
 
 // ------------------------------------------------------------- cluster PTX
@@ -337,6 +344,264 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
     cluster_wait();               // no CTA leaves while a peer may still send it a bound
 }
 
+
+// ------------------------------------------------ streaming row kernel
+// One CTA per row (persistent over rows), no cross-CTA traffic.  Pass 1
+// streams the row from HBM through a ring of kStreamStages bulk copies and
+// keeps the maximum of every 256-logit block in shared memory, and the row's
+// largest logit.  The exact key of that logit is the lower bound LB.  Pass 2
+// lists the blocks whose maximum can still reach LB with the largest noise of
+// all, then re-reads (mostly from L2) only their logits, every thread with
+// kUnroll loads in flight; per 4-group it draws the Philox words, bounds each
+// entry by fl(fl(x * invT) + T[w >> 24]) and takes the two logs only where
+// that bound passes the best key found so far.  Entries are skipped only on
+// a bound at or below a real key of the row, so the result is exact.  On a
+// peaked row pass 2 touches a block or two; on a flat row it is bound by the
+// Philox arithmetic.  The ring runs ahead across rows: the next row's first
+// chunks land during pass 2.
+constexpr int kStreamChunk = 8192;               // floats per ring slot (32 KiB)
+constexpr int kStreamStages = 3;
+constexpr int kBlock = 256;                      // logits per block maximum
+constexpr int kMaxStreamV = 1 << 22;             // block maxima kept in shared memory (64 KiB)
+constexpr int kUnroll = 8;                       // pass 2: loads in flight per thread
+constexpr int kCtrSlots = 64;                    // row-ticket counter pairs, one per launch in flight
+
+// {next row ticket, CTAs finished} per slot; zero at load, and the last CTA of
+// every launch puts its pair back to zero.
+__device__ unsigned int g_stream_ctr[2 * kCtrSlots];
+
+size_t stream_smem_bytes(int V) {
+    return static_cast<size_t>(kStreamStages) * kStreamChunk * 4 + static_cast<size_t>((V + kBlock - 1) / kBlock) * 4;
+}
+
+__global__ void __launch_bounds__(kSelThreads, 2)
+gumbel_stream_kernel(const float* __restrict__ logits, int R, int V, long long ld,
+                     const uint32_t* __restrict__ row_req, const int32_t* __restrict__ row_pos, uint32_t seed_lo,
+                     uint32_t seed_hi, float invT, int greedy, int32_t* __restrict__ tokens,
+                     unsigned int* __restrict__ ctr, const __grid_constant__ NoiseBounds nb) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    float* ring = reinterpret_cast<float*>(smem_raw);                                     // [stages][chunk]
+    float* bmax = reinterpret_cast<float*>(smem_raw + kStreamStages * kStreamChunk * 4);  // [ceil(V / 256)]
+    __shared__ uint64_t fbar[kStreamStages];
+    __shared__ unsigned long long red[kSelThreads / 32];
+    __shared__ unsigned long long bcast;
+    __shared__ unsigned long long s_best;                    // pass 2: best key any warp has found
+    __shared__ int wcount[kSelThreads / 32];
+    __shared__ int s_rows[8];                                // row of stream ordinal i at [i % 8]
+    int* live_list = reinterpret_cast<int*>(bmax);           // pass 2: live blocks, written over bmax
+    __shared__ float gtab[256];
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < kStreamStages; ++i) mbar_init(&fbar[i], 1);
+        fence_mbar_init();
+    }
+    gtab[threadIdx.x] = nb.v[threadIdx.x];
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+
+    const int n_chunks = (V + kStreamChunk - 1) / kStreamChunk;
+    const int n_blocks = (V + kBlock - 1) / kBlock;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    static_assert(kStreamChunk % kBlock == 0, "blocks never straddle chunks");
+    static_assert(kBlock == 256, "pass 2 indexes 64 groups per block");
+    // Rows are dealt out by a ticket counter, so a CTA that meets an expensive
+    // (flat) row takes fewer rows.  Thread 0 fetches the ticket of a row when
+    // it issues the row's first chunk, up to kStreamStages chunks ahead of the
+    // consumers, and posts it in s_rows (-1: no rows left); every thread reads
+    // it after at least one barrier that follows the post.
+    long long k_issued = 0;                          // thread 0: chunks issued
+    bool stream_end = false;                         // thread 0: a ticket past the last row came back
+    auto issue_next = [&]() {
+        if (stream_end) return;
+        const long long ord = k_issued / n_chunks;
+        const int c = static_cast<int>(k_issued % n_chunks);
+        if (c == 0) {
+            const unsigned t = atomicAdd(&ctr[0], 1u);
+            s_rows[ord & 7] = t < static_cast<unsigned>(R) ? static_cast<int>(t) : -1;
+            if (t >= static_cast<unsigned>(R)) {
+                stream_end = true;
+                return;
+            }
+        }
+        const long long rr = s_rows[ord & 7];
+        const int n = min(kStreamChunk, V - c * kStreamChunk);
+        const int slot = static_cast<int>(k_issued % kStreamStages);
+        mbar_arrive_expect_tx(&fbar[slot], static_cast<uint32_t>(n) * 4u);
+        bulk_g2s(ring + slot * kStreamChunk, logits + rr * ld + static_cast<long long>(c) * kStreamChunk,
+                 static_cast<uint32_t>(n) * 4u, &fbar[slot]);
+        ++k_issued;
+    };
+    if (threadIdx.x == 0)
+        for (int i = 0; i < kStreamStages; ++i) issue_next();
+    __syncthreads();
+
+    long long k = 0;                                 // next chunk to consume
+    bool ok = true;
+#pragma unroll 1
+    for (long long ord = 0;; ++ord) {
+        const int row = s_rows[ord & 7];
+        if (row < 0) break;
+        const float* x = logits + static_cast<long long>(row) * ld;
+        const uint32_t req = row_req[row];                                 // used after pass 1
+        const uint32_t pos = static_cast<uint32_t>(row_pos[row]) + 1u;   // position being selected
+        // ---- pass 1: block maxima and the row maximum (lowest index among equals)
+        float best_x = 0.0f;
+        int best_i = -1;
+#pragma unroll 1
+        for (int c = 0; c < n_chunks; ++c) {
+            const int slot = static_cast<int>(k % kStreamStages);
+            mbar_wait(&fbar[slot], static_cast<uint32_t>((k / kStreamStages) & 1), &abort_flag, &g_select_err);
+            __syncthreads();                          // a timed-out wait is seen by every thread
+            if (abort_flag) {
+                ok = false;
+                break;
+            }
+            const int n = min(kStreamChunk, V - c * kStreamChunk);   // a multiple of 4
+            const float* buf = ring + slot * kStreamChunk;
+            // warp per 256-logit block; lane l reads logits [4l, 4l+4) and [128+4l, 128+4l+4)
+#pragma unroll 1
+            for (int blk = warp; blk * kBlock < n; blk += kSelThreads / 32) {
+                float m = __int_as_float(0x7fc00000);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int e0 = blk * kBlock + h * 128 + 4 * lane;
+                    if (e0 >= n) break;
+                    const float4 v = *reinterpret_cast<const float4*>(buf + e0);
+                    const float m4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+                    m = fmaxf(m, m4);
+                    if (m4 == m4 && (best_i < 0 || m4 > best_x)) {      // lanes see their logits in index order
+                        best_x = m4;
+                        best_i = c * kStreamChunk + e0 + (v.x == m4 ? 0 : v.y == m4 ? 1 : v.z == m4 ? 2 : 3);
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                if (lane == 0) bmax[c * (kStreamChunk / kBlock) + blk] = m;
+            }
+            __syncthreads();                          // the slot is read; refill it
+            if (threadIdx.x == 0) issue_next();
+            ++k;
+        }
+        if (!ok) break;
+        unsigned long long mx = best_i >= 0 ? pack_key(best_x, static_cast<uint32_t>(best_i)) : 0ull;
+        mx = block_max64(mx, red);
+        unsigned long long best = mx;
+        if (!greedy) {
+            // LB: the exact key of the row's largest logit.
+            if (threadIdx.x == 0) {
+                unsigned long long lb = 0;
+                if (mx) {
+                    const uint32_t v = ~static_cast<uint32_t>(mx & 0xffffffffull);
+                    const U4 w = philox4x32_10(v >> 2, pos, req, 0u, seed_lo, seed_hi);
+                    const uint32_t j = v & 3u;
+                    const uint32_t wj = j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w;
+                    const float xmax = order_to_float(static_cast<uint32_t>(mx >> 32));   // the logit itself
+                    lb = pack_key(__fadd_rn(__fmul_rn(xmax, invT), gumbel_from_word(wj)), v);
+                }
+                bcast = lb;
+                s_best = lb;
+            }
+            __syncthreads();
+            best = bcast;
+            // ---- pass 2a: compact the live blocks (block maximum can still reach
+            // LB with the largest noise) into a list, in place over bmax; a
+            // window of 256 blocks at a time, reads before writes.
+            const uint32_t lbo = static_cast<uint32_t>(best >> 32);
+            int n_live = 0;
+#pragma unroll 1
+            for (int w0 = 0; w0 < n_blocks; w0 += kSelThreads) {
+                const int blk = w0 + static_cast<int>(threadIdx.x);
+                const bool live = blk < n_blocks &&
+                                  key_order(__fadd_rn(__fmul_rn(bmax[blk], invT), kNoiseBound)) >= lbo;
+                const unsigned bal = __ballot_sync(0xffffffffu, live);
+                if (lane == 0) wcount[warp] = __popc(bal);
+                __syncthreads();
+                int before = n_live, total_w = 0;
+#pragma unroll
+                for (int i = 0; i < kSelThreads / 32; ++i) {
+                    before += i < warp ? wcount[i] : 0;
+                    total_w += wcount[i];
+                }
+                if (live) live_list[before + __popc(bal & ((1u << lane) - 1u))] = blk;
+                n_live += total_w;
+                __syncthreads();
+            }
+            // ---- pass 2b: the 4-groups of the live blocks, all threads, kUnroll
+            // loads in flight per thread; 32 consecutive items share a block.
+            const int n_items = n_live * (kBlock / 4);
+#pragma unroll 1
+            for (int base = 0; base < n_items; base += kSelThreads * kUnroll) {
+                float4 v4[kUnroll];
+                int v0[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int it = base + u * kSelThreads + static_cast<int>(threadIdx.x);
+                    v0[u] = -1;
+                    if (it < n_items) {
+                        const int v = live_list[it >> 6] * kBlock + 4 * (it & 63);
+                        if (v < V) {                          // the last block may be partial
+                            v0[u] = v;
+                            v4[u] = *reinterpret_cast<const float4*>(x + v);
+                        }
+                    }
+                }
+                // Straight-line over the kUnroll groups so their Philox chains
+                // interleave.  A bound strictly below best_f (the value of the
+                // best key) cannot win; equal or NaN-free ties go to the exact
+                // packed comparison.  While best is a NaN key (order 0: a row
+                // with no number so far) nothing is pruned.
+                const bool no_prune = (best >> 32) == 0;
+                const float best_f = order_to_float(static_cast<uint32_t>(best >> 32));
+                U4 w[kUnroll];
+                bool glive[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const float m4 = fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w));
+                    glive[u] = v0[u] >= 0 && (no_prune || __fadd_rn(__fmul_rn(m4, invT), kNoiseBound) >= best_f);
+                    w[u] = philox4x32_10(static_cast<uint32_t>(max(v0[u], 0)) >> 2, pos, req, 0u, seed_lo, seed_hi);
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    if (!glive[u]) continue;
+                    const float e[4] = {v4[u].x, v4[u].y, v4[u].z, v4[u].w};
+                    const uint32_t words[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float a = __fmul_rn(e[j], invT);
+                        if (!no_prune && !(__fadd_rn(a, gtab[words[j] >> 24]) >= best_f)) continue;
+                        const uint32_t vv = static_cast<uint32_t>(v0[u] + j);
+                        best = umax64(best, pack_key(__fadd_rn(a, gumbel_from_word(words[j])), vv));
+                    }
+                }
+                // share the bound: warp maximum, then the CTA's running maximum
+                best = warp_max64(best);
+                if (lane == 0) atomicMax(&s_best, best);
+                best = umax64(best, *reinterpret_cast<volatile unsigned long long*>(&s_best));
+            }
+            best = block_max64(best, red);              // also orders pass 2's reads of bmax before the next row
+        }
+        if (threadIdx.x == 0)
+            tokens[row] = best ? static_cast<int32_t>(~static_cast<uint32_t>(best & 0xffffffffull)) : 0;
+    }
+    // After a time-out, the copies still in flight (chunks k .. k_issued - 1)
+    // land before the CTA's shared memory is released.  The last CTA to leave
+    // resets the launch's counters for the next launch that uses them.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (!ok)
+            for (long long j = k; j < k_issued; ++j)
+                mbar_wait_drain(&fbar[j % kStreamStages], static_cast<uint32_t>((j / kStreamStages) & 1));
+        __threadfence();
+        if (atomicAdd(&ctr[1], 1u) == gridDim.x - 1) {
+            ctr[0] = 0;
+            ctr[1] = 0;
+            __threadfence();
+        }
+    }
+}
+
 // ---------------------------------------------------------- Gumbel top-k
 // [COUPLING]: the Gumbel-max trick gives top-k sampling as it stands -- the k
 // largest keys, in decreasing order, are k draws without replacement from
@@ -461,6 +726,51 @@ __global__ void verify_accept_kernel(const int32_t* __restrict__ target, const i
     new_len[r] = p0[r] + L;
 }
 
+
+// Persistent launch of the streaming kernel: as many CTAs as fit on the GPU,
+// at most one per row; CTA b takes rows b, b + grid, ...
+int launch_stream_select(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                         const int32_t* row_pos, uint64_t seed, float invT, int greedy, int32_t* tokens,
+                         cudaStream_t stream) {
+    const size_t smem = stream_smem_bytes(V);
+    static int configured_device = -1;
+    static int per_sm_cache[2] = {0, 0};         // {smem the value is for, CTAs per SM}
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(gumbel_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(stream_smem_bytes(kMaxStreamV)));
+        if (e != cudaSuccess) return cuda_status(e);
+        configured_device = dev;
+        per_sm_cache[0] = 0;
+    }
+    if (per_sm_cache[0] != static_cast<int>(smem)) {
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gumbel_stream_kernel, kSelThreads, smem);
+        if (e != cudaSuccess) return cuda_status(e);
+        per_sm_cache[0] = static_cast<int>(smem);
+        per_sm_cache[1] = std::max(1, per_sm);
+    }
+    static int ctr_device = -1;
+    static unsigned int* ctr_base = nullptr;
+    if (ctr_device != dev) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_stream_ctr);
+        if (e != cudaSuccess) return cuda_status(e);
+        ctr_base = static_cast<unsigned int*>(p);
+        ctr_device = dev;
+    }
+    // Each launch takes the next counter pair of the ring (launches in flight
+    // at the same time on different streams must not share one).
+    static std::atomic<unsigned> next_slot{0};
+    unsigned int* ctr = ctr_base + 2 * (next_slot.fetch_add(1u) % kCtrSlots);
+    const long long cap = static_cast<long long>(num_sms()) * per_sm_cache[1];
+    const int grid = static_cast<int>(std::min<long long>(R, cap));
+    return launch_pdl(gumbel_stream_kernel, dim3(static_cast<unsigned>(grid)), dim3(kSelThreads), smem, stream,
+                      logits, R, V, ld, row_req, row_pos, static_cast<uint32_t>(seed & 0xffffffffull),
+                      static_cast<uint32_t>(seed >> 32), invT, greedy, tokens, ctr, noise_bounds());
+}
+
 }  // namespace
 }  // namespace biv
 
@@ -476,10 +786,16 @@ extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld
     if (!logits || !row_req || !row_pos || !tokens) return BIV_ERR_NULL;
     if (!aligned16(logits)) return BIV_ERR_ALIGN;
     const int slice = ((V / 4 + kClusterSize - 1) / kClusterSize) * 4;
-    if (slice > kMaxSliceFloats) return BIV_ERR_UNSUPPORTED;
-    if (static_cast<long long>(R) * kClusterSize > 0x7fffffffLL) return BIV_ERR_SHAPE;
+    if (V > kMaxStreamV) return BIV_ERR_UNSUPPORTED;
     const int greedy = temperature == 0.0f;
     const float invT = greedy ? 0.0f : 1.0f / temperature;   // fl(1/T), IEEE division on the host
+    // Many rows (two or more per SM) or a row too wide for one cluster: a CTA
+    // streams whole rows.  Few rows: a cluster of eight CTAs shares each row.
+    if (R >= 2 * num_sms() || slice > kMaxSliceFloats) {
+        return launch_stream_select(logits, R, V, ld, row_req, row_pos, seed, invT, greedy, tokens,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    }
+    if (static_cast<long long>(R) * kClusterSize > 0x7fffffffLL) return BIV_ERR_SHAPE;
     const size_t smem = static_cast<size_t>(slice) * 5;
 
     static int configured_device = -1;

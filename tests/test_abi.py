@@ -150,7 +150,7 @@ def test_select_and_accept_validation(lib):
     assert g(FAKE, 0, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, None) == OK
     assert g(None, 4, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, None) == NULL
     assert g(MISALIGNED, 4, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, None) == ALIGN
-    big = 8 * 57344 + 32
+    big = (1 << 22) + 4                     # past the streaming kernel's block-maximum table
     assert g(FAKE, 4, big, big, FAKE, FAKE, 1, 1.0, FAKE, None) == UNSUP
     a = lib.biv_verify_accept
     assert a(FAKE, FAKE, FAKE, 4, 0, FAKE, FAKE, None) == SHAPE

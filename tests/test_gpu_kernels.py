@@ -218,6 +218,26 @@ def test_attention_rows_are_batch_invariant():
         kd2[r, :, p + 8:] = 7.0
         vd2[r, :, p + 8:] = -3.0
     assert same_bits(_run_attn(qd, kd2, vd2, slot, pos, 8), full)
+    # ... not even NaN (keys past the last one any row reads are never multiplied in)
+    kd3, vd3 = kd.clone(), vd.clone()
+    for r, p in enumerate([100, 255, 700, 1300]):
+        kd3[r, :, p + 8:] = float("nan")
+        vd3[r, :, p + 8:] = float("nan")
+    assert same_bits(_run_attn(qd, kd3, vd3, slot, pos, 8), full)
+
+
+def test_attention_bad_position_raises_device_error():
+    q, kc, vc, slot, pos = _attn_case(2, 8, 2, 600, [100, 300], 4, seed=12)
+    qd, kd, vd = dev(q), dev(kc), dev(vc)
+    good = _run_attn(qd, kd, vd, slot, pos, 4)
+    assert B.biv_device_error() == 0
+    bad = pos.copy()
+    bad[5] = 600                                           # one past the cache
+    o = _run_attn(qd, kd, vd, slot, bad, 4)
+    assert B.biv_device_error() & 2                        # BIV_DEVERR_INDEX, and the flag is cleared
+    assert torch.count_nonzero(o[5]) == 0                  # the bad row is zeroed
+    keep = [w for w in range(8) if w != 5]
+    assert same_bits(o[keep], good[keep])                  # the other rows are unaffected
 
 
 def test_attention_first_position():
@@ -417,6 +437,85 @@ def test_gumbel_argmax_peaked_ties_and_stride():
     B.biv_gumbel_argmax(pad.cuda(), req.cuda(), pos.cuda(), SEED, 0.7, tok, V=cfg.vocab)
     assert np.array_equal(tok.cpu().numpy(), oracle.gumbel_argmax(x, req, pos, SEED, 0.7))
     B.biv_gumbel_argmax(pad[:0].cuda(), req[:0].cuda(), pos[:0].cuda(), SEED, 0.7, tok[:0], V=cfg.vocab)
+
+
+def _many_rows():
+    """A row count that sends the selection to its streaming kernel (two or
+    more rows per SM); fewer rows go to the eight-CTA cluster kernel."""
+    return 2 * torch.cuda.get_device_properties(0).multi_processor_count + 5
+
+
+@pytest.mark.parametrize("V,T", [(8196, 0.7), (4, 1.0), (24580, 0.0), (16388, 2.0), (1000, 1e-3)])
+def test_gumbel_argmax_streaming_rows_bit_exact(V, T):
+    """Many rows: one CTA per row, ring of bulk copies, block maxima, pass 2
+    over live blocks.  V spans several 8192-logit chunks and a ragged tail;
+    rows mix flat, peaked, NaN-holding, all-NaN, -inf and exact-tie rows."""
+    R = _many_rows()
+    g = synth.generator(V + 11)
+    x = torch.randn(R, V, generator=g) * 2.0
+    x[1::5, V // 3] += 40.0                       # peaked rows
+    x[2::7, :] = float("nan")                     # all-NaN rows select token 0
+    x[3::7, ::3] = float("nan")                   # scattered NaN never wins
+    x[4::9, :] = float("-inf")
+    x[4::9, V - 1] = 0.0                          # a single finite logit at the tail
+    x[5::11, :] = 1.5                             # exact ties everywhere
+    req = torch.randint(0, 2 ** 31 - 1, (R,), generator=g, dtype=torch.int64).to(torch.int32)
+    pos = torch.randint(0, 8000, (R,), generator=g, dtype=torch.int64).to(torch.int32)
+    tok = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax(x.cuda(), req.cuda(), pos.cuda(), SEED, T, tok)
+    assert np.array_equal(tok.cpu().numpy(), oracle.gumbel_argmax(x, req, pos, SEED, T))
+    # the same rows through the cluster kernel (few rows) and with a padded
+    # leading dimension: identical tokens
+    sub = [0, 1, 2, 3, 4, 5, R - 1]
+    few = torch.empty(len(sub), dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax(x[sub].cuda(), req[sub].cuda(), pos[sub].cuda(), SEED, T, few)
+    assert torch.equal(few, tok[sub])
+    pad = torch.full((R, V + 12), 1e30)
+    pad[:, :V] = x
+    tp = torch.empty(R, dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax(pad.cuda(), req.cuda(), pos.cuda(), SEED, T, tp, V=V)
+    assert torch.equal(tp, tok)
+
+
+def test_gumbel_argmax_streaming_rows_concurrent_streams_and_graph_replays():
+    """The streaming kernel deals rows out by a per-launch ticket counter that
+    the launch's last CTA resets: back-to-back launches, launches on two
+    streams at once and graph replays all select every row exactly."""
+    R, V = _many_rows() + 40, 16384
+    g = synth.generator(321)
+    xs = [torch.randn(R, V, generator=g) * 3.0 for _ in range(2)]
+    req = torch.randint(0, 2 ** 31 - 1, (R,), generator=g, dtype=torch.int64).to(torch.int32)
+    pos = torch.randint(0, 8000, (R,), generator=g, dtype=torch.int64).to(torch.int32)
+    refs = [oracle.gumbel_argmax(x, req, pos, SEED, 0.7) for x in xs]
+    xd = [x.cuda() for x in xs]
+    rq, ps = req.cuda(), pos.cuda()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    toks = [torch.full((R,), -7, dtype=torch.int32, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(5):
+        for i in range(2):
+            toks[i].fill_(-7)
+        torch.cuda.synchronize()
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                for _ in range(3):
+                    B.biv_gumbel_argmax(xd[i], rq, ps, SEED, 0.7, toks[i], stream=streams[i])
+        torch.cuda.synchronize()
+        for i in range(2):
+            assert np.array_equal(toks[i].cpu().numpy(), refs[i])
+    tok = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        B.biv_gumbel_argmax(xd[0], rq, ps, SEED, 0.7, tok, stream=s)     # first call outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        B.biv_gumbel_argmax(xd[1], rq, ps, SEED, 0.7, tok, stream=torch.cuda.current_stream())
+    for _ in range(4):
+        tok.fill_(-7)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(tok.cpu().numpy(), refs[1])
 
 
 def test_gumbel_argmax_chi_square_counts_match_oracle():
