@@ -440,7 +440,7 @@ def run_kernel_sweep(args):
     rpos = (ctx.cuda().repeat_interleave(K) + torch.arange(K, device="cuda").repeat(N)).to(torch.int32)
     ws = torch.empty(B.biv_decode_attn_workspace_size(W, sw.Hq, max_len), dtype=torch.uint8, device="cuda")
     kv_bytes = sum(2 * 2 * sw.Hkv * (int(c) + K) * sw.hd for c in ctx)
-    line("attn_split_kernel + attn_combine_kernel",
+    line("attn_tc_kernel + attn_combine_kernel",
          f"attention W={W} (64 x 16), Hq 32 / Hkv 8, lognormal ctx mean {float(ctx.float().mean()):.0f}",
          kv_bytes + 2 * 2 * W * sw.Hq * sw.hd,
          _time_us(lambda: B.biv_decode_attn_fixedsplit(q, kc, vc, slot, rpos, o, K, ws)))

@@ -7,22 +7,18 @@
 // times the verified rows of one request, fill one 128-row MMA tile
 // (G * (1 + D) <= 128).
 //
-// Phase 1, one CTA per (row tile, KV head, split of 256 absolute positions):
-// the tile holds up to 128/G consecutive rows of one request times its G
-// query heads.  K and V of the split are staged in shared memory once
-// (cp.async, XOR-swizzled 16-byte chunks) and every row of the tile reuses
-// them.  Each compute warp owns 16 tile rows; per 64-key chunk it forms
-// S = Q K^T with bf16 mma.sync (fp32 accumulate), masks keys beyond the
-// row's own position with a select, and updates an online softmax in a
-// fixed order.  The split's partial (max, sum, unnormalised output) goes to
-// the caller's workspace.  Phase 2 combines the splits 0..p/256 of each
-// (row, head) in increasing order.  Nothing in a row's arithmetic depends on
-// the other rows of the tile or the batch: masked keys contribute exact
-// zeros and chunks beyond a row's position leave its state unchanged.
-//
-// The contraction per split is tiny (16..128 rows x 256 keys x 128), so the
-// kernel is bound by reading K and V from HBM, not by the tensor pipe;
-// mma.sync is ample here.
+// Phase 1 (attn_tc_kernel): a work item is (row tile, KV head, split of 256
+// absolute positions); the tile holds up to 128/G consecutive rows of one
+// request times its G query heads, so K and V of the split are read once for
+// all of them.  S = Q K^T and O = P V run on the tensor cores with the
+// accumulators in TMEM; the softmax over the whole split runs between them
+// in registers, masking keys past each row's own position with a select.
+// The split's partial (max, sum, unnormalised output) goes to the caller's
+// workspace.  Phase 2 (attn_combine_kernel) combines the splits 0..p/256 of
+// each (row, head) in increasing order.  Nothing in a row's arithmetic
+// depends on the other rows of the tile or the batch: masked keys contribute
+// exact zeros, the MMAs contract in fixed 16-wide steps and every sum has a
+// fixed order.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -36,26 +32,8 @@ BIV_DEFINE_ERR_WORD(g_attn_err)
 
 constexpr int HD = BIV_HEAD_DIM;        // 128
 constexpr int SPLIT = BIV_KV_SPLIT;     // 256
-constexpr int CHUNK = 64;               // keys per online-softmax step
-constexpr int ROWB = HD * 2;            // 256 bytes per K/V/Q row in shared memory
+constexpr int ROWB = HD * 2;            // 256 bytes per K/V row
 constexpr int ATTN_THREADS = 256;
-constexpr int kPartialBytes = (4 * 16 * HD + 2 * 4 * 16) * 4;   // chunk partials of one 16-row block
-
-// Byte offset of (row, 16-byte chunk) in a swizzled [rows][128] bf16 tile.
-BIV_DEV uint32_t swz(int row, int chunk) {
-    return static_cast<uint32_t>(row * ROWB + ((chunk ^ (row & 7)) << 4));
-}
-
-// K or V of one split as TMA writes it: per 64-key chunk a [2 halves][64 keys]
-// [128 B] image with 128-byte swizzle (16-byte piece j of a 128-byte row r is
-// stored at piece j ^ (r % 8)).  Byte offset of (key, 16-byte piece c of the
-// 256-byte row).
-constexpr int kKvChunkBytes = CHUNK * ROWB;   // 16 KiB
-BIV_DEV uint32_t swz_kv(int key, int c) {
-    const int r = key & (CHUNK - 1);
-    return static_cast<uint32_t>((key >> 6) * kKvChunkBytes + (c >> 3) * (kKvChunkBytes / 2) + r * 128 +
-                                 (((c & 7) ^ (r & 7)) << 4));
-}
 
 BIV_DEV void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -64,27 +42,6 @@ BIV_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memo
 template <int N>
 BIV_DEV void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-BIV_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-BIV_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-// D = A (16x16 bf16, row) * B (16x8 bf16, col) + D, fp32.
-BIV_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                            uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 struct AttnParams {
@@ -209,267 +166,462 @@ BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, in
     return live_mode;
 }
 
-__global__ void __launch_bounds__(ATTN_THREADS)
-attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const AttnParams P) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
-    __shared__ int s_pos[BIV_ATTN_TILE];
-    __shared__ __align__(8) uint64_t kv_bar[SPLIT / CHUNK];    // one per 64-key chunk (K and V)
-    __shared__ int abort_flag;
-    __shared__ int s_tmax[kMaxTilesSmem];                      // largest row position per tile
-    __shared__ int s_pref[kMaxTilesSmem + 1];                  // live items before each tile; [kMax] = total
-    __shared__ int s_slot0[kMaxTilesSmem];                     // cache slot of each tile's first row
-    __shared__ int s_wsum[ATTN_THREADS / 32];
+// ------------------------------------------------- tensor-core split kernel
+// Phase 1 on the 5th-generation tensor cores.  A work item is (row tile, KV
+// head, split of 256 absolute positions); persistent CTAs deal out the live
+// items (build_tile_tables).  Per item, with M = 64 or 128 MMA rows:
+//   S = Q K^T   tcgen05.mma M x 128 x 16, 8 k-steps per 128-key half, fp32
+//               accumulators in TMEM columns [0, 256)
+//   softmax     the 8 warps read S rows from TMEM, scale them into log2
+//               units, mask keys past each row's own position with a select,
+//               take the row maximum m over the whole split, p = 2^(s - m),
+//               the fp32 sum l of p, and store bf16 p into shared memory as
+//               the A operand of
+//   O = P V     tcgen05.mma M x 128 x 16 over the split's 16-key steps (V is
+//               the MN-major B operand: one row of dims per key), fp32 in
+//               TMEM columns [256, 384)
+//   partial     (m, l, O) of every tile row that reaches the split, to the
+//               workspace that attn_combine_kernel reads.
+// Both products contract in whole 16-wide steps in a fixed order and every
+// row's arithmetic touches only its own S / P / O row, so a row's result does
+// not depend on the rest of the tile or the batch.  K and V of a split arrive
+// as 128-key TMA boxes ([2 dim halves][128 keys][128 B], 128-byte swizzle).
+// Loads run ahead: the next item's K (M = 64) and Q as soon as this item's S
+// is in TMEM, its V (and K for M = 128, whose P reuses K's space) as soon as
+// P V is.
+constexpr int kTcKeyHalfBytes = 2 * 128 * 128;    // one 128-key box of K or V: 32 KiB
+constexpr uint32_t kTmemCols = 512;                // S: [0, 256), O: [256, 384)
 
-    pdl_wait();
-    pdl_trigger();
-    if (threadIdx.x == 0) {
-        abort_flag = 0;
-        for (int c = 0; c < SPLIT / CHUNK; ++c) mbar_init(&kv_bar[c], 1);
-        fence_mbar_init();
-    }
-    const int n_tiles = P.n_tiles;
-    const bool live_mode = build_tile_tables(P, s_tmax, s_pref, s_slot0, s_wsum);
-    uint32_t kv_parity = 0;                     // bit c: phase parity of chunk barrier c
-    const long long n_work =
-        live_mode ? s_pref[kMaxTilesSmem] : static_cast<long long>(P.s_max) * P.Hkv * n_tiles;
-#pragma unroll 1
-    for (long long item = blockIdx.x; item < n_work; item += gridDim.x) {
-    int tile, kvh, split;
+template <int M>
+constexpr size_t tc_smem_bytes() {
+    return 1024 + static_cast<size_t>(M) * 256 + 4 * kTcKeyHalfBytes + (M == 64 ? M * 512 : 0);
+}
+
+// MN-major shared-memory descriptor for V with 128-byte swizzle: 64 dims
+// (128 B) per swizzled row, one row per key; 8-key atoms 1 KiB apart (stride
+// offset), the two 64-dim halves of a 128-key box 16 KiB apart (leading
+// offset) -- the reading a layout probe confirmed on the GB300.
+BIV_DEV uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(16384u >> 4) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+struct TcItem {
+    int tile, kvh, split, maxpos, slot0;
+};
+
+// Work item `item` in the live (or, past the tables, dense) numbering.
+BIV_DEV TcItem tc_decode(const AttnParams& P, bool live_mode, long long item, const int* s_pref,
+                         const int* s_tmax, const int* s_slot0) {
+    TcItem it;
     if (live_mode) {
-        // the tile whose prefix range holds the item: the last t with s_pref[t] <= item
-        int lo = 0, hi = n_tiles - 1;
+        int lo = 0, hi = P.n_tiles - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (s_pref[mid] <= item) lo = mid; else hi = mid - 1;
         }
-        tile = lo;
+        it.tile = lo;
         const int r = static_cast<int>(item - s_pref[lo]);
-        kvh = r % P.Hkv;
-        split = r / P.Hkv;
+        it.kvh = r % P.Hkv;
+        it.split = r / P.Hkv;
+        it.maxpos = s_tmax[lo];
+        it.slot0 = s_slot0[lo];
     } else {
-        tile = static_cast<int>(item % n_tiles);
-        const long long rest = item / n_tiles;
-        kvh = static_cast<int>(rest % P.Hkv);
-        split = static_cast<int>(rest / P.Hkv);
+        it.tile = static_cast<int>(item % P.n_tiles);
+        const long long rest = item / P.n_tiles;
+        it.kvh = static_cast<int>(rest % P.Hkv);
+        it.split = static_cast<int>(rest / P.Hkv);
+        it.maxpos = tile_maxpos(P, it.tile);
+        int row0, nr;
+        tile_rows_of(P, it.tile, row0, nr);
+        it.slot0 = nr > 0 ? P.row_slot[row0] : -1;
     }
-    const int key0 = split * SPLIT;
-    const int maxpos = tile < kMaxTilesSmem ? s_tmax[tile] : tile_maxpos(P, tile);
-    if (maxpos < key0) continue;                // no row of the tile reaches this split
-    int row0, nr;
-    tile_rows_of(P, tile, row0, nr);
-    const int T = nr * P.G;                     // live tile rows (row-major over (row, head))
-    const int T16 = (T + 15) & ~15;
+    return it;
+}
 
-    // a processed tile's first row has a usable slot (else the tile has no items)
-    const int slot0 = live_mode ? s_slot0[tile] : P.row_slot[row0];
-    const int n_keys = min(SPLIT, maxpos + 1 - key0);
-    const int n_chunks = (n_keys + CHUNK - 1) / CHUNK;
+template <int M>
+__global__ void __launch_bounds__(ATTN_THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const AttnParams P) {
+    static_assert(M == 64 || M == 128, "MMA rows");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;                                // [2 dim halves][M rows][128 B]
+    uint8_t* sK = sQ + M * 256;                        // [2 key halves][2 dim halves][128 keys][128 B]
+    uint8_t* sV = sK + 2 * kTcKeyHalfBytes;
+    uint8_t* sP = M == 64 ? sV + 2 * kTcKeyHalfBytes : sK;   // [4 key quarters][M rows][128 B]
+    const uint32_t uQ = smem_u32(sQ), uK = smem_u32(sK), uV = smem_u32(sV), uP = smem_u32(sP);
 
-    uint8_t* sQ = smem;                         // [T16][HD], 256-B rows, swz()
-    uint8_t* sK = smem + ((T16 * ROWB + 1023) & ~1023);   // [4 chunks] TMA images, swz_kv()
-    uint8_t* sV = sK + SPLIT * ROWB;
-    const uint32_t uQ = smem_u32(sQ), uK = smem_u32(sK), uV = smem_u32(sV);
+    __shared__ int s_pos[BIV_ATTN_TILE];
+    __shared__ __align__(8) uint64_t kbar[2], vbar[2], sbar, obar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int abort_flag;
+    __shared__ float s_mx[2][128], s_sum[2][128], s_rowm[128];
+    __shared__ int s_tmax[kMaxTilesSmem];
+    __shared__ int s_pref[kMaxTilesSmem + 1];
+    __shared__ int s_slot0[kMaxTilesSmem];
+    __shared__ int s_wsum[ATTN_THREADS / 32];
 
-    // ---- K/V of the split first: one TMA box per 64-key chunk and matrix,
-    // each chunk completing on its own barrier; then the rows' positions and
-    // Q (zero rows >= T) with cp.async.
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        fence_proxy_async_smem();               // earlier generic writes to this memory come first
-        const int kv_row = (slot0 * P.Hkv + kvh) * P.max_len + key0;
-        for (int c = 0; c < n_chunks; ++c) {
-            mbar_arrive_expect_tx(&kv_bar[c], 2u * kKvChunkBytes);
-            tma_load_3d(sK + c * kKvChunkBytes, &tmK, &kv_bar[c], 0, kv_row + c * CHUNK, 0, policy_evict_first());
-            tma_load_3d(sV + c * kKvChunkBytes, &tmV, &kv_bar[c], 0, kv_row + c * CHUNK, 0, policy_evict_first());
+        abort_flag = 0;
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kbar[i], 1);
+            mbar_init(&vbar[i], 1);
         }
+        mbar_init(&sbar, 1);
+        mbar_init(&obar, 1);
+        fence_mbar_init();
     }
-    if (threadIdx.x < nr) {
-        const int w = row0 + threadIdx.x;
-        int p = -1;
-        if (row_ok(P, w, slot0)) p = P.row_pos[w];
-        s_pos[threadIdx.x] = p;
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, kTmemCols);
+        tmem_relinquish();
     }
-    for (int idx = threadIdx.x; idx < T16 * 16; idx += ATTN_THREADS) {
-        const int t = idx >> 4, c = idx & 15;
-        if (t < T) {
+    tc_fence_before();
+    pdl_wait();
+    pdl_trigger();
+    const bool live_mode = build_tile_tables(P, s_tmax, s_pref, s_slot0, s_wsum);   // ends with a barrier
+    tc_fence_after();
+    const uint32_t tS = s_tmem, tO = s_tmem + 256;
+    const long long n_work =
+        live_mode ? s_pref[kMaxTilesSmem] : static_cast<long long>(P.s_max) * P.Hkv * P.n_tiles;
+
+    // Barrier phases: *_use counts the phases every thread has waited for (the
+    // next wait targets parity use & 1); thread 0 also counts the phases it
+    // has started (*_iss) and seen complete (*_seen), to drain after a time-out.
+    uint32_t k_use[2] = {0u, 0u}, v_use[2] = {0u, 0u}, s_use = 0u, o_use = 0u;
+    uint32_t k_iss[2] = {0u, 0u}, v_iss[2] = {0u, 0u}, s_iss = 0u, o_iss = 0u;
+    uint32_t k_seen[2] = {0u, 0u}, v_seen[2] = {0u, 0u}, s_seen = 0u, o_seen = 0u;
+
+    auto n_keys_of = [&](const TcItem& it) { return min(SPLIT, it.maxpos + 1 - it.split * SPLIT); };
+    // thread 0: the K or V boxes of an item
+    auto load_kv = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bars, uint32_t* iss, const TcItem& it) {
+        const int nkh = n_keys_of(it) > 128 ? 2 : 1;
+        const int kv_row = (it.slot0 * P.Hkv + it.kvh) * P.max_len + it.split * SPLIT;
+        for (int kh = 0; kh < nkh; ++kh) {
+            mbar_arrive_expect_tx(&bars[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
+            tma_load_3d(dst + kh * kTcKeyHalfBytes, map, &bars[kh], 0, kv_row + kh * 128, 0, policy_evict_first());
+            ++iss[kh];
+        }
+    };
+    // all threads: the item's Q rows into sQ (K-major, 128-byte swizzle)
+    auto load_q = [&](const TcItem& it) {
+        int row0, nr;
+        tile_rows_of(P, it.tile, row0, nr);
+        const int T = nr * P.G;
+        for (int idx = threadIdx.x; idx < T * 16; idx += ATTN_THREADS) {
+            const int t = idx >> 4, c = idx & 15;
             const int i = t / P.G, g = t - i * P.G;
             const __nv_bfloat16* src =
-                P.q + (static_cast<long long>(row0 + i) * P.Hq + kvh * P.G + g) * HD + c * 8;
-            cp_async16(uQ + swz(t, c), src);
-        } else {
-            *reinterpret_cast<uint4*>(sQ + swz(t, c)) = make_uint4(0, 0, 0, 0);
+                P.q + (static_cast<long long>(row0 + i) * P.Hq + it.kvh * P.G + g) * HD + c * 8;
+            cp_async16(uQ + (c >> 3) * (M * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4), src);
         }
-    }
-    cp_async_commit();
-
-    // ---- per block of 16 tile rows, warp w takes 64-key chunk w / 2 and head
-    // dims [64 (w % 2), 64 (w % 2) + 64): S = Q K^T over the chunk, its softmax,
-    // O = P V for its dims.  The four chunk partials are merged in increasing
-    // chunk order.  Every row's arithmetic is the same whatever else is in
-    // the tile.
-    cp_async_wait<0>();
-    __syncthreads();                            // Q (and the barrier init) visible to all
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 2, cq = lane & 3;     // mma fragment coordinates
-    const int ch = warp >> 1, hh = warp & 1;
-    bool have = false;                          // this warp's chunk landed
-    if (ch < n_chunks) {
-        have = mbar_wait(&kv_bar[ch], (kv_parity >> ch) & 1u, &abort_flag, &g_attn_err);
-        // Keys past the last one any row of the tile reads may hold anything
-        // (they are read in whole 64-key boxes): zero this warp's half of V there,
-        // so a masked score (p = 0) never meets a NaN.  K needs nothing: its
-        // scores are replaced by -inf with a select.
-        const int nk = n_keys - ch * CHUNK;
-        if (have && nk < CHUNK) {
-            for (int idx = lane; idx < (CHUNK - nk) * 8; idx += 32) {
-                const int key = ch * CHUNK + nk + (idx >> 3), c = hh * 8 + (idx & 7);
-                *reinterpret_cast<uint4*>(sV + swz_kv(key, c)) = make_uint4(0, 0, 0, 0);
-            }
+        cp_async_commit();
+    };
+    // the CTA's next item at or after `from` that has work (dense numbering skips dead ones)
+    auto next_live = [&](long long from) {
+        for (long long j = from; j < n_work; j += gridDim.x) {
+            if (live_mode) return j;
+            const TcItem it = tc_decode(P, false, j, s_pref, s_tmax, s_slot0);
+            if (it.maxpos >= it.split * SPLIT) return j;
         }
-        __syncwarp();
-    }
-    float* sPO = reinterpret_cast<float*>(sV + SPLIT * ROWB);    // [4 chunks][16 rows][HD]
-    float* sPM = sPO + 4 * 16 * HD;                              // [4][16] chunk maxima (log2 units)
-    float* sPL = sPM + 4 * 16;                                   // [4][16] chunk weight sums
+        return n_work;
+    };
+    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&abort_flag) != 0; };
+    // thread 0: wait for the next phase of a load barrier before issuing MMAs
+    auto take = [&](uint64_t* bar, uint32_t use, uint32_t& seen) {
+        const bool got = mbar_wait(bar, use & 1u, &abort_flag, &g_attn_err, true);
+        if (got) ++seen;
+        return got;
+    };
 
+    long long item = next_live(blockIdx.x);
+    TcItem cur = {};
+    if (item < n_work) {
+        cur = tc_decode(P, live_mode, item, s_pref, s_tmax, s_slot0);
+        if (threadIdx.x == 0) {
+            load_kv(&tmK, sK, kbar, k_iss, cur);
+            load_kv(&tmV, sV, vbar, v_iss, cur);
+        }
+        load_q(cur);
+    }
+    bool ok = true;
 #pragma unroll 1
-    for (int rb = 0; rb < T16 / 16; ++rb) {
-        const int trow_a = rb * 16 + gq, trow_b = trow_a + 8;
-        const int pos_a = trow_a < T ? s_pos[trow_a / P.G] : -1;
-        const int pos_b = trow_b < T ? s_pos[trow_b / P.G] : -1;
-        float o[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-        float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
-        if (have) {
-            // ---- S = Q K^T for 16 rows x 64 keys
-            float sc[8][4];
-#pragma unroll
-            for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(uQ + swz(rb * 16 + (lane & 15), kk * 2 + (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    const int j = lane >> 3;
-                    const int key = ch * CHUNK + np * 16 + (j >> 1) * 8 + (lane & 7);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(uK + swz_kv(key, kk * 2 + (j & 1)), b0, b1, b2, b3);
-                    mma_bf16_16816(sc[2 * np], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(sc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-            // ---- mask (select, never multiply), scale into log2 units, chunk max
-            const int kbase = key0 + ch * CHUNK + cq * 2;
-            float cmax_a = -INFINITY, cmax_b = -INFINITY;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int key = kbase + n * 8 + e;
-                    sc[n][e] = key <= pos_a ? sc[n][e] * P.scale_log2 : -INFINITY;
-                    sc[n][2 + e] = key <= pos_b ? sc[n][2 + e] * P.scale_log2 : -INFINITY;
-                    cmax_a = fmaxf(cmax_a, sc[n][e]);
-                    cmax_b = fmaxf(cmax_b, sc[n][2 + e]);
-                }
-            }
-            cmax_a = fmaxf(cmax_a, __shfl_xor_sync(0xffffffffu, cmax_a, 1));
-            cmax_a = fmaxf(cmax_a, __shfl_xor_sync(0xffffffffu, cmax_a, 2));
-            cmax_b = fmaxf(cmax_b, __shfl_xor_sync(0xffffffffu, cmax_b, 1));
-            cmax_b = fmaxf(cmax_b, __shfl_xor_sync(0xffffffffu, cmax_b, 2));
-            const float mu_a = cmax_a == -INFINITY ? 0.0f : cmax_a;   // a row with no key in the chunk
-            const float mu_b = cmax_b == -INFINITY ? 0.0f : cmax_b;
-            m_a = cmax_a;
-            m_b = cmax_b;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    sc[n][e] = exp2f(sc[n][e] - mu_a);
-                    sc[n][2 + e] = exp2f(sc[n][2 + e] - mu_b);
-                    l_a += sc[n][e];
-                    l_b += sc[n][2 + e];
-                }
-            }
-            // ---- O = P V for this warp's 64 dims (P from the S accumulators)
-#pragma unroll
-            for (int kk = 0; kk < CHUNK / 16; ++kk) {
-                const uint32_t p0 = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
-                const uint32_t p1 = pack_bf16x2(sc[2 * kk][2], sc[2 * kk][3]);
-                const uint32_t p2 = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-                const uint32_t p3 = pack_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-                for (int nd = 0; nd < 4; ++nd) {
-                    const int j = lane >> 3;
-                    const int key = ch * CHUNK + kk * 16 + (j & 1) * 8 + (lane & 7);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(uV + swz_kv(key, (hh * 4 + nd) * 2 + (j >> 1)), b0, b1, b2, b3);
-                    mma_bf16_16816(o[2 * nd], p0, p1, p2, p3, b0, b1);
-                    mma_bf16_16816(o[2 * nd + 1], p0, p1, p2, p3, b2, b3);
-                }
-            }
-            // row sums across the quad (fixed order)
-            l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-            l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-            l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-            l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    while (item < n_work) {
+        const int key0 = cur.split * SPLIT;
+        const int n_keys = n_keys_of(cur);
+        const int nkh = n_keys > 128 ? 2 : 1;
+        const int n16 = (n_keys + 15) >> 4;
+        int row0, nr;
+        tile_rows_of(P, cur.tile, row0, nr);
+        const int T = nr * P.G;
+        if (threadIdx.x < nr) {
+            const int w = row0 + threadIdx.x;
+            s_pos[threadIdx.x] = row_ok(P, w, cur.slot0) ? P.row_pos[w] : -1;
         }
-        // ---- the chunk partial into shared memory
+        const long long nxt_item = next_live(item + gridDim.x);
+        const bool has_nxt = nxt_item < n_work;
+        TcItem nxt = {};
+        if (has_nxt) nxt = tc_decode(P, live_mode, nxt_item, s_pref, s_tmax, s_slot0);
+
+        // ---- Q landed (cp.async, every thread) and visible to the tensor core
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(aborted())) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        // ---- S = Q K^T, issued by one thread
+        if (threadIdx.x == 0) {
+            bool got = true;
+            for (int kh = 0; kh < nkh && got; ++kh) got = take(&kbar[kh], k_use[kh], k_seen[kh]);
+            if (got) {
+                tc_fence_after();
+                constexpr uint32_t idS = idesc_bf16_f32(M, 128);
+                for (int kh = 0; kh < nkh; ++kh)
+                    for (int k = 0; k < HD / 16; ++k) {
+                        const uint64_t a = sw128_kmajor_desc(uQ + (k >> 2) * (M * 128) + (k & 3) * 32);
+                        const uint64_t b =
+                            sw128_kmajor_desc(uK + kh * kTcKeyHalfBytes + (k >> 2) * 16384 + (k & 3) * 32);
+                        umma_bf16(tS + kh * 128, a, b, idS, k > 0 ? 1u : 0u);
+                    }
+                umma_commit(&sbar);
+            } else {
+                mbar_arrive(&sbar);                        // nothing issued: release the waiters
+            }
+            ++s_iss;
+        }
+        for (int kh = 0; kh < nkh; ++kh) ++k_use[kh];
+        if (mbar_wait(&sbar, s_use & 1u, &abort_flag, &g_attn_err) && threadIdx.x == 0) ++s_seen;
+        ++s_use;
+        tc_fence_after();
+        // ---- S is in TMEM: this item's Q (and K for M = 64) may be overwritten
+        if (has_nxt && !aborted()) {
+            if (M == 64 && threadIdx.x == 0) load_kv(&tmK, sK, kbar, k_iss, nxt);
+            load_q(nxt);
+        }
+
+        // ---- softmax over the split, row by row
+        const int q4 = warp & 3, ch = warp >> 2;
+        const float sl2 = P.scale_log2;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+        const int r = M == 64 ? 16 * q4 + (lane & 15) : 32 * q4 + lane;
+        const int hi = M == 64 ? (lane >> 4) : 0;
+        const int pos = r < T ? s_pos[r / P.G] : -1;
+        float m = -INFINITY;
+        if (M == 64) {
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                const int c = 128 * ch + 32 * i;
+                uint32_t v[16];
+                tmem_ld16x2_sync(tS + lane_base + c, v);
+                const int kk = key0 + c + 16 * hi;
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            const int d = hh * 64 + n * 8 + cq * 2;
-            *reinterpret_cast<float2*>(sPO + (ch * 16 + gq) * HD + d) = make_float2(o[n][0], o[n][1]);
-            *reinterpret_cast<float2*>(sPO + (ch * 16 + gq + 8) * HD + d) = make_float2(o[n][2], o[n][3]);
+                for (int t = 0; t < 16; ++t)
+                    if (kk + t <= pos) m = fmaxf(m, __fmul_rn(__uint_as_float(v[t]), sl2));
+            }
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        } else {
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                const int c = 128 * ch + 32 * i;
+                uint32_t v[32];
+                tmem_ld32_sync(tS + lane_base + c, v);
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    if (key0 + c + t <= pos) m = fmaxf(m, __fmul_rn(__uint_as_float(v[t]), sl2));
+            }
         }
-        if (hh == 0 && cq == 0) {
-            sPM[ch * 16 + gq] = m_a;
-            sPM[ch * 16 + gq + 8] = m_b;
-            sPL[ch * 16 + gq] = l_a;
-            sPL[ch * 16 + gq + 8] = l_b;
+        if (hi == 0) s_mx[ch][r] = m;
+        if (__syncthreads_or(aborted())) {
+            ok = false;
+            break;
         }
-        __syncthreads();
-        // ---- merge the four chunks (increasing order), write the split's partial
+        m = fmaxf(s_mx[0][r], s_mx[1][r]);
+        const float mu = m == -INFINITY ? 0.0f : m;       // a row with no key in the split
+        // l: every 16-key group summed in key order, pairs of groups added, then
+        // ((q0 + q1) + (q2 + q3)) per 128-key half and the halves -- the same
+        // order for M = 64 and M = 128, so a row's sum never depends on the tile.
+        float l = 0.0f;
+        float gq[4];
+        if (M == 64) {
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                const int c = 128 * ch + 32 * i;
+                uint32_t v[16];
+                tmem_ld16x2_sync(tS + lane_base + c, v);
+                const int kc = c + 16 * hi;                   // first key (within the split) of these 16
+                uint32_t pk[8];
+                float lg = 0.0f;                              // this 16-key group's sum, in key order
+#pragma unroll
+                for (int t = 0; t < 16; t += 2) {
+                    const float p0 =
+                        key0 + kc + t <= pos ? exp2f(__fmul_rn(__uint_as_float(v[t]), sl2) - mu) : 0.0f;
+                    const float p1 =
+                        key0 + kc + t + 1 <= pos ? exp2f(__fmul_rn(__uint_as_float(v[t + 1]), sl2) - mu) : 0.0f;
+                    lg += p0;
+                    lg += p1;
+                    pk[t >> 1] = pack_bf16x2(p0, p1);
+                }
+                // groups 2i (hi = 0) and 2i + 1 (hi = 1) of this half: even + odd, in both threads
+                const float lo = __shfl_xor_sync(0xffffffffu, lg, 16);
+                gq[i] = hi ? lo + lg : lg + lo;
+                uint8_t* prow = sP + (kc >> 6) * (M * 128) + r * 128;
+                const int pc = (kc & 63) >> 3;
+                *reinterpret_cast<uint4*>(prow + ((pc ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(prow + (((pc + 1) ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+            l = (gq[0] + gq[1]) + (gq[2] + gq[3]);
+        } else {
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                const int c = 128 * ch + 32 * i;
+                uint32_t v[32];
+                tmem_ld32_sync(tS + lane_base + c, v);
+                uint32_t pk[16];
+                float lg[2] = {0.0f, 0.0f};                   // the two 16-key groups' sums, in key order
+#pragma unroll
+                for (int t = 0; t < 32; t += 2) {
+                    const float p0 =
+                        key0 + c + t <= pos ? exp2f(__fmul_rn(__uint_as_float(v[t]), sl2) - mu) : 0.0f;
+                    const float p1 =
+                        key0 + c + t + 1 <= pos ? exp2f(__fmul_rn(__uint_as_float(v[t + 1]), sl2) - mu) : 0.0f;
+                    lg[t >> 4] += p0;
+                    lg[t >> 4] += p1;
+                    pk[t >> 1] = pack_bf16x2(p0, p1);
+                }
+                gq[i] = lg[0] + lg[1];
+                uint8_t* prow = sP + (c >> 6) * (M * 128) + r * 128;
+                const int pc = (c & 63) >> 3;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(prow + (((pc + q) ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
+            l = (gq[0] + gq[1]) + (gq[2] + gq[3]);
+        }
+        if (hi == 0) s_sum[ch][r] = l;
+        if (hi == 0 && ch == 0) s_rowm[r] = m;
+        // ---- V rows from the split's last key up to the next 16-key step: zero
+        // (a masked p = 0 must never meet a NaN in P V)
+        if (warp == 7 && (n_keys & 15) != 0) {
+            const int kl = nkh - 1;
+            if (mbar_wait(&vbar[kl], v_use[kl] & 1u, &abort_flag, &g_attn_err)) {
+                for (int idx = lane; idx < (16 * n16 - n_keys) * 16; idx += 32) {
+                    const int key = n_keys + (idx >> 4), dh = (idx >> 3) & 1, pc = idx & 7;
+                    *reinterpret_cast<uint4*>(sV + (key >> 7) * kTcKeyHalfBytes + dh * 16384 + (key & 127) * 128 +
+                                              pc * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(aborted())) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        // ---- O = P V, issued by one thread
+        if (threadIdx.x == 0) {
+            bool got = true;
+            for (int kh = 0; kh < nkh && got; ++kh) got = take(&vbar[kh], v_use[kh], v_seen[kh]);
+            if (got) {
+                tc_fence_after();
+                constexpr uint32_t idO = idesc_bf16_f32(M, 128) | (1u << 16);   // B (V) MN-major
+                for (int st = 0; st < n16; ++st) {
+                    const uint64_t a = sw128_kmajor_desc(uP + (st >> 2) * (M * 128) + (st & 3) * 32);
+                    const uint64_t b = sw128_mnmajor_desc(uV + (st >> 3) * kTcKeyHalfBytes + (st & 7) * 2048);
+                    umma_bf16(tO, a, b, idO, st > 0 ? 1u : 0u);
+                }
+                umma_commit(&obar);
+            } else {
+                mbar_arrive(&obar);
+            }
+            ++o_iss;
+        }
+        for (int kh = 0; kh < nkh; ++kh) ++v_use[kh];
+        if (mbar_wait(&obar, o_use & 1u, &abort_flag, &g_attn_err) && threadIdx.x == 0) ++o_seen;
+        ++o_use;
+        tc_fence_after();
+        // ---- V (and, for M = 128, K's space, which held P) are free: next loads
+        if (threadIdx.x == 0 && has_nxt && !aborted()) {
+            fence_proxy_async_smem();
+            if (M == 128) load_kv(&tmK, sK, kbar, k_iss, nxt);
+            load_kv(&tmV, sV, vbar, v_iss, nxt);
+        }
+        // ---- the split's partial of every tile row that reaches it
         {
-            const int r = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
-            const int trow = rb * 16 + r;
-            const int pos = trow < T ? s_pos[trow / P.G] : -1;
-            if (pos >= key0) {
-                float M = sPM[r];
+            const int i = r / P.G, g = r - i * P.G;
+            const long long ph =
+                (static_cast<long long>(row0 + i) * P.Hq + cur.kvh * P.G + g) * P.s_max + cur.split;
+            float* dst = P.ws_o + ph * HD;
+            if (M == 64) {
+#pragma unroll 1
+                for (int j = 0; j < 2; ++j) {
+                    const int c = 64 * ch + 32 * j;
+                    uint32_t v[16];
+                    tmem_ld16x2_sync(tO + lane_base + c, v);
+                    if (pos >= key0) {
+                        float4* d4 = reinterpret_cast<float4*>(dst + c + 16 * hi);
 #pragma unroll
-                for (int c = 1; c < 4; ++c) M = fmaxf(M, sPM[c * 16 + r]);
-                float L = 0.0f;
-                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float mc = sPM[c * 16 + r];
-                    const float wc = mc == -INFINITY ? 0.0f : exp2f(mc - M);
-                    L += wc * sPL[c * 16 + r];
-                    const float4 u0 = *reinterpret_cast<const float4*>(sPO + (c * 16 + r) * HD + d0);
-                    const float4 u1 = *reinterpret_cast<const float4*>(sPO + (c * 16 + r) * HD + d0 + 4);
-                    acc[0] += wc * u0.x; acc[1] += wc * u0.y; acc[2] += wc * u0.z; acc[3] += wc * u0.w;
-                    acc[4] += wc * u1.x; acc[5] += wc * u1.y; acc[6] += wc * u1.z; acc[7] += wc * u1.w;
+                        for (int q = 0; q < 4; ++q)
+                            d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    }
                 }
-                const int i = trow / P.G, g = trow - i * P.G;
-                const long long ph = (static_cast<long long>(row0 + i) * P.Hq + kvh * P.G + g) * P.s_max + split;
-                float* dst = P.ws_o + ph * HD + d0;
-                *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-                if (d0 == 0) {
-                    P.ws_m[ph] = M;
-                    P.ws_l[ph] = L;
+            } else {
+#pragma unroll 1
+                for (int j = 0; j < 2; ++j) {
+                    const int c = 64 * ch + 32 * j;
+                    uint32_t v[32];
+                    tmem_ld32_sync(tO + lane_base + c, v);
+                    if (pos >= key0) {
+                        float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    }
                 }
             }
+            if (pos >= key0 && ch == 0 && hi == 0) {
+                P.ws_m[ph] = s_rowm[r];
+                P.ws_l[ph] = s_sum[0][r] + s_sum[1][r];
+            }
         }
-        __syncthreads();      // the partial buffers are reused by the next row block
+        tc_fence_before();
+        if (__syncthreads_or(aborted())) {              // TMEM, s_mx, s_sum, s_rowm, s_pos are reused
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        item = nxt_item;
+        cur = nxt;
     }
-    if (threadIdx.x == 0 && abort_flag)
-        for (int c = 0; c < n_chunks; ++c) mbar_wait_drain(&kv_bar[c], (kv_parity >> c) & 1u);   // land first
-    kv_parity ^= (1u << n_chunks) - 1u;
-    if (abort_flag) break;
+    // ---- leave.  After a time-out, the copies and MMAs already started
+    // complete first (bounded waits), then TMEM is freed.
+    cp_async_wait<0>();
+    if (threadIdx.x == 0 && !ok) {
+        for (int kh = 0; kh < 2; ++kh) {
+            for (uint32_t j = k_seen[kh]; j < k_iss[kh]; ++j) mbar_wait_drain(&kbar[kh], j & 1u);
+            for (uint32_t j = v_seen[kh]; j < v_iss[kh]; ++j) mbar_wait_drain(&vbar[kh], j & 1u);
+        }
+        for (uint32_t j = s_seen; j < s_iss; ++j) mbar_wait_drain(&sbar, j & 1u);
+        for (uint32_t j = o_seen; j < o_iss; ++j) mbar_wait_drain(&obar, j & 1u);
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(s_tmem, kTmemCols);
 }
 
 // One warp per (row, head): combine splits 0 .. pos/256 of the row.  Lane s
@@ -677,9 +829,6 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
     const long long n_tiles = n_groups * P.tiles_per_group;
     if (n_tiles > 0x7fffffffLL / 64 || Hkv > 65535) return BIV_ERR_SHAPE;
     P.n_tiles = static_cast<int>(n_tiles);
-    const int T16max = ((P.tile_rows * P.G + 15) / 16) * 16;
-    const size_t smem = 1024 + ((static_cast<size_t>(T16max) * ROWB + 1023) & ~static_cast<size_t>(1023)) +
-                        2 * SPLIT * ROWB + kPartialBytes;
     // K and V caches as TMA sees them: [2 halves of a row][n_slots*Hkv*max_len rows][64 elements]
     CUtensorMap tk, tv;
     {
@@ -690,7 +839,7 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
         }
         cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(n_slots) * Hkv * max_len, 2};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(ROWB), 128};
-        cuuint32_t box[3] = {64, CHUNK, 2};
+        cuuint32_t box[3] = {64, 128, 2};
         cuuint32_t es[3] = {1, 1, 1};
         const void* bases[2] = {k_cache, v_cache};
         CUtensorMap* maps[2] = {&tk, &tv};
@@ -708,15 +857,23 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             1024 + BIV_ATTN_TILE * ROWB + 2 * SPLIT * ROWB + kPartialBytes);
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(tc_smem_bytes<64>()));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(tc_smem_bytes<128>()));
         if (e != cudaSuccess) return cuda_status(e);
         configured_device = dev;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const long long n_items = static_cast<long long>(s_max) * Hkv * n_tiles;
     const int grid = static_cast<int>(std::min<long long>(n_items, num_sms()));
-    int st = launch_pdl(attn_split_kernel, dim3(static_cast<unsigned>(grid)), dim3(ATTN_THREADS), smem, s, tk, tv, P);
+    // MMA rows: 64 when the tile's G x rows fit, else 128
+    int st = P.tile_rows * P.G <= 64
+                 ? launch_pdl(attn_tc_kernel<64>, dim3(static_cast<unsigned>(grid)), dim3(ATTN_THREADS),
+                              tc_smem_bytes<64>(), s, tk, tv, P)
+                 : launch_pdl(attn_tc_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(ATTN_THREADS),
+                              tc_smem_bytes<128>(), s, tk, tv, P);
     if (st != BIV_OK) return st;
     const long long n_pairs = static_cast<long long>(W) * Hq;
     return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>((n_pairs + 7) / 8)), dim3(256), 0, s, P,

@@ -226,6 +226,17 @@ def test_attention_rows_are_batch_invariant():
     assert same_bits(_run_attn(qd, kd3, vd3, slot, pos, 8), full)
 
 
+def test_attention_rows_invariant_across_mma_shapes():
+    """A full 128-row tile (G = 8 heads x 16 rows: 128-row MMAs) and the same
+    rows one at a time (8 rows: 64-row MMAs) give the same bits, splits with a
+    ragged last 16-key step included."""
+    q, kc, vc, slot, pos = _attn_case(3, 8, 1, 1100, [5, 290, 1000], 16, seed=19)
+    qd, kd, vd = dev(q), dev(kc), dev(vc)
+    full = _run_attn(qd, kd, vd, slot, pos, 16)
+    alone = _run_attn(qd, kd, vd, slot, pos, 1)
+    assert same_bits(alone, full)
+
+
 def test_attention_bad_position_raises_device_error():
     q, kc, vc, slot, pos = _attn_case(2, 8, 2, 600, [100, 300], 4, seed=12)
     qd, kd, vd = dev(q), dev(kc), dev(vc)
