@@ -143,6 +143,9 @@ int biv_gemm_tile_n(int M, int N, int K);
  * j <= p must hold finite values.
  * workspace: device memory of at least biv_decode_attn_workspace_size(W, Hq,
  * max_len) bytes, 16-B aligned, contents ignored on entry.
+ * row_slot and row_pos are read while the previous libbiv kernel on the
+ * stream may still be finishing (programmatic dependent launch); they must
+ * not be written by that kernel.  q and the caches are read after it.
  * Requires hd == 128, kv_split == 256, Hq % Hkv == 0, Hq/Hkv <= 128.        */
 size_t biv_decode_attn_workspace_size(int W, int Hq, int max_len);
 int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, const void* v_cache,

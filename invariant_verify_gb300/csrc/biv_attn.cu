@@ -283,11 +283,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         tmem_alloc(&s_tmem, kTmemCols);
         tmem_relinquish();
     }
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
     tc_fence_before();
-    pdl_wait();
-    pdl_trigger();
+    // The tile tables read only the window's slots and positions, inputs of
+    // the call rather than outputs of the previous kernel: built while that
+    // kernel finishes.  Q, K and V are read after the wait.
     const bool live_mode = build_tile_tables(P, s_tmax, s_pref, s_slot0, s_wsum);   // ends with a barrier
     tc_fence_after();
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tS = s_tmem, tO = s_tmem + 256;
     const long long n_work =
         live_mode ? s_pref[kMaxTilesSmem] : static_cast<long long>(P.s_max) * P.Hkv * P.n_tiles;
@@ -627,17 +634,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 // One warp per (row, head): combine splits 0 .. pos/256 of the row.  Lane s
 // holds split s (32 at a time); the maximum and the weight sum are reduced
 // with a fixed xor butterfly, the outputs are summed in increasing split
-// order.  All loads of a group of splits are independent, so they overlap.
+// order.  The row's slot and position are inputs of the call, not outputs of
+// the split kernel, so they are read while it finishes; after it, one round
+// of loads fetches every lane's (m, l) and the first kCombinePre splits'
+// outputs together.
+constexpr int kCombinePre = 8;
+
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
-    pdl_wait();
-    pdl_trigger();
     const long long pair = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (pair >= static_cast<long long>(P.W) * P.Hq) return;
-    const int w = static_cast<int>(pair / P.Hq);
-    const int grp0 = (w / P.rows_per_group) * P.rows_per_group;
-    const int slot = P.row_slot[w], p = P.row_pos[w], slot0 = P.row_slot[grp0];
+    const bool in = pair < static_cast<long long>(P.W) * P.Hq;
+    int slot = -1, p = -1, slot0 = -1;
+    if (in) {
+        const int w = static_cast<int>(pair / P.Hq);
+        const int grp0 = (w / P.rows_per_group) * P.rows_per_group;
+        slot = P.row_slot[w];
+        p = P.row_pos[w];
+        slot0 = P.row_slot[grp0];
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (!in) return;
     __nv_bfloat16* dst = out + pair * HD + lane * 4;
     if (slot < 0 || slot >= P.n_slots || p < 0 || p >= P.max_len || slot != slot0) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
@@ -645,10 +663,17 @@ attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
     }
     const int ns = p / SPLIT + 1;
     const long long base = pair * P.s_max;
+    const float4* src0 = reinterpret_cast<const float4*>(P.ws_o + base * HD) + lane;
+    float4 pre[kCombinePre];
+#pragma unroll
+    for (int j = 0; j < kCombinePre; ++j)
+        pre[j] = j < ns ? src0[static_cast<long long>(j) * (HD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float m0 = lane < ns ? P.ws_m[base + lane] : -INFINITY;
+    const float l0 = lane < ns ? P.ws_l[base + lane] : 0.0f;
     // Row maximum over all splits.
     float M = -INFINITY;
     for (int s0 = 0; s0 < ns; s0 += 32) {
-        float m = (s0 + lane < ns) ? P.ws_m[base + s0 + lane] : -INFINITY;
+        float m = s0 == 0 ? m0 : (s0 + lane < ns) ? P.ws_m[base + s0 + lane] : -INFINITY;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         M = fmaxf(M, m);
@@ -657,17 +682,27 @@ attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < ns; s0 += 32) {
         const int s = s0 + lane;
-        const float wgt = (s < ns) ? exp2f(P.ws_m[base + s] - M) : 0.0f;
-        float lw = (s < ns) ? wgt * P.ws_l[base + s] : 0.0f;
+        const float ms = s0 == 0 ? m0 : (s < ns) ? P.ws_m[base + s] : -INFINITY;
+        const float ls = s0 == 0 ? l0 : (s < ns) ? P.ws_l[base + s] : 0.0f;
+        const float wgt = (s < ns) ? exp2f(ms - M) : 0.0f;
+        float lw = (s < ns) ? wgt * ls : 0.0f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
         L += lw;
         const int cnt = min(32, ns - s0);
-        const float4* src = reinterpret_cast<const float4*>(P.ws_o + (base + s0) * HD) + lane;
+        const float4* src = src0 + static_cast<long long>(s0) * (HD / 4);
 #pragma unroll 4
         for (int j = 0; j < cnt; ++j) {
             const float wj = __shfl_sync(0xffffffffu, wgt, j);
-            const float4 v = src[static_cast<long long>(j) * (HD / 4)];
+            float4 v;
+            if (s0 == 0 && j < kCombinePre) {
+                v = pre[0];
+#pragma unroll
+                for (int q = 1; q < kCombinePre; ++q)
+                    if (j == q) v = pre[q];
+            } else {
+                v = src[static_cast<long long>(j) * (HD / 4)];
+            }
             acc.x += wj * v.x;
             acc.y += wj * v.y;
             acc.z += wj * v.z;

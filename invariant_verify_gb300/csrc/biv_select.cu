@@ -360,10 +360,10 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
 // Philox arithmetic.  The ring runs ahead across rows: the next row's first
 // chunks land during pass 2.
 constexpr int kStreamChunk = 8192;               // floats per ring slot (32 KiB)
-constexpr int kStreamStages = 3;
+constexpr int kStreamStages = 2;
 constexpr int kBlock = 256;                      // logits per block maximum
 constexpr int kMaxStreamV = 1 << 22;             // block maxima kept in shared memory (64 KiB)
-constexpr int kUnroll = 8;                       // pass 2: loads in flight per thread
+constexpr int kUnroll = 4;                       // pass 2: loads in flight per thread
 constexpr int kCtrSlots = 64;                    // row-ticket counter pairs, one per launch in flight
 
 // {next row ticket, CTAs finished} per slot; zero at load, and the last CTA of
@@ -374,7 +374,7 @@ size_t stream_smem_bytes(int V) {
     return static_cast<size_t>(kStreamStages) * kStreamChunk * 4 + static_cast<size_t>((V + kBlock - 1) / kBlock) * 4;
 }
 
-__global__ void __launch_bounds__(kSelThreads, 2)
+__global__ void __launch_bounds__(kSelThreads, 3)
 gumbel_stream_kernel(const float* __restrict__ logits, int R, int V, long long ld,
                      const uint32_t* __restrict__ row_req, const int32_t* __restrict__ row_pos, uint32_t seed_lo,
                      uint32_t seed_hi, float invT, int greedy, int32_t* __restrict__ tokens,
@@ -397,6 +397,7 @@ gumbel_stream_kernel(const float* __restrict__ logits, int R, int V, long long l
         fence_mbar_init();
     }
     gtab[threadIdx.x] = nb.v[threadIdx.x];
+    const float g254 = nb.v[254];                  // largest noise bound below the top byte 255
     __syncthreads();
     pdl_wait();
     pdl_trigger();
@@ -567,8 +568,14 @@ gumbel_stream_kernel(const float* __restrict__ logits, int R, int V, long long l
                     if (!glive[u]) continue;
                     const float e[4] = {v4[u].x, v4[u].y, v4[u].z, v4[u].w};
                     const uint32_t words[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+                    // Below the top byte 255 no noise exceeds g254: if even the
+                    // group's largest logit cannot pass with it, only entries
+                    // whose word has top byte 255 need their own bound.
+                    const float m4 = fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w));
+                    const bool top_only = !no_prune && __fadd_rn(__fmul_rn(m4, invT), g254) < best_f;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
+                        if (top_only && words[j] < 0xFF000000u) continue;
                         const float a = __fmul_rn(e[j], invT);
                         if (!no_prune && !(__fadd_rn(a, gtab[words[j] >> 24]) >= best_f)) continue;
                         const uint32_t vv = static_cast<uint32_t>(v0[u] + j);
