@@ -32,6 +32,14 @@
  *     device error word, read with biv_device_error().
  *   - Inputs are never modified, except the caches of biv_kv_overwrite and the
  *     caller-provided workspace of biv_decode_attn_fixedsplit.
+ *   - Kernels launch with programmatic dependent launch: a kernel may start
+ *     while the previous libbiv kernel on the same stream is finishing, and
+ *     waits for it before reading that kernel's outputs.  A few inputs that
+ *     are never a step's intermediate results are read before that wait:
+ *     GEMM weights (B operands) and the row_slot / row_pos arrays of
+ *     attention.  They must not be written by the immediately preceding
+ *     libbiv kernel on the stream (kernels of other libraries, and copies,
+ *     are waited for in full).
  *   - No call allocates device memory.  The one exception in kind is the fixed
  *     scratch array behind biv_decode_attn_fixedsplit_noalloc, which is part
  *     of the loaded module (BIV_NOALLOC_SCRATCH_BYTES per GPU, held until the
@@ -143,9 +151,6 @@ int biv_gemm_tile_n(int M, int N, int K);
  * j <= p must hold finite values.
  * workspace: device memory of at least biv_decode_attn_workspace_size(W, Hq,
  * max_len) bytes, 16-B aligned, contents ignored on entry.
- * row_slot and row_pos are read while the previous libbiv kernel on the
- * stream may still be finishing (programmatic dependent launch); they must
- * not be written by that kernel.  q and the caches are read after it.
  * Requires hd == 128, kv_split == 256, Hq % Hkv == 0, Hq/Hkv <= 128.        */
 size_t biv_decode_attn_workspace_size(int W, int Hq, int max_len);
 int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, const void* v_cache,

@@ -211,6 +211,26 @@ BIV_DEV uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
+// Four M = 64 TMEM loads (16x32bx2, 16 columns each at c0 + 32 i), one wait.
+// The empty asm statements after the wait tie every register to it, so no
+// use of a loaded value is scheduled before the data is there.
+BIV_DEV void tmem_ld16x2_x4_sync(uint32_t taddr, const int (&c)[4], uint32_t (&v)[4][16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm volatile(
+            "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+            "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 16;"
+            : "=r"(v[i][0]), "=r"(v[i][1]), "=r"(v[i][2]), "=r"(v[i][3]), "=r"(v[i][4]), "=r"(v[i][5]),
+              "=r"(v[i][6]), "=r"(v[i][7]), "=r"(v[i][8]), "=r"(v[i][9]), "=r"(v[i][10]), "=r"(v[i][11]),
+              "=r"(v[i][12]), "=r"(v[i][13]), "=r"(v[i][14]), "=r"(v[i][15])
+            : "r"(taddr + static_cast<uint32_t>(c[i])));
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) asm volatile("" : "+r"(v[i][j]));
+}
+
 struct TcItem {
     int tile, kvh, split, maxpos, slot0;
 };
@@ -424,16 +444,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         const int hi = M == 64 ? (lane >> 4) : 0;
         const int pos = r < T ? s_pos[r / P.G] : -1;
         float m = -INFINITY;
+        const int c4[4] = {128 * ch, 128 * ch + 32, 128 * ch + 64, 128 * ch + 96};
         if (M == 64) {
-#pragma unroll 1
+            uint32_t v[4][16];
+            tmem_ld16x2_x4_sync(tS + lane_base, c4, v);
+#pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int c = 128 * ch + 32 * i;
-                uint32_t v[16];
-                tmem_ld16x2_sync(tS + lane_base + c, v);
-                const int kk = key0 + c + 16 * hi;
+                const int kk = key0 + c4[i] + 16 * hi;
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
-                    if (kk + t <= pos) m = fmaxf(m, __fmul_rn(__uint_as_float(v[t]), sl2));
+                    if (kk + t <= pos) m = fmaxf(m, __fmul_rn(__uint_as_float(v[i][t]), sl2));
             }
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
         } else {
@@ -460,11 +480,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         float l = 0.0f;
         float gq[4];
         if (M == 64) {
-#pragma unroll 1
+            uint32_t va[4][16];
+            tmem_ld16x2_x4_sync(tS + lane_base, c4, va);
+#pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int c = 128 * ch + 32 * i;
-                uint32_t v[16];
-                tmem_ld16x2_sync(tS + lane_base + c, v);
+                const uint32_t (&v)[16] = va[i];
+                const int c = c4[i];
                 const int kc = c + 16 * hi;                   // first key (within the split) of these 16
                 uint32_t pk[8];
                 float lg = 0.0f;                              // this 16-key group's sum, in key order
@@ -634,86 +655,95 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 // One warp per (row, head): combine splits 0 .. pos/256 of the row.  Lane s
 // holds split s (32 at a time); the maximum and the weight sum are reduced
 // with a fixed xor butterfly, the outputs are summed in increasing split
-// order.  The row's slot and position are inputs of the call, not outputs of
-// the split kernel, so they are read while it finishes; after it, one round
-// of loads fetches every lane's (m, l) and the first kCombinePre splits'
-// outputs together.
+// order.  The CTAs are persistent (a warp takes pairs w, w + all warps, ...).
+// A warp's first row's slot and position are inputs of the call, not outputs
+// of the split kernel, so they are read while it finishes; after it, one
+// round of loads fetches every lane's (m, l) and the first kCombinePre
+// splits' outputs together.
 constexpr int kCombinePre = 8;
+
+struct CombineRow {
+    int slot, pos, slot0;
+};
+
+BIV_DEV CombineRow combine_row(const AttnParams& P, long long pair) {
+    const int w = static_cast<int>(pair / P.Hq);
+    const int grp0 = (w / P.rows_per_group) * P.rows_per_group;
+    return CombineRow{P.row_slot[w], P.row_pos[w], P.row_slot[grp0]};
+}
 
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
-    const long long pair = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const long long n_pairs = static_cast<long long>(P.W) * P.Hq;
+    const long long first = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const long long stride = static_cast<long long>(gridDim.x) * 8;
     const int lane = threadIdx.x & 31;
-    const bool in = pair < static_cast<long long>(P.W) * P.Hq;
-    int slot = -1, p = -1, slot0 = -1;
-    if (in) {
-        const int w = static_cast<int>(pair / P.Hq);
-        const int grp0 = (w / P.rows_per_group) * P.rows_per_group;
-        slot = P.row_slot[w];
-        p = P.row_pos[w];
-        slot0 = P.row_slot[grp0];
-    }
+    CombineRow rw = first < n_pairs ? combine_row(P, first) : CombineRow{-1, -1, -1};
     pdl_wait();
     pdl_trigger();
-    if (!in) return;
-    __nv_bfloat16* dst = out + pair * HD + lane * 4;
-    if (slot < 0 || slot >= P.n_slots || p < 0 || p >= P.max_len || slot != slot0) {
-        *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
-        return;
-    }
-    const int ns = p / SPLIT + 1;
-    const long long base = pair * P.s_max;
-    const float4* src0 = reinterpret_cast<const float4*>(P.ws_o + base * HD) + lane;
-    float4 pre[kCombinePre];
-#pragma unroll
-    for (int j = 0; j < kCombinePre; ++j)
-        pre[j] = j < ns ? src0[static_cast<long long>(j) * (HD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float m0 = lane < ns ? P.ws_m[base + lane] : -INFINITY;
-    const float l0 = lane < ns ? P.ws_l[base + lane] : 0.0f;
-    // Row maximum over all splits.
-    float M = -INFINITY;
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-        float m = s0 == 0 ? m0 : (s0 + lane < ns) ? P.ws_m[base + s0 + lane] : -INFINITY;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        M = fmaxf(M, m);
-    }
-    float L = 0.0f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-        const int s = s0 + lane;
-        const float ms = s0 == 0 ? m0 : (s < ns) ? P.ws_m[base + s] : -INFINITY;
-        const float ls = s0 == 0 ? l0 : (s < ns) ? P.ws_l[base + s] : 0.0f;
-        const float wgt = (s < ns) ? exp2f(ms - M) : 0.0f;
-        float lw = (s < ns) ? wgt * ls : 0.0f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-        L += lw;
-        const int cnt = min(32, ns - s0);
-        const float4* src = src0 + static_cast<long long>(s0) * (HD / 4);
-#pragma unroll 4
-        for (int j = 0; j < cnt; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, wgt, j);
-            float4 v;
-            if (s0 == 0 && j < kCombinePre) {
-                v = pre[0];
-#pragma unroll
-                for (int q = 1; q < kCombinePre; ++q)
-                    if (j == q) v = pre[q];
-            } else {
-                v = src[static_cast<long long>(j) * (HD / 4)];
-            }
-            acc.x += wj * v.x;
-            acc.y += wj * v.y;
-            acc.z += wj * v.z;
-            acc.w += wj * v.w;
+#pragma unroll 1
+    for (long long pair = first; pair < n_pairs; pair += stride) {
+        if (pair != first) rw = combine_row(P, pair);
+        __nv_bfloat16* dst = out + pair * HD + lane * 4;
+        const int p = rw.pos;
+        if (rw.slot < 0 || rw.slot >= P.n_slots || p < 0 || p >= P.max_len || rw.slot != rw.slot0) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+            continue;
         }
+        const int ns = p / SPLIT + 1;
+        const long long base = pair * P.s_max;
+        const float4* src0 = reinterpret_cast<const float4*>(P.ws_o + base * HD) + lane;
+        float4 pre[kCombinePre];
+#pragma unroll
+        for (int j = 0; j < kCombinePre; ++j)
+            pre[j] = j < ns ? src0[static_cast<long long>(j) * (HD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float m0 = lane < ns ? P.ws_m[base + lane] : -INFINITY;
+        const float l0 = lane < ns ? P.ws_l[base + lane] : 0.0f;
+        // Row maximum over all splits.
+        float M = -INFINITY;
+        for (int s0 = 0; s0 < ns; s0 += 32) {
+            float m = s0 == 0 ? m0 : (s0 + lane < ns) ? P.ws_m[base + s0 + lane] : -INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            M = fmaxf(M, m);
+        }
+        float L = 0.0f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < ns; s0 += 32) {
+            const int s = s0 + lane;
+            const float ms = s0 == 0 ? m0 : (s < ns) ? P.ws_m[base + s] : -INFINITY;
+            const float ls = s0 == 0 ? l0 : (s < ns) ? P.ws_l[base + s] : 0.0f;
+            const float wgt = (s < ns) ? exp2f(ms - M) : 0.0f;
+            float lw = (s < ns) ? wgt * ls : 0.0f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+            L += lw;
+            const int cnt = min(32, ns - s0);
+            const float4* src = src0 + static_cast<long long>(s0) * (HD / 4);
+#pragma unroll 4
+            for (int j = 0; j < cnt; ++j) {
+                const float wj = __shfl_sync(0xffffffffu, wgt, j);
+                float4 v;
+                if (s0 == 0 && j < kCombinePre) {
+                    v = pre[0];
+#pragma unroll
+                    for (int q = 1; q < kCombinePre; ++q)
+                        if (j == q) v = pre[q];
+                } else {
+                    v = src[static_cast<long long>(j) * (HD / 4)];
+                }
+                acc.x += wj * v.x;
+                acc.y += wj * v.y;
+                acc.z += wj * v.z;
+                acc.w += wj * v.w;
+            }
+        }
+        const float inv = 1.0f / L;
+        uint2 r;
+        r.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        r.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(dst) = r;
     }
-    const float inv = 1.0f / L;
-    uint2 r;
-    r.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    r.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(dst) = r;
 }
 
 // ------------------------------------------------------------------ RoPE
@@ -911,7 +941,15 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
                               tc_smem_bytes<128>(), s, tk, tv, P);
     if (st != BIV_OK) return st;
     const long long n_pairs = static_cast<long long>(W) * Hq;
-    return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>((n_pairs + 7) / 8)), dim3(256), 0, s, P,
+    static int combine_per_sm = 0;                 // resident combine CTAs per SM
+    if (combine_per_sm == 0) {
+        int per = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_combine_kernel, 256, 0) != cudaSuccess || per < 1)
+            per = 1;
+        combine_per_sm = per;
+    }
+    const long long cgrid = std::min<long long>((n_pairs + 7) / 8, static_cast<long long>(num_sms()) * combine_per_sm);
+    return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(cgrid)), dim3(256), 0, s, P,
                       static_cast<__nv_bfloat16*>(o));
 }
 

@@ -417,14 +417,38 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const uint64_t pol_a = policy_evict_last();    // activations: reused by every CTA
+    const uint64_t pol_b = policy_evict_first();   // weights: streamed once
+    // The weights are not an output of the previous kernel: the B boxes of the
+    // first tile's first stages are requested before waiting for it (their A
+    // boxes, the previous kernel's output, after).  Each such stage's barrier
+    // expects both from the start.
+    int b_early = 0;
+    if (warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < n_work) {
+        const int n_blk0 = static_cast<int>(blockIdx.x) / m_tiles;
+        b_early = min(S, n_stage_blocks);
+        for (int sb = 0; sb < b_early; ++sb) {
+            uint8_t* sa = tiles + sb * STAGE;
+            int kb0, nkb;
+            stage_range(g, sb, kb0, nkb);
+            if (g.first1 && sb == 0) {
+                mbar_arrive_expect_tx(&full[sb], tx_bytes1);
+                tma_load_3d(sa + A_BYTES, &tmB1, &full[sb], 0, n_blk0 * BN, 0, pol_b);
+            } else if (g.three_d) {
+                mbar_arrive_expect_tx(&full[sb], tx_bytes);
+                tma_load_3d(sa + A_BYTES, &tmB, &full[sb], 0, n_blk0 * BN, kb0, pol_b);
+            } else {
+                mbar_arrive_expect_tx(&full[sb], tx_bytes);
+                tma_load_2d(sa + A_BYTES, &tmB, &full[sb], sb * kBK, n_blk0 * BN, pol_b);
+            }
+        }
+    }
     pdl_wait();       // inputs of the previous kernel are complete and visible from here on
     pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            const uint64_t pol_a = policy_evict_last();    // activations: reused by every CTA
-            const uint64_t pol_b = policy_evict_first();   // weights: streamed once
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -440,18 +464,19 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     uint8_t* sa = tiles + stage * STAGE;
                     int kb0, nkb;
                     stage_range(g, sb, kb0, nkb);
+                    const bool b_done = t == static_cast<int>(blockIdx.x) && sb < b_early;   // B requested early
                     if (g.first1 && sb == 0) {
-                        mbar_arrive_expect_tx(&full[stage], tx_bytes1);
+                        if (!b_done) mbar_arrive_expect_tx(&full[stage], tx_bytes1);
                         tma_load_3d(sa, &tmA1, &full[stage], 0, m_blk * kBM, 0, pol_a);
-                        tma_load_3d(sa + A_BYTES, &tmB1, &full[stage], 0, n_blk * BN, 0, pol_b);
+                        if (!b_done) tma_load_3d(sa + A_BYTES, &tmB1, &full[stage], 0, n_blk * BN, 0, pol_b);
                     } else if (g.three_d) {
-                        mbar_arrive_expect_tx(&full[stage], tx_bytes);
+                        if (!b_done) mbar_arrive_expect_tx(&full[stage], tx_bytes);
                         tma_load_3d(sa, &tmA, &full[stage], 0, m_blk * kBM, kb0, pol_a);
-                        tma_load_3d(sa + A_BYTES, &tmB, &full[stage], 0, n_blk * BN, kb0, pol_b);
+                        if (!b_done) tma_load_3d(sa + A_BYTES, &tmB, &full[stage], 0, n_blk * BN, kb0, pol_b);
                     } else {
-                        mbar_arrive_expect_tx(&full[stage], tx_bytes);
+                        if (!b_done) mbar_arrive_expect_tx(&full[stage], tx_bytes);
                         tma_load_2d(sa, &tmA, &full[stage], sb * kBK, m_blk * kBM, pol_a);
-                        tma_load_2d(sa + A_BYTES, &tmB, &full[stage], sb * kBK, n_blk * BN, pol_b);
+                        if (!b_done) tma_load_2d(sa + A_BYTES, &tmB, &full[stage], sb * kBK, n_blk * BN, pol_b);
                     }
                     ++issued;
                     if (++stage == S) {
