@@ -298,6 +298,18 @@ int biv_lm_head_gumbel(const void* A, const void* B, float* logits, int M, int N
                        const uint32_t* row_req, const int32_t* row_pos, uint64_t seed, float temperature,
                        int32_t* tokens, void* workspace, size_t ws_bytes, biv_stream_t stream);
 
+/* biv_lm_head_gumbel followed by biv_verify_accept in one launch less: the
+ * per-row winners and the coupled accept of each request are taken by one
+ * small kernel.  M = n_req * rows_per_req rows, request r owning rows
+ * [r*K, (r+1)*K) with K = rows_per_req; draft, p0, accept_len, new_len as in
+ * biv_verify_accept.  tokens, accept_len and new_len are bit-identical to the
+ * two calls.  Requires what both calls require.                           */
+int biv_lm_head_gumbel_accept(const void* A, const void* B, float* logits, int M, int N, int K,
+                              const uint32_t* row_req, const int32_t* row_pos, uint64_t seed, float temperature,
+                              int32_t* tokens, const int32_t* draft, const int32_t* p0, int n_req,
+                              int rows_per_req, int32_t* accept_len, int32_t* new_len, void* workspace,
+                              size_t ws_bytes, biv_stream_t stream);
+
 /* Gumbel top-k ([COUPLING]: the trick gives top-k sampling as it stands;
  * Kool, van Hoof & Welling, "Stochastic Beams and Where to Find Them"):
  * out[r * k + j] = the entry with the (j+1)-th largest key of row r, keys and

@@ -56,6 +56,8 @@ SIGNATURES = {
     "biv_ngram_draft": (_I, [_P, _I, _LL, _P, _I, _I, _I, _P, _P, _P]),
     "biv_lm_head_gumbel_workspace_size": (_SZ, [_I, _I, _I]),
     "biv_lm_head_gumbel": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _U64, _F, _P, _P, _SZ, _P]),
+    "biv_lm_head_gumbel_accept": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _U64, _F, _P, _P, _P, _I, _I, _P, _P, _P,
+                                       _SZ, _P]),
     "biv_gumbel_from_words": (_I, [_P, _LL, _P, _P]),
     "biv_verify_accept": (_I, [_P, _P, _P, _I, _I, _P, _P, _P]),
     "biv_gumbel_bucket_bounds": (_I, [_P]),
@@ -239,6 +241,18 @@ def biv_lm_head_gumbel(A, B, row_req, row_pos, seed: int, temperature: float, to
     _check("biv_lm_head_gumbel", _load().biv_lm_head_gumbel(
         _ptr(A), _ptr(B), _ptr(logits) if logits is not None else None, M, N, K, _ptr(row_req), _ptr(row_pos),
         seed & 0xFFFFFFFFFFFFFFFF, float(temperature), _ptr(tokens), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def biv_lm_head_gumbel_accept(A, B, row_req, row_pos, seed: int, temperature: float, tokens, draft, p0,
+                              n_req: int, rows_per_req: int, accept_len, new_len, workspace, logits=None,
+                              stream=None) -> None:
+    M, K = A.shape
+    N = B.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("biv_lm_head_gumbel_accept", _load().biv_lm_head_gumbel_accept(
+        _ptr(A), _ptr(B), _ptr(logits) if logits is not None else None, M, N, K, _ptr(row_req), _ptr(row_pos),
+        seed & 0xFFFFFFFFFFFFFFFF, float(temperature), _ptr(tokens), _ptr(draft), _ptr(p0), n_req, rows_per_req,
+        _ptr(accept_len), _ptr(new_len), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def biv_gumbel_noise(seed: int, row_req, row_pos, g, stream=None) -> None:

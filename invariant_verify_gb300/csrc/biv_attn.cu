@@ -211,26 +211,6 @@ BIV_DEV uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
     return d;
 }
 
-// Four M = 64 TMEM loads (16x32bx2, 16 columns each at c0 + 32 i), one wait.
-// The empty asm statements after the wait tie every register to it, so no
-// use of a loaded value is scheduled before the data is there.
-BIV_DEV void tmem_ld16x2_x4_sync(uint32_t taddr, const int (&c)[4], uint32_t (&v)[4][16]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        asm volatile(
-            "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
-            "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 16;"
-            : "=r"(v[i][0]), "=r"(v[i][1]), "=r"(v[i][2]), "=r"(v[i][3]), "=r"(v[i][4]), "=r"(v[i][5]),
-              "=r"(v[i][6]), "=r"(v[i][7]), "=r"(v[i][8]), "=r"(v[i][9]), "=r"(v[i][10]), "=r"(v[i][11]),
-              "=r"(v[i][12]), "=r"(v[i][13]), "=r"(v[i][14]), "=r"(v[i][15])
-            : "r"(taddr + static_cast<uint32_t>(c[i])));
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) asm volatile("" : "+r"(v[i][j]));
-}
-
 struct TcItem {
     int tile, kvh, split, maxpos, slot0;
 };
@@ -444,16 +424,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         const int hi = M == 64 ? (lane >> 4) : 0;
         const int pos = r < T ? s_pos[r / P.G] : -1;
         float m = -INFINITY;
-        const int c4[4] = {128 * ch, 128 * ch + 32, 128 * ch + 64, 128 * ch + 96};
         if (M == 64) {
-            uint32_t v[4][16];
-            tmem_ld16x2_x4_sync(tS + lane_base, c4, v);
-#pragma unroll
+#pragma unroll 1
             for (int i = 0; i < 4; ++i) {
-                const int kk = key0 + c4[i] + 16 * hi;
+                const int c = 128 * ch + 32 * i;
+                uint32_t v[16];
+                tmem_ld16x2_sync(tS + lane_base + c, v);
+                const int kk = key0 + c + 16 * hi;
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
-                    if (kk + t <= pos) m = fmaxf(m, __fmul_rn(__uint_as_float(v[i][t]), sl2));
+                    if (kk + t <= pos) m = fmaxf(m, __fmul_rn(__uint_as_float(v[t]), sl2));
             }
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
         } else {
@@ -480,12 +460,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         float l = 0.0f;
         float gq[4];
         if (M == 64) {
-            uint32_t va[4][16];
-            tmem_ld16x2_x4_sync(tS + lane_base, c4, va);
-#pragma unroll
+#pragma unroll 1
             for (int i = 0; i < 4; ++i) {
-                const uint32_t (&v)[16] = va[i];
-                const int c = c4[i];
+                const int c = 128 * ch + 32 * i;
+                uint32_t v[16];
+                tmem_ld16x2_sync(tS + lane_base + c, v);
                 const int kc = c + 16 * hi;                   // first key (within the split) of these 16
                 uint32_t pk[8];
                 float lg = 0.0f;                              // this 16-key group's sum, in key order

@@ -895,6 +895,35 @@ __global__ void tile_winners_kernel(const unsigned long long* __restrict__ cand,
     if (lane == 0) tokens[row] = b ? static_cast<int32_t>(~static_cast<uint32_t>(b & 0xffffffffull)) : 0;
 }
 
+// One warp per request: the per-row winners of its K rows (as
+// tile_winners_kernel), then the coupled accept of the request (as
+// verify_accept_kernel): accept length L = first j with target != draft, + 1,
+// else K; new length p0 + L.  Same integer results as the two kernels.
+__global__ void winners_accept_kernel(const unsigned long long* __restrict__ cand, int n_tiles,
+                                      int32_t* __restrict__ tokens, const int32_t* __restrict__ draft,
+                                      const int32_t* __restrict__ p0, int n_req, int K,
+                                      int32_t* __restrict__ accept_len, int32_t* __restrict__ new_len) {
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
+    const int lane = threadIdx.x & 31;
+    if (r >= n_req) return;
+    int L = K;
+    for (int j = 0; j < K; ++j) {
+        const long long row = static_cast<long long>(r) * K + j;
+        unsigned long long b = 0;
+        for (int t = lane; t < n_tiles; t += 32) b = umax64(b, cand[row * n_tiles + t]);
+        b = warp_max64(b);
+        const int32_t tok = b ? static_cast<int32_t>(~static_cast<uint32_t>(b & 0xffffffffull)) : 0;
+        if (lane == 0) tokens[row] = tok;
+        if (L == K && tok != draft[row]) L = j + 1;
+    }
+    if (lane == 0) {
+        accept_len[r] = L;
+        new_len[r] = p0[r] + L;
+    }
+}
+
 }  // namespace
 }  // namespace biv
 
@@ -1000,6 +1029,38 @@ extern "C" int biv_lm_head_gumbel(const void* A, const void* B, float* logits, i
     if (st != BIV_OK) return st;
     return launch_pdl(tile_winners_kernel, dim3((M + 7) / 8), dim3(256), 0, s,
                       static_cast<const unsigned long long*>(workspace), M, n_tiles, tokens);
+}
+
+extern "C" int biv_lm_head_gumbel_accept(const void* A, const void* B, float* logits, int M, int N, int K,
+                                         const uint32_t* row_req, const int32_t* row_pos, uint64_t seed,
+                                         float temperature, int32_t* tokens, const int32_t* draft, const int32_t* p0,
+                                         int n_req, int rows_per_req, int32_t* accept_len, int32_t* new_len,
+                                         void* workspace, size_t ws_bytes, biv_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0 || N % 8 != 0 || K % 8 != 0) return BIV_ERR_SHAPE;
+    if (n_req < 0 || rows_per_req < 1 || static_cast<long long>(n_req) * rows_per_req != M) return BIV_ERR_SHAPE;
+    if (!(temperature >= 0.0f) || !(temperature < INFINITY)) return BIV_ERR_VALUE;
+    if (M == 0) return BIV_OK;
+    if (!A || !B || !row_req || !row_pos || !tokens || !workspace || !draft || !p0 || !accept_len || !new_len)
+        return BIV_ERR_NULL;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(workspace) || (logits && !aligned16(logits)))
+        return BIV_ERR_ALIGN;
+    if (ws_bytes < biv_lm_head_gumbel_workspace_size(M, N, K)) return BIV_ERR_SHAPE;
+    const int bn = lm_head_tile_n(M, N, K);
+    const int n_tiles = static_cast<int>(ceil_div(N, bn));
+    SelectArgs sel;
+    sel.row_req = row_req;
+    sel.row_pos = row_pos;
+    sel.cand = static_cast<unsigned long long*>(workspace);
+    sel.seed_lo = static_cast<uint32_t>(seed & 0xffffffffull);
+    sel.seed_hi = static_cast<uint32_t>(seed >> 32);
+    sel.greedy = temperature == 0.0f;
+    sel.invT = sel.greedy ? 0.0f : 1.0f / temperature;    // fl(1/T), IEEE division on the host
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int st = launch_gemm<3>(A, B, logits, M, N, K, bn, s, sel);
+    if (st != BIV_OK) return st;
+    return launch_pdl(winners_accept_kernel, dim3((n_req + 7) / 8), dim3(256), 0, s,
+                      static_cast<const unsigned long long*>(workspace), n_tiles, tokens, draft, p0, n_req,
+                      rows_per_req, accept_len, new_len);
 }
 
 extern "C" int biv_rope_pack_qkv_weights(const void* w_qkv, void* w_packed, int Hq, int Hkv, int hd, int K,

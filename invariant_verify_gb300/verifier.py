@@ -87,8 +87,9 @@ class DecoderVerifier:
         ws = B.biv_decode_attn_workspace_size(W, Hq, max_len)
         self.workspace = torch.empty(max(ws, 16), device=dev, dtype=torch.uint8)
         # embed+norm; per layer QKV+RoPE, attention (two), Wo, add+norm,
-        # gate/up+SwiGLU, down, add+norm; LM head + per-row winner; accept
-        self.launches_per_step = 4 + cfg.layers * 8
+        # gate/up+SwiGLU, down, add+norm; then the LM head with the selection
+        # and one winners+accept kernel, or the LM head, selection and accept
+        self.launches_per_step = (3 if fused_select else 4) + cfg.layers * 8
 
     # -------------------------------------------------------------- stages
     def forward(self, win: Window, trace: dict | None = None) -> None:
@@ -154,8 +155,15 @@ class DecoderVerifier:
 
     def step(self, win: Window) -> None:
         self.forward(win)
-        self.lm_head(win)
-        self.select_and_accept(win)
+        if self.fused_select:
+            # LM head with the selection in its epilogue, then winners + accept in one kernel
+            B.biv_lm_head_gumbel_accept(self.hidden, self.w["lm_head"], win.row_req, win.row_pos, self.seed,
+                                        self.cfg.temperature, self.target, win.draft, win.p0,
+                                        self.accept_len.shape[0], self.rpg, self.accept_len, self.new_len,
+                                        self.select_ws, logits=self.logits)
+        else:
+            self.lm_head(win)
+            self.select_and_accept(win)
 
     def prefill(self, win: Window) -> None:
         """Deterministic prefill ([DVR] para 3: the verifier's fixed-shape

@@ -198,6 +198,30 @@ def test_lm_head_gumbel_validation(lib):
     assert f(*b) == OK
 
 
+def test_lm_head_gumbel_accept_validation(lib):
+    f = lib.biv_lm_head_gumbel_accept
+    ws = lib.biv_lm_head_gumbel_workspace_size(64, 32000, 1024)
+    #       A     B     logits M   N      K     req   pos   seed T    tok   draft p0    n  K  L     nl    ws    bytes s
+    base = [FAKE, FAKE, FAKE, 64, 32000, 1024, FAKE, FAKE, 1, 0.7, FAKE, FAKE, FAKE, 8, 8, FAKE, FAKE, FAKE, ws, None]
+    b = list(base); b[13] = 7
+    assert f(*b) == SHAPE                       # M != n_req * rows_per_req
+    b = list(base); b[14] = 0
+    assert f(*b) == SHAPE
+    b = list(base); b[4] = 32004
+    assert f(*b) == SHAPE                       # N % 8
+    b = list(base); b[9] = -1.0
+    assert f(*b) == VALUE
+    b = list(base); b[18] = ws - 8
+    assert f(*b) == SHAPE                       # workspace too small
+    for k in (11, 12, 15, 16, 17):
+        b = list(base); b[k] = None
+        assert f(*b) == NULL
+    b = list(base); b[2] = MISALIGNED
+    assert f(*b) == ALIGN
+    b = list(base); b[3] = 0; b[13] = 0
+    assert f(*b) == OK
+
+
 def test_topk_and_ngram_validation(lib):
     t = lib.biv_gumbel_topk
     assert t(FAKE, 4, 32, 32, FAKE, FAKE, 1, 0.7, 0, FAKE, None) == SHAPE          # k < 1

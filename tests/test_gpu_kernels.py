@@ -614,6 +614,37 @@ def test_lm_head_gumbel_fused_peaked_ties_and_nan():
             assert tok[0] == 777 and tok[1] == 5000
 
 
+@pytest.mark.parametrize("n_req,K", [(8, 8), (3, 5), (1, 1), (37, 4)])
+def test_lm_head_gumbel_accept_equals_two_calls(n_req, K):
+    """LM head + winners/accept in one kernel: tokens, accept lengths and new
+    lengths bit-identical to biv_lm_head_gumbel then biv_verify_accept, and
+    the accept the oracle computes from the oracle's tokens."""
+    M, N, Kd = n_req * K, 4096, 256
+    g = synth.generator(n_req * 100 + K)
+    A = synth.bf16_normal((M, Kd), 1.0, g).cuda()
+    Bw = synth.bf16_normal((N, Kd), 0.1, g).cuda()
+    req = torch.arange(M, dtype=torch.int32, device="cuda") // K * 11 + 5
+    pos = (torch.arange(M, dtype=torch.int32, device="cuda") % K) + 300
+    p0 = torch.arange(n_req, dtype=torch.int32) * 7 + 300
+    ws = torch.empty(B.biv_lm_head_gumbel_workspace_size(M, N, Kd), dtype=torch.uint8, device="cuda")
+    tok = torch.empty(M, dtype=torch.int32, device="cuda")
+    logits = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    B.biv_lm_head_gumbel(A, Bw, req, pos, SEED, 0.7, tok, ws, logits=logits)
+    # drafts: the targets with every third row wrong
+    draft = tok.clone()
+    draft[::3] = (draft[::3] + 1) % N
+    L2, n2 = (torch.empty(n_req, dtype=torch.int32, device="cuda") for _ in range(2))
+    B.biv_verify_accept(tok, draft, p0.cuda(), n_req, K, L2, n2)
+    tok1 = torch.full((M,), -1, dtype=torch.int32, device="cuda")
+    L1, n1 = (torch.full((n_req,), -1, dtype=torch.int32, device="cuda") for _ in range(2))
+    B.biv_lm_head_gumbel_accept(A, Bw, req, pos, SEED, 0.7, tok1, draft, p0.cuda(), n_req, K, L1, n1, ws)
+    assert torch.equal(tok1, tok) and torch.equal(L1, L2) and torch.equal(n1, n2)
+    ref_tok = oracle.gumbel_argmax(logits.cpu(), req.cpu(), pos.cpu(), SEED, 0.7)
+    assert np.array_equal(tok1.cpu().numpy(), ref_tok)
+    rL, rn = oracle.verify_accept(ref_tok, draft.cpu(), p0, n_req, K)
+    assert np.array_equal(L1.cpu().numpy(), rL) and np.array_equal(n1.cpu().numpy(), rn)
+
+
 def test_lm_head_gumbel_rows_invariant_across_M():
     N, K = 32000, 1024
     g = synth.generator(99)
