@@ -193,9 +193,8 @@ def marked_graphs(ver, win, n):
             with torch.cuda.graph(g):
                 ver.forward(win)
                 ea.record()
-                ver.lm_head(win)
+                ver.lm_head_accept(win)
                 eb.record()
-                ver.select_and_accept(win)
             pool.append((g, ea, eb))
         g, ea, eb = pool[0]
         g.replay()
@@ -232,13 +231,13 @@ def run_ours(args):
     # Each timed step replays one graph of the whole step.  The LM-head launch
     # is bracketed by event-record nodes inside that graph (a pool of graphs,
     # each with its own event pair, read back once its replay has finished);
-    # where event nodes are unavailable the step is replayed as three graphs
+    # where event nodes are unavailable the step is replayed as two graphs
     # with events between them.
     pool = marked_graphs(ver, win, min(K, 16))
     lm_timing = "event-record nodes around the LM-head launch inside the step graph"
     if pool is None:
         segs = ver.capture(win, segments=True)
-        lm_timing = "events between graph segments (layers | LM head | select+accept)"
+        lm_timing = "events between graph segments (layers | LM head + selection + accept)"
 
     def one_step(i):
         if pool is None:
@@ -246,7 +245,6 @@ def run_ours(args):
             seg_ev[i][0].record(stream)
             segs[1].replay()
             seg_ev[i][1].record(stream)
-            segs[2].replay()
         else:
             pool[i % len(pool)][0].replay()
 
@@ -296,12 +294,13 @@ def run_ours(args):
     hbm, bf16, src = peaks()
     M, N, Kd = cfg.W, cfg.vocab, cfg.d
     # weights + activations in, request ids / positions in, tokens out (the
-    # logits stay in TMEM; the per-tile winners are not counted)
+    # logits stay in TMEM; the per-tile winners and the accept's few bytes
+    # per request are not counted)
     lm_bytes = 2 * N * Kd + 2 * M * Kd + 12 * M
     lm_avg_s = statistics.mean(lm_ms) / 1e3
     achieved = lm_bytes / lm_avg_s / 1e9
-    roofline = {"kernel": "gemm_nosplitk_kernel<3> + tile_winners_kernel (LM head M=64 N=32000 K=1024 with "
-                          "the Gumbel-max selection in its epilogue, then the per-row winner)",
+    roofline = {"kernel": "gemm_nosplitk_kernel<3> + winners_accept_kernel (LM head M=64 N=32000 K=1024 with "
+                          "the Gumbel-max selection in its epilogue, then the per-row winners and the accept)",
                 "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",

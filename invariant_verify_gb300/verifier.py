@@ -153,8 +153,8 @@ class DecoderVerifier:
         N = self.accept_len.shape[0]
         B.biv_verify_accept(self.target, win.draft, win.p0, N, self.rpg, self.accept_len, self.new_len)
 
-    def step(self, win: Window) -> None:
-        self.forward(win)
+    def lm_head_accept(self, win: Window) -> None:
+        """Tokens, accept lengths and new lengths from the final hidden rows."""
         if self.fused_select:
             # LM head with the selection in its epilogue, then winners + accept in one kernel
             B.biv_lm_head_gumbel_accept(self.hidden, self.w["lm_head"], win.row_req, win.row_pos, self.seed,
@@ -164,6 +164,10 @@ class DecoderVerifier:
         else:
             self.lm_head(win)
             self.select_and_accept(win)
+
+    def step(self, win: Window) -> None:
+        self.forward(win)
+        self.lm_head_accept(win)
 
     def prefill(self, win: Window) -> None:
         """Deterministic prefill ([DVR] para 3: the verifier's fixed-shape
@@ -181,9 +185,9 @@ class DecoderVerifier:
     def capture(self, win: Window, segments: bool = False):
         """Capture the step on ``win``'s (static) buffers.
 
-        With ``segments`` the step is captured as three graphs -- the layers,
-        the LM-head GEMM alone, then selection + accept -- so the LM-head
-        launch can be timed with events between replays.
+        With ``segments`` the step is captured as two graphs -- the layers,
+        then the LM head with selection and accept -- so the LM-head launch
+        can be timed with events between replays.
         """
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -191,7 +195,7 @@ class DecoderVerifier:
             self.step(win)            # warm-up outside capture (sets kernel attributes)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
-        parts = [(self.forward, (win,)), (self.lm_head, (win,)), (self.select_and_accept, (win,))]
+        parts = [(self.forward, (win,)), (self.lm_head_accept, (win,))]
         if not segments:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
