@@ -103,6 +103,7 @@ BIV_DEV int tile_maxpos(const AttnParams& P, int t) {
 }
 
 constexpr int kMaxTilesSmem = 2048;
+constexpr int kMaxRowsSmem = 4096;                 // rows whose usable positions are tabulated
 
 // Per-tile tables in shared memory, built by all threads of the CTA: the
 // largest usable position of each tile (-1: none), its first row's cache
@@ -110,8 +111,11 @@ constexpr int kMaxTilesSmem = 2048;
 // (Hkv * (tmax / SPLIT + 1) each); s_pref[kMaxTilesSmem] is the live total.
 // Returns whether the tables cover every tile (else callers fall back to all
 // (split, KV head, tile) triples with the dead ones skipped).
-BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, int* s_slot0, int* s_wsum) {
+BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, int* s_slot0, int* s_wsum,
+                               int* s_rpos) {
     const int n_tiles = P.n_tiles;
+    // s_rpos: each row's usable position (-1: none), when every row is tabulated
+    const bool rows_tab = P.W <= kMaxRowsSmem && n_tiles <= kMaxTilesSmem;
     // Largest usable position of each tile, one thread per row (independent
     // loads); tiles past the table are scanned where they are processed.
     for (int t = threadIdx.x; t < min(n_tiles, kMaxTilesSmem); t += ATTN_THREADS) s_tmax[t] = -1;
@@ -126,10 +130,21 @@ BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, in
         if (w == row0) s_slot0[t] = slot0;
         if (slot0 < 0 || slot0 >= P.n_slots) {
             if (w == row0 && blockIdx.x == 0) atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
+            if (rows_tab) s_rpos[w] = -1;
             continue;
         }
+        // the row checks of row_ok(), raised once (by CTA 0)
         const int s = P.row_slot[w], p = P.row_pos[w];
-        if (s == slot0 && p >= 0 && p < P.max_len) atomicMax(&s_tmax[t], p);
+        int vp = -1;
+        if (s < 0 || s >= P.n_slots || p < 0 || p >= P.max_len) {
+            if (blockIdx.x == 0) atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
+        } else if (s != slot0) {
+            if (blockIdx.x == 0) atomicOr(&g_attn_err, BIV_DEVERR_GROUP);
+        } else {
+            vp = p;
+            atomicMax(&s_tmax[t], p);
+        }
+        if (rows_tab) s_rpos[w] = vp;
     }
     __syncthreads();
     // Live work items: tile t has Hkv * (s_tmax[t] / SPLIT + 1) of them (none
@@ -267,6 +282,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __shared__ int s_pref[kMaxTilesSmem + 1];
     __shared__ int s_slot0[kMaxTilesSmem];
     __shared__ int s_wsum[ATTN_THREADS / 32];
+    __shared__ int s_rpos[kMaxRowsSmem];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -291,7 +307,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // The tile tables read only the window's slots and positions, inputs of
     // the call rather than outputs of the previous kernel: built while that
     // kernel finishes.  Q, K and V are read after the wait.
-    const bool live_mode = build_tile_tables(P, s_tmax, s_pref, s_slot0, s_wsum);   // ends with a barrier
+    const bool live_mode = build_tile_tables(P, s_tmax, s_pref, s_slot0, s_wsum, s_rpos);   // ends with a barrier
+    const bool rows_tab = P.W <= kMaxRowsSmem && P.n_tiles <= kMaxTilesSmem;
     tc_fence_after();
     pdl_wait();
     pdl_trigger();
@@ -370,7 +387,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         const int T = nr * P.G;
         if (threadIdx.x < nr) {
             const int w = row0 + threadIdx.x;
-            s_pos[threadIdx.x] = row_ok(P, w, cur.slot0) ? P.row_pos[w] : -1;
+            s_pos[threadIdx.x] = rows_tab ? s_rpos[w] : (row_ok(P, w, cur.slot0) ? P.row_pos[w] : -1);
         }
         const long long nxt_item = next_live(item + gridDim.x);
         const bool has_nxt = nxt_item < n_work;

@@ -895,30 +895,42 @@ __global__ void tile_winners_kernel(const unsigned long long* __restrict__ cand,
     if (lane == 0) tokens[row] = b ? static_cast<int32_t>(~static_cast<uint32_t>(b & 0xffffffffull)) : 0;
 }
 
-// One warp per request: the per-row winners of its K rows (as
-// tile_winners_kernel), then the coupled accept of the request (as
-// verify_accept_kernel): accept length L = first j with target != draft, + 1,
-// else K; new length p0 + L.  Same integer results as the two kernels.
-__global__ void winners_accept_kernel(const unsigned long long* __restrict__ cand, int n_tiles,
-                                      int32_t* __restrict__ tokens, const int32_t* __restrict__ draft,
-                                      const int32_t* __restrict__ p0, int n_req, int K,
-                                      int32_t* __restrict__ accept_len, int32_t* __restrict__ new_len) {
+constexpr int kMaxAcceptRows = 8192;              // K of one request in the fused winners + accept kernel
+
+// One CTA per request: its warps take the per-row winners of the request's K
+// rows (as tile_winners_kernel, one warp per row), then one thread takes the
+// coupled accept (as verify_accept_kernel): accept length L = first j with
+// target != draft, + 1, else K; new length p0 + L.  Same integer results as
+// the two kernels.  Dynamic shared memory: K tokens.
+__global__ void __launch_bounds__(256)
+winners_accept_kernel(const unsigned long long* __restrict__ cand, int n_tiles, int32_t* __restrict__ tokens,
+                      const int32_t* __restrict__ draft, const int32_t* __restrict__ p0, int K,
+                      int32_t* __restrict__ accept_len, int32_t* __restrict__ new_len) {
+    extern __shared__ int32_t s_tok[];
     pdl_wait();
     pdl_trigger();
-    const int r = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
-    const int lane = threadIdx.x & 31;
-    if (r >= n_req) return;
-    int L = K;
-    for (int j = 0; j < K; ++j) {
+    const int r = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = warp; j < K; j += blockDim.x / 32) {
         const long long row = static_cast<long long>(r) * K + j;
         unsigned long long b = 0;
         for (int t = lane; t < n_tiles; t += 32) b = umax64(b, cand[row * n_tiles + t]);
         b = warp_max64(b);
-        const int32_t tok = b ? static_cast<int32_t>(~static_cast<uint32_t>(b & 0xffffffffull)) : 0;
-        if (lane == 0) tokens[row] = tok;
-        if (L == K && tok != draft[row]) L = j + 1;
+        if (lane == 0) {
+            const int32_t tok = b ? static_cast<int32_t>(~static_cast<uint32_t>(b & 0xffffffffull)) : 0;
+            tokens[row] = tok;
+            s_tok[j] = tok;
+        }
     }
-    if (lane == 0) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int L = K;
+        for (int j = 0; j < K; ++j) {
+            if (s_tok[j] != draft[static_cast<long long>(r) * K + j]) {
+                L = j + 1;
+                break;
+            }
+        }
         accept_len[r] = L;
         new_len[r] = p0[r] + L;
     }
@@ -1058,9 +1070,16 @@ extern "C" int biv_lm_head_gumbel_accept(const void* A, const void* B, float* lo
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int st = launch_gemm<3>(A, B, logits, M, N, K, bn, s, sel);
     if (st != BIV_OK) return st;
-    return launch_pdl(winners_accept_kernel, dim3((n_req + 7) / 8), dim3(256), 0, s,
-                      static_cast<const unsigned long long*>(workspace), n_tiles, tokens, draft, p0, n_req,
-                      rows_per_req, accept_len, new_len);
+    if (rows_per_req > kMaxAcceptRows) {          // the two kernels instead
+        const int st2 = launch_pdl(tile_winners_kernel, dim3((M + 7) / 8), dim3(256), 0, s,
+                                   static_cast<const unsigned long long*>(workspace), M, n_tiles, tokens);
+        if (st2 != BIV_OK) return st2;
+        return biv_verify_accept(tokens, draft, p0, n_req, rows_per_req, accept_len, new_len, stream);
+    }
+    return launch_pdl(winners_accept_kernel, dim3(static_cast<unsigned>(n_req)), dim3(256),
+                      static_cast<size_t>(rows_per_req) * sizeof(int32_t), s,
+                      static_cast<const unsigned long long*>(workspace), n_tiles, tokens, draft, p0, rows_per_req,
+                      accept_len, new_len);
 }
 
 extern "C" int biv_rope_pack_qkv_weights(const void* w_qkv, void* w_packed, int Hq, int Hkv, int hd, int K,

@@ -237,6 +237,27 @@ def test_attention_rows_invariant_across_mma_shapes():
     assert same_bits(alone, full)
 
 
+def test_attention_past_the_tile_tables_same_bits():
+    """Past 2048 row tiles the split kernel numbers all (split, KV head, tile)
+    triples and skips the dead ones instead of dealing out live items from
+    its shared-memory tables; rows read their positions from global memory.
+    The same rows give the same bits either way, and match the oracle."""
+    W, Hq, Hkv, max_len = 2050, 2, 2, 300
+    g = synth.generator(2050)
+    kc = synth.bf16_normal((4, Hkv, max_len, 128), 1.0, g)
+    vc = synth.bf16_normal((4, Hkv, max_len, 128), 1.0, g)
+    q = synth.bf16_normal((W, Hq, 128), 1.0, g)
+    slot = (np.arange(W) % 4).astype(np.int32)
+    pos = (np.arange(W) * 37 % 290).astype(np.int32)
+    qd, kd, vd = dev(q), dev(kc), dev(vc)
+    many = _run_attn(qd, kd, vd, slot, pos, 1)            # 2050 tiles: dense numbering
+    few = _run_attn(qd[:2048].contiguous(), kd, vd, slot[:2048], pos[:2048], 1)
+    assert same_bits(many[:2048], few)
+    rows = [0, 1000, 2049]
+    ref = oracle.attention(q[rows], kc, vc, slot[rows], pos[rows])
+    assert_close(many[rows], ref, what="attention (dense numbering)")
+
+
 def test_attention_bad_position_raises_device_error():
     q, kc, vc, slot, pos = _attn_case(2, 8, 2, 600, [100, 300], 4, seed=12)
     qd, kd, vd = dev(q), dev(kc), dev(vc)
