@@ -54,6 +54,9 @@ def parse():
                    help="instead of the step bench: no-split-K GEMM vs cuBLAS on the Llama-3-8B shapes")
     p.add_argument("--kernel-sweep", action="store_true",
                    help="instead of the step bench: HBM GB/s of RMSNorm, attention and Gumbel-max at full sizes")
+    p.add_argument("--c4-steps", action="store_true",
+                   help="instead of the step bench: verified tok/s of whole verify steps on the Llama-3-8B-shaped "
+                        "layer + LM head at the verifier sweep's windows (N x K = 8x4, 32x8, 64x16)")
     p.add_argument("--profile-case", choices=["attn16", "select1024"],
                    help="run one small case twice, for a profiler capture: attention on 16 requests x 16 rows "
                         "(C4 recipe) or selection on 1024 rows (C5 recipe, T = 0.7 then T = 0)")
@@ -578,6 +581,54 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_c4_steps(args):
+    """Whole verify steps (embed + RMSNorm, one Llama-3-8B-shaped layer, LM
+    head over 128256 tokens with the fused selection, winners + accept) at the
+    verifier sweep's windows, lognormal contexts.  Each step is one CUDA graph
+    replay; the weights (1.49 GB) and KV caches exceed L2, so no flush is
+    needed.  Device-timed with events around each replay."""
+    from invariant_verify_gb300 import synth
+    from invariant_verify_gb300.verifier import DecoderVerifier, make_window
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    hbm, bf16, src = peaks()
+    cfg = synth.SWEEP
+    w = synth.decoder_weights_device(cfg)
+    for N, K in ((8, 4), (32, 8), (64, 16)):
+        W = N * K
+        ctx = synth.context_lengths(cfg, N, seed=40 + N)
+        max_len = int(ctx.max()) + K + 16
+        caches = synth.kv_cache_device(N, cfg.Hkv, max_len, cfg.hd, ctx, seed=41 + N, layers=cfg.layers)
+        ver = DecoderVerifier(cfg, w, caches, N, max_len, W, K, keep_logits=False)
+        req = torch.arange(N, dtype=torch.int32) * 31 + 1
+        toks = torch.randint(0, cfg.vocab, (W,), generator=synth.generator(43), dtype=torch.int64).to(torch.int32)
+        win = make_window(N, K, toks, ctx, req, toks)
+        g = ver.capture(win)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        n = 20
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+        kv = sum(2 * 2 * cfg.Hkv * (int(c) + K) * cfg.hd for c in ctx)
+        wbytes = sum(t.numel() * t.element_size() for k, t in w.items() if k != "embed")
+        flops = 2 * W * (wbytes // 2) + 4 * cfg.Hq * cfg.hd * sum(int(c) + K for c in ctx) * K
+        lb = max((wbytes + kv) / (hbm * 1e9), flops / (bf16 * 1e12)) * 1e6
+        print(json.dumps({"workload": f"C4 verify step N={N} K={K} W={W}, Llama-3-8B-shaped layer + LM head "
+                                      f"(vocab {cfg.vocab}), lognormal ctx mean {float(ctx.float().mean()):.0f}",
+                          "us_per_step": round(us, 1), "verified_tok_per_s": round(W / us * 1e6, 1),
+                          "lower_bound_us": round(lb, 1), "frac_of_roofline": round(lb / us, 4),
+                          "gpu_launches_per_step": ver.launches_per_step, "peak_source": src}), flush=True)
+        del ver, caches, g
+        torch.cuda.empty_cache()
+
+
 def run_profile_case(args):
     """A small case of one kernel, launched twice (the second launch is the
     one to capture): inputs above L2 size, a few hundred MB on the device."""
@@ -620,6 +671,8 @@ if __name__ == "__main__":
     a = parse()
     if a.profile_case:
         run_profile_case(a)
+    elif a.c4_steps:
+        run_c4_steps(a)
     elif a.gemm_sweep:
         run_gemm_sweep(a)
     elif a.kernel_sweep:
