@@ -351,32 +351,32 @@ def step_work(cfg, ctx):
 
 def run_e2e(ver, win, graph, flush, cfg, K, world, device):
     """Same metric through the public API with host buffers: each step copies
-    the window's inputs from pinned host memory, runs the step, and reads the
-    accept lengths, rollback points and selected tokens back."""
-    names = ["tokens", "row_slot", "row_req", "row_pos", "draft", "p0"]
-    host_in = {n: getattr(win, n).cpu().pin_memory() for n in names}
-    outs = [ver.accept_len, ver.new_len, ver.target]
-    host_out = [o.cpu().pin_memory() for o in outs]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    the window's inputs from pinned host memory (one copy of the packed
+    inputs), runs the step, and reads the accept lengths, rollback points and
+    selected tokens back (one copy of the packed results) -- the three as
+    nodes of one CUDA graph, replayed and synchronised per step."""
+    from invariant_verify_gb300.verifier import PackedWindow, capture_e2e
+    pw = PackedWindow(cfg.N, cfg.K, device=device)
+    pw.set(win)
+    host_out = torch.empty_like(ver.results, device="cpu").pin_memory()
+    g = capture_e2e(ver, pw, host_out)
+    h2d = pw.host.numel() * pw.host.element_size()
+    d2h = host_out.numel() * host_out.element_size()
     stream = torch.cuda.current_stream()
     total = 0.0
     for i in range(K + 5):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for n in names:
-            getattr(win, n).copy_(host_in[n], non_blocking=True)
-        graph.replay()
-        for h, o in zip(host_out, outs):
-            h.copy_(o, non_blocking=True)
+        g.replay()
         stream.synchronize()
         if i >= 5:
             total += time.perf_counter() - t0
     value = cfg.W * world * K / total
     return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": K, "ms_per_step": round(total / K * 1e3, 5),
-            "how": "pinned H2D of the window inputs + CUDA-graph step + D2H of accept_len/new_len/tokens + sync"}
+            "how": "one CUDA graph per step: pinned H2D of the packed window inputs, the step, D2H of the packed "
+                   "accept_len/new_len/tokens; host wall time per step including the synchronisation"}
 
 
 # ---------------------------------------------------------- kernel sweep

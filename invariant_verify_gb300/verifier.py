@@ -80,10 +80,13 @@ class DecoderVerifier:
         if fused_select:
             n = B.biv_lm_head_gumbel_workspace_size(W, cfg.vocab, d)
             self.select_ws = torch.empty(max(n, 16), device=dev, dtype=torch.uint8)
-        self.target = torch.empty(W, device=dev, dtype=torch.int32)
         N = (W + rows_per_group - 1) // rows_per_group
-        self.accept_len = torch.empty(N, device=dev, dtype=torch.int32)
-        self.new_len = torch.empty(N, device=dev, dtype=torch.int32)
+        # the step's results, [accept_len N | new_len N | target W], in one
+        # buffer so that one copy reads them back
+        self.results = torch.empty(2 * N + W, device=dev, dtype=torch.int32)
+        self.accept_len = self.results[:N]
+        self.new_len = self.results[N:2 * N]
+        self.target = self.results[2 * N:]
         ws = B.biv_decode_attn_workspace_size(W, Hq, max_len)
         self.workspace = torch.empty(max(ws, 16), device=dev, dtype=torch.uint8)
         # embed+norm; per layer QKV+RoPE, attention (two), Wo, add+norm,
@@ -219,6 +222,43 @@ def prefill_window(prompt, slot: int, req_id: int, device="cuda") -> Window:
                       torch.zeros(P, dtype=torch.int32), device=device)
     win.row_slot.fill_(slot)
     return win
+
+
+class PackedWindow:
+    """A window whose six inputs are views of one device buffer, fed from one
+    pinned host buffer: [tokens W | row_slot W | row_req W | row_pos W |
+    draft W | p0 N] (int32), so one host-to-device copy moves a step's inputs."""
+
+    def __init__(self, N: int, K: int, device="cuda"):
+        W = N * K
+        self.host = torch.empty(5 * W + N, dtype=torch.int32).pin_memory()
+        self.dev = torch.empty(5 * W + N, dtype=torch.int32, device=device)
+        v = [self.dev[i * W:(i + 1) * W] for i in range(5)]
+        self.win = Window(tokens=v[0], row_slot=v[1], row_req=v[2], row_pos=v[3], draft=v[4], p0=self.dev[5 * W:])
+
+    def set(self, win: Window) -> None:
+        """Host copy of ``win``'s inputs (the next step's window)."""
+        parts = [win.tokens, win.row_slot, win.row_req, win.row_pos, win.draft, win.p0]
+        self.host.copy_(torch.cat([t.cpu() for t in parts]))
+
+
+def capture_e2e(ver: DecoderVerifier, pw: PackedWindow, host_results: torch.Tensor):
+    """One CUDA graph of a whole end-to-end step: the inputs' host-to-device
+    copy (pinned), the verify step, the results' device-to-host copy (pinned
+    ``host_results``, int32 [2N + W]).  Replay it, then synchronise."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pw.dev.copy_(pw.host, non_blocking=True)
+        ver.step(pw.win)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pw.dev.copy_(pw.host, non_blocking=True)
+        ver.step(pw.win)
+        host_results.copy_(ver.results, non_blocking=True)
+    return g
 
 
 def make_window(N: int, K: int, tokens, p0, req_ids, draft, device="cuda") -> Window:
