@@ -36,10 +36,11 @@
  *     while the previous libbiv kernel on the same stream is finishing, and
  *     waits for it before reading that kernel's outputs.  A few inputs that
  *     are never a step's intermediate results are read before that wait:
- *     GEMM weights (B operands) and the row_slot / row_pos arrays of
- *     attention.  They must not be written by the immediately preceding
- *     libbiv kernel on the stream (kernels of other libraries, and copies,
- *     are waited for in full).
+ *     GEMM weights (B operands), the row_slot / row_pos arrays of attention
+ *     and the cache rows of each attention row group below the group's
+ *     smallest position (the requests' committed context).  They must not be
+ *     written by the immediately preceding libbiv kernel on the stream
+ *     (kernels of other libraries, and copies, are waited for in full).
  *   - No call allocates device memory.  The one exception in kind is the fixed
  *     scratch array behind biv_decode_attn_fixedsplit_noalloc, which is part
  *     of the loaded module (BIV_NOALLOC_SCRATCH_BYTES per GPU, held until the

@@ -103,7 +103,7 @@ BIV_DEV int tile_maxpos(const AttnParams& P, int t) {
 }
 
 constexpr int kMaxTilesSmem = 2048;
-constexpr int kMaxRowsSmem = 4096;                 // rows whose usable positions are tabulated
+constexpr int kMaxRowsSmem = 2048;                 // rows whose usable positions are tabulated
 
 // Per-tile tables in shared memory, built by all threads of the CTA: the
 // largest usable position of each tile (-1: none), its first row's cache
@@ -112,13 +112,16 @@ constexpr int kMaxRowsSmem = 4096;                 // rows whose usable position
 // Returns whether the tables cover every tile (else callers fall back to all
 // (split, KV head, tile) triples with the dead ones skipped).
 BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, int* s_slot0, int* s_wsum,
-                               int* s_rpos) {
+                               int* s_rpos, int* s_gmin) {
     const int n_tiles = P.n_tiles;
     // s_rpos: each row's usable position (-1: none), when every row is tabulated
     const bool rows_tab = P.W <= kMaxRowsSmem && n_tiles <= kMaxTilesSmem;
     // Largest usable position of each tile, one thread per row (independent
     // loads); tiles past the table are scanned where they are processed.
-    for (int t = threadIdx.x; t < min(n_tiles, kMaxTilesSmem); t += ATTN_THREADS) s_tmax[t] = -1;
+    for (int t = threadIdx.x; t < min(n_tiles, kMaxTilesSmem); t += ATTN_THREADS) {
+        s_tmax[t] = -1;
+        s_gmin[t] = 0x7fffffff;             // per row group (there are no more groups than tiles)
+    }
     __syncthreads();
     for (int w = threadIdx.x; w < P.W; w += ATTN_THREADS) {
         const int group = w / P.rows_per_group;
@@ -143,6 +146,7 @@ BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, in
         } else {
             vp = p;
             atomicMax(&s_tmax[t], p);
+            atomicMin(&s_gmin[group], p);
         }
         if (rows_tab) s_rpos[w] = vp;
     }
@@ -283,6 +287,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __shared__ int s_slot0[kMaxTilesSmem];
     __shared__ int s_wsum[ATTN_THREADS / 32];
     __shared__ int s_rpos[kMaxRowsSmem];
+    __shared__ int s_gmin[kMaxTilesSmem];                      // smallest usable position of each row group
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -307,11 +312,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // The tile tables read only the window's slots and positions, inputs of
     // the call rather than outputs of the previous kernel: built while that
     // kernel finishes.  Q, K and V are read after the wait.
-    const bool live_mode = build_tile_tables(P, s_tmax, s_pref, s_slot0, s_wsum, s_rpos);   // ends with a barrier
+    const bool live_mode = build_tile_tables(P, s_tmax, s_pref, s_slot0, s_wsum, s_rpos, s_gmin);   // ends with a barrier
     const bool rows_tab = P.W <= kMaxRowsSmem && P.n_tiles <= kMaxTilesSmem;
     tc_fence_after();
-    pdl_wait();
-    pdl_trigger();
+    uint32_t early = 0;                              // thread 0: key halves of the first item already requested
     const uint32_t tS = s_tmem, tO = s_tmem + 256;
     const long long n_work =
         live_mode ? s_pref[kMaxTilesSmem] : static_cast<long long>(P.s_max) * P.Hkv * P.n_tiles;
@@ -367,11 +371,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
     long long item = next_live(blockIdx.x);
     TcItem cur = {};
+    if (item < n_work) cur = tc_decode(P, live_mode, item, s_pref, s_tmax, s_slot0);
+    // Cache rows below a row group's smallest position are the requests'
+    // committed context, never an output of the previous kernel (that one
+    // writes the window's own rows): the first item's 128-key boxes that lie
+    // wholly below it are requested before the wait.
+    if (threadIdx.x == 0 && item < n_work && live_mode) {
+        const int group = cur.tile / P.tiles_per_group;
+        const int gmin = s_gmin[group];
+        const int nkh = n_keys_of(cur) > 128 ? 2 : 1;
+        const int kv_row = (cur.slot0 * P.Hkv + cur.kvh) * P.max_len + cur.split * SPLIT;
+        for (int kh = 0; kh < nkh; ++kh) {
+            if (cur.split * SPLIT + (kh + 1) * 128 > gmin) break;
+            mbar_arrive_expect_tx(&kbar[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
+            tma_load_3d(sK + kh * kTcKeyHalfBytes, &tmK, &kbar[kh], 0, kv_row + kh * 128, 0, policy_evict_first());
+            mbar_arrive_expect_tx(&vbar[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
+            tma_load_3d(sV + kh * kTcKeyHalfBytes, &tmV, &vbar[kh], 0, kv_row + kh * 128, 0, policy_evict_first());
+            ++k_iss[kh];
+            ++v_iss[kh];
+            early |= 1u << kh;
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
     if (item < n_work) {
-        cur = tc_decode(P, live_mode, item, s_pref, s_tmax, s_slot0);
         if (threadIdx.x == 0) {
-            load_kv(&tmK, sK, kbar, k_iss, cur);
-            load_kv(&tmV, sV, vbar, v_iss, cur);
+            const int nkh = n_keys_of(cur) > 128 ? 2 : 1;
+            const int kv_row = (cur.slot0 * P.Hkv + cur.kvh) * P.max_len + cur.split * SPLIT;
+            for (int kh = 0; kh < nkh; ++kh) {
+                if (early & (1u << kh)) continue;
+                mbar_arrive_expect_tx(&kbar[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
+                tma_load_3d(sK + kh * kTcKeyHalfBytes, &tmK, &kbar[kh], 0, kv_row + kh * 128, 0,
+                            policy_evict_first());
+                mbar_arrive_expect_tx(&vbar[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
+                tma_load_3d(sV + kh * kTcKeyHalfBytes, &tmV, &vbar[kh], 0, kv_row + kh * 128, 0,
+                            policy_evict_first());
+                ++k_iss[kh];
+                ++v_iss[kh];
+            }
         }
         load_q(cur);
     }

@@ -220,6 +220,40 @@ def test_decoder_rows_bitwise_invariant(dec2):
     assert same_bits(full.logits, Lg) and same_bits(full.target, Tg)
 
 
+def test_end_to_end_graph_with_host_buffers(dec2):
+    """The end-to-end path: window inputs copied from one pinned host buffer,
+    the step, results copied back into one pinned host buffer, all in one
+    graph -- the same tokens, accept lengths and rollback points as a plain
+    step, replay after replay, and a second window through the same graph."""
+    from invariant_verify_gb300.verifier import PackedWindow, capture_e2e
+    cfg = synth.DECODER2
+    w, caches, ctx, max_len = dec2
+    W = cfg.W
+    g = synth.generator(61)
+    wins = []
+    for _ in range(2):
+        toks = torch.randint(0, cfg.vocab, (W,), generator=g, dtype=torch.int64).to(torch.int32)
+        drafts = torch.randint(0, cfg.vocab, (W,), generator=g, dtype=torch.int64).to(torch.int32)
+        wins.append(_window(cfg, ctx, toks, drafts))
+    refs = []
+    for wi in wins:
+        ver = DecoderVerifier(cfg, w, caches, cfg.N, max_len, W, cfg.K)
+        ver.step(wi)
+        torch.cuda.synchronize()
+        refs.append(ver.results.cpu().clone())
+    ver = DecoderVerifier(cfg, w, caches, cfg.N, max_len, W, cfg.K)
+    pw = PackedWindow(cfg.N, cfg.K)
+    host_out = torch.empty_like(ver.results, device="cpu").pin_memory()
+    pw.set(wins[0])
+    graph = capture_e2e(ver, pw, host_out)
+    for wi, ref in ((wins[0], refs[0]), (wins[1], refs[1]), (wins[0], refs[0])):
+        pw.set(wi)
+        host_out.fill_(-1)
+        graph.replay()
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(host_out, ref)
+
+
 def test_fast_path_kv_is_overwritten(dec2):
     # Perturb the window's cache rows (a stale fast path) before verifying:
     # the verifier overwrites them and the result equals a clean run.
