@@ -345,14 +345,46 @@ BIV_DEV uint32_t swiglu_pack(uint32_t g2, uint32_t u2) {
 // angle pos * theta^(-2i/hd); one definition for every kernel that rotates
 // (the RoPE kernels and the QKV GEMM's RoPE epilogue), so all give the same
 // bits.  Explicit roundings: no fma contraction.
-BIV_DEV void rope_pair(float a, float b, int pos, int i, int hd, float theta, __nv_bfloat16& o1,
-                       __nv_bfloat16& o2) {
-    const float inv_freq = powf(theta, -2.0f * static_cast<float>(i) / static_cast<float>(hd));
+// Rotation frequency theta^(-2i/hd) of RoPE pair i.
+BIV_DEV float rope_inv_freq(int i, int hd, float theta) {
+    return powf(theta, -2.0f * static_cast<float>(i) / static_cast<float>(hd));
+}
+
+// One RoPE pair (a, b) at position pos with the pair's frequency given.
+BIV_DEV void rope_pair_f(float a, float b, int pos, float inv_freq, __nv_bfloat16& o1, __nv_bfloat16& o2) {
     const float ang = static_cast<float>(pos) * inv_freq;
     float sn, cs;
     sincosf(ang, &sn, &cs);
     o1 = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)));
     o2 = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, cs), __fmul_rn(a, sn)));
+}
+
+BIV_DEV void rope_pair(float a, float b, int pos, int i, int hd, float theta, __nv_bfloat16& o1,
+                       __nv_bfloat16& o2) {
+    rope_pair_f(a, b, pos, rope_inv_freq(i, hd, theta), o1, o2);
+}
+
+// M = 64 accumulators, two loads and one wait: threads 0..15 get their lane's
+// columns [a, a + N) and [b, b + N), threads 16..31 the same lanes' columns
+// [a + N, a + 2N) and [b + N, b + 2N) (N = 4 or 8).
+BIV_DEV void tmem_ld16x2_x4_pair_sync(uint32_t ta, uint32_t tb, uint32_t (&a)[4], uint32_t (&b)[4]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x4.b32 {%0, %1, %2, %3}, [%8], 4;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x4.b32 {%4, %5, %6, %7}, [%9], 4;\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
+BIV_DEV void tmem_ld16x2_x8_pair_sync(uint32_t ta, uint32_t tb, uint32_t (&a)[8], uint32_t (&b)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16], 8;\n\t"
+        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17], 8;\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+          "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7])
+        : "r"(ta), "r"(tb)
+        : "memory");
 }
 
 BIV_DEV void rope_rotate(float a, float b, int pos, int i, int hd, float theta, __nv_bfloat16* o1,

@@ -135,6 +135,77 @@ struct RopeArgs {
     float theta;
 };
 
+// NP bf16 (NP / 2 packed pairs) in one vector store.
+template <int NP>
+BIV_DEV void st_bf16s(__nv_bfloat16* p, const uint32_t* v) {
+    if constexpr (NP == 8)
+        *reinterpret_cast<uint4*>(p) = make_uint4(v[0], v[1], v[2], v[3]);
+    else
+        *reinterpret_cast<uint2*>(p) = make_uint2(v[0], v[1]);
+}
+
+// One row's share of a 16-column group at output column col of the QKV tile:
+// f1 holds the fp32 accumulators of group columns jb .. jb + NP - 1 (first
+// halves of rotation pairs jb ..), f2 those of columns 8 + jb .. (their
+// partners). q and k pairs are rotated at the row's position and stored to
+// q_out or the k cache; v columns go to the v cache unrotated.
+template <int NP>
+BIV_DEV void qkv_group(const uint32_t* f1, const uint32_t* f2, int jb, int col, int row, int slot, int pos,
+                       bool write_kv, const RopeArgs& rp, const float* inv_freq) {
+    const int hd = rp.hd, half = hd / 2;
+    const int qn = rp.Hq * hd, kn = rp.Hkv * hd;
+    uint32_t a[NP / 2], b[NP / 2];                // bf16 pairs, as the plain GEMM stores them
+#pragma unroll
+    for (int e = 0; e < NP / 2; ++e) {
+        a[e] = pack_bf16x2(__uint_as_float(f1[2 * e]), __uint_as_float(f1[2 * e + 1]));
+        b[e] = pack_bf16x2(__uint_as_float(f2[2 * e]), __uint_as_float(f2[2 * e + 1]));
+    }
+    __nv_bfloat16* qkv_row = rp.qkv_out ? rp.qkv_out + static_cast<long long>(row) * (qn + 2 * kn) : nullptr;
+    if (col < qn + kn) {
+        const bool isq = col < qn;
+        const int cc = isq ? col : col - qn;
+        const int h = cc / hd, i0 = (cc % hd) / 16 * 8 + jb;
+        uint32_t o1[NP / 2], o2[NP / 2];
+#pragma unroll
+        for (int j = 0; j < NP; j += 2) {
+            __nv_bfloat16 a0, a1, b0, b1;
+            rope_pair_f(bf16lo(a[j / 2]), bf16lo(b[j / 2]), pos, inv_freq[i0 + j], a0, b0);
+            rope_pair_f(bf16hi(a[j / 2]), bf16hi(b[j / 2]), pos, inv_freq[i0 + j + 1], a1, b1);
+            o1[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(a0)) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(a1)) << 16);
+            o2[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
+        }
+        __nv_bfloat16* dst = nullptr;
+        if (isq)
+            dst = rp.q_out + (static_cast<long long>(row) * rp.Hq + h) * hd;
+        else if (write_kv)
+            dst = rp.kc + ((static_cast<long long>(slot) * rp.Hkv + h) * rp.max_len + pos) * hd;
+        if (dst) {
+            st_bf16s<NP>(dst + i0, o1);
+            st_bf16s<NP>(dst + half + i0, o2);
+        }
+        if (qkv_row) {
+            __nv_bfloat16* base = qkv_row + (isq ? 0 : qn) + h * hd;
+            st_bf16s<NP>(base + i0, a);
+            st_bf16s<NP>(base + half + i0, b);
+        }
+    } else {
+        const int cc = col - qn - kn;
+        const int h = cc / hd, d0 = cc % hd;
+        if (write_kv) {
+            __nv_bfloat16* dst = rp.vc + ((static_cast<long long>(slot) * rp.Hkv + h) * rp.max_len + pos) * hd + d0;
+            st_bf16s<NP>(dst + jb, a);
+            st_bf16s<NP>(dst + 8 + jb, b);
+        }
+        if (qkv_row) {
+            __nv_bfloat16* base = qkv_row + qn + kn + cc;
+            st_bf16s<NP>(base + jb, a);
+            st_bf16s<NP>(base + 8 + jb, b);
+        }
+    }
+}
+
 constexpr int kNoiseTableBytes = kBuckets * 4 + 256 * 4;
 constexpr int kExactBuckets = 256;
 constexpr int kChunk = 32;                    // TMEM columns per load
@@ -553,6 +624,14 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             // Largest noise of each bucket, while the first tile's data arrives.
             if (!sel.greedy) fill_noise_table(ntab, t8);
         }
+        const float* inv_freq = nullptr;
+        if constexpr (EPI == 4) {
+            // RoPE frequencies of the pairs; the first tile's vote publishes them.
+            __shared__ float s_inv_freq[128];                  // head_dim <= 256
+            for (int i = static_cast<int>(threadIdx.x) - 64; i < rp.hd / 2; i += 128)
+                s_inv_freq[i] = rope_inv_freq(i, rp.hd, rp.theta);
+            inv_freq = s_inv_freq;
+        }
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < n_work; t += gridDim.x) {
@@ -595,81 +674,63 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 if (live) sel.cand[static_cast<long long>(srow) * n_tiles + n_blk] = best;
                 epilogue_bar();       // every row is done with the buckets before the next tile's
             } else if constexpr (EPI == 4) {
+                // With M = 64 accumulators the two half-warps share each row:
+                // threads 16..31 take pairs 4..7 of every 16-column group.
+                const int prow = g.m64 ? m_blk * kBM + q * 16 + (lane & 15) : row;
+                const bool plive = prow < M;
+                const int jb = g.m64 ? 4 * (lane >> 4) : 0;
                 int slot = 0, pos = 0;
                 bool write_kv = false;
-                if (live) {
-                    pos = rp.row_pos[row];
-                    slot = rp.row_slot[row];
-                    const bool keep = !rp.rows_keep || (row % rp.K) < rp.rows_keep[row / rp.K];
+                if (plive) {
+                    pos = rp.row_pos[prow];
+                    slot = rp.row_slot[prow];
+                    const bool keep = !rp.rows_keep || (prow % rp.K) < rp.rows_keep[prow / rp.K];
                     const bool cache_ok = slot >= 0 && slot < rp.n_slots && pos >= 0 && pos < rp.max_len;
-                    if (keep && !cache_ok) atomicOr(&g_gemm_err, BIV_DEVERR_INDEX);
+                    if (keep && !cache_ok && jb == 0) atomicOr(&g_gemm_err, BIV_DEVERR_INDEX);
                     write_kv = keep && cache_ok;
                 }
-                const int hd = rp.hd, half = hd / 2;
-                const int qn = rp.Hq * hd, kn = rp.Hkv * hd;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(taddr + static_cast<uint32_t>(c), r);
-                    tmem_ld_wait();
                     const int col = n_blk * BN + c;
-                    if (!live || col >= N) continue;
-                    uint32_t v2[8];                   // bf16 pairs, as the plain GEMM stores them
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        v2[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-                    __nv_bfloat16* qkv_row =
-                        rp.qkv_out ? rp.qkv_out + static_cast<long long>(row) * (qn + 2 * kn) : nullptr;
-                    if (col < qn + kn) {
-                        const bool isq = col < qn;
-                        const int cc = isq ? col : col - qn;
-                        const int h = cc / hd, i0 = (cc % hd) / 16 * 8;
-                        uint32_t o1[4], o2[4];
-#pragma unroll
-                        for (int j = 0; j < 8; j += 2) {
-                            __nv_bfloat16 a0, a1, b0, b1;
-                            // pair j: column j (first half of the pairs) and column 8 + j
-                            rope_pair(bf16lo(v2[j / 2]), bf16lo(v2[4 + j / 2]), pos, i0 + j, hd, rp.theta, a0, b0);
-                            rope_pair(bf16hi(v2[j / 2]), bf16hi(v2[4 + j / 2]), pos, i0 + j + 1, hd, rp.theta, a1, b1);
-                            o1[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(a0)) |
-                                        (static_cast<uint32_t>(__bfloat16_as_ushort(a1)) << 16);
-                            o2[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) |
-                                        (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
-                        }
-                        __nv_bfloat16* dst = nullptr;
-                        if (isq)
-                            dst = rp.q_out + (static_cast<long long>(row) * rp.Hq + h) * hd;
-                        else if (write_kv)
-                            dst = rp.kc + ((static_cast<long long>(slot) * rp.Hkv + h) * rp.max_len + pos) * hd;
-                        if (dst) {
-                            *reinterpret_cast<uint4*>(dst + i0) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-                            *reinterpret_cast<uint4*>(dst + half + i0) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-                        }
-                        if (qkv_row) {
-                            __nv_bfloat16* b = qkv_row + (isq ? 0 : qn) + h * hd;
-                            *reinterpret_cast<uint4*>(b + i0) = make_uint4(v2[0], v2[1], v2[2], v2[3]);
-                            *reinterpret_cast<uint4*>(b + half + i0) = make_uint4(v2[4], v2[5], v2[6], v2[7]);
-                        }
+                    if (g.m64) {
+                        uint32_t ra[4], rb[4];
+                        tmem_ld16x2_x4_pair_sync(taddr + static_cast<uint32_t>(c),
+                                                 taddr + static_cast<uint32_t>(c + 8), ra, rb);
+                        if (plive && col < N) qkv_group<4>(ra, rb, jb, col, prow, slot, pos, write_kv, rp, inv_freq);
                     } else {
-                        const int cc = col - qn - kn;
-                        const int h = cc / hd, d0 = cc % hd;
-                        if (write_kv) {
-                            uint4* dst = reinterpret_cast<uint4*>(
-                                rp.vc + ((static_cast<long long>(slot) * rp.Hkv + h) * rp.max_len + pos) * hd + d0);
-                            dst[0] = make_uint4(v2[0], v2[1], v2[2], v2[3]);
-                            dst[1] = make_uint4(v2[4], v2[5], v2[6], v2[7]);
-                        }
-                        if (qkv_row) {
-                            uint4* b = reinterpret_cast<uint4*>(qkv_row + qn + kn + cc);
-                            b[0] = make_uint4(v2[0], v2[1], v2[2], v2[3]);
-                            b[1] = make_uint4(v2[4], v2[5], v2[6], v2[7]);
-                        }
+                        uint32_t r[16];
+                        tmem_ld16(taddr + static_cast<uint32_t>(c), r);
+                        tmem_ld_wait();
+                        if (live && col < N) qkv_group<8>(r, r + 8, 0, col, row, slot, pos, write_kv, rp, inv_freq);
                     }
                 }
             } else if constexpr (EPI == 2) {
                 // Columns [32j, 32j + 16) of the tile are gate rows, [32j + 16, 32j + 32)
                 // the matching up rows: act = bf16(silu(bf16(g)) * bf16(u)).
                 const int F = N / 2;
+                if (g.m64) {
+                    // the two half-warps share each row: threads 16..31 take
+                    // gate columns 8..15 of every 32-column group and their up columns
+                    const int prow = m_blk * kBM + q * 16 + (lane & 15);
+                    const int hi = lane >> 4;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        uint32_t gr[8], ur[8];
+                        tmem_ld16x2_x8_pair_sync(taddr + static_cast<uint32_t>(c),
+                                                 taddr + static_cast<uint32_t>(c + 16), gr, ur);
+                        const int col = n_blk * BN + c;
+                        if (prow < M && col < N) {
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                o[e] = swiglu_pack(
+                                    pack_bf16x2(__uint_as_float(gr[2 * e]), __uint_as_float(gr[2 * e + 1])),
+                                    pack_bf16x2(__uint_as_float(ur[2 * e]), __uint_as_float(ur[2 * e + 1])));
+                            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(C) + static_cast<long long>(prow) * F +
+                                                      col / 2 + 8 * hi) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                } else
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t gr[16], ur[16];
