@@ -263,6 +263,42 @@ BIV_DEV TcItem tc_decode(const AttnParams& P, bool live_mode, long long item, co
     return it;
 }
 
+// Largest of the first min(lim + 1, N) raw scores v[0 ..] (-inf if none): a
+// maximum is exact in any order, so four interleaved partial maxima are used.
+template <int N>
+BIV_DEV float masked_max(const uint32_t* v, int lim) {
+    float a[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (lim >= N - 1) {
+#pragma unroll
+        for (int t = 0; t < N; ++t) a[t & 3] = fmaxf(a[t & 3], __uint_as_float(v[t]));
+    } else {
+#pragma unroll
+        for (int t = 0; t < N; ++t)
+            if (t <= lim) a[t & 3] = fmaxf(a[t & 3], __uint_as_float(v[t]));
+    }
+    return fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+}
+
+// One 16-key group of a row: p_t = 2^(s_t sl2 - m) (one fused multiply-add
+// and the hardware base-2 exponential), 0 for keys t > lim; the p_t as bf16
+// pairs into pk[0..7]; returns their fp32 sum taken in key order.
+BIV_DEV float softmax_group(const uint32_t* v, float sl2, float nmu, int lim, uint32_t* pk) {
+    float p[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) p[t] = ex2_approx(fmaf(__uint_as_float(v[t]), sl2, nmu));
+    if (lim < 15) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            if (t > lim) p[t] = 0.0f;
+    }
+    float lg = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) lg += p[t];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) pk[t] = pack_bf16x2(p[2 * t], p[2 * t + 1]);
+    return lg;
+}
+
 template <int M>
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -477,61 +513,60 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         const int r = M == 64 ? 16 * q4 + (lane & 15) : 32 * q4 + lane;
         const int hi = M == 64 ? (lane >> 4) : 0;
         const int pos = r < T ? s_pos[r / P.G] : -1;
-        float m = -INFINITY;
+        // Keys 128 ch + 32 i .. + 31 form chunk i of the thread's half; chunks at
+        // or past the split's last key hold no key of any row and are skipped
+        // (P V reads P only up to the next 16-key step).
+        // The row maximum is taken over the raw scores and scaled once: scaling
+        // by sl2 > 0 rounds monotonically, so this equals the maximum of the
+        // scaled scores.
+        float mraw = -INFINITY;
+        // M = 64: the thread's 64 scores (keys 128 ch + 32 i + 16 hi + t) stay in
+        // registers from one round of loads until P is written.
+        uint32_t sv[4][16];
         if (M == 64) {
-#pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
-                const int c = 128 * ch + 32 * i;
-                uint32_t v[16];
-                tmem_ld16x2_sync(tS + lane_base + c, v);
-                const int kk = key0 + c + 16 * hi;
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    if (kk + t <= pos) m = fmaxf(m, __fmul_rn(__uint_as_float(v[t]), sl2));
+            for (int i = 0; i < 4; ++i)
+                if (128 * ch + 32 * i < n_keys) tmem_ld16x2(tS + lane_base + 128 * ch + 32 * i, sv[i]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (128 * ch + 32 * i >= n_keys) continue;
+                reg_fence16(sv[i]);
+                mraw = fmaxf(mraw, masked_max<16>(sv[i], pos - (key0 + 128 * ch + 32 * i + 16 * hi)));
             }
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+            mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 16));
         } else {
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
                 const int c = 128 * ch + 32 * i;
+                if (c >= n_keys) break;
                 uint32_t v[32];
                 tmem_ld32_sync(tS + lane_base + c, v);
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    if (key0 + c + t <= pos) m = fmaxf(m, __fmul_rn(__uint_as_float(v[t]), sl2));
+                mraw = fmaxf(mraw, masked_max<32>(v, pos - (key0 + c)));
             }
         }
+        float m = __fmul_rn(mraw, sl2);
         if (hi == 0) s_mx[ch][r] = m;
         if (__syncthreads_or(aborted())) {
             ok = false;
             break;
         }
         m = fmaxf(s_mx[0][r], s_mx[1][r]);
-        const float mu = m == -INFINITY ? 0.0f : m;       // a row with no key in the split
+        const float nmu = m == -INFINITY ? 0.0f : -m;     // a row with no key in the split
         // l: every 16-key group summed in key order, pairs of groups added, then
         // ((q0 + q1) + (q2 + q3)) per 128-key half and the halves -- the same
         // order for M = 64 and M = 128, so a row's sum never depends on the tile.
         float l = 0.0f;
-        float gq[4];
+        float gq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (M == 64) {
-#pragma unroll 1
+#pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int c = 128 * ch + 32 * i;
-                uint32_t v[16];
-                tmem_ld16x2_sync(tS + lane_base + c, v);
+                if (c >= n_keys) continue;
                 const int kc = c + 16 * hi;                   // first key (within the split) of these 16
                 uint32_t pk[8];
-                float lg = 0.0f;                              // this 16-key group's sum, in key order
-#pragma unroll
-                for (int t = 0; t < 16; t += 2) {
-                    const float p0 =
-                        key0 + kc + t <= pos ? exp2f(__fmul_rn(__uint_as_float(v[t]), sl2) - mu) : 0.0f;
-                    const float p1 =
-                        key0 + kc + t + 1 <= pos ? exp2f(__fmul_rn(__uint_as_float(v[t + 1]), sl2) - mu) : 0.0f;
-                    lg += p0;
-                    lg += p1;
-                    pk[t >> 1] = pack_bf16x2(p0, p1);
-                }
+                // this 16-key group's sum, in key order
+                const float lg = softmax_group(sv[i], sl2, nmu, pos - (key0 + kc), pk);
                 // groups 2i (hi = 0) and 2i + 1 (hi = 1) of this half: even + odd, in both threads
                 const float lo = __shfl_xor_sync(0xffffffffu, lg, 16);
                 gq[i] = hi ? lo + lg : lg + lo;
@@ -546,21 +581,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
                 const int c = 128 * ch + 32 * i;
+                if (c >= n_keys) break;
                 uint32_t v[32];
                 tmem_ld32_sync(tS + lane_base + c, v);
                 uint32_t pk[16];
-                float lg[2] = {0.0f, 0.0f};                   // the two 16-key groups' sums, in key order
-#pragma unroll
-                for (int t = 0; t < 32; t += 2) {
-                    const float p0 =
-                        key0 + c + t <= pos ? exp2f(__fmul_rn(__uint_as_float(v[t]), sl2) - mu) : 0.0f;
-                    const float p1 =
-                        key0 + c + t + 1 <= pos ? exp2f(__fmul_rn(__uint_as_float(v[t + 1]), sl2) - mu) : 0.0f;
-                    lg[t >> 4] += p0;
-                    lg[t >> 4] += p1;
-                    pk[t >> 1] = pack_bf16x2(p0, p1);
-                }
-                gq[i] = lg[0] + lg[1];
+                const float lg0 = softmax_group(v, sl2, nmu, pos - (key0 + c), pk);
+                const float lg1 = softmax_group(v + 16, sl2, nmu, pos - (key0 + c + 16), pk + 8);
+                gq[i] = lg0 + lg1;
                 uint8_t* prow = sP + (c >> 6) * (M * 128) + r * 128;
                 const int pc = (c & 63) >> 3;
 #pragma unroll
@@ -626,13 +653,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 (static_cast<long long>(row0 + i) * P.Hq + cur.kvh * P.G + g) * P.s_max + cur.split;
             float* dst = P.ws_o + ph * HD;
             if (M == 64) {
-#pragma unroll 1
+                uint32_t ov[2][16];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) tmem_ld16x2(tO + lane_base + 64 * ch + 32 * j, ov[j]);
+                tmem_ld_wait();
+#pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const int c = 64 * ch + 32 * j;
-                    uint32_t v[16];
-                    tmem_ld16x2_sync(tO + lane_base + c, v);
+                    reg_fence16(ov[j]);
+                    const uint32_t* v = ov[j];
                     if (pos >= key0) {
-                        float4* d4 = reinterpret_cast<float4*>(dst + c + 16 * hi);
+                        float4* d4 = reinterpret_cast<float4*>(dst + 64 * ch + 32 * j + 16 * hi);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
