@@ -94,20 +94,43 @@ BIV_DEV uint32_t pick_word(const U4& w, uint32_t j) {
     return j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
 }
 
-BIV_DEV void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Epilogue threads per CTA: 128 (warps 2-5, one per TMEM lane quarter), 256
+// for the fused selection (warps 2-9: two per lane quarter, each taking half of
+// a tile's columns, so two warps share every SM sub-partition's issue slots).
+template <int EPI>
+__host__ __device__ constexpr int epi_threads() { return EPI == 3 ? 256 : 128; }
 
-// Barrier over the 128 epilogue threads that also ANDs a flag across them, so
+template <int NT>
+BIV_DEV void epilogue_bar() {
+    if constexpr (NT == 256)
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+    else
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Barrier over the NT epilogue threads that also ANDs a flag across them, so
 // that a failed wait makes all of them leave the tile loop together.
+template <int NT>
 BIV_DEV bool epilogue_all(bool v) {
     uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}\n"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v))
-        : "memory");
+    if constexpr (NT == 256)
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.and.pred q, 1, 256, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}\n"
+            : "=r"(r)
+            : "r"(static_cast<uint32_t>(v))
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.and.pred q, 1, 128, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}\n"
+            : "=r"(r)
+            : "r"(static_cast<uint32_t>(v))
+            : "memory");
     return r != 0;
 }
 
@@ -211,29 +234,31 @@ constexpr int kExactBuckets = 256;
 constexpr int kChunk = 32;                    // TMEM columns per load
 constexpr int kMaxChunks = 256 / kChunk;
 
+template <int NT>
 BIV_DEV void fill_noise_table(float* ntab, float* t8) {
-    const int e = static_cast<int>(threadIdx.x) - 64;            // 0..127
-    for (int b = e; b < 256; b += 128) t8[b] = gumbel_from_word((static_cast<uint32_t>(b) << 24) | 0x00ffffffu);
-    for (int b = e; b < kExactBuckets; b += 128) {
+    const int e = static_cast<int>(threadIdx.x) - 64;            // 0..NT-1
+    for (int b = e; b < 256; b += NT) t8[b] = gumbel_from_word((static_cast<uint32_t>(b) << 24) | 0x00ffffffu);
+    for (int b = e; b < kExactBuckets; b += NT) {
         const uint32_t bb = static_cast<uint32_t>(kBuckets - kExactBuckets + b);
         ntab[bb] = gumbel_from_word((bb << (32 - kBucketBits)) | ((1u << (32 - kBucketBits)) - 1u));
     }
-    epilogue_bar();
-    for (int b = e; b < kBuckets - kExactBuckets; b += 128) ntab[b] = t8[b >> (kBucketBits - 8)];
+    epilogue_bar<NT>();
+    for (int b = e; b < kBuckets - kExactBuckets; b += NT) ntab[b] = t8[b >> (kBucketBits - 8)];
 }
 
-// Buckets of one output tile, computed by the 128 epilogue threads while the
+// Buckets of one output tile, computed by the NT epilogue threads while the
 // tile's MMAs run (the noise does not depend on the logits): for row r and
 // group gq (entries v0 = n0 + 4 gq .. v0 + 3) bk[gq * RC + r] holds the four
 // 16-bit buckets, entry j in bits [16 j, 16 j + 16) (group-major, so the 32
 // rows of a warp read 32 consecutive words).
+template <int NT>
 BIV_DEV void tile_buckets(unsigned long long* bk, int RC, int rows, int BN, int n0, int N, int row0,
                           const SelectArgs& sel) {
     const int G4 = BN / 4;
     const int total = rows * G4;
     int gq = 0, r = static_cast<int>(threadIdx.x) - 64;
     while (r >= rows) { r -= rows; ++gq; }
-    for (int idx = static_cast<int>(threadIdx.x) - 64; idx < total; idx += 128) {
+    for (int idx = static_cast<int>(threadIdx.x) - 64; idx < total; idx += NT) {
         const uint32_t v0 = static_cast<uint32_t>(n0 + 4 * gq);
         unsigned long long packed = 0;
         if (v0 < static_cast<uint32_t>(N)) {
@@ -245,7 +270,7 @@ BIV_DEV void tile_buckets(unsigned long long* bk, int RC, int rows, int BN, int 
                      (static_cast<unsigned long long>((w.z >> sh) | ((w.w >> sh) << 16)) << 32);
         }
         bk[gq * RC + r] = packed;
-        r += 128;
+        r += NT;
         while (r >= rows) { r -= rows; ++gq; }
     }
 }
@@ -291,8 +316,9 @@ BIV_DEV void seg_load<32>(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32_sync(ta
 template <>
 BIV_DEV void seg_load<16>(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16x2_sync(taddr, r); }
 
-// Winner of one tile-row of logits held in TMEM (columns [n0, n0 + BN) of a
-// row, valid below N; BN a multiple of 32), exactly as the selection kernel
+// Winner among tile columns [cb, ce) of one tile-row of logits held in TMEM
+// (columns n0 + cb .. of a row, valid below N; cb and ce multiples of 32),
+// exactly as the selection kernel
 // defines it: key = fl(fl(x * invT) + g), largest key, lowest index among
 // equal keys, a NaN never beats a number.  The row is walked in 32-column
 // chunks; with SEGW = 32 one thread owns the row (M = 128 accumulators), with
@@ -308,7 +334,7 @@ BIV_DEV void seg_load<16>(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16x2_sync(
 // of the warp needs it.  `bkrow` is the row's buckets, `cm` the thread's
 // chunk maxima (shared memory).
 template <int SEGW>
-BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N, bool live, uint32_t req,
+BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int cb, int ce, int n0, int N, bool live, uint32_t req,
                                            uint32_t pos, const SelectArgs& sel, const float* ntab,
                                            const unsigned long long* bkrow, int RC, float* cm, float* logits_row) {
     const int hoff = SEGW == 16 ? static_cast<int>(threadIdx.x & 16) : 0;
@@ -317,7 +343,7 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
     float bm2 = -INFINITY;      // the largest other bound of that entry's chunk
     int bi = -1;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += kChunk) {
+    for (int c = cb; c < ce; c += kChunk) {
         uint32_t r[SEGW];
         seg_load<SEGW>(taddr + static_cast<uint32_t>(c), r);
         if (!live) continue;
@@ -364,10 +390,10 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
     }
     unsigned long long best = 0;
     float thr = 0.0f;
-    const bool act = live && n0 + hoff < N && bi >= 0 && !sel.greedy;
-    if (live && n0 + hoff < N) {
+    const bool act = live && n0 + cb + hoff < N && bi >= 0 && !sel.greedy;
+    if (live && n0 + cb + hoff < N) {
         if (bi < 0) {
-            best = static_cast<unsigned long long>(~static_cast<uint32_t>(n0 + hoff));   // all NaN: key order 0
+            best = static_cast<unsigned long long>(~static_cast<uint32_t>(n0 + cb + hoff));   // all NaN: key order 0
         } else if (sel.greedy) {
             best = pack_key(bx, static_cast<uint32_t>(bi));
         } else {
@@ -380,7 +406,7 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
     }
     if (!sel.greedy) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += kChunk) {
+        for (int c = cb; c < ce; c += kChunk) {
             const int col0 = n0 + c + hoff;
             const bool own = bi >= col0 && bi < col0 + SEGW;
             const bool need = act && (own ? bm2 : cm[c / kChunk]) >= thr;
@@ -424,7 +450,7 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int BN, int n0, int N
 // tile-row (optional fp32 C; see biv_lm_head_gumbel), 4 = RoPE of q and k, k
 // and v into the KV cache (see biv_gemm_qkv_rope).
 template <int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + epi_threads<EPI>(), 1)
 gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                      void* __restrict__ C, const GemmArgs g, const SelectArgs sel, const RopeArgs rp) {
@@ -444,8 +470,10 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* ntab = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + kBarBytes);   // EPI 3 only
     float* t8 = ntab + kBuckets;                                                             // EPI 3 only
-    float* cmax = t8 + 256;                                                                  // EPI 3: [128][8]
-    unsigned long long* bk = reinterpret_cast<unsigned long long*>(cmax + kBM * kMaxChunks);  // EPI 3 only
+    float* cmax = t8 + 256;                                                   // EPI 3: [256][8]
+    unsigned long long* s_best = reinterpret_cast<unsigned long long*>(cmax + 2 * kBM * kMaxChunks);  // [128]
+    unsigned long long* bk = s_best + kBM;                                                   // EPI 3 only
+    constexpr int NT = epi_threads<EPI>();
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -466,7 +494,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
+            mbar_init(&tempty[a], NT);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -622,7 +650,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         const int q = warp & 3;                   // TMEM lane quarter of this warp
         if constexpr (EPI == 3) {
             // Largest noise of each bucket, while the first tile's data arrives.
-            if (!sel.greedy) fill_noise_table(ntab, t8);
+            if (!sel.greedy) fill_noise_table<NT>(ntab, t8);
         }
         const float* inv_freq = nullptr;
         if constexpr (EPI == 4) {
@@ -641,12 +669,12 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 // This tile's noise buckets while its MMAs run; the vote below is
                 // also the barrier that makes them (and the table) visible.
                 if (!sel.greedy)
-                    tile_buckets(bk, g.a_rows, min(kBM, M - m_blk * kBM), BN, n_blk * BN, N, m_blk * kBM, sel);
+                    tile_buckets<NT>(bk, g.a_rows, min(kBM, M - m_blk * kBM), BN, n_blk * BN, N, m_blk * kBM, sel);
             }
             // One thread polls the accumulator barrier; the vote hands its
             // outcome to the other 127 (no polling traffic beside the copies).
             bool ok = threadIdx.x == 64 ? mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err) : true;
-            ok = epilogue_all(ok);
+            ok = epilogue_all<NT>(ok);
             if (!ok) break;
             tc_fence_after();
             // M = 128 MMAs put tile row r in TMEM lane r; M = 64 MMAs put row r in
@@ -665,14 +693,21 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 const uint32_t pos = slive ? static_cast<uint32_t>(sel.row_pos[srow]) + 1u : 0u;
                 float* lrow = (C != nullptr && slive) ? static_cast<float*>(C) + static_cast<long long>(srow) * N
                                                       : nullptr;
-                float* cmt = cmax + (q * 32 + lane) * kMaxChunks;
-                const unsigned long long best =
-                    g.m64 ? tile_row_winner<16>(taddr, BN, n_blk * BN, N, slive, req, pos, sel, ntab, bk + srloc,
+                // warps 2-5 take the tile's first half of 32-column chunks, warps
+                // 6-9 the rest; their winners meet in shared memory
+                const int eset = (warp - 2) >> 2;
+                const int nch = BN / kChunk, h1 = (nch + 1) / 2;
+                const int cb = eset ? h1 * kChunk : 0, ce = eset ? BN : h1 * kChunk;
+                float* cmt = cmax + (eset * kBM + q * 32 + lane) * kMaxChunks;
+                unsigned long long best =
+                    g.m64 ? tile_row_winner<16>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab, bk + srloc,
                                                 g.a_rows, cmt, lrow)
-                          : tile_row_winner<32>(taddr, BN, n_blk * BN, N, slive, req, pos, sel, ntab, bk + srloc,
+                          : tile_row_winner<32>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab, bk + srloc,
                                                 g.a_rows, cmt, lrow);
-                if (live) sel.cand[static_cast<long long>(srow) * n_tiles + n_blk] = best;
-                epilogue_bar();       // every row is done with the buckets before the next tile's
+                if (eset == 1 && live) s_best[rloc] = best;
+                epilogue_bar<NT>();   // both halves' winners are in; every row is done with the buckets
+                if (eset == 0 && live)
+                    sel.cand[static_cast<long long>(srow) * n_tiles + n_blk] = umax64(best, s_best[rloc]);
             } else if constexpr (EPI == 4) {
                 // With M = 64 accumulators the two half-warps share each row:
                 // threads 16..31 take pairs 4..7 of every 16-column group.
@@ -852,7 +887,7 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
     const int tail = g.a_rows < kBM ? kTailSlack : 0;
     // EPI 3 keeps the noise table, chunk maxima and one tile of noise buckets
     // beside the ring, and takes all of the opt-in shared memory.
-    const int extra = EPI == 3 ? kNoiseTableBytes + kBM * kMaxChunks * 4 + g.a_rows * BN * 2 : 0;
+    const int extra = EPI == 3 ? kNoiseTableBytes + 2 * kBM * kMaxChunks * 4 + kBM * 8 + g.a_rows * BN * 2 : 0;
     const int ring = EPI == 3 ? kMaxSmem - 1024 - kBarBytes - extra : kRingBudget;
     if (g.three_d && g.a_rows < kBM) {
         const int per_kb = (g.a_rows + BN) * kRowBytes;
@@ -892,7 +927,8 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
     }
     const long long work = static_cast<long long>((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<long long>(work, num_sms()));
-    return launch_pdl(kern, dim3(grid), dim3(192), static_cast<size_t>(smem), stream, ta, tb, ta1, tb1, C, g, sel,
+    return launch_pdl(kern, dim3(grid), dim3(64 + epi_threads<EPI>()), static_cast<size_t>(smem), stream, ta, tb, ta1,
+                      tb1, C, g, sel,
                       rp);
 }
 
