@@ -476,22 +476,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             break;
         }
         tc_fence_after();
-        // ---- S = Q K^T, issued by one thread
-        if (threadIdx.x == 0) {
+        // ---- S = Q K^T, issued by warp 0: every lane observes the K halves (a
+        // time-out anywhere stops all), one elected lane issues the MMAs.
+        if (warp == 0) {
             bool got = true;
             for (int kh = 0; kh < nkh && got; ++kh) got = take(&kbar[kh], k_use[kh], k_seen[kh]);
+            got = __all_sync(0xffffffffu, got);
             if (got) {
                 tc_fence_after();
                 constexpr uint32_t idS = idesc_bf16_f32(M, 128);
-                for (int kh = 0; kh < nkh; ++kh)
+                const uint64_t dq = sw128_kmajor_desc(uQ), dk = sw128_kmajor_desc(uK);
+#pragma unroll
+                for (int kh = 0; kh < 2; ++kh) {
+                    if (kh >= nkh) break;
+#pragma unroll
                     for (int k = 0; k < HD / 16; ++k) {
-                        const uint64_t a = sw128_kmajor_desc(uQ + (k >> 2) * (M * 128) + (k & 3) * 32);
+                        // start addresses advance in 16-byte units inside the descriptor
+                        const uint64_t a = dq + static_cast<uint64_t>(((k >> 2) * (M * 128) + (k & 3) * 32) >> 4);
                         const uint64_t b =
-                            sw128_kmajor_desc(uK + kh * kTcKeyHalfBytes + (k >> 2) * 16384 + (k & 3) * 32);
-                        umma_bf16(tS + kh * 128, a, b, idS, k > 0 ? 1u : 0u);
+                            dk + static_cast<uint64_t>((kh * kTcKeyHalfBytes + (k >> 2) * 16384 + (k & 3) * 32) >> 4);
+                        umma_bf16_elect(tS + kh * 128, a, b, idS, k > 0 ? 1u : 0u);
                     }
-                umma_commit(&sbar);
-            } else {
+                }
+                umma_commit_elect(&sbar);
+            } else if (lane == 0) {
                 mbar_arrive(&sbar);                        // nothing issued: release the waiters
             }
             ++s_iss;
@@ -618,20 +626,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             break;
         }
         tc_fence_after();
-        // ---- O = P V, issued by one thread
-        if (threadIdx.x == 0) {
+        // ---- O = P V, issued by warp 0 like S
+        if (warp == 0) {
             bool got = true;
             for (int kh = 0; kh < nkh && got; ++kh) got = take(&vbar[kh], v_use[kh], v_seen[kh]);
+            got = __all_sync(0xffffffffu, got);
             if (got) {
                 tc_fence_after();
                 constexpr uint32_t idO = idesc_bf16_f32(M, 128) | (1u << 16);   // B (V) MN-major
+                const uint64_t dp = sw128_kmajor_desc(uP), dv = sw128_mnmajor_desc(uV);
                 for (int st = 0; st < n16; ++st) {
-                    const uint64_t a = sw128_kmajor_desc(uP + (st >> 2) * (M * 128) + (st & 3) * 32);
-                    const uint64_t b = sw128_mnmajor_desc(uV + (st >> 3) * kTcKeyHalfBytes + (st & 7) * 2048);
-                    umma_bf16(tO, a, b, idO, st > 0 ? 1u : 0u);
+                    const uint64_t a = dp + static_cast<uint64_t>(((st >> 2) * (M * 128) + (st & 3) * 32) >> 4);
+                    const uint64_t b =
+                        dv + static_cast<uint64_t>(((st >> 3) * kTcKeyHalfBytes + (st & 7) * 2048) >> 4);
+                    umma_bf16_elect(tO, a, b, idO, st > 0 ? 1u : 0u);
                 }
-                umma_commit(&obar);
-            } else {
+                umma_commit_elect(&obar);
+            } else if (lane == 0) {
                 mbar_arrive(&obar);
             }
             ++o_iss;
