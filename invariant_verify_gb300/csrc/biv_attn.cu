@@ -129,7 +129,10 @@ BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, in
         const int t = group * P.tiles_per_group + sub;
         if (t >= kMaxTilesSmem) break;                       // rows only grow the tile index
         const int row0 = group * P.rows_per_group + sub * P.tile_rows;
+        // the three loads are independent: one round trip (the inputs are cold
+        // in HBM when the kernel starts)
         const int slot0 = P.row_slot[row0];
+        const int s = P.row_slot[w], p = P.row_pos[w];
         if (w == row0) s_slot0[t] = slot0;
         if (slot0 < 0 || slot0 >= P.n_slots) {
             if (w == row0 && blockIdx.x == 0) atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
@@ -137,7 +140,6 @@ BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, in
             continue;
         }
         // the row checks of row_ok(), raised once (by CTA 0)
-        const int s = P.row_slot[w], p = P.row_pos[w];
         int vp = -1;
         if (s < 0 || s >= P.n_slots || p < 0 || p >= P.max_len) {
             if (blockIdx.x == 0) atomicOr(&g_attn_err, BIV_DEVERR_INDEX);
