@@ -510,11 +510,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         if (mbar_wait(&sbar, s_use & 1u, &abort_flag, &g_attn_err) && threadIdx.x == 0) ++s_seen;
         ++s_use;
         tc_fence_after();
-        // ---- S is in TMEM: this item's Q (and K for M = 64) may be overwritten
-        if (has_nxt && !aborted()) {
-            if (M == 64 && threadIdx.x == 0) load_kv(&tmK, sK, kbar, k_iss, nxt);
-            load_q(nxt);
-        }
+        // ---- S is in TMEM: this item's K may be overwritten (M = 64)
+        if (M == 64 && has_nxt && threadIdx.x == 0 && !aborted()) load_kv(&tmK, sK, kbar, k_iss, nxt);
 
         // ---- softmax over the split, row by row
         const int q4 = warp & 3, ch = warp >> 2;
@@ -650,6 +647,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             ++o_iss;
         }
         for (int kh = 0; kh < nkh; ++kh) ++v_use[kh];
+        // the next item's Q (this item's has been read since S landed), while P V runs
+        if (has_nxt && !aborted()) load_q(nxt);
         if (mbar_wait(&obar, o_use & 1u, &abort_flag, &g_attn_err) && threadIdx.x == 0) ++o_seen;
         ++o_use;
         tc_fence_after();
