@@ -41,10 +41,12 @@
  *     smallest position (the requests' committed context).  They must not be
  *     written by the immediately preceding libbiv kernel on the stream
  *     (kernels of other libraries, and copies, are waited for in full).
- *   - No call allocates device memory.  The one exception in kind is the fixed
- *     scratch array behind biv_decode_attn_fixedsplit_noalloc, which is part
- *     of the loaded module (BIV_NOALLOC_SCRATCH_BYTES per GPU, held until the
- *     process exits).
+ *   - No call allocates device memory.  The exceptions in kind are part of
+ *     the loaded module and held until the process exits: the fixed scratch
+ *     array behind biv_decode_attn_fixedsplit_noalloc
+ *     (BIV_NOALLOC_SCRATCH_BYTES per GPU) and the 512-byte ring of row
+ *     counters of the streaming selection (64 slots, each reset to zero by
+ *     the call that used it).
  */
 #ifndef BIV_H_
 #define BIV_H_
