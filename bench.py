@@ -259,7 +259,7 @@ def run_ours(args):
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     lm_ms = []
-    out_dir = os.path.join(ROOT, "gpurun_out")
+    out_dir = os.environ.get("BIV_BENCH_OUT_DIR", "/tmp")      # where the raw clock samples go
     clk_path = os.path.join(out_dir if os.path.isdir(out_dir) else "/tmp", f"bench_clocks_rank{rank}.csv")
     sampler, sf = clock_sampler_start(clk_path) if local == 0 else (None, None)
     if world > 1:
