@@ -377,16 +377,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
     };
     // all threads: the item's Q rows into sQ (K-major, 128-byte swizzle)
+    // Thread x copies 16-byte piece c = x % 16 of tile rows t = x / 16 + 16 j:
+    // the piece and the row's swizzle phase (t & 7) are the same for every j,
+    // and (i, g) = (t / G, t % G) advance by fixed steps, so the loop has no
+    // division.
+    const int q_c = threadIdx.x & 15, q_t0 = threadIdx.x >> 4;
+    const uint32_t q_dst0 = uQ + (q_c >> 3) * (M * 128) + q_t0 * 128 + (((q_c & 7) ^ (q_t0 & 7)) << 4);
+    const int q_di = 16 / P.G, q_dg = 16 % P.G;
+    const int q_i0 = q_t0 / P.G, q_g0 = q_t0 % P.G;
     auto load_q = [&](const TcItem& it) {
         int row0, nr;
         tile_rows_of(P, it.tile, row0, nr);
         const int T = nr * P.G;
-        for (int idx = threadIdx.x; idx < T * 16; idx += ATTN_THREADS) {
-            const int t = idx >> 4, c = idx & 15;
-            const int i = t / P.G, g = t - i * P.G;
-            const __nv_bfloat16* src =
-                P.q + (static_cast<long long>(row0 + i) * P.Hq + it.kvh * P.G + g) * HD + c * 8;
-            cp_async16(uQ + (c >> 3) * (M * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4), src);
+        const __nv_bfloat16* base = P.q + (static_cast<long long>(row0) * P.Hq + it.kvh * P.G) * HD + q_c * 8;
+        int i = q_i0, g = q_g0;
+        for (int t = q_t0, j = 0; t < T; t += 16, ++j) {
+            cp_async16(q_dst0 + static_cast<uint32_t>(j) * 2048u, base + (static_cast<long long>(i) * P.Hq + g) * HD);
+            i += q_di;
+            g += q_dg;
+            if (g >= P.G) {
+                g -= P.G;
+                ++i;
+            }
         }
         cp_async_commit();
     };
