@@ -1,22 +1,30 @@
 """Benchmark: verified tokens/s of the batch-invariant verify step.
 
-Workload: the random-init 2-layer decoder verifier (d=1024, 8 query / 2 KV
-heads of 128, SwiGLU 2816, vocab 32000, bf16 weights ~N(0, 0.02)), one
-window of N=8 requests x K=8 tokens (W = 64 rows), per-request contexts
-~U[128, 2048], fixed KV split 256, drafts with a 30% random-token error
-rate, Gumbel selection at T=0.7.  One step = the whole hot path: embed,
-2 x (RMSNorm, QKV GEMM, RoPE, KV overwrite, fixed-split attention, Wo GEMM,
-residual, RMSNorm, gate/up GEMM, SwiGLU, down GEMM, residual), RMSNorm,
-LM-head GEMM (fp32 logits), Gumbel-max selection, coupled accept.
+Workload (the default line): one Llama-3-8B-shaped decoder layer + LM head
+(d 4096, 32 query / 8 KV heads of 128, SwiGLU 14336, vocab 128256, bf16
+weights ~N(0, 0.02), random init), verifying one window of N = 64 requests x
+K = 16 tokens (W = 1024 rows).  Per-request cached contexts are lognormal
+(median 1024, sigma 1, clipped to [256, 8192]), fixed KV split 256, drafts
+that disagree with the verifier at Bernoulli(0.2) positions, Gumbel
+selection at T = 0.7.  One step = the whole hot path: embed + RMSNorm, the
+QKV GEMM with RoPE and the KV overwrite, fixed-split attention, Wo GEMM,
+residual + RMSNorm, gate/up GEMM with SwiGLU, down GEMM, residual + RMSNorm,
+the LM-head GEMM with the Gumbel-max selection in its epilogue, winners and
+the coupled accept -- replayed as one CUDA graph.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+The line also carries the 2-layer decoder window (d 1024, W = 64) as
+``decoder2_w64``, a per-kernel breakdown of the step, the dominant kernel's
+roofline, an end-to-end figure from host buffers, and the CPU oracle timed
+on a sample of the same workload.
 
 Multi-GPU (torchrun): the path shards by request, so each rank runs its own
 replica window (weak scaling, no collective on the data path); value is the
 rows of all ranks over the slowest rank's time.
 
 --impl reference times the CPU oracle (the plain C++ reference) on the same
-workload, one window row per step, on the host cores.
+workload: each step verifies one request's K window rows.
 """
 from __future__ import annotations
 
@@ -39,16 +47,18 @@ import torch  # noqa: E402
 METRIC = "verified tok/s at W=N·K, batch-invariant; % of bf16 tensor-core / HBM roofline"
 UNIT = "verified tok/s"
 L2_FLUSH_BYTES = 256 << 20
+SEED = 0x1234_5678_9ABC_DEF0
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decoder2", action="store_true", help="skip the 2-layer decoder (W = 64) extra line")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--gemm-sweep", action="store_true",
                    help="instead of the step bench: no-split-K GEMM vs cuBLAS on the Llama-3-8B shapes")
@@ -57,9 +67,8 @@ def parse():
     p.add_argument("--c4-steps", action="store_true",
                    help="instead of the step bench: verified tok/s of whole verify steps on the Llama-3-8B-shaped "
                         "layer + LM head at the verifier sweep's windows (N x K = 8x4, 32x8, 64x16)")
-    p.add_argument("--profile-case", choices=["attn16", "select1024"],
-                   help="run one small case twice, for a profiler capture: attention on 16 requests x 16 rows "
-                        "(C4 recipe) or selection on 1024 rows (C5 recipe, T = 0.7 then T = 0)")
+    p.add_argument("--profile-case", choices=["attn16", "select1024", "lmhead1024", "rmsnorm", "gemm1024"],
+                   help="run one small case twice, for a profiler capture")
     return p.parse_args()
 
 
@@ -71,41 +80,57 @@ def dist_info():
 
 
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
-    return 6800.0, 1900.0, "fallback"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def workload_config(cfg):
-    return {"workload": "2-layer decoder verifier d1024 8q/2kv hd128 ffn2816 vocab32000 (random init)",
-            "N": cfg.N, "K": cfg.K, "W": cfg.W, "layers": cfg.layers, "d": cfg.d, "vocab": cfg.vocab,
-            "ctx": f"U[{cfg.ctx_lo},{cfg.ctx_hi}]", "kv_split": cfg.kv_split, "temperature": cfg.temperature,
-            "draft_error_rate": cfg.draft_err, "l2": "flushed between timed steps (256 MiB write, outside the step events)"}
+WORKLOADS = {
+    # name: (config, N, K)
+    "c4": ("SWEEP", 64, 16),
+    "decoder2": ("DECODER2", 8, 8),
+}
+
+
+def workload_config(cfg, N, K):
+    W = N * K
+    if cfg.d == 4096:
+        name = (f"Llama-3-8B-shaped decoder layer + LM head (d4096 32q/8kv hd128 ffn14336 vocab128256, random init), "
+                f"verifier window N{N} x K{K} = W{W}, lognormal ctx")
+        ctx = f"lognormal median {cfg.ctx_median:g} sigma {cfg.ctx_sigma:g} clip [{cfg.ctx_lo},{cfg.ctx_hi}]"
+        l2 = "inputs larger than L2 (1.49 GB of weights and ~0.4 GB of KV streamed every step)"
+    else:
+        name = "2-layer decoder verifier d1024 8q/2kv hd128 ffn2816 vocab32000 (random init)"
+        ctx = f"U[{cfg.ctx_lo},{cfg.ctx_hi}]"
+        l2 = "flushed between timed steps (256 MiB write, outside the step events)"
+    return {"workload": name, "N": N, "K": K, "W": W, "layers": cfg.layers, "d": cfg.d, "vocab": cfg.vocab,
+            "ctx": ctx, "kv_split": cfg.kv_split, "temperature": cfg.temperature,
+            "draft_error_rate": cfg.draft_err, "l2": l2}
 
 
 # ------------------------------------------------------------------ setup
-def build_problem(cfg, device, rank=0):
-    """The rank's own window: requests rank*N .. rank*N + N - 1 of the job,
-    with their own contexts, caches and drafts (weak scaling)."""
+def build_problem(cfg, N, K, device, rank=0, weights=None):
+    """The rank's own window: its requests' contexts, caches and drafts from
+    replicas.rank_window_plan (weak scaling; the weights are the replicas'
+    shared model).  The drafts are fixed one position at a time from the
+    verifier's own selections, then corrupted where the plan says the drafter
+    errs."""
     from invariant_verify_gb300 import replicas, synth
     from invariant_verify_gb300.verifier import DecoderVerifier, make_window
-    w = synth.decoder_weights(cfg)
-    ctx = synth.context_lengths(cfg, cfg.N, seed=cfg.seed + 100 + rank)
-    max_len = int(ctx.max()) + 64
-    caches = synth.kv_cache(cfg.N, cfg.Hkv, max_len, cfg.hd, ctx, seed=cfg.seed + 200 + rank,
-                            layers=cfg.layers)
-    ver = DecoderVerifier(cfg, w, caches, cfg.N, max_len, cfg.W, cfg.K, device=device, fused_select=True,
-                          keep_logits=False)
-    g = synth.generator(cfg.seed + 300 + rank)
-    N, K = cfg.N, cfg.K
-    last = torch.randint(0, cfg.vocab, (N,), generator=g, dtype=torch.int64).to(torch.int32)
-    mask, ids = synth.draft_errors((N, K), cfg.draft_err, cfg.vocab, seed=cfg.seed + 400 + rank)
-    req = replicas.request_ids(replicas.rank_requests(N, rank))
-    # A drafter that is right 70% of the time: fix d_1..d_K one position at a
-    # time from the verifier's own selections (d_j feeds row j).
+    plan = replicas.rank_window_plan(cfg, N, K, rank)
+    w = synth.decoder_weights_device(cfg, device=device) if weights is None else weights
+    ctx = plan["ctx"]
+    max_len = int(ctx.max()) + K + 16
+    caches = synth.kv_cache_device(N, cfg.Hkv, max_len, cfg.hd, ctx, seed=plan["kv_seed"], layers=cfg.layers,
+                                   device=device)
+    ver = DecoderVerifier(cfg, w, caches, N, max_len, N * K, K, device=device, fused_select=True,
+                          keep_logits=False, seed=SEED)
+    last, mask, ids, req = plan["last"], plan["draft_mask"], plan["draft_ids"], plan["req_ids"]
     drafts = torch.zeros(N, K, dtype=torch.int32)
     for j in range(K):
         tokens = torch.cat([last[:, None], drafts[:, :-1]], dim=1)
@@ -115,16 +140,34 @@ def build_problem(cfg, device, rank=0):
         drafts[:, j] = torch.where(mask[:, j], ids[:, j], tgt)
     tokens = torch.cat([last[:, None], drafts[:, :-1]], dim=1)
     win = make_window(N, K, tokens.reshape(-1), ctx, req, drafts.reshape(-1), device=device)
-    return ver, win, w, caches, max_len, ctx
+    return {"cfg": cfg, "N": N, "K": K, "W": N * K, "ver": ver, "win": win, "w": w, "caches": caches,
+            "max_len": max_len, "ctx": ctx, "tokens": tokens, "drafts": drafts, "req": req}
+
+
+_SMI_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def clock_snapshot(f):
+    """One nvidia-smi sample appended to the open file ``f`` (best effort)."""
+    try:
+        out = subprocess.run(["nvidia-smi", f"--query-gpu={_SMI_QUERY}", "--format=csv,noheader,nounits"],
+                             capture_output=True, text=True, timeout=10).stdout
+        f.write(out)
+        f.flush()
+    except Exception:
+        pass
 
 
 def clock_sampler_start(path):
-    q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """A 100 ms nvidia-smi sampler over the timed region, plus one sample taken
+    right before it (another is taken right after, by clock_sampler_stop), so
+    the record is never empty however short the region."""
     try:
         f = open(path, "w")
-        p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100"],
+        clock_snapshot(f)
+        p = subprocess.Popen(["nvidia-smi", f"--query-gpu={_SMI_QUERY}", "--format=csv,noheader,nounits", "-lms", "100"],
                              stdout=f, stderr=subprocess.DEVNULL)
         return p, f
     except Exception:
@@ -132,13 +175,15 @@ def clock_sampler_start(path):
 
 
 def clock_sampler_stop(p, f, path, gpu_index):
-    if p is None:
+    if f is None:
         return None
-    p.terminate()
-    try:
-        p.wait(timeout=5)
-    except Exception:
-        p.kill()
+    if p is not None:
+        p.terminate()
+        try:
+            p.wait(timeout=5)
+        except Exception:
+            p.kill()
+    clock_snapshot(f)
     f.close()
     sm, mx, reasons = [], None, set()
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -156,14 +201,14 @@ def clock_sampler_stop(p, f, path, gpu_index):
                 reasons.add(n)
     if not sm:
         return None
-    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons),
+            "how": "nvidia-smi every 100 ms during the timed region, plus one sample just before and one just after"}
 
 
-def lm_head_traffic():
-    """Per-launch DRAM bytes of the fused LM-head/selection kernel from the
-    committed ncu summary, or None when the kernel source changed since that
-    capture."""
-    path = os.path.join(ROOT, "profiles", "lmhead_select_fused_decoder2.md")
+def profile_traffic(name):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary under
+    profiles/, or None when its sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -175,7 +220,7 @@ def lm_head_traffic():
 
 
 def kernel_source_sha256():
-    """Hash of the sources the fused LM-head/selection kernel is built from."""
+    """Hash of the sources the GEMM kernels (and the fused selection) are built from."""
     csrc = os.path.join(ROOT, "invariant_verify_gb300", "csrc")
     h = hashlib.sha256()
     for name in ("biv_gemm.cu", "biv_gumbel.cuh", "biv_common.cuh"):
@@ -211,36 +256,90 @@ def marked_graphs(ver, win, n):
         return None
 
 
-# --------------------------------------------------------------- our arm
-def run_ours(args):
-    import torch.distributed as dist
-    from invariant_verify_gb300 import replicas, synth
-    import __graft_entry__
-    rank, world, local = dist_info()
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    if rank == 0:
-        __graft_entry__.build()
-    if world > 1:
-        dist.barrier()
-    cfg = synth.DECODER2
-    ver, win, w_cpu, caches_cpu, max_len, ctx = build_problem(cfg, device, rank=rank)
-    full_graph = ver.capture(win, segments=False)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+def kernel_breakdown(ver, win, reps=7):
+    """Duration of each library call of the step: one graph with a timing
+    event recorded after every call (so consecutive calls lose their
+    programmatic-launch overlap), replayed ``reps`` times; medians in us.
+    None where events cannot be graph nodes."""
+    try:
+        marks = []
+
+        def mark(name):
+            e = torch.cuda.Event(enable_timing=True, external=True)
+            e.record()
+            marks.append((name, e))
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            e0 = torch.cuda.Event(enable_timing=True, external=True)
+            e0.record()
+            ver.step(win, mark=mark)
+        times = {name: [] for name, _ in marks}
+        for _ in range(reps):
+            g.replay()
+            torch.cuda.synchronize()
+            prev = e0
+            for name, e in marks:
+                times[name].append(prev.elapsed_time(e) * 1e3)
+                prev = e
+        return {name: statistics.median(v) for name, v in times.items()}
+    except (TypeError, RuntimeError) as exc:
+        print(f"bench: no per-kernel breakdown ({exc})", file=sys.stderr)
+        torch.cuda.synchronize()
+        return None
+
+
+def stage_work(cfg, W, K, ctx):
+    """Algorithmic (flops, bytes) of each library call of one step: weights
+    once, activations in and out, KV read; the logits never reach HBM."""
+    d, F, V, hd, Hq, Hkv = cfg.d, cfg.ffn, cfg.vocab, cfg.hd, cfg.Hq, cfg.Hkv
+    qn = cfg.qkv_n
+    ctxs = [int(c) for c in ctx]
+    kv_read = sum(2 * 2 * Hkv * (c + K) * hd for c in ctxs)
+    attn_flops = 4 * Hq * hd * sum(K * c + K * (K + 1) // 2 for c in ctxs)
+    out = {"embed_rmsnorm": (0, 2 * W * d * 3 + 2 * d + 4 * W)}
+    for l in range(cfg.layers):
+        out[f"l{l}.qkv_rope"] = (2 * W * qn * d, 2 * qn * d + 2 * W * d + 2 * W * qn)
+        out[f"l{l}.attention"] = (attn_flops, kv_read + 2 * 2 * W * Hq * hd)
+        out[f"l{l}.wo"] = (2 * W * d * Hq * hd, 2 * d * Hq * hd + 2 * W * Hq * hd + 2 * W * d)
+        out[f"l{l}.add_rmsnorm1"] = (0, 2 * W * d * 4 + 2 * d)
+        out[f"l{l}.gate_up_swiglu"] = (2 * W * 2 * F * d, 2 * 2 * F * d + 2 * W * d + 2 * W * F)
+        out[f"l{l}.down"] = (2 * W * d * F, 2 * d * F + 2 * W * F + 2 * W * d)
+        out[f"l{l}.add_rmsnorm2"] = (0, 2 * W * d * 4 + 2 * d)
+    out["lm_head_select_accept"] = (2 * W * V * d, 2 * V * d + 2 * W * d + 12 * W)
+    return out
+
+
+def step_work(cfg, W, K, ctx):
+    work = stage_work(cfg, W, K, ctx)
+    return sum(b for _, b in work.values()), sum(f for f, _ in work.values())
+
+
+def breakdown_lines(cfg, W, K, ctx, times, hbm, bf16):
+    work = stage_work(cfg, W, K, ctx)
+    rows = []
+    for name, us in times.items():
+        flops, byts = work.get(name, (0, 0))
+        t_tensor, t_hbm = flops / (bf16 * 1e12), byts / (hbm * 1e9)
+        bound = "tensor" if t_tensor >= t_hbm else "hbm"
+        rows.append({"call": name, "us": round(us, 2), "flops": flops, "bytes": byts, "bound": bound,
+                     "tflops": round(flops / us / 1e6, 1), "gbs": round(byts / us / 1e3, 1),
+                     "frac": round(max(t_tensor, t_hbm) * 1e6 / us, 4)})
+    return rows
+
+
+def time_steps(ver, win, K, warmup, world, device, rank, local, flush=None, lm_pool=True):
+    """Device time of K whole-step graph replays (events on the launching
+    stream, max over ranks) and the LM-head launch durations inside them."""
+    from invariant_verify_gb300 import replicas
     stream = torch.cuda.current_stream()
-    K = args.steps
-    # Each timed step replays one graph of the whole step.  The LM-head launch
-    # is bracketed by event-record nodes inside that graph (a pool of graphs,
-    # each with its own event pair, read back once its replay has finished);
-    # where event nodes are unavailable the step is replayed as two graphs
-    # with events between them.
-    pool = marked_graphs(ver, win, min(K, 16))
+    full_graph = ver.capture(win, segments=False)
+    pool = marked_graphs(ver, win, min(K, 16)) if lm_pool else None
     lm_timing = "event-record nodes around the LM-head launch inside the step graph"
     if pool is None:
         segs = ver.capture(win, segments=True)
         lm_timing = "events between graph segments (layers | LM head + selection + accept)"
+    seg_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)] if pool is None else None
 
     def one_step(i):
         if pool is None:
@@ -251,18 +350,18 @@ def run_ours(args):
         else:
             pool[i % len(pool)][0].replay()
 
-    seg_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)] if pool is None else None
-    for i in range(max(3, args.warmup)):
-        flush.zero_()
+    for i in range(max(3, warmup)):
+        if flush is not None:
+            flush.zero_()
         one_step(i % K)
     torch.cuda.synchronize()
-
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     lm_ms = []
     out_dir = os.environ.get("BIV_BENCH_OUT_DIR", "/tmp")      # where the raw clock samples go
     clk_path = os.path.join(out_dir if os.path.isdir(out_dir) else "/tmp", f"bench_clocks_rank{rank}.csv")
     sampler, sf = clock_sampler_start(clk_path) if local == 0 else (None, None)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -271,13 +370,15 @@ def run_ours(args):
             _, ea, eb = pool[i % len(pool)]
             eb.synchronize()                 # that graph's previous replay is done
             lm_ms.append(ea.elapsed_time(eb))
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         e = ev[i]
         e[0].record(stream)
         one_step(i)
         e[1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     wall = time.perf_counter() - t0
     clocks = clock_sampler_stop(sampler, sf, clk_path, local)
@@ -289,74 +390,18 @@ def run_ours(args):
         lm_ms = [a.elapsed_time(b) for a, b in seg_ev]
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     tot_ms = replicas.slowest(float(sum(step_ms)), device=device)
-    ms_per_step = tot_ms / K
-    value = cfg.W * world * K / (tot_ms / 1e3)
-    committed = int(ver.accept_len.sum().item())
-
-    # roofline of the dominant kernel (LM-head GEMM, HBM-bound at W=64)
-    hbm, bf16, src = peaks()
-    M, N, Kd = cfg.W, cfg.vocab, cfg.d
-    # weights + activations in, request ids / positions in, tokens out (the
-    # logits stay in TMEM; the per-tile winners and the accept's few bytes
-    # per request are not counted)
-    lm_bytes = 2 * N * Kd + 2 * M * Kd + 12 * M
-    lm_avg_s = statistics.mean(lm_ms) / 1e3
-    achieved = lm_bytes / lm_avg_s / 1e9
-    roofline = {"kernel": "gemm_nosplitk_kernel<3> + winners_accept_kernel (LM head M=64 N=32000 K=1024 with "
-                          "the Gumbel-max selection in its epilogue, then the per-row winners and the accept)",
-                "bound": "hbm",
-                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback",
-                "traffic": lm_head_traffic(), "algorithmic_bytes": lm_bytes,
-                "avg_launch_us": round(lm_avg_s * 1e6, 2), "launch_timing": lm_timing}
-    step_bytes, step_flops = step_work(cfg, ctx)
-    step_roof_us = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12)) * 1e6
-
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(ver, win, full_graph, flush, cfg, max(50, min(K, 2000)), world, device)
-
-    out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
-           "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": workload_config(cfg) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-           "roofline": roofline,
-           "step_roofline": {"bytes": step_bytes, "flops": step_flops, "lower_bound_us": round(step_roof_us, 2),
-                             "frac": round(step_roof_us / (ms_per_step * 1e3), 4)},
-           "committed_tok_per_s": round(committed * world * K / (tot_ms / 1e3), 1),
-           "gpu_launches": ver.launches_per_step * K,
-           "timed_region_wall_s": round(wall, 3),
-           "clocks": clocks, "e2e": e2e}
-    if rank == 0:
-        if not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(cfg, w_cpu, caches_cpu, max_len, win, args.cpu_seconds)
-        print(json.dumps(out), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+    return {"tot_ms": tot_ms, "lm_ms": lm_ms, "lm_timing": lm_timing, "wall": wall, "clocks": clocks,
+            "graph": full_graph}
 
 
-def step_work(cfg, ctx):
-    """Algorithmic bytes and flops of one step (weights once, KV read,
-    activations ignored; the logits never reach HBM)."""
-    W, d, F, V, hd = cfg.W, cfg.d, cfg.ffn, cfg.vocab, cfg.hd
-    per_layer_w = (cfg.qkv_n * d + d * cfg.Hq * hd + 2 * F * d + d * F) * 2
-    weights = cfg.layers * per_layer_w + V * d * 2
-    kv = sum(2 * 2 * cfg.Hkv * (int(c) + cfg.K) * hd for c in ctx) * cfg.layers
-    logits = 0
-    flops = 2 * W * (cfg.layers * per_layer_w // 2 + V * d)
-    flops += cfg.layers * sum(4 * cfg.Hq * cfg.K * (int(c) + cfg.K) * hd for c in ctx)
-    return weights + kv + logits, flops
-
-
-def run_e2e(ver, win, graph, flush, cfg, K, world, device):
+def run_e2e(ver, win, cfg, N, K, steps, world, flush=None):
     """Same metric through the public API with host buffers: each step copies
     the window's inputs from pinned host memory (one copy of the packed
     inputs), runs the step, and reads the accept lengths, rollback points and
     selected tokens back (one copy of the packed results) -- the three as
     nodes of one CUDA graph, replayed and synchronised per step."""
     from invariant_verify_gb300.verifier import PackedWindow, capture_e2e
-    pw = PackedWindow(cfg.N, cfg.K, device=device)
+    pw = PackedWindow(N, K, device=ver.x.device)
     pw.set(win)
     host_out = torch.empty_like(ver.results, device="cpu").pin_memory()
     g = capture_e2e(ver, pw, host_out)
@@ -364,19 +409,214 @@ def run_e2e(ver, win, graph, flush, cfg, K, world, device):
     d2h = host_out.numel() * host_out.element_size()
     stream = torch.cuda.current_stream()
     total = 0.0
-    for i in range(K + 5):
-        flush.zero_()
+    for i in range(steps + 5):
+        if flush is not None:
+            flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         g.replay()
         stream.synchronize()
         if i >= 5:
             total += time.perf_counter() - t0
-    value = cfg.W * world * K / total
+    value = N * K * world * steps / total
     return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": K, "ms_per_step": round(total / K * 1e3, 5),
+            "steps": steps, "ms_per_step": round(total / steps * 1e3, 5),
             "how": "one CUDA graph per step: pinned H2D of the packed window inputs, the step, D2H of the packed "
                    "accept_len/new_len/tokens; host wall time per step including the synchronisation"}
+
+
+# --------------------------------------------------------------- our arm
+def lm_roofline(cfg, W, lm_ms, lm_timing, hbm, bf16, bf16_sus, src):
+    """Roofline of the LM-head launch (GEMM with the fused selection, then the
+    winners + accept kernel): tensor-bound once W is a few hundred rows,
+    weight-streaming (HBM) below."""
+    M, N, Kd = W, cfg.vocab, cfg.d
+    flops = 2 * M * N * Kd
+    byts = 2 * N * Kd + 2 * M * Kd + 12 * M       # weights + rows in, ids/positions in, tokens out
+    avg_s = statistics.mean(lm_ms) / 1e3
+    kernel = (f"gemm_nosplitk_kernel<3> + winners_accept_kernel (LM head M={M} N={N} K={Kd} with the "
+              f"Gumbel-max selection in its epilogue, then the per-row winners and the accept)")
+    pk = "measured (MEASURED_PEAKS.json" if src == "measured" else "fallback ("
+    if flops / (bf16 * 1e12) >= byts / (hbm * 1e9):
+        ach = flops / avg_s / 1e12
+        traffic = profile_traffic("lmhead_select_fused_c4_w1024.md")
+        return {"kernel": kernel, "bound": "tensor", "achieved": round(ach, 1), "peak": bf16, "unit": "TFLOP/s",
+                "frac": round(ach / bf16, 4), "frac_of_sustained": round(ach / bf16_sus, 4),
+                "peak_source": f"{pk} bf16_tflops, burst)", "traffic": traffic, "algorithmic_flops": flops,
+                "algorithmic_bytes": byts, "avg_launch_us": round(avg_s * 1e6, 2), "launch_timing": lm_timing}
+    ach = byts / avg_s / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(ach / hbm, 4), "peak_source": f"{pk} hbm_gbs)",
+            "traffic": profile_traffic("lmhead_select_fused_decoder2.md"), "algorithmic_bytes": byts,
+            "avg_launch_us": round(avg_s * 1e6, 2), "launch_timing": lm_timing}
+
+
+def run_ours(args):
+    import torch.distributed as dist
+    from invariant_verify_gb300 import synth
+    import __graft_entry__
+    rank, world, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    hbm, bf16, bf16_sus, src = peaks()
+    K_steps = args.steps
+
+    # ---- the headline: the Llama-3-8B-shaped window N = 64 x K = 16
+    cfg = synth.SWEEP
+    N, K = 64, 16
+    W = N * K
+    pb = build_problem(cfg, N, K, device, rank=rank)
+    ver, win, ctx = pb["ver"], pb["win"], pb["ctx"]
+    t = time_steps(ver, win, K_steps, args.warmup, world, device, rank, local)
+    ms_per_step = t["tot_ms"] / K_steps
+    value = W * world * K_steps / (t["tot_ms"] / 1e3)
+    committed = int(ver.accept_len.sum().item())
+    roofline = lm_roofline(cfg, W, t["lm_ms"], t["lm_timing"], hbm, bf16, bf16_sus, src)
+    step_bytes, step_flops = step_work(cfg, W, K, ctx)
+    step_roof_us = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12)) * 1e6
+    times = kernel_breakdown(ver, win)
+    kernels = breakdown_lines(cfg, W, K, ctx, times, hbm, bf16) if times else None
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(ver, win, cfg, N, K, max(20, min(K_steps, 200)), world)
+    out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K_steps,
+           "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": workload_config(cfg, N, K) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+           "roofline": roofline,
+           "step_roofline": {"bytes": step_bytes, "flops": step_flops, "lower_bound_us": round(step_roof_us, 2),
+                             "frac": round(step_roof_us / (ms_per_step * 1e3), 4),
+                             "how": "max(bytes / hbm_gbs, flops / bf16_tflops burst), both measured peaks"},
+           "kernels": kernels,
+           "committed_tok_per_s": round(committed * world * K_steps / (t["tot_ms"] / 1e3), 1),
+           "gpu_launches": ver.launches_per_step * K_steps,
+           "timed_region_wall_s": round(t["wall"], 3),
+           "clocks": t["clocks"], "e2e": e2e}
+    cpu_src = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_src = {k: v.cpu() for k, v in pb["w"].items()}
+    del t, ver
+    torch.cuda.empty_cache()
+
+    # ---- the 2-layer decoder window (W = 64), kept as an extra figure
+    if not args.no_decoder2:
+        c2 = synth.DECODER2
+        p2 = build_problem(c2, c2.N, c2.K, device, rank=rank)
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        k2 = max(50, min(4 * K_steps, 2000))
+        t2 = time_steps(p2["ver"], p2["win"], k2, args.warmup, world, device, rank, local, flush=flush)
+        ms2 = t2["tot_ms"] / k2
+        b2, f2 = step_work(c2, c2.W, c2.K, p2["ctx"])
+        lb2 = max(b2 / (hbm * 1e9), f2 / (bf16 * 1e12)) * 1e6
+        out["decoder2_w64"] = {
+            "value": round(c2.W * world * k2 / (t2["tot_ms"] / 1e3), 1), "unit": UNIT, "steps": k2,
+            "ms_per_step": round(ms2, 5), "config": workload_config(c2, c2.N, c2.K),
+            "roofline": lm_roofline(c2, c2.W, t2["lm_ms"], t2["lm_timing"], hbm, bf16, bf16_sus, src),
+            "step_roofline": {"bytes": b2, "flops": f2, "lower_bound_us": round(lb2, 2),
+                              "frac": round(lb2 / (ms2 * 1e3), 4)},
+            "gpu_launches_per_step": p2["ver"].launches_per_step, "clocks": t2["clocks"]}
+        del p2, t2, flush
+        torch.cuda.empty_cache()
+
+    if rank == 0:
+        if cpu_src is not None:
+            out["cpu_baseline"] = cpu_baseline(cfg, cpu_src, pb, args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------- CPU oracle timing
+def oracle_request_rows(cfg, w_cpu, cache_rows, max_len, tokens, ctx_r, req_r, K):
+    """One request's K window rows verified by the oracle (fp64 forward
+    writing the rows' own K/V, then the fp32-exact selection); returns the
+    selected tokens.  ``cache_rows``: that request's (K, V) per layer, slot 0."""
+    import oracle
+    from oracle.model import OracleDecoder
+    orc = OracleDecoder(cfg, w_cpu, cache_rows, 1, max_len)
+    slot = np.zeros(K, np.int32)
+    pos = (int(ctx_r) + np.arange(K)).astype(np.int32)
+    out = orc.forward(np.asarray(tokens, np.int64), slot, pos)
+    req = np.full(K, int(req_r), np.int64)
+    return oracle.gumbel_argmax(out["logits"].astype(np.float32), req, pos, SEED, cfg.temperature)
+
+
+def oracle_rows_per_second(cfg, w_cpu, caches, max_len, tokens, ctx, req, K, seconds=None, max_steps=None,
+                           warmup=0):
+    """Rows per second of the oracle verifying whole requests (K rows each),
+    request after request, for ``seconds`` or ``max_steps`` requests."""
+    import oracle
+    N = len(ctx)
+    done_rows, spent, i = 0, 0.0, 0
+    while True:
+        r = i % N
+        rows = [(kc[r:r + 1].cpu(), vc[r:r + 1].cpu()) for kc, vc in caches]
+        t0 = time.perf_counter()
+        oracle_request_rows(cfg, w_cpu, rows, max_len, tokens[r], ctx[r], req[r], K)
+        dt = time.perf_counter() - t0
+        i += 1
+        if i <= warmup:
+            continue
+        done_rows += K
+        spent += dt
+        n_req = done_rows // K
+        if (max_steps is not None and n_req >= max_steps) or (max_steps is None and spent >= seconds):
+            break
+    return done_rows / spent, done_rows, spent, oracle.num_threads()
+
+
+def cpu_baseline(cfg, w_cpu, pb, seconds):
+    K = pb["K"]
+    v, n, spent, cores = oracle_rows_per_second(cfg, w_cpu, pb["caches"], pb["max_len"], pb["tokens"], pb["ctx"],
+                                                pb["req"], K, seconds=seconds)
+    return {"value": round(v, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n // K} whole requests of the window ({n} rows: the layer, LM head and selection in "
+                      f"fp64 / exact fp32) in {spent:.1f} s on {cores} host threads"}
+
+
+# --------------------------------------------------------- reference arm
+def run_reference(args):
+    """The oracle as it stands on the headline workload, on the host cores:
+    each step verifies one request's K window rows.  The inputs are the same
+    seeded recipe drawn on the CPU (no GPU is touched), and the drafts are
+    the recipe's (they do not change the work of a step)."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    from invariant_verify_gb300 import replicas, synth
+    from oracle import build as ob
+    ob.build()
+    cfg = synth.SWEEP
+    N, K = 64, 16
+    plan = replicas.rank_window_plan(cfg, N, K, 0)
+    ctx = plan["ctx"]
+    steps = max(1, args.steps)
+    warm = max(0, min(args.warmup, 3))
+    n_req = min(N, steps + warm)
+    # a requests' worth of inputs on the CPU: weights (seeded), the sampled
+    # requests' caches, tokens
+    w = synth.decoder_weights(cfg)
+    max_len = int(ctx[:n_req].max()) + K + 16
+    caches = synth.kv_cache(n_req, cfg.Hkv, max_len, cfg.hd, ctx[:n_req], seed=plan["kv_seed"], layers=cfg.layers)
+    tokens = torch.cat([plan["last"][:, None], plan["draft_ids"][:, :-1]], dim=1)
+    v, n, spent, cores = oracle_rows_per_second(cfg, w, caches, max_len, tokens[:n_req], ctx[:n_req],
+                                                plan["req_ids"][:n_req], K, max_steps=steps, warmup=warm)
+    out = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": world,
+           "steps": n // K, "warmup": args.warmup, "ms_per_step": round(spent / (n // K) * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": workload_config(cfg, N, K) | {"parallelism": "host cores"},
+           "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": f"each step verifies one request's {K} window rows (the layer, LM head and "
+                                      f"selection in fp64 / exact fp32)"},
+           "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
 
 
 # ---------------------------------------------------------- kernel sweep
@@ -393,18 +633,38 @@ def _time_us(fn, reps=20, warm=3):
     return statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(reps)) * 1e3
 
 
+def attention_case(N, K, seed=123):
+    """Attention inputs of the verifier sweep's recipe: N requests x K rows,
+    Llama-3-8B heads, lognormal contexts."""
+    from invariant_verify_gb300 import abi as B
+    from invariant_verify_gb300 import synth
+    sw = synth.SWEEP
+    W = N * K
+    ctx = synth.context_lengths(sw, N, seed=seed)
+    max_len = int(ctx.max()) + K + 8
+    kc, vc = synth.kv_cache_device(N, sw.Hkv, max_len, sw.hd, ctx, seed=seed + 1, layers=1)[0]
+    q = synth.bf16_normal_device((W, sw.Hq, sw.hd), 1.0, seed + 2)
+    o = torch.empty_like(q)
+    slot = torch.arange(N, dtype=torch.int32, device="cuda").repeat_interleave(K)
+    rpos = (ctx.cuda().repeat_interleave(K) + torch.arange(K, device="cuda").repeat(N)).to(torch.int32)
+    ws = torch.empty(B.biv_decode_attn_workspace_size(W, sw.Hq, max_len), dtype=torch.uint8, device="cuda")
+    kv_bytes = sum(2 * 2 * sw.Hkv * (int(c) + K) * sw.hd for c in ctx)
+    return dict(q=q, kc=kc, vc=vc, slot=slot, rpos=rpos, o=o, ws=ws, K=K, ctx=ctx,
+                bytes=kv_bytes + 2 * 2 * W * sw.Hq * sw.hd)
+
+
 def run_kernel_sweep(args):
     """Achieved HBM bandwidth of the bandwidth-bound kernels at sizes far above
     L2 (inputs > 129 MB, so no flush is needed between launches): RMSNorm over
     [32768, 4096] bf16, the selection workload (fp32 [4096, 152064], T = 0.7),
-    and the fixed-split attention of the verifier sweep's largest window
-    (64 requests x 16 rows, Llama-3-8B heads, lognormal contexts)."""
+    and the fixed-split attention of the verifier sweep's windows (Llama-3-8B
+    heads, lognormal contexts)."""
     from invariant_verify_gb300 import abi as B
     from invariant_verify_gb300 import synth
     import __graft_entry__
     __graft_entry__.build()
     torch.cuda.set_device(0)
-    hbm, _, src = peaks()
+    hbm, _, _, src = peaks()
     out = []
 
     def line(kernel, workload, nbytes, us):
@@ -433,22 +693,13 @@ def run_kernel_sweep(args):
          4 * R * cfg.vocab + 12 * R, _time_us(lambda: B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.0, tok)))
     del logits
 
-    sw = synth.SWEEP
-    N, K = 64, 16
-    W = N * K
-    ctx = synth.context_lengths(sw, N, seed=123)
-    max_len = int(ctx.max()) + K + 8
-    kc, vc = synth.kv_cache_device(N, sw.Hkv, max_len, sw.hd, ctx, seed=124, layers=1)[0]
-    q = synth.bf16_normal_device((W, sw.Hq, sw.hd), 1.0, 125)
-    o = torch.empty_like(q)
-    slot = torch.arange(N, dtype=torch.int32, device="cuda").repeat_interleave(K)
-    rpos = (ctx.cuda().repeat_interleave(K) + torch.arange(K, device="cuda").repeat(N)).to(torch.int32)
-    ws = torch.empty(B.biv_decode_attn_workspace_size(W, sw.Hq, max_len), dtype=torch.uint8, device="cuda")
-    kv_bytes = sum(2 * 2 * sw.Hkv * (int(c) + K) * sw.hd for c in ctx)
-    line("attn_tc_kernel + attn_combine_kernel",
-         f"attention W={W} (64 x 16), Hq 32 / Hkv 8, lognormal ctx mean {float(ctx.float().mean()):.0f}",
-         kv_bytes + 2 * 2 * W * sw.Hq * sw.hd,
-         _time_us(lambda: B.biv_decode_attn_fixedsplit(q, kc, vc, slot, rpos, o, K, ws)))
+    for N, K in ((64, 16), (32, 8), (8, 4)):
+        a = attention_case(N, K)
+        line("attn_tc_kernel + attn_combine_kernel",
+             f"attention W={N * K} ({N} x {K}), Hq 32 / Hkv 8, lognormal ctx mean {float(a['ctx'].float().mean()):.0f}",
+             a["bytes"], _time_us(lambda: B.biv_decode_attn_fixedsplit(a["q"], a["kc"], a["vc"], a["slot"], a["rpos"],
+                                                                       a["o"], a["K"], a["ws"])))
+        del a
     return out
 
 
@@ -462,7 +713,7 @@ def run_gemm_sweep(args):
     import __graft_entry__
     __graft_entry__.build()
     torch.cuda.set_device(0)
-    hbm, bf16, _ = peaks()
+    hbm, bf16, _, _ = peaks()
     shapes = {"qkv": (6144, 4096), "wo": (4096, 4096), "gate_up": (28672, 4096), "down": (4096, 14336),
               "lm_head": (128256, 4096)}
     Ms = [1, 8, 32, 64, 128, 256, 512, 1024]
@@ -512,75 +763,6 @@ def run_gemm_sweep(args):
     return rows
 
 
-# ------------------------------------------------------- CPU oracle timing
-def oracle_rows_per_second(cfg, w_cpu, caches_cpu, max_len, win, seconds, max_steps=None, warmup=0):
-    import oracle
-    from oracle.model import OracleDecoder
-    orc = OracleDecoder(cfg, w_cpu, caches_cpu, cfg.N, max_len)
-    tokens = win.tokens.cpu().numpy()
-    slot = win.row_slot.cpu().numpy()
-    req = win.row_req.cpu().numpy()
-    pos = win.row_pos.cpu().numpy()
-    # The window's own K/V rows must be in the cache before single rows are
-    # verified: one full oracle forward writes them (not timed).
-    orc.forward(tokens, slot, pos)
-    W = tokens.size
-    done, spent, i = 0, 0.0, 0
-    while True:
-        r = i % W
-        t0 = time.perf_counter()
-        out = orc.forward(tokens[r:r + 1], slot[r:r + 1], pos[r:r + 1])
-        oracle.gumbel_argmax(out["logits"].astype(np.float32), req[r:r + 1], pos[r:r + 1], 0x1234_5678_9ABC_DEF0,
-                             cfg.temperature)
-        dt = time.perf_counter() - t0
-        i += 1
-        if i <= warmup:
-            continue
-        done += 1
-        spent += dt
-        if (max_steps is not None and done >= max_steps) or (max_steps is None and spent >= seconds):
-            break
-    import oracle as _o
-    return done / spent, done, spent, _o.num_threads()
-
-
-def cpu_baseline(cfg, w_cpu, caches_cpu, max_len, win, seconds):
-    v, n, spent, cores = oracle_rows_per_second(cfg, w_cpu, caches_cpu, max_len, win, seconds)
-    return {"value": round(v, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n} window rows verified one at a time (all layers + LM head + selection, fp64) "
-                      f"in {spent:.1f} s on {cores} host threads"}
-
-
-# --------------------------------------------------------- reference arm
-def run_reference(args):
-    rank, world, _ = dist_info()
-    if rank != 0:
-        return
-    from invariant_verify_gb300 import replicas, synth
-    from invariant_verify_gb300.verifier import make_window
-    from oracle import build as ob
-    ob.build()
-    cfg = synth.DECODER2
-    w = synth.decoder_weights(cfg)
-    ctx = synth.context_lengths(cfg, cfg.N, seed=cfg.seed + 100)
-    max_len = int(ctx.max()) + 64
-    caches = synth.kv_cache(cfg.N, cfg.Hkv, max_len, cfg.hd, ctx, seed=cfg.seed + 200, layers=cfg.layers)
-    g = synth.generator(cfg.seed + 300)
-    toks = torch.randint(0, cfg.vocab, (cfg.W,), generator=g, dtype=torch.int64).to(torch.int32)
-    win = make_window(cfg.N, cfg.K, toks, ctx, replicas.request_ids(range(cfg.N)), toks, device="cpu")
-    steps = max(1, args.steps)
-    v, n, spent, cores = oracle_rows_per_second(cfg, w, caches, max_len, win, 0.0, max_steps=steps,
-                                                warmup=max(0, min(args.warmup, 3)))
-    out = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": world,
-           "steps": n, "warmup": args.warmup, "ms_per_step": round(spent / n * 1e3, 3), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": workload_config(cfg) | {"parallelism": "host cores"},
-           "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-                            "sample": "one window row per step (all layers + LM head + selection, fp64)"},
-           "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(out), flush=True)
-
-
 def run_c4_steps(args):
     """Whole verify steps (embed + RMSNorm, one Llama-3-8B-shaped layer, LM
     head over 128256 tokens with the fused selection, winners + accept) at the
@@ -588,22 +770,17 @@ def run_c4_steps(args):
     replay; the weights (1.49 GB) and KV caches exceed L2, so no flush is
     needed.  Device-timed with events around each replay."""
     from invariant_verify_gb300 import synth
-    from invariant_verify_gb300.verifier import DecoderVerifier, make_window
     import __graft_entry__
     __graft_entry__.build()
     torch.cuda.set_device(0)
-    hbm, bf16, src = peaks()
+    device = torch.device("cuda", 0)
+    hbm, bf16, _, src = peaks()
     cfg = synth.SWEEP
     w = synth.decoder_weights_device(cfg)
     for N, K in ((8, 4), (32, 8), (64, 16)):
         W = N * K
-        ctx = synth.context_lengths(cfg, N, seed=40 + N)
-        max_len = int(ctx.max()) + K + 16
-        caches = synth.kv_cache_device(N, cfg.Hkv, max_len, cfg.hd, ctx, seed=41 + N, layers=cfg.layers)
-        ver = DecoderVerifier(cfg, w, caches, N, max_len, W, K, keep_logits=False)
-        req = torch.arange(N, dtype=torch.int32) * 31 + 1
-        toks = torch.randint(0, cfg.vocab, (W,), generator=synth.generator(43), dtype=torch.int64).to(torch.int32)
-        win = make_window(N, K, toks, ctx, req, toks)
+        pb = build_problem(cfg, N, K, device, weights=w)
+        ver, win, ctx = pb["ver"], pb["win"], pb["ctx"]
         g = ver.capture(win)
         for _ in range(3):
             g.replay()
@@ -616,45 +793,36 @@ def run_c4_steps(args):
             b.record()
         torch.cuda.synchronize()
         us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
-        kv = sum(2 * 2 * cfg.Hkv * (int(c) + K) * cfg.hd for c in ctx)
-        wbytes = sum(t.numel() * t.element_size() for k, t in w.items() if k != "embed")
-        flops = 2 * W * (wbytes // 2) + 4 * cfg.Hq * cfg.hd * sum(int(c) + K for c in ctx) * K
-        lb = max((wbytes + kv) / (hbm * 1e9), flops / (bf16 * 1e12)) * 1e6
+        byts, flops = step_work(cfg, W, K, ctx)
+        lb = max(byts / (hbm * 1e9), flops / (bf16 * 1e12)) * 1e6
+        times = kernel_breakdown(ver, win)
         print(json.dumps({"workload": f"C4 verify step N={N} K={K} W={W}, Llama-3-8B-shaped layer + LM head "
                                       f"(vocab {cfg.vocab}), lognormal ctx mean {float(ctx.float().mean()):.0f}",
                           "us_per_step": round(us, 1), "verified_tok_per_s": round(W / us * 1e6, 1),
                           "lower_bound_us": round(lb, 1), "frac_of_roofline": round(lb / us, 4),
-                          "gpu_launches_per_step": ver.launches_per_step, "peak_source": src}), flush=True)
-        del ver, caches, g
+                          "gpu_launches_per_step": ver.launches_per_step, "peak_source": src,
+                          "kernels": breakdown_lines(cfg, W, K, ctx, times, hbm, bf16) if times else None}),
+              flush=True)
+        del ver, pb, g
         torch.cuda.empty_cache()
 
 
 def run_profile_case(args):
     """A small case of one kernel, launched twice (the second launch is the
-    one to capture): inputs above L2 size, a few hundred MB on the device."""
+    one to capture): inputs above L2 size, a few GB on the device at most."""
     import dataclasses
     from invariant_verify_gb300 import abi as B
     from invariant_verify_gb300 import synth
     import __graft_entry__
     __graft_entry__.build()
     torch.cuda.set_device(0)
-    if args.profile_case == "attn16":
-        sw = synth.SWEEP
-        N, K = 16, 16
-        W = N * K
-        ctx = synth.context_lengths(sw, N, seed=123)
-        max_len = int(ctx.max()) + K + 8
-        kc, vc = synth.kv_cache_device(N, sw.Hkv, max_len, sw.hd, ctx, seed=124, layers=1)[0]
-        q = synth.bf16_normal_device((W, sw.Hq, sw.hd), 1.0, 125)
-        o = torch.empty_like(q)
-        slot = torch.arange(N, dtype=torch.int32, device="cuda").repeat_interleave(K)
-        rpos = (ctx.cuda().repeat_interleave(K) + torch.arange(K, device="cuda").repeat(N)).to(torch.int32)
-        ws = torch.empty(B.biv_decode_attn_workspace_size(W, sw.Hq, max_len), dtype=torch.uint8, device="cuda")
+    case = args.profile_case
+    if case == "attn16":
+        a = attention_case(16, 16)
         for _ in range(2):
-            B.biv_decode_attn_fixedsplit(q, kc, vc, slot, rpos, o, K, ws)
-        kv = sum(2 * 2 * sw.Hkv * (int(c) + K) * sw.hd for c in ctx)
-        print(json.dumps({"case": "attn16", "kv_bytes": kv, "ctx_mean": float(ctx.float().mean())}))
-    else:
+            B.biv_decode_attn_fixedsplit(a["q"], a["kc"], a["vc"], a["slot"], a["rpos"], a["o"], a["K"], a["ws"])
+        print(json.dumps({"case": case, "bytes": a["bytes"], "ctx_mean": float(a["ctx"].float().mean())}))
+    elif case == "select1024":
         cfg = dataclasses.replace(synth.SELECT, requests=128)
         logits = synth.select_logits_device(cfg)
         R = cfg.R
@@ -663,7 +831,36 @@ def run_profile_case(args):
         tok = torch.empty(R, dtype=torch.int32, device="cuda")
         for T in (0.7, 0.0):
             B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, T, tok)
-        print(json.dumps({"case": "select1024", "rows": R, "vocab": cfg.vocab}))
+        print(json.dumps({"case": case, "rows": R, "vocab": cfg.vocab}))
+    elif case == "rmsnorm":
+        rows, d = 16384, 4096                     # 128 MiB in, 128 MiB out
+        x = synth.bf16_normal_device((rows, d), 1.0, 7)
+        w = torch.ones(d, dtype=torch.bfloat16, device="cuda")
+        y = torch.empty_like(x)
+        for _ in range(2):
+            B.biv_rmsnorm(x, w, y, 1e-6)
+        print(json.dumps({"case": case, "rows": rows, "d": d, "bytes": 4 * rows * d + 2 * d}))
+    elif case == "lmhead1024":
+        cfg = synth.SWEEP
+        M, N, Kd = 1024, cfg.vocab, cfg.d
+        A = synth.bf16_normal_device((M, Kd), 1.0, 11)
+        Wl = synth.bf16_normal_device((N, Kd), 0.02, 12)
+        req = torch.arange(M, dtype=torch.int32, device="cuda") // 16 * 31 + 1
+        pos = torch.arange(M, dtype=torch.int32, device="cuda") % 16 + 1000
+        tok = torch.empty(M, dtype=torch.int32, device="cuda")
+        ws = torch.empty(B.biv_lm_head_gumbel_workspace_size(M, N, Kd), dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            B.biv_lm_head_gumbel(A, Wl, req, pos, SEED, 0.7, tok, ws)
+        print(json.dumps({"case": case, "M": M, "N": N, "K": Kd, "flops": 2 * M * N * Kd,
+                          "bytes": 2 * N * Kd + 2 * M * Kd + 12 * M}))
+    else:   # gemm1024: the gate/up-shaped plain GEMM at M = 1024
+        M, N, Kd = 1024, 28672, 4096
+        A = synth.bf16_normal_device((M, Kd), 1.0, 13)
+        Wl = synth.bf16_normal_device((N, Kd), 0.02, 14)
+        C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        for _ in range(2):
+            B.biv_gemm_nosplitk(A, Wl, C)
+        print(json.dumps({"case": case, "M": M, "N": N, "K": Kd, "flops": 2 * M * N * Kd}))
     torch.cuda.synchronize()
 
 

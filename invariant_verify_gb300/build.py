@@ -40,7 +40,9 @@ def _stale(obj: str, deps: list) -> bool:
 
 def _compile(src: str, verbose_ptxas: bool) -> str:
     obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    deps = [os.path.join(CSRC, src), os.path.join(CSRC, "biv_common.cuh"), os.path.join(INCLUDE, "biv.h")]
+    # every header of the library: an object is rebuilt when any of them changes
+    headers = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
+    deps = [os.path.join(CSRC, src), *headers, os.path.join(INCLUDE, "biv.h")]
     if _stale(obj, deps) or verbose_ptxas:
         cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose_ptxas:

@@ -53,6 +53,27 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
     return cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...));
 }
 
+// The same for a kernel launched in clusters of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+int launch_cluster_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       int cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...));
+}
+
 // Each translation unit owns one device error word and registers a reader.
 typedef cudaError_t (*err_reader_fn)(uint32_t* bits, bool clear);
 void register_err_reader(err_reader_fn fn);
@@ -141,6 +162,8 @@ BIV_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+BIV_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity);
+
 // Wait for the phase of `bar` with the given parity to complete, for at most
 // about kWaitLimitNs.  The first kFastPolls polls touch nothing but the
 // barrier (reading the global timer is slow); only a wait that outlasts them
@@ -152,15 +175,22 @@ constexpr int kFastPolls = 4096;
 // spin = true polls with test_wait (no suspension: the single producer / MMA
 // threads of a pipeline react at once); spin = false uses try_wait, which may
 // park the thread until the phase completes (for warps that wait long).
+// cluster = true: try_wait with acquire at cluster scope, for a barrier that
+// threads of another CTA of the cluster arrive on.
+BIV_DEV bool mbar_poll(uint64_t* bar, uint32_t parity, bool spin, bool cluster) {
+    return cluster ? mbar_try_wait_cluster(bar, parity)
+                   : (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity));
+}
+
 BIV_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned int* err,
-                       bool spin = false) {
+                       bool spin = false, bool cluster = false) {
 #pragma unroll 1
     for (int i = 0; i < kFastPolls; ++i)
-        if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (mbar_poll(bar, parity, spin, cluster)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         for (int i = 0; i < 256; ++i)
-            if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+            if (mbar_poll(bar, parity, spin, cluster)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -216,6 +246,60 @@ BIV_DEV uint64_t policy_evict_last() {
     return p;
 }
 
+// ------------------------------------------------------------ clusters
+// Rank of this CTA in its cluster.
+BIV_DEV uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Execution and memory barrier over every thread of every CTA of the cluster
+// (the non-aligned form: the threads of a warp may arrive apart).
+BIV_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The shared::cluster address of `p` (a shared variable of this CTA) in the
+// shared memory of the cluster's CTA `rank` (the same variable there).
+BIV_DEV uint32_t mapa_shared(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Arrive once on an mbarrier of any CTA of the cluster (shared::cluster
+// address), releasing this thread's prior writes at cluster scope.
+BIV_DEV void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+}
+
+// Phase probe with acquire at cluster scope (for barriers other CTAs of the
+// cluster arrive on).
+BIV_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// 3-D tiled TMA load into this CTA's shared memory whose completion is
+// counted on an mbarrier of either CTA of the pair (shared::cluster address):
+// the loads of both CTAs of a pair feed the even CTA's barrier.
+BIV_DEV void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster_addr, int c0, int c1,
+                              int c2, uint64_t cache_policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr), "l"(cache_policy)
+        : "memory");
+}
+
 // ------------------------------------------------------------- tcgen05
 BIV_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -231,6 +315,23 @@ BIV_DEV void tmem_relinquish() {
 BIV_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
+}
+
+// The same for a CTA pair (cta_group::2): one warp of each CTA of the pair
+// executes these together; the columns are allocated at the same address in
+// both CTAs' tensor memory.
+BIV_DEV void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+BIV_DEV void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+BIV_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 BIV_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -258,6 +359,33 @@ BIV_DEV void umma_bf16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, 
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D (+)= A * B^T across a CTA pair (cta_group::2, M = 256): rows 0..127 of A
+// come from the even CTA's shared memory and rows 128..255 from the odd
+// CTA's, at the same address; likewise the first and second halves of B's N
+// rows.  Each CTA's tensor memory receives its own 128 rows of D.  Issued by
+// one elected lane of the even CTA.
+BIV_DEV void umma_bf16_pair_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                  uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on an mbarrier of either CTA of the pair (shared::cluster
+// address) when the pair MMAs issued so far by this thread complete.
+BIV_DEV void umma_commit_pair_elect(uint32_t bar_cluster_addr) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+            bar_cluster_addr)
         : "memory");
 }
 

@@ -32,6 +32,7 @@
 // in-flight copies and MMAs, frees TMEM and returns.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "biv_common.cuh"
 #include "biv_gumbel.cuh"
@@ -49,6 +50,7 @@ constexpr int kTailSlack = kBM * kRowBytes;   // the MMA may read 128 A rows pas
 constexpr int kMaxStages = 24;
 constexpr int kBarBytes = 512;
 constexpr int kWave = 152;                    // CTAs of one wave on a 152-SM part
+constexpr int kPairWave = kWave / 2;          // 2-CTA clusters of one wave
 constexpr int kMaxSmem = 227 * 1024;          // opt-in shared memory per block
 
 struct GemmArgs {
@@ -333,10 +335,30 @@ BIV_DEV void seg_load<16>(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16x2_sync(
 // largest logit.  TMEM loads are warp-wide: a chunk is reloaded when any lane
 // of the warp needs it.  `bkrow` is the row's buckets, `cm` the thread's
 // chunk maxima (shared memory).
-template <int SEGW>
+// Bounds of the 32 entries of one chunk (columns col0 .. col0 + 31, col0 a
+// multiple of 32) from Philox words drawn here: the same buckets as
+// tile_buckets stores, without the shared-memory copy (for tiles whose
+// epilogue runs under the next tile's MMAs anyway).
+BIV_DEV void fly_bounds(const uint32_t (&r)[32], uint32_t col0, uint32_t pos, uint32_t req, const SelectArgs& sel,
+                        const float* ntab, float (&bound)[32]) {
+    constexpr int sh = 32 - kBucketBits;
+#pragma unroll
+    for (int g4 = 0; g4 < 8; ++g4) {
+        const U4 w = philox4x32_10((col0 >> 2) + static_cast<uint32_t>(g4), pos, req, 0u, sel.seed_lo, sel.seed_hi);
+        bound[4 * g4 + 0] = __fadd_rn(__fmul_rn(__uint_as_float(r[4 * g4 + 0]), sel.invT), ntab[w.x >> sh]);
+        bound[4 * g4 + 1] = __fadd_rn(__fmul_rn(__uint_as_float(r[4 * g4 + 1]), sel.invT), ntab[w.y >> sh]);
+        bound[4 * g4 + 2] = __fadd_rn(__fmul_rn(__uint_as_float(r[4 * g4 + 2]), sel.invT), ntab[w.z >> sh]);
+        bound[4 * g4 + 3] = __fadd_rn(__fmul_rn(__uint_as_float(r[4 * g4 + 3]), sel.invT), ntab[w.w >> sh]);
+    }
+}
+
+// FLY: the bucket words are drawn per chunk (fly_bounds) instead of read
+// from the tile's bucket table `bkrow` (SEGW = 32 only).
+template <int SEGW, bool FLY = false>
 BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int cb, int ce, int n0, int N, bool live, uint32_t req,
                                            uint32_t pos, const SelectArgs& sel, const float* ntab,
                                            const unsigned long long* bkrow, int RC, float* cm, float* logits_row) {
+    static_assert(!FLY || SEGW == 32, "per-chunk bucket words need whole 32-column chunks per thread");
     const int hoff = SEGW == 16 ? static_cast<int>(threadIdx.x & 16) : 0;
     float bx = -INFINITY;       // largest logit (T = 0) or largest bound (T > 0)
     float bxv = 0.0f;           // the logit of that entry
@@ -353,6 +375,8 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int cb, int ce, int n
         if (sel.greedy) {
 #pragma unroll
             for (int e = 0; e < SEGW; ++e) val[e] = __uint_as_float(r[e]);
+        } else if constexpr (FLY) {
+            fly_bounds(r, static_cast<uint32_t>(col0), pos, req, sel, ntab, val);
         } else {
             seg_bounds<SEGW>(r, bkrow + ((c + hoff) / 4) * RC, RC, ntab, sel.invT, val);
         }
@@ -415,7 +439,10 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int cb, int ce, int n
             seg_load<SEGW>(taddr + static_cast<uint32_t>(c), r);
             if (!need) continue;
             float bound[SEGW];
-            seg_bounds<SEGW>(r, bkrow + ((c + hoff) / 4) * RC, RC, ntab, sel.invT, bound);
+            if constexpr (FLY)
+                fly_bounds(r, static_cast<uint32_t>(col0), pos, req, sel, ntab, bound);
+            else
+                seg_bounds<SEGW>(r, bkrow + ((c + hoff) / 4) * RC, RC, ntab, sel.invT, bound);
             const int lim = N - col0;
             uint32_t hit = 0;
 #pragma unroll
@@ -449,7 +476,16 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int cb, int ce, int n
 // activation [M, N/2]; see biv_gemm_swiglu), 3 = Gumbel-max selection of each
 // tile-row (optional fp32 C; see biv_lm_head_gumbel), 4 = RoPE of q and k, k
 // and v into the KV cache (see biv_gemm_qkv_rope).
-template <int EPI>
+// CG = 1: one CTA per tile of 128 rows.  CG = 2: a cluster of two CTAs per
+// tile of 256 rows (cta_group::2 MMAs of M = 256): each CTA copies its own
+// 128 rows of A and its half of the tile's BN rows of B into its own shared
+// memory, both CTAs' copies complete on the even CTA's stage barrier, the
+// even CTA's MMA thread issues the pair MMAs (the tensor core reads the B
+// halves of both CTAs, so every weight byte enters one SM's shared memory
+// once per pair) and each CTA's epilogue drains its own 128 rows from its own
+// tensor memory.  Per output element the MMAs, their k order and the single
+// fp32 accumulator are those of CG = 1.
+template <int EPI, int CG>
 __global__ void __launch_bounds__(64 + epi_threads<EPI>(), 1)
 gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
@@ -458,7 +494,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const int A_BYTES = g.KS * g.a_rows * kRowBytes;     // A region of a stage
-    const int STAGE = A_BYTES + g.KS * g.BN * kRowBytes;
+    const int STAGE = A_BYTES + g.KS * (g.BN / CG) * kRowBytes;
     const int S = g.stages;
     uint8_t* tiles = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE + (g.a_rows < kBM ? kTailSlack : 0));
@@ -474,11 +510,18 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     unsigned long long* s_best = reinterpret_cast<unsigned long long*>(cmax + 2 * kBM * kMaxChunks);  // [128]
     unsigned long long* bk = s_best + kBM;                                                   // EPI 3 only
     constexpr int NT = epi_threads<EPI>();
+    constexpr int TM = kBM * CG;                  // rows of one output tile
+    // CG = 2: the pair's rank (0 = the even CTA, which owns the stage and
+    // accumulator-empty barriers and issues the MMAs) and its tiles.
+    const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int unit = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int n_units = CG == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int M = g.M, N = g.N, BN = g.BN;
-    const int m_tiles = (M + kBM - 1) / kBM;
+    const int BNL = BN / CG;                      // B rows this CTA copies per tile
+    const int m_tiles = (M + TM - 1) / TM;
     const int n_tiles = (N + BN - 1) / BN;
     const int n_work = m_tiles * n_tiles;
     const int KB = g.KB;
@@ -494,7 +537,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], NT);
+            mbar_init(&tempty[a], CG == 2 ? 2 : NT);   // CG = 2: one arrival per CTA's epilogue
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -509,11 +552,19 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         }
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, g.tmem_cols);
-        tmem_relinquish();
+        if constexpr (CG == 2) {
+            tmem_alloc_pair(tmem_slot, g.tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, g.tmem_cols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync();       // both CTAs' barriers are initialised before either signals the other's
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t pol_a = policy_evict_last();    // activations: reused by every CTA
@@ -523,14 +574,19 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     // boxes, the previous kernel's output, after).  Each such stage's barrier
     // expects both from the start.
     int b_early = 0;
-    if (warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < n_work) {
-        const int n_blk0 = static_cast<int>(blockIdx.x) / m_tiles;
+    if (warp == 0 && lane == 0 && unit < n_work) {
+        const int n_blk0 = unit / m_tiles;
         b_early = min(S, n_stage_blocks);
         for (int sb = 0; sb < b_early; ++sb) {
             uint8_t* sa = tiles + sb * STAGE;
             int kb0, nkb;
             stage_range(g, sb, kb0, nkb);
-            if (g.first1 && sb == 0) {
+            if constexpr (CG == 2) {
+                // the even CTA expects both CTAs' bytes of the stage
+                if (rank == 0) mbar_arrive_expect_tx(&full[sb], 2 * tx_bytes);
+                tma_load_3d_pair(sa + A_BYTES, &tmB, mapa_shared(&full[sb], 0), 0, n_blk0 * BN + rank * BNL, kb0,
+                                 pol_b);
+            } else if (g.first1 && sb == 0) {
                 mbar_arrive_expect_tx(&full[sb], tx_bytes1);
                 tma_load_3d(sa + A_BYTES, &tmB1, &full[sb], 0, n_blk0 * BN, 0, pol_b);
             } else if (g.three_d) {
@@ -552,19 +608,24 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < n_work && ok; t += gridDim.x) {
+            for (int t = unit; t < n_work && ok; t += n_units) {
                 const int n_blk = t / m_tiles;
                 const int m_blk = t - n_blk * m_tiles;
                 for (int sb = 0; sb < n_stage_blocks; ++sb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_gemm_err, true)) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_gemm_err, true, CG == 2)) {
                         ok = false;
                         break;
                     }
                     uint8_t* sa = tiles + stage * STAGE;
                     int kb0, nkb;
                     stage_range(g, sb, kb0, nkb);
-                    const bool b_done = t == static_cast<int>(blockIdx.x) && sb < b_early;   // B requested early
-                    if (g.first1 && sb == 0) {
+                    const bool b_done = t == unit && sb < b_early;   // B requested early
+                    if constexpr (CG == 2) {
+                        const uint32_t fb = mapa_shared(&full[stage], 0);
+                        if (!b_done && rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx_bytes);
+                        tma_load_3d_pair(sa, &tmA, fb, 0, m_blk * TM + rank * kBM, kb0, pol_a);
+                        if (!b_done) tma_load_3d_pair(sa + A_BYTES, &tmB, fb, 0, n_blk * BN + rank * BNL, kb0, pol_b);
+                    } else if (g.first1 && sb == 0) {
                         if (!b_done) mbar_arrive_expect_tx(&full[stage], tx_bytes1);
                         tma_load_3d(sa, &tmA1, &full[stage], 0, m_blk * kBM, 0, pol_a);
                         if (!b_done) tma_load_3d(sa + A_BYTES, &tmB1, &full[stage], 0, n_blk * BN, 0, pol_b);
@@ -586,32 +647,43 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             }
             if (!ok) {
                 // Let the copies that may still be in flight land before the CTA exits.
-                long long first = issued > S ? issued - S : 0;
-                for (long long i = first; i < issued; ++i)
-                    mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1));
+                if (CG == 1 || rank == 0) {
+                    long long first = issued > S ? issued - S : 0;
+                    for (long long i = first; i < issued; ++i)
+                        mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1));
+                } else {
+                    // the odd CTA's copies complete on the even CTA's barriers:
+                    // give them time to land
+                    const uint64_t t0 = globaltimer();
+                    while (globaltimer() - t0 < 50000ull) {
+                    }
+                }
             }
         }
     } else if (warp == 1) {
         // --------------------------------------------------- MMA issuer
         // The whole warp walks the loop with warp-uniform operands: every lane
         // observes each barrier (a time-out anywhere stops all of them) and
-        // one elected lane issues the MMAs and their commits.
-        {
+        // one elected lane issues the MMAs and their commits.  With CG = 2 the
+        // even CTA's warp issues the pair's MMAs and signals both CTAs.
+        if (CG == 1 || rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
             bool any = false;
-            for (int t = blockIdx.x; t < n_work && ok; t += gridDim.x) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, &g_gemm_err, true))) {
+            for (int t = unit; t < n_work && ok; t += n_units) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, &g_gemm_err, true, CG == 2))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int sb = 0; sb < n_stage_blocks; ++sb) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, &g_gemm_err, true))) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&full[stage], phase, abort_flag, &g_gemm_err, true, CG == 2))) {
                         ok = false;
                         break;
                     }
@@ -623,28 +695,47 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     for (int j = 0; j < nkb; ++j) {
                         const int kb = kb0 + j;
                         const uint64_t a_desc = sw128_kmajor_desc(a_addr + static_cast<uint32_t>(j * g.a_rows * kRowBytes));
-                        const uint64_t b_desc = sw128_kmajor_desc(b_addr + static_cast<uint32_t>(j * BN * kRowBytes));
+                        const uint64_t b_desc = sw128_kmajor_desc(b_addr + static_cast<uint32_t>(j * BNL * kRowBytes));
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k) {
                             // +32 bytes along K inside the swizzle row = +2 in 16-byte units.
-                            umma_bf16_elect(d_tmem, a_desc + 2u * k, b_desc + 2u * k, g.idesc,
-                                            (kb > 0 || k > 0) ? 1u : 0u);
+                            if constexpr (CG == 2)
+                                umma_bf16_pair_elect(d_tmem, a_desc + 2u * k, b_desc + 2u * k, g.idesc,
+                                                     (kb > 0 || k > 0) ? 1u : 0u);
+                            else
+                                umma_bf16_elect(d_tmem, a_desc + 2u * k, b_desc + 2u * k, g.idesc,
+                                                (kb > 0 || k > 0) ? 1u : 0u);
                         }
                     }
                     any = true;
-                    umma_commit_elect(&empty[stage]);
+                    if constexpr (CG == 2) {
+                        // the stage is free in both CTAs once these MMAs are done
+                        umma_commit_pair_elect(mapa_shared(&empty[stage], 0));
+                        umma_commit_pair_elect(mapa_shared(&empty[stage], 1));
+                    } else {
+                        umma_commit_elect(&empty[stage]);
+                    }
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit_elect(&tfull[acc]);
+                if constexpr (CG == 2) {
+                    umma_commit_pair_elect(mapa_shared(&tfull[acc], 0));
+                    umma_commit_pair_elect(mapa_shared(&tfull[acc], 1));
+                } else {
+                    umma_commit_elect(&tfull[acc]);
+                }
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
             if (!ok && any) {
-                umma_commit_elect(drain);         // all MMAs issued so far have finished
+                // all MMAs issued so far have finished
+                if constexpr (CG == 2)
+                    umma_commit_pair_elect(mapa_shared(drain, 0));
+                else
+                    umma_commit_elect(drain);
                 if (lane == 0) mbar_wait_drain(drain, 0);
             }
         }
@@ -666,32 +757,36 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         }
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < n_work; t += gridDim.x) {
+        for (int t = unit; t < n_work; t += n_units) {
             const int n_blk = t / m_tiles;
             const int m_blk = t - n_blk * m_tiles;
-            if constexpr (EPI == 3) {
+            const int row_base = m_blk * TM + rank * kBM;          // first row of this CTA's 128
+            if constexpr (EPI == 3 && CG == 1) {
                 // This tile's noise buckets while its MMAs run; the vote below is
                 // also the barrier that makes them (and the table) visible.
+                // (CG = 2 draws them per chunk: the epilogue of a tile runs
+                // under the next tile's MMAs.)
                 if (!sel.greedy)
                     tile_buckets<NT>(bk, g.a_rows, min(kBM, M - m_blk * kBM), BN, n_blk * BN, N, m_blk * kBM, sel);
             }
             // One thread polls the accumulator barrier; the vote hands its
             // outcome to the other 127 (no polling traffic beside the copies).
-            bool ok = threadIdx.x == 64 ? mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err) : true;
+            bool ok = threadIdx.x == 64 ? mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err, false, CG == 2)
+                                        : true;
             ok = epilogue_all<NT>(ok);
             if (!ok) break;
             tc_fence_after();
             // M = 128 MMAs put tile row r in TMEM lane r; M = 64 MMAs put row r in
             // lane 32 (r / 16) + r % 16, so each warp owns 16 rows in lanes 0..15.
             const int rloc = g.m64 ? q * 16 + lane : q * 32 + lane;
-            const int row = m_blk * kBM + rloc;
+            const int row = row_base + rloc;
             const bool live = row < M && (!g.m64 || lane < 16);
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             if constexpr (EPI == 3) {
                 // with M = 64 accumulators the two half-warps share each row
                 const int srloc = g.m64 ? q * 16 + (lane & 15) : rloc;
-                const int srow = m_blk * kBM + srloc;
+                const int srow = row_base + srloc;
                 const bool slive = srow < M;
                 const uint32_t req = slive ? sel.row_req[srow] : 0u;
                 const uint32_t pos = slive ? static_cast<uint32_t>(sel.row_pos[srow]) + 1u : 0u;
@@ -703,11 +798,15 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 const int nch = BN / kChunk, h1 = (nch + 1) / 2;
                 const int cb = eset ? h1 * kChunk : 0, ce = eset ? BN : h1 * kChunk;
                 float* cmt = cmax + (eset * kBM + q * 32 + lane) * kMaxChunks;
-                unsigned long long best =
-                    g.m64 ? tile_row_winner<16>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab, bk + srloc,
-                                                g.a_rows, cmt, lrow)
-                          : tile_row_winner<32>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab, bk + srloc,
-                                                g.a_rows, cmt, lrow);
+                unsigned long long best;
+                if constexpr (CG == 2)
+                    best = tile_row_winner<32, true>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab,
+                                                     nullptr, 0, cmt, lrow);
+                else
+                    best = g.m64 ? tile_row_winner<16>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab,
+                                                       bk + srloc, g.a_rows, cmt, lrow)
+                                 : tile_row_winner<32>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab,
+                                                       bk + srloc, g.a_rows, cmt, lrow);
                 if (eset == 1 && live) s_best[rloc] = best;
                 epilogue_bar<NT>();   // both halves' winners are in; every row is done with the buckets
                 if (eset == 0 && live)
@@ -715,7 +814,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             } else if constexpr (EPI == 4) {
                 // With M = 64 accumulators the two half-warps share each row:
                 // threads 16..31 take pairs 4..7 of every 16-column group.
-                const int prow = g.m64 ? m_blk * kBM + q * 16 + (lane & 15) : row;
+                const int prow = g.m64 ? row_base + q * 16 + (lane & 15) : row;
                 const bool plive = prow < M;
                 const int jb = g.m64 ? 4 * (lane >> 4) : 0;
                 int slot = 0, pos = 0;
@@ -750,7 +849,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 if (g.m64) {
                     // the two half-warps share each row: threads 16..31 take
                     // gate columns 8..15 of every 32-column group and their up columns
-                    const int prow = m_blk * kBM + q * 16 + (lane & 15);
+                    const int prow = row_base + q * 16 + (lane & 15);
                     const int hi = lane >> 4;
 #pragma unroll 1
                     for (int c = 0; c < BN; c += 32) {
@@ -823,16 +922,31 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            if constexpr (CG == 2) {
+                // every epilogue thread of this CTA is done with the accumulator:
+                // one arrival on the even CTA's barrier
+                epilogue_bar<NT>();
+                if (threadIdx.x == 64) mbar_arrive_cluster(mapa_shared(&tempty[acc], 0));
+            } else {
+                mbar_arrive(&tempty[acc]);
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
     }
 
     tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, g.tmem_cols);
+    if constexpr (CG == 2) {
+        // neither CTA leaves while the other may still read its shared memory
+        // (pair MMAs) or signal its barriers
+        cluster_sync();
+        tc_fence_after();
+        if (warp == 1) tmem_dealloc_pair(tmem_base, g.tmem_cols);
+    } else {
+        __syncthreads();
+        tc_fence_after();
+        if (warp == 1) tmem_dealloc(tmem_base, g.tmem_cols);
+    }
 }
 
 // --------------------------------------------------------------- host side
@@ -870,17 +984,61 @@ uint32_t tmem_cols_for(int BN) {
     return c;
 }
 
-template <int EPI>
-int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream,
-                const SelectArgs& sel = SelectArgs{}, const RopeArgs& rp = RopeArgs{}) {
+// Problems of more than one 128-row tile (with K a multiple of 64) run as CTA
+// pairs: 256-row tiles, each weight tile copied once per pair.
+inline bool use_pair(int M, int K) { return M > kBM && K % kBK == 0; }
+
+constexpr int kMaxDevices = 64;
+
+// Once per device and kernel instance (from any host thread): the kernel's
+// opt-in shared memory size and, for pair kernels, how many 2-CTA clusters of
+// it can be resident at once (the persistent grid's size).  Returns a
+// biv_status.
+template <int EPI, int CG>
+int kernel_setup(int dev, int smem_max, int* resident_units) {
+    static std::mutex mu;
+    static int units[kMaxDevices] = {};           // 0 = not yet configured
+    if (dev < 0 || dev >= kMaxDevices) return BIV_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    if (units[dev] == 0) {
+        auto kern = gemm_nosplitk_kernel<EPI, CG>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+        if (e != cudaSuccess) return cuda_status(e);
+        int n = num_sms();
+        if (CG == 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(2 * num_sms()));
+            cfg.blockDim = dim3(64 + epi_threads<EPI>());
+            cfg.dynamicSmemBytes = static_cast<size_t>(smem_max);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (e != cudaSuccess) return cuda_status(e);
+            if (n <= 0) return BIV_ERR_DEVICE;
+        }
+        units[dev] = n;
+    }
+    *resident_units = units[dev];
+    return BIV_OK;
+}
+
+template <int EPI, int CG>
+int launch_gemm_cg(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream,
+                   const SelectArgs& sel, const RopeArgs& rp) {
     GemmArgs g;
     g.M = M;
     g.N = N;
     g.K = K;
     g.BN = BN;
-    g.a_rows = M >= kBM ? kBM : ((M + 7) / 8) * 8;
+    g.a_rows = (CG == 2 || M >= kBM) ? kBM : ((M + 7) / 8) * 8;
     g.KB = (K + kBK - 1) / kBK;
     g.three_d = (K % kBK == 0) ? 1 : 0;
+    const int BNL = BN / CG;                        // B rows one CTA copies per tile
     // The TMA unit spends a fixed ~275 ns per box whatever its size, so a box
     // should be as large as possible.  With one row tile (M <= 128, weight
     // streaming) each stage takes as many k-blocks as let two stages fit the
@@ -889,12 +1047,24 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
     // k-blocks per stage and as many stages as fit.
     int ks = 1;
     const int tail = g.a_rows < kBM ? kTailSlack : 0;
-    // EPI 3 keeps the noise table, chunk maxima and one tile of noise buckets
-    // beside the ring, and takes all of the opt-in shared memory.
-    const int extra = EPI == 3 ? kNoiseTableBytes + 2 * kBM * kMaxChunks * 4 + kBM * 8 + g.a_rows * BN * 2 : 0;
+    // EPI 3 keeps the noise table, chunk maxima and (CG = 1) one tile of noise
+    // buckets beside the ring, and takes all of the opt-in shared memory.
+    const int extra = EPI == 3 ? kNoiseTableBytes + 2 * kBM * kMaxChunks * 4 + kBM * 8 +
+                                     (CG == 1 ? g.a_rows * BN * 2 : 0)
+                               : 0;
     const int ring = EPI == 3 ? kMaxSmem - 1024 - kBarBytes - extra : kRingBudget;
-    const long long work = static_cast<long long>((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
-    if (g.three_d && M <= kBM) {        // one row tile: weight streaming
+    const long long work = static_cast<long long>((M + kBM * CG - 1) / (kBM * CG)) * ((N + BN - 1) / BN);
+    const int smem_max = EPI == 3 ? kMaxSmem : 1024 + kRingBudget + kBarBytes;
+    int dev = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return cuda_status(de);
+    int units = 0;
+    const int st = kernel_setup<EPI, CG>(dev, smem_max, &units);
+    if (st != BIV_OK) return st;
+    if (CG == 2) {
+        // Pairs: two k-blocks per box while the ring holds three stages.
+        if (ring / (2 * (g.a_rows + BNL) * kRowBytes) >= 3) ks = 2;
+    } else if (g.three_d && M <= kBM) {        // one row tile: weight streaming
         const int per_kb = (g.a_rows + BN) * kRowBytes;
         ks = std::max(1, (ring - tail) / (2 * per_kb));
         ks = std::min(ks, std::min(g.KB, 256));
@@ -908,13 +1078,13 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
     g.KS = ks;
     // A one-k-block first stage pays off where the MMA chain, not the copy,
     // sets the pace (narrow tiles with many k-blocks per stage).
-    g.first1 = (g.three_d && ks >= 4 && g.KB > 1) ? 1 : 0;
+    g.first1 = (CG == 1 && g.three_d && ks >= 4 && g.KB > 1) ? 1 : 0;
     g.m64 = g.a_rows <= 64 ? 1 : 0;
-    g.stages = std::min(kMaxStages, std::max(1, (ring - tail) / stage_bytes(ks, g.a_rows, BN)));
-    g.idesc = idesc_bf16_f32(g.m64 ? 64 : kBM, BN);
+    g.stages = std::min(kMaxStages, std::max(1, (ring - tail) / stage_bytes(ks, g.a_rows, BNL)));
+    g.idesc = idesc_bf16_f32(CG == 2 ? 2 * kBM : (g.m64 ? 64 : kBM), BN);
     g.tmem_cols = tmem_cols_for(BN);
     CUtensorMap ta, tb, ta1, tb1;
-    if (!encode_kmajor(&ta, A, K, M, g.a_rows, ks, g.three_d) || !encode_kmajor(&tb, B, K, N, BN, ks, g.three_d)) {
+    if (!encode_kmajor(&ta, A, K, M, g.a_rows, ks, g.three_d) || !encode_kmajor(&tb, B, K, N, BNL, ks, g.three_d)) {
         set_cuda_error(cudaErrorInvalidValue);
         return BIV_ERR_CUDA;
     }
@@ -925,21 +1095,27 @@ int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int 
         set_cuda_error(cudaErrorInvalidValue);
         return BIV_ERR_CUDA;
     }
-    const int smem = 1024 + g.stages * stage_bytes(ks, g.a_rows, BN) + tail + kBarBytes + extra;
-    auto kern = gemm_nosplitk_kernel<EPI>;
-    static int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             EPI == 3 ? kMaxSmem : 1024 + kRingBudget + kBarBytes);
-        if (e != cudaSuccess) return cuda_status(e);
-        configured_device = dev;
+    const int smem = 1024 + g.stages * stage_bytes(ks, g.a_rows, BNL) + tail + kBarBytes + extra;
+    auto kern = gemm_nosplitk_kernel<EPI, CG>;
+    const dim3 block(64 + epi_threads<EPI>());
+    if (CG == 2) {
+        const int grid = 2 * static_cast<int>(std::min<long long>(work, units));
+        return launch_cluster_pdl(kern, dim3(grid), block, static_cast<size_t>(smem), stream, 2, ta, tb, ta1, tb1, C,
+                                  g, sel, rp);
     }
     const int grid = static_cast<int>(std::min<long long>(work, num_sms()));
-    return launch_pdl(kern, dim3(grid), dim3(64 + epi_threads<EPI>()), static_cast<size_t>(smem), stream, ta, tb, ta1,
-                      tb1, C, g, sel,
-                      rp);
+    return launch_pdl(kern, dim3(grid), block, static_cast<size_t>(smem), stream, ta, tb, ta1, tb1, C, g, sel, rp);
+}
+
+// Pair tile widths: multiples of 32 in [64, 256] (each CTA copies BN / 2 rows
+// of B, whole 16-row groups).  Other widths run one CTA per 128-row tile.
+inline bool pair_bn_ok(int BN) { return BN % 32 == 0 && BN >= 64 && BN <= 256; }
+
+template <int EPI>
+int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream,
+                const SelectArgs& sel = SelectArgs{}, const RopeArgs& rp = RopeArgs{}) {
+    if (use_pair(M, K) && pair_bn_ok(BN)) return launch_gemm_cg<EPI, 2>(A, B, C, M, N, K, BN, stream, sel, rp);
+    return launch_gemm_cg<EPI, 1>(A, B, C, M, N, K, BN, stream, sel, rp);
 }
 
 int check_gemm(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K) {
@@ -1049,12 +1225,29 @@ winners_accept_kernel(const unsigned long long* __restrict__ cand, int n_tiles, 
 using namespace biv;
 
 extern "C" int biv_gemm_tile_n(int M, int N, int K) {
-    (void)K;
     const long long m_tiles = std::max<long long>(1, ceil_div(M, kBM));
     if (m_tiles == 1) {
         // Weight streaming: one wave of tiles, each as wide as that allows.
         const int bn = static_cast<int>(std::min<long long>(256, std::max<long long>(16, ceil_div(ceil_div(N, kWave), 16) * 16)));
         if (ceil_div(N, bn) <= kWave) return bn;
+    }
+    if (use_pair(M, K)) {
+        // CTA pairs (256-row tiles): the width in [64, 256], a multiple of 32,
+        // that best fills whole waves of 76 pairs (mildly preferring wide tiles).
+        const long long m_pairs = ceil_div(M, 2 * kBM);
+        int best = 256;
+        double best_score = -1.0;
+        for (int bn = 256; bn >= 64; bn -= 32) {
+            const long long tiles = m_pairs * ceil_div(N, bn);
+            const long long waves = ceil_div(tiles, kPairWave);
+            const double fill = static_cast<double>(tiles) / static_cast<double>(waves * kPairWave);
+            const double score = fill * bn / (bn + 32.0);
+            if (score > best_score + 1e-9) {
+                best_score = score;
+                best = bn;
+            }
+        }
+        return best;
     }
     // Several waves: the width in [64, 256] that best fills the waves, with a
     // mild preference for wide tiles (less activation traffic per weight byte).
@@ -1110,10 +1303,12 @@ extern "C" int biv_gemm_swiglu(const void* A, const void* B_packed, void* act, i
 }
 
 // Tile width of the fused LM head: the GEMM's rounded up to a multiple of 32
-// (whole TMEM loads), at most 128 for full 128-row tiles (the buckets of one
-// tile stay within 32 KiB of shared memory).
+// (whole TMEM loads); with one CTA per full 128-row tile at most 128 (the
+// buckets of one tile stay within 32 KiB of shared memory; CTA pairs draw
+// them per chunk instead).
 static int lm_head_tile_n(int M, int N, int K) {
     const int bn = static_cast<int>(std::min<long long>(256, ceil_div(biv_gemm_tile_n(M, N, K), 32) * 32));
+    if (use_pair(M, K) && pair_bn_ok(bn)) return bn;
     return M >= 128 ? std::min(bn, 128) : bn;
 }
 

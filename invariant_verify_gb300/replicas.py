@@ -47,3 +47,21 @@ def slowest(ms: float, device=None, group=None) -> float:
     t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
     return float(t.item())
+
+
+def rank_window_plan(cfg, n_per_rank: int, K: int, rank: int) -> dict:
+    """The seeded, host-side description of rank ``rank``'s verify window:
+    its requests' global indices and stable ids, cached context lengths, last
+    committed tokens and where its drafter errs (with the ids it then
+    proposes).  Everything is drawn from seeds that depend on the rank, so the
+    ranks' windows differ, and on nothing else, so a rank's window is the same
+    in every run and on every host."""
+    from . import synth
+    mine = rank_requests(n_per_rank, rank)
+    seed = cfg.seed + 1009 * rank
+    ctx = synth.context_lengths(cfg, n_per_rank, seed=seed + 100)
+    g = synth.generator(seed + 300)
+    last = torch.randint(0, cfg.vocab, (n_per_rank,), generator=g, dtype=torch.int64).to(torch.int32)
+    mask, ids = synth.draft_errors((n_per_rank, K), cfg.draft_err, cfg.vocab, seed=seed + 400)
+    return {"requests": mine, "req_ids": request_ids(mine), "ctx": ctx, "last": last,
+            "draft_mask": mask, "draft_ids": ids, "kv_seed": seed + 200}

@@ -95,12 +95,13 @@ class DecoderVerifier:
         self.launches_per_step = (3 if fused_select else 4) + cfg.layers * 8
 
     # -------------------------------------------------------------- stages
-    def forward(self, win: Window, trace: dict | None = None) -> None:
+    def forward(self, win: Window, trace: dict | None = None, mark=None) -> None:
         """Hidden state of every window row (cache rows written).
 
         ``trace``, if given, receives a copy of every intermediate (for
         stage-by-stage parity tests); it adds device copies, so it is not for
-        the timed path.
+        the timed path.  ``mark``, if given, is called with a stage name after
+        each library call (a benchmark records a timing event there).
         """
         c, w = self.cfg, self.w
         Hq, Hkv, hd = c.Hq, c.Hkv, c.hd
@@ -109,7 +110,12 @@ class DecoderVerifier:
             if trace is not None:
                 trace[name] = t.clone()
 
+        def done(name):
+            if mark is not None:
+                mark(name)
+
         B.biv_embed_rmsnorm(w["embed"], win.tokens, w["l0.attn_norm"], self.x, self.h, c.eps)
+        done("embed_rmsnorm")
         snap("x_in", self.x)
         for l in range(c.layers):
             snap(f"l{l}.h_attn", self.h)
@@ -119,25 +125,32 @@ class DecoderVerifier:
             B.biv_gemm_qkv_rope(self.h, w[f"l{l}.wqkv_rope"], self.q, self.kc[l], self.vc[l], win.row_slot,
                                 win.row_pos, c.rope_theta, K=self.rpg,
                                 qkv_out=self.qkv if trace is not None else None)
+            done(f"l{l}.qkv_rope")
             snap(f"l{l}.qkv", self.qkv)
             snap(f"l{l}.q", self.q)
             if trace is not None:
                 trace[f"l{l}.kc"], trace[f"l{l}.vc"] = self.kc[l].clone(), self.vc[l].clone()
             B.biv_decode_attn_fixedsplit(self.q, self.kc[l], self.vc[l], win.row_slot, win.row_pos, self.o,
                                          self.rpg, self.workspace)
+            done(f"l{l}.attention")
             snap(f"l{l}.o", self.o)
             B.biv_gemm_nosplitk(self.o.view(self.W, Hq * hd), w[f"l{l}.wo"], self.proj)
+            done(f"l{l}.wo")
             snap(f"l{l}.attn_proj", self.proj)
             B.biv_add_rmsnorm(self.x, self.proj, w[f"l{l}.ffn_norm"], self.x, self.h, c.eps)
+            done(f"l{l}.add_rmsnorm1")
             snap(f"l{l}.x_mid", self.x)
             snap(f"l{l}.h_ffn", self.h)
             B.biv_gemm_swiglu(self.h, w[f"l{l}.wgu_packed"], self.act)
+            done(f"l{l}.gate_up_swiglu")
             snap(f"l{l}.act", self.act)
             B.biv_gemm_nosplitk(self.act, w[f"l{l}.wdown"], self.proj)
+            done(f"l{l}.down")
             snap(f"l{l}.down", self.proj)
             last = l + 1 == c.layers
             gain = w["final_norm"] if last else w[f"l{l + 1}.attn_norm"]
             B.biv_add_rmsnorm(self.x, self.proj, gain, self.x, self.hidden if last else self.h, c.eps)
+            done(f"l{l}.add_rmsnorm2")
             snap(f"l{l}.x_out", self.x)
         snap("hidden", self.hidden)
 
@@ -168,9 +181,11 @@ class DecoderVerifier:
             self.lm_head(win)
             self.select_and_accept(win)
 
-    def step(self, win: Window) -> None:
-        self.forward(win)
+    def step(self, win: Window, mark=None) -> None:
+        self.forward(win, mark=mark)
         self.lm_head_accept(win)
+        if mark is not None:
+            mark("lm_head_select_accept")
 
     def prefill(self, win: Window) -> None:
         """Deterministic prefill ([DVR] para 3: the verifier's fixed-shape
