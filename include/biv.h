@@ -181,7 +181,10 @@ int biv_gqa_max_drafts(int G, int tile);
  * (biv_decode_attn_workspace_size) exceeds that return BIV_ERR_SCRATCH and
  * launch nothing.  The first call on each device looks up the array's device
  * address (with that device current), so make that first call before any
- * stream capture.  All calls share the one array and it keeps the last
+ * stream capture.  The address is kept for the life of the process: it
+ * assumes the device's primary context outlives every call (after a
+ * cudaDeviceReset the kept address is stale; do not call this entry point
+ * again in that process).  All calls share the one array and it keeps the last
  * call's contents (nothing in it has to start at zero: every partial is
  * written before it is read); calls whose kernels overlap on the GPU -- on
  * different streams, or from different threads -- race on it.  It calls no

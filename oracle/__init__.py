@@ -114,6 +114,32 @@ def round_bf16(x) -> np.ndarray:
     return from_bf16(to_bf16(x))
 
 
+def round_bf16_random(x, rng) -> np.ndarray:
+    """fp64 values rounded to one of their two bracketing bf16 values, chosen
+    at random (``rng``: a numpy Generator), returned as fp64; values a bf16
+    holds exactly are unchanged.
+
+    Any correct bf16 implementation stores, at each storage point, the
+    nearest bf16 of a value within a few fp32 ulps of the exact one, so it
+    differs from the nearest-bf16 oracle by at most one bf16 ulp per stored
+    element.  A composition that rounds every stored element in a random
+    direction departs from the oracle by up to one ulp at (about half of) all
+    elements of every storage point, an envelope for that drift; the
+    end-to-end GPU tests take their logit tolerance from it."""
+    a = _f64(x)
+    near = to_bf16(a)                               # nearest bf16 (ties to even)
+    nv = from_bf16(near)
+    # the other bracketing bf16: one step away from `near`, towards x
+    away = np.abs(a) > np.abs(nv)                   # x lies beyond `near` in magnitude
+    other = near.astype(np.int32) + np.where(away, 1, -1)
+    zero_mag = (near & 0x7FFF) == 0
+    other = np.where(zero_mag & (a != nv), (np.signbit(a).astype(np.int32) << 15) | 1, other)
+    other = (other & 0xFFFF).astype(np.uint16)
+    ov = from_bf16(other)
+    pick = rng.random(a.shape) < 0.5
+    return np.where((a != nv) & pick, ov, nv)
+
+
 def _f64(x) -> np.ndarray:
     a = _np(x)
     if a.dtype == np.uint16:
@@ -256,6 +282,25 @@ def gumbel_argmax(logits, row_req, row_pos, seed: int, temperature: float) -> np
     out = np.empty(R, np.int32)
     lib().orc_gumbel_argmax(_p(x), R, V, V, _p(rq), _p(rp), int(seed), float(temperature), _p(out))
     return out
+
+
+def gumbel_keys(logits, row_req, row_pos, seed: int, temperature: float) -> np.ndarray:
+    """The selection keys of every entry (fp32 [R, V]): key = fl(fl(x * fl(1/T))
+    + g) with g the row's noise at the selected position (row_pos + 1); the
+    logits themselves at T = 0.  numpy's fp32 multiply and add are single
+    IEEE operations, as the rule requires.  (For tests that look at key gaps.)"""
+    x = _np(logits, np.float32).astype(np.float32)
+    R, V = x.shape
+    if float(temperature) == 0.0:
+        return x.copy()
+    invT = np.float32(1.0) / np.float32(temperature)
+    rq = _np(row_req).astype(np.int64) & 0xFFFFFFFF
+    rp = _np(row_pos).astype(np.int64)
+    keys = np.empty_like(x)
+    for r in range(R):
+        g = gumbel_row(seed, int(rq[r]), int(rp[r]) + 1, V)
+        keys[r] = (x[r] * invT).astype(np.float32) + g
+    return keys
 
 
 def gumbel_topk(logits, row_req, row_pos, seed: int, temperature: float, k: int) -> np.ndarray:

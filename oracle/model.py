@@ -18,13 +18,17 @@ pages describe the verifier only as "a forward pass at a fixed batch size"
 where a bf16 verifier stores them (GEMM outputs, norm outputs, RoPE output,
 residual stream, attention output); logits stay fp32.  ``storage="f64"``
 keeps every intermediate in fp64.  The KV cache is bf16 in both modes.
+``storage="bf16_random"`` stores at the same points but rounds each element
+to one of its two bracketing bf16 values at random (``rng``), the window's
+K/V rows included: the drift envelope of implementations that round within
+one ulp at every storage point.
 """
 from __future__ import annotations
 
 import numpy as np
 
 from . import (_f64, _np, attention, from_bf16, gemm, gumbel_argmax, kv_overwrite, rmsnorm,
-               rope, round_bf16, silu_mul, to_bf16, verify_accept)
+               rope, round_bf16, round_bf16_random, silu_mul, to_bf16, verify_accept)
 
 
 class OracleDecoder:
@@ -37,9 +41,14 @@ class OracleDecoder:
                        for k, v in caches]
         self.n_slots, self.max_len = n_slots, max_len
 
-    def forward(self, tokens, row_slot, row_pos, storage: str = "bf16") -> dict:
+    def forward(self, tokens, row_slot, row_pos, storage: str = "bf16", rng=None) -> dict:
         cfg = self.cfg
-        R = round_bf16 if storage == "bf16" else (lambda a: a)
+        if storage == "bf16_random":
+            R = lambda a: round_bf16_random(a, rng)
+            KV = lambda a: to_bf16(round_bf16_random(a, rng))
+        else:
+            R = round_bf16 if storage == "bf16" else (lambda a: a)
+            KV = to_bf16
         tok = np.ascontiguousarray(_np(tokens), np.int64)
         rs = np.ascontiguousarray(_np(row_slot), np.int32)
         rp = np.ascontiguousarray(_np(row_pos), np.int32)
@@ -55,7 +64,7 @@ class OracleDecoder:
             q = R(rope(q, rp, cfg.rope_theta))
             k = rope(k, rp, cfg.rope_theta)
             kc, vc = self.caches[l]
-            kv_overwrite(kc, vc, to_bf16(k), to_bf16(v), rs, rp)
+            kv_overwrite(kc, vc, KV(k), KV(v), rs, rp)
             o = R(attention(q, kc, vc, rs, rp))
             x = R(x + R(gemm(o.reshape(W, Hq * hd), self.w[f"l{l}.wo"])))
             h = R(rmsnorm(x, self.gain[f"l{l}.ffn_norm"], cfg.eps))
@@ -64,7 +73,7 @@ class OracleDecoder:
             x = R(x + R(gemm(a, self.w[f"l{l}.wdown"])))
         hf = R(rmsnorm(x, self.gain["final_norm"], cfg.eps))
         logits = gemm(hf, self.w["lm_head"])
-        if storage == "bf16":
+        if storage != "f64":
             logits = logits.astype(np.float32).astype(np.float64)
         return {"hidden": hf, "logits": logits}
 

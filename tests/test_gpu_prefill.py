@@ -3,13 +3,14 @@ request (rows at positions 0..P-1, no split-K, fixed-split causal attention).
 Because every row is computed the same way whatever else is in the window,
 the prefill writes exactly the KV cache, and selects exactly the tokens, that
 feeding the prompt one token per step does -- checked bitwise -- and it agrees
-with the fp64 oracle within the end-to-end tolerance."""
+with the fp64 oracle's composition within the rounding-drift envelope (row
+by row, derived from the oracle; see gpu_util)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close, same_bits
+from gpu_util import check_end_to_end, e2e_logit_envelope, same_bits
 from oracle.model import OracleDecoder
 from invariant_verify_gb300 import abi as B
 from invariant_verify_gb300 import synth
@@ -17,7 +18,6 @@ from invariant_verify_gb300.verifier import DecoderVerifier, make_window, prefil
 
 pytestmark = pytest.mark.gpu
 SEED = synth.PHILOX_SEED
-E2E_LOGIT_TOL = 0.1
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -75,14 +75,11 @@ def test_prefill_against_oracle():
     torch.cuda.synchronize()
     w_cpu = {k: v.cpu() for k, v in w.items()}
     orc = OracleDecoder(cfg, w_cpu, [(k.cpu() * 0, v.cpu() * 0) for k, v in caches], 1, max_len)
-    out = orc.forward(prompt.numpy(), np.zeros(P, np.int32), np.arange(P, dtype=np.int32), storage="bf16")
-    err = assert_close(ver.logits, out["logits"], tol=E2E_LOGIT_TOL, what="prefill logits")
-    print(f"prefill logits max rel err {err:.4f}")
-    ref = oracle.gumbel_argmax(out["logits"].astype(np.float32), win.row_req.cpu(), win.row_pos.cpu(), SEED,
-                               cfg.temperature)
-    agree = int((ref == ver.target.cpu().numpy()).sum())
-    print(f"prefill token agreement {agree}/{P}")
-    assert agree >= P - P // 8
+    slot, pos = np.zeros(P, np.int32), np.arange(P, dtype=np.int32)
+    ref, tol = e2e_logit_envelope(orc, prompt.numpy(), slot, pos)
+    agree = check_end_to_end(ver.logits.cpu().numpy(), ver.target.cpu().numpy(), ref, tol, win.row_req.cpu(), pos,
+                             SEED, cfg.temperature, what="prefill")
+    print(f"prefill: envelope {tol.min():.4f}..{tol.max():.4f}, token agreement {agree}/{P}")
     # the GPU's own logits give the GPU's tokens exactly
     assert np.array_equal(oracle.gumbel_argmax(ver.logits.cpu(), win.row_req.cpu(), win.row_pos.cpu(), SEED,
                                                cfg.temperature), ver.target.cpu().numpy())

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from oracle.model import OracleDecoder
-from gpu_util import assert_close, same_bits, dev
+from gpu_util import assert_close, check_end_to_end, dev, e2e_logit_envelope, same_bits
 from invariant_verify_gb300 import abi as B
 from invariant_verify_gb300 import synth
 from invariant_verify_gb300.verifier import DecoderVerifier, Window, make_window
@@ -158,14 +158,11 @@ def test_decoder_stagewise_parity(dec2):
     assert np.array_equal(ver.new_len.cpu().numpy(), rnl)
 
 
-# End-to-end, GPU and oracle drift apart through 24 chained bf16 storage
-# points (each a rounding of up to 2^-9 relative, taken on slightly different
-# fp32 / fp64 values) and are re-amplified by the final RMSNorm; this bound
-# is for that drift, not the per-kernel tolerance.
-E2E_LOGIT_TOL = 0.1
-
-
 def test_decoder_end_to_end_against_oracle(dec2):
+    """The whole step against the oracle's own composition (no GPU value fed
+    back): logits within the rounding-drift envelope of gpu_util (derived
+    from the oracle, row by row), and every token that differs from the
+    oracle's explained by a key gap the logit drift bridges."""
     cfg = synth.DECODER2
     w, caches, ctx, max_len = dec2
     W = cfg.W
@@ -175,15 +172,11 @@ def test_decoder_end_to_end_against_oracle(dec2):
     ver.step(win)
     torch.cuda.synchronize()
     orc = OracleDecoder(cfg, w, caches, cfg.N, max_len)
-    out = orc.forward(toks.numpy(), win.row_slot.cpu().numpy(), win.row_pos.cpu().numpy(), storage="bf16")
-    err = assert_close(ver.logits, out["logits"], tol=E2E_LOGIT_TOL, what="end-to-end logits")
-    print(f"end-to-end logits max rel err {err:.4f}")
-    tgt = ver.target.cpu().numpy()
-    otg = oracle.gumbel_argmax(out["logits"].astype(np.float32), win.row_req.cpu(), win.row_pos.cpu(), SEED,
-                               cfg.temperature)
-    diff = np.nonzero(otg != tgt)[0]
-    print(f"end-to-end token agreement {W - len(diff)}/{W}")
-    assert len(diff) <= W // 8, f"{len(diff)} of {W} end-to-end tokens differ"
+    slot, pos = win.row_slot.cpu().numpy(), win.row_pos.cpu().numpy()
+    ref, tol = e2e_logit_envelope(orc, toks.numpy(), slot, pos)
+    agree = check_end_to_end(ver.logits.cpu().numpy(), ver.target.cpu().numpy(), ref, tol, win.row_req.cpu(),
+                             pos, SEED, cfg.temperature, what="2-layer decoder")
+    print(f"end-to-end: envelope {tol.min():.4f}..{tol.max():.4f}, token agreement {agree}/{W}")
 
 
 def test_decoder_rows_bitwise_invariant(dec2):

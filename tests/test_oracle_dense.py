@@ -219,3 +219,29 @@ def test_kv_overwrite_writes_only_the_window_rows():
         assert np.array_equal(vc[slots[w], :, pos[w]], vn[w])
         k0[slots[w], :, pos[w]] = kn[w]; v0[slots[w], :, pos[w]] = vn[w]
     assert np.array_equal(kc, k0) and np.array_equal(vc, v0)
+
+
+def test_random_bf16_rounding_picks_a_bracketing_value():
+    """round_bf16_random returns, for every element, one of the two bf16
+    values that bracket it (the value itself if bf16 holds it exactly), each
+    side about half the time: the grid is rebuilt here from frexp, not from
+    the oracle's bf16 conversion."""
+    rng = np.random.default_rng(3)
+    n = 40000
+    x = rng.normal(size=n) * 10.0 ** rng.integers(-30, 30, n)
+    exact = np.array([0.0, -0.0, 1.0, -2.5, 0.15625, 2.0 ** 127, -1.0 / 1024, 3.0 * 2.0 ** -100])
+    x = np.concatenate([x, exact])
+    y = oracle.round_bf16_random(x, np.random.default_rng(4))
+    m, e = np.frexp(x)                     # |x| = |m| 2^e, 0.5 <= |m| < 1
+    sp = np.ldexp(1.0, e - 8)              # bf16 spacing: 8 significant bits
+    lo, hi = np.floor(x / sp) * sp, np.ceil(x / sp) * sp
+    assert np.all((y == lo) | (y == hi))
+    assert np.array_equal(y[-len(exact):], exact)
+    inexact = lo[:n] != hi[:n]
+    up = (y[:n] == hi[:n]) & inexact
+    frac_up = up.sum() / inexact.sum()
+    assert 0.48 < frac_up < 0.52, frac_up
+    # the nearest-rounding oracle picks the nearer of the same two values
+    near = oracle.round_bf16(x[:n])
+    assert np.all((near == lo[:n]) | (near == hi[:n]))
+    assert np.all(np.abs(near - x[:n]) <= np.abs(np.where(near == lo[:n], hi[:n], lo[:n]) - x[:n]))

@@ -165,3 +165,18 @@ def test_peaked_rows_select_the_peak():
     x[np.arange(64), peak] = 100.0
     tok = oracle.gumbel_argmax(x, np.arange(64), np.arange(64), SEED, 0.7)
     assert np.array_equal(tok, peak)
+
+
+@pytest.mark.parametrize("T", [0.7, 1.0, 0.0])
+def test_gumbel_keys_argmax_is_the_selection(T):
+    """The per-entry keys the end-to-end tests use for key gaps: their
+    first largest entry is the oracle's selected token on every row."""
+    g = np.random.default_rng(17)
+    R, V = 24, 3000
+    x = (g.normal(size=(R, V)) * 3.0).astype(np.float32)
+    x[::5, 7] = x[::5].max(axis=1) + 0.01              # near-peaked rows
+    req = g.integers(0, 2 ** 31 - 1, R)
+    pos = g.integers(0, 100000, R).astype(np.int32)
+    keys = oracle.gumbel_keys(x, req, pos, SEED, T)
+    tok = oracle.gumbel_argmax(x, req, pos, SEED, T)
+    assert np.array_equal(np.argmax(keys, axis=1), tok)

@@ -96,3 +96,44 @@ def test_two_gloo_ranks_match_whole_window(tmp_path):
     assert got["slowest"] == 11.0
     # the windows differ per rank, so the check is not vacuous
     assert not np.array_equal(tgt[:cfg.N * cfg.K], tgt[cfg.N * cfg.K:])
+
+
+def _plan_rank_main(rank, port, out_path):
+    """One rank of the benchmark's host set-up: its own window plan (the
+    request block, ids, contexts, drafter errors), gathered in rank order."""
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=WORLD)
+    try:
+        cfg = synth.SWEEP
+        plan = replicas.rank_window_plan(cfg, 64, 16, rank)
+        ids = replicas.gather_in_rank_order(plan["req_ids"])
+        ctx = replicas.gather_in_rank_order(plan["ctx"])
+        mask = replicas.gather_in_rank_order(plan["draft_mask"].to(torch.int32))
+        if rank == 0:
+            torch.save({"ids": ids, "ctx": ctx, "mask": mask}, out_path)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_bench_rank_windows_disjoint_and_stable(tmp_path):
+    """The benchmark's per-rank windows (weak scaling): two gloo ranks build
+    their plans; the request ids are disjoint across ranks and are rank r's
+    block of the job, and every rank's plan is the same as one built in
+    another process (seeded by the rank only)."""
+    out = str(tmp_path / "plans.pt")
+    mp.start_processes(_plan_rank_main, args=(_free_port(), out), nprocs=WORLD, join=True, start_method="spawn")
+    got = torch.load(out)
+    cfg = synth.SWEEP
+    plans = [replicas.rank_window_plan(cfg, 64, 16, r) for r in range(WORLD)]
+    assert torch.equal(got["ids"], torch.cat([p["req_ids"] for p in plans]))
+    assert torch.equal(got["ctx"], torch.cat([p["ctx"] for p in plans]))
+    assert torch.equal(got["mask"], torch.cat([p["draft_mask"].to(torch.int32) for p in plans]))
+    ids = got["ids"].tolist()
+    assert len(set(ids)) == len(ids) == WORLD * 64
+    assert torch.equal(got["ids"][64:], replicas.request_ids(range(64, 128)))
+    # the ranks' contexts follow the workload recipe and differ between ranks
+    c = got["ctx"]
+    assert int(c.min()) >= cfg.ctx_lo and int(c.max()) <= cfg.ctx_hi
+    assert not torch.equal(c[:64], c[64:])
