@@ -67,7 +67,7 @@ def parse():
     p.add_argument("--c4-steps", action="store_true",
                    help="instead of the step bench: verified tok/s of whole verify steps on the Llama-3-8B-shaped "
                         "layer + LM head at the verifier sweep's windows (N x K = 8x4, 32x8, 64x16)")
-    p.add_argument("--profile-case", choices=["attn16", "select1024", "lmhead1024", "rmsnorm", "gemm1024"],
+    p.add_argument("--profile-case", choices=["attn16", "attn1024", "select1024", "lmhead1024", "rmsnorm", "gemm1024"],
                    help="run one small case twice, for a profiler capture")
     return p.parse_args()
 
@@ -817,8 +817,8 @@ def run_profile_case(args):
     __graft_entry__.build()
     torch.cuda.set_device(0)
     case = args.profile_case
-    if case == "attn16":
-        a = attention_case(16, 16)
+    if case in ("attn16", "attn1024"):
+        a = attention_case(16, 16) if case == "attn16" else attention_case(64, 16)
         for _ in range(2):
             B.biv_decode_attn_fixedsplit(a["q"], a["kc"], a["vc"], a["slot"], a["rpos"], a["o"], a["K"], a["ws"])
         print(json.dumps({"case": case, "bytes": a["bytes"], "ctx_mean": float(a["ctx"].float().mean())}))

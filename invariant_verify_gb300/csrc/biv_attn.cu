@@ -31,6 +31,7 @@ namespace {
 BIV_DEFINE_ERR_WORD(g_attn_err)
 
 constexpr int HD = BIV_HEAD_DIM;        // 128
+constexpr int kMaxDevices = 64;
 constexpr int SPLIT = BIV_KV_SPLIT;     // 256
 constexpr int ROWB = HD * 2;            // 256 bytes per K/V row
 constexpr int ATTN_THREADS = 256;
@@ -108,26 +109,29 @@ constexpr int kMaxRowsSmem = 2048;                 // rows whose usable position
 // Per-tile tables in shared memory, built by all threads of the CTA: the
 // largest usable position of each tile (-1: none), its first row's cache
 // slot, and the exclusive prefix sums of its live work items
-// (Hkv * (tmax / SPLIT + 1) each); s_pref[kMaxTilesSmem] is the live total.
+// (Hkv * (tmax / SPLIT + 1) each); s_pref[tile_cap] is the live total.
 // Returns whether the tables cover every tile (else callers fall back to all
 // (split, KV head, tile) triples with the dead ones skipped).
+// Only the first ATTN_THREADS threads of the CTA fill the tables; every
+// thread of the CTA must call this (it contains the CTA barriers).
 BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, int* s_slot0, int* s_wsum,
-                               int* s_rpos, int* s_gmin) {
+                               int* s_rpos, int* s_gmin, int tile_cap = kMaxTilesSmem, int row_cap = kMaxRowsSmem) {
     const int n_tiles = P.n_tiles;
+    const bool act = threadIdx.x < ATTN_THREADS;
     // s_rpos: each row's usable position (-1: none), when every row is tabulated
-    const bool rows_tab = P.W <= kMaxRowsSmem && n_tiles <= kMaxTilesSmem;
+    const bool rows_tab = P.W <= row_cap && n_tiles <= tile_cap;
     // Largest usable position of each tile, one thread per row (independent
     // loads); tiles past the table are scanned where they are processed.
-    for (int t = threadIdx.x; t < min(n_tiles, kMaxTilesSmem); t += ATTN_THREADS) {
+    for (int t = threadIdx.x; act && t < min(n_tiles, tile_cap); t += ATTN_THREADS) {
         s_tmax[t] = -1;
         s_gmin[t] = 0x7fffffff;             // per row group (there are no more groups than tiles)
     }
     __syncthreads();
-    for (int w = threadIdx.x; w < P.W; w += ATTN_THREADS) {
+    for (int w = threadIdx.x; act && w < P.W; w += ATTN_THREADS) {
         const int group = w / P.rows_per_group;
         const int sub = (w - group * P.rows_per_group) / P.tile_rows;
         const int t = group * P.tiles_per_group + sub;
-        if (t >= kMaxTilesSmem) break;                       // rows only grow the tile index
+        if (t >= tile_cap) break;                            // rows only grow the tile index
         const int row0 = group * P.rows_per_group + sub * P.tile_rows;
         // the three loads are independent: one round trip (the inputs are cold
         // in HBM when the kernel starts)
@@ -158,11 +162,11 @@ BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, in
     // CTAs can deal out exactly the live items, consecutive ones to
     // consecutive CTAs.  Tables too large for shared memory fall back to all
     // (split, KV head, tile) triples with the dead ones skipped.
-    const bool live_mode = n_tiles <= kMaxTilesSmem;
+    const bool live_mode = n_tiles <= tile_cap;
     if (live_mode) {
         // thread i scans tiles [i * per, (i + 1) * per); warp and block prefix
         const int per = (n_tiles + ATTN_THREADS - 1) / ATTN_THREADS;
-        const int t0 = min(static_cast<int>(threadIdx.x) * per, n_tiles);
+        const int t0 = act ? min(static_cast<int>(threadIdx.x) * per, n_tiles) : n_tiles;
         const int t1 = min(t0 + per, n_tiles);
         int sum = 0;
         for (int t = t0; t < t1; ++t) sum += s_tmax[t] >= 0 ? P.Hkv * (s_tmax[t] / SPLIT + 1) : 0;
@@ -173,15 +177,15 @@ BIV_DEV bool build_tile_tables(const AttnParams& P, int* s_tmax, int* s_pref, in
             const int v = __shfl_up_sync(0xffffffffu, inc, o);
             if (lane >= o) inc += v;
         }
-        if (lane == 31) s_wsum[warp] = inc;
+        if (lane == 31 && act) s_wsum[warp] = inc;
         __syncthreads();
         int base = inc - sum;
-        for (int w = 0; w < warp; ++w) base += s_wsum[w];
+        for (int w = 0; act && w < warp; ++w) base += s_wsum[w];
         for (int t = t0; t < t1; ++t) {
             s_pref[t] = base;
             base += s_tmax[t] >= 0 ? P.Hkv * (s_tmax[t] / SPLIT + 1) : 0;
         }
-        if (threadIdx.x == ATTN_THREADS - 1) s_pref[kMaxTilesSmem] = base;   // the live total
+        if (threadIdx.x == ATTN_THREADS - 1) s_pref[tile_cap] = base;        // the live total
         __syncthreads();
     }
     return live_mode;
@@ -220,12 +224,13 @@ constexpr size_t tc_smem_bytes() {
 
 // MN-major shared-memory descriptor for V with 128-byte swizzle: 64 dims
 // (128 B) per swizzled row, one row per key; 8-key atoms 1 KiB apart (stride
-// offset), the two 64-dim halves of a 128-key box 16 KiB apart (leading
-// offset) -- the reading a layout probe confirmed on the GB300.
-BIV_DEV uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+// offset), the two 64-dim halves of a box `half_stride` bytes apart (leading
+// offset; 16 KiB for a 128-key box) -- the reading a layout probe confirmed
+// on the GB300.
+BIV_DEV uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t half_stride = 16384u) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(16384u >> 4) << 16;
+    d |= static_cast<uint64_t>(half_stride >> 4) << 16;
     d |= static_cast<uint64_t>(1024u >> 4) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;
@@ -304,6 +309,7 @@ BIV_DEV float softmax_group(const uint32_t* v, float sl2, float nmu, int lim, ui
 template <int M>
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmK2, const __grid_constant__ CUtensorMap tmV2,
                const AttnParams P) {
     static_assert(M == 64 || M == 128, "MMA rows");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -345,6 +351,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (threadIdx.x == 32) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
+        prefetch_tensormap(&tmK2);
+        prefetch_tensormap(&tmV2);
     }
     tc_fence_before();
     // The tile tables read only the window's slots and positions, inputs of
@@ -366,15 +374,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     uint32_t k_seen[2] = {0u, 0u}, v_seen[2] = {0u, 0u}, s_seen = 0u, o_seen = 0u;
 
     auto n_keys_of = [&](const TcItem& it) { return min(SPLIT, it.maxpos + 1 - it.split * SPLIT); };
-    // thread 0: the K or V boxes of an item
-    auto load_kv = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bars, uint32_t* iss, const TcItem& it) {
+    // thread 0: the K or V of an item as one box ([2 dim halves][R keys][128 B],
+    // R = 256 for a split with more than 128 keys, else 128), on bars[0]
+    auto load_kv = [&](const CUtensorMap* map, const CUtensorMap* map2, uint8_t* dst, uint64_t* bars, uint32_t* iss,
+                       const TcItem& it) {
         const int nkh = n_keys_of(it) > 128 ? 2 : 1;
         const int kv_row = (it.slot0 * P.Hkv + it.kvh) * P.max_len + it.split * SPLIT;
-        for (int kh = 0; kh < nkh; ++kh) {
-            mbar_arrive_expect_tx(&bars[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
-            tma_load_3d(dst + kh * kTcKeyHalfBytes, map, &bars[kh], 0, kv_row + kh * 128, 0, policy_evict_first());
-            ++iss[kh];
-        }
+        mbar_arrive_expect_tx(&bars[0], static_cast<uint32_t>(nkh * kTcKeyHalfBytes));
+        tma_load_3d(dst, nkh == 2 ? map2 : map, &bars[0], 0, kv_row, 0, policy_evict_first());
+        ++iss[0];
     };
     // all threads: the item's Q rows into sQ (K-major, 128-byte swizzle)
     // Thread x copies 16-byte piece c = x % 16 of tile rows t = x / 16 + 16 j:
@@ -430,35 +438,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         const int group = cur.tile / P.tiles_per_group;
         const int gmin = s_gmin[group];
         const int nkh = n_keys_of(cur) > 128 ? 2 : 1;
-        const int kv_row = (cur.slot0 * P.Hkv + cur.kvh) * P.max_len + cur.split * SPLIT;
-        for (int kh = 0; kh < nkh; ++kh) {
-            if (cur.split * SPLIT + (kh + 1) * 128 > gmin) break;
-            mbar_arrive_expect_tx(&kbar[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
-            tma_load_3d(sK + kh * kTcKeyHalfBytes, &tmK, &kbar[kh], 0, kv_row + kh * 128, 0, policy_evict_first());
-            mbar_arrive_expect_tx(&vbar[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
-            tma_load_3d(sV + kh * kTcKeyHalfBytes, &tmV, &vbar[kh], 0, kv_row + kh * 128, 0, policy_evict_first());
-            ++k_iss[kh];
-            ++v_iss[kh];
-            early |= 1u << kh;
+        if (cur.split * SPLIT + nkh * 128 <= gmin) {
+            load_kv(&tmK, &tmK2, sK, kbar, k_iss, cur);
+            load_kv(&tmV, &tmV2, sV, vbar, v_iss, cur);
+            early = 1;
         }
     }
     pdl_wait();
     pdl_trigger();
     if (item < n_work) {
-        if (threadIdx.x == 0) {
-            const int nkh = n_keys_of(cur) > 128 ? 2 : 1;
-            const int kv_row = (cur.slot0 * P.Hkv + cur.kvh) * P.max_len + cur.split * SPLIT;
-            for (int kh = 0; kh < nkh; ++kh) {
-                if (early & (1u << kh)) continue;
-                mbar_arrive_expect_tx(&kbar[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
-                tma_load_3d(sK + kh * kTcKeyHalfBytes, &tmK, &kbar[kh], 0, kv_row + kh * 128, 0,
-                            policy_evict_first());
-                mbar_arrive_expect_tx(&vbar[kh], static_cast<uint32_t>(kTcKeyHalfBytes));
-                tma_load_3d(sV + kh * kTcKeyHalfBytes, &tmV, &vbar[kh], 0, kv_row + kh * 128, 0,
-                            policy_evict_first());
-                ++k_iss[kh];
-                ++v_iss[kh];
-            }
+        if (threadIdx.x == 0 && !early) {
+            load_kv(&tmK, &tmK2, sK, kbar, k_iss, cur);
+            load_kv(&tmV, &tmV2, sV, vbar, v_iss, cur);
         }
         load_q(cur);
     }
@@ -468,6 +459,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         const int key0 = cur.split * SPLIT;
         const int n_keys = n_keys_of(cur);
         const int nkh = n_keys > 128 ? 2 : 1;
+        const uint32_t DS = static_cast<uint32_t>(nkh) * 16384u;   // dim-half stride of this item's K / V box
         const int n16 = (n_keys + 15) >> 4;
         int row0, nr;
         tile_rows_of(P, cur.tile, row0, nr);
@@ -493,8 +485,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // ---- S = Q K^T, issued by warp 0: every lane observes the K halves (a
         // time-out anywhere stops all), one elected lane issues the MMAs.
         if (warp == 0) {
-            bool got = true;
-            for (int kh = 0; kh < nkh && got; ++kh) got = take(&kbar[kh], k_use[kh], k_seen[kh]);
+            bool got = take(&kbar[0], k_use[0], k_seen[0]);
             got = __all_sync(0xffffffffu, got);
             if (got) {
                 tc_fence_after();
@@ -505,10 +496,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     if (kh >= nkh) break;
 #pragma unroll
                     for (int k = 0; k < HD / 16; ++k) {
-                        // start addresses advance in 16-byte units inside the descriptor
+                        // start addresses advance in 16-byte units inside the descriptor; keys
+                        // 128 kh .. of the box start 16 KiB into each dim half
                         const uint64_t a = dq + static_cast<uint64_t>(((k >> 2) * (M * 128) + (k & 3) * 32) >> 4);
                         const uint64_t b =
-                            dk + static_cast<uint64_t>((kh * kTcKeyHalfBytes + (k >> 2) * 16384 + (k & 3) * 32) >> 4);
+                            dk + static_cast<uint64_t>((kh * 16384 + (k >> 2) * DS + (k & 3) * 32) >> 4);
                         umma_bf16_elect(tS + kh * 128, a, b, idS, k > 0 ? 1u : 0u);
                     }
                 }
@@ -518,12 +510,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             }
             ++s_iss;
         }
-        for (int kh = 0; kh < nkh; ++kh) ++k_use[kh];
+        ++k_use[0];
         if (mbar_wait(&sbar, s_use & 1u, &abort_flag, &g_attn_err) && threadIdx.x == 0) ++s_seen;
         ++s_use;
         tc_fence_after();
         // ---- S is in TMEM: this item's K may be overwritten (M = 64)
-        if (M == 64 && has_nxt && threadIdx.x == 0 && !aborted()) load_kv(&tmK, sK, kbar, k_iss, nxt);
+        if (M == 64 && has_nxt && threadIdx.x == 0 && !aborted()) load_kv(&tmK, &tmK2, sK, kbar, k_iss, nxt);
 
         // ---- softmax over the split, row by row
         const int q4 = warp & 3, ch = warp >> 2;
@@ -621,12 +613,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // ---- V rows from the split's last key up to the next 16-key step: zero
         // (a masked p = 0 must never meet a NaN in P V)
         if (warp == 7 && (n_keys & 15) != 0) {
-            const int kl = nkh - 1;
-            if (mbar_wait(&vbar[kl], v_use[kl] & 1u, &abort_flag, &g_attn_err)) {
+            if (mbar_wait(&vbar[0], v_use[0] & 1u, &abort_flag, &g_attn_err)) {
                 for (int idx = lane; idx < (16 * n16 - n_keys) * 16; idx += 32) {
                     const int key = n_keys + (idx >> 4), dh = (idx >> 3) & 1, pc = idx & 7;
-                    *reinterpret_cast<uint4*>(sV + (key >> 7) * kTcKeyHalfBytes + dh * 16384 + (key & 127) * 128 +
-                                              pc * 16) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(sV + dh * DS + key * 128 + pc * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
         }
@@ -639,17 +629,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         tc_fence_after();
         // ---- O = P V, issued by warp 0 like S
         if (warp == 0) {
-            bool got = true;
-            for (int kh = 0; kh < nkh && got; ++kh) got = take(&vbar[kh], v_use[kh], v_seen[kh]);
+            bool got = take(&vbar[0], v_use[0], v_seen[0]);
             got = __all_sync(0xffffffffu, got);
             if (got) {
                 tc_fence_after();
                 constexpr uint32_t idO = idesc_bf16_f32(M, 128) | (1u << 16);   // B (V) MN-major
-                const uint64_t dp = sw128_kmajor_desc(uP), dv = sw128_mnmajor_desc(uV);
+                const uint64_t dp = sw128_kmajor_desc(uP), dv = sw128_mnmajor_desc(uV, DS);
                 for (int st = 0; st < n16; ++st) {
                     const uint64_t a = dp + static_cast<uint64_t>(((st >> 2) * (M * 128) + (st & 3) * 32) >> 4);
-                    const uint64_t b =
-                        dv + static_cast<uint64_t>(((st >> 3) * kTcKeyHalfBytes + (st & 7) * 2048) >> 4);
+                    const uint64_t b = dv + static_cast<uint64_t>((st * 2048) >> 4);
                     umma_bf16_elect(tO, a, b, idO, st > 0 ? 1u : 0u);
                 }
                 umma_commit_elect(&obar);
@@ -658,7 +646,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             }
             ++o_iss;
         }
-        for (int kh = 0; kh < nkh; ++kh) ++v_use[kh];
+        ++v_use[0];
         // the next item's Q (this item's has been read since S landed), while P V runs
         if (has_nxt && !aborted()) load_q(nxt);
         if (mbar_wait(&obar, o_use & 1u, &abort_flag, &g_attn_err) && threadIdx.x == 0) ++o_seen;
@@ -667,8 +655,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // ---- V (and, for M = 128, K's space, which held P) are free: next loads
         if (threadIdx.x == 0 && has_nxt && !aborted()) {
             fence_proxy_async_smem();
-            if (M == 128) load_kv(&tmK, sK, kbar, k_iss, nxt);
-            load_kv(&tmV, sV, vbar, v_iss, nxt);
+            if (M == 128) load_kv(&tmK, &tmK2, sK, kbar, k_iss, nxt);
+            load_kv(&tmV, &tmV2, sV, vbar, v_iss, nxt);
         }
         // ---- the split's partial of every tile row that reaches it
         {
@@ -732,6 +720,380 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
         for (uint32_t j = s_seen; j < s_iss; ++j) mbar_wait_drain(&sbar, j & 1u);
         for (uint32_t j = o_seen; j < o_iss; ++j) mbar_wait_drain(&obar, j & 1u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(s_tmem, kTmemCols);
+}
+
+// ------------------------------------- two items in flight per SM (M = 64)
+// The same work items and the same per-row arithmetic as attn_tc_kernel<64>
+// (bit for bit: the same MMAs, maxima, exponentials and summation tree, and
+// the same split of every row's keys over two threads of two warps), but
+// each CTA runs two warpgroups of eight warps that work through alternate
+// items of the CTA's list independently, each with its own shared-memory
+// regions, barriers and half of the tensor memory.  Within a warpgroup an
+// item is still serial (S -> softmax -> P V -> partials); the other
+// warpgroup's item fills the gaps, so two items' loads and latencies overlap
+// on every SM.  Per warpgroup (96 KiB):
+//   region A (64 KiB): the split's K box for S; then its V box
+//   region B (32 KiB): Q (16 KiB) for S; then P (32 KiB)
+// and tensor memory columns [256 wg, 256 wg + 256): S, then O in the first
+// 128 of them once every thread has read its scores.  The V box is requested
+// as soon as S is in TMEM, the next item's K and Q once P V is.
+// The tile tables live in dynamic shared memory sized to the call.
+constexpr int kPPRegionA = 2 * kTcKeyHalfBytes;       // 64 KiB: K, then V
+constexpr int kPPRegionB = kTcKeyHalfBytes;           // 32 KiB: Q, then P
+constexpr int kPPGroup = kPPRegionA + kPPRegionB;     // per warpgroup
+constexpr int kPPWGThreads = 256;                     // per warpgroup
+constexpr int kPPThreads = 2 * kPPWGThreads;
+
+// Ints of the tile tables for n_tiles tiles and W rows: largest position,
+// prefix sums (+ total), first slot and smallest group position per tile,
+// each row's position, the warp sums of the scan.
+inline long long pp_table_ints(long long n_tiles, long long W) { return 4 * n_tiles + 1 + W + ATTN_THREADS / 32; }
+inline size_t pp_smem_bytes(long long n_tiles, long long W) {
+    return 1024 + 2 * static_cast<size_t>(kPPGroup) + static_cast<size_t>(pp_table_ints(n_tiles, W)) * 4;
+}
+constexpr size_t kPPSmemMax = 224 * 1024;                 // + the kernel's static shared memory <= 227 KiB
+
+// Barrier over the 256 threads of warpgroup wg that ORs a flag across them.
+BIV_DEV bool wg_sync_or(int wg, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(1 + wg)
+        : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(kPPThreads, 1)
+attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmK2, const __grid_constant__ CUtensorMap tmV2,
+               const AttnParams P) {
+    constexpr int M = 64;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = warp >> 3;                         // warpgroup
+    const int w8 = warp & 7;                          // warp within the warpgroup
+    const int wt = threadIdx.x & (kPPWGThreads - 1);  // thread within the warpgroup
+    const int q4 = w8 & 3, ch = w8 >> 2;              // TMEM lane quarter, 128-key half of the split
+    uint8_t* sA = smem + wg * kPPGroup;               // K, then V
+    uint8_t* sB = sA + kPPRegionA;                    // Q, then P
+    const uint32_t uA = smem_u32(sA), uB = smem_u32(sB);
+    const int n_tiles = P.n_tiles;
+    int* s_tmax = reinterpret_cast<int*>(smem + 2 * kPPGroup);
+    int* s_pref = s_tmax + n_tiles;                   // n_tiles + 1
+    int* s_slot0 = s_pref + n_tiles + 1;
+    int* s_gmin = s_slot0 + n_tiles;
+    int* s_rpos = s_gmin + n_tiles;
+    int* s_wsum = s_rpos + P.W;
+
+    __shared__ __align__(8) uint64_t kbar[2][2], vbar[2][2], sbar[2], obar[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int abort_flag;
+    __shared__ int s_pos[2][M];
+    __shared__ float s_mx[2][2][M], s_sum[2][2][M];
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int g = 0; g < 2; ++g) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&kbar[g][i], 1);
+                mbar_init(&vbar[g][i], 1);
+            }
+            mbar_init(&sbar[g], 1);
+            mbar_init(&obar[g], 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        prefetch_tensormap(&tmK2);
+        prefetch_tensormap(&tmV2);
+    }
+    tc_fence_before();
+    // The tables read only the window's slots and positions (inputs of the
+    // call): built while the previous kernel finishes.
+    build_tile_tables(P, s_tmax, s_pref, s_slot0, s_wsum, s_rpos, s_gmin, n_tiles, P.W);   // ends with a barrier
+    tc_fence_after();
+    const uint32_t tS = s_tmem + 256u * static_cast<uint32_t>(wg), tO = tS;
+    const long long n_work = s_pref[n_tiles];
+    const long long step = 2LL * gridDim.x;
+
+    uint64_t* kb = kbar[wg];
+    uint64_t* vb = vbar[wg];
+    uint32_t k_use[2] = {0u, 0u}, v_use[2] = {0u, 0u}, s_use = 0u, o_use = 0u;
+    uint32_t k_iss[2] = {0u, 0u}, v_iss[2] = {0u, 0u}, s_iss = 0u, o_iss = 0u;
+    uint32_t k_seen[2] = {0u, 0u}, v_seen[2] = {0u, 0u}, s_seen = 0u, o_seen = 0u;
+    uint32_t early = 0;
+
+    auto n_keys_of = [&](const TcItem& it) { return min(SPLIT, it.maxpos + 1 - it.split * SPLIT); };
+    auto kv_row_of = [&](const TcItem& it) { return (it.slot0 * P.Hkv + it.kvh) * P.max_len + it.split * SPLIT; };
+    // warpgroup thread 0: the K or V of an item as one box ([2 dim halves][R
+    // keys][128 B], R = 256 for a split with more than 128 keys, else 128)
+    auto load_box = [&](const CUtensorMap* map, const CUtensorMap* map2, uint8_t* dst, uint64_t* bar, uint32_t& iss,
+                        const TcItem& it) {
+        const int nkh = n_keys_of(it) > 128 ? 2 : 1;
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nkh * kTcKeyHalfBytes));
+        tma_load_3d(dst, nkh == 2 ? map2 : map, bar, 0, kv_row_of(it), 0, policy_evict_first());
+        ++iss;
+    };
+    // the warpgroup's threads: the item's Q rows into region B (K-major, 128-byte
+    // swizzle); thread x copies 16-byte piece x % 16 of tile rows x / 16 + 16 j
+    const int q_c = wt & 15, q_t0 = wt >> 4;
+    const uint32_t q_dst0 = uB + (q_c >> 3) * (M * 128) + q_t0 * 128 + (((q_c & 7) ^ (q_t0 & 7)) << 4);
+    const int q_di = 16 / P.G, q_dg = 16 % P.G;
+    const int q_i0 = q_t0 / P.G, q_g0 = q_t0 % P.G;
+    auto load_q = [&](const TcItem& it) {
+        int row0, nr;
+        tile_rows_of(P, it.tile, row0, nr);
+        const int T = nr * P.G;
+        const __nv_bfloat16* base = P.q + (static_cast<long long>(row0) * P.Hq + it.kvh * P.G) * HD + q_c * 8;
+        int i = q_i0, g = q_g0;
+        for (int t = q_t0, j = 0; t < T; t += 16, ++j) {
+            cp_async16(q_dst0 + static_cast<uint32_t>(j) * 2048u, base + (static_cast<long long>(i) * P.Hq + g) * HD);
+            i += q_di;
+            g += q_dg;
+            if (g >= P.G) {
+                g -= P.G;
+                ++i;
+            }
+        }
+        cp_async_commit();
+    };
+    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&abort_flag) != 0; };
+    auto take = [&](uint64_t* bar, uint32_t use, uint32_t& seen) {
+        const bool got = mbar_wait(bar, use & 1u, &abort_flag, &g_attn_err, true);
+        if (got) ++seen;
+        return got;
+    };
+
+    long long item = static_cast<long long>(blockIdx.x) + static_cast<long long>(wg) * gridDim.x;
+    TcItem cur = {};
+    if (item < n_work) cur = tc_decode(P, true, item, s_pref, s_tmax, s_slot0);
+    // K boxes of the first item that lie wholly below its row group's smallest
+    // position (committed context, not the previous kernel's output): before the wait
+    if (wt == 0 && item < n_work) {
+        const int gmin = s_gmin[cur.tile / P.tiles_per_group];
+        const int nkh = n_keys_of(cur) > 128 ? 2 : 1;
+        if (cur.split * SPLIT + nkh * 128 <= gmin) {
+            load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], cur);
+            early = 1;
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (item < n_work) {
+        if (wt == 0 && !early) load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], cur);
+        load_q(cur);
+    }
+    const float sl2 = P.scale_log2;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+    const int r = 16 * q4 + (lane & 15);              // the thread's tile row
+    const int hi = lane >> 4;
+    bool ok = true;
+#pragma unroll 1
+    while (item < n_work) {
+        const int key0 = cur.split * SPLIT;
+        const int n_keys = n_keys_of(cur);
+        const int nkh = n_keys > 128 ? 2 : 1;
+        const uint32_t DS = static_cast<uint32_t>(nkh) * 16384u;   // dim-half stride of this item's K / V box
+        const int n16 = (n_keys + 15) >> 4;
+        int row0, nr;
+        tile_rows_of(P, cur.tile, row0, nr);
+        const int T = nr * P.G;
+        if (wt < nr) s_pos[wg][wt] = s_rpos[row0 + wt];
+        const long long nxt_item = item + step;
+        const bool has_nxt = nxt_item < n_work;
+        TcItem nxt = {};
+        if (has_nxt) nxt = tc_decode(P, true, nxt_item, s_pref, s_tmax, s_slot0);
+
+        // ---- Q landed (cp.async) and visible to the tensor core; s_pos published
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (wg_sync_or(wg, aborted())) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        // ---- S = Q K^T by the warpgroup's first warp (one elected lane)
+        if (w8 == 0) {
+            bool got = take(&kb[0], k_use[0], k_seen[0]);
+            got = __all_sync(0xffffffffu, got);
+            if (got) {
+                tc_fence_after();
+                constexpr uint32_t idS = idesc_bf16_f32(M, 128);
+                const uint64_t dq = sw128_kmajor_desc(uB), dk = sw128_kmajor_desc(uA);
+#pragma unroll
+                for (int kh = 0; kh < 2; ++kh) {
+                    if (kh >= nkh) break;
+#pragma unroll
+                    for (int k = 0; k < HD / 16; ++k) {
+                        const uint64_t a = dq + static_cast<uint64_t>(((k >> 2) * (M * 128) + (k & 3) * 32) >> 4);
+                        const uint64_t b = dk + static_cast<uint64_t>((kh * 16384 + (k >> 2) * DS + (k & 3) * 32) >> 4);
+                        umma_bf16_elect(tS + kh * 128, a, b, idS, k > 0 ? 1u : 0u);
+                    }
+                }
+                umma_commit_elect(&sbar[wg]);
+            } else if (lane == 0) {
+                mbar_arrive(&sbar[wg]);                    // nothing issued: release the waiters
+            }
+            ++s_iss;
+        }
+        ++k_use[0];
+        if (mbar_wait(&sbar[wg], s_use & 1u, &abort_flag, &g_attn_err) && wt == 0) ++s_seen;
+        ++s_use;
+        tc_fence_after();
+        // ---- Q and K consumed: this item's V box into region A
+        if (wt == 0 && !aborted()) load_box(&tmV, &tmV2, sA, &vb[0], v_iss[0], cur);
+        // ---- softmax over the split; the thread's 64 scores (keys 128 ch + 32 i
+        // + 16 hi + t) stay in registers from one round of loads until P is written
+        const int pos = r < T ? s_pos[wg][r / P.G] : -1;
+        float mraw = -INFINITY;
+        uint32_t sv[4][16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (128 * ch + 32 * i < n_keys) tmem_ld16x2(tS + lane_base + 128 * ch + 32 * i, sv[i]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (128 * ch + 32 * i >= n_keys) continue;
+            reg_fence16(sv[i]);
+            mraw = fmaxf(mraw, masked_max<16>(sv[i], pos - (key0 + 128 * ch + 32 * i + 16 * hi)));
+        }
+        mraw = fmaxf(mraw, __shfl_xor_sync(0xffffffffu, mraw, 16));
+        float m = __fmul_rn(mraw, sl2);
+        if (hi == 0) s_mx[wg][ch][r] = m;
+        if (wg_sync_or(wg, aborted())) {
+            ok = false;
+            break;
+        }
+        m = fmaxf(s_mx[wg][0][r], s_mx[wg][1][r]);
+        const float nmu = m == -INFINITY ? 0.0f : -m;      // a row with no key in the split
+        // l: every 16-key group summed in key order, pairs of groups added, then
+        // ((q0 + q1) + (q2 + q3)) per 128-key half and the halves
+        float gq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = 128 * ch + 32 * i;
+            if (c >= n_keys) continue;
+            const int kc = c + 16 * hi;
+            uint32_t pk[8];
+            const float lg = softmax_group(sv[i], sl2, nmu, pos - (key0 + kc), pk);
+            const float lo = __shfl_xor_sync(0xffffffffu, lg, 16);
+            gq[i] = hi ? lo + lg : lg + lo;
+            uint8_t* prow = sB + (kc >> 6) * (M * 128) + r * 128;
+            const int pc = (kc & 63) >> 3;
+            *reinterpret_cast<uint4*>(prow + ((pc ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(prow + (((pc + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        if (hi == 0) s_sum[wg][ch][r] = (gq[0] + gq[1]) + (gq[2] + gq[3]);
+        // ---- V rows from the split's last key up to the next 16-key step: zero
+        if (w8 == 7 && (n_keys & 15) != 0) {
+            if (mbar_wait(&vb[0], v_use[0] & 1u, &abort_flag, &g_attn_err)) {
+                for (int idx = lane; idx < (16 * n16 - n_keys) * 16; idx += 32) {
+                    const int key = n_keys + (idx >> 4), dh = (idx >> 3) & 1, pc = idx & 7;
+                    *reinterpret_cast<uint4*>(sA + dh * DS + key * 128 + pc * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (wg_sync_or(wg, aborted())) {               // P written; every thread has read its S
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        // ---- O = P V into the first 128 columns of the S region
+        if (w8 == 0) {
+            bool got = take(&vb[0], v_use[0], v_seen[0]);
+            got = __all_sync(0xffffffffu, got);
+            if (got) {
+                tc_fence_after();
+                constexpr uint32_t idO = idesc_bf16_f32(M, 128) | (1u << 16);   // B (V) MN-major
+                const uint64_t dp = sw128_kmajor_desc(uB), dv = sw128_mnmajor_desc(uA, DS);
+                for (int st = 0; st < n16; ++st) {
+                    const uint64_t a = dp + static_cast<uint64_t>(((st >> 2) * (M * 128) + (st & 3) * 32) >> 4);
+                    const uint64_t b = dv + static_cast<uint64_t>((st * 2048) >> 4);
+                    umma_bf16_elect(tO, a, b, idO, st > 0 ? 1u : 0u);
+                }
+                umma_commit_elect(&obar[wg]);
+            } else if (lane == 0) {
+                mbar_arrive(&obar[wg]);
+            }
+            ++o_iss;
+        }
+        ++v_use[0];
+        if (mbar_wait(&obar[wg], o_use & 1u, &abort_flag, &g_attn_err) && wt == 0) ++o_seen;
+        ++o_use;
+        tc_fence_after();
+        // ---- P and V consumed: the next item's K and Q
+        if (has_nxt && !aborted()) {
+            if (wt == 0) {
+                fence_proxy_async_smem();
+                load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], nxt);
+            }
+            load_q(nxt);
+        }
+        // ---- the split's partial of every tile row that reaches it
+        {
+            const int i = r / P.G, g = r - i * P.G;
+            const long long ph = (static_cast<long long>(row0 + i) * P.Hq + cur.kvh * P.G + g) * P.s_max + cur.split;
+            float* dst = P.ws_o + ph * HD;
+            uint32_t ov[2][16];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tmem_ld16x2(tO + lane_base + 64 * ch + 32 * j, ov[j]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                reg_fence16(ov[j]);
+                const uint32_t* v = ov[j];
+                if (pos >= key0) {
+                    float4* d4 = reinterpret_cast<float4*>(dst + 64 * ch + 32 * j + 16 * hi);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                }
+            }
+            if (pos >= key0 && ch == 0 && hi == 0) {
+                P.ws_m[ph] = m;
+                P.ws_l[ph] = s_sum[wg][0][r] + s_sum[wg][1][r];
+            }
+        }
+        tc_fence_before();
+        if (wg_sync_or(wg, aborted())) {               // TMEM, s_mx, s_sum and s_pos are reused
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        item = nxt_item;
+        cur = nxt;
+    }
+    // ---- leave.  After a time-out, the copies and MMAs already started
+    // complete first (bounded waits), then TMEM is freed.
+    cp_async_wait<0>();
+    if (wt == 0 && !ok) {
+        for (int kh = 0; kh < 2; ++kh) {
+            for (uint32_t j = k_seen[kh]; j < k_iss[kh]; ++j) mbar_wait_drain(&kb[kh], j & 1u);
+            for (uint32_t j = v_seen[kh]; j < v_iss[kh]; ++j) mbar_wait_drain(&vb[kh], j & 1u);
+        }
+        for (uint32_t j = s_seen; j < s_iss; ++j) mbar_wait_drain(&sbar[wg], j & 1u);
+        for (uint32_t j = o_seen; j < o_iss; ++j) mbar_wait_drain(&obar[wg], j & 1u);
     }
     tc_fence_before();
     __syncthreads();
@@ -982,7 +1344,10 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
     if (n_tiles > 0x7fffffffLL / 64 || Hkv > 65535) return BIV_ERR_SHAPE;
     P.n_tiles = static_cast<int>(n_tiles);
     // K and V caches as TMA sees them: [2 halves of a row][n_slots*Hkv*max_len rows][64 elements]
-    CUtensorMap tk, tv;
+    // K and V caches as TMA sees them: [2 halves of a row][n_slots*Hkv*max_len
+    // rows][64 elements]; boxes of 128 keys (tk, tv) and of a whole 256-key
+    // split (tk2, tv2), each landing as [2 dim halves][keys][128 B]
+    CUtensorMap tk, tv, tk2, tv2;
     {
         EncodeTiledFn enc = encode_fn();
         if (!enc) {
@@ -991,11 +1356,11 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
         }
         cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(n_slots) * Hkv * max_len, 2};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(ROWB), 128};
-        cuuint32_t box[3] = {64, 128, 2};
         cuuint32_t es[3] = {1, 1, 1};
-        const void* bases[2] = {k_cache, v_cache};
-        CUtensorMap* maps[2] = {&tk, &tv};
-        for (int i = 0; i < 2; ++i) {
+        const void* bases[4] = {k_cache, v_cache, k_cache, v_cache};
+        CUtensorMap* maps[4] = {&tk, &tv, &tk2, &tv2};
+        for (int i = 0; i < 4; ++i) {
+            cuuint32_t box[3] = {64, i < 2 ? 128u : 256u, 2};
             if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(bases[i]), dims, strides, box,
                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
@@ -1005,36 +1370,53 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
         }
     }
 
-    static int configured_device = -1;
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(tc_smem_bytes<64>()));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(tc_smem_bytes<128>()));
-        if (e != cudaSuccess) return cuda_status(e);
-        configured_device = dev;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return cuda_status(de);
+    int combine_per_sm = 0;                        // resident combine CTAs per SM
+    {
+        // once per device, from any host thread: kernel attributes and occupancy
+        static std::mutex mu;
+        static int per_sm[kMaxDevices] = {};       // 0 = not yet configured
+        if (dev < 0 || dev >= kMaxDevices) return BIV_ERR_DEVICE;
+        std::lock_guard<std::mutex> lock(mu);
+        if (per_sm[dev] == 0) {
+            cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(tc_smem_bytes<64>()));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(tc_smem_bytes<128>()));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(attn_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kPPSmemMax));
+            if (e != cudaSuccess) return cuda_status(e);
+            int per = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_combine_kernel, 256, 0) != cudaSuccess ||
+                per < 1)
+                per = 1;
+            per_sm[dev] = per;
+        }
+        combine_per_sm = per_sm[dev];
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const long long n_items = static_cast<long long>(s_max) * Hkv * n_tiles;
     const int grid = static_cast<int>(std::min<long long>(n_items, num_sms()));
-    // MMA rows: 64 when the tile's G x rows fit, else 128
-    int st = P.tile_rows * P.G <= 64
-                 ? launch_pdl(attn_tc_kernel<64>, dim3(static_cast<unsigned>(grid)), dim3(ATTN_THREADS),
-                              tc_smem_bytes<64>(), s, tk, tv, P)
-                 : launch_pdl(attn_tc_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(ATTN_THREADS),
-                              tc_smem_bytes<128>(), s, tk, tv, P);
+    // MMA rows: 64 when the tile's G x rows fit, else 128.  With 64 rows and
+    // tile tables that fit beside two warpgroups' buffers, two items per SM
+    // are in flight (attn_pp_kernel); otherwise one (attn_tc_kernel).
+    const size_t pp_smem = pp_smem_bytes(n_tiles, W);
+    int st;
+    if (P.tile_rows * P.G <= 64 && pp_smem <= kPPSmemMax)
+        st = launch_pdl(attn_pp_kernel, dim3(static_cast<unsigned>(grid)), dim3(kPPThreads), pp_smem, s, tk, tv,
+                        tk2, tv2, P);
+    else if (P.tile_rows * P.G <= 64)
+        st = launch_pdl(attn_tc_kernel<64>, dim3(static_cast<unsigned>(grid)), dim3(ATTN_THREADS),
+                        tc_smem_bytes<64>(), s, tk, tv, tk2, tv2, P);
+    else
+        st = launch_pdl(attn_tc_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(ATTN_THREADS),
+                        tc_smem_bytes<128>(), s, tk, tv, tk2, tv2, P);
     if (st != BIV_OK) return st;
     const long long n_pairs = static_cast<long long>(W) * Hq;
-    static int combine_per_sm = 0;                 // resident combine CTAs per SM
-    if (combine_per_sm == 0) {
-        int per = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_combine_kernel, 256, 0) != cudaSuccess || per < 1)
-            per = 1;
-        combine_per_sm = per;
-    }
     const long long cgrid = std::min<long long>((n_pairs + 7) / 8, static_cast<long long>(num_sms()) * combine_per_sm);
     return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(cgrid)), dim3(256), 0, s, P,
                       static_cast<__nv_bfloat16*>(o));
@@ -1102,7 +1484,6 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_attn_scratch[BIV_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 

@@ -230,6 +230,14 @@ BIV_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, 
         : "memory");
 }
 
+// Prefetch one 3-D tiled box into L2 (no shared memory, no completion).
+BIV_DEV void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 BIV_DEV void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

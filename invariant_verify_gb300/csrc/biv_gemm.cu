@@ -1163,6 +1163,22 @@ __global__ void rope_pack_kernel(const __nv_bfloat16* __restrict__ src, __nv_bfl
     for (int c = threadIdx.x; c < K / 8; c += blockDim.x) out[c] = in[c];
 }
 
+// Largest of the row's n_tiles packed tile winners, taken by one warp: eight
+// independent loads in flight per lane, then the warp maximum (a maximum is
+// exact in any order).
+BIV_DEV unsigned long long row_winner(const unsigned long long* __restrict__ row_cand, int n_tiles, int lane) {
+    unsigned long long b[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int t = lane;
+    for (; t + 7 * 32 < n_tiles; t += 8 * 32) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) b[j] = umax64(b[j], row_cand[t + 32 * j]);
+    }
+    for (; t < n_tiles; t += 32) b[0] = umax64(b[0], row_cand[t]);
+#pragma unroll
+    for (int j = 1; j < 8; ++j) b[0] = umax64(b[0], b[j]);
+    return warp_max64(b[0]);
+}
+
 // tokens[row] = the index of the largest of the row's tile winners (0 for a
 // row with no number); one warp per row.
 __global__ void tile_winners_kernel(const unsigned long long* __restrict__ cand, int M, int n_tiles,
@@ -1172,9 +1188,7 @@ __global__ void tile_winners_kernel(const unsigned long long* __restrict__ cand,
     const int row = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
     const int lane = threadIdx.x & 31;
     if (row >= M) return;
-    unsigned long long b = 0;
-    for (int t = lane; t < n_tiles; t += 32) b = umax64(b, cand[static_cast<long long>(row) * n_tiles + t]);
-    b = warp_max64(b);
+    const unsigned long long b = row_winner(cand + static_cast<long long>(row) * n_tiles, n_tiles, lane);
     if (lane == 0) tokens[row] = b ? static_cast<int32_t>(~static_cast<uint32_t>(b & 0xffffffffull)) : 0;
 }
 
@@ -1185,7 +1199,7 @@ constexpr int kMaxAcceptRows = 8192;              // K of one request in the fus
 // coupled accept (as verify_accept_kernel): accept length L = first j with
 // target != draft, + 1, else K; new length p0 + L.  Same integer results as
 // the two kernels.  Dynamic shared memory: K tokens.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(1024)
 winners_accept_kernel(const unsigned long long* __restrict__ cand, int n_tiles, int32_t* __restrict__ tokens,
                       const int32_t* __restrict__ draft, const int32_t* __restrict__ p0, int K,
                       int32_t* __restrict__ accept_len, int32_t* __restrict__ new_len) {
@@ -1196,9 +1210,7 @@ winners_accept_kernel(const unsigned long long* __restrict__ cand, int n_tiles, 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int j = warp; j < K; j += blockDim.x / 32) {
         const long long row = static_cast<long long>(r) * K + j;
-        unsigned long long b = 0;
-        for (int t = lane; t < n_tiles; t += 32) b = umax64(b, cand[row * n_tiles + t]);
-        b = warp_max64(b);
+        const unsigned long long b = row_winner(cand + row * n_tiles, n_tiles, lane);
         if (lane == 0) {
             const int32_t tok = b ? static_cast<int32_t>(~static_cast<uint32_t>(b & 0xffffffffull)) : 0;
             tokens[row] = tok;
@@ -1378,7 +1390,9 @@ extern "C" int biv_lm_head_gumbel_accept(const void* A, const void* B, float* lo
         if (st2 != BIV_OK) return st2;
         return biv_verify_accept(tokens, draft, p0, n_req, rows_per_req, accept_len, new_len, stream);
     }
-    return launch_pdl(winners_accept_kernel, dim3(static_cast<unsigned>(n_req)), dim3(256),
+    // one warp per row of the request (up to 32 warps)
+    const int warps = std::min(32, std::max(1, rows_per_req));
+    return launch_pdl(winners_accept_kernel, dim3(static_cast<unsigned>(n_req)), dim3(32 * warps),
                       static_cast<size_t>(rows_per_req) * sizeof(int32_t), s,
                       static_cast<const unsigned long long*>(workspace), n_tiles, tokens, draft, p0, rows_per_req,
                       accept_len, new_len);
