@@ -67,7 +67,8 @@ def parse():
     p.add_argument("--c4-steps", action="store_true",
                    help="instead of the step bench: verified tok/s of whole verify steps on the Llama-3-8B-shaped "
                         "layer + LM head at the verifier sweep's windows (N x K = 8x4, 32x8, 64x16)")
-    p.add_argument("--profile-case", choices=["attn16", "attn1024", "select1024", "lmhead1024", "rmsnorm", "gemm1024"],
+    p.add_argument("--profile-case", choices=["attn16", "attn1024", "select1024", "lmhead1024", "rmsnorm", "gemm1024",
+                                              "qkv1024"],
                    help="run one small case twice, for a profiler capture")
     return p.parse_args()
 
@@ -88,13 +89,6 @@ def peaks():
         return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
                 float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
     return 6800.0, 1900.0, 1700.0, "fallback"
-
-
-WORKLOADS = {
-    # name: (config, N, K)
-    "c4": ("SWEEP", 64, 16),
-    "decoder2": ("DECODER2", 8, 8),
-}
 
 
 def workload_config(cfg, N, K):
@@ -853,8 +847,8 @@ def run_profile_case(args):
             B.biv_lm_head_gumbel(A, Wl, req, pos, SEED, 0.7, tok, ws)
         print(json.dumps({"case": case, "M": M, "N": N, "K": Kd, "flops": 2 * M * N * Kd,
                           "bytes": 2 * N * Kd + 2 * M * Kd + 12 * M}))
-    else:   # gemm1024: the gate/up-shaped plain GEMM at M = 1024
-        M, N, Kd = 1024, 28672, 4096
+    else:   # gemm1024 / qkv1024: the gate/up- or QKV-shaped plain GEMM at M = 1024
+        M, N, Kd = 1024, (28672 if case == "gemm1024" else 6144), 4096
         A = synth.bf16_normal_device((M, Kd), 1.0, 13)
         Wl = synth.bf16_normal_device((N, Kd), 0.02, 14)
         C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
