@@ -506,6 +506,7 @@ def run_ours(args):
         k2 = max(50, min(4 * K_steps, 2000))
         t2 = time_steps(p2["ver"], p2["win"], k2, args.warmup, world, device, rank, local, flush=flush)
         ms2 = t2["tot_ms"] / k2
+        times2 = kernel_breakdown(p2["ver"], p2["win"])
         b2, f2 = step_work(c2, c2.W, c2.K, p2["ctx"])
         lb2 = max(b2 / (hbm * 1e9), f2 / (bf16 * 1e12)) * 1e6
         out["decoder2_w64"] = {
@@ -514,6 +515,7 @@ def run_ours(args):
             "roofline": lm_roofline(c2, c2.W, t2["lm_ms"], t2["lm_timing"], hbm, bf16, bf16_sus, src),
             "step_roofline": {"bytes": b2, "flops": f2, "lower_bound_us": round(lb2, 2),
                               "frac": round(lb2 / (ms2 * 1e3), 4)},
+            "kernels": breakdown_lines(c2, c2.W, c2.K, p2["ctx"], times2, hbm, bf16) if times2 else None,
             "gpu_launches_per_step": p2["ver"].launches_per_step, "clocks": t2["clocks"]}
         del p2, t2, flush
         torch.cuda.empty_cache()
