@@ -1,5 +1,6 @@
 // Host-side plumbing of libbiv: status strings, the thread-local CUDA error
 // record, the device error word readers and the SM count.
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -28,17 +29,16 @@ void register_err_reader(err_reader_fn fn) {
 }
 
 int num_sms() {
-    static int cached_dev = -1;
-    static int cached = 0;
+    static std::atomic<int> cached[kMaxDevices];   // 0 = not yet queried (static storage: zero)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (dev != cached_dev) {
-        int n = 0;
+    if (dev < 0 || dev >= kMaxDevices) return 1;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-        cached = n;
-        cached_dev = dev;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached;
+    return n;
 }
 
 EncodeTiledFn encode_fn() {

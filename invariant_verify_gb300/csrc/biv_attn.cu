@@ -31,7 +31,6 @@ namespace {
 BIV_DEFINE_ERR_WORD(g_attn_err)
 
 constexpr int HD = BIV_HEAD_DIM;        // 128
-constexpr int kMaxDevices = 64;
 constexpr int SPLIT = BIV_KV_SPLIT;     // 256
 constexpr int ROWB = HD * 2;            // 256 bytes per K/V row
 constexpr int ATTN_THREADS = 256;

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/biv.h"
 
 #define BIV_DEV __device__ __forceinline__
@@ -24,6 +26,24 @@ inline int cuda_status(cudaError_t e) {
 inline int launch_status() { return cuda_status(cudaGetLastError()); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int num_sms();                                      // of the current device, cached
+
+// Per-device one-time set-up (kernel attributes, symbol addresses), safe to
+// call from several host threads: run(dev, f) calls f() until it returns
+// BIV_OK once for that device, and returns BIV_OK without calling it after.
+constexpr int kMaxDevices = 64;
+struct DeviceOnce {
+    std::mutex mu;
+    bool done[kMaxDevices] = {};
+    template <typename F>
+    int run(int dev, F&& f) {
+        if (dev < 0 || dev >= kMaxDevices) return BIV_ERR_DEVICE;
+        std::lock_guard<std::mutex> lock(mu);
+        if (done[dev]) return BIV_OK;
+        const int st = f();
+        if (st == BIV_OK) done[dev] = true;
+        return st;
+    }
+};
 
 // cuTensorMapEncodeTiled from the driver (through the runtime's entry-point
 // query, so no link against libcuda); null if unavailable.

@@ -988,8 +988,6 @@ uint32_t tmem_cols_for(int BN) {
 // pairs: 256-row tiles, each weight tile copied once per pair.
 inline bool use_pair(int M, int K) { return M > kBM && K % kBK == 0; }
 
-constexpr int kMaxDevices = 64;
-
 // Once per device and kernel instance (from any host thread): the kernel's
 // opt-in shared memory size and, for pair kernels, how many 2-CTA clusters of
 // it can be resident at once (the persistent grid's size).  Returns a

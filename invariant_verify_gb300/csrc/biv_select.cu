@@ -740,38 +740,44 @@ int launch_stream_select(const float* logits, int R, int V, long long ld, const 
                          const int32_t* row_pos, uint64_t seed, float invT, int greedy, int32_t* tokens,
                          cudaStream_t stream) {
     const size_t smem = stream_smem_bytes(V);
-    static int configured_device = -1;
-    static int per_sm_cache[2] = {0, 0};         // {smem the value is for, CTAs per SM}
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gumbel_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(stream_smem_bytes(kMaxStreamV)));
-        if (e != cudaSuccess) return cuda_status(e);
-        configured_device = dev;
-        per_sm_cache[0] = 0;
-    }
-    if (per_sm_cache[0] != static_cast<int>(smem)) {
-        int per_sm = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gumbel_stream_kernel, kSelThreads, smem);
-        if (e != cudaSuccess) return cuda_status(e);
-        per_sm_cache[0] = static_cast<int>(smem);
-        per_sm_cache[1] = std::max(1, per_sm);
-    }
-    static int ctr_device = -1;
-    static unsigned int* ctr_base = nullptr;
-    if (ctr_device != dev) {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_stream_ctr);
-        if (e != cudaSuccess) return cuda_status(e);
-        ctr_base = static_cast<unsigned int*>(p);
-        ctr_device = dev;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return cuda_status(de);
+    if (dev < 0 || dev >= kMaxDevices) return BIV_ERR_DEVICE;
+    int per_sm = 0;
+    unsigned int* ctr_base = nullptr;
+    {
+        // per device, from any host thread: the kernel attribute, the counter
+        // ring's device address and the occupancy at this shared-memory size
+        static std::mutex mu;
+        static unsigned int* ctr_dev[kMaxDevices] = {};
+        static size_t occ_smem[kMaxDevices] = {};
+        static int occ_per_sm[kMaxDevices] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (!ctr_dev[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(gumbel_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(stream_smem_bytes(kMaxStreamV)));
+            if (e != cudaSuccess) return cuda_status(e);
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_stream_ctr);
+            if (e != cudaSuccess) return cuda_status(e);
+            ctr_dev[dev] = static_cast<unsigned int*>(p);
+        }
+        if (occ_smem[dev] != smem) {
+            int n = 0;
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gumbel_stream_kernel, kSelThreads, smem);
+            if (e != cudaSuccess) return cuda_status(e);
+            occ_smem[dev] = smem;
+            occ_per_sm[dev] = std::max(1, n);
+        }
+        per_sm = occ_per_sm[dev];
+        ctr_base = ctr_dev[dev];
     }
     // Each launch takes the next counter pair of the ring (launches in flight
     // at the same time on different streams must not share one).
     static std::atomic<unsigned> next_slot{0};
     unsigned int* ctr = ctr_base + 2 * (next_slot.fetch_add(1u) % kCtrSlots);
-    const long long cap = static_cast<long long>(num_sms()) * per_sm_cache[1];
+    const long long cap = static_cast<long long>(num_sms()) * per_sm;
     const int grid = static_cast<int>(std::min<long long>(R, cap));
     return launch_pdl(gumbel_stream_kernel, dim3(static_cast<unsigned>(grid)), dim3(kSelThreads), smem, stream,
                       logits, R, V, ld, row_req, row_pos, static_cast<uint32_t>(seed & 0xffffffffull),
@@ -805,17 +811,15 @@ extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld
     if (static_cast<long long>(R) * kClusterSize > 0x7fffffffLL) return BIV_ERR_SHAPE;
     const size_t smem = static_cast<size_t>(slice) * 5;
 
-    static int configured_device = -1;
-    static size_t configured_smem = 0;
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev || configured_smem < smem) {
-        cudaError_t e = cudaFuncSetAttribute(gumbel_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kMaxSliceFloats * 5));
-        if (e != cudaSuccess) return cuda_status(e);
-        configured_device = dev;
-        configured_smem = kMaxSliceFloats * 5;
-    }
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return cuda_status(de);
+    static DeviceOnce once;
+    const int st = once.run(dev, [] {
+        return cuda_status(cudaFuncSetAttribute(gumbel_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                static_cast<int>(kMaxSliceFloats * 5)));
+    });
+    if (st != BIV_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(R) * kClusterSize, 1, 1);
     cfg.blockDim = dim3(kSelThreads, 1, 1);
@@ -849,15 +853,15 @@ extern "C" int biv_gumbel_topk(const float* logits, int R, int V, long long ld, 
     const int greedy = temperature == 0.0f;
     const float invT = greedy ? 0.0f : 1.0f / temperature;   // fl(1/T), IEEE division on the host
     const size_t smem = static_cast<size_t>(k) * kTopkThreads * sizeof(unsigned long long);
-    static int configured_device = -1;
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gumbel_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kMaxTopk * kTopkThreads * sizeof(unsigned long long)));
-        if (e != cudaSuccess) return cuda_status(e);
-        configured_device = dev;
-    }
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return cuda_status(de);
+    static DeviceOnce once;
+    const int st = once.run(dev, [] {
+        return cuda_status(cudaFuncSetAttribute(gumbel_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                static_cast<int>(kMaxTopk * kTopkThreads * sizeof(unsigned long long))));
+    });
+    if (st != BIV_OK) return st;
     return launch_pdl(gumbel_topk_kernel, dim3(static_cast<unsigned>(R)), dim3(kTopkThreads), smem,
                       reinterpret_cast<cudaStream_t>(stream), logits, V, ld, row_req, row_pos,
                       static_cast<uint32_t>(seed & 0xffffffffull), static_cast<uint32_t>(seed >> 32), invT, greedy, k,

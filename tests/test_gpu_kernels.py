@@ -258,6 +258,27 @@ def test_attention_past_the_tile_tables_same_bits():
     assert_close(many[rows], ref, what="attention (dense numbering)")
 
 
+def test_attention_two_item_and_one_item_kernels_same_bits():
+    """Windows whose tile tables fit beside two warpgroups' buffers run two
+    items per SM (attn_pp_kernel); 2000 one-row tiles do not, and run one
+    item per SM (attn_tc_kernel, tables still in shared memory).  The same
+    rows give the same bits either way, and match the oracle."""
+    W, Hq, Hkv, max_len = 2000, 8, 2, 1200
+    g = synth.generator(2000)
+    kc = synth.bf16_normal((8, Hkv, max_len, 128), 1.0, g)
+    vc = synth.bf16_normal((8, Hkv, max_len, 128), 1.0, g)
+    q = synth.bf16_normal((W, Hq, 128), 1.0, g)
+    slot = (np.arange(W) % 8).astype(np.int32)
+    pos = (np.arange(W) * 131 % 1150).astype(np.int32)
+    qd, kd, vd = dev(q), dev(kc), dev(vc)
+    big = _run_attn(qd, kd, vd, slot, pos, 1)             # one item per SM
+    small = _run_attn(qd[:256].contiguous(), kd, vd, slot[:256], pos[:256], 1)   # two per SM
+    assert same_bits(big[:256], small)
+    rows = [0, 77, 255, 1999]
+    ref = oracle.attention(q[rows], kc, vc, slot[rows], pos[rows])
+    assert_close(big[rows], ref, what="attention (one item per SM)")
+
+
 def test_attention_bad_position_raises_device_error():
     q, kc, vc, slot, pos = _attn_case(2, 8, 2, 600, [100, 300], 4, seed=12)
     qd, kd, vd = dev(q), dev(kc), dev(vc)
