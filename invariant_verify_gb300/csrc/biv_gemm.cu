@@ -45,7 +45,6 @@ BIV_DEFINE_ERR_WORD(g_gemm_err)
 constexpr int kBM = 128;
 constexpr int kBK = 64;                       // 64 bf16 = one 128-byte swizzle row
 constexpr int kRowBytes = kBK * 2;            // one 64-wide k-block row: 128 B
-constexpr int kRingBudget = 208 * 1024;       // bytes of pipeline stages per CTA
 constexpr int kTailSlack = kBM * kRowBytes;   // the MMA may read 128 A rows past the last stage
 constexpr int kMaxStages = 24;
 constexpr int kBarBytes = 512;
@@ -1050,9 +1049,12 @@ int launch_gemm_cg(const void* A, const void* B, void* C, int M, int N, int K, i
     const int extra = EPI == 3 ? kNoiseTableBytes + 2 * kBM * kMaxChunks * 4 + kBM * 8 +
                                      (CG == 1 ? g.a_rows * BN * 2 : 0)
                                : 0;
-    const int ring = EPI == 3 ? kMaxSmem - 1024 - kBarBytes - extra : kRingBudget;
+    // The ring takes the opt-in shared memory left after the 1 KiB alignment
+    // pad, the barriers and (non-selection epilogues) up to 1 KiB of the
+    // kernel's static shared memory.
+    const int ring = EPI == 3 ? kMaxSmem - 1024 - kBarBytes - extra : kMaxSmem - 2048 - kBarBytes;
     const long long work = static_cast<long long>((M + kBM * CG - 1) / (kBM * CG)) * ((N + BN - 1) / BN);
-    const int smem_max = EPI == 3 ? kMaxSmem : 1024 + kRingBudget + kBarBytes;
+    const int smem_max = EPI == 3 ? kMaxSmem : kMaxSmem - 1024;
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return cuda_status(de);
