@@ -148,7 +148,8 @@ def test_gemm_tile_width_does_not_change_bits():
         assert same_bits(outs[bn], outs[256]), bn
 
 
-@pytest.mark.parametrize("M,F,K", [(64, 2816, 1024), (1, 48, 64), (130, 1024, 200), (300, 112, 136)])
+@pytest.mark.parametrize("M,F,K", [(64, 2816, 1024), (1, 48, 64), (130, 1024, 200), (300, 112, 136),
+                                   (300, 1040, 256)])            # the last: 256-row CTA-pair tiles
 def test_gemm_swiglu_equals_gemm_then_silu(M, F, K):
     g = synth.generator(M + F + K)
     A = dev(synth.bf16_normal((M, K), 1.0, g))
@@ -622,7 +623,7 @@ def _fused_vs_unfused(A, Bw, T, seed=SEED, write_logits=True):
 @pytest.mark.parametrize("M,N,K,T,std", [
     (64, 32000, 1024, 0.7, 0.02), (1, 2048, 256, 1.0, 1.0 / 16), (7, 4104, 192, 0.5, 0.1),
     (130, 5000, 512, 0.7, 0.05), (64, 32000, 1024, 0.0, 0.02), (300, 2056, 136, 2.0, 0.2),
-    (16, 152064, 256, 0.7, 0.2)])
+    (16, 152064, 256, 0.7, 0.2), (1000, 8200, 256, 0.7, 0.1), (600, 4104, 320, 0.0, 0.1)])
 def test_lm_head_gumbel_fused_bit_exact(M, N, K, T, std):
     g = synth.generator(M + N + K)
     A = synth.bf16_normal((M, K), 1.0, g).cuda()
@@ -632,8 +633,9 @@ def test_lm_head_gumbel_fused_bit_exact(M, N, K, T, std):
     assert np.array_equal(tok, ref)
 
 
-def test_lm_head_gumbel_fused_peaked_ties_and_nan():
-    M, N, K = 48, 8192, 256
+@pytest.mark.parametrize("M", [48, 300])          # one CTA per 128-row tile / CTA pairs
+def test_lm_head_gumbel_fused_peaked_ties_and_nan(M):
+    N, K = 8192, 256
     g = synth.generator(4242)
     A = synth.bf16_normal((M, K), 1.0, g)
     Bw = synth.bf16_normal((N, K), 0.05, g)
