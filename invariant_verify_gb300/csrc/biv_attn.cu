@@ -774,7 +774,7 @@ BIV_DEV bool wg_sync_or(int wg, bool v) {
 __global__ void __launch_bounds__(kPPThreads, 1)
 attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                const __grid_constant__ CUtensorMap tmK2, const __grid_constant__ CUtensorMap tmV2,
-               const AttnParams P) {
+               const __grid_constant__ CUtensorMap tmQ, const AttnParams P) {
     constexpr int M = 64;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -795,10 +795,9 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     int* s_rpos = s_gmin + n_tiles;
     int* s_wsum = s_rpos + P.W;
 
-    __shared__ __align__(8) uint64_t kbar[2][2], vbar[2][2], sbar[2], obar[2];
+    __shared__ __align__(8) uint64_t kbar[2][2], vbar[2][2], qbar[2], sbar[2], obar[2];
     __shared__ uint32_t s_tmem;
     __shared__ int abort_flag;
-    __shared__ int s_pos[2][M];
     __shared__ float s_mx[2][2][M], s_sum[2][2][M];
 
     if (threadIdx.x == 0) {
@@ -808,6 +807,7 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 mbar_init(&kbar[g][i], 1);
                 mbar_init(&vbar[g][i], 1);
             }
+            mbar_init(&qbar[g], 1);
             mbar_init(&sbar[g], 1);
             mbar_init(&obar[g], 1);
         }
@@ -822,6 +822,7 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         prefetch_tensormap(&tmV);
         prefetch_tensormap(&tmK2);
         prefetch_tensormap(&tmV2);
+        prefetch_tensormap(&tmQ);
     }
     tc_fence_before();
     // The tables read only the window's slots and positions (inputs of the
@@ -834,9 +835,9 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
     uint64_t* kb = kbar[wg];
     uint64_t* vb = vbar[wg];
-    uint32_t k_use[2] = {0u, 0u}, v_use[2] = {0u, 0u}, s_use = 0u, o_use = 0u;
-    uint32_t k_iss[2] = {0u, 0u}, v_iss[2] = {0u, 0u}, s_iss = 0u, o_iss = 0u;
-    uint32_t k_seen[2] = {0u, 0u}, v_seen[2] = {0u, 0u}, s_seen = 0u, o_seen = 0u;
+    uint32_t k_use[2] = {0u, 0u}, v_use[2] = {0u, 0u}, s_use = 0u, o_use = 0u, q_use = 0u;
+    uint32_t k_iss[2] = {0u, 0u}, v_iss[2] = {0u, 0u}, s_iss = 0u, o_iss = 0u, q_iss = 0u;
+    uint32_t k_seen[2] = {0u, 0u}, v_seen[2] = {0u, 0u}, s_seen = 0u, o_seen = 0u, q_seen = 0u;
     uint32_t early = 0;
 
     auto n_keys_of = [&](const TcItem& it) { return min(SPLIT, it.maxpos + 1 - it.split * SPLIT); };
@@ -850,28 +851,19 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         tma_load_3d(dst, nkh == 2 ? map2 : map, bar, 0, kv_row_of(it), 0, policy_evict_first());
         ++iss;
     };
-    // the warpgroup's threads: the item's Q rows into region B (K-major, 128-byte
-    // swizzle); thread x copies 16-byte piece x % 16 of tile rows x / 16 + 16 j
-    const int q_c = wt & 15, q_t0 = wt >> 4;
-    const uint32_t q_dst0 = uB + (q_c >> 3) * (M * 128) + q_t0 * 128 + (((q_c & 7) ^ (q_t0 & 7)) << 4);
-    const int q_di = 16 / P.G, q_dg = 16 % P.G;
-    const int q_i0 = q_t0 / P.G, q_g0 = q_t0 % P.G;
+    // warpgroup thread 0: the item's Q tile into region B as two 4-D boxes,
+    // one per 64-dim half ([tile rows][G heads][128 B]: tile row i * G + g,
+    // K-major, 128-byte swizzle, the halves M * 128 B apart as the S MMA reads
+    // them); rows past the window are zero-filled, rows of the next group are
+    // loaded but never used.
+    const uint32_t q_bytes = static_cast<uint32_t>(P.tile_rows * P.G * HD * 2);
     auto load_q = [&](const TcItem& it) {
         int row0, nr;
         tile_rows_of(P, it.tile, row0, nr);
-        const int T = nr * P.G;
-        const __nv_bfloat16* base = P.q + (static_cast<long long>(row0) * P.Hq + it.kvh * P.G) * HD + q_c * 8;
-        int i = q_i0, g = q_g0;
-        for (int t = q_t0, j = 0; t < T; t += 16, ++j) {
-            cp_async16(q_dst0 + static_cast<uint32_t>(j) * 2048u, base + (static_cast<long long>(i) * P.Hq + g) * HD);
-            i += q_di;
-            g += q_dg;
-            if (g >= P.G) {
-                g -= P.G;
-                ++i;
-            }
-        }
-        cp_async_commit();
+        mbar_arrive_expect_tx(&qbar[wg], q_bytes);
+        tma_load_4d(sB, &tmQ, &qbar[wg], 0, it.kvh * P.G, row0, 0, policy_evict_first());
+        tma_load_4d(sB + M * 128, &tmQ, &qbar[wg], 0, it.kvh * P.G, row0, 1, policy_evict_first());
+        ++q_iss;
     };
     auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&abort_flag) != 0; };
     auto take = [&](uint64_t* bar, uint32_t use, uint32_t& seen) {
@@ -895,8 +887,8 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
     pdl_wait();
     pdl_trigger();
-    if (item < n_work) {
-        if (wt == 0 && !early) load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], cur);
+    if (item < n_work && wt == 0) {
+        if (!early) load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], cur);
         load_q(cur);
     }
     const float sl2 = P.scale_log2;
@@ -914,24 +906,15 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         int row0, nr;
         tile_rows_of(P, cur.tile, row0, nr);
         const int T = nr * P.G;
-        if (wt < nr) s_pos[wg][wt] = s_rpos[row0 + wt];
         const long long nxt_item = item + step;
         const bool has_nxt = nxt_item < n_work;
         TcItem nxt = {};
         if (has_nxt) nxt = tc_decode(P, true, nxt_item, s_pref, s_tmax, s_slot0);
 
-        // ---- Q landed (cp.async) and visible to the tensor core; s_pos published
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (wg_sync_or(wg, aborted())) {
-            ok = false;
-            break;
-        }
-        tc_fence_after();
-        // ---- S = Q K^T by the warpgroup's first warp (one elected lane)
+        // ---- S = Q K^T by the warpgroup's first warp (one elected lane), once
+        // the item's Q and K boxes have landed
         if (w8 == 0) {
-            bool got = take(&kb[0], k_use[0], k_seen[0]);
+            bool got = take(&qbar[wg], q_use, q_seen) && take(&kb[0], k_use[0], k_seen[0]);
             got = __all_sync(0xffffffffu, got);
             if (got) {
                 tc_fence_after();
@@ -954,6 +937,7 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             ++s_iss;
         }
         ++k_use[0];
+        ++q_use;
         if (mbar_wait(&sbar[wg], s_use & 1u, &abort_flag, &g_attn_err) && wt == 0) ++s_seen;
         ++s_use;
         tc_fence_after();
@@ -961,7 +945,7 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         if (wt == 0 && !aborted()) load_box(&tmV, &tmV2, sA, &vb[0], v_iss[0], cur);
         // ---- softmax over the split; the thread's 64 scores (keys 128 ch + 32 i
         // + 16 hi + t) stay in registers from one round of loads until P is written
-        const int pos = r < T ? s_pos[wg][r / P.G] : -1;
+        const int pos = r < T ? s_rpos[row0 + r / P.G] : -1;     // the row's usable position (table)
         float mraw = -INFINITY;
         uint32_t sv[4][16];
 #pragma unroll
@@ -1041,11 +1025,9 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         ++o_use;
         tc_fence_after();
         // ---- P and V consumed: the next item's K and Q
-        if (has_nxt && !aborted()) {
-            if (wt == 0) {
-                fence_proxy_async_smem();
-                load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], nxt);
-            }
+        if (has_nxt && !aborted() && wt == 0) {
+            fence_proxy_async_smem();
+            load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], nxt);
             load_q(nxt);
         }
         // ---- the split's partial of every tile row that reaches it
@@ -1057,6 +1039,14 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < 2; ++j) tmem_ld16x2(tO + lane_base + 64 * ch + 32 * j, ov[j]);
             tmem_ld_wait();
+            // O is in registers: the TMEM columns may take the next item's S
+            // while these stores drain
+            tc_fence_before();
+            if (wg_sync_or(wg, aborted())) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 reg_fence16(ov[j]);
@@ -1074,19 +1064,13 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 P.ws_l[ph] = s_sum[wg][0][r] + s_sum[wg][1][r];
             }
         }
-        tc_fence_before();
-        if (wg_sync_or(wg, aborted())) {               // TMEM, s_mx, s_sum and s_pos are reused
-            ok = false;
-            break;
-        }
-        tc_fence_after();
         item = nxt_item;
         cur = nxt;
     }
     // ---- leave.  After a time-out, the copies and MMAs already started
     // complete first (bounded waits), then TMEM is freed.
-    cp_async_wait<0>();
     if (wt == 0 && !ok) {
+        for (uint32_t j = q_seen; j < q_iss; ++j) mbar_wait_drain(&qbar[wg], j & 1u);
         for (int kh = 0; kh < 2; ++kh) {
             for (uint32_t j = k_seen[kh]; j < k_iss[kh]; ++j) mbar_wait_drain(&kb[kh], j & 1u);
             for (uint32_t j = v_seen[kh]; j < v_iss[kh]; ++j) mbar_wait_drain(&vb[kh], j & 1u);
@@ -1369,6 +1353,23 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
         }
     }
 
+    // Q as TMA sees it for the two-item kernel: [2 dim halves][W rows][Hq
+    // heads][64 elements]; a box is one dim half of a tile: [tile rows][G
+    // heads][64], i.e. tile row i * G + g
+    CUtensorMap tq;
+    {
+        EncodeTiledFn enc = encode_fn();
+        cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(W), 2};
+        cuuint64_t strides[3] = {static_cast<cuuint64_t>(ROWB), static_cast<cuuint64_t>(Hq) * ROWB, 128};
+        cuuint32_t box[4] = {64, static_cast<cuuint32_t>(P.G), static_cast<cuuint32_t>(P.tile_rows), 1};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+            set_cuda_error(cudaErrorInvalidValue);
+            return BIV_ERR_CUDA;
+        }
+    }
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return cuda_status(de);
@@ -1407,7 +1408,7 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
     int st;
     if (P.tile_rows * P.G <= 64 && pp_smem <= kPPSmemMax)
         st = launch_pdl(attn_pp_kernel, dim3(static_cast<unsigned>(grid)), dim3(kPPThreads), pp_smem, s, tk, tv,
-                        tk2, tv2, P);
+                        tk2, tv2, tq, P);
     else if (P.tile_rows * P.G <= 64)
         st = launch_pdl(attn_tc_kernel<64>, dim3(static_cast<unsigned>(grid)), dim3(ATTN_THREADS),
                         tc_smem_bytes<64>(), s, tk, tv, tk2, tv2, P);

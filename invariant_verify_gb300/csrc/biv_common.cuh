@@ -258,6 +258,17 @@ BIV_DEV void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
                  : "memory");
 }
 
+// 4-D tiled TMA load (coordinates innermost first), completion on `bar`.
+BIV_DEV void tma_load_4d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2, int c3,
+                         uint64_t cache_policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)),
+        "l"(cache_policy)
+        : "memory");
+}
+
 BIV_DEV void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
