@@ -1088,10 +1088,10 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 // holds split s (32 at a time); the maximum and the weight sum are reduced
 // with a fixed xor butterfly, the outputs are summed in increasing split
 // order.  The CTAs are persistent (a warp takes pairs w, w + all warps, ...).
-// A warp's first row's slot and position are inputs of the call, not outputs
-// of the split kernel, so they are read while it finishes; after it, one
-// round of loads fetches every lane's (m, l) and the first kCombinePre
-// splits' outputs together.
+// Slots and positions are inputs of the call, not outputs of the split
+// kernel, so the lanes read those of the warp's next 32 pairs while it
+// finishes; per pair one round of loads then fetches every lane's (m, l) and
+// the first kCombinePre splits' outputs together.
 constexpr int kCombinePre = 8;
 
 struct CombineRow {
@@ -1110,12 +1110,21 @@ attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
     const long long first = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const long long stride = static_cast<long long>(gridDim.x) * 8;
     const int lane = threadIdx.x & 31;
-    CombineRow rw = first < n_pairs ? combine_row(P, first) : CombineRow{-1, -1, -1};
+    // Lane i holds the row of the warp's pair first + i * stride (32 at a time).
+    CombineRow mine = first + lane * stride < n_pairs ? combine_row(P, first + lane * stride)
+                                                      : CombineRow{-1, -1, -1};
     pdl_wait();
     pdl_trigger();
+    int k = 0;
 #pragma unroll 1
-    for (long long pair = first; pair < n_pairs; pair += stride) {
-        if (pair != first) rw = combine_row(P, pair);
+    for (long long pair = first; pair < n_pairs; pair += stride, ++k) {
+        if (k == 32) {
+            k = 0;
+            const long long pl = pair + lane * stride;
+            mine = pl < n_pairs ? combine_row(P, pl) : CombineRow{-1, -1, -1};
+        }
+        const CombineRow rw{__shfl_sync(0xffffffffu, mine.slot, k), __shfl_sync(0xffffffffu, mine.pos, k),
+                            __shfl_sync(0xffffffffu, mine.slot0, k)};
         __nv_bfloat16* dst = out + pair * HD + lane * 4;
         const int p = rw.pos;
         if (rw.slot < 0 || rw.slot >= P.n_slots || p < 0 || p >= P.max_len || rw.slot != rw.slot0) {
@@ -1152,18 +1161,25 @@ attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
             L += lw;
             const int cnt = min(32, ns - s0);
             const float4* src = src0 + static_cast<long long>(s0) * (HD / 4);
-#pragma unroll 4
-            for (int j = 0; j < cnt; ++j) {
-                const float wj = __shfl_sync(0xffffffffu, wgt, j);
-                float4 v;
-                if (s0 == 0 && j < kCombinePre) {
-                    v = pre[0];
+            int j = 0;
+            if (s0 == 0) {
+                // the prefetched splits, indexed statically (warp-uniform guard)
 #pragma unroll
-                    for (int q = 1; q < kCombinePre; ++q)
-                        if (j == q) v = pre[q];
-                } else {
-                    v = src[static_cast<long long>(j) * (HD / 4)];
+                for (int q = 0; q < kCombinePre; ++q) {
+                    if (q < cnt) {
+                        const float wj = __shfl_sync(0xffffffffu, wgt, q);
+                        acc.x += wj * pre[q].x;
+                        acc.y += wj * pre[q].y;
+                        acc.z += wj * pre[q].z;
+                        acc.w += wj * pre[q].w;
+                    }
                 }
+                j = kCombinePre;
+            }
+#pragma unroll 4
+            for (; j < cnt; ++j) {
+                const float wj = __shfl_sync(0xffffffffu, wgt, j);
+                const float4 v = src[static_cast<long long>(j) * (HD / 4)];
                 acc.x += wj * v.x;
                 acc.y += wj * v.y;
                 acc.z += wj * v.z;
