@@ -673,11 +673,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     reg_fence16(ov[j]);
                     const uint32_t* v = ov[j];
                     if (pos >= key0) {
-                        float4* d4 = reinterpret_cast<float4*>(dst + 64 * ch + 32 * j + 16 * hi);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                        st_global_v8(dst + 64 * ch + 32 * j + 16 * hi, v);
+                        st_global_v8(dst + 64 * ch + 32 * j + 16 * hi + 8, v + 8);
                     }
                 }
             } else {
@@ -687,11 +684,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     uint32_t v[32];
                     tmem_ld32_sync(tO + lane_base + c, v);
                     if (pos >= key0) {
-                        float4* d4 = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                        for (int q = 0; q < 4; ++q) st_global_v8(dst + c + 8 * q, v + 8 * q);
                     }
                 }
             }
@@ -798,6 +792,7 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __shared__ __align__(8) uint64_t kbar[2][2], vbar[2][2], qbar[2], sbar[2], obar[2];
     __shared__ uint32_t s_tmem;
     __shared__ int abort_flag;
+    __shared__ uint32_t s_qiss[2];
     __shared__ float s_mx[2][2][M], s_sum[2][2][M];
 
     if (threadIdx.x == 0) {
@@ -887,10 +882,8 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
     pdl_wait();
     pdl_trigger();
-    if (item < n_work && wt == 0) {
-        if (!early) load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], cur);
-        load_q(cur);
-    }
+    if (item < n_work && wt == 0 && !early) load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], cur);
+    if (item < n_work && wt == 32) load_q(cur);
     const float sl2 = P.scale_log2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
     const int r = 16 * q4 + (lane & 15);              // the thread's tile row
@@ -1024,11 +1017,14 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         if (mbar_wait(&obar[wg], o_use & 1u, &abort_flag, &g_attn_err) && wt == 0) ++o_seen;
         ++o_use;
         tc_fence_after();
-        // ---- P and V consumed: the next item's K and Q
-        if (has_nxt && !aborted() && wt == 0) {
+        // ---- P and V consumed: the next item's K and Q, issued by two
+        // threads of two warps (an issue waits while the copy engine is busy)
+        if (has_nxt && !aborted() && (wt == 0 || wt == 32)) {
             fence_proxy_async_smem();
-            load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], nxt);
-            load_q(nxt);
+            if (wt == 0)
+                load_box(&tmK, &tmK2, sA, &kb[0], k_iss[0], nxt);
+            else
+                load_q(nxt);
         }
         // ---- the split's partial of every tile row that reaches it
         {
@@ -1052,11 +1048,8 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                 reg_fence16(ov[j]);
                 const uint32_t* v = ov[j];
                 if (pos >= key0) {
-                    float4* d4 = reinterpret_cast<float4*>(dst + 64 * ch + 32 * j + 16 * hi);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    st_global_v8(dst + 64 * ch + 32 * j + 16 * hi, v);
+                    st_global_v8(dst + 64 * ch + 32 * j + 16 * hi + 8, v + 8);
                 }
             }
             if (pos >= key0 && ch == 0 && hi == 0) {
@@ -1068,9 +1061,14 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         cur = nxt;
     }
     // ---- leave.  After a time-out, the copies and MMAs already started
-    // complete first (bounded waits), then TMEM is freed.
+    // complete first (bounded waits), then TMEM is freed.  (ok is uniform
+    // over the warpgroup; thread 32 issued the Q boxes, thread 0 saw them land.)
+    if (!ok) {
+        if (wt == 32) s_qiss[wg] = q_iss;
+        asm volatile("bar.sync %0, 256;" ::"r"(1 + wg) : "memory");
+    }
     if (wt == 0 && !ok) {
-        for (uint32_t j = q_seen; j < q_iss; ++j) mbar_wait_drain(&qbar[wg], j & 1u);
+        for (uint32_t j = q_seen; j < s_qiss[wg]; ++j) mbar_wait_drain(&qbar[wg], j & 1u);
         for (int kh = 0; kh < 2; ++kh) {
             for (uint32_t j = k_seen[kh]; j < k_iss[kh]; ++j) mbar_wait_drain(&kb[kh], j & 1u);
             for (uint32_t j = v_seen[kh]; j < v_iss[kh]; ++j) mbar_wait_drain(&vb[kh], j & 1u);
@@ -1292,7 +1290,7 @@ using namespace biv;
 extern "C" size_t biv_decode_attn_workspace_size(int W, int Hq, int max_len) {
     if (W <= 0 || Hq <= 0 || max_len <= 0) return 0;
     const long long pairs = static_cast<long long>(W) * Hq * splits_for(max_len);
-    return static_cast<size_t>(pairs) * (HD + 2) * sizeof(float);
+    return static_cast<size_t>(pairs) * (HD + 2) * sizeof(float) + 16;   // + room to align the partials to 32 B
 }
 
 extern "C" int biv_gqa_max_drafts(int G, int tile) {
@@ -1323,7 +1321,8 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
     P.row_slot = row_slot;
     P.row_pos = row_pos;
     const long long pairs = static_cast<long long>(W) * Hq * s_max;
-    P.ws_o = static_cast<float*>(workspace);
+    // partial outputs 32-byte aligned (whole-sector stores)
+    P.ws_o = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(workspace) + 31) & ~static_cast<uintptr_t>(31));
     P.ws_m = P.ws_o + pairs * HD;
     P.ws_l = P.ws_m + pairs;
     P.W = W;

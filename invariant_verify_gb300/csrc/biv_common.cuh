@@ -503,6 +503,15 @@ BIV_DEV void tmem_ld16x2(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// Eight 32-bit words to global memory in one 32-byte store (p 32-byte aligned):
+// a whole sector per thread where a row-per-lane layout scatters a warp's
+// stores over many rows.
+BIV_DEV void st_global_v8(void* p, const uint32_t* v) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 BIV_DEV void reg_fence16(uint32_t (&r)[16]) {
     asm volatile(""
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),

@@ -96,8 +96,9 @@ def test_gemm_tile_width_rule(lib):
 
 def test_attention_validation_and_workspace(lib):
     ws = lib.biv_decode_attn_workspace_size
-    assert ws(64, 8, 2304) == 64 * 8 * 9 * 130 * 4
-    assert ws(1, 1, 1) == 1 * 1 * 1 * 130 * 4
+    # partials (hd floats) + max + sum per (row, head, split), + 16 B to align the partials to 32 B
+    assert ws(64, 8, 2304) == 64 * 8 * 9 * 130 * 4 + 16
+    assert ws(1, 1, 1) == 1 * 1 * 1 * 130 * 4 + 16
     assert ws(0, 8, 100) == 0
     f = lib.biv_decode_attn_fixedsplit
     args = lambda **kw: [kw.get(k, v) for k, v in [
