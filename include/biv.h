@@ -226,8 +226,8 @@ int biv_rope_kv_write(const void* qkv, void* q_out, void* k_cache, void* v_cache
  * biv_rope_kv_write (same rows_keep rule, same index checks), without the
  * round trip of the projection through memory.  B_packed is W_qkv
  * ([(Hq + 2 Hkv) hd, d] nn.Linear layout) rearranged once by
- * biv_rope_pack_qkv_weights so that each 16 output columns of a q or k head
- * hold 8 rotation pairs.  A: bf16 [W, d]; q_out: bf16 [W, Hq, hd]; caches:
+ * biv_rope_pack_qkv_weights so that each 16 output columns of the q and k
+ * part hold 8 rotation pairs of one head.  A: bf16 [W, d]; q_out: bf16 [W, Hq, hd]; caches:
  * bf16 [n_slots, Hkv, max_len, hd]; qkv_out: optional bf16 [W, (Hq+2Hkv) hd]
  * receiving the unrotated projection in the original column order (NULL to
  * skip).  Requires hd % 16 == 0, hd <= 256, d % 8 == 0, Hq % Hkv == 0,
@@ -237,10 +237,11 @@ int biv_gemm_qkv_rope(const void* A, const void* B_packed, void* q_out, void* k_
                       int W, int K, int d, int Hq, int Hkv, int hd, int n_slots, int max_len, float theta,
                       biv_stream_t stream);
 
-/* Rearrange W_qkv (bf16 [(Hq + 2 Hkv) hd, K]) for biv_gemm_qkv_rope: within
- * each q or k head, packed rows 16 g .. 16 g + 7 are dims 8 g .. 8 g + 7 and
- * rows 16 g + 8 .. 16 g + 15 are dims hd/2 + 8 g .. hd/2 + 8 g + 7; v rows
- * unchanged.  w_packed must not alias w_qkv.                              */
+/* Rearrange W_qkv (bf16 [(Hq + 2 Hkv) hd, K]) for biv_gemm_qkv_rope: the
+ * q and k rows (heads h = 0 .. Hq + Hkv - 1, q heads first) are packed as
+ * [g][h][16] for frequency groups g = 0 .. hd/16 - 1: packed rows e = 0..7 of
+ * (g, h) are head h's dims 8 g + e, rows e = 8..15 its dims hd/2 + 8 g + e - 8;
+ * v rows unchanged.  w_packed must not alias w_qkv.                       */
 int biv_rope_pack_qkv_weights(const void* w_qkv, void* w_packed, int Hq, int Hkv, int hd, int K,
                               biv_stream_t stream);
 

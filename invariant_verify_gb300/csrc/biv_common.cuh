@@ -576,13 +576,23 @@ BIV_DEV float rope_inv_freq(int i, int hd, float theta) {
     return powf(theta, -2.0f * static_cast<float>(i) / static_cast<float>(hd));
 }
 
-// One RoPE pair (a, b) at position pos with the pair's frequency given.
-BIV_DEV void rope_pair_f(float a, float b, int pos, float inv_freq, __nv_bfloat16& o1, __nv_bfloat16& o2) {
-    const float ang = static_cast<float>(pos) * inv_freq;
-    float sn, cs;
+// The rotation angle of pair frequency inv_freq at position pos, as sine and cosine.
+BIV_DEV void rope_sincos(int pos, float inv_freq, float& sn, float& cs) {
+    const float ang = __fmul_rn(static_cast<float>(pos), inv_freq);
     sincosf(ang, &sn, &cs);
+}
+
+// One RoPE pair (a, b) rotated by the angle with the given sine and cosine.
+BIV_DEV void rope_rotate(float a, float b, float sn, float cs, __nv_bfloat16& o1, __nv_bfloat16& o2) {
     o1 = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, cs), __fmul_rn(b, sn)));
     o2 = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, cs), __fmul_rn(a, sn)));
+}
+
+// One RoPE pair (a, b) at position pos with the pair's frequency given.
+BIV_DEV void rope_pair_f(float a, float b, int pos, float inv_freq, __nv_bfloat16& o1, __nv_bfloat16& o2) {
+    float sn, cs;
+    rope_sincos(pos, inv_freq, sn, cs);
+    rope_rotate(a, b, sn, cs, o1, o2);
 }
 
 BIV_DEV void rope_pair(float a, float b, int pos, int i, int hd, float theta, __nv_bfloat16& o1,

@@ -144,9 +144,12 @@ BIV_DEV bool epilogue_all(bool v) {
 constexpr int kBucketBits = 12;
 constexpr int kBuckets = 1 << kBucketBits;
 // RoPE + KV-write epilogue (EPI 4) of the QKV projection: the weight rows are
-// rearranged (biv_rope_pack_qkv_weights) so that every 16 output columns of a
-// q or k head hold 8 rotation pairs -- dims i0..i0+7 then i0+hd/2..i0+hd/2+7,
-// i0 = 8 (col % hd / 16) -- and one thread rotates them from its own registers.
+// rearranged (biv_rope_pack_qkv_weights) so that every 16 output columns of
+// the q and k part hold 8 rotation pairs of one head -- dims i0..i0+7 then
+// i0+hd/2..i0+hd/2+7, i0 = 8 gq -- ordered frequency group first ([gq][head]
+// [16]), and one thread rotates them from its own registers.  A tile's columns
+// then span one or two frequency groups across many heads, so a thread takes
+// the sines and cosines of its row once per group, not once per head.
 struct RopeArgs {
     __nv_bfloat16* q_out;      // [M, Hq, hd]
     __nv_bfloat16* kc;         // [n_slots, Hkv, max_len, hd]
@@ -168,6 +171,20 @@ BIV_DEV void st_bf16s(__nv_bfloat16* p, const uint32_t* v) {
         *reinterpret_cast<uint2*>(p) = make_uint2(v[0], v[1]);
 }
 
+// The sines and cosines of one row's NP rotation pairs 8 gq + jb .. of
+// frequency group gq, kept while consecutive column groups share gq.
+template <int NP>
+struct RopeAngles {
+    int gq = -1;
+    float sn[NP], cs[NP];
+    BIV_DEV void at(int g, int jb, int pos, const float* inv_freq) {
+        if (g == gq) return;
+        gq = g;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) rope_sincos(pos, inv_freq[8 * g + jb + j], sn[j], cs[j]);
+    }
+};
+
 // One row's share of a 16-column group at output column col of the QKV tile:
 // f1 holds the fp32 accumulators of group columns jb .. jb + NP - 1 (first
 // halves of rotation pairs jb ..), f2 those of columns 8 + jb .. (their
@@ -175,7 +192,7 @@ BIV_DEV void st_bf16s(__nv_bfloat16* p, const uint32_t* v) {
 // q_out or the k cache; v columns go to the v cache unrotated.
 template <int NP>
 BIV_DEV void qkv_group(const uint32_t* f1, const uint32_t* f2, int jb, int col, int row, int slot, int pos,
-                       bool write_kv, const RopeArgs& rp, const float* inv_freq) {
+                       bool write_kv, const RopeArgs& rp, const float* inv_freq, RopeAngles<NP>& ang) {
     const int hd = rp.hd, half = hd / 2;
     const int qn = rp.Hq * hd, kn = rp.Hkv * hd;
     uint32_t a[NP / 2], b[NP / 2];                // bf16 pairs, as the plain GEMM stores them
@@ -186,15 +203,17 @@ BIV_DEV void qkv_group(const uint32_t* f1, const uint32_t* f2, int jb, int col, 
     }
     __nv_bfloat16* qkv_row = rp.qkv_out ? rp.qkv_out + static_cast<long long>(row) * (qn + 2 * kn) : nullptr;
     if (col < qn + kn) {
-        const bool isq = col < qn;
-        const int cc = isq ? col : col - qn;
-        const int h = cc / hd, i0 = (cc % hd) / 16 * 8 + jb;
+        const int nqk = rp.Hq + rp.Hkv;
+        const int gi = col / 16, gq = gi / nqk, hh = gi - gq * nqk;
+        const bool isq = hh < rp.Hq;
+        const int h = isq ? hh : hh - rp.Hq, i0 = 8 * gq + jb;
+        ang.at(gq, jb, pos, inv_freq);
         uint32_t o1[NP / 2], o2[NP / 2];
 #pragma unroll
         for (int j = 0; j < NP; j += 2) {
             __nv_bfloat16 a0, a1, b0, b1;
-            rope_pair_f(bf16lo(a[j / 2]), bf16lo(b[j / 2]), pos, inv_freq[i0 + j], a0, b0);
-            rope_pair_f(bf16hi(a[j / 2]), bf16hi(b[j / 2]), pos, inv_freq[i0 + j + 1], a1, b1);
+            rope_rotate(bf16lo(a[j / 2]), bf16lo(b[j / 2]), ang.sn[j], ang.cs[j], a0, b0);
+            rope_rotate(bf16hi(a[j / 2]), bf16hi(b[j / 2]), ang.sn[j + 1], ang.cs[j + 1], a1, b1);
             o1[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(a0)) |
                         (static_cast<uint32_t>(__bfloat16_as_ushort(a1)) << 16);
             o2[j / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) |
@@ -826,19 +845,27 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     if (keep && !cache_ok && jb == 0) atomicOr(&g_gemm_err, BIV_DEVERR_INDEX);
                     write_kv = keep && cache_ok;
                 }
+                if (g.m64) {
+                    RopeAngles<4> ang;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
-                    const int col = n_blk * BN + c;
-                    if (g.m64) {
+                    for (int c = 0; c < BN; c += 16) {
+                        const int col = n_blk * BN + c;
                         uint32_t ra[4], rb[4];
                         tmem_ld16x2_x4_pair_sync(taddr + static_cast<uint32_t>(c),
                                                  taddr + static_cast<uint32_t>(c + 8), ra, rb);
-                        if (plive && col < N) qkv_group<4>(ra, rb, jb, col, prow, slot, pos, write_kv, rp, inv_freq);
-                    } else {
+                        if (plive && col < N)
+                            qkv_group<4>(ra, rb, jb, col, prow, slot, pos, write_kv, rp, inv_freq, ang);
+                    }
+                } else {
+                    RopeAngles<8> ang;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 16) {
+                        const int col = n_blk * BN + c;
                         uint32_t r[16];
                         tmem_ld16(taddr + static_cast<uint32_t>(c), r);
                         tmem_ld_wait();
-                        if (live && col < N) qkv_group<8>(r, r + 8, 0, col, row, slot, pos, write_kv, rp, inv_freq);
+                        if (live && col < N)
+                            qkv_group<8>(r, r + 8, 0, col, row, slot, pos, write_kv, rp, inv_freq, ang);
                     }
                 }
             } else if constexpr (EPI == 2) {
@@ -1144,17 +1171,19 @@ __global__ void swiglu_pack_kernel(const __nv_bfloat16* __restrict__ src, __nv_b
     for (int c = threadIdx.x; c < K / 8; c += blockDim.x) out[c] = in[c];
 }
 
-// Packed row p of the QKV weight: in the q and k heads, rows 16 g .. 16 g + 7 of
-// a head are its dims 8 g .. 8 g + 7 and rows 16 g + 8 .. 16 g + 15 its dims
-// hd/2 + 8 g .. hd/2 + 8 g + 7 (the RoPE partners); the v heads are unchanged.
+// Packed row p of the QKV weight: the q and k part is [gq][head][16], head h
+// (q heads, then k heads) and frequency group gq: rows e = 0..7 are the head's
+// dims 8 gq + e, rows e = 8..15 its dims hd/2 + 8 gq + e - 8 (the RoPE
+// partners); the v heads are unchanged.
 __global__ void rope_pack_kernel(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst, int Hq,
                                  int Hkv, int hd, int K) {
     pdl_wait();
     const long long p = blockIdx.x;
     long long s = p;
     if (p < static_cast<long long>(Hq + Hkv) * hd) {
-        const int h = static_cast<int>(p / hd), j = static_cast<int>(p % hd);
-        const int gq = j / 16, e = j % 16;
+        const int nqk = Hq + Hkv;
+        const int gi = static_cast<int>(p / 16), e = static_cast<int>(p % 16);
+        const int gq = gi / nqk, h = gi - gq * nqk;
         const int dim = e < 8 ? 8 * gq + e : hd / 2 + 8 * gq + (e - 8);
         s = static_cast<long long>(h) * hd + dim;
     }
