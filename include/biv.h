@@ -266,7 +266,12 @@ int biv_rope_pack_qkv_weights(const void* w_qkv, void* w_packed, int Hq, int Hkv
  * aligned logits.  Two or more rows per SM are streamed one row per CTA
  * (rows dealt out by a counter of the library's; up to 64 such calls may
  * run at the same time); fewer rows are shared by eight-CTA clusters; both
- * give the same tokens.                                                   */
+ * give the same tokens.  When streaming with T > 0, rows on which many
+ * entries can still win (flat rows, up to R/8 of them) are finished by a
+ * second kernel over all SMs; its scratch (at most 64 MiB, about R/8 *
+ * (2 ceil(V/256) + 16 ceil(V/8192) + 16) bytes) comes from a memory pool of
+ * the library's, allocated and freed in the call's stream order
+ * (cudaMallocAsync while the stream is being captured into a graph).      */
 int biv_gumbel_argmax(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
                       const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
                       biv_stream_t stream);

@@ -356,9 +356,12 @@ gumbel_argmax_kernel(const float* __restrict__ logits, int V, long long ld, int 
 // entry by fl(fl(x * invT) + T[w >> 24]) and takes the two logs only where
 // that bound passes the best key found so far.  Entries are skipped only on
 // a bound at or below a real key of the row, so the result is exact.  On a
-// peaked row pass 2 touches a block or two; on a flat row it is bound by the
-// Philox arithmetic.  The ring runs ahead across rows: the next row's first
-// chunks land during pass 2.
+// peaked row pass 2 touches a block or two.  A flat row (most blocks live)
+// is bound by the Philox arithmetic, several times a row's streaming time on
+// one CTA while the others stream; it is handed off instead, in per-chunk
+// units, to a second kernel that runs over all SMs after this one
+// (gumbel_units_kernel).  The ring runs ahead across rows: the next row's
+// first chunks land during pass 2.
 constexpr int kStreamChunk = 8192;               // floats per ring slot (32 KiB)
 constexpr int kStreamStages = 2;
 constexpr int kBlock = 256;                      // logits per block maximum
@@ -370,6 +373,99 @@ constexpr int kCtrSlots = 64;                    // row-ticket counter pairs, on
 // every launch puts its pair back to zero.
 __device__ unsigned int g_stream_ctr[2 * kCtrSlots];
 
+// Rows whose live blocks are many (flat rows: the noise, not one large logit,
+// decides them) are handed from the streaming kernel to the unit kernel,
+// which spreads their work over every SM in 32 KiB units (one chunk of the
+// row and its live blocks).  Stream-ordered scratch of one call:
+struct HeavyRows {
+    unsigned int* ctr;         // {heavy slots taken, units registered, unit ticket} (zero at entry)
+    unsigned long long* best;  // [cap] the row's best packed key so far (LB at hand-off)
+    int* row_of;               // [cap] heavy slot -> row
+    int* remaining;            // [cap] units of the row not yet done
+    int4* units;               // [cap * n_chunks] (slot, chunk, first, end) into the live list
+    uint16_t* live;            // [cap][n_blocks] the row's live blocks, ascending
+    int cap;                   // heavy slots; 0 = no hand-off (every row done in place)
+    int min_live;              // a row with more live blocks than this is handed off
+};
+
+// Pass 2b over n_items 4-groups: item it is group it % 64 of block
+// blk_of(it >> 6); entry v is read at src + v - off.  Every thread runs the
+// same number of iterations (a CTA-wide running best is shared through
+// s_best).  Returns the thread's best packed key.
+template <int UNROLL, typename BlkOf>
+BIV_DEV unsigned long long groups_pass(const float* src, long long off, int n_items, BlkOf blk_of, int V, uint32_t pos,
+                                       uint32_t req, uint32_t seed_lo, uint32_t seed_hi, float invT, const float* gtab,
+                                       float g254, unsigned long long best, unsigned long long* s_best) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int base = 0; base < n_items; base += kSelThreads * UNROLL) {
+        float4 v4[UNROLL];
+        int v0[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int it = base + u * kSelThreads + static_cast<int>(threadIdx.x);
+            v0[u] = -1;
+            if (it < n_items) {
+                const int v = blk_of(it >> 6) * kBlock + 4 * (it & 63);
+                if (v < V) {                          // the last block may be partial
+                    v0[u] = v;
+                    v4[u] = *reinterpret_cast<const float4*>(src + (v - off));
+                }
+            }
+        }
+        // Straight-line over the UNROLL groups so their Philox chains
+        // interleave.  A bound strictly below best_f (the value of the
+        // best key) cannot win; equal or NaN-free ties go to the exact
+        // packed comparison.  While best is a NaN key (order 0: a row
+        // with no number so far) nothing is pruned.
+        const bool no_prune = (best >> 32) == 0;
+        const float best_f = order_to_float(static_cast<uint32_t>(best >> 32));
+        U4 w[UNROLL];
+        bool glive[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const float m4 = fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w));
+            glive[u] = v0[u] >= 0 && (no_prune || __fadd_rn(__fmul_rn(m4, invT), kNoiseBound) >= best_f);
+            w[u] = philox4x32_10(static_cast<uint32_t>(max(v0[u], 0)) >> 2, pos, req, 0u, seed_lo, seed_hi);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            if (!glive[u]) continue;
+            const float e[4] = {v4[u].x, v4[u].y, v4[u].z, v4[u].w};
+            const uint32_t words[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+            // Below the top byte 255 no noise exceeds g254: if even the
+            // group's largest logit cannot pass with it, only entries
+            // whose word has top byte 255 need their own bound.
+            const float m4 = fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w));
+            const bool top_only = !no_prune && __fadd_rn(__fmul_rn(m4, invT), g254) < best_f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (top_only && words[j] < 0xFF000000u) continue;
+                const float a = __fmul_rn(e[j], invT);
+                if (!no_prune && !(__fadd_rn(a, gtab[words[j] >> 24]) >= best_f)) continue;
+                const uint32_t vv = static_cast<uint32_t>(v0[u] + j);
+                best = umax64(best, pack_key(__fadd_rn(a, gumbel_from_word(words[j])), vv));
+            }
+        }
+        // share the bound: warp maximum, then the CTA's running maximum
+        best = warp_max64(best);
+        if (lane == 0) atomicMax(s_best, best);
+        best = umax64(best, *reinterpret_cast<volatile unsigned long long*>(s_best));
+    }
+    return best;
+}
+
+// First index i in the ascending list[0 .. n) with list[i] >= key.
+BIV_DEV int lower_bound_int(const int* list, int n, int key) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (list[mid] < key) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+
 size_t stream_smem_bytes(int V) {
     return static_cast<size_t>(kStreamStages) * kStreamChunk * 4 + static_cast<size_t>((V + kBlock - 1) / kBlock) * 4;
 }
@@ -378,7 +474,7 @@ __global__ void __launch_bounds__(kSelThreads, 3)
 gumbel_stream_kernel(const float* __restrict__ logits, int R, int V, long long ld,
                      const uint32_t* __restrict__ row_req, const int32_t* __restrict__ row_pos, uint32_t seed_lo,
                      uint32_t seed_hi, float invT, int greedy, int32_t* __restrict__ tokens,
-                     unsigned int* __restrict__ ctr, const __grid_constant__ NoiseBounds nb) {
+                     unsigned int* __restrict__ ctr, const __grid_constant__ NoiseBounds nb, const HeavyRows hv) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     float* ring = reinterpret_cast<float*>(smem_raw);                                     // [stages][chunk]
     float* bmax = reinterpret_cast<float*>(smem_raw + kStreamStages * kStreamChunk * 4);  // [ceil(V / 256)]
@@ -388,6 +484,7 @@ gumbel_stream_kernel(const float* __restrict__ logits, int R, int V, long long l
     __shared__ unsigned long long s_best;                    // pass 2: best key any warp has found
     __shared__ int wcount[kSelThreads / 32];
     __shared__ int s_rows[8];                                // row of stream ordinal i at [i % 8]
+    __shared__ int s_heavy, s_unit0;                         // hand-off: heavy slot, first unit
     int* live_list = reinterpret_cast<int*>(bmax);           // pass 2: live blocks, written over bmax
     __shared__ float gtab[256];
     __shared__ int abort_flag;
@@ -529,64 +626,57 @@ gumbel_stream_kernel(const float* __restrict__ logits, int R, int V, long long l
                 n_live += total_w;
                 __syncthreads();
             }
+            // ---- a row with many live blocks goes to the unit kernel: its live
+            // list, one unit per chunk that holds live blocks, its state.  (The
+            // slot is taken by thread 0 and broadcast; past the scratch's
+            // capacity the row is done here.)
+            if (hv.cap > 0 && n_live > hv.min_live) {
+                if (threadIdx.x == 0) s_heavy = static_cast<int>(atomicAdd(&hv.ctr[0], 1u));
+                __syncthreads();
+                const int h = s_heavy;
+                if (h < hv.cap) {
+                    for (int i = static_cast<int>(threadIdx.x); i < n_live; i += kSelThreads)
+                        hv.live[static_cast<long long>(h) * n_blocks + i] = static_cast<uint16_t>(live_list[i]);
+                    constexpr int bpc = kStreamChunk / kBlock;   // blocks per chunk
+                    int n_units = 0;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < n_chunks; c0 += kSelThreads) {
+                        const int c = c0 + static_cast<int>(threadIdx.x);
+                        int lo = 0, hi = 0;
+                        if (c < n_chunks) {
+                            lo = lower_bound_int(live_list, n_live, c * bpc);
+                            hi = lower_bound_int(live_list, n_live, (c + 1) * bpc);
+                        }
+                        const bool has = hi > lo;
+                        const unsigned bal = __ballot_sync(0xffffffffu, has);
+                        if (lane == 0) wcount[warp] = __popc(bal);
+                        __syncthreads();
+                        int before = 0, total_w = 0;
+#pragma unroll
+                        for (int i = 0; i < kSelThreads / 32; ++i) {
+                            before += i < warp ? wcount[i] : 0;
+                            total_w += wcount[i];
+                        }
+                        if (threadIdx.x == 0)
+                            s_unit0 = static_cast<int>(atomicAdd(&hv.ctr[1], static_cast<unsigned>(total_w)));
+                        __syncthreads();
+                        if (has) hv.units[s_unit0 + before + __popc(bal & ((1u << lane) - 1u))] = make_int4(h, c, lo, hi);
+                        n_units += total_w;
+                        __syncthreads();                  // wcount and s_unit0 are reused
+                    }
+                    if (threadIdx.x == 0) {
+                        hv.best[h] = best;
+                        hv.row_of[h] = row;
+                        hv.remaining[h] = n_units;
+                    }
+                    __syncthreads();                      // the live list (over bmax) is read
+                    continue;                             // the unit kernel writes the token
+                }
+            }
             // ---- pass 2b: the 4-groups of the live blocks, all threads, kUnroll
             // loads in flight per thread; 32 consecutive items share a block.
-            const int n_items = n_live * (kBlock / 4);
-#pragma unroll 1
-            for (int base = 0; base < n_items; base += kSelThreads * kUnroll) {
-                float4 v4[kUnroll];
-                int v0[kUnroll];
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int it = base + u * kSelThreads + static_cast<int>(threadIdx.x);
-                    v0[u] = -1;
-                    if (it < n_items) {
-                        const int v = live_list[it >> 6] * kBlock + 4 * (it & 63);
-                        if (v < V) {                          // the last block may be partial
-                            v0[u] = v;
-                            v4[u] = *reinterpret_cast<const float4*>(x + v);
-                        }
-                    }
-                }
-                // Straight-line over the kUnroll groups so their Philox chains
-                // interleave.  A bound strictly below best_f (the value of the
-                // best key) cannot win; equal or NaN-free ties go to the exact
-                // packed comparison.  While best is a NaN key (order 0: a row
-                // with no number so far) nothing is pruned.
-                const bool no_prune = (best >> 32) == 0;
-                const float best_f = order_to_float(static_cast<uint32_t>(best >> 32));
-                U4 w[kUnroll];
-                bool glive[kUnroll];
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const float m4 = fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w));
-                    glive[u] = v0[u] >= 0 && (no_prune || __fadd_rn(__fmul_rn(m4, invT), kNoiseBound) >= best_f);
-                    w[u] = philox4x32_10(static_cast<uint32_t>(max(v0[u], 0)) >> 2, pos, req, 0u, seed_lo, seed_hi);
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    if (!glive[u]) continue;
-                    const float e[4] = {v4[u].x, v4[u].y, v4[u].z, v4[u].w};
-                    const uint32_t words[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-                    // Below the top byte 255 no noise exceeds g254: if even the
-                    // group's largest logit cannot pass with it, only entries
-                    // whose word has top byte 255 need their own bound.
-                    const float m4 = fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w));
-                    const bool top_only = !no_prune && __fadd_rn(__fmul_rn(m4, invT), g254) < best_f;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (top_only && words[j] < 0xFF000000u) continue;
-                        const float a = __fmul_rn(e[j], invT);
-                        if (!no_prune && !(__fadd_rn(a, gtab[words[j] >> 24]) >= best_f)) continue;
-                        const uint32_t vv = static_cast<uint32_t>(v0[u] + j);
-                        best = umax64(best, pack_key(__fadd_rn(a, gumbel_from_word(words[j])), vv));
-                    }
-                }
-                // share the bound: warp maximum, then the CTA's running maximum
-                best = warp_max64(best);
-                if (lane == 0) atomicMax(&s_best, best);
-                best = umax64(best, *reinterpret_cast<volatile unsigned long long*>(&s_best));
-            }
+            best = groups_pass<kUnroll>(x, 0, n_live * (kBlock / 4), [&](int i) { return live_list[i]; }, V, pos, req,
+                                        seed_lo, seed_hi, invT, gtab, g254, best, &s_best);
             best = block_max64(best, red);              // also orders pass 2's reads of bmax before the next row
         }
         if (threadIdx.x == 0)
@@ -607,6 +697,156 @@ gumbel_stream_kernel(const float* __restrict__ logits, int R, int V, long long l
             __threadfence();
         }
     }
+}
+
+// ------------------------------------------------------------ unit kernel
+// The heavy rows' units (see HeavyRows).  Warps 0-7 compute; warp 8 is the
+// producer: it draws unit tickets, reads a unit's descriptor, row and live
+// blocks into a slot's metadata, copies the unit's chunk into the slot's
+// ring buffer (full barrier), and, once the compute warps release the slot
+// (empty barrier, one arrival per warp), raises the row's best key with the
+// unit's result by a 64-bit atomic maximum -- the unit that brings the row's
+// count of units to zero writes its token.  The compute warps run pass 2b
+// over the unit's live blocks from shared memory, starting from the row's
+// best key when the unit was drawn.  Global latency stays with the producer.
+// Exact for the same reason as the streaming kernel: only entries whose bound
+// stays below a real key of the row are skipped.
+constexpr int kUStages = 3;
+constexpr int kUThreads = kSelThreads + 32;
+
+struct UnitMeta {
+    int h, c, n_lb, row;
+    uint32_t req, pos;
+};
+
+size_t unit_smem_bytes() { return static_cast<size_t>(kUStages) * kStreamChunk * 4; }
+
+__global__ void __launch_bounds__(kUThreads, 2)
+gumbel_units_kernel(const float* __restrict__ logits, int V, long long ld, const uint32_t* __restrict__ row_req,
+                    const int32_t* __restrict__ row_pos, uint32_t seed_lo, uint32_t seed_hi, float invT,
+                    int32_t* __restrict__ tokens, const __grid_constant__ NoiseBounds nb, const HeavyRows hv) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    float* ring = reinterpret_cast<float*>(smem_raw);    // [kUStages][chunk]
+    __shared__ uint64_t full[kUStages], empty[kUStages];
+    __shared__ UnitMeta meta[kUStages];                  // h < 0: no more units
+    __shared__ int blk[kUStages][kStreamChunk / kBlock];
+    __shared__ unsigned long long best0[kUStages];       // the running best of the slot's unit
+    __shared__ unsigned long long res[kUStages];         // the slot's unit result, for the producer
+    __shared__ unsigned long long red[kUStages][kSelThreads / 32];
+    __shared__ float gtab[256];
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < kUStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kSelThreads / 32);
+        }
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 256) gtab[threadIdx.x] = nb.v[threadIdx.x];
+    const float g254 = nb.v[254];
+    __syncthreads();
+    pdl_wait();                                          // the hand-offs of the streaming kernel
+    pdl_trigger();
+    const int n_blocks = (V + kBlock - 1) / kBlock;
+    if (warp == kSelThreads / 32) {
+        // ------------------------------------------------ producer warp
+        const unsigned n_units = hv.ctr[1];
+        long long k = 0;
+        bool ok = true;
+        auto finish = [&](int s) {                       // lane 0: the unit in slot s is done
+            const int h = meta[s].h;
+            atomicMax(&hv.best[h], res[s]);
+            __threadfence();
+            if (atomicSub(&hv.remaining[h], 1) == 1) {   // the row's last unit
+                __threadfence();
+                const unsigned long long fin = atomicMax(&hv.best[h], 0ull);
+                tokens[meta[s].row] = fin ? static_cast<int32_t>(~static_cast<uint32_t>(fin & 0xffffffffull)) : 0;
+            }
+        };
+#pragma unroll 1
+        for (;; ++k) {
+            const int s = static_cast<int>(k % kUStages);
+            if (k >= kUStages) {
+                if (!mbar_wait(&empty[s], static_cast<uint32_t>((k / kUStages - 1) & 1), &abort_flag, &g_select_err)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) finish(s);
+            }
+            unsigned t = 0;
+            if (lane == 0) t = atomicAdd(&hv.ctr[2], 1u);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t >= n_units) {
+                if (lane == 0) {
+                    meta[s].h = -1;
+                    mbar_arrive(&full[s]);               // the end marker completes the phase
+                }
+                break;
+            }
+            const int4 u = hv.units[t];
+            const int n_lb = u.w - u.z;
+            const int row = hv.row_of[u.x];
+            if (lane < n_lb) blk[s][lane] = hv.live[static_cast<long long>(u.x) * n_blocks + u.z + lane];
+            if (lane == 0) {
+                meta[s] = UnitMeta{u.x, u.y, n_lb, row, row_req[row], static_cast<uint32_t>(row_pos[row]) + 1u};
+                best0[s] = *reinterpret_cast<volatile unsigned long long*>(&hv.best[u.x]);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                const int n = min(kStreamChunk, V - u.y * kStreamChunk);
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(n) * 4u);
+                bulk_g2s(ring + static_cast<long long>(s) * kStreamChunk,
+                         logits + static_cast<long long>(row) * ld + static_cast<long long>(u.y) * kStreamChunk,
+                         static_cast<uint32_t>(n) * 4u, &full[s]);
+            }
+        }
+        // the units still in the ring when the end marker went in: their results
+        if (ok) {
+#pragma unroll 1
+            for (long long j = k - kUStages + 1; j < k; ++j) {
+                if (j < 0) continue;
+                const int s = static_cast<int>(j % kUStages);
+                if (!mbar_wait(&empty[s], static_cast<uint32_t>((j / kUStages) & 1), &abort_flag, &g_select_err))
+                    break;
+                if (lane == 0) finish(s);
+            }
+        }
+        // after a time-out, every copy issued lands before the shared memory goes
+        if (lane == 0 && *reinterpret_cast<volatile int*>(&abort_flag)) {
+            for (int s = 0; s < kUStages; ++s) {
+                long long j = k - 1;                     // the last ordinal that used slot s
+                while (j >= 0 && j % kUStages != s) --j;
+                if (j >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>((j / kUStages) & 1));
+            }
+        }
+    } else {
+        // ------------------------------------------------ compute warps
+#pragma unroll 1
+        for (long long k = 0;; ++k) {
+            const int s = static_cast<int>(k % kUStages);
+            if (!mbar_wait(&full[s], static_cast<uint32_t>((k / kUStages) & 1), &abort_flag, &g_select_err)) break;
+            const UnitMeta m = meta[s];
+            if (m.h < 0) break;
+            unsigned long long b = groups_pass<kUnroll>(
+                ring + static_cast<long long>(s) * kStreamChunk, static_cast<long long>(m.c) * kStreamChunk,
+                m.n_lb * (kBlock / 4), [&](int i) { return blk[s][i]; }, V, m.pos, m.req, seed_lo, seed_hi, invT, gtab,
+                g254, best0[s], &best0[s]);
+            b = warp_max64(b);
+            if (lane == 0) red[s][warp] = b;
+            asm volatile("bar.sync 1, %0;" ::"n"(kSelThreads) : "memory");   // the compute warps only
+            if (threadIdx.x == 0) {
+                unsigned long long r = 0;
+#pragma unroll
+                for (int w = 0; w < kSelThreads / 32; ++w) r = umax64(r, red[s][w]);
+                res[s] = r;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);       // the slot is read (warp 0: and res written)
+        }
+    }
+    __syncthreads();
 }
 
 // ---------------------------------------------------------- Gumbel top-k
@@ -734,35 +974,76 @@ __global__ void verify_accept_kernel(const int32_t* __restrict__ target, const i
 }
 
 
+// A row is heavy when more than a quarter of its blocks (and more than 32)
+// stay live: a unit streams a whole chunk, which pays off only where most of
+// its blocks are live (a peaked row keeps a few live blocks and stays).  At
+// most an eighth of the rows are handed off: when most rows are flat every
+// CTA has Philox work anyway, and a row re-read right after its pass 1 still
+// sits in L2.
+constexpr int kHeavyMinLive = 32;
+constexpr size_t kHeavyScratchMax = 64ull << 20;  // heavy-row scratch of one call, at most
+
+size_t align16(size_t n) { return (n + 15) & ~static_cast<size_t>(15); }
+
 // Persistent launch of the streaming kernel: as many CTAs as fit on the GPU,
-// at most one per row; CTA b takes rows b, b + grid, ...
+// at most one per row; CTA b takes rows b, b + grid, ...  With T > 0 the heavy
+// rows' scratch is taken from a memory pool of the library's, in stream order
+// (from the stream's graph while it is being captured), the unit kernel runs
+// after the streaming kernel, and the scratch goes back to the pool in stream
+// order.
 int launch_stream_select(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
                          const int32_t* row_pos, uint64_t seed, float invT, int greedy, int32_t* tokens,
                          cudaStream_t stream) {
     const size_t smem = stream_smem_bytes(V);
+    const size_t unit_smem = unit_smem_bytes();
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return cuda_status(de);
     if (dev < 0 || dev >= kMaxDevices) return BIV_ERR_DEVICE;
-    int per_sm = 0;
+    int per_sm = 0, unit_per_sm = 0;
     unsigned int* ctr_base = nullptr;
+    cudaMemPool_t pool = nullptr;
     {
-        // per device, from any host thread: the kernel attribute, the counter
-        // ring's device address and the occupancy at this shared-memory size
+        // per device, from any host thread: the kernel attributes, the counter
+        // ring's device address, the scratch pool and the occupancy at this
+        // shared-memory size
         static std::mutex mu;
         static unsigned int* ctr_dev[kMaxDevices] = {};
+        static cudaMemPool_t pools[kMaxDevices] = {};
+        static int unit_occ[kMaxDevices] = {};
         static size_t occ_smem[kMaxDevices] = {};
         static int occ_per_sm[kMaxDevices] = {};
         std::lock_guard<std::mutex> lock(mu);
         if (!ctr_dev[dev]) {
             cudaError_t e = cudaFuncSetAttribute(gumbel_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(stream_smem_bytes(kMaxStreamV)));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gumbel_units_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(unit_smem));
+            int n = 0;
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gumbel_units_kernel, kUThreads, unit_smem);
+            if (e != cudaSuccess) return cuda_status(e);
+            // the pool keeps what it has handed out once (no release at synchronisation)
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            cudaMemPool_t mp = nullptr;
+            e = cudaMemPoolCreate(&mp, &props);
+            if (e != cudaSuccess) return cuda_status(e);
+            uint64_t keep = ~0ull;
+            e = cudaMemPoolSetAttribute(mp, cudaMemPoolAttrReleaseThreshold, &keep);
             if (e != cudaSuccess) return cuda_status(e);
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_stream_ctr);
             if (e != cudaSuccess) return cuda_status(e);
+            pools[dev] = mp;
+            unit_occ[dev] = std::max(1, n);
             ctr_dev[dev] = static_cast<unsigned int*>(p);
         }
+        pool = pools[dev];
+        unit_per_sm = unit_occ[dev];
         if (occ_smem[dev] != smem) {
             int n = 0;
             cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gumbel_stream_kernel, kSelThreads, smem);
@@ -779,9 +1060,57 @@ int launch_stream_select(const float* logits, int R, int V, long long ld, const 
     unsigned int* ctr = ctr_base + 2 * (next_slot.fetch_add(1u) % kCtrSlots);
     const long long cap = static_cast<long long>(num_sms()) * per_sm;
     const int grid = static_cast<int>(std::min<long long>(R, cap));
-    return launch_pdl(gumbel_stream_kernel, dim3(static_cast<unsigned>(grid)), dim3(kSelThreads), smem, stream,
-                      logits, R, V, ld, row_req, row_pos, static_cast<uint32_t>(seed & 0xffffffffull),
-                      static_cast<uint32_t>(seed >> 32), invT, greedy, tokens, ctr, noise_bounds());
+    const uint32_t seed_lo = static_cast<uint32_t>(seed & 0xffffffffull), seed_hi = static_cast<uint32_t>(seed >> 32);
+
+    // heavy-row scratch: {counters}{best}{row_of}{remaining}{units}{live}
+    HeavyRows hv = {};
+    void* scratch = nullptr;
+    if (!greedy) {
+        const int n_blocks = (V + kBlock - 1) / kBlock, n_chunks = (V + kStreamChunk - 1) / kStreamChunk;
+        const size_t per_row = 8 + 4 + 4 + static_cast<size_t>(n_chunks) * 16 + static_cast<size_t>(n_blocks) * 2;
+        const int hcap = static_cast<int>(
+            std::min<size_t>(static_cast<size_t>(std::max(1, R / 8)), kHeavyScratchMax / per_row));
+        const size_t o_best = 64, o_row = o_best + align16(static_cast<size_t>(hcap) * 8),
+                     o_rem = o_row + align16(static_cast<size_t>(hcap) * 4),
+                     o_units = o_rem + align16(static_cast<size_t>(hcap) * 4),
+                     o_live = o_units + static_cast<size_t>(hcap) * n_chunks * 16,
+                     bytes = o_live + align16(static_cast<size_t>(hcap) * n_blocks * 2);
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return cuda_status(e);
+        e = cs == cudaStreamCaptureStatusNone ? cudaMallocFromPoolAsync(&scratch, bytes, pool, stream)
+                                              : cudaMallocAsync(&scratch, bytes, stream);
+        if (e != cudaSuccess) return cuda_status(e);
+        uint8_t* b = static_cast<uint8_t*>(scratch);
+        e = cudaMemsetAsync(b, 0, 64, stream);                 // the counters
+        if (e != cudaSuccess) {
+            cudaFreeAsync(scratch, stream);
+            return cuda_status(e);
+        }
+        hv.ctr = reinterpret_cast<unsigned int*>(b);
+        hv.best = reinterpret_cast<unsigned long long*>(b + o_best);
+        hv.row_of = reinterpret_cast<int*>(b + o_row);
+        hv.remaining = reinterpret_cast<int*>(b + o_rem);
+        hv.units = reinterpret_cast<int4*>(b + o_units);
+        hv.live = reinterpret_cast<uint16_t*>(b + o_live);
+        hv.cap = hcap;
+        hv.min_live = std::max(kHeavyMinLive, n_blocks / 4);
+    }
+    int st = launch_pdl(gumbel_stream_kernel, dim3(static_cast<unsigned>(grid)), dim3(kSelThreads), smem, stream,
+                        logits, R, V, ld, row_req, row_pos, seed_lo, seed_hi, invT, greedy, tokens, ctr,
+                        noise_bounds(), hv);
+    if (st == BIV_OK && scratch) {
+        const int ugrid = static_cast<int>(std::min<long long>(
+            static_cast<long long>(std::max(1, R / 8)) * ((V + kStreamChunk - 1) / kStreamChunk),
+            static_cast<long long>(num_sms()) * unit_per_sm));
+        st = launch_pdl(gumbel_units_kernel, dim3(static_cast<unsigned>(ugrid)), dim3(kUThreads), unit_smem,
+                        stream, logits, V, ld, row_req, row_pos, seed_lo, seed_hi, invT, tokens, noise_bounds(), hv);
+    }
+    if (scratch) {
+        const cudaError_t e = cudaFreeAsync(scratch, stream);
+        if (st == BIV_OK && e != cudaSuccess) return cuda_status(e);
+    }
+    return st;
 }
 
 }  // namespace
