@@ -683,7 +683,7 @@ def run_kernel_sweep(args):
     req = (torch.arange(R, dtype=torch.int32, device="cuda") // cfg.K) * 7 + 3
     pos = (torch.arange(R, dtype=torch.int32, device="cuda") % cfg.K) + 1000
     tok = torch.empty(R, dtype=torch.int32, device="cuda")
-    line("gumbel_stream_kernel", "select fp32 [4096, 152064], T=0.7, 90% peaked rows",
+    line("gumbel_stream_kernel + gumbel_units_kernel", "select fp32 [4096, 152064], T=0.7, 90% peaked rows",
          4 * R * cfg.vocab + 12 * R, _time_us(lambda: B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.7, tok)))
     line("gumbel_stream_kernel", "select fp32 [4096, 152064], T=0 (greedy)",
          4 * R * cfg.vocab + 12 * R, _time_us(lambda: B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.0, tok)))
@@ -691,7 +691,7 @@ def run_kernel_sweep(args):
 
     for N, K in ((64, 16), (32, 8), (8, 4)):
         a = attention_case(N, K)
-        line("attn_tc_kernel + attn_combine_kernel",
+        line("attn_pp_kernel + attn_combine_kernel",
              f"attention W={N * K} ({N} x {K}), Hq 32 / Hkv 8, lognormal ctx mean {float(a['ctx'].float().mean()):.0f}",
              a["bytes"], _time_us(lambda: B.biv_decode_attn_fixedsplit(a["q"], a["kc"], a["vc"], a["slot"], a["rpos"],
                                                                        a["o"], a["K"], a["ws"])))
