@@ -271,7 +271,9 @@ int biv_rope_pack_qkv_weights(const void* w_qkv, void* w_packed, int Hq, int Hkv
  * second kernel over all SMs; its scratch (at most 64 MiB, about R/8 *
  * (2 ceil(V/256) + 16 ceil(V/8192) + 16) bytes) comes from a memory pool of
  * the library's, allocated and freed in the call's stream order
- * (cudaMallocAsync while the stream is being captured into a graph).      */
+ * (cudaMallocAsync while the stream is being captured into a graph).  The
+ * pool is created once per device and kept for the process: a
+ * cudaDeviceReset (or the end of the primary context) ends its use.     */
 int biv_gumbel_argmax(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
                       const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
                       biv_stream_t stream);
