@@ -310,6 +310,11 @@ BIV_DEV void seg_bounds(const uint32_t (&r)[SEGW], const unsigned long long* bkc
     }
 }
 
+// The key whose order (key_order) is o, for o != 0 (numbers).
+BIV_DEV float key_value(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
 // Largest of SEGW values (NaN only if all are NaN) and the lowest index
 // holding it (-1 if none): a tree, then a mask of the equal entries.
 template <int SEGW>
@@ -375,7 +380,8 @@ BIV_DEV void fly_bounds(const uint32_t (&r)[32], uint32_t col0, uint32_t pos, ui
 template <int SEGW, bool FLY = false>
 BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int cb, int ce, int n0, int N, bool live, uint32_t req,
                                            uint32_t pos, const SelectArgs& sel, const float* ntab,
-                                           const unsigned long long* bkrow, int RC, float* cm, float* logits_row) {
+                                           const unsigned long long* bkrow, int RC, float* cm, float* logits_row,
+                                           unsigned long long floor_key = 0) {
     static_assert(!FLY || SEGW == 32, "per-chunk bucket words need whole 32-column chunks per thread");
     const int hoff = SEGW == 16 ? static_cast<int>(threadIdx.x & 16) : 0;
     float bx = -INFINITY;       // largest logit (T = 0) or largest bound (T > 0)
@@ -444,6 +450,12 @@ BIV_DEV unsigned long long tile_row_winner(uint32_t taddr, int cb, int ce, int n
             const U4 w = philox4x32_10(v >> 2, pos, req, 0u, sel.seed_lo, sel.seed_hi);
             thr = __fadd_rn(__fmul_rn(bxv, sel.invT), gumbel_from_word(pick_word(w, v & 3u)));
             best = pack_key(thr, v);
+            // a larger real key of the row found elsewhere (floor_key, a numeric
+            // key) raises the bar for pass 2; no entry below it can win
+            if (floor_key > best && (floor_key >> 32) != 0ull) {
+                best = floor_key;
+                thr = key_value(static_cast<uint32_t>(floor_key >> 32));
+            }
         }
     }
     if (!sel.greedy) {
@@ -527,6 +539,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     float* cmax = t8 + 256;                                                   // EPI 3: [256][8]
     unsigned long long* s_best = reinterpret_cast<unsigned long long*>(cmax + 2 * kBM * kMaxChunks);  // [128]
     unsigned long long* bk = s_best + kBM;                                                   // EPI 3 only
+    unsigned long long* s_run = bk;             // EPI 3, CG = 2: [128] each row's best over the CTA's tiles
     constexpr int NT = epi_threads<EPI>();
     constexpr int TM = kBM * CG;                  // rows of one output tile
     // CG = 2: the pair's rank (0 = the even CTA, which owns the stage and
@@ -775,6 +788,8 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         }
         int acc = 0;
         uint32_t acc_phase = 0;
+        unsigned long long run = 0;                 // EPI 3, CG = 2: see below
+        int run_mblk = -1;
         for (int t = unit; t < n_work; t += n_units) {
             const int n_blk = t / m_tiles;
             const int m_blk = t - n_blk * m_tiles;
@@ -817,9 +832,17 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 const int cb = eset ? h1 * kChunk : 0, ce = eset ? BN : h1 * kChunk;
                 float* cmt = cmax + (eset * kBM + q * 32 + lane) * kMaxChunks;
                 unsigned long long best;
-                if constexpr (CG == 2)
+                if constexpr (CG == 2) {
+                    // A CTA pair keeps its row tile from one tile to the next as long
+                    // as the pairs divide the row tiles: the row's best key over the
+                    // CTA's earlier tiles (a real key of the row) then bounds pass 2
+                    // from below, so fewer chunks are revisited.
+                    if (run_mblk != m_blk) run = 0;
+                    else if (live) run = umax64(run, s_run[rloc]);
+                    run_mblk = m_blk;
                     best = tile_row_winner<32, true>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab,
-                                                     nullptr, 0, cmt, lrow);
+                                                     nullptr, 0, cmt, lrow, run);
+                }
                 else
                     best = g.m64 ? tile_row_winner<16>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab,
                                                        bk + srloc, g.a_rows, cmt, lrow)
@@ -827,8 +850,11 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                                                        bk + srloc, g.a_rows, cmt, lrow);
                 if (eset == 1 && live) s_best[rloc] = best;
                 epilogue_bar<NT>();   // both halves' winners are in; every row is done with the buckets
-                if (eset == 0 && live)
-                    sel.cand[static_cast<long long>(srow) * n_tiles + n_blk] = umax64(best, s_best[rloc]);
+                if (eset == 0 && live) {
+                    const unsigned long long w = umax64(best, s_best[rloc]);
+                    sel.cand[static_cast<long long>(srow) * n_tiles + n_blk] = w;
+                    if constexpr (CG == 2) s_run[rloc] = w;    // read by both halves at the next tile
+                }
             } else if constexpr (EPI == 4) {
                 // With M = 64 accumulators the two half-warps share each row:
                 // threads 16..31 take pairs 4..7 of every 16-column group.
@@ -1074,7 +1100,7 @@ int launch_gemm_cg(const void* A, const void* B, void* C, int M, int N, int K, i
     // EPI 3 keeps the noise table, chunk maxima and (CG = 1) one tile of noise
     // buckets beside the ring, and takes all of the opt-in shared memory.
     const int extra = EPI == 3 ? kNoiseTableBytes + 2 * kBM * kMaxChunks * 4 + kBM * 8 +
-                                     (CG == 1 ? g.a_rows * BN * 2 : 0)
+                                     (CG == 1 ? g.a_rows * BN * 2 : kBM * 8)
                                : 0;
     // The ring takes the opt-in shared memory left after the 1 KiB alignment
     // pad, the barriers and (non-selection epilogues) up to 1 KiB of the
