@@ -683,11 +683,16 @@ def run_kernel_sweep(args):
     req = (torch.arange(R, dtype=torch.int32, device="cuda") // cfg.K) * 7 + 3
     pos = (torch.arange(R, dtype=torch.int32, device="cuda") % cfg.K) + 1000
     tok = torch.empty(R, dtype=torch.int32, device="cuda")
-    line("gumbel_stream_kernel + gumbel_units_kernel", "select fp32 [4096, 152064], T=0.7, 90% peaked rows",
+    ws = torch.empty(B.biv_gumbel_argmax_workspace_size(R, cfg.vocab), dtype=torch.uint8, device="cuda")
+    line("gumbel_stream_kernel + gumbel_units_kernel",
+         "select fp32 [4096, 152064], T=0.7, 90% peaked rows (biv_gumbel_argmax_ws: flat rows to the unit kernel)",
+         4 * R * cfg.vocab + 12 * R,
+         _time_us(lambda: B.biv_gumbel_argmax_ws(logits, req, pos, synth.PHILOX_SEED, 0.7, tok, ws)))
+    line("gumbel_stream_kernel", "select fp32 [4096, 152064], T=0.7, 90% peaked rows (biv_gumbel_argmax: no workspace)",
          4 * R * cfg.vocab + 12 * R, _time_us(lambda: B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.7, tok)))
     line("gumbel_stream_kernel", "select fp32 [4096, 152064], T=0 (greedy)",
          4 * R * cfg.vocab + 12 * R, _time_us(lambda: B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.0, tok)))
-    del logits
+    del logits, ws
 
     for N, K in ((64, 16), (32, 8), (8, 4)):
         a = attention_case(N, K)
@@ -825,8 +830,9 @@ def run_profile_case(args):
         req = (torch.arange(R, dtype=torch.int32, device="cuda") // cfg.K) * 7 + 3
         pos = (torch.arange(R, dtype=torch.int32, device="cuda") % cfg.K) + 1000
         tok = torch.empty(R, dtype=torch.int32, device="cuda")
-        for T in (0.7, 0.0):
-            B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, T, tok)
+        ws = torch.empty(B.biv_gumbel_argmax_workspace_size(R, cfg.vocab), dtype=torch.uint8, device="cuda")
+        B.biv_gumbel_argmax_ws(logits, req, pos, synth.PHILOX_SEED, 0.7, tok, ws)
+        B.biv_gumbel_argmax(logits, req, pos, synth.PHILOX_SEED, 0.0, tok)
         print(json.dumps({"case": case, "rows": R, "vocab": cfg.vocab}))
     elif case == "rmsnorm":
         rows, d = 16384, 4096                     # 128 MiB in, 128 MiB out

@@ -266,17 +266,27 @@ int biv_rope_pack_qkv_weights(const void* w_qkv, void* w_packed, int Hq, int Hkv
  * aligned logits.  Two or more rows per SM are streamed one row per CTA
  * (rows dealt out by a counter of the library's; up to 64 such calls may
  * run at the same time); fewer rows are shared by eight-CTA clusters; both
- * give the same tokens.  When streaming with T > 0, rows on which many
- * entries can still win (flat rows, up to R/8 of them) are finished by a
- * second kernel over all SMs; its scratch (at most 64 MiB, about R/8 *
- * (2 ceil(V/256) + 16 ceil(V/8192) + 16) bytes) comes from a memory pool of
- * the library's, allocated and freed in the call's stream order
- * (cudaMallocAsync while the stream is being captured into a graph).  The
- * pool is created once per device and kept for the process: a
- * cudaDeviceReset (or the end of the primary context) ends its use.     */
+ * give the same tokens.  Allocates nothing.                              */
 int biv_gumbel_argmax(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
                       const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
                       biv_stream_t stream);
+
+/* biv_gumbel_argmax with a workspace: when rows are streamed and T > 0, rows
+ * on which many entries can still win (flat rows: more than a quarter of
+ * their 256-logit blocks can reach the first exact key; up to R/8 of them,
+ * the rest as in biv_gumbel_argmax) are not finished by the CTA that
+ * streamed them but handed, as one unit per 8192-logit chunk, to a second
+ * kernel that runs over all SMs after the first.  Same tokens, bit for bit.
+ * workspace: device memory of at least biv_gumbel_argmax_workspace_size(R,
+ * V) bytes (R/8 * (2 ceil(V/256) + 16 ceil(V/8192) + 16) + 64, about), 16-B
+ * aligned, owned by the caller, contents ignored on entry; one call at a
+ * time per workspace.  Errors as biv_gumbel_argmax, plus BIV_ERR_NULL /
+ * BIV_ERR_ALIGN / BIV_ERR_SHAPE for a missing, misaligned or short
+ * workspace (R > 0).                                                     */
+size_t biv_gumbel_argmax_workspace_size(int R, int V);
+int biv_gumbel_argmax_ws(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                         const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
+                         void* workspace, size_t ws_bytes, biv_stream_t stream);
 
 /* The noise g_v of biv_gumbel_argmax for v in [0, V) of each row (fp32
  * [R, V]); for tests of the noise itself.                                  */

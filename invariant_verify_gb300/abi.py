@@ -49,6 +49,8 @@ SIGNATURES = {
     "biv_gqa_max_drafts": (_I, [_I, _I]),
     "biv_kv_overwrite": (_I, [_P, _P, _P, _LL, _P, _LL, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "biv_gumbel_argmax": (_I, [_P, _I, _I, _LL, _P, _P, _U64, _F, _P, _P]),
+    "biv_gumbel_argmax_workspace_size": (_SZ, [_I, _I]),
+    "biv_gumbel_argmax_ws": (_I, [_P, _I, _I, _LL, _P, _P, _U64, _F, _P, _P, _SZ, _P]),
     "biv_gumbel_noise": (_I, [_U64, _P, _P, _I, _I, _P, _P]),
     "biv_gumbel_topk": (_I, [_P, _I, _I, _LL, _P, _P, _U64, _F, _I, _P, _P]),
     "biv_gemm_qkv_rope": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
@@ -194,6 +196,20 @@ def biv_gumbel_argmax(logits, row_req, row_pos, seed: int, temperature: float, t
     _check("biv_gumbel_argmax", _load().biv_gumbel_argmax(
         _ptr(logits), R, V, logits.stride(0), _ptr(row_req), _ptr(row_pos), seed & 0xFFFFFFFFFFFFFFFF,
         float(temperature), _ptr(tokens), _stream(stream)))
+
+
+def biv_gumbel_argmax_workspace_size(R: int, V: int) -> int:
+    return int(_load().biv_gumbel_argmax_workspace_size(R, V))
+
+
+def biv_gumbel_argmax_ws(logits, row_req, row_pos, seed: int, temperature: float, tokens, workspace,
+                         V: int | None = None, stream=None) -> None:
+    R, ld = logits.shape
+    V = ld if V is None else V
+    _check("biv_gumbel_argmax_ws", _load().biv_gumbel_argmax_ws(
+        _ptr(logits), R, V, logits.stride(0), _ptr(row_req), _ptr(row_pos), seed & 0xFFFFFFFFFFFFFFFF,
+        float(temperature), _ptr(tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
 
 
 def biv_rope_pack_qkv_weights(w_qkv, w_packed, Hq: int, Hkv: int, hd: int, stream=None) -> None:

@@ -981,19 +981,38 @@ __global__ void verify_accept_kernel(const int32_t* __restrict__ target, const i
 // CTA has Philox work anyway, and a row re-read right after its pass 1 still
 // sits in L2.
 constexpr int kHeavyMinLive = 32;
-constexpr size_t kHeavyScratchMax = 64ull << 20;  // heavy-row scratch of one call, at most
 
 size_t align16(size_t n) { return (n + 15) & ~static_cast<size_t>(15); }
 
+// The heavy-row scratch of a call with R rows of V logits, carved from the
+// caller's workspace: {counters}{best}{row_of}{remaining}{units}{live} for up
+// to R / 8 rows (at least one).
+struct HeavyLayout {
+    int cap, n_blocks, n_chunks;
+    size_t o_best, o_row, o_rem, o_units, o_live, bytes;
+};
+
+HeavyLayout heavy_layout(int R, int V) {
+    HeavyLayout L;
+    L.cap = std::max(1, R / 8);
+    L.n_blocks = (V + kBlock - 1) / kBlock;
+    L.n_chunks = (V + kStreamChunk - 1) / kStreamChunk;
+    L.o_best = 64;
+    L.o_row = L.o_best + align16(static_cast<size_t>(L.cap) * 8);
+    L.o_rem = L.o_row + align16(static_cast<size_t>(L.cap) * 4);
+    L.o_units = L.o_rem + align16(static_cast<size_t>(L.cap) * 4);
+    L.o_live = L.o_units + static_cast<size_t>(L.cap) * L.n_chunks * 16;
+    L.bytes = L.o_live + align16(static_cast<size_t>(L.cap) * L.n_blocks * 2);
+    return L;
+}
+
 // Persistent launch of the streaming kernel: as many CTAs as fit on the GPU,
-// at most one per row; CTA b takes rows b, b + grid, ...  With T > 0 the heavy
-// rows' scratch is taken from a memory pool of the library's, in stream order
-// (from the stream's graph while it is being captured), the unit kernel runs
-// after the streaming kernel, and the scratch goes back to the pool in stream
-// order.
+// at most one per row; CTA b takes rows b, b + grid, ...  With a workspace
+// and T > 0, flat rows are handed to the unit kernel, launched right after
+// (the workspace's counters are cleared first, in stream order).
 int launch_stream_select(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
                          const int32_t* row_pos, uint64_t seed, float invT, int greedy, int32_t* tokens,
-                         cudaStream_t stream) {
+                         void* workspace, cudaStream_t stream) {
     const size_t smem = stream_smem_bytes(V);
     const size_t unit_smem = unit_smem_bytes();
     int dev = 0;
@@ -1002,14 +1021,11 @@ int launch_stream_select(const float* logits, int R, int V, long long ld, const 
     if (dev < 0 || dev >= kMaxDevices) return BIV_ERR_DEVICE;
     int per_sm = 0, unit_per_sm = 0;
     unsigned int* ctr_base = nullptr;
-    cudaMemPool_t pool = nullptr;
     {
         // per device, from any host thread: the kernel attributes, the counter
-        // ring's device address, the scratch pool and the occupancy at this
-        // shared-memory size
+        // ring's device address and the occupancy at this shared-memory size
         static std::mutex mu;
         static unsigned int* ctr_dev[kMaxDevices] = {};
-        static cudaMemPool_t pools[kMaxDevices] = {};
         static int unit_occ[kMaxDevices] = {};
         static size_t occ_smem[kMaxDevices] = {};
         static int occ_per_sm[kMaxDevices] = {};
@@ -1024,25 +1040,12 @@ int launch_stream_select(const float* logits, int R, int V, long long ld, const 
             if (e == cudaSuccess)
                 e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gumbel_units_kernel, kUThreads, unit_smem);
             if (e != cudaSuccess) return cuda_status(e);
-            // the pool keeps what it has handed out once (no release at synchronisation)
-            cudaMemPoolProps props = {};
-            props.allocType = cudaMemAllocationTypePinned;
-            props.location.type = cudaMemLocationTypeDevice;
-            props.location.id = dev;
-            cudaMemPool_t mp = nullptr;
-            e = cudaMemPoolCreate(&mp, &props);
-            if (e != cudaSuccess) return cuda_status(e);
-            uint64_t keep = ~0ull;
-            e = cudaMemPoolSetAttribute(mp, cudaMemPoolAttrReleaseThreshold, &keep);
-            if (e != cudaSuccess) return cuda_status(e);
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_stream_ctr);
             if (e != cudaSuccess) return cuda_status(e);
-            pools[dev] = mp;
             unit_occ[dev] = std::max(1, n);
             ctr_dev[dev] = static_cast<unsigned int*>(p);
         }
-        pool = pools[dev];
         unit_per_sm = unit_occ[dev];
         if (occ_smem[dev] != smem) {
             int n = 0;
@@ -1062,53 +1065,31 @@ int launch_stream_select(const float* logits, int R, int V, long long ld, const 
     const int grid = static_cast<int>(std::min<long long>(R, cap));
     const uint32_t seed_lo = static_cast<uint32_t>(seed & 0xffffffffull), seed_hi = static_cast<uint32_t>(seed >> 32);
 
-    // heavy-row scratch: {counters}{best}{row_of}{remaining}{units}{live}
     HeavyRows hv = {};
-    void* scratch = nullptr;
-    if (!greedy) {
-        const int n_blocks = (V + kBlock - 1) / kBlock, n_chunks = (V + kStreamChunk - 1) / kStreamChunk;
-        const size_t per_row = 8 + 4 + 4 + static_cast<size_t>(n_chunks) * 16 + static_cast<size_t>(n_blocks) * 2;
-        const int hcap = static_cast<int>(
-            std::min<size_t>(static_cast<size_t>(std::max(1, R / 8)), kHeavyScratchMax / per_row));
-        const size_t o_best = 64, o_row = o_best + align16(static_cast<size_t>(hcap) * 8),
-                     o_rem = o_row + align16(static_cast<size_t>(hcap) * 4),
-                     o_units = o_rem + align16(static_cast<size_t>(hcap) * 4),
-                     o_live = o_units + static_cast<size_t>(hcap) * n_chunks * 16,
-                     bytes = o_live + align16(static_cast<size_t>(hcap) * n_blocks * 2);
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    const bool hand_off = workspace != nullptr && !greedy;
+    if (hand_off) {
+        const HeavyLayout L = heavy_layout(R, V);
+        uint8_t* b = static_cast<uint8_t*>(workspace);
+        const cudaError_t e = cudaMemsetAsync(b, 0, 64, stream);   // the counters
         if (e != cudaSuccess) return cuda_status(e);
-        e = cs == cudaStreamCaptureStatusNone ? cudaMallocFromPoolAsync(&scratch, bytes, pool, stream)
-                                              : cudaMallocAsync(&scratch, bytes, stream);
-        if (e != cudaSuccess) return cuda_status(e);
-        uint8_t* b = static_cast<uint8_t*>(scratch);
-        e = cudaMemsetAsync(b, 0, 64, stream);                 // the counters
-        if (e != cudaSuccess) {
-            cudaFreeAsync(scratch, stream);
-            return cuda_status(e);
-        }
         hv.ctr = reinterpret_cast<unsigned int*>(b);
-        hv.best = reinterpret_cast<unsigned long long*>(b + o_best);
-        hv.row_of = reinterpret_cast<int*>(b + o_row);
-        hv.remaining = reinterpret_cast<int*>(b + o_rem);
-        hv.units = reinterpret_cast<int4*>(b + o_units);
-        hv.live = reinterpret_cast<uint16_t*>(b + o_live);
-        hv.cap = hcap;
-        hv.min_live = std::max(kHeavyMinLive, n_blocks / 4);
+        hv.best = reinterpret_cast<unsigned long long*>(b + L.o_best);
+        hv.row_of = reinterpret_cast<int*>(b + L.o_row);
+        hv.remaining = reinterpret_cast<int*>(b + L.o_rem);
+        hv.units = reinterpret_cast<int4*>(b + L.o_units);
+        hv.live = reinterpret_cast<uint16_t*>(b + L.o_live);
+        hv.cap = L.cap;
+        hv.min_live = std::max(kHeavyMinLive, L.n_blocks / 4);
     }
     int st = launch_pdl(gumbel_stream_kernel, dim3(static_cast<unsigned>(grid)), dim3(kSelThreads), smem, stream,
                         logits, R, V, ld, row_req, row_pos, seed_lo, seed_hi, invT, greedy, tokens, ctr,
                         noise_bounds(), hv);
-    if (st == BIV_OK && scratch) {
+    if (st == BIV_OK && hand_off) {
         const int ugrid = static_cast<int>(std::min<long long>(
-            static_cast<long long>(std::max(1, R / 8)) * ((V + kStreamChunk - 1) / kStreamChunk),
+            static_cast<long long>(hv.cap) * ((V + kStreamChunk - 1) / kStreamChunk),
             static_cast<long long>(num_sms()) * unit_per_sm));
         st = launch_pdl(gumbel_units_kernel, dim3(static_cast<unsigned>(ugrid)), dim3(kUThreads), unit_smem,
                         stream, logits, V, ld, row_req, row_pos, seed_lo, seed_hi, invT, tokens, noise_bounds(), hv);
-    }
-    if (scratch) {
-        const cudaError_t e = cudaFreeAsync(scratch, stream);
-        if (st == BIV_OK && e != cudaSuccess) return cuda_status(e);
     }
     return st;
 }
@@ -1118,9 +1099,10 @@ int launch_stream_select(const float* logits, int R, int V, long long ld, const 
 
 using namespace biv;
 
-extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
-                                 const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
-                                 biv_stream_t stream) {
+// Both selection entry points; workspace (or null) as biv_gumbel_argmax_ws.
+static int gumbel_argmax_impl(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                              const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
+                              void* workspace, biv_stream_t stream) {
     if (R < 0 || V < 4 || ld < V) return BIV_ERR_SHAPE;
     if (V % 4 != 0 || ld % 4 != 0) return BIV_ERR_SHAPE;
     if (!(temperature >= 0.0f) || !(temperature < INFINITY)) return BIV_ERR_VALUE;
@@ -1134,7 +1116,7 @@ extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld
     // Many rows (two or more per SM) or a row too wide for one cluster: a CTA
     // streams whole rows.  Few rows: a cluster of eight CTAs shares each row.
     if (R >= 2 * num_sms() || slice > kMaxSliceFloats) {
-        return launch_stream_select(logits, R, V, ld, row_req, row_pos, seed, invT, greedy, tokens,
+        return launch_stream_select(logits, R, V, ld, row_req, row_pos, seed, invT, greedy, tokens, workspace,
                                     reinterpret_cast<cudaStream_t>(stream));
     }
     if (static_cast<long long>(R) * kClusterSize > 0x7fffffffLL) return BIV_ERR_SHAPE;
@@ -1168,6 +1150,29 @@ extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld
                                        static_cast<uint32_t>(seed >> 32), invT, greedy, tokens, noise_bounds());
     if (e != cudaSuccess) return cuda_status(e);
     return launch_status();
+}
+
+extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                                 const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
+                                 biv_stream_t stream) {
+    return gumbel_argmax_impl(logits, R, V, ld, row_req, row_pos, seed, temperature, tokens, nullptr, stream);
+}
+
+extern "C" size_t biv_gumbel_argmax_workspace_size(int R, int V) {
+    if (R <= 0 || V < 4 || V % 4 != 0 || V > kMaxStreamV) return 0;
+    return heavy_layout(R, V).bytes;
+}
+
+extern "C" int biv_gumbel_argmax_ws(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
+                                    const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
+                                    void* workspace, size_t ws_bytes, biv_stream_t stream) {
+    if (R < 0 || V < 4 || ld < V || V % 4 != 0 || ld % 4 != 0) return BIV_ERR_SHAPE;
+    if (R > 0) {
+        if (!workspace) return BIV_ERR_NULL;
+        if (!aligned16(workspace)) return BIV_ERR_ALIGN;
+        if (ws_bytes < biv_gumbel_argmax_workspace_size(R, V)) return BIV_ERR_SHAPE;
+    }
+    return gumbel_argmax_impl(logits, R, V, ld, row_req, row_pos, seed, temperature, tokens, workspace, stream);
 }
 
 extern "C" int biv_gumbel_topk(const float* logits, int R, int V, long long ld, const uint32_t* row_req,

@@ -153,6 +153,22 @@ def test_select_and_accept_validation(lib):
     assert g(MISALIGNED, 4, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, None) == ALIGN
     big = (1 << 22) + 4                     # past the streaming kernel's block-maximum table
     assert g(FAKE, 4, big, big, FAKE, FAKE, 1, 1.0, FAKE, None) == UNSUP
+    # the workspace entry: size = 64 B of counters + per heavy slot (R / 8 of them, at least one):
+    # best key 8 B, row 4 B, units left 4 B (each 16-B aligned as arrays), units 16 B per
+    # 8192-logit chunk, live blocks 2 B per 256-logit block
+    wsz = lib.biv_gumbel_argmax_workspace_size
+    al = lambda n: (n + 15) // 16 * 16
+    for R, V in ((4096, 152064), (17, 1000), (3, 4)):
+        cap, nb, nc = max(1, R // 8), -(-V // 256), -(-V // 8192)
+        assert wsz(R, V) == 64 + al(cap * 8) + 2 * al(cap * 4) + cap * nc * 16 + al(cap * nb * 2)
+    assert wsz(0, 32) == 0 and wsz(4, 30) == 0
+    w = lib.biv_gumbel_argmax_ws
+    ws = wsz(4, 32)
+    assert w(FAKE, 4, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, None, ws, None) == NULL
+    assert w(FAKE, 4, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, MISALIGNED, ws, None) == ALIGN
+    assert w(FAKE, 4, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, FAKE, ws - 16, None) == SHAPE
+    assert w(FAKE, 4, 30, 32, FAKE, FAKE, 1, 1.0, FAKE, FAKE, ws, None) == SHAPE
+    assert w(FAKE, 0, 32, 32, FAKE, FAKE, 1, 1.0, FAKE, None, 0, None) == OK
     a = lib.biv_verify_accept
     assert a(FAKE, FAKE, FAKE, 4, 0, FAKE, FAKE, None) == SHAPE
     assert a(FAKE, FAKE, FAKE, 0, 4, FAKE, FAKE, None) == OK

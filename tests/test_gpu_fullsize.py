@@ -45,10 +45,15 @@ def test_selection_full_size_bit_exact(T, exact_ties):
     xd = x.cuda()
     tok = torch.empty(R, dtype=torch.int32, device="cuda")
     B.biv_gumbel_argmax(xd, req.cuda(), pos.cuda(), SEED, T, tok)
+    # the workspace entry (flat rows to the unit kernel): the same tokens
+    ws = torch.empty(B.biv_gumbel_argmax_workspace_size(R, cfg.vocab), dtype=torch.uint8, device="cuda")
+    tok_ws = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax_ws(xd, req.cuda(), pos.cuda(), SEED, T, tok_ws, ws)
     torch.cuda.synchronize()
-    del xd
+    del xd, ws
     ref = oracle.gumbel_argmax(x, req, pos, SEED, T)
     assert np.array_equal(tok.cpu().numpy(), ref)
+    assert torch.equal(tok_ws, tok)
     # drafts = targets with 20% random ids; accept lengths and rollback points bit-exact
     mask, ids = synth.draft_errors((R,), cfg.draft_err, cfg.vocab, seed=92)
     draft = synth.apply_draft_errors(torch.from_numpy(ref), mask, ids)

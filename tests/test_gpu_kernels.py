@@ -529,6 +529,15 @@ def test_gumbel_argmax_streaming_rows_bit_exact(V, T):
     tp = torch.empty(R, dtype=torch.int32, device="cuda")
     B.biv_gumbel_argmax(pad.cuda(), req.cuda(), pos.cuda(), SEED, T, tp, V=V)
     assert torch.equal(tp, tok)
+    # with a workspace (flat rows handed to the unit kernel): the same tokens,
+    # also with a padded leading dimension and a workspace full of stale bytes
+    ws = torch.full((B.biv_gumbel_argmax_workspace_size(R, V),), 0xA5, dtype=torch.uint8, device="cuda")
+    tw = torch.full((R,), -3, dtype=torch.int32, device="cuda")
+    B.biv_gumbel_argmax_ws(x.cuda(), req.cuda(), pos.cuda(), SEED, T, tw, ws)
+    assert torch.equal(tw, tok)
+    tw.fill_(-3)
+    B.biv_gumbel_argmax_ws(pad.cuda(), req.cuda(), pos.cuda(), SEED, T, tw, ws, V=V)
+    assert torch.equal(tw, tok)
 
 
 def test_gumbel_argmax_streaming_rows_concurrent_streams_and_graph_replays():
@@ -570,6 +579,29 @@ def test_gumbel_argmax_streaming_rows_concurrent_streams_and_graph_replays():
         graph.replay()
         torch.cuda.synchronize()
         assert np.array_equal(tok.cpu().numpy(), refs[1])
+    # the workspace entry: one workspace per stream, back-to-back launches on two
+    # streams at once, then graph replays
+    wss = [torch.empty(B.biv_gumbel_argmax_workspace_size(R, V), dtype=torch.uint8, device="cuda")
+           for _ in range(2)]
+    for _ in range(3):
+        for i in range(2):
+            toks[i].fill_(-7)
+        torch.cuda.synchronize()
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                for _ in range(3):
+                    B.biv_gumbel_argmax_ws(xd[i], rq, ps, SEED, 0.7, toks[i], wss[i], stream=streams[i])
+        torch.cuda.synchronize()
+        for i in range(2):
+            assert np.array_equal(toks[i].cpu().numpy(), refs[i])
+    graph_ws = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ws):
+        B.biv_gumbel_argmax_ws(xd[0], rq, ps, SEED, 0.7, tok, wss[0], stream=torch.cuda.current_stream())
+    for _ in range(3):
+        tok.fill_(-7)
+        graph_ws.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(tok.cpu().numpy(), refs[0])
 
 
 def test_gumbel_argmax_chi_square_counts_match_oracle():
