@@ -280,6 +280,29 @@ def test_attention_two_item_and_one_item_kernels_same_bits():
     assert_close(big[rows], ref, what="attention (one item per SM)")
 
 
+def test_attention_combine_many_pairs_per_warp():
+    """W = 4096 rows x 32 heads = 131072 (row, head) pairs: more than 32 per
+    combine warp, so a warp reads the slots and positions of its pairs in
+    several rounds of 32.  Sampled rows match the oracle, and the first 256
+    rows give the same bits when they are the whole window."""
+    W, Hq, Hkv, K, n_slots, max_len = 4096, 32, 8, 16, 16, 700
+    g = synth.generator(4096)
+    kc = synth.bf16_normal((n_slots, Hkv, max_len, 128), 1.0, g)
+    vc = synth.bf16_normal((n_slots, Hkv, max_len, 128), 1.0, g)
+    q = synth.bf16_normal((W, Hq, 128), 1.0, g)
+    req = np.arange(W) // K
+    slot = (req % n_slots).astype(np.int32)
+    pos = ((req * 37) % 600 + 40 + np.arange(W) % K).astype(np.int32)
+    qd, kd, vd = dev(q), dev(kc), dev(vc)
+    big = _run_attn(qd, kd, vd, slot, pos, K)
+    small = _run_attn(qd[:256].contiguous(), kd, vd, slot[:256], pos[:256], K)
+    assert same_bits(big[:256], small)
+    rows = [0, 15, 2047, 3000, 4095]
+    ref = oracle.attention(q[rows], kc, vc, slot[rows], pos[rows])
+    assert_close(big[rows], ref, what="attention, 131072 pairs")
+    assert not torch.isnan(big.float()).any()
+
+
 def test_attention_bad_position_raises_device_error():
     q, kc, vc, slot, pos = _attn_case(2, 8, 2, 600, [100, 300], 4, seed=12)
     qd, kd, vd = dev(q), dev(kc), dev(vc)
