@@ -792,7 +792,7 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __shared__ __align__(8) uint64_t kbar[2][2], vbar[2][2], qbar[2], sbar[2], obar[2];
     __shared__ uint32_t s_tmem;
     __shared__ int abort_flag;
-    __shared__ uint32_t s_qiss[2];
+    __shared__ uint32_t s_qiss[2], s_viss[2];
     __shared__ float s_mx[2][2][M], s_sum[2][2][M];
 
     if (threadIdx.x == 0) {
@@ -934,8 +934,9 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         if (mbar_wait(&sbar[wg], s_use & 1u, &abort_flag, &g_attn_err) && wt == 0) ++s_seen;
         ++s_use;
         tc_fence_after();
-        // ---- Q and K consumed: this item's V box into region A
-        if (wt == 0 && !aborted()) load_box(&tmV, &tmV2, sA, &vb[0], v_iss[0], cur);
+        // ---- Q and K consumed: this item's V box into region A, issued by
+        // warp 7 (warp 0 has just issued the S MMAs and will issue P V)
+        if (wt == 224 && !aborted()) load_box(&tmV, &tmV2, sA, &vb[0], v_iss[0], cur);
         // ---- softmax over the split; the thread's 64 scores (keys 128 ch + 32 i
         // + 16 hi + t) stay in registers from one round of loads until P is written
         const int pos = r < T ? s_rpos[row0 + r / P.G] : -1;     // the row's usable position (table)
@@ -1062,17 +1063,17 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
     // ---- leave.  After a time-out, the copies and MMAs already started
     // complete first (bounded waits), then TMEM is freed.  (ok is uniform
-    // over the warpgroup; thread 32 issued the Q boxes, thread 0 saw them land.)
+    // over the warpgroup; threads 32 and 224 issued the Q and V boxes, thread 0
+    // saw them land.)
     if (!ok) {
         if (wt == 32) s_qiss[wg] = q_iss;
+        if (wt == 224) s_viss[wg] = v_iss[0];
         asm volatile("bar.sync %0, 256;" ::"r"(1 + wg) : "memory");
     }
     if (wt == 0 && !ok) {
         for (uint32_t j = q_seen; j < s_qiss[wg]; ++j) mbar_wait_drain(&qbar[wg], j & 1u);
-        for (int kh = 0; kh < 2; ++kh) {
-            for (uint32_t j = k_seen[kh]; j < k_iss[kh]; ++j) mbar_wait_drain(&kb[kh], j & 1u);
-            for (uint32_t j = v_seen[kh]; j < v_iss[kh]; ++j) mbar_wait_drain(&vb[kh], j & 1u);
-        }
+        for (uint32_t j = k_seen[0]; j < k_iss[0]; ++j) mbar_wait_drain(&kb[0], j & 1u);
+        for (uint32_t j = v_seen[0]; j < s_viss[wg]; ++j) mbar_wait_drain(&vb[0], j & 1u);
         for (uint32_t j = s_seen; j < s_iss; ++j) mbar_wait_drain(&sbar[wg], j & 1u);
         for (uint32_t j = o_seen; j < o_iss; ++j) mbar_wait_drain(&obar[wg], j & 1u);
     }
