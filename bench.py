@@ -67,8 +67,8 @@ def parse():
     p.add_argument("--c4-steps", action="store_true",
                    help="instead of the step bench: verified tok/s of whole verify steps on the Llama-3-8B-shaped "
                         "layer + LM head at the verifier sweep's windows (N x K = 8x4, 32x8, 64x16)")
-    p.add_argument("--profile-case", choices=["attn16", "attn1024", "select1024", "lmhead1024", "rmsnorm", "gemm1024",
-                                              "qkv1024"],
+    p.add_argument("--profile-case", choices=["attn16", "attn1024", "select1024", "lmhead1024", "lmhead64", "rmsnorm",
+                                              "gemm1024", "qkv1024"],
                    help="run one small case twice, for a profiler capture")
     return p.parse_args()
 
@@ -842,9 +842,10 @@ def run_profile_case(args):
         for _ in range(2):
             B.biv_rmsnorm(x, w, y, 1e-6)
         print(json.dumps({"case": case, "rows": rows, "d": d, "bytes": 4 * rows * d + 2 * d}))
-    elif case == "lmhead1024":
-        cfg = synth.SWEEP
-        M, N, Kd = 1024, cfg.vocab, cfg.d
+    elif case in ("lmhead1024", "lmhead64"):
+        # the sweep's LM head at W = 1024, or the 2-layer decoder's at W = 64
+        cfg = synth.SWEEP if case == "lmhead1024" else synth.DECODER2
+        M, N, Kd = (1024 if case == "lmhead1024" else cfg.W), cfg.vocab, cfg.d
         A = synth.bf16_normal_device((M, Kd), 1.0, 11)
         Wl = synth.bf16_normal_device((N, Kd), 0.02, 12)
         req = torch.arange(M, dtype=torch.int32, device="cuda") // 16 * 31 + 1
