@@ -374,7 +374,9 @@ def test_rope_kv_write_equals_rope_then_overwrite():
 
 
 @pytest.mark.parametrize("W,K,d,Hq,Hkv,hd", [(12, 4, 256, 8, 2, 128), (64, 8, 1024, 8, 2, 128),
-                                             (130, 1, 512, 4, 4, 64), (256, 256, 4096, 32, 8, 128)])
+                                             (130, 1, 512, 4, 4, 64), (256, 256, 4096, 32, 8, 128),
+                                             (40, 8, 512, 4, 2, 256),          # 16 frequency groups
+                                             (1024, 16, 4096, 32, 8, 128)])    # the bench's window: CTA pairs, two waves
 def test_qkv_rope_gemm_equals_gemm_then_rope_kv_write(W, K, d, Hq, Hkv, hd):
     g = synth.generator(W + d)
     n_slots, max_len = W // K + 1, 400
