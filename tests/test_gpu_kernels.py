@@ -680,7 +680,10 @@ def _fused_vs_unfused(A, Bw, T, seed=SEED, write_logits=True):
 @pytest.mark.parametrize("M,N,K,T,std", [
     (64, 32000, 1024, 0.7, 0.02), (1, 2048, 256, 1.0, 1.0 / 16), (7, 4104, 192, 0.5, 0.1),
     (130, 5000, 512, 0.7, 0.05), (64, 32000, 1024, 0.0, 0.02), (300, 2056, 136, 2.0, 0.2),
-    (16, 152064, 256, 0.7, 0.2), (1000, 8200, 256, 0.7, 0.1), (600, 4104, 320, 0.0, 0.1)])
+    (16, 152064, 256, 0.7, 0.2), (1000, 8200, 256, 0.7, 0.1), (600, 4104, 320, 0.0, 0.1),
+    # CTA pairs with many tiles each: 4 row tiles (each pair keeps its rows, and their
+    # best keys from tile to tile) and 3 row tiles (the rows change every tile)
+    (1024, 20000, 256, 0.7, 0.05), (600, 32000, 256, 0.7, 0.05)])
 def test_lm_head_gumbel_fused_bit_exact(M, N, K, T, std):
     g = synth.generator(M + N + K)
     A = synth.bf16_normal((M, K), 1.0, g).cuda()
