@@ -1086,12 +1086,45 @@ attn_pp_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 // One warp per (row, head): combine splits 0 .. pos/256 of the row.  Lane s
 // holds split s (32 at a time); the maximum and the weight sum are reduced
 // with a fixed xor butterfly, the outputs are summed in increasing split
-// order.  The CTAs are persistent (a warp takes pairs w, w + all warps, ...).
-// Slots and positions are inputs of the call, not outputs of the split
-// kernel, so the lanes read those of the warp's next 32 pairs while it
-// finishes; per pair one round of loads then fetches every lane's (m, l) and
-// the first kCombinePre splits' outputs together.
+// order.  Per pair one round of loads fetches the (m, l) of up to 64 splits
+// and the first kCombinePre splits' outputs together; the later splits come
+// kCombinePre at a time (a pair of 33 splits: five rounds of loads).
+//
+// Which warp combines which pair does not change a pair's arithmetic, so the
+// pairs are dealt for balance.  A pair of ns splits costs kCombinePre units
+// per round of loads plus one per split: the bulk of the combine runs near
+// the HBM rate, where bytes count, and its tail is a few warps' chains of
+// rounds, where rounds count.  A pair that is only zeroed costs one unit.
+// Every CTA forms the prefix sums of the rows' costs from the call's slots
+// and positions (inputs, so before the wait on the split kernel), and warp g
+// of NW takes the pairs whose cost interval starts in [T·g/NW, T·(g+1)/NW).
+// With lognormal context lengths a fixed round-robin deal gave some warps
+// twice the mean work.  Windows of more than kCombineBalancedMaxW rows (whose
+// cost table would not fit beside three CTAs per SM) keep the round-robin
+// deal.
 constexpr int kCombinePre = 8;
+constexpr int kCombineBalancedMaxW = 4096;
+
+// A pair's cost in the balanced deal (ns = 0: a pair that is only zeroed).
+__host__ __device__ inline int combine_cost(int ns) {
+    return ns > 0 ? kCombinePre * ((ns + kCombinePre - 1) / kCombinePre) + ns : 1;
+}
+
+// The balanced deal is used where warps have several pairs each (with about
+// one pair per warp, round-robin gives every warp a single pair and the
+// balanced deal could give a warp two), its tables fit in shared memory and
+// its 32-bit cost sums cannot overflow (a pair costs at most 2·s_max + kCombinePre).
+constexpr int kCombineBalancedMinPairsPerWarp = 4;
+__host__ __device__ inline bool combine_balanced(int W, int Hq, int s_max, int n_warps) {
+    return W <= kCombineBalancedMaxW &&
+           static_cast<long long>(W) * Hq >= static_cast<long long>(kCombineBalancedMinPairsPerWarp) * n_warps &&
+           static_cast<long long>(W) * Hq * (2ll * s_max + kCombinePre) < (1ll << 31);
+}
+
+// Shared-memory bytes of the balanced deal's tables (0: round-robin deal).
+inline size_t combine_smem_bytes(int W, int Hq, int s_max, int n_warps) {
+    return combine_balanced(W, Hq, s_max, n_warps) ? static_cast<size_t>(2 * W + 1) * sizeof(int) : 0;
+}
 
 struct CombineRow {
     int slot, pos, slot0;
@@ -1103,13 +1136,156 @@ BIV_DEV CombineRow combine_row(const AttnParams& P, long long pair) {
     return CombineRow{P.row_slot[w], P.row_pos[w], P.row_slot[grp0]};
 }
 
+// Splits to combine for a row (0: the row is not attended and its output is zero).
+BIV_DEV int combine_splits(const AttnParams& P, const CombineRow& rw) {
+    const int p = rw.pos;
+    if (rw.slot < 0 || rw.slot >= P.n_slots || p < 0 || p >= P.max_len || rw.slot != rw.slot0) return 0;
+    return p / SPLIT + 1;
+}
+
+// The whole warp combines pair `pair` over its ns splits (ns = 0: zeros).
+BIV_DEV void combine_pair(const AttnParams& P, __nv_bfloat16* __restrict__ out, long long pair, int ns, int lane) {
+    __nv_bfloat16* dst = out + pair * HD + lane * 4;
+    if (ns <= 0) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+        return;
+    }
+    const long long base = pair * P.s_max;
+    const float4* src0 = reinterpret_cast<const float4*>(P.ws_o + base * HD) + lane;
+    float4 pre[kCombinePre];
+#pragma unroll
+    for (int j = 0; j < kCombinePre; ++j)
+        pre[j] = j < ns ? src0[static_cast<long long>(j) * (HD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    // (m, l) of the first 64 splits in the same round (a pair of 33 splits,
+    // from a context of 8192, would otherwise wait twice more for split 33's)
+    const float m0 = lane < ns ? P.ws_m[base + lane] : -INFINITY;
+    const float l0 = lane < ns ? P.ws_l[base + lane] : 0.0f;
+    const float m1 = 32 + lane < ns ? P.ws_m[base + 32 + lane] : -INFINITY;
+    const float l1 = 32 + lane < ns ? P.ws_l[base + 32 + lane] : 0.0f;
+    // Row maximum over all splits.
+    float M = -INFINITY;
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+        float m = s0 == 0 ? m0 : s0 == 32 ? m1 : (s0 + lane < ns) ? P.ws_m[base + s0 + lane] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        M = fmaxf(M, m);
+    }
+    float L = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+        const int s = s0 + lane;
+        const float ms = s0 == 0 ? m0 : s0 == 32 ? m1 : (s < ns) ? P.ws_m[base + s] : -INFINITY;
+        const float ls = s0 == 0 ? l0 : s0 == 32 ? l1 : (s < ns) ? P.ws_l[base + s] : 0.0f;
+        const float wgt = (s < ns) ? exp2f(ms - M) : 0.0f;
+        float lw = (s < ns) ? wgt * ls : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+        L += lw;
+        const int cnt = min(32, ns - s0);
+        const float4* src = src0 + static_cast<long long>(s0) * (HD / 4);
+        for (int j0 = 0; j0 < cnt; j0 += kCombinePre) {
+            if (s0 > 0 || j0 > 0) {
+                // the next kCombinePre splits in one round of loads (the first
+                // ones were prefetched above)
+#pragma unroll
+                for (int q = 0; q < kCombinePre; ++q)
+                    pre[q] = j0 + q < cnt ? src[static_cast<long long>(j0 + q) * (HD / 4)]
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            // summed in increasing split order, indexed statically (warp-uniform guard)
+#pragma unroll
+            for (int q = 0; q < kCombinePre; ++q) {
+                if (j0 + q < cnt) {
+                    const float wj = __shfl_sync(0xffffffffu, wgt, j0 + q);
+                    acc.x += wj * pre[q].x;
+                    acc.y += wj * pre[q].y;
+                    acc.z += wj * pre[q].z;
+                    acc.w += wj * pre[q].w;
+                }
+            }
+        }
+    }
+    const float inv = 1.0f / L;
+    uint2 r;
+    r.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    r.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(dst) = r;
+}
+
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
-    const long long n_pairs = static_cast<long long>(P.W) * P.Hq;
-    const long long first = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    const long long stride = static_cast<long long>(gridDim.x) * 8;
-    const int lane = threadIdx.x & 31;
-    // Lane i holds the row of the warp's pair first + i * stride (32 at a time).
+    extern __shared__ int s_comb[];             // balanced deal: [W + 1] prefix costs, [W] splits per row
+    const int W = P.W, Hq = P.Hq;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_warps = static_cast<int>(gridDim.x) * 8;
+    const int gw = static_cast<int>(blockIdx.x) * 8 + warp;
+    if (combine_balanced(W, Hq, P.s_max, n_warps)) {
+        int* s_cum = s_comb;
+        int* s_ns = s_comb + W + 1;
+        __shared__ int s_wsum[8];
+        // each thread a contiguous run of rows: their splits and cost
+        const int per = (W + 255) / 256;
+        const int r0 = min(W, static_cast<int>(threadIdx.x) * per), r1 = min(W, r0 + per);
+        int sum = 0;
+        for (int i = r0; i < r1; ++i) {
+            const int w = i;
+            const int grp0 = (w / P.rows_per_group) * P.rows_per_group;
+            const int ns = combine_splits(P, CombineRow{P.row_slot[w], P.row_pos[w], P.row_slot[grp0]});
+            s_ns[i] = ns;
+            sum += Hq * combine_cost(ns);
+        }
+        // exclusive prefix of the threads' sums: warp scan, then the warps' totals
+        int inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        if (lane == 31) s_wsum[warp] = inc;
+        __syncthreads();
+        int run = inc - sum;
+        for (int k = 0; k < warp; ++k) run += s_wsum[k];
+        for (int i = r0; i < r1; ++i) {
+            s_cum[i] = run;
+            run += Hq * combine_cost(s_ns[i]);
+        }
+        if (threadIdx.x == 255) s_cum[W] = run;     // the last thread's run ends at the total
+        __syncthreads();
+        pdl_wait();
+        pdl_trigger();
+        const long long T = s_cum[W];
+        const long long lo = T * gw / n_warps, hi = T * (gw + 1) / n_warps;
+        // the last row whose cost interval starts at or before lo
+        int a = 0, b = W - 1;
+        while (a < b) {
+            const int m = (a + b + 1) >> 1;
+            if (s_cum[m] <= lo) a = m;
+            else b = m - 1;
+        }
+        int i = a;
+        int u = combine_cost(s_ns[i]);
+        int h = static_cast<int>((lo - s_cum[i] + u - 1) / u);   // first head starting at or after lo
+        if (h >= Hq) {
+            ++i;
+            h = 0;
+        }
+#pragma unroll 1
+        while (i < W) {
+            u = combine_cost(s_ns[i]);
+            if (s_cum[i] + static_cast<long long>(h) * u >= hi) break;
+            combine_pair(P, out, static_cast<long long>(i) * Hq + h, s_ns[i], lane);
+            if (++h == Hq) {
+                h = 0;
+                ++i;
+            }
+        }
+        return;
+    }
+    // round-robin deal: warp g takes pairs g, g + NW, ...; lane i holds the
+    // row of the warp's pair first + i * NW (32 at a time)
+    const long long n_pairs = static_cast<long long>(W) * Hq;
+    const long long first = gw;
+    const long long stride = n_warps;
     CombineRow mine = first + lane * stride < n_pairs ? combine_row(P, first + lane * stride)
                                                       : CombineRow{-1, -1, -1};
     pdl_wait();
@@ -1124,72 +1300,7 @@ attn_combine_kernel(const AttnParams P, __nv_bfloat16* __restrict__ out) {
         }
         const CombineRow rw{__shfl_sync(0xffffffffu, mine.slot, k), __shfl_sync(0xffffffffu, mine.pos, k),
                             __shfl_sync(0xffffffffu, mine.slot0, k)};
-        __nv_bfloat16* dst = out + pair * HD + lane * 4;
-        const int p = rw.pos;
-        if (rw.slot < 0 || rw.slot >= P.n_slots || p < 0 || p >= P.max_len || rw.slot != rw.slot0) {
-            *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
-            continue;
-        }
-        const int ns = p / SPLIT + 1;
-        const long long base = pair * P.s_max;
-        const float4* src0 = reinterpret_cast<const float4*>(P.ws_o + base * HD) + lane;
-        float4 pre[kCombinePre];
-#pragma unroll
-        for (int j = 0; j < kCombinePre; ++j)
-            pre[j] = j < ns ? src0[static_cast<long long>(j) * (HD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float m0 = lane < ns ? P.ws_m[base + lane] : -INFINITY;
-        const float l0 = lane < ns ? P.ws_l[base + lane] : 0.0f;
-        // Row maximum over all splits.
-        float M = -INFINITY;
-        for (int s0 = 0; s0 < ns; s0 += 32) {
-            float m = s0 == 0 ? m0 : (s0 + lane < ns) ? P.ws_m[base + s0 + lane] : -INFINITY;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            M = fmaxf(M, m);
-        }
-        float L = 0.0f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < ns; s0 += 32) {
-            const int s = s0 + lane;
-            const float ms = s0 == 0 ? m0 : (s < ns) ? P.ws_m[base + s] : -INFINITY;
-            const float ls = s0 == 0 ? l0 : (s < ns) ? P.ws_l[base + s] : 0.0f;
-            const float wgt = (s < ns) ? exp2f(ms - M) : 0.0f;
-            float lw = (s < ns) ? wgt * ls : 0.0f;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-            L += lw;
-            const int cnt = min(32, ns - s0);
-            const float4* src = src0 + static_cast<long long>(s0) * (HD / 4);
-            int j = 0;
-            if (s0 == 0) {
-                // the prefetched splits, indexed statically (warp-uniform guard)
-#pragma unroll
-                for (int q = 0; q < kCombinePre; ++q) {
-                    if (q < cnt) {
-                        const float wj = __shfl_sync(0xffffffffu, wgt, q);
-                        acc.x += wj * pre[q].x;
-                        acc.y += wj * pre[q].y;
-                        acc.z += wj * pre[q].z;
-                        acc.w += wj * pre[q].w;
-                    }
-                }
-                j = kCombinePre;
-            }
-#pragma unroll 4
-            for (; j < cnt; ++j) {
-                const float wj = __shfl_sync(0xffffffffu, wgt, j);
-                const float4 v = src[static_cast<long long>(j) * (HD / 4)];
-                acc.x += wj * v.x;
-                acc.y += wj * v.y;
-                acc.z += wj * v.z;
-                acc.w += wj * v.w;
-            }
-        }
-        const float inv = 1.0f / L;
-        uint2 r;
-        r.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        r.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(dst) = r;
+        combine_pair(P, out, pair, combine_splits(P, rw), lane);
     }
 }
 
@@ -1407,7 +1518,10 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
                                          static_cast<int>(kPPSmemMax));
             if (e != cudaSuccess) return cuda_status(e);
             int per = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_combine_kernel, 256, 0) != cudaSuccess ||
+            // with the balanced deal's largest tables
+            const size_t comb_smem = static_cast<size_t>(2 * kCombineBalancedMaxW + 1) * sizeof(int);
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_combine_kernel, 256, comb_smem) !=
+                    cudaSuccess ||
                 per < 1)
                 per = 1;
             per_sm[dev] = per;
@@ -1434,8 +1548,8 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
     if (st != BIV_OK) return st;
     const long long n_pairs = static_cast<long long>(W) * Hq;
     const long long cgrid = std::min<long long>((n_pairs + 7) / 8, static_cast<long long>(num_sms()) * combine_per_sm);
-    return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(cgrid)), dim3(256), 0, s, P,
-                      static_cast<__nv_bfloat16*>(o));
+    return launch_pdl(attn_combine_kernel, dim3(static_cast<unsigned>(cgrid)), dim3(256), combine_smem_bytes(W, Hq, P.s_max, static_cast<int>(cgrid) * 8), s,
+                      P, static_cast<__nv_bfloat16*>(o));
 }
 
 extern "C" int biv_rope_qk(const void* qkv, void* q_out, void* k_out, const int32_t* row_pos, int W, int Hq,

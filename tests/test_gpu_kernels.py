@@ -280,12 +280,15 @@ def test_attention_two_item_and_one_item_kernels_same_bits():
     assert_close(big[rows], ref, what="attention (one item per SM)")
 
 
-def test_attention_combine_many_pairs_per_warp():
-    """W = 4096 rows x 32 heads = 131072 (row, head) pairs: more than 32 per
-    combine warp, so a warp reads the slots and positions of its pairs in
-    several rounds of 32.  Sampled rows match the oracle, and the first 256
-    rows give the same bits when they are the whole window."""
-    W, Hq, Hkv, K, n_slots, max_len = 4096, 32, 8, 16, 16, 700
+@pytest.mark.parametrize("W", [4096, 4352])
+def test_attention_combine_many_pairs_per_warp(W):
+    """W x 32 heads (row, head) pairs, many per combine warp.  At W = 4096 the
+    combine deals the pairs by cost (the largest window with that deal); at
+    W = 4352 it deals them round-robin and a warp reads the slots and
+    positions of its pairs in several rounds of 32.  Sampled rows match the
+    oracle, and the first 1024 rows give the same bits when they are the whole
+    window (about nine pairs per combine warp: the balanced deal)."""
+    Hq, Hkv, K, n_slots, max_len = 32, 8, 16, 16, 700
     g = synth.generator(4096)
     kc = synth.bf16_normal((n_slots, Hkv, max_len, 128), 1.0, g)
     vc = synth.bf16_normal((n_slots, Hkv, max_len, 128), 1.0, g)
@@ -295,11 +298,11 @@ def test_attention_combine_many_pairs_per_warp():
     pos = ((req * 37) % 600 + 40 + np.arange(W) % K).astype(np.int32)
     qd, kd, vd = dev(q), dev(kc), dev(vc)
     big = _run_attn(qd, kd, vd, slot, pos, K)
-    small = _run_attn(qd[:256].contiguous(), kd, vd, slot[:256], pos[:256], K)
-    assert same_bits(big[:256], small)
-    rows = [0, 15, 2047, 3000, 4095]
+    small = _run_attn(qd[:1024].contiguous(), kd, vd, slot[:1024], pos[:1024], K)
+    assert same_bits(big[:1024], small)
+    rows = [0, 15, 2047, 3000, W - 1]
     ref = oracle.attention(q[rows], kc, vc, slot[rows], pos[rows])
-    assert_close(big[rows], ref, what="attention, 131072 pairs")
+    assert_close(big[rows], ref, what=f"attention, {W * Hq} pairs")
     assert not torch.isnan(big.float()).any()
 
 
