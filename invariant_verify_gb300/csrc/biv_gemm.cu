@@ -65,7 +65,36 @@ struct GemmArgs {
     int a_rows;      // rows of A copied per k-block (multiple of 8, <= 128)
     uint32_t idesc;  // tcgen05 instruction descriptor for M=128, N=BN
     uint32_t tmem_cols;
+    // Narrow tail (CTA pairs, fused selection): column tiles [0, nt_full) are
+    // BN wide and the rest bn_tail wide (tensor map tmB1, descriptor
+    // idesc_tail), so that the last, partial wave of full tiles becomes one
+    // wave of tiles half as wide.  bn_tail = 0: every column tile is BN wide.
+    int nt_full;
+    int bn_tail;
+    uint32_t idesc_tail;
 };
+
+// Tile t of the persistent schedule (row tiles fastest): its row tile, first
+// column, width and column-tile index (the selection's winner slot).
+struct TileAt {
+    int m_blk, col0, bn, slot;
+};
+
+BIV_DEV TileAt tile_at(const GemmArgs& g, int t, int m_tiles) {
+    const int full = g.nt_full * m_tiles;
+    if (g.bn_tail == 0 || t < full) {
+        const int nb = t / m_tiles;
+        return TileAt{t - nb * m_tiles, nb * g.BN, g.BN, nb};
+    }
+    const int u = t - full, nb = u / m_tiles;
+    return TileAt{u - nb * m_tiles, g.nt_full * g.BN + nb * g.bn_tail, g.bn_tail, g.nt_full + nb};
+}
+
+// Column tiles of the schedule (full and narrow).
+BIV_DEV int column_tiles(const GemmArgs& g) {
+    return g.bn_tail == 0 ? (g.N + g.BN - 1) / g.BN
+                          : g.nt_full + (g.N - g.nt_full * g.BN + g.bn_tail - 1) / g.bn_tail;
+}
 
 inline int stage_bytes(int KS, int a_rows, int BN) { return KS * (a_rows + BN) * kRowBytes; }
 
@@ -81,7 +110,8 @@ BIV_DEV void stage_range(const GemmArgs& g, int sb, int& kb0, int& nkb) {
 }
 
 // Selection fused into the LM-head epilogue (EPI 3): every tile-row's Gumbel
-// winner, packed as (order(key) << 32 | ~v), goes to cand[row * n_tiles + n_blk].
+// winner, packed as (order(key) << 32 | ~v), goes to cand[row * n_cols + c] for
+// column tile c (n_cols column tiles in all, see TailPlan).
 struct SelectArgs {
     const uint32_t* row_req;
     const int32_t* row_pos;
@@ -553,7 +583,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const int M = g.M, N = g.N, BN = g.BN;
     const int BNL = BN / CG;                      // B rows this CTA copies per tile
     const int m_tiles = (M + TM - 1) / TM;
-    const int n_tiles = (N + BN - 1) / BN;
+    const int n_tiles = column_tiles(g);
     const int n_work = m_tiles * n_tiles;
     const int KB = g.KB;
     const int KS = g.KS;
@@ -606,7 +636,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     // expects both from the start.
     int b_early = 0;
     if (warp == 0 && lane == 0 && unit < n_work) {
-        const int n_blk0 = unit / m_tiles;
+        const int n_blk0 = unit / m_tiles;      // a unit's first tile is a full one (the tail follows whole waves)
         b_early = min(S, n_stage_blocks);
         for (int sb = 0; sb < b_early; ++sb) {
             uint8_t* sa = tiles + sb * STAGE;
@@ -640,8 +670,11 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             long long issued = 0;
             bool ok = true;
             for (int t = unit; t < n_work && ok; t += n_units) {
-                const int n_blk = t / m_tiles;
-                const int m_blk = t - n_blk * m_tiles;
+                const TileAt ti = tile_at(g, t, m_tiles);
+                const int m_blk = ti.m_blk;
+                const int bnl_t = ti.bn / CG;
+                const CUtensorMap* tmBt = ti.bn == BN ? &tmB : &tmB1;
+                const uint32_t tx_t = static_cast<uint32_t>(A_BYTES + KS * bnl_t * kRowBytes);
                 for (int sb = 0; sb < n_stage_blocks; ++sb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_gemm_err, true, CG == 2)) {
                         ok = false;
@@ -653,21 +686,21 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     const bool b_done = t == unit && sb < b_early;   // B requested early
                     if constexpr (CG == 2) {
                         const uint32_t fb = mapa_shared(&full[stage], 0);
-                        if (!b_done && rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx_bytes);
+                        if (!b_done && rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx_t);
                         tma_load_3d_pair(sa, &tmA, fb, 0, m_blk * TM + rank * kBM, kb0, pol_a);
-                        if (!b_done) tma_load_3d_pair(sa + A_BYTES, &tmB, fb, 0, n_blk * BN + rank * BNL, kb0, pol_b);
+                        if (!b_done) tma_load_3d_pair(sa + A_BYTES, tmBt, fb, 0, ti.col0 + rank * bnl_t, kb0, pol_b);
                     } else if (g.first1 && sb == 0) {
                         if (!b_done) mbar_arrive_expect_tx(&full[stage], tx_bytes1);
                         tma_load_3d(sa, &tmA1, &full[stage], 0, m_blk * kBM, 0, pol_a);
-                        if (!b_done) tma_load_3d(sa + A_BYTES, &tmB1, &full[stage], 0, n_blk * BN, 0, pol_b);
+                        if (!b_done) tma_load_3d(sa + A_BYTES, &tmB1, &full[stage], 0, ti.col0, 0, pol_b);
                     } else if (g.three_d) {
                         if (!b_done) mbar_arrive_expect_tx(&full[stage], tx_bytes);
                         tma_load_3d(sa, &tmA, &full[stage], 0, m_blk * kBM, kb0, pol_a);
-                        if (!b_done) tma_load_3d(sa + A_BYTES, &tmB, &full[stage], 0, n_blk * BN, kb0, pol_b);
+                        if (!b_done) tma_load_3d(sa + A_BYTES, &tmB, &full[stage], 0, ti.col0, kb0, pol_b);
                     } else {
                         if (!b_done) mbar_arrive_expect_tx(&full[stage], tx_bytes);
                         tma_load_2d(sa, &tmA, &full[stage], sb * kBK, m_blk * kBM, pol_a);
-                        if (!b_done) tma_load_2d(sa + A_BYTES, &tmB, &full[stage], sb * kBK, n_blk * BN, pol_b);
+                        if (!b_done) tma_load_2d(sa + A_BYTES, &tmB, &full[stage], sb * kBK, ti.col0, pol_b);
                     }
                     ++issued;
                     if (++stage == S) {
@@ -711,6 +744,9 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     break;
                 }
                 tc_fence_after();
+                const TileAt ti = tile_at(g, t, m_tiles);
+                const uint32_t idesc_t = ti.bn == BN ? g.idesc : g.idesc_tail;
+                const int bnl_t = ti.bn / CG;
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int sb = 0; sb < n_stage_blocks; ++sb) {
                     if (!__all_sync(0xffffffffu,
@@ -726,15 +762,15 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     for (int j = 0; j < nkb; ++j) {
                         const int kb = kb0 + j;
                         const uint64_t a_desc = sw128_kmajor_desc(a_addr + static_cast<uint32_t>(j * g.a_rows * kRowBytes));
-                        const uint64_t b_desc = sw128_kmajor_desc(b_addr + static_cast<uint32_t>(j * BNL * kRowBytes));
+                        const uint64_t b_desc = sw128_kmajor_desc(b_addr + static_cast<uint32_t>(j * bnl_t * kRowBytes));
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k) {
                             // +32 bytes along K inside the swizzle row = +2 in 16-byte units.
                             if constexpr (CG == 2)
-                                umma_bf16_pair_elect(d_tmem, a_desc + 2u * k, b_desc + 2u * k, g.idesc,
+                                umma_bf16_pair_elect(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_t,
                                                      (kb > 0 || k > 0) ? 1u : 0u);
                             else
-                                umma_bf16_elect(d_tmem, a_desc + 2u * k, b_desc + 2u * k, g.idesc,
+                                umma_bf16_elect(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_t,
                                                 (kb > 0 || k > 0) ? 1u : 0u);
                         }
                     }
@@ -791,8 +827,9 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         unsigned long long run = 0;                 // EPI 3, CG = 2: see below
         int run_mblk = -1;
         for (int t = unit; t < n_work; t += n_units) {
-            const int n_blk = t / m_tiles;
-            const int m_blk = t - n_blk * m_tiles;
+            const TileAt ti = tile_at(g, t, m_tiles);
+            const int m_blk = ti.m_blk;
+            const int bnt = ti.bn, col0 = ti.col0;                 // this tile's width and first column
             const int row_base = m_blk * TM + rank * kBM;          // first row of this CTA's 128
             if constexpr (EPI == 3 && CG == 1) {
                 // This tile's noise buckets while its MMAs run; the vote below is
@@ -800,7 +837,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 // (CG = 2 draws them per chunk: the epilogue of a tile runs
                 // under the next tile's MMAs.)
                 if (!sel.greedy)
-                    tile_buckets<NT>(bk, g.a_rows, min(kBM, M - m_blk * kBM), BN, n_blk * BN, N, m_blk * kBM, sel);
+                    tile_buckets<NT>(bk, g.a_rows, min(kBM, M - m_blk * kBM), bnt, col0, N, m_blk * kBM, sel);
             }
             // One thread polls the accumulator barrier; the vote hands its
             // outcome to the other 127 (no polling traffic beside the copies).
@@ -828,8 +865,8 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 // warps 2-5 take the tile's first half of 32-column chunks, warps
                 // 6-9 the rest; their winners meet in shared memory
                 const int eset = (warp - 2) >> 2;
-                const int nch = BN / kChunk, h1 = (nch + 1) / 2;
-                const int cb = eset ? h1 * kChunk : 0, ce = eset ? BN : h1 * kChunk;
+                const int nch = bnt / kChunk, h1 = (nch + 1) / 2;
+                const int cb = eset ? h1 * kChunk : 0, ce = eset ? bnt : h1 * kChunk;
                 float* cmt = cmax + (eset * kBM + q * 32 + lane) * kMaxChunks;
                 unsigned long long best;
                 if constexpr (CG == 2) {
@@ -840,19 +877,19 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     if (run_mblk != m_blk) run = 0;
                     else if (live) run = umax64(run, s_run[rloc]);
                     run_mblk = m_blk;
-                    best = tile_row_winner<32, true>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab,
+                    best = tile_row_winner<32, true>(taddr, cb, ce, col0, N, slive, req, pos, sel, ntab,
                                                      nullptr, 0, cmt, lrow, run);
                 }
                 else
-                    best = g.m64 ? tile_row_winner<16>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab,
+                    best = g.m64 ? tile_row_winner<16>(taddr, cb, ce, col0, N, slive, req, pos, sel, ntab,
                                                        bk + srloc, g.a_rows, cmt, lrow)
-                                 : tile_row_winner<32>(taddr, cb, ce, n_blk * BN, N, slive, req, pos, sel, ntab,
+                                 : tile_row_winner<32>(taddr, cb, ce, col0, N, slive, req, pos, sel, ntab,
                                                        bk + srloc, g.a_rows, cmt, lrow);
                 if (eset == 1 && live) s_best[rloc] = best;
                 epilogue_bar<NT>();   // both halves' winners are in; every row is done with the buckets
                 if (eset == 0 && live) {
                     const unsigned long long w = umax64(best, s_best[rloc]);
-                    sel.cand[static_cast<long long>(srow) * n_tiles + n_blk] = w;
+                    sel.cand[static_cast<long long>(srow) * n_tiles + ti.slot] = w;
                     if constexpr (CG == 2) s_run[rloc] = w;    // read by both halves at the next tile
                 }
             } else if constexpr (EPI == 4) {
@@ -874,8 +911,8 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 if (g.m64) {
                     RopeAngles<4> ang;
 #pragma unroll 1
-                    for (int c = 0; c < BN; c += 16) {
-                        const int col = n_blk * BN + c;
+                    for (int c = 0; c < bnt; c += 16) {
+                        const int col = col0 + c;
                         uint32_t ra[4], rb[4];
                         tmem_ld16x2_x4_pair_sync(taddr + static_cast<uint32_t>(c),
                                                  taddr + static_cast<uint32_t>(c + 8), ra, rb);
@@ -885,8 +922,8 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 } else {
                     RopeAngles<8> ang;
 #pragma unroll 1
-                    for (int c = 0; c < BN; c += 16) {
-                        const int col = n_blk * BN + c;
+                    for (int c = 0; c < bnt; c += 16) {
+                        const int col = col0 + c;
                         uint32_t r[16];
                         tmem_ld16(taddr + static_cast<uint32_t>(c), r);
                         tmem_ld_wait();
@@ -904,11 +941,11 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     const int prow = row_base + q * 16 + (lane & 15);
                     const int hi = lane >> 4;
 #pragma unroll 1
-                    for (int c = 0; c < BN; c += 32) {
+                    for (int c = 0; c < bnt; c += 32) {
                         uint32_t gr[8], ur[8];
                         tmem_ld16x2_x8_pair_sync(taddr + static_cast<uint32_t>(c),
                                                  taddr + static_cast<uint32_t>(c + 16), gr, ur);
-                        const int col = n_blk * BN + c;
+                        const int col = col0 + c;
                         if (prow < M && col < N) {
                             uint32_t o[4];
 #pragma unroll
@@ -922,12 +959,12 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     }
                 } else
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = 0; c < bnt; c += 32) {
                     uint32_t gr[16], ur[16];
                     tmem_ld16(taddr + static_cast<uint32_t>(c), gr);
                     tmem_ld16(taddr + static_cast<uint32_t>(c + 16), ur);
                     tmem_ld_wait();
-                    const int col = n_blk * BN + c;
+                    const int col = col0 + c;
                     if (live && col < N) {
                         uint32_t o[8];
 #pragma unroll
@@ -942,14 +979,14 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 }
             } else {
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
+            for (int c = 0; c < bnt; c += 16) {
                 uint32_t r[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(c), r);
                 tmem_ld_wait();
                 if (live) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const int col = n_blk * BN + c + h * 8;
+                        const int col = col0 + c + h * 8;
                         if (col < N) {
                             const uint32_t* v = r + h * 8;
                             if constexpr (EPI == 1) {
@@ -1077,9 +1114,39 @@ int kernel_setup(int dev, int smem_max, int* resident_units) {
     return BIV_OK;
 }
 
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// The narrow tail of the fused selection's CTA-pair schedule.  With work
+// tiles on a wave of kPairWave pairs, the last wave holds r = work mod wave
+// tiles; when those are whole column tiles (row tiles fastest) and twice r
+// still fits one wave, they are re-cut into tiles half as wide (a multiple of
+// 32, at least 64), so that every pair ends with a short tile instead of some
+// pairs with a whole one.  The LM head at W = 1024 (2004 tiles of 256 columns
+// on 76 pairs: 28 in the last wave) ends about one half tile sooner.  Each
+// element's arithmetic does not depend on the tile width.
+struct TailPlan {
+    int nt_full, bn_tail, n_cols;     // full column tiles, tail width (0: none), column tiles in all
+};
+
+inline TailPlan tail_plan(int M, int N, int BN, bool pairs) {
+    const int n_tiles = static_cast<int>(ceil_div(N, BN));
+    TailPlan p{n_tiles, 0, n_tiles};
+    if (!pairs) return p;
+    const long long m_tiles = ceil_div(M, 2 * kBM);
+    const long long work = m_tiles * n_tiles;
+    const long long wave = std::min<long long>(work, kPairWave);
+    const long long r = work % wave;
+    const int bt = BN / 2;
+    if (r == 0 || r % m_tiles != 0 || 2 * r > wave || bt % 32 != 0 || bt < 64) return p;
+    const int nt_full = n_tiles - static_cast<int>(r / m_tiles);
+    const int nt_tail = static_cast<int>(ceil_div(N - static_cast<long long>(nt_full) * BN, bt));
+    if (m_tiles * nt_tail > wave) return p;
+    return TailPlan{nt_full, bt, nt_full + nt_tail};
+}
+
 template <int EPI, int CG>
 int launch_gemm_cg(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream,
-                   const SelectArgs& sel, const RopeArgs& rp) {
+                   const SelectArgs& sel, const RopeArgs& rp, int* n_cols) {
     GemmArgs g;
     g.M = M;
     g.N = N;
@@ -1106,7 +1173,7 @@ int launch_gemm_cg(const void* A, const void* B, void* C, int M, int N, int K, i
     // pad, the barriers and (non-selection epilogues) up to 1 KiB of the
     // kernel's static shared memory.
     const int ring = EPI == 3 ? kMaxSmem - 1024 - kBarBytes - extra : kMaxSmem - 2048 - kBarBytes;
-    const long long work = static_cast<long long>((M + kBM * CG - 1) / (kBM * CG)) * ((N + BN - 1) / BN);
+    const long long work = static_cast<long long>((M + kBM * CG - 1) / (kBM * CG)) * ((N + BN - 1) / BN);   // full-width tiles
     const int smem_max = EPI == 3 ? kMaxSmem : kMaxSmem - 1024;
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
@@ -1136,6 +1203,13 @@ int launch_gemm_cg(const void* A, const void* B, void* C, int M, int N, int K, i
     g.stages = std::min(kMaxStages, std::max(1, (ring - tail) / stage_bytes(ks, g.a_rows, BNL)));
     g.idesc = idesc_bf16_f32(CG == 2 ? 2 * kBM : (g.m64 ? 64 : kBM), BN);
     g.tmem_cols = tmem_cols_for(BN);
+    // the narrow tail: the fused selection on pairs, when the wave it is
+    // planned for is the resident one (a unit's first tile is then a full one)
+    const TailPlan tp = tail_plan(M, N, BN, EPI == 3 && CG == 2 && units == kPairWave);
+    g.nt_full = tp.nt_full;
+    g.bn_tail = tp.bn_tail;
+    g.idesc_tail = tp.bn_tail ? idesc_bf16_f32(2 * kBM, tp.bn_tail) : g.idesc;
+    if (n_cols) *n_cols = tp.n_cols;
     CUtensorMap ta, tb, ta1, tb1;
     if (!encode_kmajor(&ta, A, K, M, g.a_rows, ks, g.three_d) || !encode_kmajor(&tb, B, K, N, BNL, ks, g.three_d)) {
         set_cuda_error(cudaErrorInvalidValue);
@@ -1145,6 +1219,11 @@ int launch_gemm_cg(const void* A, const void* B, void* C, int M, int N, int K, i
     tb1 = tb;
     if (g.first1 &&
         (!encode_kmajor(&ta1, A, K, M, g.a_rows, 1, true) || !encode_kmajor(&tb1, B, K, N, BN, 1, true))) {
+        set_cuda_error(cudaErrorInvalidValue);
+        return BIV_ERR_CUDA;
+    }
+    // the tail's B boxes (first1 is never set with pairs)
+    if (g.bn_tail && !encode_kmajor(&tb1, B, K, N, g.bn_tail / CG, ks, g.three_d)) {
         set_cuda_error(cudaErrorInvalidValue);
         return BIV_ERR_CUDA;
     }
@@ -1166,9 +1245,10 @@ inline bool pair_bn_ok(int BN) { return BN % 32 == 0 && BN >= 64 && BN <= 256; }
 
 template <int EPI>
 int launch_gemm(const void* A, const void* B, void* C, int M, int N, int K, int BN, cudaStream_t stream,
-                const SelectArgs& sel = SelectArgs{}, const RopeArgs& rp = RopeArgs{}) {
-    if (use_pair(M, K) && pair_bn_ok(BN)) return launch_gemm_cg<EPI, 2>(A, B, C, M, N, K, BN, stream, sel, rp);
-    return launch_gemm_cg<EPI, 1>(A, B, C, M, N, K, BN, stream, sel, rp);
+                const SelectArgs& sel = SelectArgs{}, const RopeArgs& rp = RopeArgs{}, int* n_cols = nullptr) {
+    if (use_pair(M, K) && pair_bn_ok(BN))
+        return launch_gemm_cg<EPI, 2>(A, B, C, M, N, K, BN, stream, sel, rp, n_cols);
+    return launch_gemm_cg<EPI, 1>(A, B, C, M, N, K, BN, stream, sel, rp, n_cols);
 }
 
 int check_gemm(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K) {
@@ -1181,7 +1261,6 @@ int check_gemm(const void* A, const void* B, void* C, int out_dtype, int M, int 
     return BIV_OK;
 }
 
-long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 // Packed row p: block j = p / 32; rows 32j..32j+15 are gate rows 16j..16j+15,
 // rows 32j+16..32j+31 the up rows 16j..16j+15 (source: F gate rows, then F up rows).
@@ -1381,8 +1460,10 @@ static int lm_head_tile_n(int M, int N, int K) {
 
 extern "C" size_t biv_lm_head_gumbel_workspace_size(int M, int N, int K) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    const long long n_tiles = ceil_div(N, lm_head_tile_n(M, N, K));
-    return static_cast<size_t>(M) * static_cast<size_t>(n_tiles) * sizeof(unsigned long long);
+    // one winner slot per column tile, with the narrow tail where it is planned
+    const int bn = lm_head_tile_n(M, N, K);
+    const long long n_cols = tail_plan(M, N, bn, use_pair(M, K) && pair_bn_ok(bn)).n_cols;
+    return static_cast<size_t>(M) * static_cast<size_t>(n_cols) * sizeof(unsigned long long);
 }
 
 extern "C" int biv_lm_head_gumbel(const void* A, const void* B, float* logits, int M, int N, int K,
@@ -1396,7 +1477,7 @@ extern "C" int biv_lm_head_gumbel(const void* A, const void* B, float* logits, i
         return BIV_ERR_ALIGN;
     if (ws_bytes < biv_lm_head_gumbel_workspace_size(M, N, K)) return BIV_ERR_SHAPE;
     const int bn = lm_head_tile_n(M, N, K);
-    const int n_tiles = static_cast<int>(ceil_div(N, bn));
+    int n_tiles = static_cast<int>(ceil_div(N, bn));     // column tiles (winner slots per row) of the launch
     SelectArgs sel;
     sel.row_req = row_req;
     sel.row_pos = row_pos;
@@ -1406,7 +1487,7 @@ extern "C" int biv_lm_head_gumbel(const void* A, const void* B, float* logits, i
     sel.greedy = temperature == 0.0f;
     sel.invT = sel.greedy ? 0.0f : 1.0f / temperature;    // fl(1/T), IEEE division on the host
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int st = launch_gemm<3>(A, B, logits, M, N, K, bn, s, sel);
+    const int st = launch_gemm<3>(A, B, logits, M, N, K, bn, s, sel, RopeArgs{}, &n_tiles);
     if (st != BIV_OK) return st;
     return launch_pdl(tile_winners_kernel, dim3((M + 7) / 8), dim3(256), 0, s,
                       static_cast<const unsigned long long*>(workspace), M, n_tiles, tokens);
@@ -1427,7 +1508,7 @@ extern "C" int biv_lm_head_gumbel_accept(const void* A, const void* B, float* lo
         return BIV_ERR_ALIGN;
     if (ws_bytes < biv_lm_head_gumbel_workspace_size(M, N, K)) return BIV_ERR_SHAPE;
     const int bn = lm_head_tile_n(M, N, K);
-    const int n_tiles = static_cast<int>(ceil_div(N, bn));
+    int n_tiles = static_cast<int>(ceil_div(N, bn));     // column tiles (winner slots per row) of the launch
     SelectArgs sel;
     sel.row_req = row_req;
     sel.row_pos = row_pos;
@@ -1437,7 +1518,7 @@ extern "C" int biv_lm_head_gumbel_accept(const void* A, const void* B, float* lo
     sel.greedy = temperature == 0.0f;
     sel.invT = sel.greedy ? 0.0f : 1.0f / temperature;    // fl(1/T), IEEE division on the host
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int st = launch_gemm<3>(A, B, logits, M, N, K, bn, s, sel);
+    const int st = launch_gemm<3>(A, B, logits, M, N, K, bn, s, sel, RopeArgs{}, &n_tiles);
     if (st != BIV_OK) return st;
     if (rows_per_req > kMaxAcceptRows) {          // the two kernels instead
         const int st2 = launch_pdl(tile_winners_kernel, dim3((M + 7) / 8), dim3(256), 0, s,
