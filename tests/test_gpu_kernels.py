@@ -320,6 +320,28 @@ def test_attention_bad_position_raises_device_error():
     assert same_bits(o[keep], good[keep])                  # the other rows are unaffected
 
 
+def test_attention_bad_rows_with_the_balanced_combine():
+    """64 requests x 16 rows x 32 heads: enough (row, head) pairs per combine
+    warp for the cost deal.  Rows with a position past the cache are zeroed
+    (costing one unit each in the deal) and raise the device flag; every other
+    row keeps the bits of the clean window."""
+    p0 = [(37 * r) % 500 + 20 for r in range(64)]
+    q, kc, vc, slot, pos = _attn_case(64, 32, 8, 560, p0, 16, seed=31)
+    qd, kd, vd = dev(q), dev(kc), dev(vc)
+    good = _run_attn(qd, kd, vd, slot, pos, 16)
+    assert B.biv_device_error() == 0
+    bad = pos.copy()
+    rows = [3, 400, 401, 1023]
+    bad[rows] = 560                                        # one past the cache
+    o = _run_attn(qd, kd, vd, slot, bad, 16)
+    assert B.biv_device_error() & 2                        # BIV_DEVERR_INDEX, and the flag is cleared
+    assert torch.count_nonzero(o[rows]) == 0
+    keep = [w for w in range(1024) if w not in rows]
+    assert same_bits(o[keep], good[keep])
+    ref = oracle.attention(q[[0, 700]], kc, vc, slot[[0, 700]], pos[[0, 700]])
+    assert_close(good[[0, 700]], ref, what="attention, balanced combine")
+
+
 def test_attention_first_position():
     q, kc, vc, slot, pos = _attn_case(2, 4, 2, 64, [0, 0], 1, seed=4)
     o = _run_attn(dev(q), dev(kc), dev(vc), slot, pos, 1)
