@@ -125,11 +125,22 @@ BIV_DEV uint32_t pick_word(const U4& w, uint32_t j) {
     return j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
 }
 
-// Epilogue threads per CTA: 128 (warps 2-5, one per TMEM lane quarter), 256
-// for the fused selection (warps 2-9: two per lane quarter, each taking half of
-// a tile's columns, so two warps share every SM sub-partition's issue slots).
+// Epilogue threads per CTA: 256 (warps 2-9: two per TMEM lane quarter, each
+// taking half of a tile's columns, so two warps share every SM sub-partition's
+// issue slots).  With one warp per quarter the 2-layer W = 64 step was 0.7 us
+// slower (its GEMMs have a single tile per CTA, so every epilogue is on the
+// path); at W = 1024 the exposed last-tile epilogues are bound by their
+// scattered stores, not by issue, and did not change.
 template <int EPI>
-__host__ __device__ constexpr int epi_threads() { return EPI == 3 ? 256 : 128; }
+__host__ __device__ constexpr int epi_threads() { return 256; }
+
+// Column range [cb, ce) of a tile of width bn that warp set `eset` (0: warps
+// 2-5, 1: warps 6-9) takes, in whole units of `unit` columns.
+BIV_DEV void eset_columns(int bn, int unit, int eset, int& cb, int& ce) {
+    const int units = (bn + unit - 1) / unit, h = (units + 1) / 2;
+    cb = eset ? h * unit : 0;
+    ce = eset ? bn : min(bn, h * unit);
+}
 
 template <int NT>
 BIV_DEV void epilogue_bar() {
@@ -818,7 +829,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         if constexpr (EPI == 4) {
             // RoPE frequencies of the pairs; the first tile's vote publishes them.
             __shared__ float s_inv_freq[128];                  // head_dim <= 256
-            for (int i = static_cast<int>(threadIdx.x) - 64; i < rp.hd / 2; i += 128)
+            for (int i = static_cast<int>(threadIdx.x) - 64; i < rp.hd / 2; i += NT)
                 s_inv_freq[i] = rope_inv_freq(i, rp.hd, rp.theta);
             inv_freq = s_inv_freq;
         }
@@ -908,10 +919,12 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     if (keep && !cache_ok && jb == 0) atomicOr(&g_gemm_err, BIV_DEVERR_INDEX);
                     write_kv = keep && cache_ok;
                 }
+                int cb4, ce4;
+                eset_columns(bnt, 16, (warp - 2) >> 2, cb4, ce4);
                 if (g.m64) {
                     RopeAngles<4> ang;
 #pragma unroll 1
-                    for (int c = 0; c < bnt; c += 16) {
+                    for (int c = cb4; c < ce4; c += 16) {
                         const int col = col0 + c;
                         uint32_t ra[4], rb[4];
                         tmem_ld16x2_x4_pair_sync(taddr + static_cast<uint32_t>(c),
@@ -922,7 +935,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 } else {
                     RopeAngles<8> ang;
 #pragma unroll 1
-                    for (int c = 0; c < bnt; c += 16) {
+                    for (int c = cb4; c < ce4; c += 16) {
                         const int col = col0 + c;
                         uint32_t r[16];
                         tmem_ld16(taddr + static_cast<uint32_t>(c), r);
@@ -935,13 +948,15 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 // Columns [32j, 32j + 16) of the tile are gate rows, [32j + 16, 32j + 32)
                 // the matching up rows: act = bf16(silu(bf16(g)) * bf16(u)).
                 const int F = N / 2;
+                int cb2, ce2;
+                eset_columns(bnt, 32, (warp - 2) >> 2, cb2, ce2);
                 if (g.m64) {
                     // the two half-warps share each row: threads 16..31 take
                     // gate columns 8..15 of every 32-column group and their up columns
                     const int prow = row_base + q * 16 + (lane & 15);
                     const int hi = lane >> 4;
 #pragma unroll 1
-                    for (int c = 0; c < bnt; c += 32) {
+                    for (int c = cb2; c < ce2; c += 32) {
                         uint32_t gr[8], ur[8];
                         tmem_ld16x2_x8_pair_sync(taddr + static_cast<uint32_t>(c),
                                                  taddr + static_cast<uint32_t>(c + 16), gr, ur);
@@ -959,7 +974,7 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     }
                 } else
 #pragma unroll 1
-                for (int c = 0; c < bnt; c += 32) {
+                for (int c = cb2; c < ce2; c += 32) {
                     uint32_t gr[16], ur[16];
                     tmem_ld16(taddr + static_cast<uint32_t>(c), gr);
                     tmem_ld16(taddr + static_cast<uint32_t>(c + 16), ur);
@@ -978,8 +993,10 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     }
                 }
             } else {
+            int cb0, ce0;
+            eset_columns(bnt, 16, (warp - 2) >> 2, cb0, ce0);
 #pragma unroll 1
-            for (int c = 0; c < bnt; c += 16) {
+            for (int c = cb0; c < ce0; c += 16) {
                 uint32_t r[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(c), r);
                 tmem_ld_wait();
