@@ -11,20 +11,22 @@
 // MMA independently of the instruction's N (checked bitwise on the GPU for
 // N = 16..256), so the tile width is free to follow the problem size.
 //
-// Kernel layout (192 threads, one CTA per SM, persistent over tiles):
+// Kernel layout (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer: per stage one box of A [a_rows x KS*64] and one of
 //               B [BN x KS*64] (3-D tensor maps: KS k-blocks of 64 per box; the
 //               TMA unit spends a fixed ~275 ns per box whatever its size, so
 //               weight-streaming tiles take as many k-blocks per box as two
-//               stages allow), 128-byte swizzle, mbarrier transaction counts.  For M <= 128 only the real rows of A are
-//               copied (a_rows = M rounded up to 8) and packed back to back;
-//               the MMA still reads 128 rows per k-block, and the rows past
+//               stages allow), 128-byte swizzle, mbarrier transaction
+//               counts.  For M <= 128 only the real rows of A are copied
+//               (a_rows = M rounded up to 8) and packed back to back; the
+//               MMA still reads 128 rows per k-block, and the rows past
 //               a_rows hold unrelated data -- harmless, because each row of the
 //               product depends only on its own row of A and rows >= M are
 //               never stored.
 //   warp 1      TMEM allocator + MMA issuer (one elected lane); commits free smem
 //               stages and publish finished accumulators.
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 16 columns, convert, store.
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (each takes half of
+//               a tile's columns): tcgen05.ld, convert, store.
 // Two accumulators in TMEM let the epilogue of tile i overlap the MMAs of
 // tile i + 1.  Launched with programmatic dependent launch: barrier set-up
 // and TMEM allocation overlap the previous kernel.  Every wait is
@@ -851,7 +853,8 @@ gemm_nosplitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     tile_buckets<NT>(bk, g.a_rows, min(kBM, M - m_blk * kBM), bnt, col0, N, m_blk * kBM, sel);
             }
             // One thread polls the accumulator barrier; the vote hands its
-            // outcome to the other 127 (no polling traffic beside the copies).
+            // outcome to the other epilogue threads (no polling traffic beside
+            // the copies).
             bool ok = threadIdx.x == 64 ? mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_gemm_err, false, CG == 2)
                                         : true;
             ok = epilogue_all<NT>(ok);
