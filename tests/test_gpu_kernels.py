@@ -342,6 +342,26 @@ def test_attention_bad_rows_with_the_balanced_combine():
     assert_close(good[[0, 700]], ref, what="attention, balanced combine")
 
 
+@pytest.mark.parametrize("n_req,K,Hq,Hkv", [(2, 4, 8, 2), (64, 16, 32, 8)])   # round-robin / balanced combine
+def test_attention_row_outside_its_slot_group(n_req, K, Hq, Hkv):
+    """A row whose slot differs from its group's first row (rows of one group
+    must share a cache slot) raises BIV_DEVERR_GROUP and is zeroed; the other
+    rows of its group and of the window keep the bits of the clean window."""
+    p0 = [(53 * r) % 400 + 30 for r in range(n_req)]
+    q, kc, vc, slot, pos = _attn_case(n_req, Hq, Hkv, 480, p0, K, seed=17 + n_req)
+    qd, kd, vd = dev(q), dev(kc), dev(vc)
+    good = _run_attn(qd, kd, vd, slot, pos, K)
+    assert B.biv_device_error() == 0
+    bad = slot.copy()
+    w = 2                                                  # not the first row of group 0
+    bad[w] = 1                                             # another request's slot
+    o = _run_attn(qd, kd, vd, bad, pos, K)
+    assert B.biv_device_error() & 4                        # BIV_DEVERR_GROUP, and the flag is cleared
+    assert torch.count_nonzero(o[w]) == 0
+    keep = [r for r in range(n_req * K) if r != w]
+    assert same_bits(o[keep], good[keep])
+
+
 def test_attention_first_position():
     q, kc, vc, slot, pos = _attn_case(2, 4, 2, 64, [0, 0], 1, seed=4)
     o = _run_attn(dev(q), dev(kc), dev(vc), slot, pos, 1)
