@@ -94,6 +94,14 @@ int biv_version(void);                                /* 100 * major + minor */
  * synchronisation failed.  Not for the hot path. */
 int biv_device_error(uint32_t* bits_out);
 
+/* Self-test of the device-side failure detection: launches one kernel in
+ * which a thread waits, through the same bounded wait every pipeline of the
+ * library uses, on a barrier that nothing completes.  After the wait's limit
+ * (about 2 s) it gives up, raises BIV_DEVERR_TIMEOUT and returns; the next
+ * biv_device_error() reports the bit and the context stays usable.  Nothing
+ * traps, faults or spins without bound.  Not for the hot path. */
+int biv_selftest_wait_timeout(biv_stream_t stream);
+
 /* --------------------------------------------------------- RMSNorm
  * [DVR] para 1: RMSNorm with a fixed split over the hidden dimension that
  * does not depend on the batch or on how many SMs are busy.

@@ -39,6 +39,7 @@ SIGNATURES = {
     "biv_last_cuda_error": (_I, []),
     "biv_version": (_I, []),
     "biv_device_error": (_I, [_P]),
+    "biv_selftest_wait_timeout": (_I, [_P]),
     "biv_rmsnorm": (_I, [_P, _P, _P, _I, _I, _F, _P]),
     "biv_gemm_nosplitk": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "biv_gemm_nosplitk_bn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -127,6 +128,10 @@ def biv_device_error() -> int:
     bits = C.c_uint32(0)
     _check("biv_device_error", _load().biv_device_error(C.byref(bits)))
     return int(bits.value)
+
+
+def biv_selftest_wait_timeout(stream=None) -> None:
+    _check("biv_selftest_wait_timeout", _load().biv_selftest_wait_timeout(_stream(stream)))
 
 
 # ---------------------------------------------------------------- kernels

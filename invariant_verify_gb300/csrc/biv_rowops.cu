@@ -165,6 +165,20 @@ __global__ void residual_add_kernel(const __nv_bfloat16* __restrict__ x, const _
     }
 }
 
+// One thread waits on a barrier that nothing completes: the library's bounded
+// wait gives up after its time limit, raises BIV_DEVERR_TIMEOUT in this
+// module's error word and the kernel returns with the context intact.
+__global__ void wait_timeout_kernel() {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait(&bar, 0u, &abort_flag, &g_rowops_err);
+    }
+}
+
 int grid_for(long long work, int threads) {
     return static_cast<int>(std::max<long long>(1, std::min<long long>((work + threads - 1) / threads,
                                                                        static_cast<long long>(num_sms()) * 16)));
@@ -242,4 +256,14 @@ extern "C" int biv_residual_add(const void* x, const void* y, void* out, long lo
     return launch_pdl(residual_add_kernel, dim3(grid_for(n / 8, 256)), dim3(256), 0,
                       reinterpret_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(x),
                       static_cast<const __nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(out), n / 8);
+}
+
+extern "C" int biv_selftest_wait_timeout(biv_stream_t stream) {
+    biv::wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        biv::set_cuda_error(e);
+        return BIV_ERR_CUDA;
+    }
+    return BIV_OK;
 }

@@ -362,6 +362,24 @@ def test_attention_row_outside_its_slot_group(n_req, K, Hq, Hkv):
     assert same_bits(o[keep], good[keep])
 
 
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    """Failure detection without a fault: a kernel waits, through the
+    library's bounded wait, on a barrier nothing completes; it gives up,
+    raises BIV_DEVERR_TIMEOUT and returns.  Kernels launched afterwards run
+    and match the oracle."""
+    assert B.biv_device_error() == 0
+    B.biv_selftest_wait_timeout()
+    assert B.biv_device_error() & 1                        # BIV_DEVERR_TIMEOUT, and the flag is cleared
+    assert B.biv_device_error() == 0
+    g = synth.generator(99)
+    A = synth.bf16_normal((37, 256), 1.0, g)
+    Bw = synth.bf16_normal((192, 256), 0.1, g)
+    C_ = torch.empty(37, 192, dtype=torch.float32, device="cuda")
+    B.biv_gemm_nosplitk(dev(A), dev(Bw), C_)
+    assert_close(C_, oracle.gemm(A, Bw), what="GEMM after a timed-out wait")
+    assert B.biv_device_error() == 0
+
+
 def test_attention_first_position():
     q, kc, vc, slot, pos = _attn_case(2, 4, 2, 64, [0, 0], 1, seed=4)
     o = _run_attn(dev(q), dev(kc), dev(vc), slot, pos, 1)
