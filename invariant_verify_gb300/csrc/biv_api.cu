@@ -76,6 +76,7 @@ extern "C" int biv_last_cuda_error(void) { return biv::t_last_cuda_error; }
 extern "C" int biv_version(void) { return 100; }
 
 extern "C" int biv_device_error(uint32_t* bits_out) {
+    BIV_TRACE_CALL();
     if (!bits_out) return BIV_ERR_NULL;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return biv::cuda_status(e);

@@ -1406,6 +1406,7 @@ extern "C" size_t biv_decode_attn_workspace_size(int W, int Hq, int max_len) {
 }
 
 extern "C" int biv_gqa_max_drafts(int G, int tile) {
+    BIV_TRACE_CALL();
     if (G <= 0 || G > tile) return -1;
     return tile / G - 1;
 }
@@ -1414,6 +1415,7 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
                                           const int32_t* row_slot, const int32_t* row_pos, void* o, int W,
                                           int rows_per_group, int Hq, int Hkv, int hd, int n_slots, int max_len,
                                           int kv_split, void* workspace, size_t ws_bytes, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (W < 0 || Hq <= 0 || Hkv <= 0 || n_slots <= 0 || max_len <= 0 || rows_per_group <= 0)
         return BIV_ERR_SHAPE;
     if (hd != HD || kv_split != SPLIT) return BIV_ERR_UNSUPPORTED;
@@ -1554,6 +1556,7 @@ extern "C" int biv_decode_attn_fixedsplit(const void* q, const void* k_cache, co
 
 extern "C" int biv_rope_qk(const void* qkv, void* q_out, void* k_out, const int32_t* row_pos, int W, int Hq,
                            int Hkv, int hd, float theta, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (W < 0 || Hq <= 0 || Hkv < 0 || hd <= 0 || hd % 2 != 0 || hd > 256) return BIV_ERR_SHAPE;
     if (!(theta > 1.0f) || !std::isfinite(theta)) return BIV_ERR_VALUE;
     if (W == 0) return BIV_OK;
@@ -1569,6 +1572,7 @@ extern "C" int biv_rope_kv_write(const void* qkv, void* q_out, void* k_cache, vo
                                  const int32_t* row_slot, const int32_t* row_pos, const int32_t* rows_keep, int W,
                                  int K, int Hq, int Hkv, int hd, int n_slots, int max_len, float theta,
                                  biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (W < 0 || K < 1 || Hq <= 0 || Hkv <= 0 || hd <= 0 || hd % 8 != 0 || hd > 256 || n_slots <= 0 ||
         max_len <= 0)
         return BIV_ERR_SHAPE;
@@ -1587,6 +1591,7 @@ extern "C" int biv_kv_overwrite(void* k_cache, void* v_cache, const void* k_new,
                                 const void* v_new, long long v_stride, const int32_t* row_slot,
                                 const int32_t* row_pos, const int32_t* rows_keep, int W, int K, int Hkv, int hd,
                                 int n_slots, int max_len, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (W < 0 || K < 1 || Hkv <= 0 || hd <= 0 || n_slots <= 0 || max_len <= 0) return BIV_ERR_SHAPE;
     const long long row = static_cast<long long>(Hkv) * hd;
     if (hd % 8 != 0 || k_stride % 8 != 0 || v_stride % 8 != 0 || k_stride < row || v_stride < row)
@@ -1651,6 +1656,7 @@ extern "C" int biv_decode_attn_fixedsplit_noalloc(const void* q, const void* k_c
                                                   const int32_t* row_slot, const int32_t* row_pos, void* o, int W,
                                                   int rows_per_group, int Hq, int Hkv, int hd, int n_slots,
                                                   int max_len, int kv_split, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (W < 0 || Hq <= 0 || Hkv <= 0 || n_slots <= 0 || max_len <= 0 || rows_per_group <= 0)
         return BIV_ERR_SHAPE;
     if (hd != HD || kv_split != SPLIT) return BIV_ERR_UNSUPPORTED;

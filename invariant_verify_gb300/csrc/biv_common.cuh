@@ -9,10 +9,22 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/biv.h"
 
 #define BIV_DEV __device__ __forceinline__
+
+// Host-side trace range named after the ABI call (NVTX; a pointer check when no
+// tool is attached, so ncu can take `--nvtx --nvtx-include <call>/` to capture
+// one call's kernels).  Under stream capture it marks the enqueue.
+struct BivTraceScope {
+    explicit BivTraceScope(const char* name) { nvtxRangePushA(name); }
+    ~BivTraceScope() { nvtxRangePop(); }
+    BivTraceScope(const BivTraceScope&) = delete;
+    BivTraceScope& operator=(const BivTraceScope&) = delete;
+};
+#define BIV_TRACE_CALL() const BivTraceScope biv_trace_scope_(__func__)
 
 namespace biv {
 

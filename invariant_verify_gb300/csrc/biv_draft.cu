@@ -93,6 +93,7 @@ using namespace biv;
 
 extern "C" int biv_ngram_draft(const int32_t* hist, int N, long long ld, const int32_t* len, int n_max, int n_min,
                                int K, int32_t* drafts, int32_t* draft_src, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (N < 0 || ld < 1 || K < 1 || K > kMaxDrafts) return BIV_ERR_SHAPE;
     if (n_min < 1 || n_max < n_min || n_max > kMaxNgram) return BIV_ERR_VALUE;
     if (N == 0) return BIV_OK;

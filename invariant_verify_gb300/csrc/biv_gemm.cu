@@ -1391,6 +1391,7 @@ winners_accept_kernel(const unsigned long long* __restrict__ cand, int n_tiles, 
 using namespace biv;
 
 extern "C" int biv_gemm_tile_n(int M, int N, int K) {
+    BIV_TRACE_CALL();
     const long long m_tiles = std::max<long long>(1, ceil_div(M, kBM));
     if (m_tiles == 1) {
         // Weight streaming: one wave of tiles, each as wide as that allows.
@@ -1434,6 +1435,7 @@ extern "C" int biv_gemm_tile_n(int M, int N, int K) {
 
 extern "C" int biv_gemm_nosplitk_bn(const void* A, const void* B, void* C, int out_dtype, int M, int N,
                                     int K, int bn, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     int st = check_gemm(A, B, C, out_dtype, M, N, K);
     if (st != BIV_OK || M == 0) return st;
     if (bn < 16 || bn > 256 || bn % 16 != 0) return BIV_ERR_VALUE;
@@ -1444,12 +1446,14 @@ extern "C" int biv_gemm_nosplitk_bn(const void* A, const void* B, void* C, int o
 
 extern "C" int biv_gemm_nosplitk(const void* A, const void* B, void* C, int out_dtype, int M, int N, int K,
                                  biv_stream_t stream) {
+    BIV_TRACE_CALL();
     int st = check_gemm(A, B, C, out_dtype, M, N, K);
     if (st != BIV_OK || M == 0) return st;
     return biv_gemm_nosplitk_bn(A, B, C, out_dtype, M, N, K, biv_gemm_tile_n(M, N, K), stream);
 }
 
 extern "C" int biv_swiglu_pack_weights(const void* w_gu, void* w_packed, int F, int K, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (F <= 0 || K <= 0 || F % 16 != 0 || K % 8 != 0) return BIV_ERR_SHAPE;
     if (!w_gu || !w_packed) return BIV_ERR_NULL;
     if (!aligned16(w_gu) || !aligned16(w_packed)) return BIV_ERR_ALIGN;
@@ -1460,6 +1464,7 @@ extern "C" int biv_swiglu_pack_weights(const void* w_gu, void* w_packed, int F, 
 
 extern "C" int biv_gemm_swiglu(const void* A, const void* B_packed, void* act, int M, int F, int K,
                                biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (F <= 0 || F % 16 != 0) return BIV_ERR_SHAPE;
     const int N = 2 * F;
     int st = check_gemm(A, B_packed, act, BIV_BF16, M, N, K);
@@ -1489,6 +1494,7 @@ extern "C" size_t biv_lm_head_gumbel_workspace_size(int M, int N, int K) {
 extern "C" int biv_lm_head_gumbel(const void* A, const void* B, float* logits, int M, int N, int K,
                                   const uint32_t* row_req, const int32_t* row_pos, uint64_t seed, float temperature,
                                   int32_t* tokens, void* workspace, size_t ws_bytes, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (M < 0 || N <= 0 || K <= 0 || N % 8 != 0 || K % 8 != 0) return BIV_ERR_SHAPE;
     if (!(temperature >= 0.0f) || !(temperature < INFINITY)) return BIV_ERR_VALUE;
     if (M == 0) return BIV_OK;
@@ -1518,6 +1524,7 @@ extern "C" int biv_lm_head_gumbel_accept(const void* A, const void* B, float* lo
                                          float temperature, int32_t* tokens, const int32_t* draft, const int32_t* p0,
                                          int n_req, int rows_per_req, int32_t* accept_len, int32_t* new_len,
                                          void* workspace, size_t ws_bytes, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (M < 0 || N <= 0 || K <= 0 || N % 8 != 0 || K % 8 != 0) return BIV_ERR_SHAPE;
     if (n_req < 0 || rows_per_req < 1 || static_cast<long long>(n_req) * rows_per_req != M) return BIV_ERR_SHAPE;
     if (!(temperature >= 0.0f) || !(temperature < INFINITY)) return BIV_ERR_VALUE;
@@ -1556,6 +1563,7 @@ extern "C" int biv_lm_head_gumbel_accept(const void* A, const void* B, float* lo
 
 extern "C" int biv_rope_pack_qkv_weights(const void* w_qkv, void* w_packed, int Hq, int Hkv, int hd, int K,
                                          biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (Hq <= 0 || Hkv <= 0 || hd <= 0 || hd % 16 != 0 || hd > 256 || K <= 0 || K % 8 != 0) return BIV_ERR_SHAPE;
     if (!w_qkv || !w_packed) return BIV_ERR_NULL;
     if (!aligned16(w_qkv) || !aligned16(w_packed)) return BIV_ERR_ALIGN;
@@ -1573,6 +1581,7 @@ extern "C" int biv_gemm_qkv_rope(const void* A, const void* B_packed, void* q_ou
                                  void* qkv_out, const int32_t* row_slot, const int32_t* row_pos,
                                  const int32_t* rows_keep, int W, int K, int d, int Hq, int Hkv, int hd, int n_slots,
                                  int max_len, float theta, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (W < 0 || K < 1 || d <= 0 || d % 8 != 0 || Hq <= 0 || Hkv <= 0 || hd <= 0 || hd % 16 != 0 || hd > 256 ||
         n_slots <= 0 || max_len <= 0 || Hq % Hkv != 0)
         return BIV_ERR_SHAPE;

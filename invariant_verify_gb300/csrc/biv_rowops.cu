@@ -191,6 +191,7 @@ using namespace biv;
 
 extern "C" int biv_rmsnorm(const void* x, const void* w, void* y, int rows, int d, float eps,
                            biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (rows < 0 || d < 8 || d % 8 != 0 || d > 8 * 1024 * kMaxChunksPerThread) return BIV_ERR_SHAPE;
     if (!(eps > 0.0f) || !std::isfinite(eps)) return BIV_ERR_VALUE;
     if (rows == 0) return BIV_OK;
@@ -204,6 +205,7 @@ extern "C" int biv_rmsnorm(const void* x, const void* w, void* y, int rows, int 
 
 extern "C" int biv_add_rmsnorm(const void* x, const void* r, const void* w, void* x_out, void* y, int rows, int d,
                                float eps, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (rows < 0 || d < 8 || d % 8 != 0 || d > 8 * 1024 * kMaxChunksPerThread) return BIV_ERR_SHAPE;
     if (!(eps > 0.0f) || !std::isfinite(eps)) return BIV_ERR_VALUE;
     if (rows == 0) return BIV_OK;
@@ -217,6 +219,7 @@ extern "C" int biv_add_rmsnorm(const void* x, const void* r, const void* w, void
 
 extern "C" int biv_embed_rmsnorm(const void* table, const int32_t* tokens, const void* w, void* x_out, void* y,
                                  int W, int d, int vocab, float eps, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (W < 0 || d < 8 || d % 8 != 0 || d > 8 * 1024 * kMaxChunksPerThread || vocab <= 0) return BIV_ERR_SHAPE;
     if (!(eps > 0.0f) || !std::isfinite(eps)) return BIV_ERR_VALUE;
     if (W == 0) return BIV_OK;
@@ -230,6 +233,7 @@ extern "C" int biv_embed_rmsnorm(const void* table, const int32_t* tokens, const
 
 extern "C" int biv_embed(const void* table, const int32_t* tokens, void* out, int W, int d, int vocab,
                          biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (W < 0 || d <= 0 || d % 8 != 0 || vocab <= 0) return BIV_ERR_SHAPE;
     if (W == 0) return BIV_OK;
     if (!table || !tokens || !out) return BIV_ERR_NULL;
@@ -239,6 +243,7 @@ extern "C" int biv_embed(const void* table, const int32_t* tokens, void* out, in
 }
 
 extern "C" int biv_silu_mul(const void* gu, void* out, int rows, int F, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (rows < 0 || F <= 0 || F % 8 != 0) return BIV_ERR_SHAPE;
     if (rows == 0) return BIV_OK;
     if (!gu || !out) return BIV_ERR_NULL;
@@ -249,6 +254,7 @@ extern "C" int biv_silu_mul(const void* gu, void* out, int rows, int F, biv_stre
 }
 
 extern "C" int biv_residual_add(const void* x, const void* y, void* out, long long n, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (n < 0 || n % 8 != 0) return BIV_ERR_SHAPE;
     if (n == 0) return BIV_OK;
     if (!x || !y || !out) return BIV_ERR_NULL;
@@ -259,6 +265,7 @@ extern "C" int biv_residual_add(const void* x, const void* y, void* out, long lo
 }
 
 extern "C" int biv_selftest_wait_timeout(biv_stream_t stream) {
+    BIV_TRACE_CALL();
     biv::wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {

@@ -1155,6 +1155,7 @@ static int gumbel_argmax_impl(const float* logits, int R, int V, long long ld, c
 extern "C" int biv_gumbel_argmax(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
                                  const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
                                  biv_stream_t stream) {
+    BIV_TRACE_CALL();
     return gumbel_argmax_impl(logits, R, V, ld, row_req, row_pos, seed, temperature, tokens, nullptr, stream);
 }
 
@@ -1166,6 +1167,7 @@ extern "C" size_t biv_gumbel_argmax_workspace_size(int R, int V) {
 extern "C" int biv_gumbel_argmax_ws(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
                                     const int32_t* row_pos, uint64_t seed, float temperature, int32_t* tokens,
                                     void* workspace, size_t ws_bytes, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (R < 0 || V < 4 || ld < V || V % 4 != 0 || ld % 4 != 0) return BIV_ERR_SHAPE;
     if (R > 0) {
         if (!workspace) return BIV_ERR_NULL;
@@ -1178,6 +1180,7 @@ extern "C" int biv_gumbel_argmax_ws(const float* logits, int R, int V, long long
 extern "C" int biv_gumbel_topk(const float* logits, int R, int V, long long ld, const uint32_t* row_req,
                                const int32_t* row_pos, uint64_t seed, float temperature, int k, int32_t* out,
                                biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (R < 0 || V < 4 || ld < V || V % 4 != 0 || ld % 4 != 0) return BIV_ERR_SHAPE;
     if (k < 1 || k > kMaxTopk || k > V) return BIV_ERR_SHAPE;
     if (!(temperature >= 0.0f) || !(temperature < INFINITY)) return BIV_ERR_VALUE;
@@ -1204,6 +1207,7 @@ extern "C" int biv_gumbel_topk(const float* logits, int R, int V, long long ld, 
 
 extern "C" int biv_gumbel_noise(uint64_t seed, const uint32_t* row_req, const int32_t* row_pos, int R, int V,
                                 float* g, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (R < 0 || V < 0 || R > 65535) return BIV_ERR_SHAPE;
     if (R == 0 || V == 0) return BIV_OK;
     if (!row_req || !row_pos || !g) return BIV_ERR_NULL;
@@ -1214,6 +1218,7 @@ extern "C" int biv_gumbel_noise(uint64_t seed, const uint32_t* row_req, const in
 }
 
 extern "C" int biv_gumbel_from_words(const uint32_t* words, long long n, float* g, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (n < 0) return BIV_ERR_SHAPE;
     if (n == 0) return BIV_OK;
     if (!words || !g) return BIV_ERR_NULL;
@@ -1224,6 +1229,7 @@ extern "C" int biv_gumbel_from_words(const uint32_t* words, long long n, float* 
 
 extern "C" int biv_verify_accept(const int32_t* target, const int32_t* draft, const int32_t* p0, int N, int K,
                                  int32_t* accept_len, int32_t* new_len, biv_stream_t stream) {
+    BIV_TRACE_CALL();
     if (N < 0 || K < 1) return BIV_ERR_SHAPE;
     if (N == 0) return BIV_OK;
     if (!target || !draft || !p0 || !accept_len || !new_len) return BIV_ERR_NULL;
@@ -1232,6 +1238,7 @@ extern "C" int biv_verify_accept(const int32_t* target, const int32_t* draft, co
 }
 
 extern "C" int biv_gumbel_bucket_bounds(float* bounds_out) {
+    BIV_TRACE_CALL();
     if (!bounds_out) return BIV_ERR_NULL;
     const NoiseBounds& nb = noise_bounds();
     for (int b = 0; b < 256; ++b) bounds_out[b] = nb.v[b];
