@@ -70,7 +70,7 @@ struct GemmArgs {
     // Narrow tail (CTA pairs, fused selection): column tiles [0, nt_full) are
     // BN wide and the rest bn_tail wide (tensor map tmB1, descriptor
     // idesc_tail), so that the last, partial wave of full tiles becomes one
-    // wave of tiles half as wide.  bn_tail = 0: every column tile is BN wide.
+    // wave of narrower tiles.  bn_tail = 0: every column tile is BN wide.
     int nt_full;
     int bn_tail;
     uint32_t idesc_tail;
@@ -1138,12 +1138,13 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 // The narrow tail of the fused selection's CTA-pair schedule.  With work
 // tiles on a wave of kPairWave pairs, the last wave holds r = work mod wave
-// tiles; when those are whole column tiles (row tiles fastest) and twice r
-// still fits one wave, they are re-cut into tiles half as wide (a multiple of
-// 32, at least 64), so that every pair ends with a short tile instead of some
-// pairs with a whole one.  The LM head at W = 1024 (2004 tiles of 256 columns
-// on 76 pairs: 28 in the last wave) ends about one half tile sooner.  Each
-// element's arithmetic does not depend on the tile width.
+// tiles; when those are whole column tiles (row tiles fastest) they are re-cut
+// into the narrowest tiles (a multiple of 32 columns, at least 64) of which
+// one wave still holds all, so that every pair ends with one short tile
+// instead of some pairs with a whole one.  W = 1024 (2004 tiles of 256 columns
+// on 76 pairs, 28 in the last wave): 76 tiles of 96 columns; W = 256 (501 on
+// 76, 45 in the last wave): 72 of 160.  Each element's arithmetic does not
+// depend on the tile width.
 struct TailPlan {
     int nt_full, bn_tail, n_cols;     // full column tiles, tail width (0: none), column tiles in all
 };
@@ -1156,12 +1157,14 @@ inline TailPlan tail_plan(int M, int N, int BN, bool pairs) {
     const long long work = m_tiles * n_tiles;
     const long long wave = std::min<long long>(work, kPairWave);
     const long long r = work % wave;
-    const int bt = BN / 2;
-    if (r == 0 || r % m_tiles != 0 || 2 * r > wave || bt % 32 != 0 || bt < 64) return p;
+    if (r == 0 || r % m_tiles != 0) return p;
     const int nt_full = n_tiles - static_cast<int>(r / m_tiles);
-    const int nt_tail = static_cast<int>(ceil_div(N - static_cast<long long>(nt_full) * BN, bt));
-    if (m_tiles * nt_tail > wave) return p;
-    return TailPlan{nt_full, bt, nt_full + nt_tail};
+    const long long tail_cols = N - static_cast<long long>(nt_full) * BN;
+    for (int bt = 64; bt < BN; bt += 32) {
+        const long long nt_tail = ceil_div(tail_cols, bt);
+        if (m_tiles * nt_tail <= wave) return TailPlan{nt_full, bt, nt_full + static_cast<int>(nt_tail)};
+    }
+    return p;
 }
 
 template <int EPI, int CG>

@@ -747,11 +747,13 @@ def _fused_vs_unfused(A, Bw, T, seed=SEED, write_logits=True):
     # CTA pairs with many tiles each: 4 row tiles (each pair keeps its rows, and their
     # best keys from tile to tile) and 3 row tiles (the rows change every tile)
     (1024, 20000, 256, 0.7, 0.05), (600, 32000, 256, 0.7, 0.05),
-    # the last, partial wave of pair tiles re-cut into tiles half as wide: 128-column
-    # tail tiles, a ragged last one, 96-column tail tiles (192-column tiles), and
-    # two row pairs instead of four (a ragged tail again)
+    # the last, partial wave of pair tiles re-cut into the narrowest tiles one wave
+    # holds: 96-column tails (four row pairs, 192-column full tiles, two row pairs),
+    # 160 (the 4-row-tile case above), 64 (three row pairs), 128 (an exact fit),
+    # 192 and 224 (a partial last row tile); most with a ragged last tail tile
     (1024, 25600, 256, 0.7, 0.05), (1024, 25544, 256, 0.7, 0.05), (1024, 34552, 256, 0.7, 0.05),
-    (512, 51088, 256, 0.7, 0.05)])
+    (512, 51088, 256, 0.7, 0.05), (600, 40488, 256, 0.7, 0.05), (300, 9792, 256, 0.7, 0.05),
+    (300, 14600, 256, 0.7, 0.05), (300, 17032, 256, 0.7, 0.05)])
 def test_lm_head_gumbel_fused_bit_exact(M, N, K, T, std):
     g = synth.generator(M + N + K)
     A = synth.bf16_normal((M, K), 1.0, g).cuda()
